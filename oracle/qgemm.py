@@ -1,0 +1,108 @@
+"""Oracle GEMMs (float64, CPU).  Test infrastructure only.
+
+What the quantized GEMMs compute (spke.com Humming announcement, section
+"フォーマットとアーキテクチャを横断して共有されるCUDAコンポーネント": dequantization and
+scaling are part of the kernel computation, scale and bias may be fused into the
+output stage; section "WnA16": low-bit weights times 16-bit activations; section
+"W8A8 / W4A8 / W4A4": MX block-scaled weights and activations):
+
+  W4A16:  R[m,n] = sum_k a[m,k] * q[n,k] * s[n, k // G]            (+ bias[n])
+  W4A8:   R[m,n] = sum_k e4m3(a[m,k]) 2^(sa[m,k//32]-127)
+                          * e2m1(w[n,k]) 2^(sw[n,k//32]-127)      (+ bias[n])
+
+Every operand is decoded exactly into float64 and the sum over k is a float64
+matrix product (a library matmul used as one step, no blocking or reordering
+beyond it).  Weights are [N][K] (out x in), activations [M][K], results [M][N].
+
+Pins (tests/test_oracle_gemm.py): exact int64 dot products when every scale is
+1.0 and every operand an integer; exact rational (fractions.Fraction) brute force
+on tiny shapes with several groups; non-square shapes so that a transposed
+operand or a wrong group index changes the result.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import formats as F
+
+
+def dequant_int_weights(q, s_bits, group: int = 128) -> np.ndarray:
+    """q [..., N, K] integers, s_bits [..., N, K/group] BF16 bits -> float64."""
+    q = np.asarray(q).astype(np.float64)
+    s = F.decode_bf16(s_bits)
+    return q * np.repeat(s, group, axis=-1)
+
+
+def dequant_mx(codes, sf, decode) -> np.ndarray:
+    """Element codes [..., R, K] with E8M0 scales [..., R, K/32] -> float64."""
+    v = decode(codes)
+    return v * np.repeat(F.decode_e8m0(sf), 32, axis=-1)
+
+
+def gemm_w4a16(A_bits, q, s_bits, bias_bits=None, group: int = 128):
+    """A_bits [M][K] BF16, q [N][K] ints, s_bits [N][K/group] BF16 -> (R, absum)."""
+    a = F.decode_bf16(A_bits)
+    w = dequant_int_weights(q, s_bits, group)
+    r = a @ w.T
+    absum = np.abs(a) @ np.abs(w).T
+    if bias_bits is not None:
+        b = F.decode_bf16(bias_bits)
+        r = r + b[None, :]
+        absum = absum + np.abs(b)[None, :]
+    return r, absum
+
+
+def gemm_w4a8(A_codes, A_sf, w_codes, w_sf, bias_bits=None):
+    """A_codes [M][K] E4M3, A_sf [M][K/32] E8M0, w_codes [N][K] E2M1 (4-bit codes),
+    w_sf [N][K/32] E8M0 -> (R, absum)."""
+    a = dequant_mx(A_codes, A_sf, F.decode_e4m3)
+    w = dequant_mx(w_codes, w_sf, F.decode_e2m1)
+    r = a @ w.T
+    absum = np.abs(a) @ np.abs(w).T
+    if bias_bits is not None:
+        b = F.decode_bf16(bias_bits)
+        r = r + b[None, :]
+        absum = absum + np.abs(b)[None, :]
+    return r, absum
+
+
+# --------------------------------------------------------------- canonical-input drivers
+def w4a16_from_canonical(A_bits, w_canon, s_canon, K, bits, bias_bits=None, rows=None, cols=None):
+    """Unpack canonical packed words (one expert) and run :func:`gemm_w4a16`.
+    ``rows`` / ``cols`` optionally select a sample of output rows / columns."""
+    q = F.unpack_int4(w_canon, K) if bits == 4 else F.unpack_int3(w_canon, K)
+    A = np.asarray(A_bits)
+    s = np.asarray(s_canon)
+    if rows is not None:
+        A = A[rows]
+    if cols is not None:
+        q, s = q[cols], s[cols]
+        bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
+    return gemm_w4a16(A, q, s, bias_bits)
+
+
+def w4a8_from_canonical(A_codes, A_sf, w_canon, w_sf, K, bias_bits=None, rows=None, cols=None):
+    w = np.asarray(w_canon)
+    sf = np.asarray(w_sf)
+    A, Asf = np.asarray(A_codes), np.asarray(A_sf)
+    if rows is not None:
+        A, Asf = A[rows], Asf[rows]
+    if cols is not None:
+        w, sf = w[cols], sf[cols]
+        bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
+    codes = F.unpack_e2m1_bytes(w, K)
+    return gemm_w4a8(A, Asf, codes, sf, bias_bits)
+
+
+# --------------------------------------------------------------- acceptance test
+def check_bf16_result(C_bits, R, absum, elem_rel=2.0 ** -7, elem_abs=1e-6, frob_rel=2e-3):
+    """Per-element |C - R| <= elem_rel * sum_k |a_k w_k| + elem_abs and
+    ||C - R||_F <= frob_rel * ||R||_F.  Returns (ok, worst_ratio, frob)."""
+    C = F.decode_bf16(C_bits)
+    err = np.abs(C - R)
+    bound = elem_rel * absum + elem_abs
+    ratio = float(np.max(err / bound)) if err.size else 0.0
+    nr = float(np.linalg.norm(R))
+    frob = float(np.linalg.norm(C - R) / nr) if nr > 0 else float(np.linalg.norm(C - R))
+    ok = bool(np.all(np.isfinite(C)) and ratio <= 1.0 and frob <= frob_rel)
+    return ok, ratio, frob

@@ -1,0 +1,210 @@
+"""Counter-based splitmix64 streams and canonical-layout packing of synthetic data.
+
+Random numbers
+--------------
+Every tensor gets its own stream, keyed by ``(seed, tensor_id)``.  Element ``i``
+(1-based) of a stream is ``mix64(key + i * GAMMA)`` with the splitmix64 constants
+(Steele, Lea & Flood, "Fast splittable pseudorandom number generators", 2014):
+GAMMA = 0x9E3779B97F4A7C15, and ``mix64`` the published finaliser
+``z ^= z >> 30; z *= 0xBF58476D1CE4E5B9; z ^= z >> 27; z *= 0x94D049BB133111EB;
+z ^= z >> 31``.  The key itself is ``mix64(seed * GAMMA + tensor_id)``.
+
+* uniform integers in [lo, hi]: Lemire's multiply-shift on the top 32 bits,
+* uniform reals in [0, 1): the top 53 bits times 2^-53,
+* normals: Box-Muller on two consecutive uniforms (cos and sin branch).
+
+Canonical layouts (the library's input formats)
+------------------------------------------------
+* INT4: ``[..., N, K/8]`` uint32; element ``k = 8j + i`` sits at bits ``[4i, 4i+4)``
+  of word ``j``, two's complement.
+* INT3: ``[..., N, K/32, 3]`` uint32 forming a 96-bit little-endian stream per
+  32 elements; element ``i`` sits at stream bits ``[3i, 3i+3)``, two's complement.
+* E2M1: ``[..., N, K/2]`` uint8; even ``k`` in the low nibble.
+* E8M0 / E4M3 / BF16: one code per element, row-major.
+
+Casts of real samples to BF16 and E4M3 codes use PyTorch's own round-to-nearest-even
+conversions (a library routine); E4M3 samples are clamped to +-448 first.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+BASE_SEED = 20261202
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+class Stream:
+    """One splitmix64 counter stream; successive draws continue the counter."""
+
+    def __init__(self, seed: int, tensor_id: int):
+        with np.errstate(over="ignore"):
+            k = np.array([seed], dtype=np.uint64) * _GAMMA + np.uint64(tensor_id)
+        self.key = _mix64(k)[0]
+        self.counter = 0
+
+    def u64(self, n: int) -> np.ndarray:
+        idx = np.arange(self.counter + 1, self.counter + 1 + n, dtype=np.uint64)
+        self.counter += n
+        with np.errstate(over="ignore"):
+            return _mix64(self.key + idx * _GAMMA)
+
+
+def stream(cfg_id: int, tensor_id: int, seed: int = BASE_SEED) -> Stream:
+    """Stream for one tensor of one workload: seed ``seed + cfg_id``."""
+    return Stream(seed + cfg_id, tensor_id)
+
+
+# ----------------------------------------------------------------------------- draws
+def uniform_int(st: Stream, shape, lo: int, hi: int) -> np.ndarray:
+    n = int(np.prod(shape))
+    span = np.uint64(hi - lo + 1)
+    top = st.u64(n) >> np.uint64(32)
+    with np.errstate(over="ignore"):
+        r = (top * span) >> np.uint64(32)
+    return (r.astype(np.int64) + lo).reshape(shape)
+
+
+def uniform(st: Stream, shape, lo: float = 0.0, hi: float = 1.0) -> np.ndarray:
+    n = int(np.prod(shape))
+    u = (st.u64(n) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    return (lo + (hi - lo) * u).reshape(shape)
+
+
+def normal(st: Stream, shape, std: float = 1.0) -> np.ndarray:
+    n = int(np.prod(shape))
+    pairs = (n + 1) // 2
+    u = (st.u64(2 * pairs) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    u1 = 1.0 - u[0::2]  # (0, 1]
+    u2 = u[1::2]
+    r = np.sqrt(-2.0 * np.log(u1))
+    z = np.empty(2 * pairs, dtype=np.float64)
+    z[0::2] = r * np.cos(2.0 * np.pi * u2)
+    z[1::2] = r * np.sin(2.0 * np.pi * u2)
+    return (std * z[:n]).reshape(shape)
+
+
+def random_bytes(st: Stream, n: int) -> np.ndarray:
+    words = st.u64((n + 7) // 8)
+    return words.view(np.uint8)[:n].copy()
+
+
+# ----------------------------------------------------------------------------- casts
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def to_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    x = np.clip(np.asarray(x, dtype=np.float64), -448.0, 448.0)
+    t = torch.from_numpy(np.ascontiguousarray(x)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
+# ----------------------------------------------------------------------------- packing
+def pack_int4(codes: np.ndarray) -> np.ndarray:
+    """int codes in [-8, 7], shape [..., K] (K % 8 == 0) -> uint32 [..., K/8]."""
+    c = np.asarray(codes, dtype=np.int64)
+    K = c.shape[-1]
+    assert K % 8 == 0
+    nib = (c & 0xF).astype(np.uint32).reshape(*c.shape[:-1], K // 8, 8)
+    out = np.zeros(nib.shape[:-1], dtype=np.uint32)
+    for i in range(8):
+        out |= nib[..., i] << np.uint32(4 * i)
+    return out
+
+
+def pack_int3(codes: np.ndarray) -> np.ndarray:
+    """int codes in [-4, 3], shape [..., K] (K % 32 == 0) -> uint32 [..., K/32, 3]."""
+    c = np.asarray(codes, dtype=np.int64)
+    K = c.shape[-1]
+    assert K % 32 == 0
+    f = (c & 0x7).astype(np.uint64).reshape(*c.shape[:-1], K // 32, 32)
+    lo = np.zeros(f.shape[:-1], dtype=np.uint64)  # stream bits 0..63
+    hi = np.zeros(f.shape[:-1], dtype=np.uint64)  # stream bits 64..95
+    for i in range(32):
+        b = 3 * i
+        if b + 3 <= 64:
+            lo |= f[..., i] << np.uint64(b)
+        if b + 3 > 64 and b < 64:  # element 21 straddles bit 64
+            lo |= (f[..., i] << np.uint64(b)) & np.uint64(0xFFFFFFFFFFFFFFFF)
+            hi |= f[..., i] >> np.uint64(64 - b)
+        if b >= 64:
+            hi |= f[..., i] << np.uint64(b - 64)
+    out = np.empty((*f.shape[:-1], 3), dtype=np.uint32)
+    out[..., 0] = (lo & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    out[..., 1] = (lo >> np.uint64(32)).astype(np.uint32)
+    out[..., 2] = (hi & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    return out
+
+
+def pack_nibbles(codes: np.ndarray) -> np.ndarray:
+    """4-bit codes [..., K] (K even) -> uint8 [..., K/2], even k in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    assert c.shape[-1] % 2 == 0
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+# ----------------------------------------------------------------------------- problems
+def w4a16_problem(M, N, K, *, bits=4, E=1, cfg_id=0, seed=BASE_SEED,
+                  scale_lo=0.005, scale_hi=0.02, bias=False):
+    """Group-128 symmetric INT weights with BF16 scales and BF16 N(0,1) activations."""
+    qmax = 7 if bits == 4 else 3
+    q = uniform_int(stream(cfg_id, 1, seed), (E, N, K), -qmax, qmax).astype(np.int8)
+    s = to_bf16_bits(uniform(stream(cfg_id, 2, seed), (E, N, K // 128), scale_lo, scale_hi))
+    a = to_bf16_bits(normal(stream(cfg_id, 3, seed), (M, K)))
+    w = pack_int4(q) if bits == 4 else pack_int3(q)
+    out = dict(A=a, q=q, w_canon=w, s_canon=s, E=E, N=N, K=K, M=M, bits=bits)
+    if bias:
+        out["bias"] = to_bf16_bits(normal(stream(cfg_id, 4, seed), (E, N)))
+    return out
+
+
+def w4a8_problem(M, N, K, *, E=1, cfg_id=1, seed=BASE_SEED, sf_lo=118, sf_hi=126,
+                 bias=False):
+    """MXFP4 weights (uniform over the 16 E2M1 codes) and MXFP8 activations
+    (E4M3 codes of N(0,1) samples), both with group-32 E8M0 scales uniform in
+    [sf_lo, sf_hi]."""
+    nib = random_bytes(stream(cfg_id, 11, seed), E * N * K // 2)
+    w_canon = nib.reshape(E, N, K // 2)
+    w_sf = uniform_int(stream(cfg_id, 12, seed), (E, N, K // 32), sf_lo, sf_hi).astype(np.uint8)
+    a = to_e4m3_codes(normal(stream(cfg_id, 13, seed), (M, K)))
+    a_sf = uniform_int(stream(cfg_id, 14, seed), (M, K // 32), sf_lo, sf_hi).astype(np.uint8)
+    out = dict(A=a, A_sf=a_sf, w_canon=w_canon, s_canon=w_sf, E=E, N=N, K=K, M=M)
+    if bias:
+        out["bias"] = to_bf16_bits(normal(stream(cfg_id, 15, seed), (E, N)))
+    return out
+
+
+def unpack_nibbles_layout(w_canon: np.ndarray) -> np.ndarray:
+    """Inverse of :func:`pack_nibbles` (a layout helper for test inputs, no decoding)."""
+    lo = w_canon & 0xF
+    hi = w_canon >> 4
+    out = np.empty((*w_canon.shape[:-1], w_canon.shape[-1] * 2), dtype=np.uint8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
+
+
+def router_logits(T, E, *, cfg_id=3, seed=BASE_SEED, bias_std=1.5):
+    """Router logits N(0,1) plus a per-expert bias N(0, bias_std), float32 [T][E]."""
+    b = normal(stream(cfg_id, 21, seed), (E,), bias_std)
+    x = normal(stream(cfg_id, 22, seed), (T, E))
+    return (x + b[None, :]).astype(np.float32)
+
+
+__all__ = [
+    "BASE_SEED", "Stream", "stream", "uniform_int", "uniform", "normal", "random_bytes",
+    "to_bf16_bits", "to_e4m3_codes", "pack_int4", "pack_int3", "pack_nibbles",
+    "unpack_nibbles_layout", "w4a16_problem", "w4a8_problem", "router_logits",
+]

@@ -1,0 +1,203 @@
+"""Pins for the oracle GEMMs (CPU only): exact integer dot products, exact rational
+brute force on tiny shapes, and planted mistakes that the pins must catch."""
+from fractions import Fraction
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import formats as F
+from oracle import qgemm as Q
+import synth
+
+
+def bf16_bits_of(x):
+    return synth.to_bf16_bits(np.asarray(x, dtype=np.float64))
+
+
+# ----------------------------------------------------------------------------- W4A16
+def test_w4a16_exact_integer_dot():
+    """All scales 1.0 and integer activations (|a| <= 256 is exact in BF16): the float64
+    result must equal the int64 dot product exactly.  Shapes are non-square."""
+    rng = np.random.default_rng(10)
+    M, N, K = 5, 7, 384
+    a = rng.integers(-256, 257, (M, K))
+    q = rng.integers(-7, 8, (N, K))
+    s = np.full((N, K // 128), 0x3F80, dtype=np.uint16)  # BF16 1.0
+    R, absum = Q.gemm_w4a16(bf16_bits_of(a), q, s)
+    assert np.array_equal(R, (a @ q.T).astype(np.float64))
+    assert np.array_equal(absum, (np.abs(a) @ np.abs(q).T).astype(np.float64))
+
+
+def test_w4a16_exact_from_canonical_int3_and_int4():
+    rng = np.random.default_rng(11)
+    M, N, K = 3, 6, 256
+    a = rng.integers(-100, 101, (M, K))
+    for bits, qmax, pack in ((4, 7, synth.pack_int4), (3, 3, synth.pack_int3)):
+        q = rng.integers(-qmax, qmax + 1, (N, K))
+        s = np.full((N, K // 128), 0x3F80, dtype=np.uint16)
+        R, _ = Q.w4a16_from_canonical(bf16_bits_of(a), pack(q), s, K, bits)
+        assert np.array_equal(R, (a @ q.T).astype(np.float64))
+
+
+def _exact_w4a16(a_bits, q, s_bits, group=128):
+    """Exact rational evaluation; BF16 widened through torch (a library routine)."""
+    a = torch.from_numpy(a_bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    s = torch.from_numpy(s_bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    M, K = a.shape
+    N = q.shape[0]
+    R = [[Fraction(0)] * N for _ in range(M)]
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                acc += Fraction(a[m, k]) * int(q[n, k]) * Fraction(s[n, k // group])
+            R[m][n] = acc
+    return R
+
+
+def test_w4a16_fraction_brute_force_groups():
+    rng = np.random.default_rng(12)
+    M, N, K = 2, 3, 256  # two groups of 128
+    a_bits = bf16_bits_of(rng.standard_normal((M, K)))
+    q = rng.integers(-7, 8, (N, K))
+    s_bits = bf16_bits_of(rng.uniform(0.005, 0.02, (N, K // 128)))
+    R, absum = Q.gemm_w4a16(a_bits, q, s_bits)
+    ex = _exact_w4a16(a_bits, q, s_bits)
+    for m in range(M):
+        for n in range(N):
+            assert abs(Fraction(R[m, n]) - ex[m][n]) <= Fraction(2.0 ** -50) * Fraction(absum[m, n])
+
+
+def test_w4a16_bias_added():
+    rng = np.random.default_rng(13)
+    a = rng.integers(-8, 9, (2, 128))
+    q = rng.integers(-7, 8, (3, 128))
+    s = np.full((3, 1), 0x3F80, dtype=np.uint16)
+    b = bf16_bits_of([0.5, -2.0, 3.25])
+    R, _ = Q.gemm_w4a16(bf16_bits_of(a), q, s, b)
+    assert np.array_equal(R, a @ q.T + np.array([0.5, -2.0, 3.25])[None, :])
+
+
+# ----------------------------------------------------------------------------- W4A8
+E4M3_INT = {}  # integer value -> E4M3 code, built from torch's decoder (a library routine)
+for _c in range(256):
+    if (_c & 0x7F) == 0x7F:
+        continue
+    _v = float(torch.tensor([_c], dtype=torch.uint8).view(torch.float8_e4m3fn).double())
+    if _v == int(_v) and abs(_v) <= 16 and not (_v == 0 and _c != 0):
+        E4M3_INT[int(_v)] = _c
+E2M1_INT = {0: 0, 1: 2, 2: 4, 3: 5, 4: 6, 6: 7, -1: 10, -2: 12, -3: 13, -4: 14, -6: 15}
+
+
+def test_w4a8_exact_integer_dot():
+    """Scale bytes 127 (2^0) and integer-valued E4M3 / E2M1 codes: exact int64 match."""
+    rng = np.random.default_rng(20)
+    M, N, K = 4, 6, 96
+    av = rng.integers(-16, 17, (M, K))
+    wv = rng.choice(list(E2M1_INT), (N, K))
+    a_codes = np.vectorize(E4M3_INT.get)(av).astype(np.uint8)
+    w_codes = np.vectorize(E2M1_INT.get)(wv).astype(np.uint8)
+    R, absum = Q.gemm_w4a8(a_codes, np.full((M, K // 32), 127, np.uint8),
+                           w_codes, np.full((N, K // 32), 127, np.uint8))
+    assert np.array_equal(R, (av @ wv.T).astype(np.float64))
+    assert np.array_equal(absum, (np.abs(av) @ np.abs(wv).T).astype(np.float64))
+
+
+def test_w4a8_power_of_two_scales_exact():
+    """Per-group scale exponents: R = sum_g 2^(ea_g + ew_g - 254) * (int dot of group g)."""
+    rng = np.random.default_rng(21)
+    M, N, K = 3, 5, 128
+    av = rng.integers(-16, 17, (M, K))
+    wv = rng.choice(list(E2M1_INT), (N, K))
+    ea = rng.integers(118, 127, (M, K // 32))
+    ew = rng.integers(118, 127, (N, K // 32))
+    R, _ = Q.gemm_w4a8(np.vectorize(E4M3_INT.get)(av).astype(np.uint8), ea.astype(np.uint8),
+                       np.vectorize(E2M1_INT.get)(wv).astype(np.uint8), ew.astype(np.uint8))
+    for m in range(M):
+        for n in range(N):
+            exact = Fraction(0)
+            for g in range(K // 32):
+                d = int(av[m, 32 * g:32 * g + 32] @ wv[n, 32 * g:32 * g + 32])
+                exact += Fraction(d) * Fraction(2) ** (int(ea[m, g]) + int(ew[n, g]) - 254)
+            assert Fraction(R[m, n]) == exact
+
+
+def test_w4a8_fraction_brute_force_random_codes():
+    """Random codes over the whole E4M3 / E2M1 ranges, exact rationals via torch decoding."""
+    rng = np.random.default_rng(22)
+    M, N, K = 2, 3, 64
+    a_codes = synth.to_e4m3_codes(rng.standard_normal((M, K)) * 30)
+    w_codes = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    a_sf = rng.integers(118, 127, (M, K // 32)).astype(np.uint8)
+    w_sf = rng.integers(118, 127, (N, K // 32)).astype(np.uint8)
+    R, absum = Q.gemm_w4a8(a_codes, a_sf, w_codes, w_sf)
+    a = torch.from_numpy(a_codes).view(torch.float8_e4m3fn).double().numpy()
+    from test_oracle_formats import e2m1_closed_form
+    for m in range(M):
+        for n in range(N):
+            ex = sum(Fraction(a[m, k]) * Fraction(math.ldexp(1, int(a_sf[m, k // 32]) - 127))
+                     * Fraction(e2m1_closed_form(int(w_codes[n, k])))
+                     * Fraction(math.ldexp(1, int(w_sf[n, k // 32]) - 127)) for k in range(K))
+            assert abs(Fraction(R[m, n]) - ex) <= Fraction(2.0 ** -50) * Fraction(absum[m, n])
+
+
+def test_w4a8_from_canonical_nibble_order():
+    """k even in the low nibble: a weight row [1, 6, 0, ...] packs as byte 0x72."""
+    K = 32
+    w = np.zeros((1, K // 2), np.uint8)
+    w[0, 0] = 0x72  # k0 = code 2 (1.0), k1 = code 7 (6.0)
+    a = np.zeros((1, K), np.uint8)
+    a[0, 0] = E4M3_INT[3]
+    a[0, 1] = E4M3_INT[5]
+    sf = np.full((1, 1), 127, np.uint8)
+    R, _ = Q.w4a8_from_canonical(a, sf, w, sf, K)
+    assert R[0, 0] == 3 * 1 + 5 * 6
+
+
+# ----------------------------------------------------------------------------- acceptance checker
+def test_check_bf16_result_accepts_rounded_and_rejects_wrong():
+    rng = np.random.default_rng(30)
+    R = rng.standard_normal((16, 16)) * 10
+    absum = np.abs(R) * 4 + 1
+    ok, ratio, frob = Q.check_bf16_result(bf16_bits_of(R), R, absum)
+    assert ok and ratio < 0.5
+    bad = R.copy()
+    bad[3, 4] += 0.2 * absum[3, 4]
+    ok, _, _ = Q.check_bf16_result(bf16_bits_of(bad), R, absum)
+    assert not ok
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+def test_planted_wrong_e2m1_entry_is_caught(monkeypatch):
+    from test_oracle_formats import e2m1_closed_form
+    bad = F._E2M1_MAG.copy()
+    bad[5] = 2.5  # should be 3.0
+    monkeypatch.setattr(F, "_E2M1_MAG", bad)
+    got = F.decode_e2m1(np.arange(16))
+    assert not np.array_equal(got, [e2m1_closed_form(c) for c in range(16)])
+
+
+def test_planted_wrong_group_size_is_caught(monkeypatch):
+    orig = Q.dequant_mx
+
+    def wrong_group(codes, sf, decode):  # scale group 64 instead of 32
+        v = decode(codes)
+        return v * np.repeat(F.decode_e8m0(sf), 64, axis=-1)[..., :v.shape[-1]]
+
+    monkeypatch.setattr(Q, "dequant_mx", wrong_group)
+    with pytest.raises(AssertionError):
+        test_w4a8_power_of_two_scales_exact()
+    monkeypatch.setattr(Q, "dequant_mx", orig)
+
+
+def test_planted_transposed_operand_is_caught(monkeypatch):
+    def transposed(A_bits, q, s_bits, bias_bits=None, group=128):
+        a = F.decode_bf16(A_bits)
+        w = Q.dequant_int_weights(q, s_bits, group)
+        return (a @ w.T)[:, ::-1], np.abs(a) @ np.abs(w).T  # columns in the wrong order
+
+    monkeypatch.setattr(Q, "gemm_w4a16", transposed)
+    with pytest.raises(AssertionError):
+        test_w4a16_exact_integer_dot()
