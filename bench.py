@@ -1,0 +1,356 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized-GEMM hot path on GB300.
+
+Headline workload: the dense W4A8 (MXFP4 x MXFP8, group-32 E8M0) GEMM at
+(M, N, K) = (4096, 3072, 4096) and (4096, 14336, 4096); one step = both GEMMs through
+qgemm_dense, inputs resident in HBM, L2 flushed (a 256 MiB write) before every step
+outside the timed events.  Metric: TFLOP/s (2 M N K per GEMM).  Other workloads
+(W4A16 M=8 GEMV, M=1 decode sweep, MoE) are reported under "extra".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (float64 numpy) on a bounded sample of the same
+workload on this host's cores.  Under torchrun every rank runs an independent replica
+(the path has no exchange step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+SHAPES = [(4096, 3072, 4096), (4096, 14336, 4096)]
+METRIC = "W4A8/W4A16 GEMM TFLOPS and M=1 weight GB/s, % of GB300 roofline"
+WORKLOAD = "dense W4A8 MXFP4xMXFP8 g32 (4096,3072,4096)+(4096,14336,4096)"
+
+
+def flops_of(shapes):
+    return sum(2.0 * m * n * k for m, n, k in shapes)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        loaded = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- our arm
+class W4A8Problem:
+    def __init__(self, M, N, K, cfg_id=1):
+        import moe_qw_repack_gb300.qw as Q
+        self.Q = Q
+        p = synth.w4a8_problem(M, N, K, cfg_id=cfg_id)
+        self.M, self.N, self.K = M, N, K
+        self.desc = Q.qw_repack_query(Q.QW_W_MXFP4_G32, 1, N, K)
+        self.wp, self.sp = Q.empty_packed(self.desc)
+        err = Q.new_error_flag()
+        Q.qw_repack(self.desc, torch.from_numpy(p["w_canon"]).cuda(),
+                    torch.from_numpy(p["s_canon"]).cuda(), self.wp, self.sp, err)
+        assert Q.qw_read_error(err) == 0
+        self.A_host = torch.from_numpy(p["A"]).pin_memory()
+        self.Asf_host = torch.from_numpy(p["A_sf"]).pin_memory()
+        self.A = self.A_host.cuda()
+        self.Asf = self.Asf_host.cuda()
+        self.C = torch.empty((M, N), dtype=torch.int16, device="cuda")
+        self.C_host = torch.empty((M, N), dtype=torch.int16).pin_memory()
+        self.err = Q.new_error_flag()
+
+    def run(self, A=None, Asf=None):
+        Q = self.Q
+        Q.qgemm_dense(self.desc, self.wp, self.sp, Q.QW_A_MXFP8_G32, self.A if A is None else A,
+                      self.Asf if Asf is None else Asf, None, self.C, self.M, None, 0, self.err)
+
+
+def l2_flusher():
+    buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        buf.fill_(1)
+    return flush
+
+
+def time_steps(fns, steps, warmup, flush, world):
+    """Warm up, then time exactly `steps` steps; each step = fns in order, L2 flushed before
+    the step outside the events.  Returns (per-step ms list, per-fn ms lists)."""
+    for _ in range(warmup):
+        flush()
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in fns] for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        for j, f in enumerate(fns):
+            evs[i][j][0].record()
+            f()
+            evs[i][j][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    per_fn = [[evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(steps)] for j in range(len(fns))]
+    per_step = [sum(per_fn[j][i] for j in range(len(fns))) for i in range(steps)]
+    return per_step, per_fn
+
+
+def extra_w4a16(steps, warmup, flush, world):
+    """Config 1 (M=8, N=K=2048 INT4) and the M=1 decode sweep: kernel time, weight GB/s."""
+    import moe_qw_repack_gb300.qw as Q
+    out = {}
+    peaks, _ = measured_peaks()
+    cases = [("cfg1_w4a16_m8_2048x2048_int4", 8, 2048, 2048, 4)]
+    for bits in (4, 3):
+        for (N, K) in [(14336, 4096), (4096, 14336), (4096, 4096)]:
+            cases.append((f"cfg3_m1_{N}x{K}_int{bits}", 1, N, K, bits))
+    for name, M, N, K, bits in cases:
+        p = synth.w4a16_problem(M, N, K, bits=bits, cfg_id=0 if M == 8 else 2)
+        wfmt = Q.QW_W_INT4_G128_BF16 if bits == 4 else Q.QW_W_INT3_G128_BF16
+        d = Q.qw_repack_query(wfmt, 1, N, K)
+        wp, sp = Q.empty_packed(d)
+        Q.qw_repack(d, torch.from_numpy(p["w_canon"]).cuda(), torch.from_numpy(p["s_canon"]).cuda(), wp, sp)
+        A = torch.from_numpy(p["A"].view(np.int16)).cuda()
+        C = torch.empty((M, N), dtype=torch.int16, device="cuda")
+        fn = lambda: Q.qgemm_dense(d, wp, sp, Q.QW_A_BF16, A, None, None, C, M)  # noqa: E731
+        per_step, _ = time_steps([fn], steps, warmup, flush, world)
+        ms = statistics.median(per_step)
+        wbytes = N * K * bits / 8 + N * (K // 128) * 2  # packed weights + BF16 scales
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 2), "weight_GBps": round(gbs, 1),
+                     "hbm_frac": round(gbs / peaks["hbm_gbs"], 3),
+                     "tflops": round(2 * M * N * K / (ms * 1e-3) / 1e12, 3)}
+    return out
+
+
+def run_ours(args, world, rank):
+    import moe_qw_repack_gb300.qw as Q
+    peaks, peak_src = measured_peaks()
+    probs = [W4A8Problem(m, n, k) for m, n, k in SHAPES]
+    flush = l2_flusher()
+    fns = [pr.run for pr in probs]
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        t0 = time.perf_counter()
+        per_step, per_fn = time_steps(fns, args.steps, args.warmup, flush, world)
+        wall = time.perf_counter() - t0
+    for pr in probs:
+        code = Q.qw_read_error(pr.err)
+        if code != 0:
+            raise RuntimeError(f"device error flag {code}")
+    ms = max_over_ranks(sum(per_step) / len(per_step), world)
+    F = flops_of(SHAPES)
+    value = F * world / (ms * 1e-3) / 1e12
+    # roofline of the dominant kernel (the W4A8 GEMM, all of the step's launches)
+    kern_ms = sum(statistics.mean(v) for v in per_fn)
+    achieved = F / (kern_ms * 1e-3) / 1e12
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # FP8 dense = 2 x BF16 dense (nominal ratio 4.5 / 2.25)
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "gemm_w4a8_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath))
+            src = open(os.path.join(ROOT, "moe_qw_repack_gb300", "csrc", "gemm_w4a8_tc.cu"), "rb").read()
+            import hashlib
+            if tj.get("source_sha256") == hashlib.sha256(src).hexdigest():
+                traffic = tj.get("dram_bytes_per_step")
+        except (OSError, ValueError):
+            traffic = None
+
+    # end to end: pinned host inputs -> device, both GEMMs, results -> pinned host
+    def e2e_step():
+        for pr in probs:
+            pr.A.copy_(pr.A_host, non_blocking=True)
+            pr.Asf.copy_(pr.Asf_host, non_blocking=True)
+            pr.run()
+            pr.C_host.copy_(pr.C, non_blocking=True)
+    e_step, _ = time_steps([e2e_step], max(3, args.steps // 2), 2, flush, world)
+    e_ms = max_over_ranks(statistics.mean(e_step), world)
+    h2d = sum(pr.A.numel() + pr.Asf.numel() for pr in probs)
+    d2h = sum(pr.C.numel() * 2 for pr in probs)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xe2m1",
+        "data": "synthetic (splitmix64 seed 20261202; E2M1 uniform over 16 codes, E4M3 of N(0,1), "
+                "E8M0 uniform 118..126)",
+        "config": {"workload": WORKLOAD, "l2": "flushed (256 MiB write) before every step",
+                   "per_gemm_ms": [round(statistics.mean(v), 4) for v in per_fn],
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(F * world / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": len(fns) * args.steps,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(achieved / fp8_peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 burst x 2 (FP8 / BF16 nominal)"},
+        "clocks": clk.summary(),
+        "wall_s_timed_loop": round(wall, 3),
+    }
+    if not args.no_extra:
+        line["extra"] = extra_w4a16(max(5, args.steps), 3, flush, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    return line
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def cpu_baseline(rows_b=1024):
+    """Time the float64 oracle on a bounded sample: all of (4096,3072,4096) plus the first
+    `rows_b` rows of (4096,14336,4096)."""
+    from oracle import qgemm as OQ
+    sample = [(4096, 3072, 4096, None), (4096, 14336, 4096, np.arange(rows_b))]
+    flops = 0.0
+    t = 0.0
+    for M, N, K, rows in sample:
+        p = synth.w4a8_problem(M, N, K, cfg_id=1)
+        t0 = time.perf_counter()
+        OQ.w4a8_from_canonical(p["A"], p["A_sf"], p["w_canon"][0], p["s_canon"][0], K, rows=rows)
+        t += time.perf_counter() - t0
+        flops += 2.0 * (M if rows is None else len(rows)) * N * K
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(flops / t / 1e12, 5), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"(4096,3072,4096) all rows + (4096,14336,4096) first {rows_b} rows; "
+                      f"{flops / 1e9:.0f} GFLOP in {t:.1f} s (decode + float64 matmul)"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    vals = []
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; warm-up steps are skipped deliberately
+    cb = None
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cb = cpu_baseline(rows_b=256)
+        vals.append(cb["value"])
+    wall = time.perf_counter() - t0
+    v = statistics.median(vals)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall / args.steps * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": cb["sample"]},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        line = run_reference(args, world, rank)
+    else:
+        world, rank, _ = dist_setup()
+        line = run_ours(args, world, rank)
+    if line is not None and int(os.environ.get("RANK", "0")) == 0:
+        print(json.dumps(line), flush=True)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,225 @@
+/*
+ * qw.h - C ABI of the GB300 (sm_103a) low-bit weight-quantized GEMM library.
+ *
+ * The operations follow the Humming kernel library as its announcement describes it
+ * (spke.com, "quantized推論のための高速かつ柔軟なカーネル「Humming」を発表"):
+ *   - preprocessing validates parameters, pads dimensions and repacks the weight and
+ *     scale tensors into kernel-friendly layouts (section "ワークロードごとのチューニング
+ *     とJITコンパイル");
+ *   - dequantization and scaling run inside the kernel; scale and bias are fused into
+ *     the output stage (section "フォーマットとアーキテクチャを横断して共有される
+ *     CUDAコンポーネント");
+ *   - dense and MoE GEMMs have their own scheduling; MoE has a Grouped path over
+ *     expert-contiguous tokens (sections "WnA16" and "W8A8 / W4A8 / W4A4");
+ *   - symmetric integer weights are converted at preprocessing into a zero-exponent
+ *     code for fast dequantization (section "量子化サポート").
+ * Formats: W4A16 = group-128 symmetric INT4 / INT3 weights with BF16 scales times BF16
+ * activations; W4A8 = MXFP4 (E2M1 + group-32 E8M0) weights times MXFP8 (E4M3 + group-32
+ * E8M0) activations (aireiter.com "vLLM Humming performance benchmark", section
+ * "H100 group-32 W4A8").
+ *
+ * Conventions shared by every entry point
+ *   - The caller owns every buffer.  Pointers are DEVICE pointers unless the comment
+ *     says "host".  The library never allocates, never synchronises the stream (except
+ *     qw_read_error, which exists to do so) and never exits or asserts.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  All
+ *     device work of a call is enqueued on it, in order.
+ *   - Shape, pointer-alignment and size errors are detected on the host before any
+ *     launch and returned as a qw_status; nothing is enqueued in that case.
+ *   - Value errors found on the device (an INT4 code -8, an INT3 code -4, an E8M0 scale
+ *     0xFF, an E4M3 NaN scale is not checked) and bounded waits that gave up are
+ *     reported through `d_err` (int32 in device memory, may be NULL): the first error
+ *     code written wins (atomic compare-and-swap from 0).  The caller zeroes it and
+ *     reads it when convenient, e.g. with qw_read_error.
+ *   - Weights are logically [N][K] (output x input), activations [M][K] row-major,
+ *     results [M][N] row-major BF16 (round to nearest even of the FP32 accumulator).
+ *   - Every kernel is deterministic: no floating-point atomics, fixed reduction order.
+ */
+#ifndef QW_H
+#define QW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qw_status {
+  QW_OK = 0,
+  QW_ERR_INVALID_ARG = 1,  /* null pointer, non-positive or inconsistent size        */
+  QW_ERR_UNSUPPORTED = 2,  /* format / shape combination this build does not run      */
+  QW_ERR_ALIGNMENT = 3,    /* a pointer or pitch violates the stated alignment         */
+  QW_ERR_VALUE = 4,        /* a code outside its format's valid set (device-detected)  */
+  QW_ERR_WORKSPACE = 5,    /* workspace missing or smaller than the queried size       */
+  QW_ERR_TIMEOUT = 6,      /* a bounded device wait gave up (device-detected)          */
+  QW_ERR_CUDA = 7          /* a CUDA runtime / driver call failed                      */
+} qw_status;
+
+typedef enum qw_wfmt {
+  QW_W_INT4_G128_BF16 = 0, /* symmetric INT4 in [-7,7], BF16 scale per 128 along K      */
+  QW_W_INT3_G128_BF16 = 1, /* symmetric INT3 in [-3,3], BF16 scale per 128 along K      */
+  QW_W_MXFP4_G32 = 2       /* E2M1 codes, E8M0 scale per 32 along K                      */
+} qw_wfmt;
+
+typedef enum qw_afmt {
+  QW_A_BF16 = 0,           /* BF16 [rows][K]                                          */
+  QW_A_MXFP8_G32 = 1       /* E4M3 codes [rows][K] + E8M0 scales [rows][K/32]          */
+} qw_afmt;
+
+/* Description of one repacked weight set (E experts; E = 1 for a dense layer).
+ * Filled by qw_repack_query; treat as read-only. */
+typedef struct qw_packed_desc {
+  int32_t wfmt;            /* qw_wfmt                                                  */
+  int32_t E, N, K;         /* logical sizes                                            */
+  int32_t N_pad, K_pad;    /* padded sizes of the packed layout                        */
+  int32_t group;           /* 128 (INT) or 32 (MXFP4)                                  */
+  int32_t reserved;
+  uint64_t w_bytes;        /* size of w_packed in bytes (all experts)                  */
+  uint64_t s_bytes;        /* size of s_packed in bytes (all experts)                  */
+  uint64_t w_expert_stride;/* bytes between consecutive experts in w_packed            */
+  uint64_t s_expert_stride;/* bytes between consecutive experts in s_packed            */
+} qw_packed_desc;
+
+/* Status text (static storage; never NULL). */
+const char* qw_status_str(int32_t status);
+
+/* ABI version of this library (major * 100 + minor). */
+int32_t qw_version(void);
+
+/* --------------------------------------------------------------------------------------
+ * qw_repack_query - sizes of the packed layout for E experts of an N x K weight.
+ * Requirements: E >= 1, N >= 1, K >= 1; K % 128 == 0 for the INT formats, K % 32 == 0
+ * for MXFP4.  Padding: INT formats pad N to a multiple of 16; MXFP4 pads N to a multiple
+ * of 128 and K to a multiple of 128.  `out` is a host pointer.
+ * Returns QW_ERR_INVALID_ARG / QW_ERR_UNSUPPORTED on a bad request, else QW_OK.
+ */
+qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_packed_desc* out);
+
+/* --------------------------------------------------------------------------------------
+ * qw_repack - validate, pad and repack canonical weights and scales (the preprocessing
+ * step of the spke.com announcement, section "ワークロードごとのチューニングとJITコンパイル").
+ *
+ * Canonical inputs (device, contiguous, experts outermost):
+ *   INT4:  w_canon uint32 [E][N][K/8]; element k = 8j+i at bits [4i,4i+4) of word j,
+ *          two's complement.  s_canon BF16 [E][N][K/128].
+ *   INT3:  w_canon uint32 [E][N][K/32][3]; a 96-bit little-endian stream per 32
+ *          elements, element i at stream bits [3i,3i+3), two's complement.
+ *          s_canon BF16 [E][N][K/128].
+ *   MXFP4: w_canon uint8 [E][N][K/2], even k in the low nibble.  s_canon uint8 E8M0
+ *          [E][N][K/32].
+ * Packed outputs (device, sizes from `desc`, 256-byte aligned):
+ *   INT4:  per expert [K/128][N_pad/16] blocks of 1 KiB: 32 lanes x 8 words; word w of
+ *          lane l holds the eight weights that lane l of an m16n8k16 MMA needs for the
+ *          w-th 16-wide k step of the group, as excess-8 nibbles (q + 8).
+ *          Scales BF16 [K/128][N_pad].
+ *   INT3:  per expert [K/128][N_pad/16] blocks of 768 B: 32 lanes x 4 words holding the
+ *          low two bits of q + 4 for the lane's 64 weights, then 32 lanes x 2 words
+ *          holding their third bit.  Scales BF16 [K/128][N_pad].
+ *   MXFP4: codes uint8 [N_pad][K_pad/2] (canonical order, zero-padded); scales E8M0 in
+ *          512-byte chunks per 128 rows x 4 groups, chunk (r/128, g/4) at
+ *          ((r/128) * (K_pad/128) + g/4) * 512, byte (r%32)*16 + ((r%128)/32)*4 + g%4;
+ *          padding bytes are 127 (scale 1).
+ * The zero-exponent codes: the announcement's section "量子化サポート" states that a
+ * symmetric INT without its minimum has the value set of a float with zero exponent
+ * bits; the excess code used here is that value set shifted so that its bit pattern
+ * drops straight into a BF16 mantissa (one logic op and one subtract per two weights).
+ * Device-detected errors: INT4 -8, INT3 -4, E8M0 0xFF -> QW_ERR_VALUE in *d_err (the
+ * offending element is packed as 0).  Alignment: w_canon / s_canon 4-byte aligned
+ * (INT) or 1 (MXFP4); w_packed / s_packed 256-byte aligned.
+ */
+qw_status qw_repack(const qw_packed_desc* desc, const void* w_canon, const void* s_canon,
+                    void* w_packed, void* s_packed, int32_t* d_err, void* stream);
+
+/* qw_unpack - exact inverse of qw_repack (for round-trip checks): writes canonical
+ * w_canon / s_canon from the packed buffers.  Padding is dropped. */
+qw_status qw_unpack(const qw_packed_desc* desc, const void* w_packed, const void* s_packed,
+                    void* w_canon, void* s_canon, int32_t* d_err, void* stream);
+
+/* --------------------------------------------------------------------------------------
+ * qgemm_workspace_size - bytes of device workspace qgemm_dense / qgemm_moe_grouped need
+ * for up to `max_rows` activation rows (host output `bytes`; 0 is a valid answer).
+ */
+qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t max_rows,
+                               uint64_t* bytes);
+
+/* --------------------------------------------------------------------------------------
+ * qgemm_dense - C[M][N] = bf16( sum_k a[m,k] * w[n,k] + bias[n] ) with the weight
+ * dequantization (and, for W4A8, both block scales) applied inside the kernel.
+ *   W4A16: desc->wfmt INT4/INT3, afmt QW_A_BF16, A BF16 [M][K], A_sf NULL.
+ *   W4A8:  desc->wfmt MXFP4,     afmt QW_A_MXFP8_G32, A E4M3 [M][K], A_sf E8M0 [M][K/32].
+ *   bias:  BF16 [N] or NULL.  C: BF16 [M][N].  desc->E must be 1.
+ * Dispatch by M (the device heuristic of the announcement, section "デバイスパラメータに
+ * 基づくパフォーマンスチューニング"): W4A16 with M <= 64 streams the weights through a
+ * split-K tensor-core GEMV; W4A8 runs the TMA + tcgen05 block-scaled GEMM.
+ * Alignment: A, C 16-byte aligned with K % 8 == 0 (BF16) or K % 16 == 0 (E4M3);
+ * A_sf 4-byte aligned.  M >= 0 (M == 0 is a no-op).
+ */
+qw_status qgemm_dense(const qw_packed_desc* desc, const void* w_packed, const void* s_packed,
+                      int32_t afmt, const void* A, const void* A_sf, const void* bias,
+                      void* C, int64_t M, void* workspace, uint64_t ws_bytes,
+                      int32_t* d_err, void* stream);
+
+/* --------------------------------------------------------------------------------------
+ * qgemm_moe_route - top-k routing and expert sort for the Grouped MoE layout.
+ *   logits float32 [T][E] (device).  Outputs (device, int32):
+ *     topk_ids      [T][topk]: the topk experts with the largest logit in descending
+ *                   order, equal logits to the lower expert index;
+ *     expert_offsets[E+1]: exclusive prefix sum of the per-expert pair counts;
+ *     sorted_pairs  [T*topk]: pair ids p = t*topk + j ordered by (expert, p).
+ *   Requires 1 <= topk <= 32, topk <= E <= 1024, T >= 0.  Workspace from
+ *   qgemm_moe_route_workspace_size.  Bit-exact and deterministic.
+ */
+qw_status qgemm_moe_route_workspace_size(int32_t T, int32_t E, int32_t topk, uint64_t* bytes);
+qw_status qgemm_moe_route(const float* logits, int32_t T, int32_t E, int32_t topk,
+                          int32_t* topk_ids, int32_t* sorted_pairs, int32_t* expert_offsets,
+                          void* workspace, uint64_t ws_bytes, int32_t* d_err, void* stream);
+
+/* --------------------------------------------------------------------------------------
+ * qgemm_moe_permute - gather activation rows into the expert-contiguous order:
+ *   A_sorted[r] = A[sorted_pairs[r] / topk] for r < P (and the same for A_sf rows when
+ *   afmt is QW_A_MXFP8_G32; A_sf / A_sf_sorted are NULL for BF16).
+ *   A: [T][K] in afmt; A_sorted: [P][K].  Rows are 16-byte aligned (K*elem % 16 == 0).
+ */
+qw_status qgemm_moe_permute(int32_t afmt, const void* A, const void* A_sf, int32_t K,
+                            const int32_t* sorted_pairs, int64_t P, int32_t topk,
+                            void* A_sorted, void* A_sf_sorted, void* stream);
+
+/* --------------------------------------------------------------------------------------
+ * qgemm_moe_grouped - Grouped MoE GEMM: for every expert e and every row r in
+ * [expert_offsets[e], expert_offsets[e+1]):
+ *   C[r][n] = bf16( sum_k A_sorted[r][k] * W_e[n][k] + bias[e][n] ).
+ *   expert_offsets: device int32 [E+1], non-decreasing, offsets[0] == 0 and
+ *   offsets[E] == total_rows (read on the device; no host round trip).
+ *   A_sorted / A_sf_sorted as for qgemm_dense with total_rows rows; bias BF16 [E][N] or
+ *   NULL; C BF16 [total_rows][N].  The per-expert tile queue is built on the device in
+ *   the workspace (qgemm_workspace_size with max_rows = total_rows).  Dimensions need
+ *   not be multiples of 256 (e.g. an intermediate size of 640).
+ */
+qw_status qgemm_moe_grouped(const qw_packed_desc* desc, const void* w_packed,
+                            const void* s_packed, int32_t afmt, const void* A_sorted,
+                            const void* A_sf_sorted, const int32_t* expert_offsets,
+                            int64_t total_rows, const void* bias, void* C, void* workspace,
+                            uint64_t ws_bytes, int32_t* d_err, void* stream);
+
+/* --------------------------------------------------------------------------------------
+ * qw_read_error - synchronise `stream`, copy *d_err to the host (`host_code`, host
+ * pointer) and return it as a qw_status (QW_ERR_CUDA if the synchronisation fails).
+ */
+qw_status qw_read_error(const int32_t* d_err, void* stream, int32_t* host_code);
+
+/* --------------------------------------------------------------------------------------
+ * qw_test_wait_timeout - diagnostics for the bounded waits every kernel relies on: one
+ * CTA waits on an mbarrier that nothing ever arrives on, through the same bounded-wait
+ * routine the GEMM pipelines use, and must give up after `limit_ns` (0 .. 2e9) with
+ * QW_ERR_TIMEOUT in *d_err.  It exercises failure handling without hanging or
+ * faulting the GPU.  (Failure handling of this kind is the pages' own advice: keep a
+ * fallback because shape routing and backend checks fail - aireiter.com, "Backend
+ * routing can block a valid Humming configuration".)
+ */
+qw_status qw_test_wait_timeout(int32_t* d_err, int64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QW_H */

@@ -1,0 +1,417 @@
+// gemm_w4a8_tc.cu - large-M W4A8 path: MXFP4 weights x MXFP8 activations on the
+// sm_103a block-scaled tensor cores.
+//
+// What it computes (aireiter.com "vLLM Humming performance benchmark", section "H100
+// group-32 W4A8": MXFP4 weights, MXFP8 activations, group-32 scales; spke.com Humming
+// announcement, section "W8A8 / W4A8 / W4A4": Blackwell runs the MX formats natively):
+//   C[m][n] = bf16( sum_k e4m3(a[m][k]) 2^(sa[m][k/32]-127) e2m1(w[n][k]) 2^(sw[n][k/32]-127)
+//                   + bias[n] )
+// The pages' Hopper design upcasts FP4 to FP8 inside the SM; on sm_103a the tensor core
+// takes E4M3 x E2M1 with per-32 E8M0 scales directly (tcgen05.mma kind::mxf8f6f4
+// block_scale), so the "dequantization" is the MMA itself.
+//
+// Structure (one persistent CTA per SM, 128 x 256 output tiles, K in steps of 128):
+//   warp 0      TMA producer: A tile (E4M3, 128 x 128 B, 128-byte swizzle), B tile
+//               (E2M1 codes unpacked by TMA to one byte per code, 256 x 128), and the
+//               repacked B scale chunks (bulk copies) into a 4-stage ring;
+//   warp 1      TMEM owner and single-thread MMA issuer: tcgen05.cp the stage's scale
+//               factors into TMEM, four 128x256x32 block-scaled MMAs, commit -> frees
+//               the stage; commit -> accumulator full at the end of a tile;
+//   warp 2      A scale loader: reads the canonical [rows][K/32] E8M0 bytes and writes
+//               the 32 x 16-byte image tcgen05.cp expects (row r -> lane r % 32,
+//               column r / 32, byte = group within the 128-wide K step);
+//   warps 3-10  epilogue: tcgen05.ld the FP32 accumulator (each warp one 32-lane
+//               quadrant x 128 columns), add bias, round to BF16, release TMEM, store.
+// Every mbarrier wait is bounded; on expiry the kernel raises QW_ERR_TIMEOUT, lets its
+// copies in flight land, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "qw_common.cuh"
+#include "qw_internal.h"
+
+namespace qw {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int A_BYTES = BM * BK;  // E4M3, one byte per element
+constexpr int B_BYTES = BN * BK;  // E2M1 unpacked by TMA: 16 codes in 8 bytes + 8 gap bytes
+constexpr int B_TX_BYTES = BN * BK / 2;  // the unpacking load credits the packed global bytes
+constexpr int SFA_BYTES = 512, SFB_CHUNK = 512, SFB_BYTES = 2 * SFB_CHUNK;
+constexpr int NUM_WARPS = 11, NUM_THREADS = NUM_WARPS * 32;
+constexpr int EPI_WARP0 = 3, NUM_EPI_WARPS = 8;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_COL0 = 256;      // accumulator uses columns [0, 256)
+constexpr uint32_t SF_COLS_PER_STAGE = 12;  // 4 (A: 128 rows) + 8 (B: 256 rows)
+constexpr size_t SMEM_BYTES =
+    (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + 256 + 1024;
+
+// Instruction descriptor, kind::mxf8f6f4: A = E4M3 (0), B = E2M1 (5), both K-major,
+// N >> 3 at bit 17, scale type UE8M0 (bit 23), M >> 4 at bit 24; the B / A scale
+// factor byte selectors sit at bits 4 and 29.
+constexpr uint32_t IDESC = (0u << 7) | (5u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+struct Params {
+  int64_t rows;           // activation rows (M, or total grouped rows)
+  int32_t N, N_pad, K, K_pad;
+  int32_t num_m_tiles;    // dense only
+  int32_t num_n_tiles;
+  const uint8_t* A_sf;    // [rows][K/32]
+  const uint8_t* s_packed;
+  int64_t s_estride;
+  const uint16_t* bias;   // [E][N] or null
+  uint16_t* C;            // [rows][N]
+  const int32_t* queue;   // grouped tile queue (BM rows per entry) or null
+  int32_t* err;
+};
+
+struct Tile {
+  int e, n0;
+  int64_t rb, re;
+};
+
+__device__ __forceinline__ Tile tile_at(const Params& p, int64_t t) {
+  Tile x;
+  const int nb = (int)(t % p.num_n_tiles);
+  const int64_t mt = t / p.num_n_tiles;
+  x.n0 = nb * BN;
+  if (p.queue) {
+    x.e = __ldg(p.queue + 1 + 3 * mt);
+    x.rb = __ldg(p.queue + 2 + 3 * mt);
+    x.re = __ldg(p.queue + 3 + 3 * mt);
+  } else {
+    x.e = 0;
+    x.rb = mt * BM;
+    x.re = min64(p.rows, x.rb + BM);
+  }
+  return x;
+}
+
+__device__ __forceinline__ uint32_t load_sf_word(const Params& p, int64_t r, int kb) {
+  const int G = p.K / 32;  // canonical groups per row
+  const int g0 = kb * 4;
+  if (r >= p.rows) return 0x7F7F7F7Fu;
+  const uint8_t* row = p.A_sf + r * (int64_t)G;
+  if ((G & 3) == 0 && g0 + 3 < G) return __ldg(reinterpret_cast<const uint32_t*>(row + g0));
+  uint32_t w = 0;
+  for (int j = 0; j < 4; ++j) w |= (uint32_t)(g0 + j < G ? __ldg(row + g0 + j) : 127) << (8 * j);
+  return w;
+}
+
+// Wait for a phase without the CTA-wide abort shortcut (used when draining copies).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_w4a8_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + STAGES * A_BYTES;
+  uint8_t* sSFA = sB + STAGES * B_BYTES;
+  uint8_t* sSFB = sSFA + STAGES * SFA_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * SFB_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* final_bar = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1 + 32);  // producer arrive.expect_tx + 32 scale-loader lanes
+      mbar_init(&empty[s], 1);      // MMA commit
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, NUM_EPI_WARPS);
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const int64_t num_m = p.queue ? (int64_t)__ldg(p.queue) : (int64_t)p.num_m_tiles;
+  const int64_t num_tiles = num_m * p.num_n_tiles;
+  const int KB = p.K_pad / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_phase = 0;  // per-stage bitmasks for the final drain
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        const Tile x = tile_at(p, t);
+        const int nchunks = (x.n0 + 128 < p.N_pad) ? 2 : 1;
+        const uint8_t* sfb = p.s_packed + x.e * p.s_estride;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_TX_BYTES + nchunks * SFB_CHUNK);
+          tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, (int32_t)x.rb);
+          tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK,
+                      x.e * p.N_pad + x.n0);
+          for (int c = 0; c < nchunks; ++c)
+            bulk_load(sSFB + stage * SFB_BYTES + c * SFB_CHUNK,
+                      sfb + ((int64_t)(x.n0 / 128 + c) * KB + kb) * SFB_CHUNK, SFB_CHUNK,
+                      &full[stage]);
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // let every copy this thread issued land before shared memory goes away
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s)) drain_wait(&full[s], (issued_phase >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_col = tbase + SF_COL0 + stage * SF_COLS_PER_STAGE;
+          const uint32_t sfb_col = sfa_col + 4;
+          tc_cp_32x128b_warpx4(sfa_col, smem_desc(smem_u32(sSFA + stage * SFA_BYTES), 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfb_col, smem_desc(smem_u32(sSFB + stage * SFB_BYTES), 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfb_col + 4, smem_desc(smem_u32(sSFB + stage * SFB_BYTES + SFB_CHUNK),
+                                                      0, 128, 0));
+          const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk) {
+            const uint64_t ad = smem_desc(a0 + kk * 32, 16, 1024, 2);
+            const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
+            const uint32_t id = IDESC | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
+            tc_mma_mxf8f6f4(tbase, ad, bd, id, sfa_col, sfb_col, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+        acc_phase ^= 1u;
+      }
+      // every MMA this thread issued has finished before TMEM is released
+      tc_commit(final_bar);
+      drain_wait(final_bar, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ A scale loader
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      const Tile x = tile_at(p, t);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        uint4 v;
+        v.x = load_sf_word(p, x.rb + lane, kb);
+        v.y = load_sf_word(p, x.rb + 32 + lane, kb);
+        v.z = load_sf_word(p, x.rb + 64 + lane, kb);
+        v.w = load_sf_word(p, x.rb + 96 + lane, kb);
+        *reinterpret_cast<uint4*>(sSFA + stage * SFA_BYTES + lane * 16) = v;
+        fence_proxy_async_smem();
+        mbar_arrive(&full[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                        // TMEM lane quadrant of this warp
+    const int half = (warp - EPI_WARP0) / 4;       // accumulator columns [128 half, +128)
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const Tile x = tile_at(p, t);
+      if (!mbar_wait(acc_full, acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int64_t row = x.rb + 32 * q + lane;
+      const int col0 = x.n0 + 128 * half;
+      uint32_t packed[64];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t r[32];
+        tc_ld_32x32b_x32(tbase + ((uint32_t)(32 * q) << 16) + 128 * half + 32 * j, r);
+        tc_wait_ld();
+        float b[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) b[i] = 0.f;
+        if (p.bias) {
+          const uint16_t* bp = p.bias + (int64_t)x.e * p.N + col0 + 32 * j;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col0 + 32 * j + i < p.N) b[i] = __uint_as_float((uint32_t)__ldg(bp + i) << 16);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          packed[16 * j + i] = pack_bf16x2(__uint_as_float(r[2 * i]) + b[2 * i],
+                                           __uint_as_float(r[2 * i + 1]) + b[2 * i + 1]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      if (row < x.re) {
+        uint16_t* crow = p.C + row * (int64_t)p.N + col0;
+        if (col0 + 128 <= p.N && (p.N & 7) == 0) {
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            reinterpret_cast<uint4*>(crow)[v] =
+                make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            if (col0 + 2 * i < p.N) crow[2 * i] = (uint16_t)(packed[i] & 0xFFFFu);
+            if (col0 + 2 * i + 1 < p.N) crow[2 * i + 1] = (uint16_t)(packed[i] >> 16);
+          }
+        }
+      }
+      acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+}  // namespace
+
+uint64_t gemm_w4a8_workspace(const qw_packed_desc& d, int64_t max_rows) {
+  return d.E > 1 ? tile_queue_bytes(d.E, max_rows, BM) : 0;
+}
+
+qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                           const void* A, const void* A_sf, const void* bias, void* C,
+                           const RowSet& rs, void* ws, uint64_t ws_bytes, int32_t* err,
+                           cudaStream_t st) {
+  if (rs.rows == 0) return QW_OK;
+  auto enc = encode_fn();
+  if (!enc) return QW_ERR_CUDA;
+  if (rs.rows > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
+
+  CUtensorMap tmA, tmB;
+  {
+    cuuint64_t gdim[2] = {(cuuint64_t)d.K, (cuuint64_t)rs.rows};
+    cuuint64_t gstr[1] = {(cuuint64_t)d.K};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(A), gdim, gstr, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QW_ERR_ALIGNMENT;
+  }
+  {
+    cuuint64_t gdim[2] = {(cuuint64_t)d.K_pad, (cuuint64_t)d.E * (cuuint64_t)d.N_pad};
+    cuuint64_t gstr[1] = {(cuuint64_t)(d.K_pad / 2)};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tmB, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(w_packed), gdim,
+            gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QW_ERR_ALIGNMENT;
+  }
+
+  Params p{};
+  p.rows = rs.rows;
+  p.N = d.N;
+  p.N_pad = d.N_pad;
+  p.K = d.K;
+  p.K_pad = d.K_pad;
+  p.num_n_tiles = (d.N + BN - 1) / BN;
+  p.num_m_tiles = (int32_t)((rs.rows + BM - 1) / BM);
+  p.A_sf = static_cast<const uint8_t*>(A_sf);
+  p.s_packed = static_cast<const uint8_t*>(s_packed);
+  p.s_estride = (int64_t)d.s_expert_stride;
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.C = static_cast<uint16_t*>(C);
+  p.err = err;
+  int64_t max_m_tiles = p.num_m_tiles;
+  if (rs.offsets) {
+    const uint64_t need = tile_queue_bytes(rs.E, rs.rows, BM);
+    if (ws == nullptr || ws_bytes < need) return QW_ERR_WORKSPACE;
+    int32_t* queue = static_cast<int32_t*>(ws);
+    max_m_tiles = (int64_t)(need / 4 - 1) / 3;
+    qw_status s = launch_build_tile_queue(rs.offsets, rs.E, BM, queue, max_m_tiles, err, st);
+    if (s != QW_OK) return s;
+    p.queue = queue;
+  }
+
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_w4a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return QW_ERR_CUDA;
+
+  const int64_t tiles_max = max_m_tiles * p.num_n_tiles;
+  const int sms = device_sm_count();
+  const unsigned grid = (unsigned)(tiles_max < sms ? (tiles_max < 1 ? 1 : tiles_max) : sms);
+  gemm_w4a8_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
+
+}  // namespace qw

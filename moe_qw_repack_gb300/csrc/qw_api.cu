@@ -1,0 +1,266 @@
+// qw_api.cu - the extern "C" entry points declared in include/qw.h: host-side
+// validation of every argument (the library returns a status and never asserts; the
+// pages' vLLM issue #60700 is the cautionary tale of a shape check that asserted) and
+// dispatch to the kernels.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "../../include/qw.h"
+#include "qw_internal.h"
+
+namespace qw {
+
+int device_sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+qw_status check_desc(const qw_packed_desc* d) {
+  if (!d) return QW_ERR_INVALID_ARG;
+  qw_packed_desc ref;
+  if (qw_repack_query(d->wfmt, d->E, d->N, d->K, &ref) != QW_OK) return QW_ERR_INVALID_ARG;
+  if (ref.N_pad != d->N_pad || ref.K_pad != d->K_pad || ref.w_bytes != d->w_bytes ||
+      ref.s_bytes != d->s_bytes || ref.group != d->group)
+    return QW_ERR_INVALID_ARG;
+  return QW_OK;
+}
+
+qw_status check_afmt(const qw_packed_desc* d, int32_t afmt, const void* A_sf) {
+  if (d->wfmt == QW_W_MXFP4_G32) {
+    if (afmt != QW_A_MXFP8_G32) return QW_ERR_UNSUPPORTED;
+    if (!A_sf) return QW_ERR_INVALID_ARG;
+  } else {
+    if (afmt != QW_A_BF16) return QW_ERR_UNSUPPORTED;
+  }
+  return QW_OK;
+}
+
+}  // namespace
+}  // namespace qw
+
+using namespace qw;
+
+extern "C" {
+
+const char* qw_status_str(int32_t s) {
+  switch (s) {
+    case QW_OK: return "ok";
+    case QW_ERR_INVALID_ARG: return "invalid argument";
+    case QW_ERR_UNSUPPORTED: return "unsupported format or shape";
+    case QW_ERR_ALIGNMENT: return "misaligned pointer or pitch";
+    case QW_ERR_VALUE: return "code outside its format's valid set";
+    case QW_ERR_WORKSPACE: return "workspace missing or too small";
+    case QW_ERR_TIMEOUT: return "bounded device wait gave up";
+    case QW_ERR_CUDA: return "CUDA call failed";
+    default: return "unknown status";
+  }
+}
+
+int32_t qw_version(void) { return 100; }
+
+qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_packed_desc* out) {
+  if (!out || E < 1 || N < 1 || K < 1) return QW_ERR_INVALID_ARG;
+  qw_packed_desc d{};
+  d.wfmt = wfmt;
+  d.E = E;
+  d.N = N;
+  d.K = K;
+  switch (wfmt) {
+    case QW_W_INT4_G128_BF16:
+    case QW_W_INT3_G128_BF16: {
+      if (K % kIntGroup) return QW_ERR_UNSUPPORTED;
+      d.group = kIntGroup;
+      d.N_pad = (int32_t)round_up(N, 16);
+      d.K_pad = K;
+      const int64_t blocks = (int64_t)(K / kIntGroup) * (d.N_pad / 16);
+      d.w_expert_stride =
+          (uint64_t)blocks * (wfmt == QW_W_INT4_G128_BF16 ? kInt4BlockBytes : kInt3BlockBytes);
+      d.s_expert_stride = (uint64_t)round_up((int64_t)(K / kIntGroup) * d.N_pad * 2, 256);
+      break;
+    }
+    case QW_W_MXFP4_G32: {
+      if (K % kMxGroup) return QW_ERR_UNSUPPORTED;
+      d.group = kMxGroup;
+      d.N_pad = (int32_t)round_up(N, 128);
+      d.K_pad = (int32_t)round_up(K, 128);
+      d.w_expert_stride = (uint64_t)d.N_pad * (d.K_pad / 2);
+      d.s_expert_stride = (uint64_t)(d.N_pad / 128) * (d.K_pad / 128) * kSfChunkBytes;
+      break;
+    }
+    default:
+      return QW_ERR_UNSUPPORTED;
+  }
+  if ((int64_t)d.N_pad * E > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
+  d.w_bytes = d.w_expert_stride * (uint64_t)E;
+  d.s_bytes = d.s_expert_stride * (uint64_t)E;
+  *out = d;
+  return QW_OK;
+}
+
+qw_status qw_repack(const qw_packed_desc* desc, const void* w_canon, const void* s_canon,
+                    void* w_packed, void* s_packed, int32_t* d_err, void* stream) {
+  qw_status s = check_desc(desc);
+  if (s != QW_OK) return s;
+  if (!w_canon || !s_canon || !w_packed || !s_packed) return QW_ERR_INVALID_ARG;
+  if (desc->wfmt != QW_W_MXFP4_G32 && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
+    return QW_ERR_ALIGNMENT;
+  if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
+  return launch_repack(*desc, w_canon, s_canon, w_packed, s_packed, d_err,
+                       static_cast<cudaStream_t>(stream));
+}
+
+qw_status qw_unpack(const qw_packed_desc* desc, const void* w_packed, const void* s_packed,
+                    void* w_canon, void* s_canon, int32_t* d_err, void* stream) {
+  qw_status s = check_desc(desc);
+  if (s != QW_OK) return s;
+  if (!w_canon || !s_canon || !w_packed || !s_packed) return QW_ERR_INVALID_ARG;
+  if (desc->wfmt != QW_W_MXFP4_G32 && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
+    return QW_ERR_ALIGNMENT;
+  if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
+  return launch_unpack(*desc, w_packed, s_packed, w_canon, s_canon, d_err,
+                       static_cast<cudaStream_t>(stream));
+}
+
+qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t max_rows,
+                               uint64_t* bytes) {
+  qw_status s = check_desc(desc);
+  if (s != QW_OK) return s;
+  if (!bytes || max_rows < 0) return QW_ERR_INVALID_ARG;
+  if ((s = check_afmt(desc, afmt, reinterpret_cast<const void*>(1))) != QW_OK) return s;
+  *bytes = desc->wfmt == QW_W_MXFP4_G32 ? gemm_w4a8_workspace(*desc, max_rows)
+                                        : gemv_w4a16_workspace(*desc, max_rows);
+  return QW_OK;
+}
+
+static qw_status check_gemm_args(const qw_packed_desc* desc, const void* w_packed,
+                                 const void* s_packed, int32_t afmt, const void* A,
+                                 const void* A_sf, void* C, int64_t rows) {
+  qw_status s = check_desc(desc);
+  if (s != QW_OK) return s;
+  if ((s = check_afmt(desc, afmt, A_sf)) != QW_OK) return s;
+  if (rows < 0) return QW_ERR_INVALID_ARG;
+  if (rows > 0 && (!w_packed || !s_packed || !A || !C)) return QW_ERR_INVALID_ARG;
+  if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
+  if (!aligned(A, 16) || !aligned(C, 4)) return QW_ERR_ALIGNMENT;
+  if (desc->wfmt == QW_W_MXFP4_G32) {
+    if (desc->K % 16) return QW_ERR_ALIGNMENT;  // TMA row pitch of the E4M3 activations
+    if (!aligned(A_sf, 4)) return QW_ERR_ALIGNMENT;
+  } else if (desc->K % 8) {
+    return QW_ERR_ALIGNMENT;
+  }
+  return QW_OK;
+}
+
+qw_status qgemm_dense(const qw_packed_desc* desc, const void* w_packed, const void* s_packed,
+                      int32_t afmt, const void* A, const void* A_sf, const void* bias, void* C,
+                      int64_t M, void* workspace, uint64_t ws_bytes, int32_t* d_err,
+                      void* stream) {
+  qw_status s = check_gemm_args(desc, w_packed, s_packed, afmt, A, A_sf, C, M);
+  if (s != QW_OK) return s;
+  if (desc->E != 1) return QW_ERR_INVALID_ARG;
+  if (bias && !aligned(bias, 2)) return QW_ERR_ALIGNMENT;
+  if (M == 0) return QW_OK;
+  RowSet rs{M, nullptr, 1};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (desc->wfmt == QW_W_MXFP4_G32)
+    return launch_gemm_w4a8(*desc, w_packed, s_packed, A, A_sf, bias, C, rs, workspace, ws_bytes,
+                            d_err, st);
+  return launch_gemv_w4a16(*desc, w_packed, s_packed, A, bias, C, rs, workspace, ws_bytes, d_err,
+                           st);
+}
+
+qw_status qgemm_moe_route_workspace_size(int32_t T, int32_t E, int32_t topk, uint64_t* bytes) {
+  if (!bytes || T < 0 || topk < 1 || topk > 32 || E < topk || E > 1024) return QW_ERR_INVALID_ARG;
+  *bytes = moe_route_workspace(T, E, topk);
+  return QW_OK;
+}
+
+qw_status qgemm_moe_route(const float* logits, int32_t T, int32_t E, int32_t topk,
+                          int32_t* topk_ids, int32_t* sorted_pairs, int32_t* expert_offsets,
+                          void* workspace, uint64_t ws_bytes, int32_t* d_err, void* stream) {
+  if (T < 0 || topk < 1 || topk > 32 || E < topk || E > 1024) return QW_ERR_INVALID_ARG;
+  if (!expert_offsets) return QW_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !topk_ids || !sorted_pairs)) return QW_ERR_INVALID_ARG;
+  if ((int64_t)T * topk > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
+  if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(sorted_pairs, 4) ||
+      !aligned(expert_offsets, 4))
+    return QW_ERR_ALIGNMENT;
+  if (!workspace || ws_bytes < moe_route_workspace(T, E, topk)) return QW_ERR_WORKSPACE;
+  return launch_moe_route(logits, T, E, topk, topk_ids, sorted_pairs, expert_offsets, workspace,
+                          ws_bytes, d_err, static_cast<cudaStream_t>(stream));
+}
+
+qw_status qgemm_moe_permute(int32_t afmt, const void* A, const void* A_sf, int32_t K,
+                            const int32_t* sorted_pairs, int64_t P, int32_t topk, void* A_sorted,
+                            void* A_sf_sorted, void* stream) {
+  if (afmt != QW_A_BF16 && afmt != QW_A_MXFP8_G32) return QW_ERR_UNSUPPORTED;
+  if (K < 1 || P < 0 || topk < 1) return QW_ERR_INVALID_ARG;
+  if (P == 0) return QW_OK;
+  if (!A || !sorted_pairs || !A_sorted) return QW_ERR_INVALID_ARG;
+  const int64_t row_bytes = (int64_t)K * (afmt == QW_A_BF16 ? 2 : 1);
+  if (row_bytes % 16 || !aligned(A, 16) || !aligned(A_sorted, 16) || !aligned(sorted_pairs, 4))
+    return QW_ERR_ALIGNMENT;
+  if (afmt == QW_A_MXFP8_G32) {
+    if (K % 32) return QW_ERR_UNSUPPORTED;
+    if (!A_sf || !A_sf_sorted) return QW_ERR_INVALID_ARG;
+  }
+  return launch_moe_permute(afmt, A, A_sf, K, sorted_pairs, P, topk, A_sorted, A_sf_sorted,
+                            static_cast<cudaStream_t>(stream));
+}
+
+qw_status qgemm_moe_grouped(const qw_packed_desc* desc, const void* w_packed,
+                            const void* s_packed, int32_t afmt, const void* A_sorted,
+                            const void* A_sf_sorted, const int32_t* expert_offsets,
+                            int64_t total_rows, const void* bias, void* C, void* workspace,
+                            uint64_t ws_bytes, int32_t* d_err, void* stream) {
+  qw_status s = check_gemm_args(desc, w_packed, s_packed, afmt, A_sorted, A_sf_sorted, C,
+                                total_rows);
+  if (s != QW_OK) return s;
+  if (!expert_offsets || !aligned(expert_offsets, 4)) return QW_ERR_INVALID_ARG;
+  if (desc->E > 1024) return QW_ERR_UNSUPPORTED;
+  if (bias && !aligned(bias, 2)) return QW_ERR_ALIGNMENT;
+  if (total_rows == 0) return QW_OK;
+  uint64_t need = 0;
+  qgemm_workspace_size(desc, afmt, total_rows, &need);
+  if (!workspace || ws_bytes < need) return QW_ERR_WORKSPACE;
+  RowSet rs{total_rows, expert_offsets, desc->E};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (desc->wfmt == QW_W_MXFP4_G32)
+    return launch_gemm_w4a8(*desc, w_packed, s_packed, A_sorted, A_sf_sorted, bias, C, rs,
+                            workspace, ws_bytes, d_err, st);
+  return launch_gemv_w4a16(*desc, w_packed, s_packed, A_sorted, bias, C, rs, workspace, ws_bytes,
+                           d_err, st);
+}
+
+qw_status qw_read_error(const int32_t* d_err, void* stream, int32_t* host_code) {
+  if (!d_err || !host_code) return QW_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QW_ERR_CUDA;
+  if (cudaMemcpy(host_code, d_err, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return QW_ERR_CUDA;
+  return static_cast<qw_status>(*host_code);
+}
+
+qw_status qw_test_wait_timeout(int32_t* d_err, int64_t limit_ns, void* stream) {
+  if (!d_err || limit_ns < 0 || limit_ns > 2000000000LL) return QW_ERR_INVALID_ARG;
+  return launch_wait_timeout_probe(d_err, limit_ns, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// qw_internal.h - host-side launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/qw.h"
+
+namespace qw {
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// Packed-layout geometry shared by repack and the GEMM kernels.
+constexpr int kIntGroup = 128;       // K elements per BF16 scale (INT formats)
+constexpr int kMxGroup = 32;         // K elements per E8M0 scale (MX formats)
+constexpr int kInt4BlockBytes = 1024;  // 16 rows x 128 k of INT4, fragment order
+constexpr int kInt3BlockBytes = 768;   // 16 rows x 128 k of INT3 (two bit planes)
+constexpr int kSfChunkBytes = 512;     // 128 rows x 4 groups of E8M0 scales
+
+qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void* s_canon,
+                        void* w_packed, void* s_packed, int32_t* err, cudaStream_t st);
+qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                        void* w_canon, void* s_canon, int32_t* err, cudaStream_t st);
+
+// Rows of a GEMM call: dense (offsets == nullptr, rows [0, M)) or grouped by expert
+// (device offsets [E+1]; the work list of (expert, row tile) is built on the device).
+struct RowSet {
+  int64_t rows;                // M (dense) or total rows (grouped)
+  const int32_t* offsets;      // device [E+1] or nullptr
+  int32_t E;
+};
+
+// Small-M W4A16: tensor-core GEMV over the fragment-ordered packed weights.
+qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                            const void* A, const void* bias, void* C, const RowSet& rs,
+                            void* ws, uint64_t ws_bytes, int32_t* err, cudaStream_t st);
+uint64_t gemv_w4a16_workspace(const qw_packed_desc& d, int64_t max_rows);
+
+// Large-M W4A8: TMA + tcgen05 block-scaled GEMM.
+qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                           const void* A, const void* A_sf, const void* bias, void* C,
+                           const RowSet& rs, void* ws, uint64_t ws_bytes, int32_t* err,
+                           cudaStream_t st);
+uint64_t gemm_w4a8_workspace(const qw_packed_desc& d, int64_t max_rows);
+
+// MoE scheduling.
+qw_status launch_moe_route(const float* logits, int32_t T, int32_t E, int32_t topk,
+                           int32_t* topk_ids, int32_t* sorted_pairs, int32_t* offsets, void* ws,
+                           uint64_t ws_bytes, int32_t* err, cudaStream_t st);
+uint64_t moe_route_workspace(int32_t T, int32_t E, int32_t topk);
+qw_status launch_moe_permute(int32_t afmt, const void* A, const void* A_sf, int32_t K,
+                             const int32_t* sorted_pairs, int64_t P, int32_t topk,
+                             void* A_sorted, void* A_sf_sorted, cudaStream_t st);
+
+// Device tile queue for grouped GEMMs: entry = (expert, row_begin, row_end) for each
+// tile of `tile_rows` rows of every expert; count at queue[0].
+uint64_t tile_queue_bytes(int32_t E, int64_t rows, int32_t tile_rows);
+qw_status launch_build_tile_queue(const int32_t* offsets, int32_t E, int32_t tile_rows,
+                                  int32_t* queue, int64_t max_entries, int32_t* err,
+                                  cudaStream_t st);
+
+qw_status launch_wait_timeout_probe(int32_t* err, int64_t limit_ns, cudaStream_t st);
+
+}  // namespace qw

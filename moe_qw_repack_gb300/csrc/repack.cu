@@ -1,0 +1,371 @@
+// repack.cu - preprocessing: validate, pad and repack canonical weights and scales
+// into the layouts the GEMM kernels stream (spke.com Humming announcement, section
+// "ワークロードごとのチューニングとJITコンパイル": preprocessing validates parameters,
+// pads dimensions and repacks tensors for the target kernel), plus the exact inverse.
+//
+// Integer weights are rewritten as excess codes (q + 2^(b-1)): the zero-exponent
+// value set of section "量子化サポート" shifted so that the code drops directly into
+// a BF16 mantissa next to a fixed exponent.
+#include "qw_common.cuh"
+#include "qw_internal.h"
+
+namespace qw {
+namespace {
+
+// ----------------------------------------------------------------------------- INT4
+// Canonical nibble of (row n, column k): two's complement, word k/8, bits 4*(k%8).
+__device__ __forceinline__ uint32_t int4_canon_nib(const uint32_t* wc, int32_t K, int64_t n,
+                                                   int32_t k) {
+  return (wc[n * (K / 8) + k / 8] >> (4 * (k % 8))) & 0xFu;
+}
+
+// Mapping of one packed INT4 word (lane l, k16 step s of a 16 x 128 block) to the
+// weights it holds: nibble i feeds register r = i & 3 of the m16n8k16 A fragment,
+// half h = i >> 2; row = g + 8 * (r & 1), k = 2t + h + 8 * (r >> 1), g = l / 4, t = l % 4.
+__device__ __forceinline__ void int4_nib_pos(int l, int s, int i, int& row, int& k) {
+  const int g = l >> 2, t = l & 3, r = i & 3, h = i >> 2;
+  row = g + 8 * (r & 1);
+  k = 16 * s + 2 * t + h + 8 * (r >> 1);
+}
+
+__global__ void repack_int4_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K, int32_t* err) {
+  const int64_t per_expert = (int64_t)(K / 128) * (N_pad / 16) * 256;
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    int64_t rem = idx % per_expert;
+    const int64_t blk = rem / 256;  // G * (N_pad/16) + nb
+    const int w = (int)(rem % 256);
+    const int lane = w / 8, s = w % 8;
+    const int G = (int)(blk / (N_pad / 16));
+    const int nb = (int)(blk % (N_pad / 16));
+    const uint32_t* wce = wc + e * (int64_t)N * (K / 8);
+    uint32_t out = 0;
+    for (int i = 0; i < 8; ++i) {
+      int row, k;
+      int4_nib_pos(lane, s, i, row, k);
+      const int64_t n = (int64_t)nb * 16 + row;
+      uint32_t nib = 0;  // q = 0 for padding rows
+      if (n < N) {
+        nib = int4_canon_nib(wce, K, n, G * 128 + k);
+        if (nib == 8u) {  // -8 is outside the symmetric range
+          set_error(err, QW_ERR_VALUE);
+          nib = 0;
+        }
+      }
+      out |= ((nib ^ 8u) & 0xFu) << (4 * i);  // excess-8 code q + 8
+    }
+    wp[idx] = out;
+  }
+}
+
+__global__ void unpack_int4_kernel(const uint32_t* __restrict__ wp, uint32_t* __restrict__ wc,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K) {
+  // one thread per canonical word (8 consecutive k of one row)
+  const int64_t per_expert = (int64_t)N * (K / 8);
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t n = rem / (K / 8);
+    const int k0 = (int)(rem % (K / 8)) * 8;
+    const uint32_t* wpe = wp + e * (int64_t)(K / 128) * (N_pad / 16) * 256;
+    uint32_t out = 0;
+    for (int j = 0; j < 8; ++j) {
+      const int k = k0 + j;
+      const int G = k / 128, kk = k % 128, s = kk / 16, kl = kk % 16;
+      const int nb = (int)(n / 16), row = (int)(n % 16);
+      // invert int4_nib_pos: row = g + 8(r&1), kl = 2t + h + 8(r>>1)
+      const int g = row & 7, r0 = row >> 3, r1 = kl >> 3, t = (kl & 7) >> 1, h = kl & 1;
+      const int lane = g * 4 + t, i = (r0 | (r1 << 1)) + 4 * h;
+      const uint32_t word = wpe[((int64_t)G * (N_pad / 16) + nb) * 256 + lane * 8 + s];
+      const uint32_t code = (word >> (4 * i)) & 0xFu;
+      out |= ((code ^ 8u) & 0xFu) << (4 * j);
+    }
+    wc[idx] = out;
+  }
+}
+
+// ----------------------------------------------------------------------------- INT3
+__device__ __forceinline__ int32_t int3_canon(const uint32_t* wc, int32_t K, int64_t n, int32_t k) {
+  const uint32_t* blk = wc + (n * (K / 32) + k / 32) * 3;
+  const int bit = 3 * (k % 32);
+  const int w = bit / 32, off = bit % 32;
+  uint32_t v = blk[w] >> off;
+  if (off > 29) v |= blk[w + 1] << (32 - off);
+  v &= 7u;
+  return (v >= 4u) ? (int32_t)v - 8 : (int32_t)v;
+}
+
+// Packed INT3 of lane l, step s, register r, half h: the lo plane keeps u & 3 in word
+// s/2 at bits 2 * (4 * (s % 2) + r) + 16 h; the hi plane keeps u >> 2 in word s/4 at bit
+// 4 * (s % 4) + r + 16 h; u = q + 4.
+__global__ void repack_int3_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K, int32_t* err) {
+  const int64_t per_expert = (int64_t)(K / 128) * (N_pad / 16) * 32;  // (block, lane)
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t blk = rem / 32;
+    const int lane = (int)(rem % 32);
+    const int G = (int)(blk / (N_pad / 16));
+    const int nb = (int)(blk % (N_pad / 16));
+    const uint32_t* wce = wc + e * (int64_t)N * (K / 32) * 3;
+    uint32_t lo[4] = {0, 0, 0, 0}, hi[2] = {0, 0};
+    const int g = lane >> 2, t = lane & 3;
+    for (int s = 0; s < 8; ++s)
+      for (int r = 0; r < 4; ++r)
+        for (int h = 0; h < 2; ++h) {
+          const int row = g + 8 * (r & 1);
+          const int k = G * 128 + 16 * s + 2 * t + h + 8 * (r >> 1);
+          const int64_t n = (int64_t)nb * 16 + row;
+          int32_t q = 0;
+          if (n < N) {
+            q = int3_canon(wce, K, n, k);
+            if (q == -4) {
+              set_error(err, QW_ERR_VALUE);
+              q = 0;
+            }
+          }
+          const uint32_t u = (uint32_t)(q + 4);
+          lo[s / 2] |= (u & 3u) << (2 * (4 * (s % 2) + r) + 16 * h);
+          hi[s / 4] |= ((u >> 2) & 1u) << (4 * (s % 4) + r + 16 * h);
+        }
+    uint32_t* out = wp + e * (int64_t)(K / 128) * (N_pad / 16) * 192 + blk * 192;
+    for (int i = 0; i < 4; ++i) out[lane * 4 + i] = lo[i];
+    for (int i = 0; i < 2; ++i) out[128 + lane * 2 + i] = hi[i];
+  }
+}
+
+__global__ void unpack_int3_kernel(const uint32_t* __restrict__ wp, uint32_t* __restrict__ wc,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K) {
+  // one thread per canonical 32-element block (3 words)
+  const int64_t per_expert = (int64_t)N * (K / 32);
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t n = rem / (K / 32);
+    const int k0 = (int)(rem % (K / 32)) * 32;
+    const uint32_t* wpe = wp + e * (int64_t)(K / 128) * (N_pad / 16) * 192;
+    uint32_t w3[3] = {0, 0, 0};
+    for (int j = 0; j < 32; ++j) {
+      const int k = k0 + j;
+      const int G = k / 128, kk = k % 128, s = kk / 16, kl = kk % 16;
+      const int nb = (int)(n / 16), row = (int)(n % 16);
+      const int g = row & 7, r = (row >> 3) | ((kl >> 3) << 1), t = (kl & 7) >> 1, h = kl & 1;
+      const int lane = g * 4 + t;
+      const uint32_t* blk = wpe + ((int64_t)G * (N_pad / 16) + nb) * 192;
+      const uint32_t L = blk[lane * 4 + s / 2], H = blk[128 + lane * 2 + s / 4];
+      const uint32_t u = ((L >> (2 * (4 * (s % 2) + r) + 16 * h)) & 3u) |
+                         (((H >> (4 * (s % 4) + r + 16 * h)) & 1u) << 2);
+      const uint32_t code = (uint32_t)((int32_t)u - 4) & 7u;  // back to two's complement
+      const int bit = 3 * j;
+      w3[bit / 32] |= code << (bit % 32);
+      if (bit % 32 > 29) w3[bit / 32 + 1] |= code >> (32 - bit % 32);
+    }
+    uint32_t* o = wc + idx * 3;
+    o[0] = w3[0];
+    o[1] = w3[1];
+    o[2] = w3[2];
+  }
+}
+
+// ----------------------------------------------------------------------------- INT scales
+// canonical [E][N][K/128] <-> packed [E][K/128][N_pad] (zero padded)
+__global__ void repack_int_scales_kernel(const uint16_t* __restrict__ sc, uint16_t* __restrict__ sp,
+                                         int32_t E, int32_t N, int32_t N_pad, int32_t G) {
+  const int64_t total = (int64_t)E * G * N_pad;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / ((int64_t)G * N_pad);
+    const int64_t rem = idx % ((int64_t)G * N_pad);
+    const int g = (int)(rem / N_pad);
+    const int n = (int)(rem % N_pad);
+    sp[idx] = (n < N) ? sc[(e * N + n) * G + g] : (uint16_t)0;
+  }
+}
+__global__ void unpack_int_scales_kernel(const uint16_t* __restrict__ sp, uint16_t* __restrict__ sc,
+                                         int32_t E, int32_t N, int32_t N_pad, int32_t G) {
+  const int64_t total = (int64_t)E * N * G;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / ((int64_t)N * G);
+    const int64_t rem = idx % ((int64_t)N * G);
+    const int n = (int)(rem / G);
+    const int g = (int)(rem % G);
+    sc[idx] = sp[(e * G + g) * N_pad + n];
+  }
+}
+
+// ----------------------------------------------------------------------------- MXFP4
+// codes: canonical [E][N][K/2] -> packed [E][N_pad][K_pad/2], 4 bytes per thread
+__global__ void repack_mxfp4_codes_kernel(const uint8_t* __restrict__ wc, uint8_t* __restrict__ wp,
+                                          int32_t E, int32_t N, int32_t N_pad, int32_t K,
+                                          int32_t K_pad) {
+  const int64_t wpr = K_pad / 8;  // packed words per row
+  const int64_t total = (int64_t)E * N_pad * wpr;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t er = idx / wpr;  // e * N_pad + n
+    const int64_t e = er / N_pad;
+    const int64_t n = er % N_pad;
+    const int64_t b0 = (idx % wpr) * 4;  // byte within the packed row
+    uint32_t v = 0;
+    if (n < N) {
+      const uint8_t* src = wc + (e * N + n) * (int64_t)(K / 2);
+      for (int j = 0; j < 4; ++j)
+        if (b0 + j < K / 2) v |= (uint32_t)src[b0 + j] << (8 * j);
+    }
+    reinterpret_cast<uint32_t*>(wp)[idx] = v;
+  }
+}
+__global__ void unpack_mxfp4_codes_kernel(const uint8_t* __restrict__ wp, uint8_t* __restrict__ wc,
+                                          int32_t E, int32_t N, int32_t N_pad, int32_t K,
+                                          int32_t K_pad) {
+  const int64_t total = (int64_t)E * N * (K / 2);
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t er = idx / (K / 2);
+    const int64_t e = er / N, n = er % N;
+    const int64_t b = idx % (K / 2);
+    wc[idx] = wp[(e * N_pad + n) * (int64_t)(K_pad / 2) + b];
+  }
+}
+
+// Offset of scale (row r, group g) in the 128 x 4 chunked layout of one expert.
+__device__ __forceinline__ int64_t sf_chunk_offset(int64_t r, int g, int K_pad) {
+  return ((r / 128) * (K_pad / 128) + g / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + g % 4;
+}
+
+__global__ void repack_mx_scales_kernel(const uint8_t* __restrict__ sc, uint8_t* __restrict__ sp,
+                                        int32_t E, int32_t N, int32_t N_pad, int32_t K,
+                                        int32_t K_pad, int32_t* err) {
+  const int Gp = K_pad / 32, Gc = K / 32;
+  const int64_t per_expert = (int64_t)N_pad * Gp;
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t r = rem / Gp;
+    const int g = (int)(rem % Gp);
+    uint8_t v = 127;  // scale 1 for padding
+    if (r < N && g < Gc) {
+      v = sc[(e * N + r) * Gc + g];
+      if (v == 0xFF) {
+        set_error(err, QW_ERR_VALUE);
+        v = 127;
+      }
+    }
+    sp[e * per_expert + sf_chunk_offset(r, g, K_pad)] = v;
+  }
+}
+__global__ void unpack_mx_scales_kernel(const uint8_t* __restrict__ sp, uint8_t* __restrict__ sc,
+                                        int32_t E, int32_t N, int32_t N_pad, int32_t K,
+                                        int32_t K_pad) {
+  const int Gp = K_pad / 32, Gc = K / 32;
+  const int64_t total = (int64_t)E * N * Gc;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / ((int64_t)N * Gc);
+    const int64_t rem = idx % ((int64_t)N * Gc);
+    const int64_t r = rem / Gc;
+    const int g = (int)(rem % Gc);
+    sc[idx] = sp[e * (int64_t)N_pad * Gp + sf_chunk_offset(r, g, K_pad)];
+  }
+}
+
+int grid_for(int64_t total, int threads) {
+  int64_t b = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)device_sm_count() * 32;
+  if (b > cap) b = cap;
+  return (int)(b < 1 ? 1 : b);
+}
+
+}  // namespace
+
+qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void* s_canon,
+                        void* w_packed, void* s_packed, int32_t* err, cudaStream_t st) {
+  const int T = 256;
+  switch (d.wfmt) {
+    case QW_W_INT4_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 256;
+      repack_int4_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_canon,
+                                                        (uint32_t*)w_packed, d.E, d.N, d.N_pad,
+                                                        d.K, err);
+      break;
+    }
+    case QW_W_INT3_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 32;
+      repack_int3_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_canon,
+                                                        (uint32_t*)w_packed, d.E, d.N, d.N_pad,
+                                                        d.K, err);
+      break;
+    }
+    case QW_W_MXFP4_G32: {
+      const int64_t tw = (int64_t)d.E * d.N_pad * (d.K_pad / 8);
+      repack_mxfp4_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
+          (const uint8_t*)w_canon, (uint8_t*)w_packed, d.E, d.N, d.N_pad, d.K, d.K_pad);
+      const int64_t ts = (int64_t)d.E * d.N_pad * (d.K_pad / 32);
+      repack_mx_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
+          (const uint8_t*)s_canon, (uint8_t*)s_packed, d.E, d.N, d.N_pad, d.K, d.K_pad, err);
+      break;
+    }
+    default:
+      return QW_ERR_UNSUPPORTED;
+  }
+  if (d.wfmt != QW_W_MXFP4_G32) {
+    const int64_t ts = (int64_t)d.E * (d.K / 128) * d.N_pad;
+    repack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
+        (const uint16_t*)s_canon, (uint16_t*)s_packed, d.E, d.N, d.N_pad, d.K / 128);
+  }
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
+
+qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                        void* w_canon, void* s_canon, int32_t* err, cudaStream_t st) {
+  (void)err;
+  const int T = 256;
+  switch (d.wfmt) {
+    case QW_W_INT4_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * d.N * (d.K / 8);
+      unpack_int4_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_packed,
+                                                        (uint32_t*)w_canon, d.E, d.N, d.N_pad,
+                                                        d.K);
+      break;
+    }
+    case QW_W_INT3_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * d.N * (d.K / 32);
+      unpack_int3_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_packed,
+                                                        (uint32_t*)w_canon, d.E, d.N, d.N_pad,
+                                                        d.K);
+      break;
+    }
+    case QW_W_MXFP4_G32: {
+      const int64_t tw = (int64_t)d.E * d.N * (d.K / 2);
+      unpack_mxfp4_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
+          (const uint8_t*)w_packed, (uint8_t*)w_canon, d.E, d.N, d.N_pad, d.K, d.K_pad);
+      const int64_t ts = (int64_t)d.E * d.N * (d.K / 32);
+      unpack_mx_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
+          (const uint8_t*)s_packed, (uint8_t*)s_canon, d.E, d.N, d.N_pad, d.K, d.K_pad);
+      break;
+    }
+    default:
+      return QW_ERR_UNSUPPORTED;
+  }
+  if (d.wfmt != QW_W_MXFP4_G32) {
+    const int64_t ts = (int64_t)d.E * d.N * (d.K / 128);
+    unpack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
+        (const uint16_t*)s_packed, (uint16_t*)s_canon, d.E, d.N, d.N_pad, d.K / 128);
+  }
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
+
+}  // namespace qw

@@ -9,7 +9,8 @@ GAMMA = 0x9E3779B97F4A7C15, and ``mix64`` the published finaliser
 ``z ^= z >> 30; z *= 0xBF58476D1CE4E5B9; z ^= z >> 27; z *= 0x94D049BB133111EB;
 z ^= z >> 31``.  The key itself is ``mix64(seed * GAMMA + tensor_id)``.
 
-* uniform integers in [lo, hi]: Lemire's multiply-shift on the top 32 bits,
+* uniform integers in [lo, hi]: Lemire's multiply-shift on each 32-bit half of a
+  draw (high half first),
 * uniform reals in [0, 1): the top 53 bits times 2^-53,
 * normals: Box-Muller on two consecutive uniforms (cos and sin branch).
 
@@ -66,32 +67,52 @@ def stream(cfg_id: int, tensor_id: int, seed: int = BASE_SEED) -> Stream:
 
 
 # ----------------------------------------------------------------------------- draws
+_CHUNK = 1 << 24  # draws per chunk (keeps the uint64 temporaries small)
+
+
+def _chunks(n):
+    for lo in range(0, n, _CHUNK):
+        yield lo, min(n, lo + _CHUNK)
+
+
 def uniform_int(st: Stream, shape, lo: int, hi: int) -> np.ndarray:
+    """Two draws per 64-bit output: element 2j from its high 32 bits, 2j+1 from its low
+    32 bits, each mapped to [lo, hi] by Lemire's multiply-shift."""
     n = int(np.prod(shape))
     span = np.uint64(hi - lo + 1)
-    top = st.u64(n) >> np.uint64(32)
-    with np.errstate(over="ignore"):
-        r = (top * span) >> np.uint64(32)
-    return (r.astype(np.int64) + lo).reshape(shape)
+    out = np.empty(n + 1, dtype=np.int64 if (hi > 127 or lo < -128) else np.int16)
+    for a, b in _chunks(n):
+        z = st.u64((b - a + 1) // 2)
+        with np.errstate(over="ignore"):
+            hi32 = ((z >> np.uint64(32)) * span) >> np.uint64(32)
+            lo32 = ((z & np.uint64(0xFFFFFFFF)) * span) >> np.uint64(32)
+        out[a:a + 2 * z.size:2] = hi32.astype(np.int64) + lo
+        out[a + 1:a + 2 * z.size:2] = lo32.astype(np.int64) + lo
+    return out[:n].reshape(shape)
 
 
 def uniform(st: Stream, shape, lo: float = 0.0, hi: float = 1.0) -> np.ndarray:
     n = int(np.prod(shape))
-    u = (st.u64(n) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
-    return (lo + (hi - lo) * u).reshape(shape)
+    out = np.empty(n, dtype=np.float64)
+    for a, b in _chunks(n):
+        u = (st.u64(b - a) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        out[a:b] = lo + (hi - lo) * u
+    return out.reshape(shape)
 
 
 def normal(st: Stream, shape, std: float = 1.0) -> np.ndarray:
     n = int(np.prod(shape))
-    pairs = (n + 1) // 2
-    u = (st.u64(2 * pairs) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
-    u1 = 1.0 - u[0::2]  # (0, 1]
-    u2 = u[1::2]
-    r = np.sqrt(-2.0 * np.log(u1))
-    z = np.empty(2 * pairs, dtype=np.float64)
-    z[0::2] = r * np.cos(2.0 * np.pi * u2)
-    z[1::2] = r * np.sin(2.0 * np.pi * u2)
-    return (std * z[:n]).reshape(shape)
+    out = np.empty(n + 1, dtype=np.float64)
+    for a, b in _chunks(n):
+        m = b - a
+        pairs = (m + 1) // 2
+        u = (st.u64(2 * pairs) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        u1 = 1.0 - u[0::2]  # (0, 1]
+        u2 = u[1::2]
+        r = np.sqrt(-2.0 * np.log(u1))
+        out[a:a + 2 * pairs:2] = r * np.cos(2.0 * np.pi * u2)
+        out[a + 1:a + 2 * pairs:2] = r * np.sin(2.0 * np.pi * u2)
+    return (std * out[:n]).reshape(shape)
 
 
 def random_bytes(st: Stream, n: int) -> np.ndarray:
@@ -114,14 +135,11 @@ def to_e4m3_codes(x: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------- packing
 def pack_int4(codes: np.ndarray) -> np.ndarray:
     """int codes in [-8, 7], shape [..., K] (K % 8 == 0) -> uint32 [..., K/8]."""
-    c = np.asarray(codes, dtype=np.int64)
-    K = c.shape[-1]
-    assert K % 8 == 0
-    nib = (c & 0xF).astype(np.uint32).reshape(*c.shape[:-1], K // 8, 8)
-    out = np.zeros(nib.shape[:-1], dtype=np.uint32)
-    for i in range(8):
-        out |= nib[..., i] << np.uint32(4 * i)
-    return out
+    c = np.asarray(codes)
+    assert c.shape[-1] % 8 == 0
+    nib = (c.astype(np.int8).view(np.uint8) & np.uint8(0xF))
+    # two nibbles per byte (even k low), four bytes per little-endian word
+    return np.ascontiguousarray(pack_nibbles(nib)).view("<u4").astype(np.uint32, copy=False)
 
 
 def pack_int3(codes: np.ndarray) -> np.ndarray:

@@ -1,0 +1,119 @@
+"""The C-ABI library loads, exports every symbol include/qw.h declares, and rejects bad
+arguments on the host (no GPU needed: validation happens before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "qw.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(q\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def Q():
+    import moe_qw_repack_gb300.qw as q
+    return q
+
+
+def test_header_declares_the_boundary():
+    fns = header_functions()
+    for name in ("qw_repack", "qw_unpack", "qw_repack_query", "qgemm_dense", "qgemm_moe_grouped",
+                 "qgemm_moe_route", "qgemm_moe_permute", "qgemm_workspace_size"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(Q):
+    lib = ctypes.CDLL(Q.lib_path())
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    assert set(header_functions()) <= set(Q.EXPORTS)
+
+
+def test_status_strings(Q):
+    for s in range(8):
+        assert Q.status_str(s)
+    assert Q.status_str(99) == "unknown status"
+
+
+@pytest.mark.parametrize("wfmt,N,K,npad,kpad,wb,sb", [
+    (0, 2048, 2048, 2048, 2048, 2048 * 2048 // 2, 2048 * 16 * 2),
+    (0, 40, 256, 48, 256, 48 * 256 // 2, 256),  # scales padded to 256 B
+    (1, 4096, 4096, 4096, 4096, 4096 * 4096 * 3 // 8, 4096 * 32 * 2),
+    (2, 3072, 4096, 3072, 4096, 3072 * 2048, 3072 * 128),
+    (2, 640, 96, 640, 128, 640 * 64, 640 * 4),
+])
+def test_repack_query_sizes(Q, wfmt, N, K, npad, kpad, wb, sb):
+    d = Q.qw_repack_query(wfmt, 1, N, K)
+    assert (d.N_pad, d.K_pad, d.w_bytes, d.s_bytes) == (npad, kpad, wb, sb)
+
+
+def test_repack_query_rejects(Q):
+    for args in [(0, 1, 16, 100), (1, 1, 16, 64), (2, 1, 16, 48), (9, 1, 16, 128), (0, 0, 16, 128),
+                 (0, 1, 0, 128)]:
+        with pytest.raises(Q.QwError):
+            Q.qw_repack_query(*args)
+
+
+def test_gemm_host_validation(Q):
+    d = Q.qw_repack_query(Q.QW_W_MXFP4_G32, 1, 256, 256)
+    good = 1 << 20  # fake, never dereferenced: every call below fails validation first
+    with pytest.raises(Q.QwError) as e:  # wrong activation format for MXFP4 weights
+        Q.qgemm_dense(d, good, good, Q.QW_A_BF16, good, None, None, good, 4, stream=0)
+    assert e.value.status == Q.QW_ERR_UNSUPPORTED
+    with pytest.raises(Q.QwError) as e:  # missing activation scales
+        Q.qgemm_dense(d, good, good, Q.QW_A_MXFP8_G32, good, None, None, good, 4, stream=0)
+    assert e.value.status == Q.QW_ERR_INVALID_ARG
+    with pytest.raises(Q.QwError) as e:  # misaligned packed weights
+        Q.qgemm_dense(d, good + 16, good, Q.QW_A_MXFP8_G32, good, good, None, good, 4, stream=0)
+    assert e.value.status == Q.QW_ERR_ALIGNMENT
+    with pytest.raises(Q.QwError) as e:  # negative M
+        Q.qgemm_dense(d, good, good, Q.QW_A_MXFP8_G32, good, good, None, good, -1, stream=0)
+    assert e.value.status == Q.QW_ERR_INVALID_ARG
+    bad = Q.qw_repack_query(Q.QW_W_MXFP4_G32, 1, 256, 256)
+    bad.N_pad = 128  # tampered descriptor
+    with pytest.raises(Q.QwError) as e:
+        Q.qgemm_dense(bad, good, good, Q.QW_A_MXFP8_G32, good, good, None, good, 4, stream=0)
+    assert e.value.status == Q.QW_ERR_INVALID_ARG
+    d2 = Q.qw_repack_query(Q.QW_W_MXFP4_G32, 8, 256, 256)
+    with pytest.raises(Q.QwError) as e:  # dense call with several experts
+        Q.qgemm_dense(d2, good, good, Q.QW_A_MXFP8_G32, good, good, None, good, 4, stream=0)
+    assert e.value.status == Q.QW_ERR_INVALID_ARG
+    with pytest.raises(Q.QwError) as e:  # grouped call without workspace
+        Q.qgemm_moe_grouped(d2, good, good, Q.QW_A_MXFP8_G32, good, good, good, 100, None, good,
+                            None, 0, stream=0)
+    assert e.value.status == Q.QW_ERR_WORKSPACE
+    # M == 0 is a valid no-op that launches nothing
+    Q.qgemm_dense(d, good, good, Q.QW_A_MXFP8_G32, good, good, None, good, 0, stream=0)
+
+
+def test_route_host_validation(Q):
+    good = 1 << 20
+    for T, E, k in [(-1, 8, 2), (4, 8, 0), (4, 8, 33), (4, 4, 8), (4, 2048, 8)]:
+        with pytest.raises(Q.QwError) as e:
+            Q.qgemm_moe_route(good, T, E, k, good, good, good, good, 1 << 30, stream=0)
+        assert e.value.status == Q.QW_ERR_INVALID_ARG
+    with pytest.raises(Q.QwError) as e:
+        Q.qgemm_moe_route(good, 4, 8, 2, good, good, good, good, 0, stream=0)
+    assert e.value.status == Q.QW_ERR_WORKSPACE
+    assert Q.qgemm_moe_route_workspace_size(4096, 256, 8) == 128 * 256 * 4
+
+
+def test_permute_host_validation(Q):
+    good = 1 << 20
+    with pytest.raises(Q.QwError) as e:  # BF16 row of 12 bytes is not 16-byte aligned
+        Q.qgemm_moe_permute(Q.QW_A_BF16, good, None, 6, good, 4, 2, good, None, stream=0)
+    assert e.value.status == Q.QW_ERR_ALIGNMENT
+    Q.qgemm_moe_permute(Q.QW_A_BF16, good, None, 64, good, 0, 2, good, None, stream=0)  # P == 0
+
+
+def test_timeout_probe_validation(Q):
+    with pytest.raises(Q.QwError):
+        Q.qw_test_wait_timeout(None, 1000, stream=0)
+    with pytest.raises(Q.QwError):
+        Q.qw_test_wait_timeout(1 << 20, 3_000_000_000, stream=0)

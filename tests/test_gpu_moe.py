@@ -1,0 +1,121 @@
+"""MoE routing (bit-exact) and grouped GEMM parity on the GPU against the oracle."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import moe as OM
+from oracle import qgemm as OQ
+from oracle import formats as OF
+from qwtest import dev, host, qw, repack, route, u16_view
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,E,k", [(4096, 256, 8), (1, 128, 8), (16, 128, 8), (256, 128, 8),
+                                   (2048, 128, 8), (8192, 128, 8), (3, 6, 3), (100, 1000, 32),
+                                   (0, 64, 4), (7, 33, 1)])
+def test_route_bit_exact(T, E, k):
+    logits = synth.router_logits(T, E, cfg_id=3)
+    ids, sp, off = route(logits, k)
+    rids, rcounts, roff, rsp = OM.route(logits, k)
+    assert np.array_equal(ids, rids)
+    assert np.array_equal(off, roff)
+    assert np.array_equal(sp, rsp)
+
+
+def test_route_ties_bit_exact():
+    rng = np.random.default_rng(9)
+    logits = rng.integers(-2, 3, (300, 40)).astype(np.float32)  # heavy ties
+    ids, sp, off = route(logits, 6)
+    rids, _, roff, rsp = OM.route(logits, 6)
+    assert np.array_equal(ids, rids) and np.array_equal(off, roff) and np.array_equal(sp, rsp)
+
+
+@functools.lru_cache(maxsize=4)
+def _weights(kind, E, N, K, bits, cfg_id):
+    if kind == "mx":
+        return synth.w4a8_problem(1, N, K, E=E, cfg_id=cfg_id)
+    return synth.w4a16_problem(1, N, K, bits=bits, E=E, cfg_id=cfg_id)
+
+
+def run_moe(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4):
+    """Route -> permute -> grouped GEMM through the C ABI.  Returns host arrays."""
+    Q = qw()
+    logits = synth.router_logits(T, E, cfg_id=cfg_id)
+    kind = "mx" if wfmt == Q.QW_W_MXFP4_G32 else "int"
+    w = _weights(kind, E, N, K, bits, cfg_id)
+    if kind == "mx":
+        a = synth.w4a8_problem(T, 32, K, cfg_id=cfg_id + 1000)
+        p = dict(w, A=a["A"], A_sf=a["A_sf"])
+    else:
+        a = synth.w4a16_problem(T, 16, K, cfg_id=cfg_id + 1000)
+        p = dict(w, A=a["A"])
+    d, wp, sp_ = repack(wfmt, E, N, K, p["w_canon"], p["s_canon"])
+    P = T * topk
+    lg = dev(logits)
+    ids = torch.empty((T, topk), dtype=torch.int32, device="cuda")
+    sp = torch.empty((P,), dtype=torch.int32, device="cuda")
+    off = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+    n = Q.qgemm_moe_route_workspace_size(T, E, topk)
+    rws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    Q.qgemm_moe_route(lg, T, E, topk, ids, sp, off, rws, n)
+    if afmt == Q.QW_A_BF16:
+        A = dev(p["A"].view(np.int16))
+        As = torch.empty((P, K), dtype=torch.int16, device="cuda")
+        Q.qgemm_moe_permute(afmt, A, None, K, sp, P, topk, As, None)
+        Asf_s = None
+    else:
+        A = dev(p["A"])
+        Asf = dev(p["A_sf"])
+        As = torch.empty((P, K), dtype=torch.uint8, device="cuda")
+        Asf_s = torch.empty((P, K // 32), dtype=torch.uint8, device="cuda")
+        Q.qgemm_moe_permute(afmt, A, Asf, K, sp, P, topk, As, Asf_s)
+    C = torch.full((P, N), -1, dtype=torch.int16, device="cuda")
+    wsn = Q.qgemm_workspace_size(d, afmt, P)
+    ws = torch.empty(max(wsn, 16), dtype=torch.uint8, device="cuda")
+    err = Q.new_error_flag()
+    Q.qgemm_moe_grouped(d, wp, sp_, afmt, As, Asf_s, off, P, None, C, ws, wsn, err)
+    assert Q.qw_read_error(err) == 0
+    return p, logits, host(sp), host(off), u16_view(C)
+
+
+@pytest.mark.parametrize("E,T,K,N", [(8, 40, 256, 384), (16, 64, 512, 512), (32, 300, 128, 640)])
+def test_moe_grouped_w4a8_small(E, T, K, N):
+    Q = qw()
+    p, logits, sp, off, C = run_moe(Q.QW_A_MXFP8_G32, Q.QW_W_MXFP4_G32, E, T, K, N, 8, 300 + E)
+    _, _, roff, rsp = OM.route(logits, 8)
+    assert np.array_equal(off, roff) and np.array_equal(sp, rsp)
+    tok = rsp // 8
+    codes = OF.unpack_e2m1_bytes(p["w_canon"], K)
+    R, S = OM.grouped_w4a8(p["A"][tok], p["A_sf"][tok], roff, codes, p["s_canon"])
+    ok, ratio, frob = OQ.check_bf16_result(C, R, S)
+    assert ok, (ratio, frob)
+
+
+@pytest.mark.parametrize("T", [1, 16, 64])
+@pytest.mark.parametrize("bits", [4, 3])
+def test_moe_grouped_w4a16_small_t(T, bits):
+    """E=128 top-8, intermediate 640: up-projection K=4096 -> N=1280 (gate+up)."""
+    Q = qw()
+    p, logits, sp, off, C = run_moe(Q.QW_A_BF16, 0 if bits == 4 else 1, 128, T, 4096, 1280, 8,
+                                    4, bits=bits)
+    _, _, roff, rsp = OM.route(logits, 8)
+    tok = rsp // 8
+    q = OF.unpack_int4(p["w_canon"], 4096) if bits == 4 else OF.unpack_int3(p["w_canon"], 4096)
+    R, S = OM.grouped_w4a16(p["A"][tok], roff, q, p["s_canon"])
+    ok, ratio, frob = OQ.check_bf16_result(C, R, S)
+    assert ok, (ratio, frob)
+
+
+def test_moe_grouped_w4a16_down_k640():
+    """Down-projection K=640 -> N=4096 (K not a multiple of 256) on a per-pair input."""
+    Q = qw()
+    p, logits, sp, off, C = run_moe(Q.QW_A_BF16, 0, 128, 16, 640, 4096, 8, 4)
+    _, _, roff, rsp = OM.route(logits, 8)
+    R, S = OM.grouped_w4a16(p["A"][rsp // 8], roff, OF.unpack_int4(p["w_canon"], 640),
+                            p["s_canon"])
+    ok, ratio, frob = OQ.check_bf16_result(C, R, S)
+    assert ok, (ratio, frob)
