@@ -64,7 +64,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -88,7 +88,7 @@ class ClockSampler:
         sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         loaded = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
@@ -285,24 +285,28 @@ def run_ours(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- oracle arm
-def cpu_baseline(rows_b=1024):
+def cpu_baseline(rows_b=4096, min_seconds=10.0):
     """Time the float64 oracle on a bounded sample: all of (4096,3072,4096) plus the first
-    `rows_b` rows of (4096,14336,4096)."""
+    `rows_b` rows of (4096,14336,4096), repeated until at least `min_seconds` of CPU work."""
     from oracle import qgemm as OQ
     sample = [(4096, 3072, 4096, None), (4096, 14336, 4096, np.arange(rows_b))]
+    probs = [synth.w4a8_problem(M, N, K, cfg_id=1) for M, N, K, _ in sample]
     flops = 0.0
     t = 0.0
-    for M, N, K, rows in sample:
-        p = synth.w4a8_problem(M, N, K, cfg_id=1)
-        t0 = time.perf_counter()
-        OQ.w4a8_from_canonical(p["A"], p["A_sf"], p["w_canon"][0], p["s_canon"][0], K, rows=rows)
-        t += time.perf_counter() - t0
-        flops += 2.0 * (M if rows is None else len(rows)) * N * K
+    reps = 0
+    while t < min_seconds and reps < 8:
+        for (M, N, K, rows), p in zip(sample, probs):
+            t0 = time.perf_counter()
+            OQ.w4a8_from_canonical(p["A"], p["A_sf"], p["w_canon"][0], p["s_canon"][0], K,
+                                   rows=rows)
+            t += time.perf_counter() - t0
+            flops += 2.0 * (M if rows is None else len(rows)) * N * K
+        reps += 1
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": round(flops / t / 1e12, 5), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"(4096,3072,4096) all rows + (4096,14336,4096) first {rows_b} rows; "
-                      f"{flops / 1e9:.0f} GFLOP in {t:.1f} s (decode + float64 matmul)"}
+            "sample": f"(4096,3072,4096) all rows + (4096,14336,4096) first {rows_b} rows, "
+                      f"x{reps}: {flops / 1e9:.0f} GFLOP in {t:.1f} s (decode + float64 matmul)"}
 
 
 def run_reference(args, world, rank):
@@ -314,7 +318,7 @@ def run_reference(args, world, rank):
     cb = None
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        cb = cpu_baseline(rows_b=256)
+        cb = cpu_baseline(rows_b=1024, min_seconds=0.0)
         vals.append(cb["value"])
     wall = time.perf_counter() - t0
     v = statistics.median(vals)
@@ -331,7 +335,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true")
