@@ -176,6 +176,25 @@ qw_status qgemm_moe_route(const float* logits, int32_t T, int32_t E, int32_t top
                           void* workspace, uint64_t ws_bytes, int32_t* d_err, void* stream);
 
 /* --------------------------------------------------------------------------------------
+ * qgemm_moe_route_noalloc - qgemm_moe_route without a caller-provided workspace, for
+ * callers that cannot allocate device memory (for example a plugin whose host framework
+ * owns all device memory through its own pool, or a decode loop in which an allocation,
+ * which may synchronise the device, is not allowed).  The pages have no counterpart:
+ * this is an interface convenience of this library, not part of the method.
+ *   Arguments and results are those of qgemm_moe_route.  The routing scratch lives in a
+ *   static device array of QW_NOALLOC_ROUTE_SCRATCH_BYTES (1 MiB) that every GPU loading
+ *   the library holds until the process exits; requests needing more scratch than that
+ *   (ceil(T * topk / 256) * E * 4 bytes) are rejected with QW_ERR_WORKSPACE.  Nothing is
+ *   allocated.  All calls share the array: calls that overlap on the GPU race and give
+ *   undefined results.  The first call on each device looks up the array's device address
+ *   (with that device current); make it before any stream capture.
+ */
+#define QW_NOALLOC_ROUTE_SCRATCH_BYTES (1u << 20)
+qw_status qgemm_moe_route_noalloc(const float* logits, int32_t T, int32_t E, int32_t topk,
+                                  int32_t* topk_ids, int32_t* sorted_pairs,
+                                  int32_t* expert_offsets, int32_t* d_err, void* stream);
+
+/* --------------------------------------------------------------------------------------
  * qgemm_moe_permute - gather activation rows into the expert-contiguous order:
  *   A_sorted[r] = A[sorted_pairs[r] / topk] for r < P (and the same for A_sf rows when
  *   afmt is QW_A_MXFP8_G32; A_sf / A_sf_sorted are NULL for BF16).

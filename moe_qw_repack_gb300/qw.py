@@ -34,6 +34,7 @@ EXPORTS = (
     "qw_status_str", "qw_version", "qw_repack_query", "qw_repack", "qw_unpack",
     "qgemm_workspace_size", "qgemm_dense", "qgemm_moe_route_workspace_size", "qgemm_moe_route",
     "qgemm_moe_permute", "qgemm_moe_grouped", "qw_read_error", "qw_test_wait_timeout",
+    "qgemm_moe_route_noalloc",
 )
 
 
@@ -73,6 +74,7 @@ _SIGS = {
     "qgemm_moe_grouped": (_I32, [_DESC, _P, _P, _I32, _P, _P, _P, _I64, _P, _P, _P, _U64, _P, _P]),
     "qw_read_error": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
     "qw_test_wait_timeout": (_I32, [_P, _I64, _P]),
+    "qgemm_moe_route_noalloc": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
 }
 
 
@@ -172,6 +174,16 @@ def qgemm_moe_route(logits, T, E, topk, topk_ids, sorted_pairs, expert_offsets, 
     _check("qgemm_moe_route", LIB.qgemm_moe_route(
         _ptr(logits), T, E, topk, _ptr(topk_ids), _ptr(sorted_pairs), _ptr(expert_offsets),
         _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)))
+
+
+def qgemm_moe_route_noalloc(logits, T, E, topk, topk_ids, sorted_pairs, expert_offsets,
+                            d_err=None, stream=None):
+    """Routing without a workspace argument, for callers that cannot allocate device
+    memory: the library's static device scratch is used (see include/qw.h for its size
+    limit and the rule that overlapping calls race)."""
+    _check("qgemm_moe_route_noalloc", LIB.qgemm_moe_route_noalloc(
+        _ptr(logits), T, E, topk, _ptr(topk_ids), _ptr(sorted_pairs), _ptr(expert_offsets),
+        _ptr(d_err), _stream(stream)))
 
 
 def qgemm_moe_permute(afmt, A, A_sf, K, sorted_pairs, P, topk, A_sorted, A_sf_sorted,
