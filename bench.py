@@ -202,7 +202,9 @@ def extra_w4a16(steps, warmup, flush, world):
         Q.qw_repack(d, torch.from_numpy(p["w_canon"]).cuda(), torch.from_numpy(p["s_canon"]).cuda(), wp, sp)
         A = torch.from_numpy(p["A"].view(np.int16)).cuda()
         C = torch.empty((M, N), dtype=torch.int16, device="cuda")
-        fn = lambda: Q.qgemm_dense(d, wp, sp, Q.QW_A_BF16, A, None, None, C, M)  # noqa: E731
+        wsn = Q.qgemm_workspace_size(d, Q.QW_A_BF16, M)
+        ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
+        fn = lambda: Q.qgemm_dense(d, wp, sp, Q.QW_A_BF16, A, None, None, C, M, ws, wsn)  # noqa: E731
         per_step, _ = time_steps([fn], steps, warmup, flush, world)
         ms = statistics.median(per_step)
         wbytes = N * K * bits / 8 + N * (K // 128) * 2  # packed weights + BF16 scales
@@ -210,6 +212,71 @@ def extra_w4a16(steps, warmup, flush, world):
         out[name] = {"us": round(ms * 1e3, 2), "weight_GBps": round(gbs, 1),
                      "hbm_frac": round(gbs / peaks["hbm_gbs"], 3),
                      "tflops": round(2 * M * N * K / (ms * 1e-3) / 1e12, 3)}
+    return out
+
+
+def extra_moe(steps, warmup, flush, world):
+    """Grouped MoE workloads: W4A8 (E=256, top-8, T=4096, 7168 -> 4096) and the W4A16
+    intermediate-640 token sweep (E=128, top-8, up 4096 -> 1280 plus down 640 -> 4096).
+    One step = route + permute + grouped GEMM(s); inputs drawn on the device."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import moe_qw_repack_gb300.qw as Q
+    import synth.device as sd
+    from qwtest import moe_pipeline
+    peaks, _ = measured_peaks()
+    out = {}
+    # -- W4A8, E=256
+    E, T, K, N, k = 256, 4096, 7168, 4096, 8
+    r = moe_pipeline(Q.QW_A_MXFP8_G32, Q.QW_W_MXFP4_G32, E, T, K, N, k, cfg_id=3)
+    per_step, per_fn = time_steps([r["route"], r["permute"], r["gemm"]], steps, warmup, flush, world)
+    assert Q.qw_read_error(r["err"]) == 0
+    cnt = np.diff(r["offsets"].cpu().numpy())
+    active = int((cnt > 0).sum())
+    P = T * k
+    flop = 2.0 * P * N * K
+    gemm_ms = statistics.median(per_fn[2])
+    tot_ms = statistics.median(per_step)
+    wbytes = active * (N * K // 2 + N * K // 32)
+    out["cfg4_moe_w4a8_E256_T4096"] = {
+        "us_total": round(tot_ms * 1e3, 1), "us_route": round(statistics.median(per_fn[0]) * 1e3, 1),
+        "us_permute": round(statistics.median(per_fn[1]) * 1e3, 1), "us_gemm": round(gemm_ms * 1e3, 1),
+        "gemm_tflops": round(flop / (gemm_ms * 1e-3) / 1e12, 1),
+        "gemm_frac_fp8_peak": round(flop / (gemm_ms * 1e-3) / 1e12 / (2 * peaks["bf16_tflops"]), 3),
+        "active_experts": active, "active_weight_GB": round(wbytes / 1e9, 3),
+        "weight_stream_frac_hbm": round(wbytes / (gemm_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}
+    del r
+    torch.cuda.empty_cache()
+    # -- W4A16, E=128, intermediate 640
+    E, k = 128, 8
+    up_w = sd.int_weights(E, 1280, 4096, bits=4, cfg_id=4)
+    dn_w = sd.int_weights(E, 4096, 640, bits=4, cfg_id=4)
+    for T in (1, 16, 256, 2048, 8192):
+        P = T * k
+        up = moe_pipeline(Q.QW_A_BF16, Q.QW_W_INT4_G128_BF16, E, T, 4096, 1280, k, cfg_id=4,
+                          weights=up_w)
+        x = sd.bf16_activations(P, 640, cfg_id=40 + T)
+        dn = moe_pipeline(Q.QW_A_BF16, Q.QW_W_INT4_G128_BF16, E, T, 640, 4096, k, cfg_id=4,
+                          weights=dn_w, x_sorted=x, route_from=up)
+        n_steps = steps if T <= 256 else max(5, steps // 4)
+        per_step, per_fn = time_steps([up["route"], up["permute"], up["gemm"], dn["gemm"]],
+                                      n_steps, warmup, flush, world)
+        assert Q.qw_read_error(up["err"]) == 0 and Q.qw_read_error(dn["err"]) == 0
+        cnt = np.diff(up["offsets"].cpu().numpy())
+        active = int((cnt > 0).sum())
+        up_ms, dn_ms = statistics.median(per_fn[2]), statistics.median(per_fn[3])
+        wbytes_up = active * (1280 * 4096 // 2 + 1280 * 32 * 2)
+        wbytes_dn = active * (4096 * 640 // 2 + 4096 * 5 * 2)
+        flop = 2.0 * P * (1280 * 4096 + 4096 * 640)
+        out[f"cfg5_moe_w4a16_E128_T{T}"] = {
+            "us_total": round(statistics.median(per_step) * 1e3, 1),
+            "us_up": round(up_ms * 1e3, 1), "us_down": round(dn_ms * 1e3, 1),
+            "gemm_tflops": round(flop / ((up_ms + dn_ms) * 1e-3) / 1e12, 2),
+            "active_experts": active,
+            "weight_GBps": round((wbytes_up + wbytes_dn) / ((up_ms + dn_ms) * 1e-3) / 1e9, 1),
+            "weight_frac_hbm": round((wbytes_up + wbytes_dn) / ((up_ms + dn_ms) * 1e-3) / 1e9
+                                     / peaks["hbm_gbs"], 3)}
+        del up, dn, x
+        torch.cuda.empty_cache()
     return out
 
 
@@ -278,7 +345,8 @@ def run_ours(args, world, rank):
         "wall_s_timed_loop": round(wall, 3),
     }
     if not args.no_extra:
-        line["extra"] = extra_w4a16(max(5, args.steps), 3, flush, world)
+        line["extra"] = extra_w4a16(max(5, min(args.steps, 200)), 3, flush, world)
+        line["extra"].update(extra_moe(max(5, min(args.steps, 40)), 3, flush, world))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     return line
@@ -340,12 +408,17 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-w4a16", action="store_true",
+                    help="time only the W4A16 GEMV workloads (a profiling aid)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         world = int(os.environ.get("WORLD_SIZE", "1"))
         line = run_reference(args, world, rank)
+    elif args.only_w4a16:
+        world, rank, _ = dist_setup()
+        line = {"extra": extra_w4a16(args.steps, args.warmup, l2_flusher(), world)}
     else:
         world, rank, _ = dist_setup()
         line = run_ours(args, world, rank)

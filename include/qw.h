@@ -109,13 +109,14 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *   MXFP4: w_canon uint8 [E][N][K/2], even k in the low nibble.  s_canon uint8 E8M0
  *          [E][N][K/32].
  * Packed outputs (device, sizes from `desc`, 256-byte aligned):
- *   INT4:  per expert [K/128][N_pad/16] blocks of 1 KiB: 32 lanes x 8 words; word w of
- *          lane l holds the eight weights that lane l of an m16n8k16 MMA needs for the
- *          w-th 16-wide k step of the group, as excess-8 nibbles (q + 8).
- *          Scales BF16 [K/128][N_pad].
+ *   INT4:  per expert [K/128][N_pad/16] blocks of 1 KiB: 32 lanes x 8 words; word s of
+ *          lane l = 4g + t holds the eight weights lane l feeds to the s-th m16n8k16 MMA of
+ *          the group, as excess-8 nibbles (q + 8): nibble i -> row g + 8 (i & 1),
+ *          k = 32t + 4s + 2 ((i >> 1) & 1) + (i >> 2).  Lane t of a row quad thus owns k in
+ *          [32t, 32t + 32) of the group.  Scales BF16 [K/128][N_pad].
  *   INT3:  per expert [K/128][N_pad/16] blocks of 768 B: 32 lanes x 4 words holding the
- *          low two bits of q + 4 for the lane's 64 weights, then 32 lanes x 2 words
- *          holding their third bit.  Scales BF16 [K/128][N_pad].
+ *          low two bits of q + 4 for the lane's 64 weights (the INT4 (row, k) assignment),
+ *          then 32 lanes x 2 words holding their third bit.  Scales BF16 [K/128][N_pad].
  *   MXFP4: codes uint8 [N_pad][K_pad/2] (canonical order, zero-padded); scales E8M0 in
  *          512-byte chunks per 128 rows x 4 groups, chunk (r/128, g/4) at
  *          ((r/128) * (K_pad/128) + g/4) * 512, byte (r%32)*16 + ((r%128)/32)*4 + g%4;
@@ -139,6 +140,10 @@ qw_status qw_unpack(const qw_packed_desc* desc, const void* w_packed, const void
 /* --------------------------------------------------------------------------------------
  * qgemm_workspace_size - bytes of device workspace qgemm_dense / qgemm_moe_grouped need
  * for up to `max_rows` activation rows (host output `bytes`; 0 is a valid answer).
+ * The workspace holds split-K partial sums, split-K tickets and the grouped tile queue.
+ * Zero-fill it once after allocating it: the tickets must start at zero, and every call
+ * that completes leaves them at zero again.  After a call that reported QW_ERR_TIMEOUT,
+ * zero it again.  Calls that share one workspace must not overlap on the GPU.
  */
 qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t max_rows,
                                uint64_t* bytes);
@@ -151,7 +156,9 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
  *   bias:  BF16 [N] or NULL.  C: BF16 [M][N].  desc->E must be 1.
  * Dispatch by M (the device heuristic of the announcement, section "デバイスパラメータに
  * 基づくパフォーマンスチューニング"): W4A16 with M <= 64 streams the weights through a
- * split-K tensor-core GEMV; W4A8 runs the TMA + tcgen05 block-scaled GEMM.
+ * split-K tensor-core GEMV, larger M dequantizes into tensor memory and runs tcgen05 BF16
+ * MMAs (grouped calls switch at 64 rows per expert on average); W4A8 runs the TMA +
+ * tcgen05 block-scaled GEMM.
  * Alignment: A, C 16-byte aligned with K % 8 == 0 (BF16) or K % 16 == 0 (E4M3);
  * A_sf 4-byte aligned.  M >= 0 (M == 0 is a no-op).
  */

@@ -1,0 +1,475 @@
+// gemm_w4a16_tc.cu - large-M W4A16 path: INT4/INT3 weights dequantized inside the SM and
+// multiplied on the sm_103a tensor cores (tcgen05, BF16 operands, FP32 accumulation).
+//
+// What it computes (spke.com Humming announcement, "WnA16"; "フォーマットとアーキテクチャ
+// を横断して共有されるCUDAコンポーネント": dequantization and scaling inside the kernel,
+// bias in the output stage):
+//     C[m][n] = bf16( sum_g s[n][g] * sum_{k in g} a[m][k] * q[n][k] + bias[n] )
+// The integer weights go to the tensor core exactly (|q| <= 7 is exact in BF16); each
+// scale group's sum is accumulated on its own and multiplied by the group scale in FP32,
+// so no weight is ever rounded (rounding q * s to BF16 alone would cost ~2^-9 relative
+// per weight).
+//
+// Structure (persistent, one CTA per SM; a tile is 128 weight rows x 128 tokens; one
+// pipeline stage is one scale group of 128 k):
+//   warp 0      producer: TMA loads of the activation tile (two 128 x 64 BF16 boxes,
+//               128-byte swizzle) and a bulk copy of the 8 packed 16 x 128 weight blocks
+//               into a 4-stage ring;
+//   warp 1      TMEM owner and MMA issuer: per group, eight 128x128x16 MMAs with the
+//               weights as the A operand read from tensor memory and the tokens as the B
+//               operand, into one of two per-group accumulators;
+//   warps 2-5   dequantizers: thread = weight row = TMEM lane; each turns its row's excess
+//               codes into BF16 integers (code | 0x4300 = 128 + code, minus the excess) and
+//               writes the 16-wide k slices straight into the stage's TMEM columns
+//               (tcgen05.st) - the dequantized operand never touches shared memory;
+//   warps 6-13  promotion and epilogue: read each group's accumulator (tcgen05.ld), add
+//               scale x it to FP32 registers, release it; at the end of the tile add bias,
+//               round to BF16 and store C[token][row] (lanes = consecutive rows).
+// Every wait is bounded; on expiry the kernel reports QW_ERR_TIMEOUT and shuts down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "qw_common.cuh"
+#include "qw_internal.h"
+
+namespace qw {
+namespace {
+
+constexpr int BW = 128;  // weight rows per tile (MMA M)
+constexpr int BT = 128;  // tokens per tile (MMA N)
+constexpr int STAGES = 4;
+constexpr int ACT_BOX = BT * 64 * 2;  // 128 tokens x 64 k of BF16
+constexpr int ACT_BYTES = 2 * ACT_BOX;
+constexpr int NUM_DQ_WARPS = 4, NUM_EPI_WARPS = 8;
+constexpr int DQ_WARP0 = 2, EPI_WARP0 = DQ_WARP0 + NUM_DQ_WARPS;
+constexpr int NUM_THREADS = (EPI_WARP0 + NUM_EPI_WARPS) * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_COL0 = 2 * BT;  // the two per-group accumulators use columns [0, 256)
+
+// kind::f16 instruction descriptor: FP32 accumulator (bit 4), A = B = BF16 (bits 7, 10),
+// both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BT >> 3) << 17) |
+                           ((uint32_t)(BW >> 4) << 24);
+
+template <int BITS>
+struct Geo {
+  static constexpr int BLK = BITS == 4 ? 1024 : 768;
+  static constexpr int WBYTES = 8 * BLK;
+  // stages start on 1 KiB boundaries: the 128-byte-swizzled activation boxes need it
+  static constexpr int STAGE = (ACT_BYTES + WBYTES + 1023) / 1024 * 1024;
+};
+
+struct Params {
+  int64_t rows;  // tokens (M, or total grouped rows)
+  int32_t N, N_pad, K;
+  int32_t num_m_tiles;  // dense only
+  int32_t num_n_tiles;
+  const uint8_t* wp;
+  const uint16_t* sp16;          // BF16 scales [E][K/128][N_pad]
+  int64_t w_estride;             // bytes
+  int64_t s_estride_elems;
+  const uint16_t* bias;
+  uint16_t* C;
+  const int32_t* queue;
+  int32_t* err;
+};
+
+struct Tile {
+  int e, nt;
+  int64_t rb, re;
+};
+
+__device__ __forceinline__ Tile tile_at(const Params& p, int64_t t) {
+  Tile x;
+  x.nt = (int)(t % p.num_n_tiles);
+  const int64_t mt = t / p.num_n_tiles;
+  if (p.queue) {
+    x.e = __ldg(p.queue + 1 + 3 * mt);
+    x.rb = __ldg(p.queue + 2 + 3 * mt);
+    x.re = __ldg(p.queue + 3 + 3 * mt);
+  } else {
+    x.e = 0;
+    x.rb = mt * BT;
+    x.re = min64(p.rows, x.rb + BT);
+  }
+  return x;
+}
+
+__device__ __forceinline__ void tc_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// D(tmem) (+)= A(tmem) x B(smem)^T, BF16 operands, FP32 accumulation.
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d, uint32_t a_tmem, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16x2_sub_u32(uint32_t x, uint32_t y) {
+  // x - y for a pair of BF16 values; here the difference is an exact small integer
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&x);
+  __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&y);
+  __nv_bfloat162 r = __hsub2(a, b);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const Params p) {
+  using GE = Geo<BITS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * GE::STAGE);
+  uint64_t* aready = full + STAGES;
+  uint64_t* empty = aready + STAGES;
+  uint64_t* acc_full = empty + STAGES;   // [2] per-group accumulators
+  uint64_t* acc_empty = acc_full + 2;    // [2]
+  uint64_t* final_bar = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&aready[s], NUM_DQ_WARPS);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], NUM_EPI_WARPS);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tmA);
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const int64_t num_m = p.queue ? (int64_t)__ldg(p.queue) : (int64_t)p.num_m_tiles;
+  const int64_t num_tiles = num_m * p.num_n_tiles;
+  const int G = p.K / 128;
+  const int nblocks = p.N_pad / 16;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        const Tile x = tile_at(p, t);
+        const int nbs = min(8, nblocks - x.nt * 8);
+        const uint8_t* wsrc = p.wp + x.e * p.w_estride + (int64_t)x.nt * 8 * GE::BLK;
+        for (int g = 0; g < G; ++g) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * GE::STAGE;
+          mbar_arrive_expect_tx(&full[stage], ACT_BYTES + nbs * GE::BLK);
+          tma_load_2d(st, &tmA, &full[stage], g * 128, (int32_t)x.rb);
+          tma_load_2d(st + ACT_BOX, &tmA, &full[stage], g * 128 + 64, (int32_t)x.rb);
+          bulk_load(st + ACT_BYTES, wsrc + (int64_t)g * nblocks * GE::BLK, nbs * GE::BLK,
+                    &full[stage]);
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s)) drain_wait(&full[s], (issued_phase >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      uint64_t gi = 0;  // groups issued so far: accumulator gi & 1
+      for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int g = 0; g < G; ++g, ++gi) {
+          const int ab = (int)(gi & 1);
+          const uint32_t use = (uint32_t)(gi >> 1) & 1u;
+          if (!mbar_wait(&acc_empty[ab], use ^ 1u, abort_flag, p.err) ||
+              !mbar_wait(&aready[stage], phase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t act = smem_u32(smem + stage * GE::STAGE);
+          const uint32_t d = tbase + ab * BT;
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const uint64_t bd = smem_desc(act + (s / 4) * ACT_BOX + (s % 4) * 32, 16, 1024, 2);
+            tc_mma_f16_tmem_a(d, tbase + A_COL0 + 64 * stage + 8 * s, bd, IDESC, s != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          tc_commit(&acc_full[ab]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      tc_commit(final_bar);
+      drain_wait(final_bar, 0);
+    }
+  } else if (warp < EPI_WARP0) {
+    // ------------------------------------------------------------ dequantizers
+    // Thread = weight row r of the tile = TMEM lane.  The packed block stores, for lane slot
+    // 4 g + t, the pairs of rows g and g + 8 at k = 32t + 4s + 2 x' + {0, 1}; so the 16-wide
+    // k slice s' of row r sits in slot 4 (r & 7) + s'/2, steps 4 (s' % 2) .. + 3, fragment
+    // registers r0 and r0 + 2 (r0 = (r >> 3) & 1): one 16-byte shared load per slice.
+    const int q = warp & 3;          // TMEM lane quadrant
+    const int r = 32 * q + lane;     // weight row of the tile = TMEM lane
+    const int b = r >> 4, g8 = r & 7, r0 = (r >> 3) & 1;
+    const uint32_t magic = 0x43004300u;
+    const uint32_t excess = BITS == 4 ? 0x43084308u : 0x43044304u;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      const Tile x = tile_at(p, t);
+      const int nbs = min(8, nblocks - x.nt * 8);
+      const bool live = b < nbs;
+      for (int g = 0; g < G; ++g) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t blk = smem_u32(smem + stage * GE::STAGE) + ACT_BYTES + b * GE::BLK;
+#pragma unroll
+        for (int sl = 0; sl < 8; ++sl) {
+          const int slot = 4 * g8 + (sl >> 1);   // lane slot holding this k slice
+          const int sh = sl & 1;                 // its steps 4 sh .. 4 sh + 3
+          uint32_t col[8];
+          if (live) {
+            if constexpr (BITS == 4) {
+              const uint4 v = lds128(blk + slot * 32 + sh * 16);
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const int xr = r0 + 2 * (c & 1);
+                const uint32_t code = (w[c >> 1] >> (4 * xr)) & 0x000F000Fu;
+                col[c] = bf16x2_sub_u32(code | magic, excess);
+              }
+            } else {
+              const uint2 lo = lds64(blk + slot * 16 + sh * 8);
+              const uint32_t hi = lds32(blk + 512 + slot * 8 + sh * 4);
+              const uint32_t L[2] = {lo.x, lo.y};
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const int j = c >> 1, xr = r0 + 2 * (c & 1);
+                const int ls = 2 * (4 * (j & 1) + xr);
+                const int hs = 4 * j + xr;
+                const uint32_t code =
+                    ((L[j >> 1] >> ls) & 0x00030003u) | (((hi >> hs) & 0x00010001u) << 2);
+                col[c] = bf16x2_sub_u32(code | magic, excess);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) col[c] = 0u;
+          }
+          tc_st_32x32b_x8(tbase + ((uint32_t)(32 * q) << 16) + A_COL0 + 64 * stage + 8 * sl, col);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&aready[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ promotion + epilogue
+    const int q = warp & 3;                    // TMEM lane quadrant = 32 weight rows
+    const int half = (warp - EPI_WARP0) >> 2;  // tokens [64 half, 64 half + 64) of the tile
+    uint64_t gi = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      const Tile x = tile_at(p, t);
+      const int n = x.nt * BW + 32 * q + lane;
+      const bool nvalid = n < p.N;
+      const uint16_t* srow = p.sp16 + x.e * p.s_estride_elems + (nvalid ? n : 0);
+      float acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+      uint32_t s_next = __ldg(srow);
+      for (int g = 0; g < G; ++g, ++gi) {
+        const float sc = __uint_as_float(s_next << 16);
+        if (g + 1 < G) s_next = __ldg(srow + (int64_t)(g + 1) * p.N_pad);
+        const int ab = (int)(gi & 1);
+        const uint32_t use = (uint32_t)(gi >> 1) & 1u;
+        if (!mbar_wait(&acc_full[ab], use, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ta = tbase + ((uint32_t)(32 * q) << 16) + ab * BT + 64 * half;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[32];
+          tc_ld_32x32b_x32(ta + 32 * hh, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[32 * hh + i] = fmaf(sc, __uint_as_float(v[i]), acc[32 * hh + i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      }
+      if (!ok) break;
+      if (nvalid) {
+        const float bias = p.bias ? __uint_as_float((uint32_t)__ldg(p.bias + (int64_t)x.e * p.N + n) << 16) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const int64_t tok = x.rb + 64 * half + i;
+          if (tok < x.re) {
+            __nv_bfloat16 h = __float2bfloat16_rn(acc[i] + bias);
+            p.C[tok * p.N + n] = *reinterpret_cast<uint16_t*>(&h);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+template <int BITS>
+qw_status launch_bits(const CUtensorMap& tmA, const Params& p, int64_t tiles_max,
+                      cudaStream_t st) {
+  using GE = Geo<BITS>;
+  const size_t smem = (size_t)STAGES * GE::STAGE + 256 + 1024;  // ring + barriers + alignment
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      gemm_w4a16_tc_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (attr != cudaSuccess) return QW_ERR_CUDA;
+  const int sms = device_sm_count();
+  const unsigned grid = (unsigned)(tiles_max < sms ? (tiles_max < 1 ? 1 : tiles_max) : sms);
+  gemm_w4a16_tc_kernel<BITS><<<grid, NUM_THREADS, smem, st>>>(tmA, p);
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
+
+}  // namespace
+
+uint64_t gemm_w4a16_tc_workspace(const qw_packed_desc& d, int64_t max_rows) {
+  return d.E > 1 ? tile_queue_bytes(d.E, max_rows, BT) : 0;
+}
+
+qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
+                               const void* s_packed, const void* A, const void* bias, void* C,
+                               const RowSet& rs, void* ws, uint64_t ws_bytes, int32_t* err,
+                               cudaStream_t st) {
+  if (rs.rows == 0) return QW_OK;
+  auto enc = encode_fn();
+  if (!enc) return QW_ERR_CUDA;
+  if (rs.rows > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
+  CUtensorMap tmA;
+  cuuint64_t gdim[2] = {(cuuint64_t)d.K, (cuuint64_t)rs.rows};
+  cuuint64_t gstr[1] = {(cuuint64_t)d.K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)BT};
+  cuuint32_t es[2] = {1, 1};
+  if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), gdim, gstr, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return QW_ERR_ALIGNMENT;
+  Params p{};
+  p.rows = rs.rows;
+  p.N = d.N;
+  p.N_pad = d.N_pad;
+  p.K = d.K;
+  p.num_n_tiles = (d.N_pad + BW - 1) / BW;
+  p.num_m_tiles = (int32_t)((rs.rows + BT - 1) / BT);
+  p.wp = static_cast<const uint8_t*>(w_packed);
+  p.sp16 = static_cast<const uint16_t*>(s_packed);
+  p.w_estride = (int64_t)d.w_expert_stride;
+  p.s_estride_elems = (int64_t)(d.s_expert_stride / 2);
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.C = static_cast<uint16_t*>(C);
+  p.err = err;
+  int64_t max_m = p.num_m_tiles;
+  if (rs.offsets) {
+    const uint64_t need = tile_queue_bytes(rs.E, rs.rows, BT);
+    if (ws == nullptr || ws_bytes < need) return QW_ERR_WORKSPACE;
+    int32_t* queue = static_cast<int32_t*>(ws);
+    max_m = (int64_t)(need / 4 - 1) / 3;
+    const qw_status s =
+        launch_build_tile_queue(rs.offsets, rs.E, BT, rs.rows, queue, max_m, err, st);
+    if (s != QW_OK) return s;
+    p.queue = queue;
+  }
+  const int64_t tiles_max = max_m * p.num_n_tiles;
+  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_bits<4>(tmA, p, tiles_max, st)
+                                       : launch_bits<3>(tmA, p, tiles_max, st);
+}
+
+}  // namespace qw

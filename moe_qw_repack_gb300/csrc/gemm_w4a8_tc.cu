@@ -273,24 +273,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t row = x.rb + 32 * q + lane;
       const int col0 = x.n0 + 128 * half;
       uint32_t packed[64];
+      // two 32-column loads in flight per wait: the drain gates the next tile's first MMA
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t r[32];
-        tc_ld_32x32b_x32(tbase + ((uint32_t)(32 * q) << 16) + 128 * half + 32 * j, r);
+      for (int jj = 0; jj < 2; ++jj) {
+        uint32_t r[2][32];
+        const uint32_t ta = tbase + ((uint32_t)(32 * q) << 16) + 128 * half + 64 * jj;
+        tc_ld_32x32b_x32(ta, r[0]);
+        tc_ld_32x32b_x32(ta + 32, r[1]);
         tc_wait_ld();
-        float b[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) b[i] = 0.f;
-        if (p.bias) {
-          const uint16_t* bp = p.bias + (int64_t)x.e * p.N + col0 + 32 * j;
+        for (int h = 0; h < 2; ++h) {
+          const int j = 2 * jj + h;
+          float b[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (col0 + 32 * j + i < p.N) b[i] = __uint_as_float((uint32_t)__ldg(bp + i) << 16);
+          for (int i = 0; i < 32; ++i) b[i] = 0.f;
+          if (p.bias) {
+            const uint16_t* bp = p.bias + (int64_t)x.e * p.N + col0 + 32 * j;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col0 + 32 * j + i < p.N) b[i] = __uint_as_float((uint32_t)__ldg(bp + i) << 16);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[16 * j + i] = pack_bf16x2(__uint_as_float(r[h][2 * i]) + b[2 * i],
+                                             __uint_as_float(r[h][2 * i + 1]) + b[2 * i + 1]);
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          packed[16 * j + i] = pack_bf16x2(__uint_as_float(r[2 * i]) + b[2 * i],
-                                           __uint_as_float(r[2 * i + 1]) + b[2 * i + 1]);
       }
       tc_fence_before();
       __syncwarp();
@@ -394,7 +401,8 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
     if (ws == nullptr || ws_bytes < need) return QW_ERR_WORKSPACE;
     int32_t* queue = static_cast<int32_t*>(ws);
     max_m_tiles = (int64_t)(need / 4 - 1) / 3;
-    qw_status s = launch_build_tile_queue(rs.offsets, rs.E, BM, queue, max_m_tiles, err, st);
+    qw_status s = launch_build_tile_queue(rs.offsets, rs.E, BM, rs.rows, queue, max_m_tiles, err,
+                                           st);
     if (s != QW_OK) return s;
     p.queue = queue;
   }

@@ -150,7 +150,8 @@ __global__ void __launch_bounds__(kChunk)
 // -------------------------------------------------------------------- tile queue (one CTA)
 __global__ void __launch_bounds__(1024)
     tile_queue_kernel(const int32_t* __restrict__ offsets, int32_t E, int32_t TR,
-                      int32_t* __restrict__ queue, int64_t max_entries, int32_t* err) {
+                      int64_t total_rows, int32_t* __restrict__ queue, int64_t max_entries,
+                      int32_t* err) {
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
   if (threadIdx.x == 0) carry = 0;
@@ -160,11 +161,15 @@ __global__ void __launch_bounds__(1024)
     const int e = e0 + threadIdx.x;
     int32_t b = 0, n = 0, cntile = 0;
     if (e < E) {
-      b = __ldg(offsets + e);
-      n = __ldg(offsets + e + 1) - b;
-      if (n < 0) {
+      // the offsets come from the caller's device memory: a segment outside
+      // [0, total_rows] or a decreasing pair is reported and contributes no tiles, so
+      // that no kernel ever touches a row outside the buffers
+      const int64_t lo = __ldg(offsets + e), hi = __ldg(offsets + e + 1);
+      if (lo < 0 || hi < lo || hi > total_rows) {
         set_error(err, QW_ERR_INVALID_ARG);
-        n = 0;
+      } else {
+        b = (int32_t)lo;
+        n = (int32_t)(hi - lo);
       }
       cntile = (n + TR - 1) / TR;
     }
@@ -305,9 +310,10 @@ uint64_t tile_queue_bytes(int32_t E, int64_t rows, int32_t tile_rows) {
 }
 
 qw_status launch_build_tile_queue(const int32_t* offsets, int32_t E, int32_t tile_rows,
-                                  int32_t* queue, int64_t max_entries, int32_t* err,
-                                  cudaStream_t st) {
-  tile_queue_kernel<<<1, 1024, 0, st>>>(offsets, E, tile_rows, queue, max_entries, err);
+                                  int64_t total_rows, int32_t* queue, int64_t max_entries,
+                                  int32_t* err, cudaStream_t st) {
+  tile_queue_kernel<<<1, 1024, 0, st>>>(offsets, E, tile_rows, total_rows, queue, max_entries,
+                                        err);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 

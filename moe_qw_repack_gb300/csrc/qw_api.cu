@@ -145,8 +145,13 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
   if (s != QW_OK) return s;
   if (!bytes || max_rows < 0) return QW_ERR_INVALID_ARG;
   if ((s = check_afmt(desc, afmt, reinterpret_cast<const void*>(1))) != QW_OK) return s;
-  *bytes = desc->wfmt == QW_W_MXFP4_G32 ? gemm_w4a8_workspace(*desc, max_rows)
-                                        : gemv_w4a16_workspace(*desc, max_rows);
+  if (desc->wfmt == QW_W_MXFP4_G32) {
+    *bytes = gemm_w4a8_workspace(*desc, max_rows);
+  } else {
+    const uint64_t a = gemv_w4a16_workspace(*desc, max_rows);
+    const uint64_t b = gemm_w4a16_tc_workspace(*desc, max_rows);
+    *bytes = a > b ? a : b;
+  }
   return QW_OK;
 }
 
@@ -183,6 +188,9 @@ qw_status qgemm_dense(const qw_packed_desc* desc, const void* w_packed, const vo
   if (desc->wfmt == QW_W_MXFP4_G32)
     return launch_gemm_w4a8(*desc, w_packed, s_packed, A, A_sf, bias, C, rs, workspace, ws_bytes,
                             d_err, st);
+  if (M > kW4A16TensorCoreRows)
+    return launch_gemm_w4a16_tc(*desc, w_packed, s_packed, A, bias, C, rs, workspace, ws_bytes,
+                                d_err, st);
   return launch_gemv_w4a16(*desc, w_packed, s_packed, A, bias, C, rs, workspace, ws_bytes, d_err,
                            st);
 }
@@ -246,6 +254,9 @@ qw_status qgemm_moe_grouped(const qw_packed_desc* desc, const void* w_packed,
   if (desc->wfmt == QW_W_MXFP4_G32)
     return launch_gemm_w4a8(*desc, w_packed, s_packed, A_sorted, A_sf_sorted, bias, C, rs,
                             workspace, ws_bytes, d_err, st);
+  if (total_rows >= kW4A16TensorCoreRows * desc->E)
+    return launch_gemm_w4a16_tc(*desc, w_packed, s_packed, A_sorted, bias, C, rs, workspace,
+                                ws_bytes, d_err, st);
   return launch_gemv_w4a16(*desc, w_packed, s_packed, A_sorted, bias, C, rs, workspace, ws_bytes,
                            d_err, st);
 }

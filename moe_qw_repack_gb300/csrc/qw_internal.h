@@ -37,6 +37,17 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
                             void* ws, uint64_t ws_bytes, int32_t* err, cudaStream_t st);
 uint64_t gemv_w4a16_workspace(const qw_packed_desc& d, int64_t max_rows);
 
+// Large-M W4A16: in-SM dequantization into tensor memory + tcgen05 BF16 GEMM.
+qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
+                               const void* s_packed, const void* A, const void* bias, void* C,
+                               const RowSet& rs, void* ws, uint64_t ws_bytes, int32_t* err,
+                               cudaStream_t st);
+uint64_t gemm_w4a16_tc_workspace(const qw_packed_desc& d, int64_t max_rows);
+
+// Rows per token tile from which W4A16 runs on the tensor-core path (dense M, or the
+// average rows per expert of a grouped call); below it the GEMV streams the weights.
+constexpr int64_t kW4A16TensorCoreRows = 64;
+
 // Large-M W4A8: TMA + tcgen05 block-scaled GEMM.
 qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
                            const void* A, const void* A_sf, const void* bias, void* C,
@@ -56,9 +67,11 @@ qw_status launch_moe_permute(int32_t afmt, const void* A, const void* A_sf, int3
 // Device tile queue for grouped GEMMs: entry = (expert, row_begin, row_end) for each
 // tile of `tile_rows` rows of every expert; count at queue[0].
 uint64_t tile_queue_bytes(int32_t E, int64_t rows, int32_t tile_rows);
+// Offsets outside [0, total_rows] or decreasing are reported (QW_ERR_INVALID_ARG) and
+// produce no tiles.
 qw_status launch_build_tile_queue(const int32_t* offsets, int32_t E, int32_t tile_rows,
-                                  int32_t* queue, int64_t max_entries, int32_t* err,
-                                  cudaStream_t st);
+                                  int64_t total_rows, int32_t* queue, int64_t max_entries,
+                                  int32_t* err, cudaStream_t st);
 
 qw_status launch_wait_timeout_probe(int32_t* err, int64_t limit_ns, cudaStream_t st);
 

@@ -19,13 +19,16 @@ __device__ __forceinline__ uint32_t int4_canon_nib(const uint32_t* wc, int32_t K
   return (wc[n * (K / 8) + k / 8] >> (4 * (k % 8))) & 0xFu;
 }
 
-// Mapping of one packed INT4 word (lane l, k16 step s of a 16 x 128 block) to the
-// weights it holds: nibble i feeds register r = i & 3 of the m16n8k16 A fragment,
-// half h = i >> 2; row = g + 8 * (r & 1), k = 2t + h + 8 * (r >> 1), g = l / 4, t = l % 4.
+// Mapping of one packed INT4 word (lane l, MMA step s of a 16 x 128 block) to the
+// weights it holds: nibble i feeds register r = i & 3 of the m16n8k16 A fragment, half
+// h = i >> 2; row = g + 8 * (r & 1), k = 32t + 4s + 2 * (r >> 1) + h, g = l / 4, t = l % 4.
+// The MMA does not care which real k sits in which of its k slots as long as the B
+// operand agrees, so lane t of every row quad owns k in [32t, 32t + 32) of the group:
+// its activations for a whole group are 64 contiguous bytes.
 __device__ __forceinline__ void int4_nib_pos(int l, int s, int i, int& row, int& k) {
   const int g = l >> 2, t = l & 3, r = i & 3, h = i >> 2;
   row = g + 8 * (r & 1);
-  k = 16 * s + 2 * t + h + 8 * (r >> 1);
+  k = 32 * t + 4 * s + 2 * (r >> 1) + h;
 }
 
 __global__ void repack_int4_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
@@ -76,10 +79,11 @@ __global__ void unpack_int4_kernel(const uint32_t* __restrict__ wp, uint32_t* __
     uint32_t out = 0;
     for (int j = 0; j < 8; ++j) {
       const int k = k0 + j;
-      const int G = k / 128, kk = k % 128, s = kk / 16, kl = kk % 16;
+      const int G = k / 128, kk = k % 128;
       const int nb = (int)(n / 16), row = (int)(n % 16);
-      // invert int4_nib_pos: row = g + 8(r&1), kl = 2t + h + 8(r>>1)
-      const int g = row & 7, r0 = row >> 3, r1 = kl >> 3, t = (kl & 7) >> 1, h = kl & 1;
+      // invert int4_nib_pos: row = g + 8(r&1), kk = 32t + 4s + 2(r>>1) + h
+      const int g = row & 7, r0 = row >> 3, t = kk >> 5, s = (kk & 31) >> 2;
+      const int r1 = (kk & 3) >> 1, h = kk & 1;
       const int lane = g * 4 + t, i = (r0 | (r1 << 1)) + 4 * h;
       const uint32_t word = wpe[((int64_t)G * (N_pad / 16) + nb) * 256 + lane * 8 + s];
       const uint32_t code = (word >> (4 * i)) & 0xFu;
@@ -100,7 +104,8 @@ __device__ __forceinline__ int32_t int3_canon(const uint32_t* wc, int32_t K, int
   return (v >= 4u) ? (int32_t)v - 8 : (int32_t)v;
 }
 
-// Packed INT3 of lane l, step s, register r, half h: the lo plane keeps u & 3 in word
+// Packed INT3 of lane l, step s, register r, half h (same (row, k) as the INT4 words:
+// row g + 8 (r & 1), k 32t + 4s + 2 (r >> 1) + h): the lo plane keeps u & 3 in word
 // s/2 at bits 2 * (4 * (s % 2) + r) + 16 h; the hi plane keeps u >> 2 in word s/4 at bit
 // 4 * (s % 4) + r + 16 h; u = q + 4.
 __global__ void repack_int3_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
@@ -122,7 +127,7 @@ __global__ void repack_int3_kernel(const uint32_t* __restrict__ wc, uint32_t* __
       for (int r = 0; r < 4; ++r)
         for (int h = 0; h < 2; ++h) {
           const int row = g + 8 * (r & 1);
-          const int k = G * 128 + 16 * s + 2 * t + h + 8 * (r >> 1);
+          const int k = G * 128 + 32 * t + 4 * s + 2 * (r >> 1) + h;
           const int64_t n = (int64_t)nb * 16 + row;
           int32_t q = 0;
           if (n < N) {
@@ -157,9 +162,10 @@ __global__ void unpack_int3_kernel(const uint32_t* __restrict__ wp, uint32_t* __
     uint32_t w3[3] = {0, 0, 0};
     for (int j = 0; j < 32; ++j) {
       const int k = k0 + j;
-      const int G = k / 128, kk = k % 128, s = kk / 16, kl = kk % 16;
+      const int G = k / 128, kk = k % 128;
       const int nb = (int)(n / 16), row = (int)(n % 16);
-      const int g = row & 7, r = (row >> 3) | ((kl >> 3) << 1), t = (kl & 7) >> 1, h = kl & 1;
+      const int t = kk >> 5, s = (kk & 31) >> 2, h = kk & 1;
+      const int g = row & 7, r = (row >> 3) | (((kk & 3) >> 1) << 1);
       const int lane = g * 4 + t;
       const uint32_t* blk = wpe + ((int64_t)G * (N_pad / 16) + nb) * 192;
       const uint32_t L = blk[lane * 4 + s / 2], H = blk[128 + lane * 2 + s / 4];

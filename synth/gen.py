@@ -116,8 +116,11 @@ def normal(st: Stream, shape, std: float = 1.0) -> np.ndarray:
 
 
 def random_bytes(st: Stream, n: int) -> np.ndarray:
-    words = st.u64((n + 7) // 8)
-    return words.view(np.uint8)[:n].copy()
+    out = np.empty(((n + 7) // 8) * 8, dtype=np.uint8)
+    nw = out.size // 8
+    for a, b in _chunks(nw):
+        out[8 * a:8 * b] = st.u64(b - a).view(np.uint8)
+    return out[:n]
 
 
 # ----------------------------------------------------------------------------- casts

@@ -50,7 +50,7 @@ def dense_w4a16(prob, bias=None, M=None):
     C = torch.full((M, prob["N"]), -1, dtype=torch.int16, device="cuda")
     b = None if bias is None else dev(bias.view(np.int16))
     ws_n = Q.qgemm_workspace_size(d, Q.QW_A_BF16, M)
-    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(ws_n, 16), dtype=torch.uint8, device="cuda")
     err = Q.new_error_flag()
     Q.qgemm_dense(d, wp, sp, Q.QW_A_BF16, A, None, b, C, M, ws, ws_n, err)
     assert Q.qw_read_error(err) == 0
@@ -67,7 +67,7 @@ def dense_w4a8(prob, bias=None):
     C = torch.full((M, prob["N"]), -1, dtype=torch.int16, device="cuda")
     b = None if bias is None else dev(bias.view(np.int16))
     ws_n = Q.qgemm_workspace_size(d, Q.QW_A_MXFP8_G32, M)
-    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(ws_n, 16), dtype=torch.uint8, device="cuda")
     err = Q.new_error_flag()
     Q.qgemm_dense(d, wp, sp, Q.QW_A_MXFP8_G32, A, Asf, b, C, M, ws, ws_n, err)
     code = Q.qw_read_error(err)
@@ -88,3 +88,89 @@ def route(logits_np, topk):
     Q.qgemm_moe_route(lg, T, E, topk, ids, sp, off, ws, n, err)
     assert Q.qw_read_error(err) == 0
     return host(ids)[:T], host(sp)[:T * topk], host(off)
+
+
+# ----------------------------------------------------------------------------- full-size MoE
+def moe_pipeline(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4, weights=None, x_sorted=None,
+                 route_from=None):
+    """Route -> permute -> grouped GEMM through the C ABI on device-generated inputs.
+    Returns a dict of device tensors (inputs and outputs) for sampled oracle checks.
+    ``route_from`` reuses another pipeline's routing (e.g. the down projection after the
+    up projection); its ``route`` step then does nothing."""
+    import synth
+    import synth.device as sd
+    Q = qw()
+    P = T * topk
+    logits = synth.router_logits(T, E, cfg_id=cfg_id)
+    lg = dev(logits)
+    if weights is None:
+        weights = (sd.mxfp4_weights(E, N, K, cfg_id=cfg_id) if wfmt == Q.QW_W_MXFP4_G32
+                   else sd.int_weights(E, N, K, bits=bits, cfg_id=cfg_id))
+    w_canon, s_canon = weights
+    d = Q.qw_repack_query(wfmt, E, N, K)
+    wp, spk = Q.empty_packed(d)
+    err = Q.new_error_flag()
+    Q.qw_repack(d, w_canon, s_canon, wp, spk, err)
+    assert Q.qw_read_error(err) == 0
+    ids = torch.empty((max(T, 1), topk), dtype=torch.int32, device="cuda")
+    sp = torch.empty((max(P, 1),), dtype=torch.int32, device="cuda")
+    off = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+    n = Q.qgemm_moe_route_workspace_size(T, E, topk)
+    rws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    out = dict(logits=logits, w_canon=w_canon, s_canon=s_canon, desc=d, wp=wp, sp_packed=spk,
+               sorted_pairs=sp, offsets=off, topk_ids=ids)
+
+    def route():
+        Q.qgemm_moe_route(lg, T, E, topk, ids, sp, off, rws, n)
+
+    if route_from is not None:
+        ids, sp, off = route_from["topk_ids"], route_from["sorted_pairs"], route_from["offsets"]
+        out.update(sorted_pairs=sp, offsets=off, topk_ids=ids, logits=route_from["logits"])
+
+        def route():  # noqa: F811  (routing shared with `route_from`)
+            pass
+
+    if afmt == Q.QW_A_MXFP8_G32:
+        A, Asf = sd.mxfp8_activations(T, K, cfg_id=cfg_id)
+        As = torch.empty((P, K), dtype=torch.uint8, device="cuda")
+        Asf_s = torch.empty((P, K // 32), dtype=torch.uint8, device="cuda")
+        out.update(A=A, A_sf=Asf)
+    else:
+        A = sd.bf16_activations(T, K, cfg_id=cfg_id) if x_sorted is None else None
+        As = torch.empty((P, K), dtype=torch.int16, device="cuda") if x_sorted is None else x_sorted
+        Asf, Asf_s = None, None
+        out.update(A=A)
+
+    def permute():
+        if x_sorted is None:
+            Q.qgemm_moe_permute(afmt, A, Asf, K, sp, P, topk, As, Asf_s)
+
+    C = torch.empty((P, N), dtype=torch.int16, device="cuda")
+    wsn = Q.qgemm_workspace_size(d, afmt, P)
+    ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
+
+    def gemm():
+        Q.qgemm_moe_grouped(d, wp, spk, afmt, As, Asf_s, off, P, None, C, ws, wsn, err)
+
+    out.update(A_sorted=As, A_sf_sorted=Asf_s, C=C, err=err, route=route, permute=permute,
+               gemm=gemm)
+    return out
+
+
+def sample_rows_per_expert(offsets, per_expert=2, max_experts=None, seed=0):
+    """Row indices of the grouped output: the first, last (and a middle) row of sampled
+    non-empty experts, always including the largest and smallest non-empty ones."""
+    off = np.asarray(offsets, dtype=np.int64)
+    counts = np.diff(off)
+    nz = np.nonzero(counts)[0]
+    if max_experts is not None and nz.size > max_experts:
+        rng = np.random.default_rng(seed)
+        keep = set(rng.choice(nz, max_experts - 2, replace=False).tolist())
+        keep |= {int(nz[np.argmax(counts[nz])]), int(nz[np.argmin(counts[nz])])}
+        nz = np.array(sorted(keep))
+    rows = []
+    for e in nz:
+        b, c = off[e], counts[e]
+        cand = [b, b + c - 1, b + c // 2][:max(1, per_expert)]
+        rows.extend(sorted(set(int(r) for r in cand)))
+    return np.array(rows, dtype=np.int64)

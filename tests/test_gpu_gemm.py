@@ -108,3 +108,32 @@ def test_config2b_w4a8_full_size_sampled_rows():
     R, S = OQ.w4a8_from_canonical(p["A"], p["A_sf"], p["w_canon"][0], p["s_canon"][0], 4096,
                                   rows=rows)
     assert_parity(C[rows], R, S, "config 2b")
+
+
+# ----------------------------------------------------------------------------- W4A16 large M
+@pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("M,N,K", [(65, 40, 128), (128, 128, 256), (257, 200, 640),
+                                   (300, 1280, 4096), (129, 4096, 640)])
+def test_w4a16_tensor_core_shapes(bits, M, N, K):
+    """M > 64 runs the tcgen05 path: dequantized BF16 weights written into tensor memory."""
+    p = synth.w4a16_problem(M, N, K, bits=bits, cfg_id=400 + M)
+    C = dense_w4a16(p)
+    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, bits)
+    assert_parity(C, R, S, f"W{bits}A16 TC {M}x{N}x{K}")
+
+
+def test_w4a16_tensor_core_bias():
+    p = synth.w4a16_problem(150, 96, 384, bits=4, cfg_id=430, bias=True)
+    C = dense_w4a16(p, bias=p["bias"][0])
+    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], 384, 4,
+                                   bias_bits=p["bias"][0])
+    assert_parity(C, R, S, "W4A16 TC bias")
+
+
+def test_w4a16_tensor_core_large_sampled_rows():
+    """(4096, 4096, 4096) INT4 on the tensor-core path; 256 sampled rows checked in full."""
+    p = synth.w4a16_problem(4096, 4096, 4096, bits=4, cfg_id=431)
+    C = dense_w4a16(p)
+    rows = np.concatenate([np.array([0, 77, 127]) + 128 * i for i in range(32)])
+    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], 4096, 4, rows=rows)
+    assert_parity(C[rows], R, S, "W4A16 TC 4096^3")

@@ -75,7 +75,7 @@ def run_moe(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4):
         Q.qgemm_moe_permute(afmt, A, Asf, K, sp, P, topk, As, Asf_s)
     C = torch.full((P, N), -1, dtype=torch.int16, device="cuda")
     wsn = Q.qgemm_workspace_size(d, afmt, P)
-    ws = torch.empty(max(wsn, 16), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
     err = Q.new_error_flag()
     Q.qgemm_moe_grouped(d, wp, sp_, afmt, As, Asf_s, off, P, None, C, ws, wsn, err)
     assert Q.qw_read_error(err) == 0
@@ -119,3 +119,24 @@ def test_moe_grouped_w4a16_down_k640():
                             p["s_canon"])
     ok, ratio, frob = OQ.check_bf16_result(C, R, S)
     assert ok, (ratio, frob)
+
+
+@pytest.mark.parametrize("bad", ["decreasing", "past_end", "negative"])
+def test_grouped_rejects_bad_device_offsets(bad):
+    """Offsets live in device memory, so the host cannot check them: the device tile-queue
+    builder reports them (QW_ERR_INVALID_ARG) and schedules no tile for the bad segment."""
+    Q = qw()
+    E, P, K, N = 4, 64, 128, 64
+    p = synth.w4a16_problem(P, N, K, bits=4, E=E, cfg_id=77)
+    d, wp, sp_ = repack(Q.QW_W_INT4_G128_BF16, E, N, K, p["w_canon"], p["s_canon"])
+    offs = {"decreasing": [0, 40, 20, 50, 64], "past_end": [0, 16, 32, 48, 100000],
+            "negative": [-1000, 16, 32, 48, 64]}[bad]
+    off = torch.tensor(offs, dtype=torch.int32, device="cuda")
+    A = dev(p["A"].view(np.int16))
+    C = torch.full((P, N), 0x7FC0, dtype=torch.int16, device="cuda")
+    wsn = Q.qgemm_workspace_size(d, Q.QW_A_BF16, P)
+    ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
+    err = Q.new_error_flag()
+    Q.qgemm_moe_grouped(d, wp, sp_, Q.QW_A_BF16, A, None, off, P, None, C, ws, wsn, err)
+    assert Q.qw_read_error(err) == Q.QW_ERR_INVALID_ARG
+    assert float((torch.ones(2, device="cuda") * 3).sum()) == 6.0  # context still usable
