@@ -92,11 +92,13 @@ def route(logits_np, topk):
 
 # ----------------------------------------------------------------------------- full-size MoE
 def moe_pipeline(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4, weights=None, x_sorted=None,
-                 route_from=None):
+                 route_from=None, replicas=1):
     """Route -> permute -> grouped GEMM through the C ABI on device-generated inputs.
     Returns a dict of device tensors (inputs and outputs) for sampled oracle checks.
     ``route_from`` reuses another pipeline's routing (e.g. the down projection after the
-    up projection); its ``route`` step then does nothing."""
+    up projection); its ``route`` step then does nothing.  ``replicas`` > 1 keeps that many
+    copies of the packed weights; ``gemm(i)`` reads copy i mod replicas (timing loops use
+    it so that consecutive steps do not find the weights in L2)."""
     import synth
     import synth.device as sd
     Q = qw()
@@ -120,14 +122,14 @@ def moe_pipeline(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4, weights=None, x_s
     out = dict(logits=logits, w_canon=w_canon, s_canon=s_canon, desc=d, wp=wp, sp_packed=spk,
                sorted_pairs=sp, offsets=off, topk_ids=ids)
 
-    def route():
+    def route(i=0):
         Q.qgemm_moe_route(lg, T, E, topk, ids, sp, off, rws, n)
 
     if route_from is not None:
         ids, sp, off = route_from["topk_ids"], route_from["sorted_pairs"], route_from["offsets"]
         out.update(sorted_pairs=sp, offsets=off, topk_ids=ids, logits=route_from["logits"])
 
-        def route():  # noqa: F811  (routing shared with `route_from`)
+        def route(i=0):  # noqa: F811  (routing shared with `route_from`)
             pass
 
     if afmt == Q.QW_A_MXFP8_G32:
@@ -141,7 +143,7 @@ def moe_pipeline(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4, weights=None, x_s
         Asf, Asf_s = None, None
         out.update(A=A)
 
-    def permute():
+    def permute(i=0):
         if x_sorted is None:
             Q.qgemm_moe_permute(afmt, A, Asf, K, sp, P, topk, As, Asf_s)
 
@@ -149,11 +151,19 @@ def moe_pipeline(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4, weights=None, x_s
     wsn = Q.qgemm_workspace_size(d, afmt, P)
     ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
 
-    def gemm():
-        Q.qgemm_moe_grouped(d, wp, spk, afmt, As, Asf_s, off, P, None, C, ws, wsn, err)
+    wps = [(wp, spk)] + [(wp.clone(), spk.clone()) for _ in range(replicas - 1)]
+
+    def set_replicas(r):
+        """Keep r copies of the packed weights (r >= 1)."""
+        del wps[max(1, r):]
+        wps.extend((wp.clone(), spk.clone()) for _ in range(r - len(wps)))
+
+    def gemm(i=0):
+        w, s = wps[i % len(wps)]
+        Q.qgemm_moe_grouped(d, w, s, afmt, As, Asf_s, off, P, None, C, ws, wsn, err)
 
     out.update(A_sorted=As, A_sf_sorted=Asf_s, C=C, err=err, route=route, permute=permute,
-               gemm=gemm)
+               gemm=gemm, set_replicas=set_replicas)
     return out
 
 
