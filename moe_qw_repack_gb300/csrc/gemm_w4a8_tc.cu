@@ -17,10 +17,15 @@
 //   warp 1      TMEM owner and single-thread MMA issuer: tcgen05.cp the stage's scale
 //               factors into TMEM, four 128x256x32 block-scaled MMAs, commit -> frees
 //               the stage; commit -> accumulator full at the end of a tile;
-//   warp 2      A scale loader: reads the canonical [rows][K/32] E8M0 bytes and writes
-//               the 32 x 16-byte image tcgen05.cp expects (row r -> lane r % 32,
-//               column r / 32, byte = group within the 128-wide K step);
-//   warps 3-10  epilogue: tcgen05.ld the FP32 accumulator (each warp one 32-lane
+//   warp 2      A scale fetcher: reads the canonical [rows][K/32] E8M0 bytes three stages
+//               ahead into registers and writes the 32 x 16-byte image tcgen05.cp
+//               expects (row r -> lane r % 32, column r / 32, byte = group within the
+//               128-wide K step) into an 8-slot staging ring;
+//   warp 3      A scale writer: copies a staged image into the stage once the stage is
+//               free, then the proxy fence that lets the tensor core read it.  (A
+//               fence waits for the thread's outstanding memory operations; keeping the
+//               global loads in another warp keeps them off the fence.)
+//   warps 4-11  epilogue: tcgen05.ld the FP32 accumulator (each warp one 32-lane
 //               quadrant x 128 columns), add bias, round to BF16, release TMEM, store.
 // Every mbarrier wait is bounded; on expiry the kernel raises QW_ERR_TIMEOUT, lets its
 // copies in flight land, frees TMEM and returns.
@@ -40,13 +45,14 @@ constexpr int A_BYTES = BM * BK;  // E4M3, one byte per element
 constexpr int B_BYTES = BN * BK;  // E2M1 unpacked by TMA: 16 codes in 8 bytes + 8 gap bytes
 constexpr int B_TX_BYTES = BN * BK / 2;  // the unpacking load credits the packed global bytes
 constexpr int SFA_BYTES = 512, SFB_CHUNK = 512, SFB_BYTES = 2 * SFB_CHUNK;
-constexpr int NUM_WARPS = 11, NUM_THREADS = NUM_WARPS * 32;
-constexpr int EPI_WARP0 = 3, NUM_EPI_WARPS = 8;
+constexpr int NUM_WARPS = 12, NUM_THREADS = NUM_WARPS * 32;
+constexpr int EPI_WARP0 = 4, NUM_EPI_WARPS = 8;
+constexpr int SF_STAGING = 8;  // staged A scale images (512 B each)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = 256;      // accumulator uses columns [0, 256)
 constexpr uint32_t SF_COLS_PER_STAGE = 12;  // 4 (A: 128 rows) + 8 (B: 256 rows)
-constexpr size_t SMEM_BYTES =
-    (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) + 256 + 1024;
+constexpr size_t SMEM_BYTES = (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) +
+                              (size_t)SF_STAGING * SFA_BYTES + 512 + 1024;
 
 // Instruction descriptor, kind::mxf8f6f4: A = E4M3 (0), B = E2M1 (5), both K-major,
 // N >> 3 at bit 17, scale type UE8M0 (bit 23), M >> 4 at bit 24; the B / A scale
@@ -117,9 +123,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sB = sA + STAGES * A_BYTES;
   uint8_t* sSFA = sB + STAGES * B_BYTES;
   uint8_t* sSFB = sSFA + STAGES * SFA_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFB + STAGES * SFB_BYTES);
+  uint8_t* sStage = sSFB + STAGES * SFB_BYTES;  // staged A scale images
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + SF_STAGING * SFA_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
+  uint64_t* sfull = empty + STAGES;   // staging slot written (32 fetcher lanes)
+  uint64_t* sempty = sfull + SF_STAGING;  // staging slot read (writer)
+  uint64_t* acc_full = sempty + SF_STAGING;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* final_bar = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
@@ -129,8 +138,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1 + 32);  // producer arrive.expect_tx + 32 scale-loader lanes
+      mbar_init(&full[s], 1 + 32);  // producer arrive.expect_tx + 32 scale-writer lanes
       mbar_init(&empty[s], 1);      // MMA commit
+    }
+    for (int s = 0; s < SF_STAGING; ++s) {
+      mbar_init(&sfull[s], 32);
+      mbar_init(&sempty[s], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, NUM_EPI_WARPS);
@@ -236,25 +249,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       drain_wait(final_bar, 0);
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ A scale loader
-    int stage = 0;
+    // ------------------------------------------------------------ A scale fetcher
+    // Global loads run three elements ahead of the staging writes; this warp never fences.
+    constexpr int AHEAD = 3;
+    int64_t lt = blockIdx.x;  // load cursor: tile and K step
+    int lkb = 0;
+    Tile lx = tile_at(p, lt < num_tiles ? lt : 0);
+    auto load_next = [&]() {
+      uint4 v = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      if (lt < num_tiles) {
+        v.x = load_sf_word(p, lx.rb + lane, lkb);
+        v.y = load_sf_word(p, lx.rb + 32 + lane, lkb);
+        v.z = load_sf_word(p, lx.rb + 64 + lane, lkb);
+        v.w = load_sf_word(p, lx.rb + 96 + lane, lkb);
+        if (++lkb == KB) {
+          lkb = 0;
+          lt += gridDim.x;
+          if (lt < num_tiles) lx = tile_at(p, lt);
+        }
+      }
+      return v;
+    };
+    uint4 ring[AHEAD];
+#pragma unroll
+    for (int i = 0; i < AHEAD; ++i) ring[i] = load_next();
+    int slot = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-      const Tile x = tile_at(p, t);
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
+        if (!mbar_wait(&sempty[slot], phase ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        uint4 v;
-        v.x = load_sf_word(p, x.rb + lane, kb);
-        v.y = load_sf_word(p, x.rb + 32 + lane, kb);
-        v.z = load_sf_word(p, x.rb + 64 + lane, kb);
-        v.w = load_sf_word(p, x.rb + 96 + lane, kb);
+        *reinterpret_cast<uint4*>(sStage + slot * SFA_BYTES + lane * 16) = ring[0];
+        mbar_arrive(&sfull[slot]);
+#pragma unroll
+        for (int i = 0; i + 1 < AHEAD; ++i) ring[i] = ring[i + 1];
+        ring[AHEAD - 1] = load_next();
+        if (++slot == SF_STAGING) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ A scale writer
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, sphase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&sfull[slot], sphase, abort_flag, p.err) ||
+            !mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint4 v = *reinterpret_cast<const uint4*>(sStage + slot * SFA_BYTES + lane * 16);
         *reinterpret_cast<uint4*>(sSFA + stage * SFA_BYTES + lane * 16) = v;
-        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[slot]);
+        fence_proxy_async_smem();  // only shared-memory accesses are outstanding here
         mbar_arrive(&full[stage]);
+        if (++slot == SF_STAGING) {
+          slot = 0;
+          sphase ^= 1u;
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
