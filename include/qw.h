@@ -112,8 +112,9 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *   INT4:  per expert [K/128][N_pad/16] blocks of 1 KiB: 32 lanes x 8 words; word s of
  *          lane l = 4g + t holds the eight weights lane l feeds to the s-th m16n8k16 MMA of
  *          the group, as excess-8 nibbles (q + 8): nibble i -> row g + 8 (i & 1),
- *          k = 32t + 4s + 2 ((i >> 1) & 1) + (i >> 2).  Lane t of a row quad thus owns k in
- *          [32t, 32t + 32) of the group.  Scales BF16 [K/128][N_pad].
+ *          k = 16s + 4t + 2 ((i >> 1) & 1) + (i >> 2) - rows g and g + 8 at the four k's
+ *          16s + 4t .. 16s + 4t + 3 (also the register layout of a 16-lane TMEM store).
+ *          Scales BF16 [K/128][N_pad].
  *   INT3:  per expert [K/128][N_pad/16] blocks of 768 B: 32 lanes x 4 words holding the
  *          low two bits of q + 4 for the lane's 64 weights (the INT4 (row, k) assignment),
  *          then 32 lanes x 2 words holding their third bit.  Scales BF16 [K/128][N_pad].

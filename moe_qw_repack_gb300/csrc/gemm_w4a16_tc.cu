@@ -18,10 +18,13 @@
 //   warp 1      TMEM owner and MMA issuer: per group, eight 128x128x16 MMAs with the
 //               weights as the A operand read from tensor memory and the tokens as the B
 //               operand, into one of two per-group accumulators;
-//   warps 2-5   dequantizers: thread = weight row = TMEM lane; each turns its row's excess
-//               codes into BF16 integers (code | 0x4300 = 128 + code, minus the excess) and
-//               writes the 16-wide k slices straight into the stage's TMEM columns
-//               (tcgen05.st) - the dequantized operand never touches shared memory;
+//   warps 2-5   dequantizers: warp q covers TMEM lanes 32q .. 32q + 31, i.e. two packed
+//               16 x 128 blocks; each lane decodes its own eight fragment words into BF16
+//               integers (code | 0x4300 = 128 + code, minus the excess) and one
+//               tcgen05.st.16x256b.x8 per block puts them at the rows and k columns of the
+//               stage's A operand - the packed layout is the register layout of that store,
+//               so the dequantized operand never touches shared memory and no lane moves data
+//               for another;
 //   warps 6-13  promotion and epilogue: read each group's accumulator (tcgen05.ld), add
 //               scale x it to FP32 registers, release it; at the end of the tile add bias,
 //               round to BF16 and store C[token][row] (lanes = consecutive rows).
@@ -97,11 +100,18 @@ __device__ __forceinline__ Tile tile_at(const Params& p, int64_t t) {
   return x;
 }
 
-__device__ __forceinline__ void tc_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+// 16 TMEM lanes x 64 columns: thread 4g + t, repetition j puts registers 4j .. 4j + 3 at
+// (lane g, column 8j + 2t), (g, 8j + 2t + 1), (g + 8, 8j + 2t), (g + 8, 8j + 2t + 1).
+__device__ __forceinline__ void tc_st_16x256b_x8(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 __device__ __forceinline__ void tc_wait_st() {
@@ -125,11 +135,6 @@ __device__ __forceinline__ uint32_t bf16x2_sub_u32(uint32_t x, uint32_t y) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -263,13 +268,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp < EPI_WARP0) {
     // ------------------------------------------------------------ dequantizers
-    // Thread = weight row r of the tile = TMEM lane.  The packed block stores, for lane slot
-    // 4 g + t, the pairs of rows g and g + 8 at k = 32t + 4s + 2 x' + {0, 1}; so the 16-wide
-    // k slice s' of row r sits in slot 4 (r & 7) + s'/2, steps 4 (s' % 2) .. + 3, fragment
-    // registers r0 and r0 + 2 (r0 = (r >> 3) & 1): one 16-byte shared load per slice.
-    const int q = warp & 3;          // TMEM lane quadrant
-    const int r = 32 * q + lane;     // weight row of the tile = TMEM lane
-    const int b = r >> 4, g8 = r & 7, r0 = (r >> 3) & 1;
+    // Lane 4g + t holds, in word s of a packed block, rows g and g + 8 at k = 16s + 4t ..
+    // 16s + 4t + 3: decoded to four BF16 pairs (a0..a3 = row g k+0/1, row g+8 k+0/1, row g
+    // k+2/3, row g+8 k+2/3) they are exactly repetition s of a 16x256b TMEM store.
+    const int q = warp & 3;  // TMEM lane quadrant: blocks 2q and 2q + 1 of the tile
     const uint32_t magic = 0x43004300u;
     const uint32_t excess = BITS == 4 ? 0x43084308u : 0x43044304u;
     int stage = 0;
@@ -278,47 +280,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
       const Tile x = tile_at(p, t);
       const int nbs = min(8, nblocks - x.nt * 8);
-      const bool live = b < nbs;
       for (int g = 0; g < G; ++g) {
         if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        const uint32_t blk = smem_u32(smem + stage * GE::STAGE) + ACT_BYTES + b * GE::BLK;
 #pragma unroll
-        for (int sl = 0; sl < 8; ++sl) {
-          const int slot = 4 * g8 + (sl >> 1);   // lane slot holding this k slice
-          const int sh = sl & 1;                 // its steps 4 sh .. 4 sh + 3
-          uint32_t col[8];
-          if (live) {
+        for (int hb = 0; hb < 2; ++hb) {
+          const int b = 2 * q + hb;
+          const uint32_t blk = smem_u32(smem + stage * GE::STAGE) + ACT_BYTES + b * GE::BLK;
+          uint32_t v[32];
+          if (b < nbs) {
             if constexpr (BITS == 4) {
-              const uint4 v = lds128(blk + slot * 32 + sh * 16);
-              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+              const uint4 w0 = lds128(blk + lane * 32), w1 = lds128(blk + lane * 32 + 16);
+              const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const int xr = r0 + 2 * (c & 1);
-                const uint32_t code = (w[c >> 1] >> (4 * xr)) & 0x000F000Fu;
-                col[c] = bf16x2_sub_u32(code | magic, excess);
+              for (int st = 0; st < 8; ++st) {
+                v[4 * st + 0] = bf16x2_sub_u32((w[st] & 0x000F000Fu) | magic, excess);
+                v[4 * st + 2] = bf16x2_sub_u32(((w[st] >> 4) & 0x000F000Fu) | magic, excess);
+                v[4 * st + 1] = bf16x2_sub_u32(((w[st] >> 8) & 0x000F000Fu) | magic, excess);
+                v[4 * st + 3] = bf16x2_sub_u32(((w[st] >> 12) & 0x000F000Fu) | magic, excess);
               }
             } else {
-              const uint2 lo = lds64(blk + slot * 16 + sh * 8);
-              const uint32_t hi = lds32(blk + 512 + slot * 8 + sh * 4);
-              const uint32_t L[2] = {lo.x, lo.y};
+              const uint4 lo = lds128(blk + lane * 16);
+              const uint2 hi = lds64(blk + 512 + lane * 8);
+              const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w}, H[2] = {hi.x, hi.y};
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const int j = c >> 1, xr = r0 + 2 * (c & 1);
-                const int ls = 2 * (4 * (j & 1) + xr);
-                const int hs = 4 * j + xr;
-                const uint32_t code =
-                    ((L[j >> 1] >> ls) & 0x00030003u) | (((hi >> hs) & 0x00010001u) << 2);
-                col[c] = bf16x2_sub_u32(code | magic, excess);
-              }
+              for (int st = 0; st < 8; ++st)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                  const int ls = 2 * (4 * (st & 1) + r), hs = 4 * (st & 3) + r;
+                  const uint32_t code = ((L[st >> 1] >> ls) & 0x00030003u) |
+                                        (((H[st >> 2] >> hs) & 0x00010001u) << 2);
+                  // register r (row g + 8 (r & 1), k + 2 (r >> 1)) -> store slot
+                  v[4 * st + ((r & 1) << 1) + (r >> 1)] = bf16x2_sub_u32(code | magic, excess);
+                }
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) col[c] = 0u;
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
           }
-          tc_st_32x32b_x8(tbase + ((uint32_t)(32 * q) << 16) + A_COL0 + 64 * stage + 8 * sl, col);
+          tc_st_16x256b_x8(tbase + ((uint32_t)(32 * q + 16 * hb) << 16) + A_COL0 + 64 * stage, v);
         }
         tc_wait_st();
         tc_fence_before();

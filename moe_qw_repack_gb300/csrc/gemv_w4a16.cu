@@ -244,13 +244,14 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
     int e, nb;
     int64_t rb, re;
     item_of<MCH>(p, blockIdx.x + it * gridDim.x, nblocks, e, nb, rb, re);
-    // B operand: lane (g, t) reads token rb + 8c + g at k = 32t .. 32t + 31 of each group;
-    // rows past the tile read row rb (their results land in outputs nobody stores)
+    // B operand: lane (g, t) reads token rb + 8c + g at k = 16s + 4t .. 16s + 4t + 3 for
+    // MMA step s (8 bytes); rows past the tile read row rb (their results land in outputs
+    // nobody stores)
     const uint16_t* arow[MCH];
 #pragma unroll
     for (int c = 0; c < MCH; ++c) {
       const int64_t r = rb + 8 * c + g;
-      arow[c] = p.A + (r < re ? r : rb) * (int64_t)p.K + 32 * t;
+      arow[c] = p.A + (r < re ? r : rb) * (int64_t)p.K + 4 * t;
     }
     float acc[MCH][4];
 #pragma unroll
@@ -286,18 +287,14 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
 #pragma unroll
               for (int i = 0; i < 4; ++i) pr[c][i] = sm[c][i] = 0.f;
             if constexpr (MCH == 1) {
-              // 16 contiguous bytes of the lane's k-slice serve two MMA steps
-              const uint4* qa = reinterpret_cast<const uint4*>(abase[0] + j * 128);
+              const uint2* qa = reinterpret_cast<const uint2*>(abase[0] + j * 128);
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const uint4 x = __ldg(qa + v);
+              for (int st = 0; st < 8; ++st) {
+                const uint2 x = __ldg(qa + 4 * st);  // k = 16 st + 4t .. + 3
                 uint32_t a[4];
-                biased_all<BITS>(w, 2 * v, a);
+                biased_all<BITS>(w, st, a);
                 mma_bf16_16816(pr[0], a, x.x, x.y);
                 mma_bf16_16816(sm[0], ones, x.x, x.y);
-                biased_all<BITS>(w, 2 * v + 1, a);
-                mma_bf16_16816(pr[0], a, x.z, x.w);
-                mma_bf16_16816(sm[0], ones, x.z, x.w);
               }
             } else {
 #pragma unroll
@@ -306,7 +303,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
                 biased_all<BITS>(w, s, a);
 #pragma unroll
                 for (int c = 0; c < MCH; ++c) {
-                  const uint2 x = __ldg(reinterpret_cast<const uint2*>(abase[c] + j * 128 + 4 * s));
+                  const uint2 x = __ldg(reinterpret_cast<const uint2*>(abase[c] + j * 128 + 16 * s));
                   mma_bf16_16816(pr[c], a, x.x, x.y);
                   mma_bf16_16816(sm[c], ones, x.x, x.y);
                 }
@@ -333,7 +330,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
               for (int r = 0; r < 4; ++r) a[r] = bf16x2_sub(a[r], bias2);  // exact
 #pragma unroll
               for (int c = 0; c < MCH; ++c) {
-                const uint2 x = __ldg(reinterpret_cast<const uint2*>(abase[c] + j * 128 + 4 * s));
+                const uint2 x = __ldg(reinterpret_cast<const uint2*>(abase[c] + j * 128 + 16 * s));
                 mma_bf16_16816(part[c], a, x.x, x.y);
               }
             }

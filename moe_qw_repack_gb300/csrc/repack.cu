@@ -19,16 +19,18 @@ __device__ __forceinline__ uint32_t int4_canon_nib(const uint32_t* wc, int32_t K
   return (wc[n * (K / 8) + k / 8] >> (4 * (k % 8))) & 0xFu;
 }
 
-// Mapping of one packed INT4 word (lane l, MMA step s of a 16 x 128 block) to the
-// weights it holds: nibble i feeds register r = i & 3 of the m16n8k16 A fragment, half
-// h = i >> 2; row = g + 8 * (r & 1), k = 32t + 4s + 2 * (r >> 1) + h, g = l / 4, t = l % 4.
-// The MMA does not care which real k sits in which of its k slots as long as the B
-// operand agrees, so lane t of every row quad owns k in [32t, 32t + 32) of the group:
-// its activations for a whole group are 64 contiguous bytes.
+// Mapping of one packed INT4 word (lane l, step s of a 16 x 128 block) to the weights it
+// holds: nibble i feeds register r = i & 3 of the m16n8k16 A fragment, half h = i >> 2;
+// row = g + 8 * (r & 1), k = 16s + 4t + 2 * (r >> 1) + h, g = l / 4, t = l % 4.
+// Word s thus holds rows g and g + 8 at the four k's 16s + 4t .. 16s + 4t + 3.  The
+// synchronous MMA does not care which real k sits in which of its k slots as long as the
+// B operand agrees (lane t's activations for step s are 8 contiguous bytes), and the same
+// four registers are exactly what tcgen05.st.16x256b puts at TMEM lanes g, g + 8 and
+// columns 8s + 2t, 8s + 2t + 1 - the tensor-core path stores decoded words as they are.
 __device__ __forceinline__ void int4_nib_pos(int l, int s, int i, int& row, int& k) {
   const int g = l >> 2, t = l & 3, r = i & 3, h = i >> 2;
   row = g + 8 * (r & 1);
-  k = 32 * t + 4 * s + 2 * (r >> 1) + h;
+  k = 16 * s + 4 * t + 2 * (r >> 1) + h;
 }
 
 __global__ void repack_int4_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
@@ -81,9 +83,9 @@ __global__ void unpack_int4_kernel(const uint32_t* __restrict__ wp, uint32_t* __
       const int k = k0 + j;
       const int G = k / 128, kk = k % 128;
       const int nb = (int)(n / 16), row = (int)(n % 16);
-      // invert int4_nib_pos: row = g + 8(r&1), kk = 32t + 4s + 2(r>>1) + h
-      const int g = row & 7, r0 = row >> 3, t = kk >> 5, s = (kk & 31) >> 2;
-      const int r1 = (kk & 3) >> 1, h = kk & 1;
+      // invert int4_nib_pos: row = g + 8(r&1), kk = 16s + 4t + 2(r>>1) + h
+      const int g = row & 7, r0 = row >> 3, t = (kk >> 2) & 3, s = kk >> 4;
+      const int r1 = (kk >> 1) & 1, h = kk & 1;
       const int lane = g * 4 + t, i = (r0 | (r1 << 1)) + 4 * h;
       const uint32_t word = wpe[((int64_t)G * (N_pad / 16) + nb) * 256 + lane * 8 + s];
       const uint32_t code = (word >> (4 * i)) & 0xFu;
@@ -105,7 +107,7 @@ __device__ __forceinline__ int32_t int3_canon(const uint32_t* wc, int32_t K, int
 }
 
 // Packed INT3 of lane l, step s, register r, half h (same (row, k) as the INT4 words:
-// row g + 8 (r & 1), k 32t + 4s + 2 (r >> 1) + h): the lo plane keeps u & 3 in word
+// row g + 8 (r & 1), k 16s + 4t + 2 (r >> 1) + h): the lo plane keeps u & 3 in word
 // s/2 at bits 2 * (4 * (s % 2) + r) + 16 h; the hi plane keeps u >> 2 in word s/4 at bit
 // 4 * (s % 4) + r + 16 h; u = q + 4.
 __global__ void repack_int3_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
@@ -127,7 +129,7 @@ __global__ void repack_int3_kernel(const uint32_t* __restrict__ wc, uint32_t* __
       for (int r = 0; r < 4; ++r)
         for (int h = 0; h < 2; ++h) {
           const int row = g + 8 * (r & 1);
-          const int k = G * 128 + 32 * t + 4 * s + 2 * (r >> 1) + h;
+          const int k = G * 128 + 16 * s + 4 * t + 2 * (r >> 1) + h;
           const int64_t n = (int64_t)nb * 16 + row;
           int32_t q = 0;
           if (n < N) {
@@ -164,8 +166,8 @@ __global__ void unpack_int3_kernel(const uint32_t* __restrict__ wp, uint32_t* __
       const int k = k0 + j;
       const int G = k / 128, kk = k % 128;
       const int nb = (int)(n / 16), row = (int)(n % 16);
-      const int t = kk >> 5, s = (kk & 31) >> 2, h = kk & 1;
-      const int g = row & 7, r = (row >> 3) | (((kk & 3) >> 1) << 1);
+      const int t = (kk >> 2) & 3, s = kk >> 4, h = kk & 1;
+      const int g = row & 7, r = (row >> 3) | (((kk >> 1) & 1) << 1);
       const int lane = g * 4 + t;
       const uint32_t* blk = wpe + ((int64_t)G * (N_pad / 16) + nb) * 192;
       const uint32_t L = blk[lane * 4 + s / 2], H = blk[128 + lane * 2 + s / 4];

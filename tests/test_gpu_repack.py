@@ -46,7 +46,7 @@ def test_mxfp4_roundtrip_bit_exact(E, N, K):
 
 def test_int4_packed_codes_are_excess8_fragments():
     """One 16 x 128 block: word (lane, step) nibble i holds q[row][k] + 8 with the m16n8k16
-    fragment mapping row = g + 8(r & 1), k = 32t + 4s + 2(r >> 1) + h (r = i & 3, h = i >> 2)."""
+    fragment mapping row = g + 8(r & 1), k = 16s + 4t + 2(r >> 1) + h (r = i & 3, h = i >> 2)."""
     rng = np.random.default_rng(5)
     q = rng.integers(-7, 8, (1, 16, 128))
     s = synth.to_bf16_bits(np.ones((1, 16, 1)))
@@ -60,7 +60,7 @@ def test_int4_packed_codes_are_excess8_fragments():
         for step in range(8):
             for i in range(8):
                 r, h = i & 3, i >> 2
-                row, k = g + 8 * (r & 1), 32 * t + 4 * step + 2 * (r >> 1) + h
+                row, k = g + 8 * (r & 1), 16 * step + 4 * t + 2 * (r >> 1) + h
                 assert (words[lane, step] >> (4 * i)) & 0xF == q[0, row, k] + 8
 
 
