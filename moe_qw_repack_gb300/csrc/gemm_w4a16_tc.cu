@@ -27,11 +27,18 @@
 //               for another;
 //   warps 6-13  promotion and epilogue: read each group's accumulator (tcgen05.ld), add
 //               scale x it to FP32 registers, release it; at the end of the tile add bias,
-//               round to BF16 and store C[token][row] (lanes = consecutive rows).
+//               round to BF16 and write the tile into a shared-memory staging tile
+//               [token][row] (lanes = consecutive rows: conflict-free 2-byte stores), which
+//               one thread hands to a TMA store - the warps go straight back to promoting
+//               the next tile instead of issuing 64 narrow global stores each.  MoE tiles
+//               that end inside a tile of 128 tokens (the next rows belong to another
+//               expert) and outputs whose row pitch is not a multiple of 16 bytes are stored
+//               directly instead.
 // Every wait is bounded; on expiry the kernel reports QW_ERR_TIMEOUT and shuts down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "qw_common.cuh"
@@ -77,6 +84,7 @@ struct Params {
   uint16_t* C;
   const int32_t* queue;
   int32_t* err;
+  int32_t tma_store;  // C's tensor map is valid (row pitch a multiple of 16 bytes)
 };
 
 struct Tile {
@@ -135,6 +143,12 @@ __device__ __forceinline__ uint32_t bf16x2_sub_u32(uint32_t x, uint32_t y) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// (a & b) | c in one logic instruction (written out so the compiler cannot split it)
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -154,13 +168,31 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) break;
 }
 
+__device__ __forceinline__ void tma_store_2d(const void* map, uint32_t smem_src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   map),
+               "r"(x), "r"(y), "r"(smem_src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+constexpr int STAGING_BYTES = BT * BW * 2;  // one BF16 output tile [token][row]
+
 template <int BITS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const Params p) {
+    gemm_w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmC, const Params p) {
   using GE = Geo<BITS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * GE::STAGE);
+  uint8_t* staging = smem + STAGES * GE::STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + STAGING_BYTES);
   uint64_t* aready = full + STAGES;
   uint64_t* empty = aready + STAGES;
   uint64_t* acc_full = empty + STAGES;   // [2] per-group accumulators
@@ -296,10 +328,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
               for (int st = 0; st < 8; ++st) {
-                v[4 * st + 0] = bf16x2_sub_u32((w[st] & 0x000F000Fu) | magic, excess);
-                v[4 * st + 2] = bf16x2_sub_u32(((w[st] >> 4) & 0x000F000Fu) | magic, excess);
-                v[4 * st + 1] = bf16x2_sub_u32(((w[st] >> 8) & 0x000F000Fu) | magic, excess);
-                v[4 * st + 3] = bf16x2_sub_u32(((w[st] >> 12) & 0x000F000Fu) | magic, excess);
+                v[4 * st + 0] = bf16x2_sub_u32(and_or(w[st], 0x000F000Fu, magic), excess);
+                v[4 * st + 2] = bf16x2_sub_u32(and_or(w[st] >> 4, 0x000F000Fu, magic), excess);
+                v[4 * st + 1] = bf16x2_sub_u32(and_or(w[st] >> 8, 0x000F000Fu, magic), excess);
+                v[4 * st + 3] = bf16x2_sub_u32(and_or(w[st] >> 12, 0x000F000Fu, magic), excess);
               }
             } else {
               const uint4 lo = lds128(blk + lane * 16);
@@ -310,10 +342,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                   const int ls = 2 * (4 * (st & 1) + r), hs = 4 * (st & 3) + r;
-                  const uint32_t code = ((L[st >> 1] >> ls) & 0x00030003u) |
-                                        (((H[st >> 2] >> hs) & 0x00010001u) << 2);
+                  const uint32_t hb = hs >= 2 ? H[st >> 2] >> (hs - 2) : H[st >> 2] << (2 - hs);
+                  const uint32_t biased =
+                      and_or(hb, 0x00040004u, and_or(L[st >> 1] >> ls, 0x00030003u, magic));
                   // register r (row g + 8 (r & 1), k + 2 (r >> 1)) -> store slot
-                  v[4 * st + ((r & 1) << 1) + (r >> 1)] = bf16x2_sub_u32(code | magic, excess);
+                  v[4 * st + ((r & 1) << 1) + (r >> 1)] = bf16x2_sub_u32(biased, excess);
                 }
             }
           } else {
@@ -371,8 +404,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) mbar_arrive(&acc_empty[ab]);
       }
       if (!ok) break;
-      if (nvalid) {
-        const float bias = p.bias ? __uint_as_float((uint32_t)__ldg(p.bias + (int64_t)x.e * p.N + n) << 16) : 0.f;
+      const float bias =
+          (p.bias && nvalid) ? __uint_as_float((uint32_t)__ldg(p.bias + (int64_t)x.e * p.N + n) << 16)
+                             : 0.f;
+      // dense tiles may run past the last row (the store clips them); MoE tiles may not
+      if (p.tma_store && (!p.queue || x.re - x.rb == BT)) {
+        const bool issuer = warp == EPI_WARP0 && lane == 0;
+        if (issuer) bulk_wait_read_all();  // the previous tile's store has read the staging
+        asm volatile("bar.sync 1, %0;" ::"r"(NUM_EPI_WARPS * 32) : "memory");
+        const uint32_t sbase = smem_u32(staging) + (uint32_t)(64 * half) * (BW * 2) +
+                               (uint32_t)(32 * q + lane) * 2;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          __nv_bfloat16 h = __float2bfloat16_rn(acc[i] + bias);
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(sbase + i * (BW * 2)),
+                       "h"(*reinterpret_cast<uint16_t*>(&h))
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 1, %0;" ::"r"(NUM_EPI_WARPS * 32) : "memory");
+        if (issuer) tma_store_2d(&tmC, smem_u32(staging), x.nt * BW, (int32_t)x.rb);
+      } else if (nvalid) {
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           const int64_t tok = x.rb + 64 * half + i;
@@ -383,6 +435,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+    if (warp == EPI_WARP0 && lane == 0) bulk_wait_all();  // stores done before exit
   }
 
   tc_fence_before();
@@ -408,16 +461,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int BITS>
-qw_status launch_bits(const CUtensorMap& tmA, const Params& p, int64_t tiles_max,
-                      cudaStream_t st) {
+qw_status launch_bits(const CUtensorMap& tmA, const CUtensorMap& tmC, const Params& p,
+                      int64_t tiles_max, cudaStream_t st) {
   using GE = Geo<BITS>;
-  const size_t smem = (size_t)STAGES * GE::STAGE + 256 + 1024;  // ring + barriers + alignment
+  // ring + output staging + barriers + alignment
+  const size_t smem = (size_t)STAGES * GE::STAGE + STAGING_BYTES + 256 + 1024;
   static const cudaError_t attr = cudaFuncSetAttribute(
       gemm_w4a16_tc_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return QW_ERR_CUDA;
   const int sms = device_sm_count();
   const unsigned grid = (unsigned)(tiles_max < sms ? (tiles_max < 1 ? 1 : tiles_max) : sms);
-  gemm_w4a16_tc_kernel<BITS><<<grid, NUM_THREADS, smem, st>>>(tmA, p);
+  gemm_w4a16_tc_kernel<BITS><<<grid, NUM_THREADS, smem, st>>>(tmA, tmC, p);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 
@@ -444,7 +498,22 @@ qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return QW_ERR_ALIGNMENT;
+  // output map: BF16 [rows][N], box 128 rows of N x 128 tokens, no swizzle; only when the
+  // row pitch is a multiple of 16 bytes (otherwise the kernel stores directly)
+  CUtensorMap tmC;
+  memset(&tmC, 0, sizeof(tmC));
+  bool tma_store = (d.N % 8) == 0 && (reinterpret_cast<uintptr_t>(C) % 16) == 0;
+  if (tma_store) {
+    cuuint64_t cdim[2] = {(cuuint64_t)d.N, (cuuint64_t)rs.rows};
+    cuuint64_t cstr[1] = {(cuuint64_t)d.N * 2};
+    cuuint32_t cbox[2] = {(cuuint32_t)BW, (cuuint32_t)BT};
+    tma_store = enc(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, cdim, cstr, cbox, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   Params p{};
+  p.tma_store = tma_store ? 1 : 0;
   p.rows = rs.rows;
   p.N = d.N;
   p.N_pad = d.N_pad;
@@ -470,8 +539,8 @@ qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
     p.queue = queue;
   }
   const int64_t tiles_max = max_m * p.num_n_tiles;
-  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_bits<4>(tmA, p, tiles_max, st)
-                                       : launch_bits<3>(tmA, p, tiles_max, st);
+  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_bits<4>(tmA, tmC, p, tiles_max, st)
+                                       : launch_bits<3>(tmA, tmC, p, tiles_max, st);
 }
 
 }  // namespace qw
