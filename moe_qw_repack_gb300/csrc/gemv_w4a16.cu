@@ -1,6 +1,7 @@
-// gemv_w4a16.cu - small-M W4A16 path: the packed weights stream once from HBM through a
-// deep shared-memory ring (bulk copies), are dequantized in registers and multiplied on
-// the tensor cores.
+// gemv_w4a16.cu - small-M W4A16 path: the packed weights stream once from HBM, are
+// dequantized in registers and multiplied on the tensor cores.  Two kernels share the
+// decode and MMA code: a register-ring kernel for dense calls and a TMA-ring kernel for
+// grouped (MoE) calls.
 //
 // What it computes (spke.com Humming announcement, "WnA16"; "フォーマットとアーキテクチャ
 // を横断して共有されるCUDAコンポーネント": dequantization and scaling inside the kernel,
@@ -9,33 +10,43 @@
 //
 // Design (GB300).  At M <= 64 the work is bound by HBM: 0.5 (INT4) or 0.375 (INT3) bytes
 // per weight against 2M flops.  Two things decide the speed: enough bytes in flight per SM
-// at every moment, and few issued instructions per weight (measured: the SM's issue slots,
-// not DRAM, limited the first versions of this kernel).
-//   - A work item is one 16-row block of N (times up to 8 x MCH token rows) over the whole
-//     of K; the 8 warps of a CTA split its scale groups into contiguous ranges and meet in
-//     shared memory at the end of the item (fixed-order sum: deterministic, no workspace).
-//   - A warp walks its (item, batch of NB groups) sequence with the next batch's packed
-//     words already loading into registers: each slot of the register ring is refilled
-//     (16-byte streaming loads of the lane's own fragment words, which the repack stored
-//     contiguously) right after the group in it is taken for compute, across item
-//     boundaries, so loads stay in flight while the CTA computes and reduces.
-//   - Codes become BF16 with one logic op per two weights: code | 0x4300 is the BF16 number
-//     128 + code.  With up to 16 token rows the MMA takes these biased values as they are
-//     and one extra MMA per step against an all-ones fragment yields the activation sums,
-//     so the group sum is P - (128 + excess) * sum(a) in FP32 (no BF16 subtracts); with
-//     more rows the bias is subtracted in BF16 (exact, small integers).  Per-group sums are
-//     scaled by the BF16 group scale in FP32.
-// The tensor pipe is mostly idle at these sizes, so the synchronous MMA is the natural
-// instruction.  No thread waits on another CTA or on a flag.
+// at every moment (HBM latency under load is microseconds), and few issued instructions
+// per weight (the SM's issue slots, not DRAM, limited the first versions of this kernel).
+// A work item is one 16-row block of N (times up to 8 x MCH token rows) over the whole of
+// K; the warps of a CTA split its scale groups and meet in shared memory at the end of the
+// item (fixed-order sum: deterministic, no workspace).
+//   - Dense (gemv_reg_kernel): 8 warps per CTA each own a contiguous range of groups and
+//     walk their (item, batch of 4 groups) sequence with the next batch's packed words
+//     already loading into a register ring (16-byte loads of the lane's own fragment
+//     words), refilled across item boundaries.
+//   - Grouped, and dense with 17-64 rows (gemv_tma_kernel): one producer thread per CTA
+//     streams an item's groups
+//     eight at a time: a 4-D tensor map views the packed weights as [expert][group][16-row
+//     block][1 KiB], so one TMA copy brings 8 groups of a block (8 KiB; 1 KiB copies
+//     measured far below HBM speed on this GPU, 4-8 KiB ones reach it) plus a 3-D copy of
+//     their scales into a 4-stage ring; four consumer warps take two groups of every stage
+//     (every consumer visits every stage in order, so the barrier phase parity cannot
+//     alias).  With MoE tiles of a few rows and short K (e.g. 640) this keeps more bytes in
+//     flight than the register ring; with dense shapes of few items the register ring's
+//     finer split of K wins (both measured).
+// Codes become BF16 with one logic op per two weights: code | 0x4300 is the BF16 number
+// 128 + code.  With up to 16 token rows the MMA takes these biased values as they are and
+// one extra MMA per step against an all-ones fragment yields the activation sums, so the
+// group sum is P - (128 + excess) * sum(a) in FP32 (no BF16 subtracts); with more rows the
+// bias is subtracted in BF16 (exact, small integers).  Per-group sums are scaled by the
+// BF16 group scale in FP32.  The tensor pipe is mostly idle at these sizes, so the
+// synchronous MMA is the natural instruction.  No thread waits on another CTA; every
+// mbarrier wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "qw_common.cuh"
 #include "qw_internal.h"
 
 namespace qw {
 namespace {
-
-constexpr int kWarps = 8;        // warps per CTA (split K of one item)
-// resident CTAs per SM a variant is built for (token rows cost registers)
-__host__ __device__ constexpr int ctas_per_sm(int mch) { return 2; }
 
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
   __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
@@ -98,6 +109,46 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint64_t* bar, int32_t c0,
+                                            int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint64_t* bar, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- register-ring kernel (dense)
+constexpr int kWarps = 8;        // warps per CTA (split K of one item)
+// resident CTAs per SM a variant is built for (token rows cost registers)
+__host__ __device__ constexpr int ctas_per_sm(int mch) { return 2; }
 
 template <int BITS>
 struct Geo {
@@ -195,7 +246,7 @@ __device__ __forceinline__ void biased_all(const uint32_t (&w)[Geo<BITS>::WPG], 
 
 template <int BITS, int MCH>
 __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
-    gemv_w4a16_kernel(const Params p) {
+    gemv_reg_kernel(const Params p) {
   using GE = Geo<BITS>;
   constexpr int WPG = GE::WPG;
   constexpr int NB = batch_groups(MCH);
@@ -373,8 +424,8 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
 }
 
 template <int BITS, int MCH>
-qw_status launch_variant(const Params& p, int64_t size_items, cudaStream_t st) {
-  auto kern = gemv_w4a16_kernel<BITS, MCH>;
+qw_status launch_reg_variant(const Params& p, int64_t size_items, cudaStream_t st) {
+  auto kern = gemv_reg_kernel<BITS, MCH>;
   const size_t smem = (size_t)kWarps * MCH * 128 * sizeof(float);
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -391,11 +442,338 @@ qw_status launch_variant(const Params& p, int64_t size_items, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 
+
+// ---------------------------------------------------------------- TMA-ring kernel (grouped)
+constexpr int kConsumers = 4;
+constexpr int kTmaThreads = (kConsumers + 1) * 32;
+constexpr int kStageGroups = 8;  // scale groups per stage (one TMA copy)
+constexpr int kStages = 4;
+
+__host__ __device__ constexpr int tma_ctas_per_sm(int mch) { return mch >= 4 ? 2 : 4; }
+
+template <int BITS>
+struct TmaGeo {
+  static constexpr int BLK = BITS == 4 ? 1024 : 768;  // one 16 x 128 block
+  static constexpr int W_STAGE = kStageGroups * BLK;
+  static constexpr int S_STAGE = kStageGroups * 16 * 2;  // BF16 scales of 16 rows x 8 groups
+  static constexpr int STAGE = W_STAGE + S_STAGE;
+  static constexpr float BIAS = BITS == 4 ? 136.f : 132.f;  // 128 + excess
+};
+
+template <int BITS, int MCH>
+constexpr size_t tma_smem_bytes() {
+  return 128 + (size_t)kStages * TmaGeo<BITS>::STAGE + 2 * 8 * kStages +
+         (size_t)kConsumers * MCH * 128 * 4 + 16;
+}
+
+struct TmaParams {
+  const uint16_t* A;
+  const uint16_t* bias;
+  uint16_t* C;
+  int32_t N, N_pad, K;
+  int64_t M;             // dense rows (unused when grouped)
+  const int32_t* queue;  // grouped tile queue or null
+  int32_t* err;
+};
+
+// One work item = (expert e, 16-row block nb, token rows [rb, re)), re - rb <= 8 * MCH.
+template <int MCH>
+__device__ __forceinline__ void tma_item_of(const TmaParams& p, uint32_t item, uint32_t nblocks, int& e,
+                                        int& nb, int64_t& rb, int64_t& re) {
+  const uint32_t tile = item / nblocks;
+  nb = (int)(item - tile * nblocks);
+  if (p.queue) {
+    e = __ldg(p.queue + 1 + 3 * tile);
+    rb = __ldg(p.queue + 2 + 3 * tile);
+    re = __ldg(p.queue + 3 + 3 * tile);
+  } else {
+    e = 0;
+    rb = (int64_t)tile * (8 * MCH);
+    re = min64(p.M, rb + 8 * MCH);
+  }
+}
+
+template <int BITS, int MCH>
+__global__ void __launch_bounds__(kTmaThreads, tma_ctas_per_sm(MCH))
+    gemv_tma_kernel(const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmS, const TmaParams p) {
+  using GE = TmaGeo<BITS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kStages * GE::STAGE);
+  uint64_t* empty = full + kStages;
+  float* red = reinterpret_cast<float*>(empty + kStages);  // [consumer][MCH][4][32]
+  volatile int* flags = reinterpret_cast<volatile int*>(red + kConsumers * MCH * 128);
+  // flags[0]: abort; flags[1]: abort as seen at the end of the current item
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const uint32_t nblocks = (uint32_t)(p.N_pad / 16);
+  const int G = p.K / 128;
+  const int chunks = (G + kStageGroups - 1) / kStageGroups;  // stages per item
+  // item counts stay below 2^31 (checked on the host): 32-bit index arithmetic
+  const uint32_t n_items = p.queue ? (uint32_t)__ldg(p.queue) * nblocks
+                                   : nblocks * (uint32_t)((p.M + 8 * MCH - 1) / (8 * MCH));
+  volatile int* abort_flag = flags;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmW);
+      tma_prefetch_desc(&tmS);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_phase = 0;  // per stage: used, phase of its last copy
+      bool ok = true;
+      for (uint32_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        int e, nb;
+        int64_t rb, re;
+        tma_item_of<MCH>(p, item, nblocks, e, nb, rb, re);
+        for (int c = 0; c < chunks; ++c) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = smem_u32(ring + stage * GE::STAGE);
+          mbar_arrive_expect_tx(&full[stage], GE::STAGE);
+          tma_load_4d(dst, &tmW, &full[stage], 0, nb, c * kStageGroups, e);
+          tma_load_3d(dst + GE::W_STAGE, &tmS, &full[stage], nb * 16, c * kStageGroups, e);
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // let every copy issued here land before the CTA's shared memory goes away
+      for (int s = 0; s < kStages; ++s)
+        if (issued & (1u << s)) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(&full[s], (issued_phase >> s) & 1u))
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int cw = warp - 1;
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t ring_base = smem_u32(ring);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (uint32_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+      int e, nb;
+      int64_t rb, re;
+      tma_item_of<MCH>(p, item, nblocks, e, nb, rb, re);
+      // B operand: lane (g, t) reads token rb + 8c + g at k = 16s + 4t .. 16s + 4t + 3 for
+      // MMA step s (8 bytes); rows past the tile read row rb (their results land in outputs
+      // nobody stores)
+      const uint16_t* arow[MCH];
+#pragma unroll
+      for (int c = 0; c < MCH; ++c) {
+        const int64_t r = rb + 8 * c + g;
+        arow[c] = p.A + (r < re ? r : rb) * (int64_t)p.K + 4 * t;
+      }
+      float acc[MCH][4];
+#pragma unroll
+      for (int c = 0; c < MCH; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[c][i] = 0.f;
+
+      for (int ch = 0; ch < chunks; ++ch) {
+        if (ok && !mbar_wait(&full[stage], phase, abort_flag, p.err)) ok = false;
+        if (ok) {
+          const uint32_t sbase = ring_base + stage * GE::STAGE;
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = 2 * cw + jj;  // group within the stage
+            const int gg = ch * kStageGroups + j;
+            if (gg < G) {
+              const uint32_t blk = sbase + j * GE::BLK;
+              uint32_t w[8];
+              if constexpr (BITS == 4) {
+                const uint4 v0 = lds128(blk + lane * 32), v1 = lds128(blk + lane * 32 + 16);
+                w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+                w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+              } else {
+                const uint4 lo = lds128(blk + lane * 16);
+                const uint2 hi = lds64(blk + 512 + lane * 8);
+                w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+                w[4] = hi.x; w[5] = hi.y; w[6] = 0; w[7] = 0;
+              }
+              // BF16 scales of rows g (low half) and g + 8 (high half) of this group
+              const uint32_t srow = sbase + GE::W_STAGE + j * 32;
+              const uint32_t sc = __byte_perm(lds32(srow + (g & ~1) * 2),
+                                              lds32(srow + ((g + 8) & ~1) * 2),
+                                              (g & 1) ? 0x7632 : 0x5410);
+              const float s_lo = __uint_as_float(sc << 16);
+              const float s_hi = __uint_as_float(sc & 0xFFFF0000u);
+              const int koff = gg * 128;
+              if constexpr (MCH <= 2) {
+                const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
+                float pr[MCH][4], sm[MCH][4];
+#pragma unroll
+                for (int c = 0; c < MCH; ++c)
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) pr[c][i] = sm[c][i] = 0.f;
+#pragma unroll
+                for (int st = 0; st < 8; ++st) {
+                  uint32_t a[4];
+                  biased<BITS>(st, w, a);
+#pragma unroll
+                  for (int c = 0; c < MCH; ++c) {
+                    const uint2 x = __ldg(reinterpret_cast<const uint2*>(arow[c] + koff + 16 * st));
+                    mma_bf16_16816(pr[c], a, x.x, x.y);
+                    mma_bf16_16816(sm[c], ones, x.x, x.y);
+                  }
+                }
+#pragma unroll
+                for (int c = 0; c < MCH; ++c)
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    acc[c][i] = fmaf(i < 2 ? s_lo : s_hi, fmaf(-GE::BIAS, sm[c][i], pr[c][i]),
+                                     acc[c][i]);
+              } else {
+                const uint32_t bias2 = BITS == 4 ? 0x43084308u : 0x43044304u;  // BF16 pair of BIAS
+                float part[MCH][4];
+#pragma unroll
+                for (int c = 0; c < MCH; ++c)
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) part[c][i] = 0.f;
+#pragma unroll
+                for (int st = 0; st < 8; ++st) {
+                  uint32_t a[4];
+                  biased<BITS>(st, w, a);
+#pragma unroll
+                  for (int r = 0; r < 4; ++r) a[r] = bf16x2_sub(a[r], bias2);  // exact
+#pragma unroll
+                  for (int c = 0; c < MCH; ++c) {
+                    const uint2 x = __ldg(reinterpret_cast<const uint2*>(arow[c] + koff + 16 * st));
+                    mma_bf16_16816(part[c], a, x.x, x.y);
+                  }
+                }
+#pragma unroll
+                for (int c = 0; c < MCH; ++c)
+#pragma unroll
+                  for (int i = 0; i < 4; ++i)
+                    acc[c][i] = fmaf(i < 2 ? s_lo : s_hi, part[c][i], acc[c][i]);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[stage]);  // this warp is done with the stage
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+
+      // ---------------------------------------------------------- reduce and store
+#pragma unroll
+      for (int c = 0; c < MCH; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) red[((cw * MCH + c) * 4 + i) * 32 + lane] = acc[c][i];
+      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");  // consumers only
+      if (threadIdx.x == 32) flags[1] = *abort_flag;
+      for (int o = threadIdx.x - 32; o < MCH * 128; o += kConsumers * 32) {
+        float v = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kConsumers; ++w2) v += red[w2 * MCH * 128 + o];
+        // fragment (lane l, register i) -> weight row gq + 8 (i >> 1), token 2 tt + (i & 1)
+        const int c = o >> 7, i = (o >> 5) & 3, l = o & 31;
+        const int gq = l >> 2, tt = l & 3;
+        const int n = nb * 16 + gq + 8 * (i >> 1);
+        const int64_t r = rb + 8 * c + 2 * tt + (i & 1);
+        if (n < p.N && r < re) {
+          if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + (int64_t)e * p.N + n) << 16);
+          __nv_bfloat16 h = __float2bfloat16_rn(v);
+          p.C[r * p.N + n] = *reinterpret_cast<uint16_t*>(&h);
+        }
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+      if (flags[1]) break;  // one snapshot for all consumers: they stop together
+    }
+  }
+  __syncthreads();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+template <int BITS, int MCH>
+qw_status launch_tma_variant(const CUtensorMap& tmW, const CUtensorMap& tmS, const TmaParams& p,
+                         int64_t size_items, cudaStream_t st) {
+  auto kern = gemv_tma_kernel<BITS, MCH>;
+  const size_t smem = tma_smem_bytes<BITS, MCH>();
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (attr != cudaSuccess) return QW_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTmaThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  int64_t grid = (int64_t)device_sm_count() * per_sm;
+  if (grid > size_items) grid = size_items;
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(tmW, tmS, p);
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
+
 int mch_for_rows(int64_t rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8; }
 
 int mch_for(const qw_packed_desc& d, int64_t rows, bool grouped) {
   if (!grouped) return mch_for_rows(rows);
   return mch_for_rows((rows + d.E - 1) / d.E);  // average rows per expert
+}
+
+// Dense calls with up to 16 token rows: the register-ring kernel.
+qw_status launch_dense_reg(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                           const void* A, const void* bias, void* C, int64_t M, int mch,
+                           cudaStream_t st) {
+  const int G = d.K / kIntGroup;
+  Params p{};
+  p.wp = static_cast<const uint8_t*>(w_packed);
+  p.sp = static_cast<const uint16_t*>(s_packed);
+  p.A = static_cast<const uint16_t*>(A);
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.C = static_cast<uint16_t*>(C);
+  p.N = d.N;
+  p.N_pad = d.N_pad;
+  p.K = d.K;
+  p.M = M;
+  p.w_estride = (int64_t)d.w_expert_stride;
+  p.s_estride = (int64_t)(d.s_expert_stride / 2);
+  p.gpw = (G + kWarps - 1) / kWarps;
+  const int64_t items = (d.N_pad / 16) * ((M + 8 * mch - 1) / (8 * mch));
+  if (items > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
+  const bool int4 = d.wfmt == QW_W_INT4_G128_BF16;
+  if (mch == 1)
+    return int4 ? launch_reg_variant<4, 1>(p, items, st) : launch_reg_variant<3, 1>(p, items, st);
+  return int4 ? launch_reg_variant<4, 2>(p, items, st) : launch_reg_variant<3, 2>(p, items, st);
 }
 
 }  // namespace
@@ -411,10 +789,41 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
                             void* ws, uint64_t ws_bytes, int32_t* err, cudaStream_t st) {
   const bool grouped = rs.offsets != nullptr;
   const int mch = mch_for(d, rs.rows, grouped);
-  const int G = d.K / 128;
-  Params p{};
-  p.wp = static_cast<const uint8_t*>(w_packed);
-  p.sp = static_cast<const uint16_t*>(s_packed);
+  if (!grouped && mch <= 2)
+    return launch_dense_reg(d, w_packed, s_packed, A, bias, C, rs.rows, mch, st);
+  // Grouped calls (over the device tile queue) and dense calls of 17-64 rows: the TMA ring.
+  const bool int4 = d.wfmt == QW_W_INT4_G128_BF16;
+  const int blk = int4 ? kInt4BlockBytes : kInt3BlockBytes;
+  const int G = d.K / kIntGroup;
+  const int64_t nblocks = d.N_pad / 16;
+  auto enc = encode_fn();
+  if (!enc) return QW_ERR_CUDA;
+  // weights: [E][G][N_pad/16][block] as 8-byte elements; one copy = 8 groups of a block
+  CUtensorMap tmW, tmS;
+  {
+    cuuint64_t dim[4] = {(cuuint64_t)(blk / 8), (cuuint64_t)nblocks, (cuuint64_t)G,
+                         (cuuint64_t)d.E};
+    cuuint64_t str[3] = {(cuuint64_t)blk, (cuuint64_t)(nblocks * blk),
+                         (cuuint64_t)d.w_expert_stride};
+    cuuint32_t box[4] = {(cuuint32_t)(blk / 8), 1, (cuuint32_t)kStageGroups, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4, const_cast<void*>(w_packed), dim, str, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QW_ERR_ALIGNMENT;
+  }
+  // scales: BF16 [E][G][N_pad]; one copy = the 16 rows of a block x 8 groups
+  {
+    cuuint64_t dim[3] = {(cuuint64_t)d.N_pad, (cuuint64_t)G, (cuuint64_t)d.E};
+    cuuint64_t str[2] = {(cuuint64_t)d.N_pad * 2, (cuuint64_t)d.s_expert_stride};
+    cuuint32_t box[3] = {16, (cuuint32_t)kStageGroups, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tmS, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(s_packed), dim, str, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QW_ERR_ALIGNMENT;
+  }
+  TmaParams p{};
   p.A = static_cast<const uint16_t*>(A);
   p.bias = static_cast<const uint16_t*>(bias);
   p.C = static_cast<uint16_t*>(C);
@@ -422,10 +831,7 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   p.N_pad = d.N_pad;
   p.K = d.K;
   p.M = rs.rows;
-  p.w_estride = (int64_t)d.w_expert_stride;
-  p.s_estride = (int64_t)(d.s_expert_stride / 2);
-  p.gpw = (G + kWarps - 1) / kWarps;
-  const int64_t nblocks = d.N_pad / 16;
+  p.err = err;
   int64_t max_items = nblocks * ((rs.rows + 8 * mch - 1) / (8 * mch));
   int64_t size_items = max_items;  // what the grid is sized for
   if (grouped) {
@@ -445,13 +851,11 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
     if (size_items > max_items) size_items = max_items;
   }
   if (max_items > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
-  (void)err;
-  const bool int4 = d.wfmt == QW_W_INT4_G128_BF16;
   switch (mch) {
-    case 1: return int4 ? launch_variant<4, 1>(p, size_items, st) : launch_variant<3, 1>(p, size_items, st);
-    case 2: return int4 ? launch_variant<4, 2>(p, size_items, st) : launch_variant<3, 2>(p, size_items, st);
-    case 4: return int4 ? launch_variant<4, 4>(p, size_items, st) : launch_variant<3, 4>(p, size_items, st);
-    default: return int4 ? launch_variant<4, 8>(p, size_items, st) : launch_variant<3, 8>(p, size_items, st);
+    case 1: return int4 ? launch_tma_variant<4, 1>(tmW, tmS, p, size_items, st) : launch_tma_variant<3, 1>(tmW, tmS, p, size_items, st);
+    case 2: return int4 ? launch_tma_variant<4, 2>(tmW, tmS, p, size_items, st) : launch_tma_variant<3, 2>(tmW, tmS, p, size_items, st);
+    case 4: return int4 ? launch_tma_variant<4, 4>(tmW, tmS, p, size_items, st) : launch_tma_variant<3, 4>(tmW, tmS, p, size_items, st);
+    default: return int4 ? launch_tma_variant<4, 8>(tmW, tmS, p, size_items, st) : launch_tma_variant<3, 8>(tmW, tmS, p, size_items, st);
   }
 }
 
