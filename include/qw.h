@@ -156,9 +156,9 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
  *   W4A8:  desc->wfmt MXFP4,     afmt QW_A_MXFP8_G32, A E4M3 [M][K], A_sf E8M0 [M][K/32].
  *   bias:  BF16 [N] or NULL.  C: BF16 [M][N].  desc->E must be 1.
  * Dispatch by M (the device heuristic of the announcement, section "デバイスパラメータに
- * 基づくパフォーマンスチューニング"): W4A16 with M <= 64 streams the weights through a
+ * 基づくパフォーマンスチューニング"): W4A16 with M <= 16 streams the weights through a
  * split-K tensor-core GEMV, larger M dequantizes into tensor memory and runs tcgen05 BF16
- * MMAs (grouped calls switch at 64 rows per expert on average); W4A8 runs the TMA +
+ * MMAs (grouped calls switch at 16 rows per expert on average); W4A8 runs the TMA +
  * tcgen05 block-scaled GEMM.
  * Alignment: A, C 16-byte aligned with K % 8 == 0 (BF16) or K % 16 == 0 (E4M3);
  * A_sf 4-byte aligned.  M >= 0 (M == 0 is a no-op).

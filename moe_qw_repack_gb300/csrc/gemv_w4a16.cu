@@ -8,7 +8,7 @@
 // bias fused into the output stage):
 //     C[m][n] = bf16( sum_g s[n][g] * sum_{k in g} a[m][k] * q[n][k]  + bias[n] )
 //
-// Design (GB300).  At M <= 64 the work is bound by HBM: 0.5 (INT4) or 0.375 (INT3) bytes
+// Design (GB300).  At M <= 16 the work is bound by HBM: 0.5 (INT4) or 0.375 (INT3) bytes
 // per weight against 2M flops.  Two things decide the speed: enough bytes in flight per SM
 // at every moment (HBM latency under load is microseconds), and few issued instructions
 // per weight (the SM's issue slots, not DRAM, limited the first versions of this kernel).
@@ -19,7 +19,7 @@
 //     walk their (item, batch of 4 groups) sequence with the next batch's packed words
 //     already loading into a register ring (16-byte loads of the lane's own fragment
 //     words), refilled across item boundaries.
-//   - Grouped, and dense with 17-64 rows (gemv_tma_kernel): one producer thread per CTA
+//   - Grouped (gemv_tma_kernel): one producer thread per CTA
 //     streams an item's groups
 //     eight at a time: a 4-D tensor map views the packed weights as [expert][group][16-row
 //     block][1 KiB], so one TMA copy brings 8 groups of a block (8 KiB; 1 KiB copies
@@ -743,7 +743,9 @@ qw_status launch_tma_variant(const CUtensorMap& tmW, const CUtensorMap& tmS, con
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 
-int mch_for_rows(int64_t rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : rows <= 32 ? 4 : 8; }
+// Token rows per item / 8: the dispatcher sends dense calls of at most 16 rows and grouped
+// calls averaging fewer than 16 rows per expert here (busier experts get more tiles).
+int mch_for_rows(int64_t rows) { return rows <= 8 ? 1 : 2; }
 
 int mch_for(const qw_packed_desc& d, int64_t rows, bool grouped) {
   if (!grouped) return mch_for_rows(rows);
@@ -791,7 +793,8 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   const int mch = mch_for(d, rs.rows, grouped);
   if (!grouped && mch <= 2)
     return launch_dense_reg(d, w_packed, s_packed, A, bias, C, rs.rows, mch, st);
-  // Grouped calls (over the device tile queue) and dense calls of 17-64 rows: the TMA ring.
+  // Grouped calls (over the device tile queue), and dense calls the dispatcher sends here
+  // with more rows: the TMA ring.
   const bool int4 = d.wfmt == QW_W_INT4_G128_BF16;
   const int blk = int4 ? kInt4BlockBytes : kInt3BlockBytes;
   const int G = d.K / kIntGroup;
@@ -851,12 +854,11 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
     if (size_items > max_items) size_items = max_items;
   }
   if (max_items > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
-  switch (mch) {
-    case 1: return int4 ? launch_tma_variant<4, 1>(tmW, tmS, p, size_items, st) : launch_tma_variant<3, 1>(tmW, tmS, p, size_items, st);
-    case 2: return int4 ? launch_tma_variant<4, 2>(tmW, tmS, p, size_items, st) : launch_tma_variant<3, 2>(tmW, tmS, p, size_items, st);
-    case 4: return int4 ? launch_tma_variant<4, 4>(tmW, tmS, p, size_items, st) : launch_tma_variant<3, 4>(tmW, tmS, p, size_items, st);
-    default: return int4 ? launch_tma_variant<4, 8>(tmW, tmS, p, size_items, st) : launch_tma_variant<3, 8>(tmW, tmS, p, size_items, st);
-  }
+  if (mch == 1)
+    return int4 ? launch_tma_variant<4, 1>(tmW, tmS, p, size_items, st)
+                : launch_tma_variant<3, 1>(tmW, tmS, p, size_items, st);
+  return int4 ? launch_tma_variant<4, 2>(tmW, tmS, p, size_items, st)
+              : launch_tma_variant<3, 2>(tmW, tmS, p, size_items, st);
 }
 
 }  // namespace qw

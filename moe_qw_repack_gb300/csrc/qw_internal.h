@@ -44,9 +44,12 @@ qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
                                cudaStream_t st);
 uint64_t gemm_w4a16_tc_workspace(const qw_packed_desc& d, int64_t max_rows);
 
-// Rows per token tile from which W4A16 runs on the tensor-core path (dense M, or the
-// average rows per expert of a grouped call); below it the GEMV streams the weights.
-constexpr int64_t kW4A16TensorCoreRows = 64;
+// Rows from which W4A16 runs on the tensor-core path (dense M above it, or a grouped call
+// averaging at least this many rows per expert); below it the GEMV streams the weights.
+// Measured on GB300 (14336 x 4096 INT4): the GEMV is faster at M <= 16, the tcgen05 path
+// from M = 32 (23.8 vs 36.3 us); MoE up projection E=128: GEMV 214 us vs tcgen05 114 us
+// at 16 rows per expert.
+constexpr int64_t kW4A16TensorCoreRows = 16;
 
 // Large-M W4A8: TMA + tcgen05 block-scaled GEMM.
 qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,

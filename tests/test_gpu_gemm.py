@@ -20,9 +20,10 @@ def assert_parity(C, R, absum, what=""):
 
 # ----------------------------------------------------------------------------- W4A16 small M
 @pytest.mark.parametrize("bits", [4, 3])
-@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (3, 40, 384), (8, 2048, 2048), (17, 96, 256),
-                                   (33, 200, 640), (64, 128, 1024), (130, 48, 256)])
+@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (3, 40, 384), (8, 2048, 2048), (13, 96, 256),
+                                   (16, 200, 640), (16, 128, 1024)])
 def test_w4a16_small_shapes(bits, M, N, K):
+    """M <= 16 runs the split-K tensor-core GEMV (one or two 8-row token slices)."""
     p = synth.w4a16_problem(M, N, K, bits=bits, cfg_id=100 + M)
     C = dense_w4a16(p)
     R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, bits)
@@ -112,10 +113,11 @@ def test_config2b_w4a8_full_size_sampled_rows():
 
 # ----------------------------------------------------------------------------- W4A16 large M
 @pytest.mark.parametrize("bits", [4, 3])
-@pytest.mark.parametrize("M,N,K", [(65, 40, 128), (128, 128, 256), (257, 200, 640),
-                                   (300, 1280, 4096), (129, 4096, 640)])
+@pytest.mark.parametrize("M,N,K", [(17, 96, 256), (33, 200, 640), (64, 128, 1024),
+                                   (65, 40, 128), (128, 128, 256), (130, 48, 256),
+                                   (257, 200, 640), (300, 1280, 4096), (129, 4096, 640)])
 def test_w4a16_tensor_core_shapes(bits, M, N, K):
-    """M > 64 runs the tcgen05 path: dequantized BF16 weights written into tensor memory."""
+    """M > 16 runs the tcgen05 path: dequantized BF16 weights written into tensor memory."""
     p = synth.w4a16_problem(M, N, K, bits=bits, cfg_id=400 + M)
     C = dense_w4a16(p)
     R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, bits)

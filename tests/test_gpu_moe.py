@@ -110,6 +110,20 @@ def test_moe_grouped_w4a16_small_t(T, bits):
     assert ok, (ratio, frob)
 
 
+@pytest.mark.parametrize("T", [12, 32])
+def test_moe_grouped_w4a16_around_the_path_switch(T):
+    """E=8 top-8: 12 rows per expert (GEMV, two 8-row slices per tile) and 32 rows per
+    expert (tcgen05 path); K=1024 -> N=512."""
+    Q = qw()
+    p, logits, sp, off, C = run_moe(Q.QW_A_BF16, 0, 8, T, 1024, 512, 8, 5)
+    _, _, roff, rsp = OM.route(logits, 8)
+    assert np.array_equal(off, roff) and np.array_equal(sp, rsp)
+    R, S = OM.grouped_w4a16(p["A"][rsp // 8], roff, OF.unpack_int4(p["w_canon"], 1024),
+                            p["s_canon"])
+    ok, ratio, frob = OQ.check_bf16_result(C, R, S)
+    assert ok, (ratio, frob)
+
+
 def test_moe_grouped_w4a16_down_k640():
     """Down-projection K=640 -> N=4096 (K not a multiple of 256) on a per-pair input."""
     Q = qw()
