@@ -12,4 +12,4 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its CPU-baseline 
 Pin status of every function (what checks it against something other than itself)
 is listed in each module's docstring; nothing here is "parity unpinned".
 """
-from . import formats, qgemm, moe  # noqa: F401
+from . import act, formats, qgemm, moe  # noqa: F401
