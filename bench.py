@@ -266,7 +266,8 @@ def extra_w4a16(steps, warmup, world, only=None):
 def extra_moe(steps, warmup, world, only=None):
     """Grouped MoE workloads: W4A8 (E=256, top-8, T=4096, 7168 -> 4096) and the W4A16
     intermediate-640 token sweep (E=128, top-8, up 4096 -> 1280 plus down 640 -> 4096).
-    One step = route + permute + grouped GEMM(s); inputs drawn on the device.  Steps are
+    One step = route + permute + grouped GEMM(s) (+ for W4A16 the SiLU*mul between the
+    projections and the top-k combine after them); inputs drawn on the device.  Steps are
     replayed from a CUDA graph; each part is also timed alone the same way."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import moe_qw_repack_gb300.qw as Q
@@ -300,7 +301,19 @@ def extra_moe(steps, warmup, world, only=None):
         "active_experts": active, "active_weight_GB": round(wbytes / 1e9, 3),
         "weight_stream_frac_hbm": round(wbytes / (gemm_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
         "steps": n, "graph": graph}
-    del r
+    # BF16 -> MXFP8 activation quantizer for the same tokens (T x hidden 7168)
+    xa = sd.bf16_activations(T, K, cfg_id=3)
+    qa = torch.empty((T, K), dtype=torch.uint8, device="cuda")
+    qsf = torch.empty((T, K // 32), dtype=torch.uint8, device="cuda")
+    qerr = Q.new_error_flag()
+    q_ms = time_region([lambda i: Q.qw_quantize_mxfp8(xa, T, K, qa, qsf, qerr)], steps, warmup,
+                       world, graph_steps=4)[0]
+    assert Q.qw_read_error(qerr) == 0
+    qbytes = T * K * 2 + T * K + T * K // 32
+    out["cfg4_moe_w4a8_E256_T4096"].update({
+        "us_quantize_bf16_to_mxfp8": round(q_ms * 1e3, 1),
+        "quantize_frac_hbm": round(qbytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)})
+    del r, xa, qa, qsf
     torch.cuda.empty_cache()
     return _extra_moe_w4a16(steps, warmup, world, only, parts, out, peaks)
 
@@ -331,20 +344,36 @@ def _extra_moe_w4a16(steps, warmup, world, only, parts, out, peaks):
         R = min(32, replicas_for(n_active * (1280 * 4096 // 2 + 4096 * 640 // 2)))
         up["set_replicas"](R)
         dn["set_replicas"](R)
+        # the layer's remaining steps: silu(gate) * up -> the down projection's input x, and
+        # the top-k weighted combine of the down projection's rows back to the T tokens
+        lg = up["logits_dev"]
+        y = torch.empty((T, 4096), dtype=torch.int16, device="cuda")
+        cws_n = Q.qgemm_moe_combine_workspace_size(T, k)
+        cws = torch.empty(cws_n, dtype=torch.uint8, device="cuda")
+        cerr = Q.new_error_flag()
+
+        def silu(i, up=up, x=x, P=P):
+            Q.qw_silu_mul(up["C"], P, 640, x)
+
+        def combine(i, dn=dn, up=up, lg=lg, y=y, T=T, cws=cws, cws_n=cws_n, cerr=cerr):
+            Q.qgemm_moe_combine(dn["C"], up["sorted_pairs"], up["topk_ids"], lg, T, E, k, 4096,
+                                y, cws, cws_n, cerr)
         n_steps = max(steps, R) if T <= 256 else max(5, steps // 4)
-        tot, each, n, graph = parts([up["route"], up["permute"], up["gemm"], dn["gemm"]], n_steps,
-                                    max(R, 4))
+        tot, each, n, graph = parts([up["route"], up["permute"], up["gemm"], silu, dn["gemm"],
+                                     combine], n_steps, max(R, 4))
+        assert Q.qw_read_error(cerr) == 0
         assert Q.qw_read_error(up["err"]) == 0 and Q.qw_read_error(dn["err"]) == 0
         cnt = np.diff(up["offsets"].cpu().numpy())
         active = int((cnt > 0).sum())
-        up_ms, dn_ms = each[2], each[3]
+        up_ms, dn_ms = each[2], each[4]
         wbytes_up = active * (1280 * 4096 // 2 + 1280 * 32 * 2)
         wbytes_dn = active * (4096 * 640 // 2 + 4096 * 5 * 2)
         flop = 2.0 * P * (1280 * 4096 + 4096 * 640)
         out[names[T]] = {
             "us_total": round(tot * 1e3, 1), "us_route": round(each[0] * 1e3, 1),
             "us_permute": round(each[1] * 1e3, 1),
-            "us_up": round(up_ms * 1e3, 1), "us_down": round(dn_ms * 1e3, 1),
+            "us_up": round(up_ms * 1e3, 1), "us_silu_mul": round(each[3] * 1e3, 1),
+            "us_down": round(dn_ms * 1e3, 1), "us_combine": round(each[5] * 1e3, 1),
             "gemm_tflops": round(flop / ((up_ms + dn_ms) * 1e-3) / 1e12, 2),
             "active_experts": active,
             "weight_GBps": round((wbytes_up + wbytes_dn) / ((up_ms + dn_ms) * 1e-3) / 1e9, 1),

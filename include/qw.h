@@ -213,6 +213,43 @@ qw_status qgemm_moe_permute(int32_t afmt, const void* A, const void* A_sf, int32
                             void* A_sorted, void* A_sf_sorted, void* stream);
 
 /* --------------------------------------------------------------------------------------
+ * Activation-side steps around the GEMMs of a MoE layer (the pages time gate-up + down as
+ * one unit, spke.com announcement "パフォーマンス"; MXFP8 activations: "W8A8 / W4A8 / W4A4").
+ *
+ * qw_quantize_mxfp8 - BF16 activations -> the W4A8 GEMM's MXFP8 input.  Per group of 32
+ *   consecutive values of a row (OCP Microscaling v1.0 conversion): X = floor(log2(max|v|))
+ *   - 8 clamped to [-127, 127], A_sf = X + 127 (E8M0); A_q = E4M3(v / 2^X) rounded to
+ *   nearest even and saturated to +-448; an all-zero group gets A_sf = 0.
+ *   A: BF16 [rows][K]; A_q: uint8 [rows][K]; A_sf: uint8 [rows][K/32] (device).
+ *   K % 32 == 0; A 16-byte aligned, A_q 8-byte aligned.  A non-finite input sets
+ *   QW_ERR_VALUE in d_err (its group's outputs are then unspecified).
+ */
+qw_status qw_quantize_mxfp8(const void* A, int64_t rows, int32_t K, void* A_q, void* A_sf,
+                            int32_t* d_err, void* stream);
+
+/* qw_silu_mul - Y[r][i] = bf16( silu(GU[r][i]) * GU[r][I + i] ), silu(g) = g / (1 + e^-g):
+ *   the fused gate+up projection output (gate in the first half of each row) -> the down
+ *   projection's input.  GU: BF16 [rows][2I]; Y: BF16 [rows][I] (device).  FP32 arithmetic,
+ *   BF16 round-to-nearest-even.  I % 8 == 0; GU and Y 16-byte aligned.
+ */
+qw_status qw_silu_mul(const void* GU, int64_t rows, int32_t I, void* Y, void* stream);
+
+/* qgemm_moe_combine - out[t][n] = bf16( sum_j w[t][j] * Y[row of pair t*topk + j][n] ):
+ *   the down projection's rows (in the sorted-pair order of qgemm_moe_route, row r holding
+ *   pair sorted_pairs[r]) weighted and summed back per token, w[t][.] = softmax of token
+ *   t's topk selected logits (logits[t][topk_ids[t][j]]), FP32.
+ *   Y: BF16 [T*topk][N]; sorted_pairs int32 [T*topk]; topk_ids int32 [T][topk]; logits
+ *   float32 [T][E]; out: BF16 [T][N] (all device).  N % 8 == 0; Y, out 16-byte aligned;
+ *   1 <= topk <= 32.  workspace: >= qgemm_moe_combine_workspace_size(T, topk) device
+ *   bytes (scratch, any content).  Out-of-range ids or pairs set QW_ERR_INVALID_ARG in d_err.
+ */
+qw_status qgemm_moe_combine_workspace_size(int32_t T, int32_t topk, uint64_t* bytes);
+qw_status qgemm_moe_combine(const void* Y, const int32_t* sorted_pairs, const int32_t* topk_ids,
+                            const float* logits, int32_t T, int32_t E, int32_t topk, int32_t N,
+                            void* out, void* workspace, uint64_t ws_bytes, int32_t* d_err,
+                            void* stream);
+
+/* --------------------------------------------------------------------------------------
  * qgemm_moe_grouped - Grouped MoE GEMM: for every expert e and every row r in
  * [expert_offsets[e], expert_offsets[e+1]):
  *   C[r][n] = bf16( sum_k A_sorted[r][k] * W_e[n][k] + bias[e][n] ).

@@ -234,6 +234,51 @@ qw_status qgemm_moe_permute(int32_t afmt, const void* A, const void* A_sf, int32
                             static_cast<cudaStream_t>(stream));
 }
 
+qw_status qw_quantize_mxfp8(const void* A, int64_t rows, int32_t K, void* A_q, void* A_sf,
+                            int32_t* d_err, void* stream) {
+  if (rows < 0 || K < 32) return QW_ERR_INVALID_ARG;
+  if (K % 32) return QW_ERR_UNSUPPORTED;
+  if (rows == 0) return QW_OK;
+  if (!A || !A_q || !A_sf) return QW_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(A_q, 8)) return QW_ERR_ALIGNMENT;
+  if (rows * (int64_t)(K / 8) > ((int64_t)1 << 40)) return QW_ERR_UNSUPPORTED;
+  return launch_quantize_mxfp8(A, rows, K, A_q, A_sf, d_err, static_cast<cudaStream_t>(stream));
+}
+
+qw_status qw_silu_mul(const void* GU, int64_t rows, int32_t I, void* Y, void* stream) {
+  if (rows < 0 || I < 1) return QW_ERR_INVALID_ARG;
+  if (I % 8) return QW_ERR_UNSUPPORTED;
+  if (rows == 0) return QW_OK;
+  if (!GU || !Y) return QW_ERR_INVALID_ARG;
+  if (!aligned(GU, 16) || !aligned(Y, 16)) return QW_ERR_ALIGNMENT;
+  return launch_silu_mul(GU, rows, I, Y, static_cast<cudaStream_t>(stream));
+}
+
+qw_status qgemm_moe_combine_workspace_size(int32_t T, int32_t topk, uint64_t* bytes) {
+  if (!bytes || T < 0 || topk < 1 || topk > 32) return QW_ERR_INVALID_ARG;
+  *bytes = (uint64_t)T * (uint64_t)topk * 4 + 256;
+  return QW_OK;
+}
+
+qw_status qgemm_moe_combine(const void* Y, const int32_t* sorted_pairs, const int32_t* topk_ids,
+                            const float* logits, int32_t T, int32_t E, int32_t topk, int32_t N,
+                            void* out, void* workspace, uint64_t ws_bytes, int32_t* d_err,
+                            void* stream) {
+  if (T < 0 || E < 1 || topk < 1 || topk > 32 || topk > E || N < 1) return QW_ERR_INVALID_ARG;
+  if (N % 8) return QW_ERR_UNSUPPORTED;
+  if (T == 0) return QW_OK;
+  if (!Y || !sorted_pairs || !topk_ids || !logits || !out) return QW_ERR_INVALID_ARG;
+  if (!aligned(Y, 16) || !aligned(out, 16) || !aligned(sorted_pairs, 4) || !aligned(topk_ids, 4) ||
+      !aligned(logits, 4))
+    return QW_ERR_ALIGNMENT;
+  uint64_t need = 0;
+  qgemm_moe_combine_workspace_size(T, topk, &need);
+  if (!workspace || ws_bytes < need || !aligned(workspace, 4)) return QW_ERR_WORKSPACE;
+  return launch_moe_combine(Y, sorted_pairs, topk_ids, logits, T, E, topk, N, out,
+                            static_cast<int32_t*>(workspace), d_err,
+                            static_cast<cudaStream_t>(stream));
+}
+
 qw_status qgemm_moe_grouped(const qw_packed_desc* desc, const void* w_packed,
                             const void* s_packed, int32_t afmt, const void* A_sorted,
                             const void* A_sf_sorted, const int32_t* expert_offsets,

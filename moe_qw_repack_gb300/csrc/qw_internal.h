@@ -51,6 +51,14 @@ uint64_t gemm_w4a16_tc_workspace(const qw_packed_desc& d, int64_t max_rows);
 // at 16 rows per expert.
 constexpr int64_t kW4A16TensorCoreRows = 16;
 
+// Activation-side MoE steps (act.cu).
+qw_status launch_quantize_mxfp8(const void* A, int64_t rows, int32_t K, void* Q, void* SF,
+                                int32_t* err, cudaStream_t st);
+qw_status launch_silu_mul(const void* GU, int64_t rows, int32_t I, void* Y, cudaStream_t st);
+qw_status launch_moe_combine(const void* Y, const int32_t* sorted_pairs, const int32_t* topk_ids,
+                             const float* logits, int32_t T, int32_t E, int32_t topk, int32_t N,
+                             void* out, int32_t* inv, int32_t* err, cudaStream_t st);
+
 // Large-M W4A8: TMA + tcgen05 block-scaled GEMM.
 qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
                            const void* A, const void* A_sf, const void* bias, void* C,

@@ -34,7 +34,8 @@ EXPORTS = (
     "qw_status_str", "qw_version", "qw_repack_query", "qw_repack", "qw_unpack",
     "qgemm_workspace_size", "qgemm_dense", "qgemm_moe_route_workspace_size", "qgemm_moe_route",
     "qgemm_moe_permute", "qgemm_moe_grouped", "qw_read_error", "qw_test_wait_timeout",
-    "qgemm_moe_route_noalloc",
+    "qgemm_moe_route_noalloc", "qw_quantize_mxfp8", "qw_silu_mul",
+    "qgemm_moe_combine_workspace_size", "qgemm_moe_combine",
 )
 
 
@@ -75,6 +76,10 @@ _SIGS = {
     "qw_read_error": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
     "qw_test_wait_timeout": (_I32, [_P, _I64, _P]),
     "qgemm_moe_route_noalloc": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
+    "qw_quantize_mxfp8": (_I32, [_P, _I64, _I32, _P, _P, _P, _P]),
+    "qw_silu_mul": (_I32, [_P, _I64, _I32, _P, _P]),
+    "qgemm_moe_combine_workspace_size": (_I32, [_I32, _I32, ctypes.POINTER(_U64)]),
+    "qgemm_moe_combine": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _U64, _P, _P]),
 }
 
 
@@ -198,6 +203,29 @@ def qgemm_moe_grouped(desc, w_packed, s_packed, afmt, A_sorted, A_sf_sorted, exp
     _check("qgemm_moe_grouped", LIB.qgemm_moe_grouped(
         ctypes.byref(desc), _ptr(w_packed), _ptr(s_packed), afmt, _ptr(A_sorted),
         _ptr(A_sf_sorted), _ptr(expert_offsets), total_rows, _ptr(bias), _ptr(C),
+        _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)))
+
+
+def qw_quantize_mxfp8(A, rows, K, A_q, A_sf, d_err=None, stream=None):
+    _check("qw_quantize_mxfp8", LIB.qw_quantize_mxfp8(_ptr(A), rows, K, _ptr(A_q), _ptr(A_sf),
+                                                      _ptr(d_err), _stream(stream)))
+
+
+def qw_silu_mul(GU, rows, I, Y, stream=None):
+    _check("qw_silu_mul", LIB.qw_silu_mul(_ptr(GU), rows, I, _ptr(Y), _stream(stream)))
+
+
+def qgemm_moe_combine_workspace_size(T: int, topk: int) -> int:
+    n = _U64(0)
+    _check("qgemm_moe_combine_workspace_size",
+           LIB.qgemm_moe_combine_workspace_size(T, topk, ctypes.byref(n)))
+    return n.value
+
+
+def qgemm_moe_combine(Y, sorted_pairs, topk_ids, logits, T, E, topk, N, out, workspace,
+                      ws_bytes, d_err=None, stream=None):
+    _check("qgemm_moe_combine", LIB.qgemm_moe_combine(
+        _ptr(Y), _ptr(sorted_pairs), _ptr(topk_ids), _ptr(logits), T, E, topk, N, _ptr(out),
         _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)))
 
 

@@ -119,8 +119,8 @@ def moe_pipeline(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4, weights=None, x_s
     off = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
     n = Q.qgemm_moe_route_workspace_size(T, E, topk)
     rws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
-    out = dict(logits=logits, w_canon=w_canon, s_canon=s_canon, desc=d, wp=wp, sp_packed=spk,
-               sorted_pairs=sp, offsets=off, topk_ids=ids)
+    out = dict(logits=logits, logits_dev=lg, w_canon=w_canon, s_canon=s_canon, desc=d, wp=wp,
+               sp_packed=spk, sorted_pairs=sp, offsets=off, topk_ids=ids)
 
     def route(i=0):
         Q.qgemm_moe_route(lg, T, E, topk, ids, sp, off, rws, n)

@@ -117,3 +117,30 @@ def test_timeout_probe_validation(Q):
         Q.qw_test_wait_timeout(None, 1000, stream=0)
     with pytest.raises(Q.QwError):
         Q.qw_test_wait_timeout(1 << 20, 3_000_000_000, stream=0)
+
+
+def test_activation_steps_host_validation(Q):
+    good = 1 << 20
+    for K, status in [(48, Q.QW_ERR_UNSUPPORTED), (16, Q.QW_ERR_INVALID_ARG)]:
+        with pytest.raises(Q.QwError) as e:
+            Q.qw_quantize_mxfp8(good, 4, K, good, good, stream=0)
+        assert e.value.status == status
+    with pytest.raises(Q.QwError) as e:  # A not 16-byte aligned
+        Q.qw_quantize_mxfp8(good + 8, 4, 64, good, good, stream=0)
+    assert e.value.status == Q.QW_ERR_ALIGNMENT
+    Q.qw_quantize_mxfp8(good, 0, 64, good, good, stream=0)  # no rows: a no-op
+    with pytest.raises(Q.QwError) as e:
+        Q.qw_silu_mul(good, 4, 12, good, stream=0)
+    assert e.value.status == Q.QW_ERR_UNSUPPORTED
+    with pytest.raises(Q.QwError) as e:
+        Q.qw_silu_mul(good, 4, 64, good + 4, stream=0)
+    assert e.value.status == Q.QW_ERR_ALIGNMENT
+    assert Q.qgemm_moe_combine_workspace_size(4096, 8) == 4096 * 8 * 4 + 256
+    for T, E, k, N, status in [(4, 8, 0, 64, Q.QW_ERR_INVALID_ARG), (4, 8, 9, 64, Q.QW_ERR_INVALID_ARG),
+                               (4, 8, 2, 12, Q.QW_ERR_UNSUPPORTED)]:
+        with pytest.raises(Q.QwError) as e:
+            Q.qgemm_moe_combine(good, good, good, good, T, E, k, N, good, good, 1 << 20, stream=0)
+        assert e.value.status == status
+    with pytest.raises(Q.QwError) as e:
+        Q.qgemm_moe_combine(good, good, good, good, 4, 8, 2, 64, good, good, 8, stream=0)
+    assert e.value.status == Q.QW_ERR_WORKSPACE
