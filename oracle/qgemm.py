@@ -66,6 +66,21 @@ def gemm_w4a8(A_codes, A_sf, w_codes, w_sf, bias_bits=None):
     return r, absum
 
 
+def gemm_w8a8(A_codes, A_sf, w_codes, w_sf, bias_bits=None):
+    """MXFP8 x MXFP8: A_codes [M][K] E4M3, A_sf [M][K/32] E8M0, w_codes [N][K] E4M3 byte
+    codes, w_sf [N][K/32] E8M0 -> (R, absum).  The pages' "W8A8" MX kind (spke.com
+    announcement, "W8A8 / W4A8 / W4A4")."""
+    a = dequant_mx(A_codes, A_sf, F.decode_e4m3)
+    w = dequant_mx(w_codes, w_sf, F.decode_e4m3)
+    r = a @ w.T
+    absum = np.abs(a) @ np.abs(w).T
+    if bias_bits is not None:
+        b = F.decode_bf16(bias_bits)
+        r = r + b[None, :]
+        absum = absum + np.abs(b)[None, :]
+    return r, absum
+
+
 # --------------------------------------------------------------- canonical-input drivers
 def w4a16_from_canonical(A_bits, w_canon, s_canon, K, bits, bias_bits=None, rows=None, cols=None):
     """Unpack canonical packed words (one expert) and run :func:`gemm_w4a16`.

@@ -201,3 +201,36 @@ def test_planted_transposed_operand_is_caught(monkeypatch):
     monkeypatch.setattr(Q, "gemm_w4a16", transposed)
     with pytest.raises(AssertionError):
         test_w4a16_exact_integer_dot()
+
+
+def test_w8a8_exact_integer_dot():
+    """Integer-valued E4M3 codes with unit scales: an exact integer dot product."""
+    rng = np.random.default_rng(31)
+    M, N, K = 3, 4, 64
+    ints = rng.integers(-16, 17, (M, K))
+    wint = rng.integers(-16, 17, (N, K))
+    enc = {v: c for c, v in enumerate(F.decode_e4m3(np.arange(127))) if float(v).is_integer()}
+    code = lambda v: (enc[abs(int(v))] | (0x80 if v < 0 else 0))  # noqa: E731
+    A = np.vectorize(code)(ints).astype(np.uint8)
+    W = np.vectorize(code)(wint).astype(np.uint8)
+    ones_a = np.full((M, K // 32), 127, np.uint8)
+    ones_w = np.full((N, K // 32), 127, np.uint8)
+    R, S = Q.gemm_w8a8(A, ones_a, W, ones_w)
+    assert np.array_equal(R, (ints @ wint.T).astype(np.float64))
+
+
+def test_w8a8_equals_w4a8_on_e2m1_values():
+    """E2M1 values are E4M3 values: re-encoding the E2M1 weights as E4M3 codes (with the
+    E4M3 encoder of oracle/act) must give the W4A8 result exactly."""
+    from oracle import act as OA
+    rng = np.random.default_rng(32)
+    M, N, K = 5, 7, 96
+    A = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    A[(A & 0x7F) == 0x7F] = 0
+    Asf = rng.integers(118, 127, (M, K // 32)).astype(np.uint8)
+    w4 = rng.integers(0, 16, (N, K))
+    wsf = rng.integers(118, 127, (N, K // 32)).astype(np.uint8)
+    w8 = OA.encode_e4m3(F.decode_e2m1(w4))
+    R4, S4 = Q.gemm_w4a8(A, Asf, w4, wsf)
+    R8, S8 = Q.gemm_w8a8(A, Asf, w8, wsf)
+    assert np.array_equal(R4, R8) and np.array_equal(S4, S8)
