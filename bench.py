@@ -263,6 +263,33 @@ def extra_w4a16(steps, warmup, world, only=None):
     return out
 
 
+def extra_w8a8(steps, warmup, world):
+    """W8A8 MX kind (MXFP8 weights x MXFP8 activations) on the headline's larger shape."""
+    import moe_qw_repack_gb300.qw as Q
+    peaks, _ = measured_peaks()
+    M, N, K = 4096, 14336, 4096
+    p = synth.w8a8_problem(M, N, K, cfg_id=7)
+    d = Q.qw_repack_query(Q.QW_W_MXFP8_G32, 1, N, K)
+    wp, sp = Q.empty_packed(d)
+    Q.qw_repack(d, torch.from_numpy(p["w_canon"]).cuda(), torch.from_numpy(p["s_canon"]).cuda(),
+                wp, sp)
+    A, Asf = torch.from_numpy(p["A"]).cuda(), torch.from_numpy(p["A_sf"]).cuda()
+    step_in = d.w_bytes + d.s_bytes + A.numel() + Asf.numel()
+    R = replicas_for(step_in)
+    copies = [(wp, sp, A, Asf)] + [(wp.clone(), sp.clone(), A.clone(), Asf.clone())
+                                   for _ in range(R - 1)]
+    C = torch.empty((M, N), dtype=torch.int16, device="cuda")
+
+    def fn(i):
+        w, s, a, asf = copies[i % R]
+        Q.qgemm_dense(d, w, s, Q.QW_A_MXFP8_G32, a, asf, None, C, M, None, 0)
+    ms, n, _ = time_region([fn], steps, warmup, world)
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    return {"w8a8_mxfp8_4096x14336x4096": {"us": round(ms * 1e3, 1), "tflops": round(tf, 1),
+                                           "frac_fp8_peak": round(tf / (2 * peaks["bf16_tflops"]), 3),
+                                           "input_copies": R, "steps": n}}
+
+
 def extra_moe(steps, warmup, world, only=None):
     """Grouped MoE workloads: W4A8 (E=256, top-8, T=4096, 7168 -> 4096) and the W4A16
     intermediate-640 token sweep (E=128, top-8, up 4096 -> 1280 plus down 640 -> 4096).
@@ -457,6 +484,7 @@ def run_ours(args, world, rank):
     torch.cuda.empty_cache()
     if not args.no_extra:
         line["extra"] = extra_w4a16(max(5, min(args.steps, 200)), 3, world)
+        line["extra"].update(extra_w8a8(max(5, min(args.steps, 100)), 3, world))
         line["extra"].update(extra_moe(max(5, min(args.steps, 40)), 3, world))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

@@ -59,7 +59,8 @@ typedef enum qw_status {
 typedef enum qw_wfmt {
   QW_W_INT4_G128_BF16 = 0, /* symmetric INT4 in [-7,7], BF16 scale per 128 along K      */
   QW_W_INT3_G128_BF16 = 1, /* symmetric INT3 in [-3,3], BF16 scale per 128 along K      */
-  QW_W_MXFP4_G32 = 2       /* E2M1 codes, E8M0 scale per 32 along K                      */
+  QW_W_MXFP4_G32 = 2,      /* E2M1 codes, E8M0 scale per 32 along K                      */
+  QW_W_MXFP8_G32 = 3       /* E4M3 codes, E8M0 scale per 32 along K (the W8A8 MX kind)    */
 } qw_wfmt;
 
 typedef enum qw_afmt {
@@ -108,6 +109,7 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *          s_canon BF16 [E][N][K/128].
  *   MXFP4: w_canon uint8 [E][N][K/2], even k in the low nibble.  s_canon uint8 E8M0
  *          [E][N][K/32].
+ *   MXFP8: w_canon uint8 [E][N][K] E4M3 codes.  s_canon uint8 E8M0 [E][N][K/32].
  * Packed outputs (device, sizes from `desc`, 256-byte aligned):
  *   INT4:  per expert [K/128][N_pad/16] blocks of 1 KiB: 32 lanes x 8 words; word s of
  *          lane l = 4g + t holds the eight weights lane l feeds to the s-th m16n8k16 MMA of
@@ -122,11 +124,13 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *          512-byte chunks per 128 rows x 4 groups, chunk (r/128, g/4) at
  *          ((r/128) * (K_pad/128) + g/4) * 512, byte (r%32)*16 + ((r%128)/32)*4 + g%4;
  *          padding bytes are 127 (scale 1).
+ *   MXFP8: codes uint8 [N_pad][K_pad] (canonical order, zero-padded); scales as MXFP4.
  * The zero-exponent codes: the announcement's section "量子化サポート" states that a
  * symmetric INT without its minimum has the value set of a float with zero exponent
  * bits; the excess code used here is that value set shifted so that its bit pattern
  * drops straight into a BF16 mantissa (one logic op and one subtract per two weights).
- * Device-detected errors: INT4 -8, INT3 -4, E8M0 0xFF -> QW_ERR_VALUE in *d_err (the
+ * Device-detected errors: INT4 -8, INT3 -4, E4M3 NaN (0x7F, 0xFF), E8M0 0xFF ->
+ * QW_ERR_VALUE in *d_err (the
  * offending element is packed as 0).  Alignment: w_canon / s_canon 4-byte aligned
  * (INT) or 1 (MXFP4); w_packed / s_packed 256-byte aligned.
  */

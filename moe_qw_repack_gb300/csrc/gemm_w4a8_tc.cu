@@ -1,5 +1,6 @@
 // gemm_w4a8_tc.cu - large-M W4A8 path: MXFP4 weights x MXFP8 activations on the
-// sm_103a block-scaled tensor cores.
+// sm_103a block-scaled tensor cores (and the W8A8 MX kind: MXFP8 weights, the same kernel
+// with E4M3 as the B type).
 //
 // What it computes (aireiter.com "vLLM Humming performance benchmark", section "H100
 // group-32 W4A8": MXFP4 weights, MXFP8 activations, group-32 scales; spke.com Humming
@@ -42,8 +43,12 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
 constexpr int A_BYTES = BM * BK;  // E4M3, one byte per element
-constexpr int B_BYTES = BN * BK;  // E2M1 unpacked by TMA: 16 codes in 8 bytes + 8 gap bytes
-constexpr int B_TX_BYTES = BN * BK / 2;  // the unpacking load credits the packed global bytes
+// B in shared memory is one byte per element either way: E4M3 codes as they are, or E2M1
+// codes unpacked by TMA (16 codes in 8 bytes + 8 gap bytes)
+constexpr int B_BYTES = BN * BK;
+// bytes a B load credits to the barrier: the packed global bytes
+template <bool W8>
+__host__ __device__ constexpr int b_tx_bytes() { return W8 ? BN * BK : BN * BK / 2; }
 constexpr int SFA_BYTES = 512, SFB_CHUNK = 512, SFB_BYTES = 2 * SFB_CHUNK;
 constexpr int NUM_WARPS = 12, NUM_THREADS = NUM_WARPS * 32;
 constexpr int EPI_WARP0 = 4, NUM_EPI_WARPS = 8;
@@ -54,11 +59,14 @@ constexpr uint32_t SF_COLS_PER_STAGE = 12;  // 4 (A: 128 rows) + 8 (B: 256 rows)
 constexpr size_t SMEM_BYTES = (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) +
                               (size_t)SF_STAGING * SFA_BYTES + 512 + 1024;
 
-// Instruction descriptor, kind::mxf8f6f4: A = E4M3 (0), B = E2M1 (5), both K-major,
-// N >> 3 at bit 17, scale type UE8M0 (bit 23), M >> 4 at bit 24; the B / A scale
+// Instruction descriptor, kind::mxf8f6f4: A = E4M3 (0), B = E2M1 (5) or E4M3 (0), both
+// K-major, N >> 3 at bit 17, scale type UE8M0 (bit 23), M >> 4 at bit 24; the B / A scale
 // factor byte selectors sit at bits 4 and 29.
-constexpr uint32_t IDESC = (0u << 7) | (5u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
-                           ((uint32_t)(BM >> 4) << 24);
+template <bool W8>
+__host__ __device__ constexpr uint32_t idesc() {
+  return (0u << 7) | ((W8 ? 0u : 5u) << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(BM >> 4) << 24);
+}
 
 struct Params {
   int64_t rows;           // activation rows (M, or total grouped rows)
@@ -114,6 +122,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) break;
 }
 
+template <bool W8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a8_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const Params p) {
@@ -184,7 +193,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_TX_BYTES + nchunks * SFB_CHUNK);
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + b_tx_bytes<W8>() + nchunks * SFB_CHUNK);
           tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, (int32_t)x.rb);
           tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK,
                       x.e * p.N_pad + x.n0);
@@ -231,7 +240,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < BK / 32; ++kk) {
             const uint64_t ad = smem_desc(a0 + kk * 32, 16, 1024, 2);
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
-            const uint32_t id = IDESC | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
+            const uint32_t id = idesc<W8>() | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
             tc_mma_mxf8f6f4(tbase, ad, bd, id, sfa_col, sfb_col, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
@@ -418,6 +427,7 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   auto enc = encode_fn();
   if (!enc) return QW_ERR_CUDA;
   if (rs.rows > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
+  const bool w8 = d.wfmt == QW_W_MXFP8_G32;
 
   CUtensorMap tmA, tmB;
   {
@@ -432,10 +442,11 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   }
   {
     cuuint64_t gdim[2] = {(cuuint64_t)d.K_pad, (cuuint64_t)d.E * (cuuint64_t)d.N_pad};
-    cuuint64_t gstr[1] = {(cuuint64_t)(d.K_pad / 2)};
+    cuuint64_t gstr[1] = {(cuuint64_t)(w8 ? d.K_pad : d.K_pad / 2)};
     cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
     cuuint32_t es[2] = {1, 1};
-    if (enc(&tmB, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(w_packed), gdim,
+    if (enc(&tmB, w8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2,
+            const_cast<void*>(w_packed), gdim,
             gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return QW_ERR_ALIGNMENT;
@@ -470,15 +481,21 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_w4a8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(gemm_w4a8_kernel<false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(gemm_w4a8_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return QW_ERR_CUDA;
 
   const int64_t tiles_max = max_m_tiles * p.num_n_tiles;
   const int sms = device_sm_count();
   const unsigned grid = (unsigned)(tiles_max < sms ? (tiles_max < 1 ? 1 : tiles_max) : sms);
-  gemm_w4a8_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+  if (w8)
+    gemm_w4a8_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+  else
+    gemm_w4a8_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 

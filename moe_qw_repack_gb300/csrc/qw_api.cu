@@ -31,6 +31,9 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// block-scaled MX weight formats (E8M0 scale per 32 along K, tcgen05 block-scaled MMA)
+bool is_mx(int32_t wfmt) { return wfmt == QW_W_MXFP4_G32 || wfmt == QW_W_MXFP8_G32; }
+
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 qw_status check_desc(const qw_packed_desc* d) {
@@ -44,7 +47,7 @@ qw_status check_desc(const qw_packed_desc* d) {
 }
 
 qw_status check_afmt(const qw_packed_desc* d, int32_t afmt, const void* A_sf) {
-  if (d->wfmt == QW_W_MXFP4_G32) {
+  if (is_mx(d->wfmt)) {
     if (afmt != QW_A_MXFP8_G32) return QW_ERR_UNSUPPORTED;
     if (!A_sf) return QW_ERR_INVALID_ARG;
   } else {
@@ -96,12 +99,14 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
       d.s_expert_stride = (uint64_t)round_up((int64_t)(K / kIntGroup) * d.N_pad * 2, 256);
       break;
     }
-    case QW_W_MXFP4_G32: {
+    case QW_W_MXFP4_G32:
+    case QW_W_MXFP8_G32: {
       if (K % kMxGroup) return QW_ERR_UNSUPPORTED;
       d.group = kMxGroup;
       d.N_pad = (int32_t)round_up(N, 128);
       d.K_pad = (int32_t)round_up(K, 128);
-      d.w_expert_stride = (uint64_t)d.N_pad * (d.K_pad / 2);
+      d.w_expert_stride =
+          (uint64_t)d.N_pad * (wfmt == QW_W_MXFP4_G32 ? d.K_pad / 2 : d.K_pad);
       d.s_expert_stride = (uint64_t)(d.N_pad / 128) * (d.K_pad / 128) * kSfChunkBytes;
       break;
     }
@@ -120,7 +125,7 @@ qw_status qw_repack(const qw_packed_desc* desc, const void* w_canon, const void*
   qw_status s = check_desc(desc);
   if (s != QW_OK) return s;
   if (!w_canon || !s_canon || !w_packed || !s_packed) return QW_ERR_INVALID_ARG;
-  if (desc->wfmt != QW_W_MXFP4_G32 && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
+  if (!is_mx(desc->wfmt) && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
     return QW_ERR_ALIGNMENT;
   if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
   return launch_repack(*desc, w_canon, s_canon, w_packed, s_packed, d_err,
@@ -132,7 +137,7 @@ qw_status qw_unpack(const qw_packed_desc* desc, const void* w_packed, const void
   qw_status s = check_desc(desc);
   if (s != QW_OK) return s;
   if (!w_canon || !s_canon || !w_packed || !s_packed) return QW_ERR_INVALID_ARG;
-  if (desc->wfmt != QW_W_MXFP4_G32 && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
+  if (!is_mx(desc->wfmt) && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
     return QW_ERR_ALIGNMENT;
   if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
   return launch_unpack(*desc, w_packed, s_packed, w_canon, s_canon, d_err,
@@ -145,7 +150,7 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
   if (s != QW_OK) return s;
   if (!bytes || max_rows < 0) return QW_ERR_INVALID_ARG;
   if ((s = check_afmt(desc, afmt, reinterpret_cast<const void*>(1))) != QW_OK) return s;
-  if (desc->wfmt == QW_W_MXFP4_G32) {
+  if (is_mx(desc->wfmt)) {
     *bytes = gemm_w4a8_workspace(*desc, max_rows);
   } else {
     const uint64_t a = gemv_w4a16_workspace(*desc, max_rows);
@@ -165,7 +170,7 @@ static qw_status check_gemm_args(const qw_packed_desc* desc, const void* w_packe
   if (rows > 0 && (!w_packed || !s_packed || !A || !C)) return QW_ERR_INVALID_ARG;
   if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
   if (!aligned(A, 16) || !aligned(C, 4)) return QW_ERR_ALIGNMENT;
-  if (desc->wfmt == QW_W_MXFP4_G32) {
+  if (is_mx(desc->wfmt)) {
     if (desc->K % 16) return QW_ERR_ALIGNMENT;  // TMA row pitch of the E4M3 activations
     if (!aligned(A_sf, 4)) return QW_ERR_ALIGNMENT;
   } else if (desc->K % 8) {
@@ -185,7 +190,7 @@ qw_status qgemm_dense(const qw_packed_desc* desc, const void* w_packed, const vo
   if (M == 0) return QW_OK;
   RowSet rs{M, nullptr, 1};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (desc->wfmt == QW_W_MXFP4_G32)
+  if (is_mx(desc->wfmt))
     return launch_gemm_w4a8(*desc, w_packed, s_packed, A, A_sf, bias, C, rs, workspace, ws_bytes,
                             d_err, st);
   if (M > kW4A16TensorCoreRows)
@@ -296,7 +301,7 @@ qw_status qgemm_moe_grouped(const qw_packed_desc* desc, const void* w_packed,
   if (!workspace || ws_bytes < need) return QW_ERR_WORKSPACE;
   RowSet rs{total_rows, expert_offsets, desc->E};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (desc->wfmt == QW_W_MXFP4_G32)
+  if (is_mx(desc->wfmt))
     return launch_gemm_w4a8(*desc, w_packed, s_packed, A_sorted, A_sf_sorted, bias, C, rs,
                             workspace, ws_bytes, d_err, st);
   if (total_rows >= kW4A16TensorCoreRows * desc->E)

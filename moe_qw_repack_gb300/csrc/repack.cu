@@ -247,6 +247,49 @@ __global__ void unpack_mxfp4_codes_kernel(const uint8_t* __restrict__ wp, uint8_
   }
 }
 
+// ----------------------------------------------------------------------------- MXFP8
+// codes: canonical [E][N][K] -> packed [E][N_pad][K_pad], 4 bytes per thread; E4M3 NaN
+// codes (0x7F, 0xFF) are value errors and packed as 0
+__global__ void repack_mxfp8_codes_kernel(const uint8_t* __restrict__ wc, uint8_t* __restrict__ wp,
+                                          int32_t E, int32_t N, int32_t N_pad, int32_t K,
+                                          int32_t K_pad, int32_t* err) {
+  const int64_t wpr = K_pad / 4;  // packed words per row
+  const int64_t total = (int64_t)E * N_pad * wpr;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t er = idx / wpr;
+    const int64_t e = er / N_pad;
+    const int64_t n = er % N_pad;
+    const int64_t b0 = (idx % wpr) * 4;
+    uint32_t v = 0;
+    if (n < N) {
+      const uint8_t* src = wc + (e * N + n) * (int64_t)K;
+      for (int j = 0; j < 4; ++j)
+        if (b0 + j < K) {
+          uint32_t c = src[b0 + j];
+          if ((c & 0x7Fu) == 0x7Fu) {
+            set_error(err, QW_ERR_VALUE);
+            c = 0;
+          }
+          v |= c << (8 * j);
+        }
+    }
+    reinterpret_cast<uint32_t*>(wp)[idx] = v;
+  }
+}
+__global__ void unpack_mxfp8_codes_kernel(const uint8_t* __restrict__ wp, uint8_t* __restrict__ wc,
+                                          int32_t E, int32_t N, int32_t N_pad, int32_t K,
+                                          int32_t K_pad) {
+  const int64_t total = (int64_t)E * N * K;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t er = idx / K;
+    const int64_t e = er / N, n = er % N;
+    const int64_t b = idx % K;
+    wc[idx] = wp[(e * N_pad + n) * (int64_t)K_pad + b];
+  }
+}
+
 // Offset of scale (row r, group g) in the 128 x 4 chunked layout of one expert.
 __device__ __forceinline__ int64_t sf_chunk_offset(int64_t r, int g, int K_pad) {
   return ((r / 128) * (K_pad / 128) + g / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + g % 4;
@@ -317,10 +360,17 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
                                                         d.K, err);
       break;
     }
-    case QW_W_MXFP4_G32: {
-      const int64_t tw = (int64_t)d.E * d.N_pad * (d.K_pad / 8);
-      repack_mxfp4_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
-          (const uint8_t*)w_canon, (uint8_t*)w_packed, d.E, d.N, d.N_pad, d.K, d.K_pad);
+    case QW_W_MXFP4_G32:
+    case QW_W_MXFP8_G32: {
+      if (d.wfmt == QW_W_MXFP4_G32) {
+        const int64_t tw = (int64_t)d.E * d.N_pad * (d.K_pad / 8);
+        repack_mxfp4_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
+            (const uint8_t*)w_canon, (uint8_t*)w_packed, d.E, d.N, d.N_pad, d.K, d.K_pad);
+      } else {
+        const int64_t tw = (int64_t)d.E * d.N_pad * (d.K_pad / 4);
+        repack_mxfp8_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
+            (const uint8_t*)w_canon, (uint8_t*)w_packed, d.E, d.N, d.N_pad, d.K, d.K_pad, err);
+      }
       const int64_t ts = (int64_t)d.E * d.N_pad * (d.K_pad / 32);
       repack_mx_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
           (const uint8_t*)s_canon, (uint8_t*)s_packed, d.E, d.N, d.N_pad, d.K, d.K_pad, err);
@@ -329,7 +379,7 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
     default:
       return QW_ERR_UNSUPPORTED;
   }
-  if (d.wfmt != QW_W_MXFP4_G32) {
+  if (d.wfmt != QW_W_MXFP4_G32 && d.wfmt != QW_W_MXFP8_G32) {
     const int64_t ts = (int64_t)d.E * (d.K / 128) * d.N_pad;
     repack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
         (const uint16_t*)s_canon, (uint16_t*)s_packed, d.E, d.N, d.N_pad, d.K / 128);
@@ -356,10 +406,17 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
                                                         d.K);
       break;
     }
-    case QW_W_MXFP4_G32: {
-      const int64_t tw = (int64_t)d.E * d.N * (d.K / 2);
-      unpack_mxfp4_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
-          (const uint8_t*)w_packed, (uint8_t*)w_canon, d.E, d.N, d.N_pad, d.K, d.K_pad);
+    case QW_W_MXFP4_G32:
+    case QW_W_MXFP8_G32: {
+      if (d.wfmt == QW_W_MXFP4_G32) {
+        const int64_t tw = (int64_t)d.E * d.N * (d.K / 2);
+        unpack_mxfp4_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
+            (const uint8_t*)w_packed, (uint8_t*)w_canon, d.E, d.N, d.N_pad, d.K, d.K_pad);
+      } else {
+        const int64_t tw = (int64_t)d.E * d.N * d.K;
+        unpack_mxfp8_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
+            (const uint8_t*)w_packed, (uint8_t*)w_canon, d.E, d.N, d.N_pad, d.K, d.K_pad);
+      }
       const int64_t ts = (int64_t)d.E * d.N * (d.K / 32);
       unpack_mx_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
           (const uint8_t*)s_packed, (uint8_t*)s_canon, d.E, d.N, d.N_pad, d.K, d.K_pad);
@@ -368,7 +425,7 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
     default:
       return QW_ERR_UNSUPPORTED;
   }
-  if (d.wfmt != QW_W_MXFP4_G32) {
+  if (d.wfmt != QW_W_MXFP4_G32 && d.wfmt != QW_W_MXFP8_G32) {
     const int64_t ts = (int64_t)d.E * d.N * (d.K / 128);
     unpack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
         (const uint16_t*)s_packed, (uint16_t*)s_canon, d.E, d.N, d.N_pad, d.K / 128);

@@ -27,6 +27,7 @@ QW_ERR_CUDA = 7
 QW_W_INT4_G128_BF16 = 0
 QW_W_INT3_G128_BF16 = 1
 QW_W_MXFP4_G32 = 2
+QW_W_MXFP8_G32 = 3
 QW_A_BF16 = 0
 QW_A_MXFP8_G32 = 1
 

@@ -207,6 +207,20 @@ def w4a8_problem(M, N, K, *, E=1, cfg_id=1, seed=BASE_SEED, sf_lo=118, sf_hi=126
     return out
 
 
+def w8a8_problem(M, N, K, *, E=1, cfg_id=1, seed=BASE_SEED, sf_lo=118, sf_hi=126,
+                 bias=False):
+    """MXFP8 weights and activations: E4M3 codes of N(0,1) samples with group-32 E8M0
+    scales uniform in [sf_lo, sf_hi]."""
+    w = to_e4m3_codes(normal(stream(cfg_id, 16, seed), (E * N, K))).reshape(E, N, K)
+    w_sf = uniform_int(stream(cfg_id, 17, seed), (E, N, K // 32), sf_lo, sf_hi).astype(np.uint8)
+    a = to_e4m3_codes(normal(stream(cfg_id, 13, seed), (M, K)))
+    a_sf = uniform_int(stream(cfg_id, 14, seed), (M, K // 32), sf_lo, sf_hi).astype(np.uint8)
+    out = dict(A=a, A_sf=a_sf, w_canon=w, s_canon=w_sf, E=E, N=N, K=K, M=M)
+    if bias:
+        out["bias"] = to_bf16_bits(normal(stream(cfg_id, 15, seed), (E, N)))
+    return out
+
+
 def unpack_nibbles_layout(w_canon: np.ndarray) -> np.ndarray:
     """Inverse of :func:`pack_nibbles` (a layout helper for test inputs, no decoding)."""
     lo = w_canon & 0xF
@@ -227,5 +241,5 @@ def router_logits(T, E, *, cfg_id=3, seed=BASE_SEED, bias_std=1.5):
 __all__ = [
     "BASE_SEED", "Stream", "stream", "uniform_int", "uniform", "normal", "random_bytes",
     "to_bf16_bits", "to_e4m3_codes", "pack_int4", "pack_int3", "pack_nibbles",
-    "unpack_nibbles_layout", "w4a16_problem", "w4a8_problem", "router_logits",
+    "unpack_nibbles_layout", "w4a16_problem", "w4a8_problem", "w8a8_problem", "router_logits",
 ]

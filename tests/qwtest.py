@@ -57,10 +57,10 @@ def dense_w4a16(prob, bias=None, M=None):
     return u16_view(C)
 
 
-def dense_w4a8(prob, bias=None):
+def dense_w4a8(prob, bias=None, wfmt=None):
     Q = qw()
-    d, wp, sp = repack(Q.QW_W_MXFP4_G32, 1, prob["N"], prob["K"], prob["w_canon"],
-                       prob["s_canon"])
+    wfmt = Q.QW_W_MXFP4_G32 if wfmt is None else wfmt
+    d, wp, sp = repack(wfmt, 1, prob["N"], prob["K"], prob["w_canon"], prob["s_canon"])
     A = dev(prob["A"])
     Asf = dev(prob["A_sf"])
     M = prob["A"].shape[0]
