@@ -143,6 +143,13 @@ __device__ __forceinline__ uint32_t bf16x2_sub_u32(uint32_t x, uint32_t y) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// acc (an FP32 pair, low = first) += s2 * (x0, x1): one packed two-wide FMA
+__device__ __forceinline__ void fma2_acc(uint64_t& acc, uint64_t s2, uint32_t x0, uint32_t x1) {
+  asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%2, %3};\n\tfma.rn.f32x2 %0, %1, t, %0;\n\t}"
+      : "+l"(acc)
+      : "l"(s2), "r"(x0), "r"(x1));
+}
+
 // (a & b) | c in one logic instruction (written out so the compiler cannot split it)
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -376,12 +383,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int n = x.nt * BW + 32 * q + lane;
       const bool nvalid = n < p.N;
       const uint16_t* srow = p.sp16 + x.e * p.s_estride_elems + (nvalid ? n : 0);
-      float acc[64];
+      uint64_t acc2[32];  // FP32 pairs (tokens 2i, 2i + 1), promoted with packed FMAs
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+      for (int i = 0; i < 32; ++i) acc2[i] = 0ull;
       uint32_t s_next = __ldg(srow);
       for (int g = 0; g < G; ++g, ++gi) {
-        const float sc = __uint_as_float(s_next << 16);
+        const uint32_t scb = s_next << 16;  // the group scale as FP32 bits
+        const uint64_t sc2 = ((uint64_t)scb << 32) | scb;
         if (g + 1 < G) s_next = __ldg(srow + (int64_t)(g + 1) * p.N_pad);
         const int ab = (int)(gi & 1);
         const uint32_t use = (uint32_t)(gi >> 1) & 1u;
@@ -397,13 +405,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_ld_32x32b_x32(ta + 32 * hh, v);
           tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[32 * hh + i] = fmaf(sc, __uint_as_float(v[i]), acc[32 * hh + i]);
+          for (int i = 0; i < 16; ++i) fma2_acc(acc2[16 * hh + i], sc2, v[2 * i], v[2 * i + 1]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[ab]);
       }
       if (!ok) break;
+      float acc[64];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        acc[2 * i] = __uint_as_float((uint32_t)acc2[i]);
+        acc[2 * i + 1] = __uint_as_float((uint32_t)(acc2[i] >> 32));
+      }
       const float bias =
           (p.bias && nvalid) ? __uint_as_float((uint32_t)__ldg(p.bias + (int64_t)x.e * p.N + n) << 16)
                              : 0.f;
