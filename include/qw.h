@@ -23,7 +23,13 @@
  *     says "host".  The library never allocates, never synchronises the stream (except
  *     qw_read_error, which exists to do so) and never exits or asserts.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  All
- *     device work of a call is enqueued on it, in order.
+ *     device work of a call is enqueued on it, in order.  The W4A16 GEMV kernels (M <= 16,
+ *     and grouped calls below the tensor-core switch) are launched as programmatic
+ *     dependents of the previous kernel on the stream: they may start reading w_packed and
+ *     s_packed while that kernel finishes, and wait for it before anything else.  So the
+ *     weights of such a call must not be written by the kernel enqueued immediately before
+ *     it (qw_repack followed at once by a GEMV is fine: qw_repack's kernels do not release
+ *     their dependents early, so the GEMV starts after they complete).
  *   - Shape, pointer-alignment and size errors are detected on the host before any
  *     launch and returned as a qw_status; nothing is enqueued in that case.
  *   - Value errors found on the device (an INT4 code -8, an INT3 code -4, an E8M0 scale

@@ -1,7 +1,10 @@
 // gemv_w4a16.cu - small-M W4A16 path: the packed weights stream once from HBM, are
-// dequantized in registers and multiplied on the tensor cores.  Two kernels share the
-// decode and MMA code: a register-ring kernel for dense calls and a TMA-ring kernel for
-// grouped (MoE) calls.
+// dequantized in registers and multiplied on the tensor cores.  Three kernels share the
+// decode and MMA code: a staged-activation kernel for single-token decode over large
+// matrices, a register-ring kernel for the other dense calls and a TMA-ring kernel for
+// grouped (MoE) calls.  All three are launched as programmatic dependents of the previous
+// kernel on the stream (griddepcontrol): back-to-back GEMVs overlap one launch's ramp-up
+// with the previous one's tail, and only weights are read before the wait.
 //
 // What it computes (spke.com Humming announcement, "WnA16"; "フォーマットとアーキテクチャ
 // を横断して共有されるCUDAコンポーネント": dequantization and scaling inside the kernel,
@@ -19,6 +22,10 @@
 //     walk their (item, batch of 4 groups) sequence with the next batch's packed words
 //     already loading into a register ring (16-byte loads of the lane's own fragment
 //     words), refilled across item boundaries.
+//   - Single-token decode (gemv_m8_kernel): as the register ring, plus activations staged
+//     in shared memory in B-fragment order and per-group activation sums, which replace the
+//     all-ones MMA below (fewer issued instructions per weight: the decode GEMV is bound by
+//     issue slots as much as by HBM).
 //   - Grouped (gemv_tma_kernel): one producer thread per CTA
 //     streams an item's groups
 //     eight at a time: a 4-D tensor map views the packed weights as [expert][group][16-row
@@ -159,6 +166,34 @@ struct Geo {
 
 // groups per batch = register ring depth (token rows cost registers)
 __host__ __device__ constexpr int batch_groups(int mch) { return mch >= 4 ? 2 : 4; }
+// Programmatic dependent launch: the next kernel on the stream may start once every CTA of
+// this one has run this (its CTAs then fill SMs as this kernel's CTAs retire) ...
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and waits here until the previous kernel has finished and its writes are visible.
+// Only the packed weights and scales are read before this point.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch as a programmatic dependent of the previous kernel on the stream: the kernel may
+// start streaming weights while that kernel drains; it executes griddepcontrol.wait before
+// it touches anything the previous kernel may have written.
+template <class Kern, class... Args>
+qw_status launch_pdl(Kern kern, unsigned grid, unsigned threads, size_t smem, cudaStream_t st,
+                     const Args&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return QW_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
 
 struct Params {
   const uint8_t* wp;
@@ -281,6 +316,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
       rsc += p.N_pad;
     }
   };
+  pdl_launch_dependents();
   {
     const BatchPtr b0 = batch_ptr<BITS, MCH, NB>(p, 0, total, nbat, g0, cnt, nblocks, g);
     rw = b0.w;
@@ -289,6 +325,8 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
 #pragma unroll
     for (int j = 0; j < NB; ++j) refill(j);
   }
+  // activations, bias and the output belong to the stream's order from here on
+  pdl_wait();
 
   uint32_t qb = 0;
   for (uint32_t it = 0; it < my_items; ++it) {
@@ -438,18 +476,243 @@ qw_status launch_reg_variant(const Params& p, int64_t size_items, cudaStream_t s
   int64_t grid = (int64_t)device_sm_count() * per_sm;
   if (grid > size_items) grid = size_items;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kWarps * 32, smem, st>>>(p);
-  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+  return launch_pdl(kern, (unsigned)grid, kWarps * 32, smem, st, p);
 }
 
 
-// ---------------------------------------------------------------- TMA-ring kernel (grouped)
-constexpr int kConsumers = 4;
-constexpr int kTmaThreads = (kConsumers + 1) * 32;
-constexpr int kStageGroups = 8;  // scale groups per stage (one TMA copy)
-constexpr int kStages = 4;
+// ---------------------------------------------------------------- dense kernel, M <= 8
+// One token tile of at most 8 rows.  After griddepcontrol.wait the CTA stages the
+// activations once, in the order the MMA's B fragments read them ([group][step pair][row][t]
+// 16-byte chunks: one conflict-free 16-byte shared load feeds two MMA steps), together with
+// every row's sum over every scale group.  With those sums known the biased codes need no
+// all-ones MMA: the group sum is P - (128 + excess) * sum(a), one MMA per step.  The weights
+// stream through each warp's register ring as in gemv_reg_kernel; batch pointers advance
+// incrementally (no division per batch).  Items are 16-row blocks; the CTA's warps split
+// the scale groups and meet in a double-buffered shared reduction (one barrier per item).
+constexpr int kM8Warps = 8;
+constexpr int kM8Ring = 4;  // groups per batch = register ring depth
+// largest shared-memory footprint sent to the kernel: two CTAs per SM still fit
+constexpr size_t kM8MaxSmem = 96 * 1024;
+// smallest matrix (N x K weights) sent to it
+constexpr int64_t kM8MinWeights = int64_t(1) << 25;
 
-__host__ __device__ constexpr int tma_ctas_per_sm(int mch) { return mch >= 4 ? 2 : 4; }
+struct M8Params {
+  const uint8_t* wp;
+  const uint16_t* sp;
+  const uint16_t* A;
+  const uint16_t* bias;
+  uint16_t* C;
+  int32_t N, N_pad, K, M;  // M <= 8
+  int32_t gpw;             // scale groups per warp
+};
+
+__host__ __device__ constexpr size_t m8_act_bytes(int K, int M) {
+  return (size_t)(K / 128) * 4 * M * 64;
+}
+constexpr size_t m8_smem_bytes(int K, int M) {
+  return m8_act_bytes(K, M) + (size_t)(K / 128) * 8 * 4 + 2 * kM8Warps * 4 * 32 * 4;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Params p) {
+  using GE = Geo<BITS>;
+  constexpr int WPG = GE::WPG;
+  constexpr int R = kM8Ring;
+  extern __shared__ uint4 m8_smem[];
+  const int G = p.K >> 7;
+  uint8_t* act = reinterpret_cast<uint8_t*>(m8_smem);
+  float* gsum = reinterpret_cast<float*>(act + m8_act_bytes(p.K, p.M));  // [G][8 tokens]
+  float* red = gsum + G * 8;                                               // [2][warp][4][32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t nblocks = (uint32_t)(p.N_pad >> 4);
+  const int g0 = min(G, warp * p.gpw);
+  const int cnt = min(G, g0 + p.gpw) - g0;  // this warp's groups per item (may be 0)
+  const int nbat = (cnt + R - 1) / R;
+  const int64_t gstride = (int64_t)nblocks * GE::BLK;  // bytes between groups of a block
+  const uint32_t my_items =
+      blockIdx.x < nblocks ? (nblocks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  pdl_launch_dependents();
+
+  // register ring and the running pointers of the batch that refills it
+  uint32_t wb[R][WPG];
+  uint32_t sc[R];
+  const uint8_t* rw = nullptr;
+  const uint16_t* rs = nullptr;
+  int rng = 0;                    // groups in the refilling batch
+  uint32_t nx_it = 0;             // (item, chunk) of the refilling batch
+  int nx_c = 0;
+  auto point = [&](uint32_t it, int c) {
+    rng = 0;
+    if (it < my_items && c < nbat) {
+      const uint32_t nb = blockIdx.x + it * gridDim.x;
+      const int gb = g0 + R * c;
+      rw = p.wp + ((int64_t)gb * nblocks + nb) * GE::BLK;
+      rs = p.sp + (int64_t)gb * p.N_pad + nb * 16 + g;
+      rng = min(R, g0 + cnt - gb);
+    }
+  };
+  auto advance = [&]() {
+    if (++nx_c == nbat) {
+      nx_c = 0;
+      ++nx_it;
+    }
+    point(nx_it, nx_c);
+  };
+  auto refill = [&](int j) {
+    if (j < rng) {
+      load_words<BITS>(rw + j * gstride, lane, wb[j]);
+      const uint16_t* q = rs + (int64_t)j * p.N_pad;
+      sc[j] = __byte_perm(__ldg(q), __ldg(q + 8), 0x5410);
+    }
+  };
+  point(0, 0);
+#pragma unroll
+  for (int j = 0; j < R; ++j) refill(j);
+  advance();
+
+  // ---- activations and group sums (the previous kernel's output may be A).  Each warp
+  // stages the chunks of its own groups (all loads first), so it only waits for itself.
+  pdl_wait();
+  {
+    const int per_row = cnt * 16;      // 16-byte chunks of one row in this warp's groups
+    const int nchunk = p.M * per_row;  // a multiple of 16
+    for (int b0 = 0; b0 < nchunk; b0 += 32 * 8) {
+      uint4 v[8];
+      int rowv[8], k0v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int q = b0 + 32 * u + lane;
+        const int row = q / per_row;
+        const int k0 = g0 * 128 + (q - row * per_row) * 8;
+        rowv[u] = row;
+        k0v[u] = k0;
+        v[u] = q < nchunk ? __ldg(reinterpret_cast<const uint4*>(p.A + (int64_t)row * p.K + k0))
+                          : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int q = b0 + 32 * u + lane;
+        if (b0 + 32 * u >= nchunk) break;  // warp-uniform
+        const int row = rowv[u], k0 = k0v[u];
+        const int gg = k0 >> 7, st = (k0 >> 4) & 7, tt = (k0 >> 2) & 3;
+        if (q < nchunk) {
+          uint8_t* dst = act + ((gg * 4 + (st >> 1)) * p.M + row) * 64 + tt * 16 + (st & 1) * 8;
+          *reinterpret_cast<uint2*>(dst) = make_uint2(v[u].x, v[u].y);
+          *reinterpret_cast<uint2*>(dst + 16) = make_uint2(v[u].z, v[u].w);
+        }
+        const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        float sum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          sum += __uint_as_float(w4[h] << 16) + __uint_as_float(w4[h] & 0xFFFF0000u);
+        // the 16 chunks of one (row, group) sit in 16 consecutive lanes
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        if (q < nchunk && (lane & 15) == 0) gsum[gg * 8 + row] = sum;
+      }
+    }
+    for (int i = lane; i < cnt * 8; i += 32)
+      if ((i & 7) >= p.M) gsum[g0 * 8 + i] = 0.f;  // token columns past M (never stored)
+  }
+  __syncwarp();
+
+  const uint32_t act_lane = smem_u32(act) + (uint32_t)(((g < p.M ? g : 0) * 4 + t) * 16);
+  const uint32_t jj_stride = (uint32_t)p.M * 64;  // bytes between step pairs
+  const uint32_t gsum_lane = smem_u32(gsum) + (uint32_t)(2 * t * 4);
+  for (uint32_t it = 0; it < my_items; ++it) {
+    const uint32_t nb = blockIdx.x + it * gridDim.x;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < nbat; ++c) {
+      const int gb = g0 + R * c;
+      const int ng = min(R, g0 + cnt - gb);
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        if (j < ng) {
+          if (j > 0) refill(j - 1);  // slot j - 1 is free: next batch's group j - 1
+          const int gg = gb + j;
+          const uint32_t ab = act_lane + (uint32_t)gg * 4 * jj_stride;
+          float pr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint4 x = lds128(ab + jj * jj_stride);
+            uint32_t a[4];
+            biased_all<BITS>(wb[j], 2 * jj, a);
+            mma_bf16_16816(pr, a, x.x, x.y);
+            biased_all<BITS>(wb[j], 2 * jj + 1, a);
+            mma_bf16_16816(pr, a, x.z, x.w);
+          }
+          const uint2 sm2 = lds64(gsum_lane + (uint32_t)gg * 32);
+          const float sm0 = __uint_as_float(sm2.x), sm1 = __uint_as_float(sm2.y);
+          const float s_lo = __uint_as_float(sc[j] << 16);
+          const float s_hi = __uint_as_float(sc[j] & 0xFFFF0000u);
+          acc[0] = fmaf(s_lo, fmaf(-GE::BIAS, sm0, pr[0]), acc[0]);
+          acc[1] = fmaf(s_lo, fmaf(-GE::BIAS, sm1, pr[1]), acc[1]);
+          acc[2] = fmaf(s_hi, fmaf(-GE::BIAS, sm0, pr[2]), acc[2]);
+          acc[3] = fmaf(s_hi, fmaf(-GE::BIAS, sm1, pr[3]), acc[3]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < R; ++j)
+        if (j >= ng - 1) refill(j);  // slots not refilled inside the loop
+      advance();
+    }
+
+    // split-K reduction over the CTA's warps, fixed order; one barrier per item
+    float* rb = red + (it & 1) * (kM8Warps * 128);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rb[(warp * 4 + i) * 32 + lane] = acc[i];
+    __syncthreads();
+    for (int o = threadIdx.x; o < 16 * p.M; o += kM8Warps * 32) {
+      const int nl = o & 15, m = o >> 4;
+      const int l = (nl & 7) * 4 + (m >> 1), i = (nl >> 3) * 2 + (m & 1);
+      float v = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kM8Warps; ++w2) v += rb[(w2 * 4 + i) * 32 + l];
+      const int n = (int)nb * 16 + nl;
+      if (n < p.N) {
+        if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + n) << 16);
+        __nv_bfloat16 h = __float2bfloat16_rn(v);
+        p.C[(int64_t)m * p.N + n] = *reinterpret_cast<uint16_t*>(&h);
+      }
+    }
+  }
+}
+
+template <int BITS>
+qw_status launch_m8_variant(const M8Params& p, cudaStream_t st) {
+  auto kern = gemv_m8_kernel<BITS>;
+  const size_t smem = m8_smem_bytes(p.K, p.M);
+  // one attribute call sized for the largest staging this kernel is sent (see the dispatch)
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kM8MaxSmem);
+  if (attr != cudaSuccess) return QW_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kM8Warps * 32, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t items = p.N_pad / 16;
+  int64_t grid = (int64_t)device_sm_count() * per_sm;
+  if (grid > items) grid = items;
+  if (grid < 1) grid = 1;
+  return launch_pdl(kern, (unsigned)grid, kM8Warps * 32, smem, st, p);
+}
+
+// ---------------------------------------------------------------- TMA-ring kernel
+constexpr int kStageGroups = 8;  // scale groups per stage (one TMA copy)
+
+// Shape of a TMA-ring launch: consumer warps, ring stages, resident CTAs per SM.
+template <int CONS_, int STAGES_, int CTAS_>
+struct Ring {
+  static constexpr int CONS = CONS_, STAGES = STAGES_, CTAS = CTAS_;
+  static constexpr int THREADS = (CONS + 1) * 32;
+  static constexpr int GPC = kStageGroups / CONS;  // groups of a stage per consumer
+  static_assert(kStageGroups % CONS == 0, "consumers split a stage evenly");
+};
+// grouped (MoE) calls: many short items, several CTAs per SM
+using GroupedRing = Ring<4, 4, 4>;
 
 template <int BITS>
 struct TmaGeo {
@@ -460,10 +723,10 @@ struct TmaGeo {
   static constexpr float BIAS = BITS == 4 ? 136.f : 132.f;  // 128 + excess
 };
 
-template <int BITS, int MCH>
+template <int BITS, int MCH, class R>
 constexpr size_t tma_smem_bytes() {
-  return 128 + (size_t)kStages * TmaGeo<BITS>::STAGE + 2 * 8 * kStages +
-         (size_t)kConsumers * MCH * 128 * 4 + 16;
+  return 128 + (size_t)R::STAGES * TmaGeo<BITS>::STAGE + 2 * 8 * R::STAGES +
+         (size_t)R::CONS * MCH * 128 * 4 + 16;
 }
 
 struct TmaParams {
@@ -493,24 +756,25 @@ __device__ __forceinline__ void tma_item_of(const TmaParams& p, uint32_t item, u
   }
 }
 
-template <int BITS, int MCH>
-__global__ void __launch_bounds__(kTmaThreads, tma_ctas_per_sm(MCH))
+template <int BITS, int MCH, class R>
+__global__ void __launch_bounds__(R::THREADS, R::CTAS)
     gemv_tma_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmS, const TmaParams p) {
   using GE = TmaGeo<BITS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
-  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kStages * GE::STAGE);
-  uint64_t* empty = full + kStages;
-  float* red = reinterpret_cast<float*>(empty + kStages);  // [consumer][MCH][4][32]
-  volatile int* flags = reinterpret_cast<volatile int*>(red + kConsumers * MCH * 128);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + R::STAGES * GE::STAGE);
+  uint64_t* empty = full + R::STAGES;
+  float* red = reinterpret_cast<float*>(empty + R::STAGES);  // [consumer][MCH][4][32]
+  volatile int* flags = reinterpret_cast<volatile int*>(red + R::CONS * MCH * 128);
   // flags[0]: abort; flags[1]: abort as seen at the end of the current item
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < R::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers);
+      mbar_init(&empty[s], R::CONS);
     }
     flags[0] = 0;
     flags[1] = 0;
@@ -531,6 +795,8 @@ __global__ void __launch_bounds__(kTmaThreads, tma_ctas_per_sm(MCH))
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       tma_prefetch_desc(&tmS);
+      // dense calls stream weights at once; the tile queue is the previous kernel's output
+      if (p.queue) pdl_wait();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_phase = 0;  // per stage: used, phase of its last copy
@@ -550,14 +816,14 @@ __global__ void __launch_bounds__(kTmaThreads, tma_ctas_per_sm(MCH))
           tma_load_3d(dst + GE::W_STAGE, &tmS, &full[stage], nb * 16, c * kStageGroups, e);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
+          if (++stage == R::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       // let every copy issued here land before the CTA's shared memory goes away
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < R::STAGES; ++s)
         if (issued & (1u << s)) {
           const uint64_t t0 = globaltimer_ns();
           while (!mbar_try_wait(&full[s], (issued_phase >> s) & 1u))
@@ -568,6 +834,7 @@ __global__ void __launch_bounds__(kTmaThreads, tma_ctas_per_sm(MCH))
     // ------------------------------------------------------------ consumers
     const int cw = warp - 1;
     const int g = lane >> 2, t = lane & 3;
+    pdl_wait();  // activations, queue, bias and output
     const uint32_t ring_base = smem_u32(ring);
     int stage = 0;
     uint32_t phase = 0;
@@ -596,8 +863,8 @@ __global__ void __launch_bounds__(kTmaThreads, tma_ctas_per_sm(MCH))
         if (ok) {
           const uint32_t sbase = ring_base + stage * GE::STAGE;
 #pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            const int j = 2 * cw + jj;  // group within the stage
+          for (int jj = 0; jj < R::GPC; ++jj) {
+            const int j = R::GPC * cw + jj;  // group within the stage
             const int gg = ch * kStageGroups + j;
             if (gg < G) {
               const uint32_t blk = sbase + j * GE::BLK;
@@ -674,7 +941,7 @@ __global__ void __launch_bounds__(kTmaThreads, tma_ctas_per_sm(MCH))
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[stage]);  // this warp is done with the stage
         }
-        if (++stage == kStages) {
+        if (++stage == R::STAGES) {
           stage = 0;
           phase ^= 1u;
         }
@@ -685,12 +952,12 @@ __global__ void __launch_bounds__(kTmaThreads, tma_ctas_per_sm(MCH))
       for (int c = 0; c < MCH; ++c)
 #pragma unroll
         for (int i = 0; i < 4; ++i) red[((cw * MCH + c) * 4 + i) * 32 + lane] = acc[c][i];
-      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");  // consumers only
+      asm volatile("bar.sync 1, %0;" ::"r"(R::CONS * 32) : "memory");  // consumers only
       if (threadIdx.x == 32) flags[1] = *abort_flag;
-      for (int o = threadIdx.x - 32; o < MCH * 128; o += kConsumers * 32) {
+      for (int o = threadIdx.x - 32; o < MCH * 128; o += R::CONS * 32) {
         float v = 0.f;
 #pragma unroll
-        for (int w2 = 0; w2 < kConsumers; ++w2) v += red[w2 * MCH * 128 + o];
+        for (int w2 = 0; w2 < R::CONS; ++w2) v += red[w2 * MCH * 128 + o];
         // fragment (lane l, register i) -> weight row gq + 8 (i >> 1), token 2 tt + (i & 1)
         const int c = o >> 7, i = (o >> 5) & 3, l = o & 31;
         const int gq = l >> 2, tt = l & 3;
@@ -702,7 +969,7 @@ __global__ void __launch_bounds__(kTmaThreads, tma_ctas_per_sm(MCH))
           p.C[r * p.N + n] = *reinterpret_cast<uint16_t*>(&h);
         }
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(R::CONS * 32) : "memory");
       if (flags[1]) break;  // one snapshot for all consumers: they stop together
     }
   }
@@ -723,24 +990,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BITS, int MCH>
+template <int BITS, int MCH, class R>
 qw_status launch_tma_variant(const CUtensorMap& tmW, const CUtensorMap& tmS, const TmaParams& p,
                          int64_t size_items, cudaStream_t st) {
-  auto kern = gemv_tma_kernel<BITS, MCH>;
-  const size_t smem = tma_smem_bytes<BITS, MCH>();
+  auto kern = gemv_tma_kernel<BITS, MCH, R>;
+  const size_t smem = tma_smem_bytes<BITS, MCH, R>();
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return QW_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTmaThreads, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, R::THREADS, smem) !=
           cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   int64_t grid = (int64_t)device_sm_count() * per_sm;
   if (grid > size_items) grid = size_items;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(tmW, tmS, p);
-  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+  return launch_pdl(kern, (unsigned)grid, R::THREADS, smem, st, tmW, tmS, p);
 }
 
 // Token rows per item / 8: the dispatcher sends dense calls of at most 16 rows and grouped
@@ -752,7 +1018,25 @@ int mch_for(const qw_packed_desc& d, int64_t rows, bool grouped) {
   return mch_for_rows((rows + d.E - 1) / d.E);  // average rows per expert
 }
 
-// Dense calls with up to 16 token rows: the register-ring kernel.
+// Dense calls of at most 8 token rows whose activations fit the staging buffer.
+qw_status launch_dense_m8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                          const void* A, const void* bias, void* C, int M, cudaStream_t st) {
+  const int G = d.K / kIntGroup;
+  M8Params p{};
+  p.wp = static_cast<const uint8_t*>(w_packed);
+  p.sp = static_cast<const uint16_t*>(s_packed);
+  p.A = static_cast<const uint16_t*>(A);
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.C = static_cast<uint16_t*>(C);
+  p.N = d.N;
+  p.N_pad = d.N_pad;
+  p.K = d.K;
+  p.M = M;
+  p.gpw = (G + kM8Warps - 1) / kM8Warps;
+  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_m8_variant<4>(p, st) : launch_m8_variant<3>(p, st);
+}
+
+// Other dense calls with up to 16 token rows: the register-ring kernel.
 qw_status launch_dense_reg(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
                            const void* A, const void* bias, void* C, int64_t M, int mch,
                            cudaStream_t st) {
@@ -791,7 +1075,12 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
                             void* ws, uint64_t ws_bytes, int32_t* err, cudaStream_t st) {
   const bool grouped = rs.offsets != nullptr;
   const int mch = mch_for(d, rs.rows, grouped);
-  if (!grouped && mch <= 2)
+  // single-token decode over a large matrix: the staged kernel (its staging pays off once a
+  // warp streams many groups; measured slower on matrices of 16 M weights and below)
+  if (!grouped && rs.rows == 1 && (int64_t)d.N * d.K >= kM8MinWeights &&
+      (reinterpret_cast<uintptr_t>(A) & 15) == 0 && m8_smem_bytes(d.K, 1) <= kM8MaxSmem)
+    return launch_dense_m8(d, w_packed, s_packed, A, bias, C, 1, st);
+  if (!grouped)
     return launch_dense_reg(d, w_packed, s_packed, A, bias, C, rs.rows, mch, st);
   // Grouped calls (over the device tile queue), and dense calls the dispatcher sends here
   // with more rows: the TMA ring.
@@ -855,10 +1144,10 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   }
   if (max_items > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
   if (mch == 1)
-    return int4 ? launch_tma_variant<4, 1>(tmW, tmS, p, size_items, st)
-                : launch_tma_variant<3, 1>(tmW, tmS, p, size_items, st);
-  return int4 ? launch_tma_variant<4, 2>(tmW, tmS, p, size_items, st)
-              : launch_tma_variant<3, 2>(tmW, tmS, p, size_items, st);
+    return int4 ? launch_tma_variant<4, 1, GroupedRing>(tmW, tmS, p, size_items, st)
+                : launch_tma_variant<3, 1, GroupedRing>(tmW, tmS, p, size_items, st);
+  return int4 ? launch_tma_variant<4, 2, GroupedRing>(tmW, tmS, p, size_items, st)
+              : launch_tma_variant<3, 2, GroupedRing>(tmW, tmS, p, size_items, st);
 }
 
 }  // namespace qw

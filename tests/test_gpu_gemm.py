@@ -57,6 +57,19 @@ def test_config3_m1_decode_full(bits, N, K):
     assert_parity(C, R, S, f"config 3 W{bits} {N}x{K}")
 
 
+@pytest.mark.parametrize("bits", [4, 3])
+def test_m1_staged_kernel_ragged_n_odd_groups_bias(bits):
+    """Single-token decode over a matrix large enough for the staged-activation kernel, with
+    N not a multiple of 16, an odd group count (33: the last warp of a CTA gets no group) and
+    a bias."""
+    N, K = 8200, 4224
+    p = synth.w4a16_problem(1, N, K, bits=bits, cfg_id=121, bias=True)
+    C = dense_w4a16(p, bias=p["bias"][0])
+    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, bits,
+                                   bias_bits=p["bias"][0])
+    assert_parity(C, R, S, f"M=1 W{bits} {N}x{K} bias")
+
+
 # ----------------------------------------------------------------------------- W4A8
 def test_w4a8_single_tile_integer_exact():
     """All scales 2^0 and small integer codes: one 128 x 256 x 128 tile must be exact."""
