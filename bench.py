@@ -263,6 +263,38 @@ def extra_w4a16(steps, warmup, world, only=None):
     return out
 
 
+def extra_w4a8_decode(steps, warmup, world):
+    """Single-token W4A8 (MXFP4 weights x MXFP8 activations) decode on the M=1 decode
+    shapes: device time per GEMM (CUDA graph of back-to-back launches over weight copies
+    that do not fit L2), weight GB/s (E2M1 codes + E8M0 scales)."""
+    import moe_qw_repack_gb300.qw as Q
+    out = {}
+    peaks, _ = measured_peaks()
+    for (N, K) in [(14336, 4096), (4096, 14336), (4096, 4096)]:
+        p = synth.w4a8_problem(1, N, K, cfg_id=260)
+        d = Q.qw_repack_query(Q.QW_W_MXFP4_G32, 1, N, K)
+        wp, sp = Q.empty_packed(d)
+        Q.qw_repack(d, torch.from_numpy(p["w_canon"]).cuda(), torch.from_numpy(p["s_canon"]).cuda(),
+                    wp, sp)
+        wbytes = N * K // 2 + N * K // 32
+        R = replicas_for(wp.numel() + sp.numel())
+        copies = [(wp, sp)] + [(wp.clone(), sp.clone()) for _ in range(R - 1)]
+        A, Asf = torch.from_numpy(p["A"]).cuda(), torch.from_numpy(p["A_sf"]).cuda()
+        C = torch.empty((1, N), dtype=torch.int16, device="cuda")
+
+        def fn(i, copies=copies, d=d, A=A, Asf=Asf, C=C):
+            w, s = copies[i % len(copies)]
+            Q.qgemm_dense(d, w, s, Q.QW_A_MXFP8_G32, A, Asf, None, C, 1, None, 0)
+        ms, n, graph = time_region([fn], max(steps, R), warmup, world, graph_steps=R)
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        out[f"w4a8_m1_{N}x{K}"] = {"us": round(ms * 1e3, 2), "weight_GBps": round(gbs, 1),
+                                   "hbm_frac": round(gbs / peaks["hbm_gbs"], 3),
+                                   "launches": n, "weight_copies": R, "graph": graph}
+        del copies
+        torch.cuda.empty_cache()
+    return out
+
+
 def extra_w8a8(steps, warmup, world):
     """W8A8 MX kind (MXFP8 weights x MXFP8 activations) on the headline's larger shape."""
     import moe_qw_repack_gb300.qw as Q
@@ -485,6 +517,7 @@ def run_ours(args, world, rank):
     if not args.no_extra:
         line["extra"] = extra_w4a16(max(5, min(args.steps, 200)), 3, world)
         line["extra"].update(extra_w8a8(max(5, min(args.steps, 100)), 3, world))
+        line["extra"].update(extra_w4a8_decode(max(5, min(args.steps, 200)), 3, world))
         line["extra"].update(extra_moe(max(5, min(args.steps, 40)), 3, world))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

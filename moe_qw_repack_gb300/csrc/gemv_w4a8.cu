@@ -1,0 +1,271 @@
+// gemv_w4a8.cu - small-M W4A8 path: MXFP4 weights (E2M1 codes, E8M0 scale per 32 along K)
+// times MXFP8 activations (E4M3 codes, E8M0 scale per 32) for at most 8 token rows.
+//
+// What it computes (spke.com Humming announcement, "W8A8 / W4A8 / W4A4": MX formats with
+// group-32 E8M0 scales on both operands; OCP Microscaling v1.0 defines the element values):
+//     C[m][n] = bf16( sum_g 2^(sa[m][g] - 127) 2^(sw[n][g] - 127)
+//                           sum_{k in g} e4m3(a[m][k]) e2m1(w[n][k])  + bias[n] )
+// At a handful of token rows the block-scaled tensor-core GEMM leaves most of its 128-row
+// tile empty and streams every weight tile from few SMs; this path streams the packed
+// weights once across all SMs instead (HBM-bound, like the W4A16 GEMV).
+//
+// Decode: every E2M1 and E4M3 value is exact in FP16 (E4M3 spans 2^-9 .. 448), so one
+// hardware conversion per pair (cvt.rn.f16x2.e2m1x2 / .e4m3x2) feeds a synchronous FP16
+// MMA with FP32 accumulation: the products are exact and each group's sum is one FP32
+// accumulation; the two group scales multiply it in FP32.
+//
+// Layout: the packed weights are the block-scaled GEMM's (row-major codes, N padded to 128
+// rows and K to 128), so one repack serves both paths.  A scale group of 32 k is two MMA
+// steps; lane (g, t) of a warp takes k = 8t .. 8t + 7 of the group (4 code bytes) for
+// weight rows g and g + 8, and the same k of token row g for the B fragment - any fixed
+// assignment of k to MMA slots gives the same sum, as long as both operands use it.
+// Work item = 16 weight rows over all of K; the 8 warps of a CTA split the groups and meet
+// in shared memory (fixed-order sum).  Each warp keeps the next 16 groups' code words in a
+// register ring (4 KiB per warp in flight).  Launched as a programmatic dependent: only
+// weights and their scales are read before griddepcontrol.wait.
+#include "qw_common.cuh"
+#include "qw_internal.h"
+
+namespace qw {
+namespace {
+
+constexpr int kW8Warps = 8;
+constexpr int kW8Ring = 16;  // scale groups per batch (two code words per group and lane)
+
+// two E2M1 codes (the low byte of `byte`, first code in the low nibble) -> FP16 pair
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+      : "=r"(d)
+      : "r"(byte));
+  return d;
+}
+// two E4M3 codes (the low 16 bits of `pair`, first code in the low byte) -> FP16 pair
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)pair));
+  return d;
+}
+// E8M0 byte -> 2^(s - 127) as FP32 (s = 0 is the subnormal 2^-127; 0xFF never reaches here:
+// repack and the callers' quantizer reject it)
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  return __uint_as_float(s ? (s << 23) : 0x00400000u);
+}
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+struct W4A8GemvParams {
+  const uint8_t* wp;   // codes [N_pad][K_pad / 2]
+  const uint8_t* sp;   // E8M0 in 512-byte chunks of 128 rows x 4 groups
+  const uint8_t* A;    // E4M3 [M][K]
+  const uint8_t* Asf;  // E8M0 [M][K / 32]
+  const uint16_t* bias;
+  uint16_t* C;
+  int32_t N, N_pad, K, K_pad, M;
+  int32_t gpw;  // scale groups per warp, a multiple of 4
+};
+
+// Byte offset of the 4 scales (row r, groups 4q .. 4q + 3) in the chunked layout.
+__device__ __forceinline__ int64_t sf_word_offset(int64_t r, int q, int K_pad) {
+  return ((r >> 7) * (K_pad >> 7) + q) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
+}
+
+__global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8GemvParams p) {
+  constexpr int R = kW8Ring;
+  __shared__ float red[2][kW8Warps * 128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = p.K >> 5;
+  const uint32_t nblocks = (uint32_t)(p.N_pad >> 4);
+  const int g0 = min(G, warp * p.gpw);
+  const int cnt = min(G, g0 + p.gpw) - g0;  // this warp's groups per item (may be 0)
+  const int nbat = (cnt + R - 1) / R;
+  const int64_t row_bytes = p.K_pad >> 1;
+  const uint32_t my_items =
+      blockIdx.x < nblocks ? (nblocks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  pdl_launch_dependents();
+
+  // ring: code words of rows g and g + 8 for the batch's groups, and their scale words
+  uint32_t wr[R][2];
+  uint32_t sw[R / 4][2];
+  const uint8_t* rw = nullptr;  // row g's code bytes at the refilling batch's first group
+  int rg = 0;                   // first group of the refilling batch
+  int rng = 0;                  // its group count (0: nothing left)
+  int64_t rrow = 0;             // row g of the refilling batch's item
+  uint32_t nx_it = 0;
+  int nx_c = 0;
+  auto point = [&](uint32_t it, int c) {
+    rng = 0;
+    if (it < my_items && c < nbat) {
+      const uint32_t nb = blockIdx.x + it * gridDim.x;
+      rg = g0 + R * c;
+      rrow = (int64_t)nb * 16 + g;
+      rw = p.wp + rrow * row_bytes + rg * 16 + 4 * t;
+      rng = min(R, g0 + cnt - rg);
+    }
+  };
+  auto advance = [&]() {
+    if (++nx_c == nbat) {
+      nx_c = 0;
+      ++nx_it;
+    }
+    point(nx_it, nx_c);
+  };
+  // slot j's code words; scale word b covers slots 4b .. 4b + 3 (rg is a multiple of 4)
+  auto refill_w = [&](int j) {
+    if (j < rng) {
+      wr[j][0] = __ldcs(reinterpret_cast<const uint32_t*>(rw + j * 16));
+      wr[j][1] = __ldcs(reinterpret_cast<const uint32_t*>(rw + 8 * row_bytes + j * 16));
+    }
+  };
+  auto refill_s = [&](int b) {
+    if (4 * b < rng) {
+      const int q = (rg >> 2) + b;
+      sw[b][0] = __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(rrow, q, p.K_pad)));
+      sw[b][1] =
+          __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(rrow + 8, q, p.K_pad)));
+    }
+  };
+  point(0, 0);
+#pragma unroll
+  for (int j = 0; j < R; ++j) refill_w(j);
+#pragma unroll
+  for (int b = 0; b < R / 4; ++b) refill_s(b);
+  advance();
+
+  pdl_wait();  // activations, their scales, bias and the output
+  // B operand: token row g (rows past M read row 0; their results are never stored); the
+  // D fragment's columns are tokens 2t and 2t + 1
+  const int KG = p.K >> 5;
+  const uint8_t* arow = p.A + (int64_t)(g < p.M ? g : 0) * p.K + 8 * t;
+  const uint8_t* sfa0 = p.Asf + (int64_t)(2 * t < p.M ? 2 * t : 0) * KG;
+  const uint8_t* sfa1 = p.Asf + (int64_t)(2 * t + 1 < p.M ? 2 * t + 1 : 0) * KG;
+
+  for (uint32_t it = 0; it < my_items; ++it) {
+    const uint32_t nb = blockIdx.x + it * gridDim.x;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < nbat; ++c) {
+      const int gb = g0 + R * c;
+      const int ng = min(R, g0 + cnt - gb);
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        if (j < ng) {
+          const int gg = gb + j;
+          const uint2 x = __ldg(reinterpret_cast<const uint2*>(arow + gg * 32));
+          const uint32_t wa = wr[j][0], wb = wr[j][1];
+          const uint32_t swa = sw[j >> 2][0], swb = sw[j >> 2][1];
+          // slot j (and after its last group, scale word j / 4) is free: start loading the
+          // next batch's
+          refill_w(j);
+          if ((j & 3) == 3) refill_s(j >> 2);
+          float pr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int st = 0; st < 2; ++st) {
+            const int sh = 16 * st;  // code bytes 2st, 2st + 1 of each row
+            uint32_t a[4];
+            // (the conversion reads the low byte of its operand)
+            a[0] = e2m1x2_to_f16x2(wa >> sh);
+            a[1] = e2m1x2_to_f16x2(wb >> sh);
+            a[2] = e2m1x2_to_f16x2(wa >> (sh + 8));
+            a[3] = e2m1x2_to_f16x2(wb >> (sh + 8));
+            const uint32_t xv = st ? x.y : x.x;
+            mma_f16_16816(pr, a, e4m3x2_to_f16x2(xv & 0xFFFFu), e4m3x2_to_f16x2(xv >> 16));
+          }
+          const int sb = 8 * (gg & 3);  // this group's byte in the scale words
+          const float fw0 = e8m0_to_f32((swa >> sb) & 0xFFu);
+          const float fw1 = e8m0_to_f32((swb >> sb) & 0xFFu);
+          const float fa0 = e8m0_to_f32(__ldg(sfa0 + gg));
+          const float fa1 = e8m0_to_f32(__ldg(sfa1 + gg));
+          acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
+          acc[1] = fmaf(pr[1] * fw0, fa1, acc[1]);
+          acc[2] = fmaf(pr[2] * fw1, fa0, acc[2]);
+          acc[3] = fmaf(pr[3] * fw1, fa1, acc[3]);
+        }
+      }
+      // slots and scale words the loop did not reach
+#pragma unroll
+      for (int j = 0; j < R; ++j)
+        if (j >= ng) refill_w(j);
+#pragma unroll
+      for (int b = 0; b < R / 4; ++b)
+        if (4 * b + 3 >= ng) refill_s(b);
+      advance();
+    }
+
+    // split-K reduction over the CTA's warps, fixed order; one barrier per item
+    float* rb = red[it & 1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rb[(warp * 4 + i) * 32 + lane] = acc[i];
+    __syncthreads();
+    for (int o = threadIdx.x; o < 16 * p.M; o += kW8Warps * 32) {
+      const int nl = o & 15, m = o >> 4;
+      const int l = (nl & 7) * 4 + (m >> 1), i = (nl >> 3) * 2 + (m & 1);
+      float v = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kW8Warps; ++w2) v += rb[(w2 * 4 + i) * 32 + l];
+      const int n = (int)nb * 16 + nl;
+      if (n < p.N) {
+        if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + n) << 16);
+        __nv_bfloat16 h = __float2bfloat16_rn(v);
+        p.C[(int64_t)m * p.N + n] = *reinterpret_cast<uint16_t*>(&h);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                           const void* A, const void* A_sf, const void* bias, void* C, int M,
+                           cudaStream_t st) {
+  if (M < 1 || M > kW4A8GemvRows || d.E != 1 || d.wfmt != QW_W_MXFP4_G32) return QW_ERR_UNSUPPORTED;
+  W4A8GemvParams p{};
+  p.wp = static_cast<const uint8_t*>(w_packed);
+  p.sp = static_cast<const uint8_t*>(s_packed);
+  p.A = static_cast<const uint8_t*>(A);
+  p.Asf = static_cast<const uint8_t*>(A_sf);
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.C = static_cast<uint16_t*>(C);
+  p.N = d.N;
+  p.N_pad = d.N_pad;
+  p.K = d.K;
+  p.K_pad = d.K_pad;
+  p.M = M;
+  const int G = d.K / kMxGroup;
+  p.gpw = ((G + kW8Warps - 1) / kW8Warps + 3) / 4 * 4;
+  auto kern = gemv_w4a8_kernel;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kW8Warps * 32, 0) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t items = d.N_pad / 16;
+  int64_t grid = (int64_t)device_sm_count() * per_sm;
+  if (grid > items) grid = items;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kW8Warps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return QW_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
+
+}  // namespace qw

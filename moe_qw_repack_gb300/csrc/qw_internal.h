@@ -66,6 +66,12 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
                            cudaStream_t st);
 uint64_t gemm_w4a8_workspace(const qw_packed_desc& d, int64_t max_rows);
 
+// Dense W4A8 (MXFP4 weights) calls of at most this many rows run the streaming GEMV.
+constexpr int kW4A8GemvRows = 8;
+qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                           const void* A, const void* A_sf, const void* bias, void* C, int M,
+                           cudaStream_t st);
+
 // MoE scheduling.
 qw_status launch_moe_route(const float* logits, int32_t T, int32_t E, int32_t topk,
                            int32_t* topk_ids, int32_t* sorted_pairs, int32_t* offsets, void* ws,

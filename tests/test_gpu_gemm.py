@@ -105,6 +105,56 @@ def test_w4a8_k_not_multiple_of_128_and_bias():
     assert_parity(C, R, S, "W4A8 K=96 + bias")
 
 
+# ----------------------------------------------------------------------------- W4A8 small M
+@pytest.mark.parametrize("M", [1, 2, 5, 8])
+def test_w4a8_gemv_integer_exact(M):
+    """M <= 8 runs the streaming W4A8 GEMV; with unit scales and small integer codes every
+    group sum is an exact integer, so the output equals the oracle's BF16 rounding."""
+    rng = np.random.default_rng(70 + M)
+    N, K = 272, 384
+    int_e4m3 = [0x00, 0x38, 0x40, 0x44, 0xB8, 0xC0, 0xC4]  # 0, 1, 2, 3, -1, -2, -3
+    int_e2m1 = [0, 2, 4, 5, 10, 12, 13]                   # 0, 1, 2, 3, -1, -2, -3
+    A = rng.choice(int_e4m3, (M, K)).astype(np.uint8)
+    W = rng.choice(int_e2m1, (N, K)).astype(np.uint8)
+    p = dict(A=A, A_sf=np.full((M, K // 32), 127, np.uint8), w_canon=synth.pack_nibbles(W)[None],
+             s_canon=np.full((1, N, K // 32), 127, np.uint8), N=N, K=K)
+    C = dense_w4a8(p)
+    R, S = OQ.gemm_w4a8(A, p["A_sf"], W, p["s_canon"][0])
+    assert np.array_equal(C, synth.to_bf16_bits(R))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 144, 32), (3, 264, 96), (8, 1000, 640), (2, 130, 4096),
+                                   (7, 4096, 1024)])
+def test_w4a8_gemv_shapes(M, N, K):
+    """Ragged N (padded to 128 rows), K not a multiple of 128 and group counts that leave
+    some warps of a CTA without work.  (With only a few dozen outputs the Frobenius bound
+    can fail for the correctly rounded BF16 result itself - e.g. 16 outputs of K = 32 -
+    so the smallest case keeps 144.)"""
+    p = synth.w4a8_problem(M, N, K, cfg_id=240 + M)
+    C = dense_w4a8(p)
+    R, S = OQ.w4a8_from_canonical(p["A"], p["A_sf"], p["w_canon"][0], p["s_canon"][0], K)
+    assert_parity(C, R, S, f"W4A8 GEMV {M}x{N}x{K}")
+
+
+def test_w4a8_gemv_bias_and_wide_scales():
+    """Bias, and E8M0 scales over a wide range (2^-47 .. 2^43) on both sides, so group
+    products span ~2^-94 .. 2^86 (inside BF16's range)."""
+    p = synth.w4a8_problem(4, 520, 512, cfg_id=250, bias=True, sf_lo=80, sf_hi=170)
+    C = dense_w4a8(p, bias=p["bias"][0])
+    R, S = OQ.w4a8_from_canonical(p["A"], p["A_sf"], p["w_canon"][0], p["s_canon"][0], 512,
+                                  bias_bits=p["bias"][0])
+    assert_parity(C, R, S, "W4A8 GEMV bias, wide scales")
+
+
+@pytest.mark.parametrize("N,K", [(14336, 4096), (4096, 14336)])
+def test_w4a8_gemv_m1_decode_full(N, K):
+    """Single-token W4A8 decode at full size, every output element."""
+    p = synth.w4a8_problem(1, N, K, cfg_id=260)
+    C = dense_w4a8(p)
+    R, S = OQ.w4a8_from_canonical(p["A"], p["A_sf"], p["w_canon"][0], p["s_canon"][0], K)
+    assert_parity(C, R, S, f"W4A8 M=1 {N}x{K}")
+
+
 def test_config2a_w4a8_full():
     """(M,N,K) = (4096, 3072, 4096) MXFP4 x MXFP8 group-32, every output element."""
     p = synth.w4a8_problem(4096, 3072, 4096, cfg_id=1)
