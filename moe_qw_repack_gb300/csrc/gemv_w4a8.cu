@@ -21,8 +21,10 @@
 // assignment of k to MMA slots gives the same sum, as long as both operands use it.
 // Work item = 16 weight rows over all of K; the 8 warps of a CTA split the groups and meet
 // in shared memory (fixed-order sum).  Each warp keeps the next 16 groups' code words in a
-// register ring (4 KiB per warp in flight).  Launched as a programmatic dependent: only
-// weights and their scales are read before griddepcontrol.wait.
+// register ring (4 KiB per warp in flight) and stages its groups' activations once, already
+// decoded (FP16 B fragments and FP32 scales in shared memory), so the inner loop is two
+// shared loads, eight conversions and two MMAs per group.  Launched as a programmatic
+// dependent: only weights and their scales are read before griddepcontrol.wait.
 #include "qw_common.cuh"
 #include "qw_internal.h"
 
@@ -83,6 +85,7 @@ __device__ __forceinline__ int64_t sf_word_offset(int64_t r, int q, int K_pad) {
 __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8GemvParams p) {
   constexpr int R = kW8Ring;
   __shared__ float red[2][kW8Warps * 128];
+  extern __shared__ uint4 w8_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int G = p.K >> 5;
@@ -144,13 +147,31 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
   for (int b = 0; b < R / 4; ++b) refill_s(b);
   advance();
 
-  pdl_wait();  // activations, their scales, bias and the output
+  // ---- activations (the previous kernel's output may be A): each warp stages its own
+  // groups once, decoded - B fragments as FP16 pairs [group][row][t][4 x f16x2] and the
+  // scales as FP32 [group][8 tokens] (tokens past M get 0: never stored)
+  pdl_wait();
+  const int KG = p.K >> 5;
+  uint8_t* act = reinterpret_cast<uint8_t*>(w8_smem);
+  float* fa = reinterpret_cast<float*>(act + (size_t)G * p.M * 64);
+  for (int q = lane; q < cnt * p.M * 4; q += 32) {
+    const int tt = q & 3, m = (q >> 2) % p.M, gl = (q >> 2) / p.M;
+    const int gg = g0 + gl;
+    const uint2 x = __ldg(reinterpret_cast<const uint2*>(p.A + (int64_t)m * p.K + gg * 32 + 8 * tt));
+    const uint4 v = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16),
+                               e4m3x2_to_f16x2(x.y), e4m3x2_to_f16x2(x.y >> 16));
+    *reinterpret_cast<uint4*>(act + ((gg * p.M + m) * 4 + tt) * 16) = v;
+  }
+  for (int q = lane; q < cnt * 8; q += 32) {
+    const int tok = q & 7, gg = g0 + (q >> 3);
+    fa[gg * 8 + tok] = tok < p.M ? e8m0_to_f32(__ldg(p.Asf + (int64_t)tok * KG + gg)) : 0.f;
+  }
+  __syncwarp();
   // B operand: token row g (rows past M read row 0; their results are never stored); the
   // D fragment's columns are tokens 2t and 2t + 1
-  const int KG = p.K >> 5;
-  const uint8_t* arow = p.A + (int64_t)(g < p.M ? g : 0) * p.K + 8 * t;
-  const uint8_t* sfa0 = p.Asf + (int64_t)(2 * t < p.M ? 2 * t : 0) * KG;
-  const uint8_t* sfa1 = p.Asf + (int64_t)(2 * t + 1 < p.M ? 2 * t + 1 : 0) * KG;
+  const uint32_t act_lane = smem_u32(act) + (uint32_t)(((g < p.M ? g : 0) * 4 + t) * 16);
+  const uint32_t grp_stride = (uint32_t)p.M * 64;
+  const uint32_t fa_lane = smem_u32(fa) + (uint32_t)(2 * t * 4);
 
   for (uint32_t it = 0; it < my_items; ++it) {
     const uint32_t nb = blockIdx.x + it * gridDim.x;
@@ -162,7 +183,14 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
       for (int j = 0; j < R; ++j) {
         if (j < ng) {
           const int gg = gb + j;
-          const uint2 x = __ldg(reinterpret_cast<const uint2*>(arow + gg * 32));
+          uint4 x;
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                       : "r"(act_lane + (uint32_t)gg * grp_stride));
+          uint2 f2;
+          asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                       : "=r"(f2.x), "=r"(f2.y)
+                       : "r"(fa_lane + (uint32_t)gg * 32));
           const uint32_t wa = wr[j][0], wb = wr[j][1];
           const uint32_t swa = sw[j >> 2][0], swb = sw[j >> 2][1];
           // slot j (and after its last group, scale word j / 4) is free: start loading the
@@ -179,14 +207,12 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
             a[1] = e2m1x2_to_f16x2(wb >> sh);
             a[2] = e2m1x2_to_f16x2(wa >> (sh + 8));
             a[3] = e2m1x2_to_f16x2(wb >> (sh + 8));
-            const uint32_t xv = st ? x.y : x.x;
-            mma_f16_16816(pr, a, e4m3x2_to_f16x2(xv & 0xFFFFu), e4m3x2_to_f16x2(xv >> 16));
+            mma_f16_16816(pr, a, st ? x.z : x.x, st ? x.w : x.y);
           }
-          const int sb = 8 * (gg & 3);  // this group's byte in the scale words
+          const int sb = 8 * (j & 3);  // this group's byte in the scale words (gb % 4 == 0)
           const float fw0 = e8m0_to_f32((swa >> sb) & 0xFFu);
           const float fw1 = e8m0_to_f32((swb >> sb) & 0xFFu);
-          const float fa0 = e8m0_to_f32(__ldg(sfa0 + gg));
-          const float fa1 = e8m0_to_f32(__ldg(sfa1 + gg));
+          const float fa0 = __uint_as_float(f2.x), fa1 = __uint_as_float(f2.y);
           acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
           acc[1] = fmaf(pr[1] * fw0, fa1, acc[1]);
           acc[2] = fmaf(pr[2] * fw1, fa0, acc[2]);
@@ -229,7 +255,9 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
 qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
                            const void* A, const void* A_sf, const void* bias, void* C, int M,
                            cudaStream_t st) {
-  if (M < 1 || M > kW4A8GemvRows || d.E != 1 || d.wfmt != QW_W_MXFP4_G32) return QW_ERR_UNSUPPORTED;
+  if (M < 1 || M > kW4A8GemvRows || d.E != 1 || d.wfmt != QW_W_MXFP4_G32 ||
+      w4a8_gemv_smem_bytes(d.K, M) > kW4A8GemvMaxSmem)
+    return QW_ERR_UNSUPPORTED;
   W4A8GemvParams p{};
   p.wp = static_cast<const uint8_t*>(w_packed);
   p.sp = static_cast<const uint8_t*>(s_packed);
@@ -245,8 +273,12 @@ qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   const int G = d.K / kMxGroup;
   p.gpw = ((G + kW8Warps - 1) / kW8Warps + 3) / 4 * 4;
   auto kern = gemv_w4a8_kernel;
+  const size_t smem = w4a8_gemv_smem_bytes(d.K, M);
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kW4A8GemvMaxSmem);
+  if (attr != cudaSuccess) return QW_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kW8Warps * 32, 0) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kW8Warps * 32, smem) !=
           cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
@@ -257,7 +289,7 @@ qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kW8Warps * 32);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

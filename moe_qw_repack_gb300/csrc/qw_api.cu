@@ -190,7 +190,8 @@ qw_status qgemm_dense(const qw_packed_desc* desc, const void* w_packed, const vo
   if (M == 0) return QW_OK;
   RowSet rs{M, nullptr, 1};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (desc->wfmt == QW_W_MXFP4_G32 && M <= kW4A8GemvRows)
+  if (desc->wfmt == QW_W_MXFP4_G32 && M <= kW4A8GemvRows &&
+      w4a8_gemv_smem_bytes(desc->K, (int)M) <= kW4A8GemvMaxSmem)
     return launch_gemv_w4a8(*desc, w_packed, s_packed, A, A_sf, bias, C, (int)M, st);
   if (is_mx(desc->wfmt))
     return launch_gemm_w4a8(*desc, w_packed, s_packed, A, A_sf, bias, C, rs, workspace, ws_bytes,

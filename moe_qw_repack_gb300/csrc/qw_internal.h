@@ -66,8 +66,14 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
                            cudaStream_t st);
 uint64_t gemm_w4a8_workspace(const qw_packed_desc& d, int64_t max_rows);
 
-// Dense W4A8 (MXFP4 weights) calls of at most this many rows run the streaming GEMV.
+// Dense W4A8 (MXFP4 weights) calls of at most this many rows whose staged activations
+// (FP16 B fragments and FP32 scales of every group) fit kW4A8GemvMaxSmem run the
+// streaming GEMV.
 constexpr int kW4A8GemvRows = 8;
+constexpr size_t kW4A8GemvMaxSmem = 96 * 1024;
+constexpr size_t w4a8_gemv_smem_bytes(int K, int M) {
+  return (size_t)(K / 32) * ((size_t)M * 64 + 32);
+}
 qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
                            const void* A, const void* A_sf, const void* bias, void* C, int M,
                            cudaStream_t st);
