@@ -346,6 +346,11 @@ def extra_moe(steps, warmup, world, only=None):
     r = moe_pipeline(Q.QW_A_MXFP8_G32, Q.QW_W_MXFP4_G32, E, T, K, N, k, cfg_id=3)
     tot, each, n, graph = parts([r["route"], r["permute"], r["gemm"]], steps, 4)
     assert Q.qw_read_error(r["err"]) == 0
+    # the Indexed path: route + one GEMM that gathers the rows by pair id (no permute)
+    tot_ix, _, _ = time_region([r["route"], r["gemm_indexed"]], steps, warmup, world,
+                               graph_steps=4)
+    gemm_ix = time_region([r["gemm_indexed"]], steps, 1, world, graph_steps=4)[0]
+    assert Q.qw_read_error(r["err"]) == 0
     cnt = np.diff(r["offsets"].cpu().numpy())
     active = int((cnt > 0).sum())
     P = T * k
@@ -357,6 +362,7 @@ def extra_moe(steps, warmup, world, only=None):
         "us_permute": round(each[1] * 1e3, 1), "us_gemm": round(gemm_ms * 1e3, 1),
         "gemm_tflops": round(flop / (gemm_ms * 1e-3) / 1e12, 1),
         "gemm_frac_fp8_peak": round(flop / (gemm_ms * 1e-3) / 1e12 / (2 * peaks["bf16_tflops"]), 3),
+        "us_total_indexed": round(tot_ix * 1e3, 1), "us_gemm_indexed": round(gemm_ix * 1e3, 1),
         "active_experts": active, "active_weight_GB": round(wbytes / 1e9, 3),
         "weight_stream_frac_hbm": round(wbytes / (gemm_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
         "steps": n, "graph": graph}

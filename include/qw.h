@@ -277,6 +277,27 @@ qw_status qgemm_moe_grouped(const qw_packed_desc* desc, const void* w_packed,
                             uint64_t ws_bytes, int32_t* d_err, void* stream);
 
 /* --------------------------------------------------------------------------------------
+ * qgemm_moe_grouped_indexed - the Indexed MoE path (spke.com announcement, "WnA16" /
+ * "W8A8 / W4A8 / W4A4": Indexed and Grouped MoE layouts): qgemm_moe_grouped with the
+ * permutation folded into the kernel.  Problem row r (in the expert-contiguous order of
+ * qgemm_moe_route) reads activation row sorted_pairs[r] / topk of the UNPERMUTED input:
+ *   C[r][n] = bf16( sum_k A[sorted_pairs[r] / topk][k] * W_e[n][k] + bias[e][n] )
+ * for r in [expert_offsets[e], expert_offsets[e+1]); the result equals
+ * qgemm_moe_permute followed by qgemm_moe_grouped, bit for bit.
+ *   MX weight formats only (W4A8 / W8A8; other formats return QW_ERR_UNSUPPORTED).
+ *   A: E4M3 [T][K]; A_sf: E8M0 [T][K/32]; sorted_pairs: device int32 [total_rows] with
+ *   total_rows <= T * topk; the rest as for qgemm_moe_grouped (same workspace size).
+ *   A pair outside [0, T*topk) sets QW_ERR_INVALID_ARG in d_err (its row reads token 0).
+ */
+qw_status qgemm_moe_grouped_indexed(const qw_packed_desc* desc, const void* w_packed,
+                                    const void* s_packed, int32_t afmt, const void* A,
+                                    const void* A_sf, int64_t T, const int32_t* sorted_pairs,
+                                    int32_t topk, const int32_t* expert_offsets,
+                                    int64_t total_rows, const void* bias, void* C,
+                                    void* workspace, uint64_t ws_bytes, int32_t* d_err,
+                                    void* stream);
+
+/* --------------------------------------------------------------------------------------
  * qw_read_error - synchronise `stream`, copy *d_err to the host (`host_code`, host
  * pointer) and return it as a qw_status (QW_ERR_CUDA if the synchronisation fails).
  */

@@ -26,6 +26,10 @@
 //               free, then the proxy fence that lets the tensor core read it.  (A
 //               fence waits for the thread's outstanding memory operations; keeping the
 //               global loads in another warp keeps them off the fence.)
+//   Indexed MoE calls skip the separate permutation: problem row r is activation row
+//   sorted_pairs[r] / topk, fetched by TMA gather4 copies (four 128-byte rows each, a
+//   one-row tensor-map box) whose row indices warp 0 looks up a tile ahead; the scale
+//   fetcher reads the same rows' scales.  The results are those of permute + grouped.
 //   warps 4-11  epilogue: tcgen05.ld the FP32 accumulator (each warp one 32-lane
 //               quadrant x 128 columns), add bias, round to BF16, release TMEM, store.
 // Every mbarrier wait is bounded; on expiry the kernel raises QW_ERR_TIMEOUT, lets its
@@ -57,7 +61,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL0 = 256;      // accumulator uses columns [0, 256)
 constexpr uint32_t SF_COLS_PER_STAGE = 12;  // 4 (A: 128 rows) + 8 (B: 256 rows)
 constexpr size_t SMEM_BYTES = (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) +
-                              (size_t)SF_STAGING * SFA_BYTES + 512 + 1024;
+                              (size_t)SF_STAGING * SFA_BYTES + BM * 4 + 512 + 1024;
 
 // Instruction descriptor, kind::mxf8f6f4: A = E4M3 (0), B = E2M1 (5) or E4M3 (0), both
 // K-major, N >> 3 at bit 17, scale type UE8M0 (bit 23), M >> 4 at bit 24; the B / A scale
@@ -80,6 +84,11 @@ struct Params {
   uint16_t* C;            // [rows][N]
   const int32_t* queue;   // grouped tile queue (BM rows per entry) or null
   int32_t* err;
+  // indexed grouped calls: problem row r reads activation row gather[r] / topk (of
+  // a_rows); the activation tile is then fetched with TMA gather4, four rows per copy
+  const int32_t* gather;
+  int32_t topk;
+  int64_t a_rows;
 };
 
 struct Tile {
@@ -104,15 +113,42 @@ __device__ __forceinline__ Tile tile_at(const Params& p, int64_t t) {
   return x;
 }
 
-__device__ __forceinline__ uint32_t load_sf_word(const Params& p, int64_t r, int kb) {
+// Scales of activation row `ar` (an act_row result, or -1 past the problem) for K step kb.
+__device__ __forceinline__ uint32_t load_sf_word(const Params& p, int64_t ar, int kb) {
   const int G = p.K / 32;  // canonical groups per row
   const int g0 = kb * 4;
-  if (r >= p.rows) return 0x7F7F7F7Fu;
-  const uint8_t* row = p.A_sf + r * (int64_t)G;
+  if (ar < 0) return 0x7F7F7F7Fu;
+  const uint8_t* row = p.A_sf + ar * (int64_t)G;
   if ((G & 3) == 0 && g0 + 3 < G) return __ldg(reinterpret_cast<const uint32_t*>(row + g0));
   uint32_t w = 0;
   for (int j = 0; j < 4; ++j) w |= (uint32_t)(g0 + j < G ? __ldg(row + g0 + j) : 127) << (8 * j);
   return w;
+}
+
+// Activation row of problem row r: itself, or (indexed calls) the token of pair gather[r].
+// Rows past the problem (tile tails) read row `fallback`; a pair outside [0, a_rows * topk)
+// raises QW_ERR_INVALID_ARG and reads row 0.
+__device__ __forceinline__ int64_t act_row(const Params& p, int64_t r, int64_t fallback) {
+  if (r >= p.rows) r = fallback;
+  if (!p.gather) return r;
+  const int32_t pair = __ldg(p.gather + r);
+  const int64_t tok = pair >= 0 ? (int64_t)(pair / p.topk) : -1;
+  if (tok < 0 || tok >= p.a_rows) {
+    set_error(p.err, QW_ERR_INVALID_ARG);
+    return 0;
+  }
+  return tok;
+}
+
+// Four 128-byte rows of a tensor map with a one-row box into consecutive 128-byte rows of
+// shared memory (the swizzle follows the destination address, as for a tiled load).
+__device__ __forceinline__ void tma_gather4(void* dst, const void* map, uint64_t* bar, int32_t col,
+                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // Wait for a phase without the CTA-wide abort shortcut (used when draining copies).
@@ -133,7 +169,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* sSFA = sB + STAGES * B_BYTES;
   uint8_t* sSFB = sSFA + STAGES * SFA_BYTES;
   uint8_t* sStage = sSFB + STAGES * SFB_BYTES;  // staged A scale images
-  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + SF_STAGING * SFA_BYTES);
+  int32_t* sIdx = reinterpret_cast<int32_t*>(sStage + SF_STAGING * SFA_BYTES);  // [BM] rows
+  uint64_t* full = reinterpret_cast<uint64_t*>(sIdx + BM);
   uint64_t* empty = full + STAGES;
   uint64_t* sfull = empty + STAGES;   // staging slot written (32 fetcher lanes)
   uint64_t* sempty = sfull + SF_STAGING;  // staging slot read (writer)
@@ -179,22 +216,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0, issued_phase = 0;  // per-stage bitmasks for the final drain
-      bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        const Tile x = tile_at(p, t);
+    // Lane 0 issues every copy.  Indexed calls: the whole warp looks up the next tile's 128
+    // activation rows while lane 0 streams the current one, and hands them over through
+    // shared memory at the tile boundary.
+    int32_t nxt[4];
+    auto rows_of = [&](int64_t t) {
+      const Tile y = tile_at(p, t);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) nxt[j] = (int32_t)act_row(p, y.rb + 32 * j + lane, y.rb);
+    };
+    if (p.gather && blockIdx.x < num_tiles) rows_of(blockIdx.x);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_phase = 0;  // per-stage bitmasks for the final drain
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      const Tile x = tile_at(p, t);
+      if (p.gather) {
+        __syncwarp();  // lane 0 is done with the previous tile's rows
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sIdx[32 * j + lane] = nxt[j];
+        __syncwarp();
+        if (t + gridDim.x < num_tiles) rows_of(t + gridDim.x);
+      }
+      if (lane == 0) {
         const int nchunks = (x.n0 + 128 < p.N_pad) ? 2 : 1;
         const uint8_t* sfb = p.s_packed + x.e * p.s_estride;
+        // indexed calls gather only the tile's own rows (groups of four): the rows past
+        // them keep stale shared memory and produce outputs that are never stored
+        const int ngather = p.gather ? (int)((min64(x.re - x.rb, BM) + 3) / 4) : 0;
+        const uint32_t a_tx = p.gather ? (uint32_t)ngather * 4 * BK : A_BYTES;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], A_BYTES + b_tx_bytes<W8>() + nchunks * SFB_CHUNK);
-          tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, (int32_t)x.rb);
+          mbar_arrive_expect_tx(&full[stage], a_tx + b_tx_bytes<W8>() + nchunks * SFB_CHUNK);
+          if (p.gather) {
+            for (int i = 0; i < ngather; ++i)
+              tma_gather4(sA + stage * A_BYTES + i * 4 * BK, &tmA, &full[stage], kb * BK,
+                          sIdx[4 * i], sIdx[4 * i + 1], sIdx[4 * i + 2], sIdx[4 * i + 3]);
+          } else {
+            tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, (int32_t)x.rb);
+          }
           tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK,
                       x.e * p.N_pad + x.n0);
           for (int c = 0; c < nchunks; ++c)
@@ -209,10 +273,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      // let every copy this thread issued land before shared memory goes away
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    }
+    // let every copy lane 0 issued land before shared memory goes away
+    if (lane == 0)
       for (int s = 0; s < STAGES; ++s)
         if (issued & (1u << s)) drain_wait(&full[s], (issued_phase >> s) & 1u);
-    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -263,18 +329,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int AHEAD = 3;
     int64_t lt = blockIdx.x;  // load cursor: tile and K step
     int lkb = 0;
-    Tile lx = tile_at(p, lt < num_tiles ? lt : 0);
+    int64_t ar[4];            // activation rows of this lane's four tile rows (-1: none)
+    auto rows_of = [&](int64_t t) {
+      const Tile y = tile_at(p, t);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t r = y.rb + 32 * j + lane;
+        ar[j] = r < p.rows ? act_row(p, r, y.rb) : -1;
+      }
+    };
+    if (lt < num_tiles) rows_of(lt);
     auto load_next = [&]() {
       uint4 v = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       if (lt < num_tiles) {
-        v.x = load_sf_word(p, lx.rb + lane, lkb);
-        v.y = load_sf_word(p, lx.rb + 32 + lane, lkb);
-        v.z = load_sf_word(p, lx.rb + 64 + lane, lkb);
-        v.w = load_sf_word(p, lx.rb + 96 + lane, lkb);
+        v.x = load_sf_word(p, ar[0], lkb);
+        v.y = load_sf_word(p, ar[1], lkb);
+        v.z = load_sf_word(p, ar[2], lkb);
+        v.w = load_sf_word(p, ar[3], lkb);
         if (++lkb == KB) {
           lkb = 0;
           lt += gridDim.x;
-          if (lt < num_tiles) lx = tile_at(p, lt);
+          if (lt < num_tiles) rows_of(lt);
         }
       }
       return v;
@@ -431,9 +506,12 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
 
   CUtensorMap tmA, tmB;
   {
-    cuuint64_t gdim[2] = {(cuuint64_t)d.K, (cuuint64_t)rs.rows};
+    // indexed calls read the unpermuted activations one row per box (gather4 copies)
+    const bool gather = rs.gather != nullptr;
+    if (gather && (rs.a_rows < 1 || rs.a_rows > 0x7FFFFFFFLL)) return QW_ERR_UNSUPPORTED;
+    cuuint64_t gdim[2] = {(cuuint64_t)d.K, (cuuint64_t)(gather ? rs.a_rows : rs.rows)};
     cuuint64_t gstr[1] = {(cuuint64_t)d.K};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+    cuuint32_t box[2] = {(cuuint32_t)BK, gather ? 1u : (cuuint32_t)BM};
     cuuint32_t es[2] = {1, 1};
     if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(A), gdim, gstr, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -466,6 +544,9 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   p.bias = static_cast<const uint16_t*>(bias);
   p.C = static_cast<uint16_t*>(C);
   p.err = err;
+  p.gather = rs.gather;
+  p.topk = rs.topk;
+  p.a_rows = rs.a_rows;
   int64_t max_m_tiles = p.num_m_tiles;
   if (rs.offsets) {
     const uint64_t need = tile_queue_bytes(rs.E, rs.rows, BM);

@@ -314,6 +314,31 @@ qw_status qgemm_moe_grouped(const qw_packed_desc* desc, const void* w_packed,
                            d_err, st);
 }
 
+qw_status qgemm_moe_grouped_indexed(const qw_packed_desc* desc, const void* w_packed,
+                                    const void* s_packed, int32_t afmt, const void* A,
+                                    const void* A_sf, int64_t T, const int32_t* sorted_pairs,
+                                    int32_t topk, const int32_t* expert_offsets,
+                                    int64_t total_rows, const void* bias, void* C,
+                                    void* workspace, uint64_t ws_bytes, int32_t* d_err,
+                                    void* stream) {
+  qw_status s = check_gemm_args(desc, w_packed, s_packed, afmt, A, A_sf, C, total_rows);
+  if (s != QW_OK) return s;
+  if (!is_mx(desc->wfmt)) return QW_ERR_UNSUPPORTED;
+  if (!expert_offsets || !aligned(expert_offsets, 4)) return QW_ERR_INVALID_ARG;
+  if (desc->E > 1024) return QW_ERR_UNSUPPORTED;
+  if (topk < 1 || T < 0 || T > 0x7FFFFFFFLL || total_rows > T * (int64_t)topk)
+    return QW_ERR_INVALID_ARG;
+  if (total_rows > 0 && (!sorted_pairs || !aligned(sorted_pairs, 4))) return QW_ERR_INVALID_ARG;
+  if (bias && !aligned(bias, 2)) return QW_ERR_ALIGNMENT;
+  if (total_rows == 0) return QW_OK;
+  uint64_t need = 0;
+  qgemm_workspace_size(desc, afmt, total_rows, &need);
+  if (!workspace || ws_bytes < need) return QW_ERR_WORKSPACE;
+  RowSet rs{total_rows, expert_offsets, desc->E, sorted_pairs, topk, T};
+  return launch_gemm_w4a8(*desc, w_packed, s_packed, A, A_sf, bias, C, rs, workspace, ws_bytes,
+                          d_err, static_cast<cudaStream_t>(stream));
+}
+
 qw_status qw_read_error(const int32_t* d_err, void* stream, int32_t* host_code) {
   if (!d_err || !host_code) return QW_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QW_ERR_CUDA;

@@ -29,6 +29,11 @@ struct RowSet {
   int64_t rows;                // M (dense) or total rows (grouped)
   const int32_t* offsets;      // device [E+1] or nullptr
   int32_t E;
+  // Indexed grouped calls: row r of the problem is activation row gather[r] / topk of an
+  // unpermuted [a_rows][K] input (gather = the router's sorted pair ids); else nullptr.
+  const int32_t* gather = nullptr;
+  int32_t topk = 1;
+  int64_t a_rows = 0;
 };
 
 // Small-M W4A16: tensor-core GEMV over the fragment-ordered packed weights.

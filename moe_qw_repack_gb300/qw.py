@@ -34,7 +34,8 @@ QW_A_MXFP8_G32 = 1
 EXPORTS = (
     "qw_status_str", "qw_version", "qw_repack_query", "qw_repack", "qw_unpack",
     "qgemm_workspace_size", "qgemm_dense", "qgemm_moe_route_workspace_size", "qgemm_moe_route",
-    "qgemm_moe_permute", "qgemm_moe_grouped", "qw_read_error", "qw_test_wait_timeout",
+    "qgemm_moe_permute", "qgemm_moe_grouped", "qgemm_moe_grouped_indexed", "qw_read_error",
+    "qw_test_wait_timeout",
     "qgemm_moe_route_noalloc", "qw_quantize_mxfp8", "qw_silu_mul",
     "qgemm_moe_combine_workspace_size", "qgemm_moe_combine",
 )
@@ -74,6 +75,8 @@ _SIGS = {
     "qgemm_moe_route": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _U64, _P, _P]),
     "qgemm_moe_permute": (_I32, [_I32, _P, _P, _I32, _P, _I64, _I32, _P, _P, _P]),
     "qgemm_moe_grouped": (_I32, [_DESC, _P, _P, _I32, _P, _P, _P, _I64, _P, _P, _P, _U64, _P, _P]),
+    "qgemm_moe_grouped_indexed": (_I32, [_DESC, _P, _P, _I32, _P, _P, _I64, _P, _I32, _P, _I64,
+                                         _P, _P, _P, _U64, _P, _P]),
     "qw_read_error": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
     "qw_test_wait_timeout": (_I32, [_P, _I64, _P]),
     "qgemm_moe_route_noalloc": (_I32, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
@@ -204,6 +207,15 @@ def qgemm_moe_grouped(desc, w_packed, s_packed, afmt, A_sorted, A_sf_sorted, exp
     _check("qgemm_moe_grouped", LIB.qgemm_moe_grouped(
         ctypes.byref(desc), _ptr(w_packed), _ptr(s_packed), afmt, _ptr(A_sorted),
         _ptr(A_sf_sorted), _ptr(expert_offsets), total_rows, _ptr(bias), _ptr(C),
+        _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)))
+
+
+def qgemm_moe_grouped_indexed(desc, w_packed, s_packed, afmt, A, A_sf, T, sorted_pairs, topk,
+                              expert_offsets, total_rows, bias, C, workspace=None, ws_bytes=0,
+                              d_err=None, stream=None):
+    _check("qgemm_moe_grouped_indexed", LIB.qgemm_moe_grouped_indexed(
+        ctypes.byref(desc), _ptr(w_packed), _ptr(s_packed), afmt, _ptr(A), _ptr(A_sf), T,
+        _ptr(sorted_pairs), topk, _ptr(expert_offsets), total_rows, _ptr(bias), _ptr(C),
         _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream)))
 
 

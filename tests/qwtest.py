@@ -162,8 +162,15 @@ def moe_pipeline(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4, weights=None, x_s
         w, s = wps[i % len(wps)]
         Q.qgemm_moe_grouped(d, w, s, afmt, As, Asf_s, off, P, None, C, ws, wsn, err)
 
+    def gemm_indexed(i=0):
+        """The Indexed path: the grouped GEMM reading the unpermuted activations by pair id
+        (MX formats; replaces permute + gemm)."""
+        w, s = wps[i % len(wps)]
+        Q.qgemm_moe_grouped_indexed(d, w, s, afmt, A, Asf, T, sp, topk, off, P, None, C, ws,
+                                    wsn, err)
+
     out.update(A_sorted=As, A_sf_sorted=Asf_s, C=C, err=err, route=route, permute=permute,
-               gemm=gemm, set_replicas=set_replicas)
+               gemm=gemm, gemm_indexed=gemm_indexed, set_replicas=set_replicas)
     return out
 
 

@@ -92,6 +92,31 @@ def test_gemm_host_validation(Q):
     Q.qgemm_dense(d, good, good, Q.QW_A_MXFP8_G32, good, good, None, good, 0, stream=0)
 
 
+def test_grouped_indexed_host_validation(Q):
+    good = 1 << 20
+    d = Q.qw_repack_query(Q.QW_W_MXFP4_G32, 8, 256, 256)
+    cases = [  # (T, topk, total_rows, workspace bytes, expected status)
+        (10, 2, 21, 1 << 20, Q.QW_ERR_INVALID_ARG),   # more rows than T * topk pairs
+        (10, 0, 4, 1 << 20, Q.QW_ERR_INVALID_ARG),    # topk < 1
+        (-1, 2, 0, 1 << 20, Q.QW_ERR_INVALID_ARG),    # negative T
+        (10, 2, 20, 0, Q.QW_ERR_WORKSPACE),           # no workspace
+    ]
+    for T, k, rows, ws, want in cases:
+        with pytest.raises(Q.QwError) as e:
+            Q.qgemm_moe_grouped_indexed(d, good, good, Q.QW_A_MXFP8_G32, good, good, T, good, k,
+                                        good, rows, None, good, good if ws else None, ws,
+                                        stream=0)
+        assert e.value.status == want, (T, k, rows, ws)
+    di = Q.qw_repack_query(Q.QW_W_INT4_G128_BF16, 8, 256, 256)
+    with pytest.raises(Q.QwError) as e:  # the indexed path takes the MX formats only
+        Q.qgemm_moe_grouped_indexed(di, good, good, Q.QW_A_BF16, good, None, 10, good, 2, good,
+                                    20, None, good, good, 1 << 20, stream=0)
+    assert e.value.status == Q.QW_ERR_UNSUPPORTED
+    # zero rows: a valid no-op
+    Q.qgemm_moe_grouped_indexed(d, good, good, Q.QW_A_MXFP8_G32, good, good, 10, good, 2, good,
+                                0, None, good, None, 0, stream=0)
+
+
 def test_route_host_validation(Q):
     good = 1 << 20
     for T, E, k in [(-1, 8, 2), (4, 8, 0), (4, 8, 33), (4, 4, 8), (4, 2048, 8)]:

@@ -41,8 +41,9 @@ def _weights(kind, E, N, K, bits, cfg_id):
     return synth.w4a16_problem(1, N, K, bits=bits, E=E, cfg_id=cfg_id)
 
 
-def run_moe(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4):
-    """Route -> permute -> grouped GEMM through the C ABI.  Returns host arrays."""
+def run_moe(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4, indexed=False):
+    """Route -> permute -> grouped GEMM through the C ABI.  Returns host arrays (and, with
+    ``indexed``, also the output of the indexed call on the unpermuted activations)."""
     Q = qw()
     logits = synth.router_logits(T, E, cfg_id=cfg_id)
     kind = "mx" if wfmt == Q.QW_W_MXFP4_G32 else "int"
@@ -79,7 +80,13 @@ def run_moe(afmt, wfmt, E, T, K, N, topk, cfg_id, bits=4):
     err = Q.new_error_flag()
     Q.qgemm_moe_grouped(d, wp, sp_, afmt, As, Asf_s, off, P, None, C, ws, wsn, err)
     assert Q.qw_read_error(err) == 0
-    return p, logits, host(sp), host(off), u16_view(C)
+    if not indexed:
+        return p, logits, host(sp), host(off), u16_view(C)
+    Ci = torch.full((P, N), -1, dtype=torch.int16, device="cuda")
+    Q.qgemm_moe_grouped_indexed(d, wp, sp_, afmt, A, Asf, T, sp, topk, off, P, None, Ci, ws, wsn,
+                                err)
+    assert Q.qw_read_error(err) == 0
+    return p, logits, host(sp), host(off), u16_view(C), u16_view(Ci)
 
 
 @pytest.mark.parametrize("E,T,K,N", [(8, 40, 256, 384), (16, 64, 512, 512), (32, 300, 128, 640)])
@@ -93,6 +100,44 @@ def test_moe_grouped_w4a8_small(E, T, K, N):
     R, S = OM.grouped_w4a8(p["A"][tok], p["A_sf"][tok], roff, codes, p["s_canon"])
     ok, ratio, frob = OQ.check_bf16_result(C, R, S)
     assert ok, (ratio, frob)
+
+
+@pytest.mark.parametrize("E,T,K,N,topk", [(8, 40, 256, 384, 8), (16, 300, 640, 256, 2),
+                                          (32, 129, 128, 640, 4), (4, 3, 96, 256, 1)])
+def test_moe_grouped_indexed_w4a8_equals_permute_then_grouped(E, T, K, N, topk):
+    """The Indexed path (rows gathered by pair id inside the kernel, TMA gather4) gives the
+    permuted path's output bit for bit, and both match the oracle."""
+    Q = qw()
+    p, logits, sp, off, C, Ci = run_moe(Q.QW_A_MXFP8_G32, Q.QW_W_MXFP4_G32, E, T, K, N, topk,
+                                        310 + E, indexed=True)
+    assert np.array_equal(C, Ci), f"{np.sum(C != Ci)} of {C.size} differ"
+    _, _, roff, rsp = OM.route(logits, topk)
+    tok = rsp // topk
+    codes = OF.unpack_e2m1_bytes(p["w_canon"], K)
+    R, S = OM.grouped_w4a8(p["A"][tok], p["A_sf"][tok], roff, codes, p["s_canon"])
+    ok, ratio, frob = OQ.check_bf16_result(Ci, R, S)
+    assert ok, (ratio, frob)
+
+
+def test_moe_grouped_indexed_flags_bad_pairs():
+    """A pair id outside [0, T*topk) is reported through the device error flag (its row
+    reads token 0) instead of being followed out of bounds."""
+    Q = qw()
+    E, T, K, N, topk = 4, 16, 128, 256, 2
+    w = _weights("mx", E, N, K, 4, 330)
+    a = synth.w4a8_problem(T, 32, K, cfg_id=331)
+    d, wp, spk = repack(Q.QW_W_MXFP4_G32, E, N, K, w["w_canon"], w["s_canon"])
+    P = T * topk
+    pairs = np.arange(P, dtype=np.int32)
+    pairs[5] = P + 7
+    off = np.array([0, 8, 16, 24, 32], dtype=np.int32)
+    C = torch.zeros((P, N), dtype=torch.int16, device="cuda")
+    wsn = Q.qgemm_workspace_size(d, Q.QW_A_MXFP8_G32, P)
+    ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
+    err = Q.new_error_flag()
+    Q.qgemm_moe_grouped_indexed(d, wp, spk, Q.QW_A_MXFP8_G32, dev(a["A"]), dev(a["A_sf"]), T,
+                                dev(pairs), topk, dev(off), P, None, C, ws, wsn, err)
+    assert Q.qw_read_error(err) == Q.QW_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("T", [1, 16, 64])
