@@ -9,6 +9,11 @@ output stage; section "WnA16": low-bit weights times 16-bit activations; section
   W4A16:  R[m,n] = sum_k a[m,k] * q[n,k] * s[n, k // G]            (+ bias[n])
   W4A8:   R[m,n] = sum_k e4m3(a[m,k]) 2^(sa[m,k//32]-127)
                           * e2m1(w[n,k]) 2^(sw[n,k//32]-127)      (+ bias[n])
+  W4A4:   R[m,n] = sum_k e2m1(a[m,k]) e4m3(sa[m,k//16])
+                          * e2m1(w[n,k]) e4m3(sw[n,k//16])        (+ bias[n])
+          (NVFP4 x NVFP4, the section's W4A4 / "NVFP4 x NVFP4 W4A4": E2M1 elements
+          with an unsigned E4M3 scale per 16 along K; the format's optional per-tensor
+          FP32 factor is left to the caller, as a plain multiplier of C)
 
 Every operand is decoded exactly into float64 and the sum over k is a float64
 matrix product (a library matmul used as one step, no blocking or reordering
@@ -81,6 +86,29 @@ def gemm_w8a8(A_codes, A_sf, w_codes, w_sf, bias_bits=None):
     return r, absum
 
 
+def dequant_nv(codes, sf, group: int = 16) -> np.ndarray:
+    """E2M1 codes [..., R, K] with E4M3 block scales [..., R, K/16] -> float64.  The
+    scale is unsigned: a set sign bit or the NaN code is a FormatError."""
+    sfa = np.asarray(sf).astype(np.int64)
+    if np.any((sfa & 0x80) != 0) or np.any((sfa & 0x7F) == 0x7F):
+        raise F.FormatError("NVFP4 scale must be a finite non-negative E4M3 code")
+    return F.decode_e2m1(codes) * np.repeat(F.decode_e4m3(sfa), group, axis=-1)
+
+
+def gemm_w4a4(A_codes, A_sf, w_codes, w_sf, bias_bits=None):
+    """NVFP4 x NVFP4: A_codes [M][K] and w_codes [N][K] E2M1 4-bit codes, A_sf [M][K/16]
+    and w_sf [N][K/16] E4M3 scale codes -> (R, absum)."""
+    a = dequant_nv(A_codes, A_sf)
+    w = dequant_nv(w_codes, w_sf)
+    r = a @ w.T
+    absum = np.abs(a) @ np.abs(w).T
+    if bias_bits is not None:
+        b = F.decode_bf16(bias_bits)
+        r = r + b[None, :]
+        absum = absum + np.abs(b)[None, :]
+    return r, absum
+
+
 # --------------------------------------------------------------- canonical-input drivers
 def w4a16_from_canonical(A_bits, w_canon, s_canon, K, bits, bias_bits=None, rows=None, cols=None):
     """Unpack canonical packed words (one expert) and run :func:`gemm_w4a16`.
@@ -107,6 +135,19 @@ def w4a8_from_canonical(A_codes, A_sf, w_canon, w_sf, K, bias_bits=None, rows=No
         bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
     codes = F.unpack_e2m1_bytes(w, K)
     return gemm_w4a8(A, Asf, codes, sf, bias_bits)
+
+
+def w4a4_from_canonical(A_packed, A_sf, w_canon, w_sf, K, bias_bits=None, rows=None, cols=None):
+    """Packed E2M1 activations [M][K/2] and weights [N][K/2] (even k in the low nibble)
+    with their E4M3 scales -> :func:`gemm_w4a4`."""
+    w, sf = np.asarray(w_canon), np.asarray(w_sf)
+    A, Asf = np.asarray(A_packed), np.asarray(A_sf)
+    if rows is not None:
+        A, Asf = A[rows], Asf[rows]
+    if cols is not None:
+        w, sf = w[cols], sf[cols]
+        bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
+    return gemm_w4a4(F.unpack_e2m1_bytes(A, K), Asf, F.unpack_e2m1_bytes(w, K), sf, bias_bits)
 
 
 # --------------------------------------------------------------- acceptance test

@@ -221,6 +221,21 @@ def w8a8_problem(M, N, K, *, E=1, cfg_id=1, seed=BASE_SEED, sf_lo=118, sf_hi=126
     return out
 
 
+def w4a4_problem(M, N, K, *, E=1, cfg_id=1, seed=BASE_SEED, sf_lo=0x28, sf_hi=0x48,
+                 bias=False):
+    """NVFP4 weights and activations: E2M1 codes uniform over the 16 codes (random
+    nibbles, even k in the low nibble) with one unsigned E4M3 scale per 16 along K, its code
+    uniform in [sf_lo, sf_hi] (0x28..0x48 = 0.125 .. 4.0)."""
+    w = random_bytes(stream(cfg_id, 23, seed), E * N * K // 2).reshape(E, N, K // 2)
+    w_sf = uniform_int(stream(cfg_id, 24, seed), (E, N, K // 16), sf_lo, sf_hi).astype(np.uint8)
+    a = random_bytes(stream(cfg_id, 25, seed), M * K // 2).reshape(M, K // 2)
+    a_sf = uniform_int(stream(cfg_id, 26, seed), (M, K // 16), sf_lo, sf_hi).astype(np.uint8)
+    out = dict(A=a, A_sf=a_sf, w_canon=w, s_canon=w_sf, E=E, N=N, K=K, M=M)
+    if bias:
+        out["bias"] = to_bf16_bits(normal(stream(cfg_id, 27, seed), (E, N)))
+    return out
+
+
 def unpack_nibbles_layout(w_canon: np.ndarray) -> np.ndarray:
     """Inverse of :func:`pack_nibbles` (a layout helper for test inputs, no decoding)."""
     lo = w_canon & 0xF
@@ -241,5 +256,6 @@ def router_logits(T, E, *, cfg_id=3, seed=BASE_SEED, bias_std=1.5):
 __all__ = [
     "BASE_SEED", "Stream", "stream", "uniform_int", "uniform", "normal", "random_bytes",
     "to_bf16_bits", "to_e4m3_codes", "pack_int4", "pack_int3", "pack_nibbles",
-    "unpack_nibbles_layout", "w4a16_problem", "w4a8_problem", "w8a8_problem", "router_logits",
+    "unpack_nibbles_layout", "w4a16_problem", "w4a8_problem", "w8a8_problem", "w4a4_problem",
+    "router_logits",
 ]

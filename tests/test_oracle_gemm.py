@@ -234,3 +234,99 @@ def test_w8a8_equals_w4a8_on_e2m1_values():
     R4, S4 = Q.gemm_w4a8(A, Asf, w4, wsf)
     R8, S8 = Q.gemm_w8a8(A, Asf, w8, wsf)
     assert np.array_equal(R4, R8) and np.array_equal(S4, S8)
+
+
+# ----------------------------------------------------------------------------- W4A4 (NVFP4)
+E4M3_ONE = 0x38  # 1.0
+E2M1_INT = {0: 0, 1: 2, 2: 4, 3: 5, 4: 6, 6: 7}  # integer magnitude -> E2M1 code
+
+
+def _e2m1_int_codes(rng, shape):
+    mags = rng.choice([0, 1, 2, 3, 4, 6], shape)
+    neg = rng.integers(0, 2, shape).astype(bool)
+    codes = np.vectorize(lambda v: E2M1_INT[int(v)])(mags).astype(np.uint8)
+    return np.where(neg, codes | 8, codes).astype(np.uint8), np.where(neg, -mags, mags)
+
+
+def test_w4a4_exact_integer_dot():
+    """Unit scales and integer-valued E2M1 codes: an exact integer dot product."""
+    rng = np.random.default_rng(41)
+    M, N, K = 3, 5, 64
+    A, ai = _e2m1_int_codes(rng, (M, K))
+    W, wi = _e2m1_int_codes(rng, (N, K))
+    R, S = Q.gemm_w4a4(A, np.full((M, K // 16), E4M3_ONE, np.uint8), W,
+                       np.full((N, K // 16), E4M3_ONE, np.uint8))
+    assert np.array_equal(R, (ai @ wi.T).astype(np.float64))
+    assert np.array_equal(S, (np.abs(ai) @ np.abs(wi).T).astype(np.float64))
+
+
+def test_w4a4_equals_w4a8_with_power_of_two_scales():
+    """E2M1 values are E4M3 values and a power-of-two E4M3 scale is an E8M0 scale: with
+    both 16-groups of every 32-group sharing one such scale, W4A4 must equal W4A8 on the
+    same values exactly."""
+    from oracle import act as OA
+    rng = np.random.default_rng(42)
+    M, N, K = 4, 6, 128
+    A4 = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    W4 = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    ea = rng.integers(-6, 8, (M, K // 32))          # exponents representable as E4M3 normals
+    ew = rng.integers(-6, 8, (N, K // 32))
+    e4m3_pow2 = lambda e: ((e + 7) << 3).astype(np.uint8)  # noqa: E731  (sign 0, mantissa 0)
+    Asf16 = np.repeat(e4m3_pow2(ea), 2, axis=1)
+    Wsf16 = np.repeat(e4m3_pow2(ew), 2, axis=1)
+    assert np.array_equal(F.decode_e4m3(Asf16), np.repeat(np.exp2(ea), 2, axis=1))
+    R4, S4 = Q.gemm_w4a4(A4, Asf16, W4, Wsf16)
+    A8 = OA.encode_e4m3(F.decode_e2m1(A4))
+    R8, S8 = Q.gemm_w4a8(A8, (ea + 127).astype(np.uint8), W4, (ew + 127).astype(np.uint8))
+    assert np.array_equal(R4, R8) and np.array_equal(S4, S8)
+
+
+def test_w4a4_fraction_brute_force_groups():
+    """Random codes and random finite E4M3 scales, exact rationals, three 16-groups."""
+    rng = np.random.default_rng(43)
+    M, N, K = 2, 3, 48
+    A = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    W = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    Asf = rng.integers(0, 0x7F, (M, K // 16)).astype(np.uint8)
+    Wsf = rng.integers(0, 0x7F, (N, K // 16)).astype(np.uint8)
+    R, absum = Q.gemm_w4a4(A, Asf, W, Wsf)
+    from test_oracle_formats import e2m1_closed_form
+    a_s = torch.from_numpy(Asf).view(torch.float8_e4m3fn).double().numpy()
+    w_s = torch.from_numpy(Wsf).view(torch.float8_e4m3fn).double().numpy()
+    for m in range(M):
+        for n in range(N):
+            ex = sum(Fraction(e2m1_closed_form(int(A[m, k]))) * Fraction(a_s[m, k // 16])
+                     * Fraction(e2m1_closed_form(int(W[n, k]))) * Fraction(w_s[n, k // 16])
+                     for k in range(K))
+            assert abs(Fraction(R[m, n]) - ex) <= Fraction(2.0 ** -50) * Fraction(absum[m, n])
+
+
+def test_w4a4_from_canonical_nibble_order():
+    """Even k in the low nibble on both operands: A row bytes [0x52] (k0 = 1.0, k1 = 3.0)
+    times W row bytes [0x74] (k0 = 2.0, k1 = 6.0) = 1*2 + 3*6."""
+    K = 16
+    A = np.zeros((1, K // 2), np.uint8)
+    A[0, 0] = 0x52
+    W = np.zeros((1, K // 2), np.uint8)
+    W[0, 0] = 0x74
+    one = np.full((1, 1), E4M3_ONE, np.uint8)
+    R, _ = Q.w4a4_from_canonical(A, one, W, one, K)
+    assert R[0, 0] == 1 * 2 + 3 * 6
+
+
+def test_w4a4_rejects_negative_and_nan_scales():
+    A = np.zeros((1, 16), np.uint8)
+    for bad in (0x80 | E4M3_ONE, 0x7F):
+        with pytest.raises(F.FormatError):
+            Q.gemm_w4a4(A, np.full((1, 1), bad, np.uint8), A, np.full((1, 1), E4M3_ONE, np.uint8))
+
+
+def test_planted_wrong_nvfp4_group_is_caught(monkeypatch):
+    orig = Q.dequant_nv
+
+    def wrong_group(codes, sf, group=16):  # each 16-group takes its neighbour's scale
+        return orig(codes, np.roll(np.asarray(sf), 1, axis=-1), group=group)
+
+    monkeypatch.setattr(Q, "dequant_nv", wrong_group)
+    with pytest.raises(AssertionError):
+        test_w4a4_fraction_brute_force_groups()
