@@ -295,6 +295,34 @@ def extra_w4a8_decode(steps, warmup, world):
     return out
 
 
+def extra_w4a4(steps, warmup, world):
+    """W4A4 (NVFP4 x NVFP4, tcgen05 kind::mxf4nvf4) on the headline's larger shape.  The
+    FP4 dense denominator is 6 x the measured BF16 burst (nominal 13.5 / 2.25 PF/s)."""
+    import moe_qw_repack_gb300.qw as Q
+    peaks, _ = measured_peaks()
+    M, N, K = 4096, 14336, 4096
+    p = synth.w4a4_problem(M, N, K, cfg_id=760)
+    d = Q.qw_repack_query(Q.QW_W_NVFP4_G16, 1, N, K)
+    wp, sp = Q.empty_packed(d)
+    Q.qw_repack(d, torch.from_numpy(p["w_canon"]).cuda(), torch.from_numpy(p["s_canon"]).cuda(),
+                wp, sp)
+    A, Asf = torch.from_numpy(p["A"]).cuda(), torch.from_numpy(p["A_sf"]).cuda()
+    step_in = d.w_bytes + d.s_bytes + A.numel() + Asf.numel()
+    R = replicas_for(step_in)
+    copies = [(wp, sp, A, Asf)] + [(wp.clone(), sp.clone(), A.clone(), Asf.clone())
+                                   for _ in range(R - 1)]
+    C = torch.empty((M, N), dtype=torch.int16, device="cuda")
+
+    def fn(i):
+        w, s, a, asf = copies[i % R]
+        Q.qgemm_dense(d, w, s, Q.QW_A_NVFP4_G16, a, asf, None, C, M, None, 0)
+    ms, n, _ = time_region([fn], steps, warmup, world)
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    return {"w4a4_nvfp4_4096x14336x4096": {"us": round(ms * 1e3, 1), "tflops": round(tf, 1),
+                                           "frac_fp4_peak": round(tf / (6 * peaks["bf16_tflops"]), 3),
+                                           "input_copies": R, "steps": n}}
+
+
 def extra_w8a8(steps, warmup, world):
     """W8A8 MX kind (MXFP8 weights x MXFP8 activations) on the headline's larger shape."""
     import moe_qw_repack_gb300.qw as Q
@@ -523,6 +551,7 @@ def run_ours(args, world, rank):
     if not args.no_extra:
         line["extra"] = extra_w4a16(max(5, min(args.steps, 200)), 3, world)
         line["extra"].update(extra_w8a8(max(5, min(args.steps, 100)), 3, world))
+        line["extra"].update(extra_w4a4(max(5, min(args.steps, 100)), 3, world))
         line["extra"].update(extra_w4a8_decode(max(5, min(args.steps, 200)), 3, world))
         line["extra"].update(extra_moe(max(5, min(args.steps, 40)), 3, world))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -66,12 +66,15 @@ typedef enum qw_wfmt {
   QW_W_INT4_G128_BF16 = 0, /* symmetric INT4 in [-7,7], BF16 scale per 128 along K      */
   QW_W_INT3_G128_BF16 = 1, /* symmetric INT3 in [-3,3], BF16 scale per 128 along K      */
   QW_W_MXFP4_G32 = 2,      /* E2M1 codes, E8M0 scale per 32 along K                      */
-  QW_W_MXFP8_G32 = 3       /* E4M3 codes, E8M0 scale per 32 along K (the W8A8 MX kind)    */
+  QW_W_MXFP8_G32 = 3,      /* E4M3 codes, E8M0 scale per 32 along K (the W8A8 MX kind)    */
+  QW_W_NVFP4_G16 = 4       /* E2M1 codes, unsigned E4M3 scale per 16 along K (W4A4)       */
 } qw_wfmt;
 
 typedef enum qw_afmt {
   QW_A_BF16 = 0,           /* BF16 [rows][K]                                          */
-  QW_A_MXFP8_G32 = 1       /* E4M3 codes [rows][K] + E8M0 scales [rows][K/32]          */
+  QW_A_MXFP8_G32 = 1,      /* E4M3 codes [rows][K] + E8M0 scales [rows][K/32]          */
+  QW_A_NVFP4_G16 = 2       /* E2M1 codes [rows][K/2] (even k in the low nibble) +
+                              unsigned E4M3 scales [rows][K/16]                            */
 } qw_afmt;
 
 /* Description of one repacked weight set (E experts; E = 1 for a dense layer).
@@ -80,7 +83,7 @@ typedef struct qw_packed_desc {
   int32_t wfmt;            /* qw_wfmt                                                  */
   int32_t E, N, K;         /* logical sizes                                            */
   int32_t N_pad, K_pad;    /* padded sizes of the packed layout                        */
-  int32_t group;           /* 128 (INT) or 32 (MXFP4)                                  */
+  int32_t group;           /* 128 (INT), 32 (MXFP4 / MXFP8) or 16 (NVFP4)              */
   int32_t reserved;
   uint64_t w_bytes;        /* size of w_packed in bytes (all experts)                  */
   uint64_t s_bytes;        /* size of s_packed in bytes (all experts)                  */
@@ -97,8 +100,9 @@ int32_t qw_version(void);
 /* --------------------------------------------------------------------------------------
  * qw_repack_query - sizes of the packed layout for E experts of an N x K weight.
  * Requirements: E >= 1, N >= 1, K >= 1; K % 128 == 0 for the INT formats, K % 32 == 0
- * for MXFP4.  Padding: INT formats pad N to a multiple of 16; MXFP4 pads N to a multiple
- * of 128 and K to a multiple of 128.  `out` is a host pointer.
+ * for MXFP4 / MXFP8 / NVFP4.  Padding: INT formats pad N to a multiple of 16; the MX
+ * formats pad N to a multiple of 128 and K to a multiple of 128 (NVFP4: 256).  `out` is a
+ * host pointer.
  * Returns QW_ERR_INVALID_ARG / QW_ERR_UNSUPPORTED on a bad request, else QW_OK.
  */
 qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_packed_desc* out);
@@ -116,6 +120,7 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *   MXFP4: w_canon uint8 [E][N][K/2], even k in the low nibble.  s_canon uint8 E8M0
  *          [E][N][K/32].
  *   MXFP8: w_canon uint8 [E][N][K] E4M3 codes.  s_canon uint8 E8M0 [E][N][K/32].
+ *   NVFP4: w_canon uint8 [E][N][K/2] as MXFP4.  s_canon uint8 E4M3 [E][N][K/16] (unsigned).
  * Packed outputs (device, sizes from `desc`, 256-byte aligned):
  *   INT4:  per expert [K/128][N_pad/16] blocks of 1 KiB: 32 lanes x 8 words; word s of
  *          lane l = 4g + t holds the eight weights lane l feeds to the s-th m16n8k16 MMA of
@@ -131,6 +136,12 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *          ((r/128) * (K_pad/128) + g/4) * 512, byte (r%32)*16 + ((r%128)/32)*4 + g%4;
  *          padding bytes are 127 (scale 1).
  *   MXFP8: codes uint8 [N_pad][K_pad] (canonical order, zero-padded); scales as MXFP4.
+ *   NVFP4: codes as MXFP4 with K_pad a multiple of 256; scales E4M3 in 2048-byte chunks per
+ *          128 rows x 16 groups (256 k), chunk (r/128, g/16) at
+ *          ((r/128) * (K_pad/256) + g/16) * 2048, byte ((g%16)/4) * 512 + (r%32)*16 +
+ *          ((r%128)/32)*4 + g%4 (four 512-byte images, one per 64-k MMA); padding bytes
+ *          are 0x38 (scale 1).  A scale with its sign bit set or the NaN code is a
+ *          value error (packed as 0x38).
  * The zero-exponent codes: the announcement's section "量子化サポート" states that a
  * symmetric INT without its minimum has the value set of a float with zero exponent
  * bits; the excess code used here is that value set shifted so that its bit pattern
@@ -164,6 +175,10 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
  * dequantization (and, for W4A8, both block scales) applied inside the kernel.
  *   W4A16: desc->wfmt INT4/INT3, afmt QW_A_BF16, A BF16 [M][K], A_sf NULL.
  *   W4A8:  desc->wfmt MXFP4,     afmt QW_A_MXFP8_G32, A E4M3 [M][K], A_sf E8M0 [M][K/32].
+ *   W8A8:  desc->wfmt MXFP8,     afmt QW_A_MXFP8_G32, as W4A8.
+ *   W4A4:  desc->wfmt NVFP4,     afmt QW_A_NVFP4_G16, A E2M1 [M][K/2], A_sf E4M3 [M][K/16]
+ *          (NVFP4 x NVFP4 on tcgen05 kind::mxf4nvf4; a per-tensor FP32 factor of the
+ *          format, if any, is the caller's to apply to C).
  *   bias:  BF16 [N] or NULL.  C: BF16 [M][N].  desc->E must be 1.
  * Dispatch by M (the device heuristic of the announcement, section "デバイスパラメータに
  * 基づくパフォーマンスチューニング"): W4A16 with M <= 16 streams the weights through a
@@ -215,8 +230,8 @@ qw_status qgemm_moe_route_noalloc(const float* logits, int32_t T, int32_t E, int
 /* --------------------------------------------------------------------------------------
  * qgemm_moe_permute - gather activation rows into the expert-contiguous order:
  *   A_sorted[r] = A[sorted_pairs[r] / topk] for r < P (and the same for A_sf rows when
- *   afmt is QW_A_MXFP8_G32; A_sf / A_sf_sorted are NULL for BF16).
- *   A: [T][K] in afmt; A_sorted: [P][K].  Rows are 16-byte aligned (K*elem % 16 == 0).
+ *   afmt is QW_A_MXFP8_G32 or QW_A_NVFP4_G16; A_sf / A_sf_sorted are NULL for BF16).
+ *   A: [T][K] in afmt; A_sorted: [P][K].  Rows are 16-byte multiples (2K, K or K/2 bytes).
  */
 qw_status qgemm_moe_permute(int32_t afmt, const void* A, const void* A_sf, int32_t K,
                             const int32_t* sorted_pairs, int64_t P, int32_t topk,

@@ -1,6 +1,8 @@
 // gemm_w4a8_tc.cu - large-M W4A8 path: MXFP4 weights x MXFP8 activations on the
-// sm_103a block-scaled tensor cores (and the W8A8 MX kind: MXFP8 weights, the same kernel
-// with E4M3 as the B type).
+// sm_103a block-scaled tensor cores, and on the same skeleton the W8A8 MX kind (MXFP8
+// weights: E4M3 as the B type) and W4A4 (NVFP4 x NVFP4: tcgen05 kind::mxf4nvf4 with
+// scale_vec::4X - both operands packed E2M1 in shared memory, 256 k per stage, an
+// unsigned E4M3 scale per 16 k, four scale images per stage instead of one).
 //
 // What it computes (aireiter.com "vLLM Humming performance benchmark", section "H100
 // group-32 W4A8": MXFP4 weights, MXFP8 activations, group-32 scales; spke.com Humming
@@ -45,31 +47,69 @@
 namespace qw {
 namespace {
 
+// BK = bytes of a row per stage (128: one 128-byte swizzle atom)
 constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
-constexpr int A_BYTES = BM * BK;  // E4M3, one byte per element
-// B in shared memory is one byte per element either way: E4M3 codes as they are, or E2M1
-// codes unpacked by TMA (16 codes in 8 bytes + 8 gap bytes)
+constexpr int A_BYTES = BM * BK;
+// B in shared memory: E4M3 codes as they are, E2M1 codes unpacked by TMA to one byte each
+// (W4A8: 16 codes in 8 bytes + 8 gap bytes), or packed E2M1 (W4A4)
 constexpr int B_BYTES = BN * BK;
-// bytes a B load credits to the barrier: the packed global bytes
-template <bool W8>
-__host__ __device__ constexpr int b_tx_bytes() { return W8 ? BN * BK : BN * BK / 2; }
-constexpr int SFA_BYTES = 512, SFB_CHUNK = 512, SFB_BYTES = 2 * SFB_CHUNK;
 constexpr int NUM_WARPS = 12, NUM_THREADS = NUM_WARPS * 32;
 constexpr int EPI_WARP0 = 4, NUM_EPI_WARPS = 8;
-constexpr int SF_STAGING = 8;  // staged A scale images (512 B each)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t SF_COL0 = 256;      // accumulator uses columns [0, 256)
-constexpr uint32_t SF_COLS_PER_STAGE = 12;  // 4 (A: 128 rows) + 8 (B: 256 rows)
-constexpr size_t SMEM_BYTES = (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) +
-                              (size_t)SF_STAGING * SFA_BYTES + BM * 4 + 512 + 1024;
+constexpr uint32_t SF_COL0 = 256;  // accumulator uses columns [0, 256)
 
-// Instruction descriptor, kind::mxf8f6f4: A = E4M3 (0), B = E2M1 (5) or E4M3 (0), both
-// K-major, N >> 3 at bit 17, scale type UE8M0 (bit 23), M >> 4 at bit 24; the B / A scale
-// factor byte selectors sit at bits 4 and 29.
-template <bool W8>
+enum Kind { kW4A8 = 0, kW8A8 = 1, kW4A4 = 2 };
+
+// Per-kind constants.  A scale image is the 32 x 16-byte block tcgen05.cp.32x128b.warpx4
+// copies for 128 rows (row r -> lane r % 32, column (r % 128) / 32, four scale bytes):
+// one image covers a stage's four 32-k groups (1X, E8M0) or one 64-k MMA's four 16-k groups
+// (4X, E4M3).
+template <int KIND>
+struct KT {
+  static constexpr bool NV = KIND == kW4A4;
+  static constexpr int IMG = NV ? 4 : 1;        // scale images per 128 rows and stage
+  static constexpr int KSTEP = NV ? 256 : 128;  // K elements per stage
+  static constexpr int GROUP = NV ? 16 : 32;    // K elements per scale
+  // bytes a B load credits to its barrier: the global bytes
+  static constexpr int B_TX = KIND == kW8A8 ? BN * BK : (KIND == kW4A8 ? BN * BK / 2 : BN * BK);
+  static constexpr int SFA_BYTES = 512 * IMG;
+  static constexpr int SFB_CHUNK = 512 * IMG;  // 128 B rows
+  static constexpr int SFB_BYTES = 2 * SFB_CHUNK;
+  static constexpr uint32_t SF_COLS_PER_STAGE = 12 * IMG;  // A: 4 per image, B: 8 per image
+  static constexpr int SF_STAGING = NV ? 4 : 8;            // staged A scale slots
+  static constexpr uint32_t SF_PAD = NV ? 0x38383838u : 0x7F7F7F7Fu;  // scale 1
+  static constexpr size_t SMEM_BYTES =
+      (size_t)STAGES * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) +
+      (size_t)SF_STAGING * SFA_BYTES + BM * 4 + 512 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+// Instruction descriptor.  kind::mxf8f6f4: A = E4M3 (0), B = E2M1 (5) or E4M3 (0), scale
+// type UE8M0 (bit 23 set); kind::mxf4nvf4: A = B = E2M1 (1), scale type UE4M3 (bit 23
+// clear).  Both K-major, N >> 3 at bit 17, M >> 4 at bit 24; the B / A scale-factor byte
+// selectors sit at bits 4 and 29 (1X only; 4X reads a whole 32-bit column per MMA).
+template <int KIND>
 __host__ __device__ constexpr uint32_t idesc() {
-  return (0u << 7) | ((W8 ? 0u : 5u) << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
-         ((uint32_t)(BM >> 4) << 24);
+  return KIND == kW4A4
+             ? ((1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                ((uint32_t)(BM >> 4) << 24))
+             : ((0u << 7) | ((KIND == kW8A8 ? 0u : 5u) << 10) | ((uint32_t)(BN >> 3) << 17) |
+                (1u << 23) | ((uint32_t)(BM >> 4) << 24));
+}
+
+// D(tmem) (+)= A x B^T, both packed E2M1 in shared memory, a UE4M3 scale per 16 k read from
+// TMEM (four per row and MMA).
+__device__ __forceinline__ void tc_mma_mxf4nvf4_4x(uint32_t d_tmem, uint64_t a_desc,
+                                                   uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
 }
 
 struct Params {
@@ -113,15 +153,19 @@ __device__ __forceinline__ Tile tile_at(const Params& p, int64_t t) {
   return x;
 }
 
-// Scales of activation row `ar` (an act_row result, or -1 past the problem) for K step kb.
-__device__ __forceinline__ uint32_t load_sf_word(const Params& p, int64_t ar, int kb) {
-  const int G = p.K / 32;  // canonical groups per row
-  const int g0 = kb * 4;
-  if (ar < 0) return 0x7F7F7F7Fu;
+// Scale word i of activation row `ar` (an act_row result, or -1 past the problem) for K
+// step kb: the four scale bytes of groups 4 (IMG kb + i) .. + 3, padded with scale 1.
+template <int KIND>
+__device__ __forceinline__ uint32_t load_sf_word(const Params& p, int64_t ar, int kb, int i) {
+  using T = KT<KIND>;
+  const int G = p.K / T::GROUP;  // canonical groups per row
+  const int g0 = (kb * T::IMG + i) * 4;
+  if (ar < 0) return T::SF_PAD;
   const uint8_t* row = p.A_sf + ar * (int64_t)G;
   if ((G & 3) == 0 && g0 + 3 < G) return __ldg(reinterpret_cast<const uint32_t*>(row + g0));
   uint32_t w = 0;
-  for (int j = 0; j < 4; ++j) w |= (uint32_t)(g0 + j < G ? __ldg(row + g0 + j) : 127) << (8 * j);
+  for (int j = 0; j < 4; ++j)
+    w |= (uint32_t)(g0 + j < G ? __ldg(row + g0 + j) : (T::SF_PAD & 0xFFu)) << (8 * j);
   return w;
 }
 
@@ -158,10 +202,13 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) break;
 }
 
-template <bool W8>
+template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a8_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using T = KT<KIND>;
+  constexpr int SFA_BYTES = T::SFA_BYTES, SFB_BYTES = T::SFB_BYTES, SFB_CHUNK = T::SFB_CHUNK;
+  constexpr int SF_STAGING = T::SF_STAGING, IMG = T::IMG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -212,7 +259,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int64_t num_m = p.queue ? (int64_t)__ldg(p.queue) : (int64_t)p.num_m_tiles;
   const int64_t num_tiles = num_m * p.num_n_tiles;
-  const int KB = p.K_pad / BK;
+  const int KB = p.K_pad / T::KSTEP;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -251,7 +298,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], a_tx + b_tx_bytes<W8>() + nchunks * SFB_CHUNK);
+          mbar_arrive_expect_tx(&full[stage], a_tx + T::B_TX + nchunks * SFB_CHUNK);
           if (p.gather) {
             for (int i = 0; i < ngather; ++i)
               tma_gather4(sA + stage * A_BYTES + i * 4 * BK, &tmA, &full[stage], kb * BK,
@@ -294,20 +341,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sfa_col = tbase + SF_COL0 + stage * SF_COLS_PER_STAGE;
-          const uint32_t sfb_col = sfa_col + 4;
-          tc_cp_32x128b_warpx4(sfa_col, smem_desc(smem_u32(sSFA + stage * SFA_BYTES), 0, 128, 0));
-          tc_cp_32x128b_warpx4(sfb_col, smem_desc(smem_u32(sSFB + stage * SFB_BYTES), 0, 128, 0));
-          tc_cp_32x128b_warpx4(sfb_col + 4, smem_desc(smem_u32(sSFB + stage * SFB_BYTES + SFB_CHUNK),
-                                                      0, 128, 0));
+          // scale images into TMEM: image i of A at columns sfa + 4i, image i of B's two
+          // 128-row chunks at sfb + 8i and sfb + 8i + 4 (1X: one image per stage, read by
+          // byte selector; 4X: one image per MMA)
+          const uint32_t sfa_col = tbase + SF_COL0 + stage * T::SF_COLS_PER_STAGE;
+          const uint32_t sfb_col = sfa_col + 4 * IMG;
+#pragma unroll
+          for (int i = 0; i < IMG; ++i) {
+            tc_cp_32x128b_warpx4(sfa_col + 4 * i,
+                                 smem_desc(smem_u32(sSFA + stage * SFA_BYTES + i * 512), 0, 128, 0));
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              tc_cp_32x128b_warpx4(
+                  sfb_col + 8 * i + 4 * c,
+                  smem_desc(smem_u32(sSFB + stage * SFB_BYTES + c * SFB_CHUNK + i * 512), 0, 128, 0));
+          }
           const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
           const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk) {
+          for (int kk = 0; kk < BK / 32; ++kk) {  // 32 bytes of each row per MMA
             const uint64_t ad = smem_desc(a0 + kk * 32, 16, 1024, 2);
             const uint64_t bd = smem_desc(b0 + kk * 32, 16, 1024, 2);
-            const uint32_t id = idesc<W8>() | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
-            tc_mma_mxf8f6f4(tbase, ad, bd, id, sfa_col, sfb_col, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (T::NV) {
+              tc_mma_mxf4nvf4_4x(tbase, ad, bd, idesc<KIND>(), sfa_col + 4 * kk, sfb_col + 8 * kk,
+                                 (kb | kk) != 0 ? 1u : 0u);
+            } else {
+              const uint32_t id = idesc<KIND>() | ((uint32_t)kk << 4) | ((uint32_t)kk << 29);
+              tc_mma_mxf8f6f4(tbase, ad, bd, id, sfa_col, sfb_col, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -339,22 +400,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     };
     if (lt < num_tiles) rows_of(lt);
+    // one ring entry: image i, word j = scales of row 32 j + lane for the stage
+    struct Entry {
+      uint4 v[IMG];
+    };
     auto load_next = [&]() {
-      uint4 v = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      Entry e;
+#pragma unroll
+      for (int i = 0; i < IMG; ++i) e.v[i] = make_uint4(T::SF_PAD, T::SF_PAD, T::SF_PAD, T::SF_PAD);
       if (lt < num_tiles) {
-        v.x = load_sf_word(p, ar[0], lkb);
-        v.y = load_sf_word(p, ar[1], lkb);
-        v.z = load_sf_word(p, ar[2], lkb);
-        v.w = load_sf_word(p, ar[3], lkb);
+#pragma unroll
+        for (int i = 0; i < IMG; ++i) {
+          e.v[i].x = load_sf_word<KIND>(p, ar[0], lkb, i);
+          e.v[i].y = load_sf_word<KIND>(p, ar[1], lkb, i);
+          e.v[i].z = load_sf_word<KIND>(p, ar[2], lkb, i);
+          e.v[i].w = load_sf_word<KIND>(p, ar[3], lkb, i);
+        }
         if (++lkb == KB) {
           lkb = 0;
           lt += gridDim.x;
           if (lt < num_tiles) rows_of(lt);
         }
       }
-      return v;
+      return e;
     };
-    uint4 ring[AHEAD];
+    Entry ring[AHEAD];
 #pragma unroll
     for (int i = 0; i < AHEAD; ++i) ring[i] = load_next();
     int slot = 0;
@@ -366,7 +436,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
-        *reinterpret_cast<uint4*>(sStage + slot * SFA_BYTES + lane * 16) = ring[0];
+#pragma unroll
+        for (int i = 0; i < IMG; ++i)
+          *reinterpret_cast<uint4*>(sStage + slot * SFA_BYTES + i * 512 + lane * 16) = ring[0].v[i];
         mbar_arrive(&sfull[slot]);
 #pragma unroll
         for (int i = 0; i + 1 < AHEAD; ++i) ring[i] = ring[i + 1];
@@ -389,8 +461,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
-        const uint4 v = *reinterpret_cast<const uint4*>(sStage + slot * SFA_BYTES + lane * 16);
-        *reinterpret_cast<uint4*>(sSFA + stage * SFA_BYTES + lane * 16) = v;
+#pragma unroll
+        for (int i = 0; i < IMG; ++i) {
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(sStage + slot * SFA_BYTES + i * 512 + lane * 16);
+          *reinterpret_cast<uint4*>(sSFA + stage * SFA_BYTES + i * 512 + lane * 16) = v;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sempty[slot]);
         fence_proxy_async_smem();  // only shared-memory accesses are outstanding here
@@ -503,14 +579,16 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   if (!enc) return QW_ERR_CUDA;
   if (rs.rows > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
   const bool w8 = d.wfmt == QW_W_MXFP8_G32;
+  const bool nv = d.wfmt == QW_W_NVFP4_G16;  // packed E2M1 activations: K / 2 bytes per row
+  const int64_t a_row_bytes = nv ? d.K / 2 : d.K;
 
   CUtensorMap tmA, tmB;
   {
     // indexed calls read the unpermuted activations one row per box (gather4 copies)
     const bool gather = rs.gather != nullptr;
     if (gather && (rs.a_rows < 1 || rs.a_rows > 0x7FFFFFFFLL)) return QW_ERR_UNSUPPORTED;
-    cuuint64_t gdim[2] = {(cuuint64_t)d.K, (cuuint64_t)(gather ? rs.a_rows : rs.rows)};
-    cuuint64_t gstr[1] = {(cuuint64_t)d.K};
+    cuuint64_t gdim[2] = {(cuuint64_t)a_row_bytes, (cuuint64_t)(gather ? rs.a_rows : rs.rows)};
+    cuuint64_t gstr[1] = {(cuuint64_t)a_row_bytes};
     cuuint32_t box[2] = {(cuuint32_t)BK, gather ? 1u : (cuuint32_t)BM};
     cuuint32_t es[2] = {1, 1};
     if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(A), gdim, gstr, box, es,
@@ -519,11 +597,15 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
       return QW_ERR_ALIGNMENT;
   }
   {
-    cuuint64_t gdim[2] = {(cuuint64_t)d.K_pad, (cuuint64_t)d.E * (cuuint64_t)d.N_pad};
+    // W4A8: E2M1 codes unpacked by TMA (K_pad elements per row); W8A8: E4M3 bytes;
+    // W4A4: packed E2M1 bytes (K_pad / 2 per row)
+    cuuint64_t gdim[2] = {(cuuint64_t)(nv ? d.K_pad / 2 : d.K_pad),
+                          (cuuint64_t)d.E * (cuuint64_t)d.N_pad};
     cuuint64_t gstr[1] = {(cuuint64_t)(w8 ? d.K_pad : d.K_pad / 2)};
     cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
     cuuint32_t es[2] = {1, 1};
-    if (enc(&tmB, w8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2,
+    if (enc(&tmB,
+            (w8 || nv) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2,
             const_cast<void*>(w_packed), gdim,
             gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -562,11 +644,17 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_w4a8_kernel<false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    attr_err = cudaFuncSetAttribute(gemm_w4a8_kernel<kW4A8>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)KT<kW4A8>::SMEM_BYTES);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(gemm_w4a8_kernel<true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+      attr_err = cudaFuncSetAttribute(gemm_w4a8_kernel<kW8A8>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)KT<kW8A8>::SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(gemm_w4a8_kernel<kW4A4>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)KT<kW4A4>::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return QW_ERR_CUDA;
 
@@ -574,9 +662,11 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   const int sms = device_sm_count();
   const unsigned grid = (unsigned)(tiles_max < sms ? (tiles_max < 1 ? 1 : tiles_max) : sms);
   if (w8)
-    gemm_w4a8_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+    gemm_w4a8_kernel<kW8A8><<<grid, NUM_THREADS, KT<kW8A8>::SMEM_BYTES, st>>>(tmA, tmB, p);
+  else if (nv)
+    gemm_w4a8_kernel<kW4A4><<<grid, NUM_THREADS, KT<kW4A4>::SMEM_BYTES, st>>>(tmA, tmB, p);
   else
-    gemm_w4a8_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+    gemm_w4a8_kernel<kW4A8><<<grid, NUM_THREADS, KT<kW4A8>::SMEM_BYTES, st>>>(tmA, tmB, p);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 

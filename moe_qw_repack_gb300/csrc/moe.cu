@@ -292,12 +292,13 @@ qw_status launch_moe_permute(int32_t afmt, const void* A, const void* A_sf, int3
                              const int32_t* sorted_pairs, int64_t P, int32_t topk,
                              void* A_sorted, void* A_sf_sorted, cudaStream_t st) {
   if (P == 0) return QW_OK;
-  const int64_t row_bytes = (int64_t)K * (afmt == QW_A_BF16 ? 2 : 1);
+  const int64_t row_bytes =
+      afmt == QW_A_BF16 ? 2 * (int64_t)K : (afmt == QW_A_NVFP4_G16 ? K / 2 : (int64_t)K);
   const int64_t vecs = row_bytes / 16;
   permute_rows_kernel<<<grid_cap(P * vecs, 256), 256, 0, st>>>(
       (const uint4*)A, (uint4*)A_sorted, vecs, sorted_pairs, P, topk);
-  if (afmt == QW_A_MXFP8_G32) {
-    const int64_t sb = K / 32;
+  if (afmt != QW_A_BF16) {
+    const int64_t sb = K / (afmt == QW_A_NVFP4_G16 ? 16 : 32);  // scale bytes per row
     permute_bytes_kernel<<<grid_cap(P * sb, 256), 256, 0, st>>>(
         (const uint8_t*)A_sf, (uint8_t*)A_sf_sorted, sb, sorted_pairs, P, topk);
   }

@@ -32,7 +32,10 @@ namespace {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // block-scaled MX weight formats (E8M0 scale per 32 along K, tcgen05 block-scaled MMA)
-bool is_mx(int32_t wfmt) { return wfmt == QW_W_MXFP4_G32 || wfmt == QW_W_MXFP8_G32; }
+// block-scaled formats: the tcgen05 kind::mxf8f6f4 / kind::mxf4nvf4 GEMM
+bool is_mx(int32_t wfmt) {
+  return wfmt == QW_W_MXFP4_G32 || wfmt == QW_W_MXFP8_G32 || wfmt == QW_W_NVFP4_G16;
+}
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
@@ -48,7 +51,8 @@ qw_status check_desc(const qw_packed_desc* d) {
 
 qw_status check_afmt(const qw_packed_desc* d, int32_t afmt, const void* A_sf) {
   if (is_mx(d->wfmt)) {
-    if (afmt != QW_A_MXFP8_G32) return QW_ERR_UNSUPPORTED;
+    if (afmt != (d->wfmt == QW_W_NVFP4_G16 ? QW_A_NVFP4_G16 : QW_A_MXFP8_G32))
+      return QW_ERR_UNSUPPORTED;
     if (!A_sf) return QW_ERR_INVALID_ARG;
   } else {
     if (afmt != QW_A_BF16) return QW_ERR_UNSUPPORTED;
@@ -108,6 +112,15 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
       d.w_expert_stride =
           (uint64_t)d.N_pad * (wfmt == QW_W_MXFP4_G32 ? d.K_pad / 2 : d.K_pad);
       d.s_expert_stride = (uint64_t)(d.N_pad / 128) * (d.K_pad / 128) * kSfChunkBytes;
+      break;
+    }
+    case QW_W_NVFP4_G16: {
+      if (K % 32) return QW_ERR_UNSUPPORTED;  // packed rows of 16-byte multiples
+      d.group = kNvGroup;
+      d.N_pad = (int32_t)round_up(N, 128);
+      d.K_pad = (int32_t)round_up(K, 256);
+      d.w_expert_stride = (uint64_t)d.N_pad * (d.K_pad / 2);
+      d.s_expert_stride = (uint64_t)(d.N_pad / 128) * (d.K_pad / 256) * kNvChunkBytes;
       break;
     }
     default:
@@ -171,7 +184,8 @@ static qw_status check_gemm_args(const qw_packed_desc* desc, const void* w_packe
   if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
   if (!aligned(A, 16) || !aligned(C, 4)) return QW_ERR_ALIGNMENT;
   if (is_mx(desc->wfmt)) {
-    if (desc->K % 16) return QW_ERR_ALIGNMENT;  // TMA row pitch of the E4M3 activations
+    // TMA row pitch of the activations: K bytes (E4M3) or K/2 bytes (E2M1), 16-byte multiple
+    if (desc->K % (desc->wfmt == QW_W_NVFP4_G16 ? 32 : 16)) return QW_ERR_ALIGNMENT;
     if (!aligned(A_sf, 4)) return QW_ERR_ALIGNMENT;
   } else if (desc->K % 8) {
     return QW_ERR_ALIGNMENT;
@@ -227,15 +241,18 @@ qw_status qgemm_moe_route(const float* logits, int32_t T, int32_t E, int32_t top
 qw_status qgemm_moe_permute(int32_t afmt, const void* A, const void* A_sf, int32_t K,
                             const int32_t* sorted_pairs, int64_t P, int32_t topk, void* A_sorted,
                             void* A_sf_sorted, void* stream) {
-  if (afmt != QW_A_BF16 && afmt != QW_A_MXFP8_G32) return QW_ERR_UNSUPPORTED;
+  if (afmt != QW_A_BF16 && afmt != QW_A_MXFP8_G32 && afmt != QW_A_NVFP4_G16)
+    return QW_ERR_UNSUPPORTED;
   if (K < 1 || P < 0 || topk < 1) return QW_ERR_INVALID_ARG;
   if (P == 0) return QW_OK;
   if (!A || !sorted_pairs || !A_sorted) return QW_ERR_INVALID_ARG;
-  const int64_t row_bytes = (int64_t)K * (afmt == QW_A_BF16 ? 2 : 1);
+  if (afmt == QW_A_NVFP4_G16 && K % 2) return QW_ERR_UNSUPPORTED;
+  const int64_t row_bytes =
+      afmt == QW_A_BF16 ? 2 * (int64_t)K : (afmt == QW_A_NVFP4_G16 ? K / 2 : (int64_t)K);
   if (row_bytes % 16 || !aligned(A, 16) || !aligned(A_sorted, 16) || !aligned(sorted_pairs, 4))
     return QW_ERR_ALIGNMENT;
-  if (afmt == QW_A_MXFP8_G32) {
-    if (K % 32) return QW_ERR_UNSUPPORTED;
+  if (afmt != QW_A_BF16) {
+    if (K % (afmt == QW_A_NVFP4_G16 ? 16 : 32)) return QW_ERR_UNSUPPORTED;
     if (!A_sf || !A_sf_sorted) return QW_ERR_INVALID_ARG;
   }
   return launch_moe_permute(afmt, A, A_sf, K, sorted_pairs, P, topk, A_sorted, A_sf_sorted,

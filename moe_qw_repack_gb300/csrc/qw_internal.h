@@ -17,6 +17,8 @@ constexpr int kMxGroup = 32;         // K elements per E8M0 scale (MX formats)
 constexpr int kInt4BlockBytes = 1024;  // 16 rows x 128 k of INT4, fragment order
 constexpr int kInt3BlockBytes = 768;   // 16 rows x 128 k of INT3 (two bit planes)
 constexpr int kSfChunkBytes = 512;     // 128 rows x 4 groups of E8M0 scales
+constexpr int kNvGroup = 16;           // K elements per E4M3 scale (NVFP4)
+constexpr int kNvChunkBytes = 2048;    // 128 rows x 16 groups of E4M3 scales (NVFP4)
 
 qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void* s_canon,
                         void* w_packed, void* s_packed, int32_t* err, cudaStream_t st);

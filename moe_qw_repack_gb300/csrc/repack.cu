@@ -333,6 +333,54 @@ __global__ void unpack_mx_scales_kernel(const uint8_t* __restrict__ sp, uint8_t*
   }
 }
 
+// ----------------------------------------------------------------------------- NVFP4
+// Offset of scale (row r, group g of 16) in the 128-row x 16-group chunked layout of one
+// expert: four 512-byte images per chunk, one per 64-k MMA, each in the image layout of
+// the E8M0 chunks (lane r % 32, column (r % 128) / 32, byte g % 4).
+__device__ __forceinline__ int64_t nv_sf_offset(int64_t r, int g, int K_pad) {
+  return ((r / 128) * (K_pad / 256) + g / 16) * 2048 + ((g % 16) / 4) * 512 + (r % 32) * 16 +
+         ((r % 128) / 32) * 4 + g % 4;
+}
+
+__global__ void repack_nv_scales_kernel(const uint8_t* __restrict__ sc, uint8_t* __restrict__ sp,
+                                        int32_t E, int32_t N, int32_t N_pad, int32_t K,
+                                        int32_t K_pad, int32_t* err) {
+  const int Gp = K_pad / 16, Gc = K / 16;
+  const int64_t per_expert = (int64_t)N_pad * Gp;
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t r = rem / Gp;
+    const int g = (int)(rem % Gp);
+    uint8_t v = 0x38;  // scale 1 for padding
+    if (r < N && g < Gc) {
+      v = sc[(e * N + r) * Gc + g];
+      if ((v & 0x80) || v == 0x7F) {  // unsigned scale: no sign, no NaN
+        set_error(err, QW_ERR_VALUE);
+        v = 0x38;
+      }
+    }
+    sp[e * per_expert + nv_sf_offset(r, g, K_pad)] = v;
+  }
+}
+
+__global__ void unpack_nv_scales_kernel(const uint8_t* __restrict__ sp, uint8_t* __restrict__ sc,
+                                        int32_t E, int32_t N, int32_t N_pad, int32_t K,
+                                        int32_t K_pad) {
+  const int Gp = K_pad / 16, Gc = K / 16;
+  const int64_t total = (int64_t)E * N * Gc;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / ((int64_t)N * Gc);
+    const int64_t rem = idx % ((int64_t)N * Gc);
+    const int64_t r = rem / Gc;
+    const int g = (int)(rem % Gc);
+    sc[idx] = sp[e * (int64_t)N_pad * Gp + nv_sf_offset(r, g, K_pad)];
+  }
+}
+
 int grid_for(int64_t total, int threads) {
   int64_t b = (total + threads - 1) / threads;
   const int64_t cap = (int64_t)device_sm_count() * 32;
@@ -376,10 +424,19 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
           (const uint8_t*)s_canon, (uint8_t*)s_packed, d.E, d.N, d.N_pad, d.K, d.K_pad, err);
       break;
     }
+    case QW_W_NVFP4_G16: {
+      const int64_t tw = (int64_t)d.E * d.N_pad * (d.K_pad / 8);
+      repack_mxfp4_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
+          (const uint8_t*)w_canon, (uint8_t*)w_packed, d.E, d.N, d.N_pad, d.K, d.K_pad);
+      const int64_t ts = (int64_t)d.E * d.N_pad * (d.K_pad / 16);
+      repack_nv_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
+          (const uint8_t*)s_canon, (uint8_t*)s_packed, d.E, d.N, d.N_pad, d.K, d.K_pad, err);
+      break;
+    }
     default:
       return QW_ERR_UNSUPPORTED;
   }
-  if (d.wfmt != QW_W_MXFP4_G32 && d.wfmt != QW_W_MXFP8_G32) {
+  if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16) {
     const int64_t ts = (int64_t)d.E * (d.K / 128) * d.N_pad;
     repack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
         (const uint16_t*)s_canon, (uint16_t*)s_packed, d.E, d.N, d.N_pad, d.K / 128);
@@ -422,10 +479,19 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
           (const uint8_t*)s_packed, (uint8_t*)s_canon, d.E, d.N, d.N_pad, d.K, d.K_pad);
       break;
     }
+    case QW_W_NVFP4_G16: {
+      const int64_t tw = (int64_t)d.E * d.N * (d.K / 2);
+      unpack_mxfp4_codes_kernel<<<grid_for(tw, T), T, 0, st>>>(
+          (const uint8_t*)w_packed, (uint8_t*)w_canon, d.E, d.N, d.N_pad, d.K, d.K_pad);
+      const int64_t ts = (int64_t)d.E * d.N * (d.K / 16);
+      unpack_nv_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
+          (const uint8_t*)s_packed, (uint8_t*)s_canon, d.E, d.N, d.N_pad, d.K, d.K_pad);
+      break;
+    }
     default:
       return QW_ERR_UNSUPPORTED;
   }
-  if (d.wfmt != QW_W_MXFP4_G32 && d.wfmt != QW_W_MXFP8_G32) {
+  if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16) {
     const int64_t ts = (int64_t)d.E * d.N * (d.K / 128);
     unpack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
         (const uint16_t*)s_packed, (uint16_t*)s_canon, d.E, d.N, d.N_pad, d.K / 128);
