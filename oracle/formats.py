@@ -82,6 +82,27 @@ def unpack_int4(words, K: int) -> np.ndarray:
     return out
 
 
+def unpack_uint4(words, K: int) -> np.ndarray:
+    """uint32 [..., K/8] -> int16 [..., K] in [0, 15]; element k = 8j + i at bits
+    [4i, 4i + 4) of word j (the INT4 packing, read unsigned)."""
+    w = np.asarray(words).astype(np.uint32)
+    assert w.shape[-1] * 8 == K
+    out = np.empty((*w.shape[:-1], K), dtype=np.int16)
+    for i in range(8):
+        out[..., i::8] = ((w >> np.uint32(4 * i)) & np.uint32(0xF)).astype(np.int16)
+    return out
+
+
+def split_zp_scales(words):
+    """Asymmetric INT4 group words uint32 [..., G]: bits 0-15 the BF16 scale, bits 16-23
+    the zero point (0..15), bits 24-31 zero -> (scale BF16 bits uint16, zero point int16)."""
+    w = np.asarray(words).astype(np.uint32)
+    z = ((w >> np.uint32(16)) & np.uint32(0xFF)).astype(np.int16)
+    if np.any((w >> np.uint32(24)) != 0) or np.any(z > 15):
+        raise FormatError("zero point outside [0, 15]")
+    return (w & np.uint32(0xFFFF)).astype(np.uint16), z
+
+
 def unpack_int3(words, K: int) -> np.ndarray:
     """uint32 [..., K/32, 3] -> int8 [..., K]; element i of each 32-block at stream
     bits [3i, 3i+3) of the 96-bit little-endian stream (word 0 = bits 0..31);

@@ -7,6 +7,9 @@ output stage; section "WnA16": low-bit weights times 16-bit activations; section
 "W8A8 / W4A8 / W4A4": MX block-scaled weights and activations):
 
   W4A16:  R[m,n] = sum_k a[m,k] * q[n,k] * s[n, k // G]            (+ bias[n])
+  W4A16 with zero points (asymmetric INT4, the section "背景"'s symmetric / asymmetric
+  quantization): R[m,n] = sum_k a[m,k] * (q[n,k] - z[n, k // G]) * s[n, k // G],
+          q and z unsigned 4-bit                                    (+ bias[n])
   W4A8:   R[m,n] = sum_k e4m3(a[m,k]) 2^(sa[m,k//32]-127)
                           * e2m1(w[n,k]) 2^(sw[n,k//32]-127)      (+ bias[n])
   W4A4:   R[m,n] = sum_k e2m1(a[m,k]) e4m3(sa[m,k//16])
@@ -55,6 +58,13 @@ def gemm_w4a16(A_bits, q, s_bits, bias_bits=None, group: int = 128):
         r = r + b[None, :]
         absum = absum + np.abs(b)[None, :]
     return r, absum
+
+
+def gemm_w4a16_zp(A_bits, q, s_bits, z, bias_bits=None, group: int = 128):
+    """A_bits [M][K] BF16, q [N][K] unsigned codes, s_bits [N][K/group] BF16 scales, z
+    [N][K/group] zero points -> (R, absum) of w = s * (q - z)."""
+    qz = np.asarray(q).astype(np.int64) - np.repeat(np.asarray(z).astype(np.int64), group, axis=-1)
+    return gemm_w4a16(A_bits, qz, s_bits, bias_bits, group)
 
 
 def gemm_w4a8(A_codes, A_sf, w_codes, w_sf, bias_bits=None):
@@ -122,6 +132,21 @@ def w4a16_from_canonical(A_bits, w_canon, s_canon, K, bits, bias_bits=None, rows
         q, s = q[cols], s[cols]
         bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
     return gemm_w4a16(A, q, s, bias_bits)
+
+
+def w4a16_zp_from_canonical(A_bits, w_canon, sz_canon, K, bias_bits=None, rows=None,
+                            cols=None):
+    """Unsigned INT4 words and (scale, zero point) group words of one expert ->
+    :func:`gemm_w4a16_zp`."""
+    q = F.unpack_uint4(w_canon, K)
+    s, z = F.split_zp_scales(sz_canon)
+    A = np.asarray(A_bits)
+    if rows is not None:
+        A = A[rows]
+    if cols is not None:
+        q, s, z = q[cols], s[cols], z[cols]
+        bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
+    return gemm_w4a16_zp(A, q, s, z, bias_bits)
 
 
 def w4a8_from_canonical(A_codes, A_sf, w_canon, w_sf, K, bias_bits=None, rows=None, cols=None):

@@ -191,6 +191,23 @@ def w4a16_problem(M, N, K, *, bits=4, E=1, cfg_id=0, seed=BASE_SEED,
     return out
 
 
+def w4a16_zp_problem(M, N, K, *, E=1, cfg_id=0, seed=BASE_SEED, scale_lo=0.005,
+                     scale_hi=0.02, bias=False):
+    """Group-128 asymmetric INT4 weights: unsigned codes uniform in [0, 15], a BF16 scale
+    U[scale_lo, scale_hi] and a zero point uniform in [0, 15] per group, packed as
+    uint32 group words (scale bits 0-15, zero point bits 16-23); BF16 N(0,1) activations."""
+    q = uniform_int(stream(cfg_id, 30, seed), (E, N, K), 0, 15).astype(np.uint8)
+    s = to_bf16_bits(uniform(stream(cfg_id, 31, seed), (E, N, K // 128), scale_lo, scale_hi))
+    z = uniform_int(stream(cfg_id, 32, seed), (E, N, K // 128), 0, 15).astype(np.uint32)
+    a = to_bf16_bits(normal(stream(cfg_id, 33, seed), (M, K)))
+    w = np.ascontiguousarray(pack_nibbles(q)).view("<u4").astype(np.uint32, copy=False)
+    sz = (s.astype(np.uint32) | (z << np.uint32(16))).astype(np.uint32)
+    out = dict(A=a, w_canon=w, s_canon=sz, E=E, N=N, K=K, M=M, bits=4, zp=True)
+    if bias:
+        out["bias"] = to_bf16_bits(normal(stream(cfg_id, 34, seed), (E, N)))
+    return out
+
+
 def w4a8_problem(M, N, K, *, E=1, cfg_id=1, seed=BASE_SEED, sf_lo=118, sf_hi=126,
                  bias=False):
     """MXFP4 weights (uniform over the 16 E2M1 codes) and MXFP8 activations
@@ -256,6 +273,7 @@ def router_logits(T, E, *, cfg_id=3, seed=BASE_SEED, bias_std=1.5):
 __all__ = [
     "BASE_SEED", "Stream", "stream", "uniform_int", "uniform", "normal", "random_bytes",
     "to_bf16_bits", "to_e4m3_codes", "pack_int4", "pack_int3", "pack_nibbles",
-    "unpack_nibbles_layout", "w4a16_problem", "w4a8_problem", "w8a8_problem", "w4a4_problem",
+    "unpack_nibbles_layout", "w4a16_problem", "w4a16_zp_problem", "w4a8_problem", "w8a8_problem",
+    "w4a4_problem",
     "router_logits",
 ]

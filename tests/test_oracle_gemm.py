@@ -330,3 +330,58 @@ def test_planted_wrong_nvfp4_group_is_caught(monkeypatch):
     monkeypatch.setattr(Q, "dequant_nv", wrong_group)
     with pytest.raises(AssertionError):
         test_w4a4_fraction_brute_force_groups()
+
+
+# ----------------------------------------------------------------------------- W4A16 zero points
+def test_w4a16_zp_exact_integer_dot():
+    """Unit scales: sum_k a (q - z) with integer activations is an exact integer."""
+    rng = np.random.default_rng(51)
+    M, N, K = 3, 4, 256
+    a = rng.integers(-20, 21, (M, K))
+    q = rng.integers(0, 16, (N, K))
+    z = rng.integers(0, 16, (N, K // 128))
+    A = synth.to_bf16_bits(a.astype(np.float64))
+    one = synth.to_bf16_bits(np.ones((N, K // 128)))
+    R, S = Q.gemm_w4a16_zp(A, q, one, z)
+    want = a @ (q - np.repeat(z, 128, axis=1)).T
+    assert np.array_equal(R, want.astype(np.float64))
+
+
+def test_w4a16_zp_with_zero_point_8_is_the_symmetric_code():
+    """q - 8 is the two's-complement INT4 value of the excess code: with z = 8 everywhere
+    the asymmetric GEMM must equal the symmetric one on q - 8 exactly."""
+    p = synth.w4a16_problem(5, 40, 384, bits=4, cfg_id=52)
+    q_signed = F.unpack_int4(p["w_canon"][0], 384).astype(np.int64)
+    R1, S1 = Q.gemm_w4a16(p["A"], q_signed, p["s_canon"][0])
+    R2, S2 = Q.gemm_w4a16_zp(p["A"], q_signed + 8, p["s_canon"][0],
+                             np.full((40, 3), 8, np.int64))
+    assert np.array_equal(R1, R2) and np.array_equal(S1, S2)
+
+
+def test_w4a16_zp_fraction_brute_force_and_canonical_words():
+    """Packed words (unsigned nibbles, scale + zero-point group words) decoded by the
+    canonical driver against exact rationals on a tiny shape with two groups."""
+    p = synth.w4a16_zp_problem(2, 3, 256, cfg_id=53)
+    R, absum = Q.w4a16_zp_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], 256)
+    a = F.decode_bf16(p["A"])
+    words = p["w_canon"][0]
+    sz = p["s_canon"][0].astype(np.int64)
+    for m in range(2):
+        for n in range(3):
+            ex = Fraction(0)
+            for k in range(256):
+                q = (int(words[n, k // 8]) >> (4 * (k % 8))) & 0xF
+                g = k // 128
+                s = Fraction(float(F.decode_bf16(np.uint16(sz[n, g] & 0xFFFF))))
+                z = (int(sz[n, g]) >> 16) & 0xFF
+                ex += Fraction(float(a[m, k])) * (q - z) * s
+            assert abs(Fraction(R[m, n]) - ex) <= Fraction(2.0 ** -50) * Fraction(absum[m, n])
+
+
+def test_split_zp_scales_rejects_bad_words():
+    with pytest.raises(F.FormatError):
+        F.split_zp_scales(np.array([0x3F80 | (16 << 16)], np.uint32))
+    with pytest.raises(F.FormatError):
+        F.split_zp_scales(np.array([0x3F80 | (1 << 24)], np.uint32))
+    s, z = F.split_zp_scales(np.array([0x3F80 | (15 << 16)], np.uint32))
+    assert s[0] == 0x3F80 and z[0] == 15
