@@ -63,12 +63,14 @@ constexpr uint32_t A_COL0 = 2 * BT;  // the two per-group accumulators use colum
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BT >> 3) << 17) |
                            ((uint32_t)(BW >> 4) << 24);
 
-template <int BITS>
+template <int BITS, bool ZP>
 struct Geo {
   static constexpr int BLK = BITS == 4 ? 1024 : 768;
   static constexpr int WBYTES = 8 * BLK;
+  // asymmetric INT4: the tile's 128 rows of BF16 128 + zero point for the stage's group
+  static constexpr int ZBYTES = ZP ? BW * 2 : 0;
   // stages start on 1 KiB boundaries: the 128-byte-swizzled activation boxes need it
-  static constexpr int STAGE = (ACT_BYTES + WBYTES + 1023) / 1024 * 1024;
+  static constexpr int STAGE = (ACT_BYTES + WBYTES + ZBYTES + 1023) / 1024 * 1024;
 };
 
 struct Params {
@@ -78,6 +80,7 @@ struct Params {
   int32_t num_n_tiles;
   const uint8_t* wp;
   const uint16_t* sp16;          // BF16 scales [E][K/128][N_pad]
+  const uint16_t* zp16;          // asymmetric INT4: BF16 128 + z, same layout (else null)
   int64_t w_estride;             // bytes
   int64_t s_estride_elems;
   const uint16_t* bias;
@@ -156,6 +159,11 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -191,11 +199,11 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 constexpr int STAGING_BYTES = BT * BW * 2;  // one BF16 output tile [token][row]
 
-template <int BITS>
+template <int BITS, bool ZP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmC, const Params p) {
-  using GE = Geo<BITS>;
+  using GE = Geo<BITS, ZP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* staging = smem + STAGES * GE::STAGE;
@@ -254,11 +262,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           uint8_t* st = smem + stage * GE::STAGE;
-          mbar_arrive_expect_tx(&full[stage], ACT_BYTES + nbs * GE::BLK);
+          mbar_arrive_expect_tx(&full[stage], ACT_BYTES + nbs * GE::BLK + (ZP ? nbs * 32 : 0));
           tma_load_2d(st, &tmA, &full[stage], g * 128, (int32_t)x.rb);
           tma_load_2d(st + ACT_BOX, &tmA, &full[stage], g * 128 + 64, (int32_t)x.rb);
           bulk_load(st + ACT_BYTES, wsrc + (int64_t)g * nblocks * GE::BLK, nbs * GE::BLK,
                     &full[stage]);
+          if constexpr (ZP)
+            bulk_load(st + ACT_BYTES + GE::WBYTES,
+                      p.zp16 + x.e * p.s_estride_elems + (int64_t)g * p.N_pad + x.nt * BW,
+                      nbs * 32, &full[stage]);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -333,12 +345,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (BITS == 4) {
               const uint4 w0 = lds128(blk + lane * 32), w1 = lds128(blk + lane * 32 + 16);
               const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+              // the excess of rows g and g + 8: the constant, or (asymmetric) 128 + z
+              uint32_t ex_lo = excess, ex_hi = excess;
+              if constexpr (ZP) {
+                const uint32_t zrow = smem_u32(smem + stage * GE::STAGE) + ACT_BYTES + GE::WBYTES +
+                                      (uint32_t)(16 * b + (lane >> 2)) * 2;
+                ex_lo = lds16(zrow) * 0x10001u;
+                ex_hi = lds16(zrow + 16) * 0x10001u;
+              }
 #pragma unroll
               for (int st = 0; st < 8; ++st) {
-                v[4 * st + 0] = bf16x2_sub_u32(and_or(w[st], 0x000F000Fu, magic), excess);
-                v[4 * st + 2] = bf16x2_sub_u32(and_or(w[st] >> 4, 0x000F000Fu, magic), excess);
-                v[4 * st + 1] = bf16x2_sub_u32(and_or(w[st] >> 8, 0x000F000Fu, magic), excess);
-                v[4 * st + 3] = bf16x2_sub_u32(and_or(w[st] >> 12, 0x000F000Fu, magic), excess);
+                // registers 4st, 4st + 1 hold row g; 4st + 2, 4st + 3 row g + 8
+                v[4 * st + 0] = bf16x2_sub_u32(and_or(w[st], 0x000F000Fu, magic), ex_lo);
+                v[4 * st + 2] = bf16x2_sub_u32(and_or(w[st] >> 4, 0x000F000Fu, magic), ex_hi);
+                v[4 * st + 1] = bf16x2_sub_u32(and_or(w[st] >> 8, 0x000F000Fu, magic), ex_lo);
+                v[4 * st + 3] = bf16x2_sub_u32(and_or(w[st] >> 12, 0x000F000Fu, magic), ex_hi);
               }
             } else {
               const uint4 lo = lds128(blk + lane * 16);
@@ -474,18 +495,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BITS>
+template <int BITS, bool ZP>
 qw_status launch_bits(const CUtensorMap& tmA, const CUtensorMap& tmC, const Params& p,
                       int64_t tiles_max, cudaStream_t st) {
-  using GE = Geo<BITS>;
+  using GE = Geo<BITS, ZP>;
   // ring + output staging + barriers + alignment
   const size_t smem = (size_t)STAGES * GE::STAGE + STAGING_BYTES + 256 + 1024;
   static const cudaError_t attr = cudaFuncSetAttribute(
-      gemm_w4a16_tc_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      gemm_w4a16_tc_kernel<BITS, ZP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return QW_ERR_CUDA;
   const int sms = device_sm_count();
   const unsigned grid = (unsigned)(tiles_max < sms ? (tiles_max < 1 ? 1 : tiles_max) : sms);
-  gemm_w4a16_tc_kernel<BITS><<<grid, NUM_THREADS, smem, st>>>(tmA, tmC, p);
+  gemm_w4a16_tc_kernel<BITS, ZP><<<grid, NUM_THREADS, smem, st>>>(tmA, tmC, p);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 
@@ -538,6 +559,8 @@ qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
   p.sp16 = static_cast<const uint16_t*>(s_packed);
   p.w_estride = (int64_t)d.w_expert_stride;
   p.s_estride_elems = (int64_t)(d.s_expert_stride / 2);
+  if (d.wfmt == QW_W_UINT4ZP_G128_BF16)  // the second plane: half an expert's scale stride
+    p.zp16 = p.sp16 + d.s_expert_stride / 4;
   p.bias = static_cast<const uint16_t*>(bias);
   p.C = static_cast<uint16_t*>(C);
   p.err = err;
@@ -553,8 +576,9 @@ qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
     p.queue = queue;
   }
   const int64_t tiles_max = max_m * p.num_n_tiles;
-  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_bits<4>(tmA, tmC, p, tiles_max, st)
-                                       : launch_bits<3>(tmA, tmC, p, tiles_max, st);
+  if (d.wfmt == QW_W_UINT4ZP_G128_BF16) return launch_bits<4, true>(tmA, tmC, p, tiles_max, st);
+  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_bits<4, false>(tmA, tmC, p, tiles_max, st)
+                                       : launch_bits<3, false>(tmA, tmC, p, tiles_max, st);
 }
 
 }  // namespace qw

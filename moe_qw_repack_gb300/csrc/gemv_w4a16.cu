@@ -206,6 +206,7 @@ struct Params {
   const int32_t* queue;  // grouped tile queue or null
   int64_t w_estride, s_estride;  // bytes, BF16 elements
   int32_t gpw;           // scale groups per warp
+  int64_t zplane;        // asymmetric INT4: BF16 elements from a scale to its 128 + z
 };
 
 // One work item = (expert e, 16-row block nb, token rows [rb, re)), re - rb <= 8 * MCH.
@@ -279,7 +280,7 @@ __device__ __forceinline__ void biased_all(const uint32_t (&w)[Geo<BITS>::WPG], 
   biased<BITS>(s, w8, a);
 }
 
-template <int BITS, int MCH>
+template <int BITS, int MCH, bool ZP>
 __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
     gemv_reg_kernel(const Params p) {
   using GE = Geo<BITS>;
@@ -304,6 +305,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
   // register ring: the batch being computed next
   uint32_t wb[NB][WPG];
   uint32_t sc[NB];  // BF16 scales of rows g (low half) and g + 8 (high half)
+  uint32_t zc[NB];  // asymmetric INT4: BF16 128 + z of rows g and g + 8
   // refills walk the next batch's groups in slot order with running pointers
   const uint8_t* rw = nullptr;
   const uint16_t* rsc = nullptr;
@@ -312,6 +314,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
     if (j < rng) {
       load_words<BITS>(rw, lane, wb[j]);
       sc[j] = __byte_perm(__ldg(rsc), __ldg(rsc + 8), 0x5410);
+      if constexpr (ZP) zc[j] = __byte_perm(__ldg(rsc + p.zplane), __ldg(rsc + p.zplane + 8), 0x5410);
       rw += gstride_w;
       rsc += p.N_pad;
     }
@@ -398,13 +401,17 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
                 }
               }
             }
+            // the excess of rows g and g + 8: 128 + excess, or (asymmetric) 128 + z
+            const float b_lo = ZP ? __uint_as_float(zc[j] << 16) : GE::BIAS;
+            const float b_hi = ZP ? __uint_as_float(zc[j] & 0xFFFF0000u) : GE::BIAS;
 #pragma unroll
             for (int c = 0; c < MCH; ++c)
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                acc[c][i] = fmaf(i < 2 ? s_lo : s_hi, fmaf(-GE::BIAS, sm[c][i], pr[c][i]),
+                acc[c][i] = fmaf(i < 2 ? s_lo : s_hi, fmaf(i < 2 ? -b_lo : -b_hi, sm[c][i], pr[c][i]),
                                  acc[c][i]);
           } else {
+            static_assert(!ZP, "the asymmetric format runs with at most 16 token rows");
             const uint32_t bias2 = BITS == 4 ? 0x43084308u : 0x43044304u;  // BF16 pair of BIAS
             float part[MCH][4];
 #pragma unroll
@@ -461,9 +468,9 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
   }
 }
 
-template <int BITS, int MCH>
+template <int BITS, int MCH, bool ZP>
 qw_status launch_reg_variant(const Params& p, int64_t size_items, cudaStream_t st) {
-  auto kern = gemv_reg_kernel<BITS, MCH>;
+  auto kern = gemv_reg_kernel<BITS, MCH, ZP>;
   const size_t smem = (size_t)kWarps * MCH * 128 * sizeof(float);
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -504,6 +511,7 @@ struct M8Params {
   uint16_t* C;
   int32_t N, N_pad, K, M;  // M <= 8
   int32_t gpw;             // scale groups per warp
+  int64_t zplane;          // asymmetric INT4: BF16 elements from a scale to its 128 + z
 };
 
 __host__ __device__ constexpr size_t m8_act_bytes(int K, int M) {
@@ -513,7 +521,7 @@ constexpr size_t m8_smem_bytes(int K, int M) {
   return m8_act_bytes(K, M) + (size_t)(K / 128) * 8 * 4 + 2 * kM8Warps * 4 * 32 * 4;
 }
 
-template <int BITS>
+template <int BITS, bool ZP>
 __global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Params p) {
   using GE = Geo<BITS>;
   constexpr int WPG = GE::WPG;
@@ -538,6 +546,7 @@ __global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Param
   // register ring and the running pointers of the batch that refills it
   uint32_t wb[R][WPG];
   uint32_t sc[R];
+  uint32_t zc[R];  // asymmetric INT4: BF16 128 + z of rows g and g + 8
   const uint8_t* rw = nullptr;
   const uint16_t* rs = nullptr;
   int rng = 0;                    // groups in the refilling batch
@@ -565,6 +574,7 @@ __global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Param
       load_words<BITS>(rw + j * gstride, lane, wb[j]);
       const uint16_t* q = rs + (int64_t)j * p.N_pad;
       sc[j] = __byte_perm(__ldg(q), __ldg(q + 8), 0x5410);
+      if constexpr (ZP) zc[j] = __byte_perm(__ldg(q + p.zplane), __ldg(q + p.zplane + 8), 0x5410);
     }
   };
   point(0, 0);
@@ -647,10 +657,13 @@ __global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Param
           const float sm0 = __uint_as_float(sm2.x), sm1 = __uint_as_float(sm2.y);
           const float s_lo = __uint_as_float(sc[j] << 16);
           const float s_hi = __uint_as_float(sc[j] & 0xFFFF0000u);
-          acc[0] = fmaf(s_lo, fmaf(-GE::BIAS, sm0, pr[0]), acc[0]);
-          acc[1] = fmaf(s_lo, fmaf(-GE::BIAS, sm1, pr[1]), acc[1]);
-          acc[2] = fmaf(s_hi, fmaf(-GE::BIAS, sm0, pr[2]), acc[2]);
-          acc[3] = fmaf(s_hi, fmaf(-GE::BIAS, sm1, pr[3]), acc[3]);
+          // the excess of rows g and g + 8: 128 + excess, or (asymmetric) 128 + z
+          const float b_lo = ZP ? __uint_as_float(zc[j] << 16) : GE::BIAS;
+          const float b_hi = ZP ? __uint_as_float(zc[j] & 0xFFFF0000u) : GE::BIAS;
+          acc[0] = fmaf(s_lo, fmaf(-b_lo, sm0, pr[0]), acc[0]);
+          acc[1] = fmaf(s_lo, fmaf(-b_lo, sm1, pr[1]), acc[1]);
+          acc[2] = fmaf(s_hi, fmaf(-b_hi, sm0, pr[2]), acc[2]);
+          acc[3] = fmaf(s_hi, fmaf(-b_hi, sm1, pr[3]), acc[3]);
         }
       }
 #pragma unroll
@@ -680,9 +693,9 @@ __global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Param
   }
 }
 
-template <int BITS>
+template <int BITS, bool ZP>
 qw_status launch_m8_variant(const M8Params& p, cudaStream_t st) {
-  auto kern = gemv_m8_kernel<BITS>;
+  auto kern = gemv_m8_kernel<BITS, ZP>;
   const size_t smem = m8_smem_bytes(p.K, p.M);
   // one attribute call sized for the largest staging this kernel is sent (see the dispatch)
   static const cudaError_t attr = cudaFuncSetAttribute(
@@ -714,18 +727,19 @@ struct Ring {
 // grouped (MoE) calls: many short items, several CTAs per SM
 using GroupedRing = Ring<4, 4, 4>;
 
-template <int BITS>
+template <int BITS, bool ZP>
 struct TmaGeo {
   static constexpr int BLK = BITS == 4 ? 1024 : 768;  // one 16 x 128 block
   static constexpr int W_STAGE = kStageGroups * BLK;
   static constexpr int S_STAGE = kStageGroups * 16 * 2;  // BF16 scales of 16 rows x 8 groups
-  static constexpr int STAGE = W_STAGE + S_STAGE;
+  // asymmetric INT4: the same rows and groups of BF16 128 + z follow the scales
+  static constexpr int STAGE = W_STAGE + S_STAGE * (ZP ? 2 : 1);
   static constexpr float BIAS = BITS == 4 ? 136.f : 132.f;  // 128 + excess
 };
 
-template <int BITS, int MCH, class R>
+template <int BITS, int MCH, class R, bool ZP>
 constexpr size_t tma_smem_bytes() {
-  return 128 + (size_t)R::STAGES * TmaGeo<BITS>::STAGE + 2 * 8 * R::STAGES +
+  return 128 + (size_t)R::STAGES * TmaGeo<BITS, ZP>::STAGE + 2 * 8 * R::STAGES +
          (size_t)R::CONS * MCH * 128 * 4 + 16;
 }
 
@@ -756,11 +770,12 @@ __device__ __forceinline__ void tma_item_of(const TmaParams& p, uint32_t item, u
   }
 }
 
-template <int BITS, int MCH, class R>
+template <int BITS, int MCH, class R, bool ZP>
 __global__ void __launch_bounds__(R::THREADS, R::CTAS)
     gemv_tma_kernel(const __grid_constant__ CUtensorMap tmW,
-                    const __grid_constant__ CUtensorMap tmS, const TmaParams p) {
-  using GE = TmaGeo<BITS>;
+                    const __grid_constant__ CUtensorMap tmS,
+                    const __grid_constant__ CUtensorMap tmZ, const TmaParams p) {
+  using GE = TmaGeo<BITS, ZP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + R::STAGES * GE::STAGE);
@@ -814,6 +829,9 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
           mbar_arrive_expect_tx(&full[stage], GE::STAGE);
           tma_load_4d(dst, &tmW, &full[stage], 0, nb, c * kStageGroups, e);
           tma_load_3d(dst + GE::W_STAGE, &tmS, &full[stage], nb * 16, c * kStageGroups, e);
+          if constexpr (ZP)
+            tma_load_3d(dst + GE::W_STAGE + GE::S_STAGE, &tmZ, &full[stage], nb * 16,
+                        c * kStageGroups, e);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == R::STAGES) {
@@ -886,6 +904,16 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
                                               (g & 1) ? 0x7632 : 0x5410);
               const float s_lo = __uint_as_float(sc << 16);
               const float s_hi = __uint_as_float(sc & 0xFFFF0000u);
+              // the excess of rows g and g + 8: 128 + excess, or (asymmetric) 128 + z
+              float b_lo = GE::BIAS, b_hi = GE::BIAS;
+              if constexpr (ZP) {
+                const uint32_t zrow = srow + GE::S_STAGE;
+                const uint32_t zc = __byte_perm(lds32(zrow + (g & ~1) * 2),
+                                                lds32(zrow + ((g + 8) & ~1) * 2),
+                                                (g & 1) ? 0x7632 : 0x5410);
+                b_lo = __uint_as_float(zc << 16);
+                b_hi = __uint_as_float(zc & 0xFFFF0000u);
+              }
               const int koff = gg * 128;
               if constexpr (MCH <= 2) {
                 const uint32_t ones[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};
@@ -909,9 +937,10 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
                 for (int c = 0; c < MCH; ++c)
 #pragma unroll
                   for (int i = 0; i < 4; ++i)
-                    acc[c][i] = fmaf(i < 2 ? s_lo : s_hi, fmaf(-GE::BIAS, sm[c][i], pr[c][i]),
+                    acc[c][i] = fmaf(i < 2 ? s_lo : s_hi, fmaf(i < 2 ? -b_lo : -b_hi, sm[c][i], pr[c][i]),
                                      acc[c][i]);
               } else {
+                static_assert(!ZP, "the asymmetric format runs with at most 16 token rows");
                 const uint32_t bias2 = BITS == 4 ? 0x43084308u : 0x43044304u;  // BF16 pair of BIAS
                 float part[MCH][4];
 #pragma unroll
@@ -990,11 +1019,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BITS, int MCH, class R>
-qw_status launch_tma_variant(const CUtensorMap& tmW, const CUtensorMap& tmS, const TmaParams& p,
-                         int64_t size_items, cudaStream_t st) {
-  auto kern = gemv_tma_kernel<BITS, MCH, R>;
-  const size_t smem = tma_smem_bytes<BITS, MCH, R>();
+template <int BITS, int MCH, class R, bool ZP>
+qw_status launch_tma_variant(const CUtensorMap& tmW, const CUtensorMap& tmS, const CUtensorMap& tmZ,
+                             const TmaParams& p, int64_t size_items, cudaStream_t st) {
+  auto kern = gemv_tma_kernel<BITS, MCH, R, ZP>;
+  const size_t smem = tma_smem_bytes<BITS, MCH, R, ZP>();
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return QW_ERR_CUDA;
@@ -1006,7 +1035,7 @@ qw_status launch_tma_variant(const CUtensorMap& tmW, const CUtensorMap& tmS, con
   int64_t grid = (int64_t)device_sm_count() * per_sm;
   if (grid > size_items) grid = size_items;
   if (grid < 1) grid = 1;
-  return launch_pdl(kern, (unsigned)grid, R::THREADS, smem, st, tmW, tmS, p);
+  return launch_pdl(kern, (unsigned)grid, R::THREADS, smem, st, tmW, tmS, tmZ, p);
 }
 
 // Token rows per item / 8: the dispatcher sends dense calls of at most 16 rows and grouped
@@ -1033,7 +1062,12 @@ qw_status launch_dense_m8(const qw_packed_desc& d, const void* w_packed, const v
   p.K = d.K;
   p.M = M;
   p.gpw = (G + kM8Warps - 1) / kM8Warps;
-  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_m8_variant<4>(p, st) : launch_m8_variant<3>(p, st);
+  if (d.wfmt == QW_W_UINT4ZP_G128_BF16) {
+    p.zplane = (int64_t)(d.s_expert_stride / 4);  // the second BF16 plane
+    return launch_m8_variant<4, true>(p, st);
+  }
+  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_m8_variant<4, false>(p, st)
+                                       : launch_m8_variant<3, false>(p, st);
 }
 
 // Other dense calls with up to 16 token rows: the register-ring kernel.
@@ -1056,10 +1090,17 @@ qw_status launch_dense_reg(const qw_packed_desc& d, const void* w_packed, const 
   p.gpw = (G + kWarps - 1) / kWarps;
   const int64_t items = (d.N_pad / 16) * ((M + 8 * mch - 1) / (8 * mch));
   if (items > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
+  if (d.wfmt == QW_W_UINT4ZP_G128_BF16) {
+    p.zplane = (int64_t)(d.s_expert_stride / 4);  // the second BF16 plane
+    return mch == 1 ? launch_reg_variant<4, 1, true>(p, items, st)
+                    : launch_reg_variant<4, 2, true>(p, items, st);
+  }
   const bool int4 = d.wfmt == QW_W_INT4_G128_BF16;
   if (mch == 1)
-    return int4 ? launch_reg_variant<4, 1>(p, items, st) : launch_reg_variant<3, 1>(p, items, st);
-  return int4 ? launch_reg_variant<4, 2>(p, items, st) : launch_reg_variant<3, 2>(p, items, st);
+    return int4 ? launch_reg_variant<4, 1, false>(p, items, st)
+                : launch_reg_variant<3, 1, false>(p, items, st);
+  return int4 ? launch_reg_variant<4, 2, false>(p, items, st)
+              : launch_reg_variant<3, 2, false>(p, items, st);
 }
 
 }  // namespace
@@ -1084,14 +1125,15 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
     return launch_dense_reg(d, w_packed, s_packed, A, bias, C, rs.rows, mch, st);
   // Grouped calls (over the device tile queue), and dense calls the dispatcher sends here
   // with more rows: the TMA ring.
-  const bool int4 = d.wfmt == QW_W_INT4_G128_BF16;
+  const bool zp = d.wfmt == QW_W_UINT4ZP_G128_BF16;
+  const bool int4 = d.wfmt == QW_W_INT4_G128_BF16 || zp;
   const int blk = int4 ? kInt4BlockBytes : kInt3BlockBytes;
   const int G = d.K / kIntGroup;
   const int64_t nblocks = d.N_pad / 16;
   auto enc = encode_fn();
   if (!enc) return QW_ERR_CUDA;
   // weights: [E][G][N_pad/16][block] as 8-byte elements; one copy = 8 groups of a block
-  CUtensorMap tmW, tmS;
+  CUtensorMap tmW, tmS, tmZ;
   {
     cuuint64_t dim[4] = {(cuuint64_t)(blk / 8), (cuuint64_t)nblocks, (cuuint64_t)G,
                          (cuuint64_t)d.E};
@@ -1114,6 +1156,15 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return QW_ERR_ALIGNMENT;
+    // asymmetric INT4: the plane of 128 + z, half an expert's scale stride further on
+    tmZ = tmS;
+    if (zp) {
+      void* zbase = static_cast<uint8_t*>(const_cast<void*>(s_packed)) + d.s_expert_stride / 2;
+      if (enc(&tmZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, zbase, dim, str, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return QW_ERR_ALIGNMENT;
+    }
   }
   TmaParams p{};
   p.A = static_cast<const uint16_t*>(A);
@@ -1144,10 +1195,12 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   }
   if (max_items > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
   if (mch == 1)
-    return int4 ? launch_tma_variant<4, 1, GroupedRing>(tmW, tmS, p, size_items, st)
-                : launch_tma_variant<3, 1, GroupedRing>(tmW, tmS, p, size_items, st);
-  return int4 ? launch_tma_variant<4, 2, GroupedRing>(tmW, tmS, p, size_items, st)
-              : launch_tma_variant<3, 2, GroupedRing>(tmW, tmS, p, size_items, st);
+    return zp     ? launch_tma_variant<4, 1, GroupedRing, true>(tmW, tmS, tmZ, p, size_items, st)
+           : int4 ? launch_tma_variant<4, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
+                  : launch_tma_variant<3, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st);
+  return zp     ? launch_tma_variant<4, 2, GroupedRing, true>(tmW, tmS, tmZ, p, size_items, st)
+         : int4 ? launch_tma_variant<4, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
+                : launch_tma_variant<3, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st);
 }
 
 }  // namespace qw

@@ -92,15 +92,18 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
   d.K = K;
   switch (wfmt) {
     case QW_W_INT4_G128_BF16:
-    case QW_W_INT3_G128_BF16: {
+    case QW_W_INT3_G128_BF16:
+    case QW_W_UINT4ZP_G128_BF16: {
       if (K % kIntGroup) return QW_ERR_UNSUPPORTED;
       d.group = kIntGroup;
       d.N_pad = (int32_t)round_up(N, 16);
       d.K_pad = K;
       const int64_t blocks = (int64_t)(K / kIntGroup) * (d.N_pad / 16);
       d.w_expert_stride =
-          (uint64_t)blocks * (wfmt == QW_W_INT4_G128_BF16 ? kInt4BlockBytes : kInt3BlockBytes);
-      d.s_expert_stride = (uint64_t)round_up((int64_t)(K / kIntGroup) * d.N_pad * 2, 256);
+          (uint64_t)blocks * (wfmt == QW_W_INT3_G128_BF16 ? kInt3BlockBytes : kInt4BlockBytes);
+      // one BF16 plane of scales (UINT4ZP: a second plane of 128 + zero point)
+      d.s_expert_stride = (uint64_t)round_up((int64_t)(K / kIntGroup) * d.N_pad * 2, 256) *
+                          (wfmt == QW_W_UINT4ZP_G128_BF16 ? 2 : 1);
       break;
     }
     case QW_W_MXFP4_G32:
@@ -140,6 +143,7 @@ qw_status qw_repack(const qw_packed_desc* desc, const void* w_canon, const void*
   if (!w_canon || !s_canon || !w_packed || !s_packed) return QW_ERR_INVALID_ARG;
   if (!is_mx(desc->wfmt) && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
     return QW_ERR_ALIGNMENT;
+  if (desc->wfmt == QW_W_UINT4ZP_G128_BF16 && !aligned(s_canon, 4)) return QW_ERR_ALIGNMENT;
   if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
   return launch_repack(*desc, w_canon, s_canon, w_packed, s_packed, d_err,
                        static_cast<cudaStream_t>(stream));
@@ -152,6 +156,7 @@ qw_status qw_unpack(const qw_packed_desc* desc, const void* w_packed, const void
   if (!w_canon || !s_canon || !w_packed || !s_packed) return QW_ERR_INVALID_ARG;
   if (!is_mx(desc->wfmt) && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
     return QW_ERR_ALIGNMENT;
+  if (desc->wfmt == QW_W_UINT4ZP_G128_BF16 && !aligned(s_canon, 4)) return QW_ERR_ALIGNMENT;
   if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
   return launch_unpack(*desc, w_packed, s_packed, w_canon, s_canon, d_err,
                        static_cast<cudaStream_t>(stream));

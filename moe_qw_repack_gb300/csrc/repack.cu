@@ -33,8 +33,11 @@ __device__ __forceinline__ void int4_nib_pos(int l, int s, int i, int& row, int&
   k = 16 * s + 4 * t + 2 * (r >> 1) + h;
 }
 
+// `unsigned_codes`: the asymmetric format's q in [0, 15] is packed as it is (its zero point
+// plays the excess); otherwise the symmetric q becomes the excess-8 code q + 8.
 __global__ void repack_int4_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
-                                   int32_t E, int32_t N, int32_t N_pad, int32_t K, int32_t* err) {
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K, int32_t* err,
+                                   bool unsigned_codes) {
   const int64_t per_expert = (int64_t)(K / 128) * (N_pad / 16) * 256;
   const int64_t total = per_expert * E;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -55,19 +58,22 @@ __global__ void repack_int4_kernel(const uint32_t* __restrict__ wc, uint32_t* __
       uint32_t nib = 0;  // q = 0 for padding rows
       if (n < N) {
         nib = int4_canon_nib(wce, K, n, G * 128 + k);
-        if (nib == 8u) {  // -8 is outside the symmetric range
+        if (!unsigned_codes && nib == 8u) {  // -8 is outside the symmetric range
           set_error(err, QW_ERR_VALUE);
           nib = 0;
         }
+      } else if (!unsigned_codes) {
+        nib = 0;
       }
-      out |= ((nib ^ 8u) & 0xFu) << (4 * i);  // excess-8 code q + 8
+      out |= ((unsigned_codes ? nib : (nib ^ 8u)) & 0xFu) << (4 * i);
     }
     wp[idx] = out;
   }
 }
 
 __global__ void unpack_int4_kernel(const uint32_t* __restrict__ wp, uint32_t* __restrict__ wc,
-                                   int32_t E, int32_t N, int32_t N_pad, int32_t K) {
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K,
+                                   bool unsigned_codes) {
   // one thread per canonical word (8 consecutive k of one row)
   const int64_t per_expert = (int64_t)N * (K / 8);
   const int64_t total = per_expert * E;
@@ -89,7 +95,7 @@ __global__ void unpack_int4_kernel(const uint32_t* __restrict__ wp, uint32_t* __
       const int lane = g * 4 + t, i = (r0 | (r1 << 1)) + 4 * h;
       const uint32_t word = wpe[((int64_t)G * (N_pad / 16) + nb) * 256 + lane * 8 + s];
       const uint32_t code = (word >> (4 * i)) & 0xFu;
-      out |= ((code ^ 8u) & 0xFu) << (4 * j);
+      out |= ((unsigned_codes ? code : (code ^ 8u)) & 0xFu) << (4 * j);
     }
     wc[idx] = out;
   }
@@ -209,6 +215,47 @@ __global__ void unpack_int_scales_kernel(const uint16_t* __restrict__ sp, uint16
     const int n = (int)(rem / G);
     const int g = (int)(rem % G);
     sc[idx] = sp[(e * G + g) * N_pad + n];
+  }
+}
+
+// Asymmetric INT4 group words (BF16 scale | zero point << 16) -> the scale plane [G][N_pad]
+// and the plane of BF16 128 + z (0x4300 | z, exact), per expert at `plane` halfwords apart.
+__global__ void repack_zp_scales_kernel(const uint32_t* __restrict__ sc, uint16_t* __restrict__ sp,
+                                        int32_t E, int32_t N, int32_t N_pad, int32_t G,
+                                        int64_t plane, int32_t* err) {
+  const int64_t total = (int64_t)E * G * N_pad;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / ((int64_t)G * N_pad);
+    const int64_t rem = idx % ((int64_t)G * N_pad);
+    const int g = (int)(rem / N_pad);
+    const int n = (int)(rem % N_pad);
+    uint32_t w = 0;
+    if (n < N) {
+      w = sc[(e * N + n) * G + g];
+      if ((w >> 20) != 0) {  // zero point above 15 or stray high bits
+        set_error(err, QW_ERR_VALUE);
+        w &= 0xFFFFu;
+      }
+    }
+    uint16_t* spe = sp + e * 2 * plane;
+    spe[rem] = (uint16_t)(w & 0xFFFFu);
+    spe[plane + rem] = (uint16_t)(0x4300u | (w >> 16));
+  }
+}
+__global__ void unpack_zp_scales_kernel(const uint16_t* __restrict__ sp, uint32_t* __restrict__ sc,
+                                        int32_t E, int32_t N, int32_t N_pad, int32_t G,
+                                        int64_t plane) {
+  const int64_t total = (int64_t)E * N * G;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / ((int64_t)N * G);
+    const int64_t rem = idx % ((int64_t)N * G);
+    const int n = (int)(rem / G);
+    const int g = (int)(rem % G);
+    const uint16_t* spe = sp + e * 2 * plane;
+    const int64_t at = (int64_t)g * N_pad + n;
+    sc[idx] = (uint32_t)spe[at] | ((uint32_t)(spe[plane + at] & 0xFFu) << 16);
   }
 }
 
@@ -394,11 +441,19 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
                         void* w_packed, void* s_packed, int32_t* err, cudaStream_t st) {
   const int T = 256;
   switch (d.wfmt) {
-    case QW_W_INT4_G128_BF16: {
+    case QW_W_INT4_G128_BF16:
+    case QW_W_UINT4ZP_G128_BF16: {
+      const bool zp = d.wfmt == QW_W_UINT4ZP_G128_BF16;
       const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 256;
       repack_int4_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_canon,
                                                         (uint32_t*)w_packed, d.E, d.N, d.N_pad,
-                                                        d.K, err);
+                                                        d.K, err, zp);
+      if (zp) {
+        const int64_t ts = (int64_t)d.E * (d.K / 128) * d.N_pad;
+        repack_zp_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
+            (const uint32_t*)s_canon, (uint16_t*)s_packed, d.E, d.N, d.N_pad, d.K / 128,
+            (int64_t)(d.s_expert_stride / 4), err);
+      }
       break;
     }
     case QW_W_INT3_G128_BF16: {
@@ -449,11 +504,19 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
   (void)err;
   const int T = 256;
   switch (d.wfmt) {
-    case QW_W_INT4_G128_BF16: {
+    case QW_W_INT4_G128_BF16:
+    case QW_W_UINT4ZP_G128_BF16: {
+      const bool zp = d.wfmt == QW_W_UINT4ZP_G128_BF16;
       const int64_t tw = (int64_t)d.E * d.N * (d.K / 8);
       unpack_int4_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_packed,
                                                         (uint32_t*)w_canon, d.E, d.N, d.N_pad,
-                                                        d.K);
+                                                        d.K, zp);
+      if (zp) {
+        const int64_t ts = (int64_t)d.E * d.N * (d.K / 128);
+        unpack_zp_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
+            (const uint16_t*)s_packed, (uint32_t*)s_canon, d.E, d.N, d.N_pad, d.K / 128,
+            (int64_t)(d.s_expert_stride / 4));
+      }
       break;
     }
     case QW_W_INT3_G128_BF16: {
