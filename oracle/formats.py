@@ -82,6 +82,20 @@ def unpack_int4(words, K: int) -> np.ndarray:
     return out
 
 
+def unpack_int2(words, K: int) -> np.ndarray:
+    """uint32 [..., K/16] -> int8 [..., K]; element k = 16j + i at bits [2i, 2i + 2) of
+    word j, two's complement; -2 rejected (the symmetric range is {-1, 0, 1})."""
+    w = np.asarray(words).astype(np.uint32)
+    assert w.shape[-1] * 16 == K
+    out = np.empty((*w.shape[:-1], K), dtype=np.int8)
+    for i in range(16):
+        f = ((w >> np.uint32(2 * i)) & np.uint32(3)).astype(np.int16)
+        out[..., i::16] = np.where(f >= 2, f - 4, f)
+    if np.any(out == -2):
+        raise FormatError("INT2 code -2 is outside the symmetric range")
+    return out
+
+
 def unpack_uint4(words, K: int) -> np.ndarray:
     """uint32 [..., K/8] -> int16 [..., K] in [0, 15]; element k = 8j + i at bits
     [4i, 4i + 4) of word j (the INT4 packing, read unsigned)."""

@@ -123,7 +123,7 @@ def gemm_w4a4(A_codes, A_sf, w_codes, w_sf, bias_bits=None):
 def w4a16_from_canonical(A_bits, w_canon, s_canon, K, bits, bias_bits=None, rows=None, cols=None):
     """Unpack canonical packed words (one expert) and run :func:`gemm_w4a16`.
     ``rows`` / ``cols`` optionally select a sample of output rows / columns."""
-    q = F.unpack_int4(w_canon, K) if bits == 4 else F.unpack_int3(w_canon, K)
+    q = {4: F.unpack_int4, 3: F.unpack_int3, 2: F.unpack_int2}[bits](w_canon, K)
     A = np.asarray(A_bits)
     s = np.asarray(s_canon)
     if rows is not None:

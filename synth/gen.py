@@ -145,6 +145,18 @@ def pack_int4(codes: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(pack_nibbles(nib)).view("<u4").astype(np.uint32, copy=False)
 
 
+def pack_int2(codes: np.ndarray) -> np.ndarray:
+    """int codes in [-2, 1], shape [..., K] (K % 16 == 0) -> uint32 [..., K/16]; element
+    k = 16j + i at bits [2i, 2i + 2) of word j."""
+    c = np.asarray(codes).astype(np.int64) & 3
+    assert c.shape[-1] % 16 == 0
+    c = c.reshape(*c.shape[:-1], c.shape[-1] // 16, 16).astype(np.uint64)
+    w = np.zeros(c.shape[:-1], dtype=np.uint64)
+    for i in range(16):
+        w |= c[..., i] << np.uint64(2 * i)
+    return w.astype(np.uint32)
+
+
 def pack_int3(codes: np.ndarray) -> np.ndarray:
     """int codes in [-4, 3], shape [..., K] (K % 32 == 0) -> uint32 [..., K/32, 3]."""
     c = np.asarray(codes, dtype=np.int64)
@@ -180,11 +192,11 @@ def pack_nibbles(codes: np.ndarray) -> np.ndarray:
 def w4a16_problem(M, N, K, *, bits=4, E=1, cfg_id=0, seed=BASE_SEED,
                   scale_lo=0.005, scale_hi=0.02, bias=False):
     """Group-128 symmetric INT weights with BF16 scales and BF16 N(0,1) activations."""
-    qmax = 7 if bits == 4 else 3
+    qmax = {4: 7, 3: 3, 2: 1}[bits]
     q = uniform_int(stream(cfg_id, 1, seed), (E, N, K), -qmax, qmax).astype(np.int8)
     s = to_bf16_bits(uniform(stream(cfg_id, 2, seed), (E, N, K // 128), scale_lo, scale_hi))
     a = to_bf16_bits(normal(stream(cfg_id, 3, seed), (M, K)))
-    w = pack_int4(q) if bits == 4 else pack_int3(q)
+    w = {4: pack_int4, 3: pack_int3, 2: pack_int2}[bits](q)
     out = dict(A=a, q=q, w_canon=w, s_canon=s, E=E, N=N, K=K, M=M, bits=bits)
     if bias:
         out["bias"] = to_bf16_bits(normal(stream(cfg_id, 4, seed), (E, N)))
@@ -272,7 +284,7 @@ def router_logits(T, E, *, cfg_id=3, seed=BASE_SEED, bias_std=1.5):
 
 __all__ = [
     "BASE_SEED", "Stream", "stream", "uniform_int", "uniform", "normal", "random_bytes",
-    "to_bf16_bits", "to_e4m3_codes", "pack_int4", "pack_int3", "pack_nibbles",
+    "to_bf16_bits", "to_e4m3_codes", "pack_int4", "pack_int3", "pack_int2", "pack_nibbles",
     "unpack_nibbles_layout", "w4a16_problem", "w4a16_zp_problem", "w4a8_problem", "w8a8_problem",
     "w4a4_problem",
     "router_logits",

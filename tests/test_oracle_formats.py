@@ -114,6 +114,33 @@ def test_int3_minus4_rejected():
         F.unpack_int3(words, 32)
 
 
+def _int2_word_by_bitstring(values):
+    """Independent construction: 2-bit two's-complement fields, LSB first."""
+    bits = "".join(format(v & 3, "02b")[::-1] for v in values)
+    return int(bits[::-1], 2)
+
+
+def test_int2_hand_word():
+    # [1, -1, 0, 1, 0 ...]: fields 01, 11, 00, 01 -> 0b01_00_11_01 = 0x4D
+    vals = [1, -1, 0, 1] + [0] * 12
+    assert _int2_word_by_bitstring(vals) == 0x4D
+    assert F.unpack_int2(np.array([0x4D], dtype=np.uint32), 16).tolist() == vals
+
+
+def test_int2_random_vs_bitstring_construction():
+    rng = np.random.default_rng(2)
+    for _ in range(50):
+        vals = rng.integers(-1, 2, 32).tolist()
+        words = np.array([[_int2_word_by_bitstring(vals[:16]), _int2_word_by_bitstring(vals[16:])]],
+                         dtype=np.uint32)
+        assert F.unpack_int2(words, 32).tolist() == [vals]
+
+
+def test_int2_minus2_rejected():
+    with pytest.raises(F.FormatError):
+        F.unpack_int2(np.array([0x2], dtype=np.uint32), 16)
+
+
 # ----------------------------------------------------------------------------- e0m equivalence
 @pytest.mark.parametrize("bits", [8, 4, 3])
 def test_e0m_value_set_equals_symmetric_int(bits):

@@ -385,3 +385,19 @@ def test_split_zp_scales_rejects_bad_words():
         F.split_zp_scales(np.array([0x3F80 | (1 << 24)], np.uint32))
     s, z = F.split_zp_scales(np.array([0x3F80 | (15 << 16)], np.uint32))
     assert s[0] == 0x3F80 and z[0] == 15
+
+
+def test_w4a16_int2_from_canonical_exact():
+    """INT2 words through the canonical driver: unit scales and integer activations give the
+    exact integer product of the codes decoded bit by bit here."""
+    rng = np.random.default_rng(54)
+    M, N, K = 3, 5, 256
+    q = rng.integers(-1, 2, (N, K))
+    a = rng.integers(-9, 10, (M, K))
+    words = np.zeros((N, K // 16), np.uint32)
+    for n in range(N):
+        for k in range(K):
+            words[n, k // 16] |= np.uint32((int(q[n, k]) & 3) << (2 * (k % 16)))
+    one = synth.to_bf16_bits(np.ones((N, K // 128)))
+    R, _ = Q.w4a16_from_canonical(synth.to_bf16_bits(a.astype(np.float64)), words, one, K, 2)
+    assert np.array_equal(R, (a @ q.T).astype(np.float64))
