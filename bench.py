@@ -233,11 +233,12 @@ def extra_w4a16(steps, warmup, world, only=None):
     for bits in (4, 3):
         for (N, K) in [(14336, 4096), (4096, 14336), (4096, 4096)]:
             cases.append((f"cfg3_m1_{N}x{K}_int{bits}", 1, N, K, bits))
+    cases.append(("m1_14336x4096_int2", 1, 14336, 4096, 2))  # INT2 WnA16 (no workload of its own)
     for name, M, N, K, bits in cases:
         if only and only not in name:
             continue
         p = synth.w4a16_problem(M, N, K, bits=bits, cfg_id=0 if M == 8 else 2)
-        wfmt = Q.QW_W_INT4_G128_BF16 if bits == 4 else Q.QW_W_INT3_G128_BF16
+        wfmt = {4: Q.QW_W_INT4_G128_BF16, 3: Q.QW_W_INT3_G128_BF16, 2: Q.QW_W_INT2_G128_BF16}[bits]
         d = Q.qw_repack_query(wfmt, 1, N, K)
         wp, sp = Q.empty_packed(d)
         Q.qw_repack(d, torch.from_numpy(p["w_canon"]).cuda(), torch.from_numpy(p["s_canon"]).cuda(), wp, sp)

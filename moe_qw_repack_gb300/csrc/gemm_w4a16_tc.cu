@@ -65,7 +65,7 @@ constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BT >
 
 template <int BITS, bool ZP>
 struct Geo {
-  static constexpr int BLK = BITS == 4 ? 1024 : 768;
+  static constexpr int BLK = BITS * 256;  // one packed 16 x 128 block
   static constexpr int WBYTES = 8 * BLK;
   // asymmetric INT4: the tile's 128 rows of BF16 128 + zero point for the stage's group
   static constexpr int ZBYTES = ZP ? BW * 2 : 0;
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // k+2/3, row g+8 k+2/3) they are exactly repetition s of a 16x256b TMEM store.
     const int q = warp & 3;  // TMEM lane quadrant: blocks 2q and 2q + 1 of the tile
     const uint32_t magic = 0x43004300u;
-    const uint32_t excess = BITS == 4 ? 0x43084308u : 0x43044304u;
+    const uint32_t excess = 0x43004300u + 0x10001u * (1u << (BITS - 1));  // BF16 pair 128 + excess
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -361,6 +361,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 v[4 * st + 1] = bf16x2_sub_u32(and_or(w[st] >> 8, 0x000F000Fu, magic), ex_lo);
                 v[4 * st + 3] = bf16x2_sub_u32(and_or(w[st] >> 12, 0x000F000Fu, magic), ex_hi);
               }
+            } else if constexpr (BITS == 2) {
+              const uint4 lo = lds128(blk + lane * 16);
+              const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+              for (int st = 0; st < 8; ++st)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                  const uint32_t biased =
+                      and_or(L[st >> 1] >> (2 * (4 * (st & 1) + r)), 0x00030003u, magic);
+                  // register r (row g + 8 (r & 1), k + 2 (r >> 1)) -> store slot
+                  v[4 * st + ((r & 1) << 1) + (r >> 1)] = bf16x2_sub_u32(biased, excess);
+                }
             } else {
               const uint4 lo = lds128(blk + lane * 16);
               const uint2 hi = lds64(blk + 512 + lane * 8);
@@ -577,6 +589,7 @@ qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
   }
   const int64_t tiles_max = max_m * p.num_n_tiles;
   if (d.wfmt == QW_W_UINT4ZP_G128_BF16) return launch_bits<4, true>(tmA, tmC, p, tiles_max, st);
+  if (d.wfmt == QW_W_INT2_G128_BF16) return launch_bits<2, false>(tmA, tmC, p, tiles_max, st);
   return d.wfmt == QW_W_INT4_G128_BF16 ? launch_bits<4, false>(tmA, tmC, p, tiles_max, st)
                                        : launch_bits<3, false>(tmA, tmC, p, tiles_max, st);
 }

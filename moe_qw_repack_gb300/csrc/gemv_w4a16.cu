@@ -72,7 +72,7 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 // Step S of a group -> four BF16x2 A-fragment registers holding 128 + code.
 // INT4: word S of the lane's eight, nibble pairs at shifts 0, 4, 8, 12 (one shift and one
 // logic op per pair).  INT3: low two bits from lo-plane word S/2, third bit from hi-plane
-// word S/4 (two shifts and two logic ops per pair).
+// word S/4 (two shifts and two logic ops per pair).  INT2: the INT3 lo plane alone.
 template <int BITS, int S>
 __device__ __forceinline__ void biased_step(const uint32_t (&w)[8], uint32_t (&a)[4]) {
   const uint32_t magic = 0x43004300u;  // BF16 pair (128, 128)
@@ -82,6 +82,10 @@ __device__ __forceinline__ void biased_step(const uint32_t (&w)[8], uint32_t (&a
     a[1] = and_or(x >> 4, 0x000F000Fu, magic);
     a[2] = and_or(x >> 8, 0x000F000Fu, magic);
     a[3] = and_or(x >> 12, 0x000F000Fu, magic);
+  } else if constexpr (BITS == 2) {
+    const uint32_t L = w[S / 2];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a[r] = and_or(L >> (2 * (4 * (S & 1) + r)), 0x00030003u, magic);
   } else {
     const uint32_t L = w[S / 2], H = w[4 + S / 4];
 #pragma unroll
@@ -159,9 +163,9 @@ __host__ __device__ constexpr int ctas_per_sm(int mch) { return 2; }
 
 template <int BITS>
 struct Geo {
-  static constexpr int BLK = BITS == 4 ? 1024 : 768;   // one 16 x 128 block
-  static constexpr int WPG = BITS == 4 ? 8 : 6;        // words per lane and group
-  static constexpr float BIAS = BITS == 4 ? 136.f : 132.f;  // 128 + excess
+  static constexpr int BLK = BITS * 256;                      // one 16 x 128 block
+  static constexpr int WPG = BITS * 2;                        // words per lane and group
+  static constexpr float BIAS = 128.f + (1 << (BITS - 1));   // 128 + excess
 };
 
 // groups per batch = register ring depth (token rows cost registers)
@@ -226,7 +230,8 @@ __device__ __forceinline__ void item_of(const Params& p, uint32_t item, uint32_t
   }
 }
 
-// The lane's packed words of one 16 x 128 block (INT4: 8 words; INT3: 4 lo + 2 hi words).
+// The lane's packed words of one 16 x 128 block (INT4: 8 words; INT3: 4 lo + 2 hi words;
+// INT2: 4 words).
 template <int BITS>
 __device__ __forceinline__ void load_words(const uint8_t* blk, int lane,
                                            uint32_t (&w)[Geo<BITS>::WPG]) {
@@ -235,6 +240,9 @@ __device__ __forceinline__ void load_words(const uint8_t* blk, int lane,
     const uint4 v1 = __ldcs(reinterpret_cast<const uint4*>(blk) + lane * 2 + 1);
     w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
     w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+  } else if constexpr (BITS == 2) {
+    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(blk) + lane);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
   } else {
     const uint4 lo = __ldcs(reinterpret_cast<const uint4*>(blk) + lane);
     const uint2 hi = __ldcs(reinterpret_cast<const uint2*>(blk + 512) + lane);
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
                                  acc[c][i]);
           } else {
             static_assert(!ZP, "the asymmetric format runs with at most 16 token rows");
-            const uint32_t bias2 = BITS == 4 ? 0x43084308u : 0x43044304u;  // BF16 pair of BIAS
+            const uint32_t bias2 = 0x43004300u + 0x10001u * (1u << (BITS - 1));  // BF16 pair of BIAS
             float part[MCH][4];
 #pragma unroll
             for (int c = 0; c < MCH; ++c)
@@ -729,12 +737,12 @@ using GroupedRing = Ring<4, 4, 4>;
 
 template <int BITS, bool ZP>
 struct TmaGeo {
-  static constexpr int BLK = BITS == 4 ? 1024 : 768;  // one 16 x 128 block
+  static constexpr int BLK = BITS * 256;  // one 16 x 128 block
   static constexpr int W_STAGE = kStageGroups * BLK;
   static constexpr int S_STAGE = kStageGroups * 16 * 2;  // BF16 scales of 16 rows x 8 groups
   // asymmetric INT4: the same rows and groups of BF16 128 + z follow the scales
   static constexpr int STAGE = W_STAGE + S_STAGE * (ZP ? 2 : 1);
-  static constexpr float BIAS = BITS == 4 ? 136.f : 132.f;  // 128 + excess
+  static constexpr float BIAS = 128.f + (1 << (BITS - 1));  // 128 + excess
 };
 
 template <int BITS, int MCH, class R, bool ZP>
@@ -891,6 +899,10 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
                 const uint4 v0 = lds128(blk + lane * 32), v1 = lds128(blk + lane * 32 + 16);
                 w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
                 w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+              } else if constexpr (BITS == 2) {
+                const uint4 v = lds128(blk + lane * 16);
+                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+                w[4] = w[5] = w[6] = w[7] = 0;
               } else {
                 const uint4 lo = lds128(blk + lane * 16);
                 const uint2 hi = lds64(blk + 512 + lane * 8);
@@ -941,7 +953,7 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
                                      acc[c][i]);
               } else {
                 static_assert(!ZP, "the asymmetric format runs with at most 16 token rows");
-                const uint32_t bias2 = BITS == 4 ? 0x43084308u : 0x43044304u;  // BF16 pair of BIAS
+                const uint32_t bias2 = 0x43004300u + 0x10001u * (1u << (BITS - 1));  // BF16 pair of BIAS
                 float part[MCH][4];
 #pragma unroll
                 for (int c = 0; c < MCH; ++c)
@@ -1066,6 +1078,7 @@ qw_status launch_dense_m8(const qw_packed_desc& d, const void* w_packed, const v
     p.zplane = (int64_t)(d.s_expert_stride / 4);  // the second BF16 plane
     return launch_m8_variant<4, true>(p, st);
   }
+  if (d.wfmt == QW_W_INT2_G128_BF16) return launch_m8_variant<2, false>(p, st);
   return d.wfmt == QW_W_INT4_G128_BF16 ? launch_m8_variant<4, false>(p, st)
                                        : launch_m8_variant<3, false>(p, st);
 }
@@ -1095,6 +1108,9 @@ qw_status launch_dense_reg(const qw_packed_desc& d, const void* w_packed, const 
     return mch == 1 ? launch_reg_variant<4, 1, true>(p, items, st)
                     : launch_reg_variant<4, 2, true>(p, items, st);
   }
+  if (d.wfmt == QW_W_INT2_G128_BF16)
+    return mch == 1 ? launch_reg_variant<2, 1, false>(p, items, st)
+                    : launch_reg_variant<2, 2, false>(p, items, st);
   const bool int4 = d.wfmt == QW_W_INT4_G128_BF16;
   if (mch == 1)
     return int4 ? launch_reg_variant<4, 1, false>(p, items, st)
@@ -1127,7 +1143,8 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   // with more rows: the TMA ring.
   const bool zp = d.wfmt == QW_W_UINT4ZP_G128_BF16;
   const bool int4 = d.wfmt == QW_W_INT4_G128_BF16 || zp;
-  const int blk = int4 ? kInt4BlockBytes : kInt3BlockBytes;
+  const bool int2 = d.wfmt == QW_W_INT2_G128_BF16;
+  const int blk = int4 ? kInt4BlockBytes : (int2 ? kInt2BlockBytes : kInt3BlockBytes);
   const int G = d.K / kIntGroup;
   const int64_t nblocks = d.N_pad / 16;
   auto enc = encode_fn();
@@ -1197,9 +1214,11 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   if (mch == 1)
     return zp     ? launch_tma_variant<4, 1, GroupedRing, true>(tmW, tmS, tmZ, p, size_items, st)
            : int4 ? launch_tma_variant<4, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
+           : int2 ? launch_tma_variant<2, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
                   : launch_tma_variant<3, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st);
   return zp     ? launch_tma_variant<4, 2, GroupedRing, true>(tmW, tmS, tmZ, p, size_items, st)
          : int4 ? launch_tma_variant<4, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
+         : int2 ? launch_tma_variant<2, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
                 : launch_tma_variant<3, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st);
 }
 

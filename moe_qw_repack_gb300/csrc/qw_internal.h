@@ -15,6 +15,7 @@ int device_sm_count();
 constexpr int kIntGroup = 128;       // K elements per BF16 scale (INT formats)
 constexpr int kMxGroup = 32;         // K elements per E8M0 scale (MX formats)
 constexpr int kInt4BlockBytes = 1024;  // 16 rows x 128 k of INT4, fragment order
+constexpr int kInt2BlockBytes = 512;   // 16 rows x 128 k of INT2, fragment order
 constexpr int kInt3BlockBytes = 768;   // 16 rows x 128 k of INT3 (two bit planes)
 constexpr int kSfChunkBytes = 512;     // 128 rows x 4 groups of E8M0 scales
 constexpr int kNvGroup = 16;           // K elements per E4M3 scale (NVFP4)

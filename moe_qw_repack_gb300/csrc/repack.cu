@@ -191,6 +191,73 @@ __global__ void unpack_int3_kernel(const uint32_t* __restrict__ wp, uint32_t* __
   }
 }
 
+// ----------------------------------------------------------------------------- INT2
+// Packed INT2 of lane l, step s, register r, half h (the INT4 (row, k) assignment): word s/2
+// of the lane's four keeps u = q + 2 at bits 2 * (4 * (s % 2) + r) + 16 h (the INT3 low plane).
+__global__ void repack_int2_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K, int32_t* err) {
+  const int64_t per_expert = (int64_t)(K / 128) * (N_pad / 16) * 32;  // (block, lane)
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t blk = rem / 32;
+    const int lane = (int)(rem % 32);
+    const int G = (int)(blk / (N_pad / 16));
+    const int nb = (int)(blk % (N_pad / 16));
+    const uint32_t* wce = wc + e * (int64_t)N * (K / 16);
+    uint32_t lo[4] = {0, 0, 0, 0};
+    const int g = lane >> 2, t = lane & 3;
+    for (int s = 0; s < 8; ++s)
+      for (int r = 0; r < 4; ++r)
+        for (int h = 0; h < 2; ++h) {
+          const int row = g + 8 * (r & 1);
+          const int k = G * 128 + 16 * s + 4 * t + 2 * (r >> 1) + h;
+          const int64_t n = (int64_t)nb * 16 + row;
+          int32_t q = 0;
+          if (n < N) {
+            const uint32_t f = (wce[n * (K / 16) + k / 16] >> (2 * (k % 16))) & 3u;
+            q = f >= 2u ? (int32_t)f - 4 : (int32_t)f;
+            if (q == -2) {  // outside the symmetric range
+              set_error(err, QW_ERR_VALUE);
+              q = 0;
+            }
+          }
+          lo[s / 2] |= (uint32_t)(q + 2) << (2 * (4 * (s % 2) + r) + 16 * h);
+        }
+    uint32_t* out = wp + e * (int64_t)(K / 128) * (N_pad / 16) * 128 + blk * 128;
+    for (int i = 0; i < 4; ++i) out[lane * 4 + i] = lo[i];
+  }
+}
+
+__global__ void unpack_int2_kernel(const uint32_t* __restrict__ wp, uint32_t* __restrict__ wc,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K) {
+  // one thread per canonical word (16 consecutive k of one row)
+  const int64_t per_expert = (int64_t)N * (K / 16);
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t n = rem / (K / 16);
+    const int k0 = (int)(rem % (K / 16)) * 16;
+    const uint32_t* wpe = wp + e * (int64_t)(K / 128) * (N_pad / 16) * 128;
+    uint32_t out = 0;
+    for (int j = 0; j < 16; ++j) {
+      const int k = k0 + j;
+      const int G = k / 128, kk = k % 128;
+      const int nb = (int)(n / 16), row = (int)(n % 16);
+      const int t = (kk >> 2) & 3, s = kk >> 4, h = kk & 1;
+      const int g = row & 7, r = (row >> 3) | (((kk >> 1) & 1) << 1);
+      const uint32_t L = wpe[((int64_t)G * (N_pad / 16) + nb) * 128 + (g * 4 + t) * 4 + s / 2];
+      const uint32_t u = (L >> (2 * (4 * (s % 2) + r) + 16 * h)) & 3u;
+      out |= ((u - 2u) & 3u) << (2 * j);  // back to two's complement
+    }
+    wc[idx] = out;
+  }
+}
+
 // ----------------------------------------------------------------------------- INT scales
 // canonical [E][N][K/128] <-> packed [E][K/128][N_pad] (zero padded)
 __global__ void repack_int_scales_kernel(const uint16_t* __restrict__ sc, uint16_t* __restrict__ sp,
@@ -456,6 +523,13 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
       }
       break;
     }
+    case QW_W_INT2_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 32;
+      repack_int2_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_canon,
+                                                        (uint32_t*)w_packed, d.E, d.N, d.N_pad,
+                                                        d.K, err);
+      break;
+    }
     case QW_W_INT3_G128_BF16: {
       const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 32;
       repack_int3_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_canon,
@@ -491,7 +565,8 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
     default:
       return QW_ERR_UNSUPPORTED;
   }
-  if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16) {
+  if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16 ||
+      d.wfmt == QW_W_INT2_G128_BF16) {
     const int64_t ts = (int64_t)d.E * (d.K / 128) * d.N_pad;
     repack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
         (const uint16_t*)s_canon, (uint16_t*)s_packed, d.E, d.N, d.N_pad, d.K / 128);
@@ -517,6 +592,13 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
             (const uint16_t*)s_packed, (uint32_t*)s_canon, d.E, d.N, d.N_pad, d.K / 128,
             (int64_t)(d.s_expert_stride / 4));
       }
+      break;
+    }
+    case QW_W_INT2_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * d.N * (d.K / 16);
+      unpack_int2_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_packed,
+                                                        (uint32_t*)w_canon, d.E, d.N, d.N_pad,
+                                                        d.K);
       break;
     }
     case QW_W_INT3_G128_BF16: {
@@ -554,7 +636,8 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
     default:
       return QW_ERR_UNSUPPORTED;
   }
-  if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16) {
+  if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16 ||
+      d.wfmt == QW_W_INT2_G128_BF16) {
     const int64_t ts = (int64_t)d.E * d.N * (d.K / 128);
     unpack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
         (const uint16_t*)s_packed, (uint16_t*)s_canon, d.E, d.N, d.N_pad, d.K / 128);

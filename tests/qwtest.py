@@ -43,7 +43,8 @@ def repack(wfmt, E, N, K, w_canon, s_canon):
 
 def dense_w4a16(prob, bias=None, M=None):
     Q = qw()
-    wfmt = Q.QW_W_INT4_G128_BF16 if prob["bits"] == 4 else Q.QW_W_INT3_G128_BF16
+    wfmt = {4: Q.QW_W_INT4_G128_BF16, 3: Q.QW_W_INT3_G128_BF16,
+            2: Q.QW_W_INT2_G128_BF16}[prob["bits"]]
     d, wp, sp = repack(wfmt, 1, prob["N"], prob["K"], prob["w_canon"], prob["s_canon"])
     A = dev(prob["A"].view(np.int16))
     M = prob["A"].shape[0] if M is None else M

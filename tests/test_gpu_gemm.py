@@ -19,7 +19,7 @@ def assert_parity(C, R, absum, what=""):
 
 
 # ----------------------------------------------------------------------------- W4A16 small M
-@pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("bits", [4, 3, 2])
 @pytest.mark.parametrize("M,N,K", [(1, 16, 128), (3, 40, 384), (8, 2048, 2048), (13, 96, 256),
                                    (16, 200, 640), (16, 128, 1024)])
 def test_w4a16_small_shapes(bits, M, N, K):
@@ -57,7 +57,7 @@ def test_config3_m1_decode_full(bits, N, K):
     assert_parity(C, R, S, f"config 3 W{bits} {N}x{K}")
 
 
-@pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("bits", [4, 3, 2])
 def test_m1_staged_kernel_ragged_n_odd_groups_bias(bits):
     """Single-token decode over a matrix large enough for the staged-activation kernel, with
     N not a multiple of 16, an odd group count (33: the last warp of a CTA gets no group) and
@@ -175,7 +175,7 @@ def test_config2b_w4a8_full_size_sampled_rows():
 
 
 # ----------------------------------------------------------------------------- W4A16 large M
-@pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("bits", [4, 3, 2])
 @pytest.mark.parametrize("M,N,K", [(17, 96, 256), (33, 200, 640), (64, 128, 1024),
                                    (65, 40, 128), (128, 128, 256), (130, 48, 256),
                                    (257, 200, 640), (300, 1280, 4096), (129, 4096, 640)])

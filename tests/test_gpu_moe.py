@@ -141,15 +141,15 @@ def test_moe_grouped_indexed_flags_bad_pairs():
 
 
 @pytest.mark.parametrize("T", [1, 16, 64])
-@pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("bits", [4, 3, 2])
 def test_moe_grouped_w4a16_small_t(T, bits):
     """E=128 top-8, intermediate 640: up-projection K=4096 -> N=1280 (gate+up)."""
     Q = qw()
-    p, logits, sp, off, C = run_moe(Q.QW_A_BF16, 0 if bits == 4 else 1, 128, T, 4096, 1280, 8,
+    p, logits, sp, off, C = run_moe(Q.QW_A_BF16, {4: 0, 3: 1, 2: 6}[bits], 128, T, 4096, 1280, 8,
                                     4, bits=bits)
     _, _, roff, rsp = OM.route(logits, 8)
     tok = rsp // 8
-    q = OF.unpack_int4(p["w_canon"], 4096) if bits == 4 else OF.unpack_int3(p["w_canon"], 4096)
+    q = {4: OF.unpack_int4, 3: OF.unpack_int3, 2: OF.unpack_int2}[bits](p["w_canon"], 4096)
     R, S = OM.grouped_w4a16(p["A"][tok], roff, q, p["s_canon"])
     ok, ratio, frob = OQ.check_bf16_result(C, R, S)
     assert ok, (ratio, frob)

@@ -23,11 +23,11 @@ def roundtrip(wfmt, E, N, K, w_canon, s_canon):
     return host(wc2), host(sc2), d, wp, sp
 
 
-@pytest.mark.parametrize("bits", [4, 3])
+@pytest.mark.parametrize("bits", [4, 3, 2])
 @pytest.mark.parametrize("E,N,K", [(1, 2048, 2048), (3, 40, 384), (2, 1280, 4096), (1, 16, 128)])
 def test_int_roundtrip_bit_exact(bits, E, N, K):
     p = synth.w4a16_problem(1, N, K, bits=bits, E=E, cfg_id=50 + bits)
-    wfmt = 0 if bits == 4 else 1
+    wfmt = {4: 0, 3: 1, 2: 6}[bits]
     wc2, sc2, _, _, _ = roundtrip(wfmt, E, N, K, p["w_canon"], p["s_canon"])
     assert np.array_equal(wc2, p["w_canon"].reshape(-1).view(np.uint8))
     assert np.array_equal(sc2, p["s_canon"].reshape(-1).view(np.uint8))
@@ -99,3 +99,16 @@ def test_bounded_wait_reports_timeout():
     assert Q.qw_read_error(err) == Q.QW_ERR_TIMEOUT
     x = torch.ones(4, device="cuda")
     assert float((x + 1).sum()) == 8.0
+
+
+def test_int2_minus2_flagged():
+    Q = qw()
+    N, K = 16, 128
+    p = synth.w4a16_problem(1, N, K, bits=2, cfg_id=59)
+    bad = p["w_canon"].copy()
+    bad[0, 3, 2] = (bad[0, 3, 2] & ~np.uint32(3 << 6)) | np.uint32(2 << 6)  # element 35 = -2
+    d = Q.qw_repack_query(Q.QW_W_INT2_G128_BF16, 1, N, K)
+    wp, sp = Q.empty_packed(d)
+    err = Q.new_error_flag()
+    Q.qw_repack(d, dev(bad), dev(p["s_canon"]), wp, sp, err)
+    assert Q.qw_read_error(err) == Q.QW_ERR_VALUE
