@@ -81,7 +81,7 @@ const char* qw_status_str(int32_t s) {
   }
 }
 
-int32_t qw_version(void) { return 100; }
+int32_t qw_version(void) { return 200; }
 
 qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_packed_desc* out) {
   if (!out || E < 1 || N < 1 || K < 1) return QW_ERR_INVALID_ARG;
