@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Param
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int q = b0 + 32 * u + lane;
-        const int row = q / per_row;
+        const int row = p.M == 1 ? 0 : q / per_row;  // no division for single-token decode
         const int k0 = g0 * 128 + (q - row * per_row) * 8;
         rowv[u] = row;
         k0v[u] = k0;
