@@ -10,6 +10,9 @@ output stage; section "WnA16": low-bit weights times 16-bit activations; section
   W4A16 with zero points (asymmetric INT4, the section "背景"'s symmetric / asymmetric
   quantization): R[m,n] = sum_k a[m,k] * (q[n,k] - z[n, k // G]) * s[n, k // G],
           q and z unsigned 4-bit                                    (+ bias[n])
+  FP8-weight WnA16 (the section "WnA16"'s floating-point weights up to FP8; E4M3 codes
+  with the same BF16 group-128 scales as the integer formats):
+          R[m,n] = sum_k a[m,k] * e4m3(w[n,k]) * s[n, k // G]          (+ bias[n])
   W4A8:   R[m,n] = sum_k e4m3(a[m,k]) 2^(sa[m,k//32]-127)
                           * e2m1(w[n,k]) 2^(sw[n,k//32]-127)      (+ bias[n])
   W4A4:   R[m,n] = sum_k e2m1(a[m,k]) e4m3(sa[m,k//16])
@@ -25,7 +28,9 @@ beyond it).  Weights are [N][K] (out x in), activations [M][K], results [M][N].
 Pins (tests/test_oracle_gemm.py): exact int64 dot products when every scale is
 1.0 and every operand an integer; exact rational (fractions.Fraction) brute force
 on tiny shapes with several groups; non-square shapes so that a transposed
-operand or a wrong group index changes the result.
+operand or a wrong group index changes the result; FP8-weight: equality with the W4A16
+GEMM on E4M3 codes of integers, and exact rationals over every finite E4M3 code from
+PyTorch's float8_e4m3fn values.
 """
 from __future__ import annotations
 
@@ -65,6 +70,12 @@ def gemm_w4a16_zp(A_bits, q, s_bits, z, bias_bits=None, group: int = 128):
     [N][K/group] zero points -> (R, absum) of w = s * (q - z)."""
     qz = np.asarray(q).astype(np.int64) - np.repeat(np.asarray(z).astype(np.int64), group, axis=-1)
     return gemm_w4a16(A_bits, qz, s_bits, bias_bits, group)
+
+
+def gemm_w8a16_fp8(A_bits, w_codes, s_bits, bias_bits=None, group: int = 128):
+    """A_bits [M][K] BF16, w_codes [N][K] E4M3, s_bits [N][K/group] BF16 -> (R, absum) of
+    w = e4m3(code) * s: the W4A16 product with decoded E4M3 values in place of integers."""
+    return gemm_w4a16(A_bits, F.decode_e4m3(w_codes), s_bits, bias_bits, group)
 
 
 def gemm_w4a8(A_codes, A_sf, w_codes, w_sf, bias_bits=None):
@@ -132,6 +143,19 @@ def w4a16_from_canonical(A_bits, w_canon, s_canon, K, bits, bias_bits=None, rows
         q, s = q[cols], s[cols]
         bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
     return gemm_w4a16(A, q, s, bias_bits)
+
+
+def fp8w_from_canonical(A_bits, w_canon, s_canon, bias_bits=None, rows=None, cols=None):
+    """E4M3 codes [N][K] and BF16 group scales of one expert -> :func:`gemm_w8a16_fp8`
+    (canonical FP8 codes are already one byte per weight)."""
+    A = np.asarray(A_bits)
+    w, s = np.asarray(w_canon), np.asarray(s_canon)
+    if rows is not None:
+        A = A[rows]
+    if cols is not None:
+        w, s = w[cols], s[cols]
+        bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
+    return gemm_w8a16_fp8(A, w, s, bias_bits)
 
 
 def w4a16_zp_from_canonical(A_bits, w_canon, sz_canon, K, bias_bits=None, rows=None,

@@ -220,6 +220,21 @@ def w4a16_zp_problem(M, N, K, *, E=1, cfg_id=0, seed=BASE_SEED, scale_lo=0.005,
     return out
 
 
+def fp8w_problem(M, N, K, *, E=1, cfg_id=0, seed=BASE_SEED, scale_lo=0.005, scale_hi=0.02,
+                 bias=False):
+    """FP8-weight WnA16: E4M3 codes of N(0,1) samples times 2^u, u uniform in [-10, 6] per
+    element (clipped to +-448), so the codes span every E4M3 exponent, subnormals included;
+    a BF16 scale U[scale_lo, scale_hi] per group of 128 along K; BF16 N(0,1) activations."""
+    mag = np.exp2(uniform(stream(cfg_id, 44, seed), (E * N, K), -10.0, 6.0))
+    w = to_e4m3_codes(normal(stream(cfg_id, 40, seed), (E * N, K)) * mag).reshape(E, N, K)
+    s = to_bf16_bits(uniform(stream(cfg_id, 41, seed), (E, N, K // 128), scale_lo, scale_hi))
+    a = to_bf16_bits(normal(stream(cfg_id, 42, seed), (M, K)))
+    out = dict(A=a, w_canon=w, s_canon=s, E=E, N=N, K=K, M=M, fp8=True)
+    if bias:
+        out["bias"] = to_bf16_bits(normal(stream(cfg_id, 43, seed), (E, N)))
+    return out
+
+
 def w4a8_problem(M, N, K, *, E=1, cfg_id=1, seed=BASE_SEED, sf_lo=118, sf_hi=126,
                  bias=False):
     """MXFP4 weights (uniform over the 16 E2M1 codes) and MXFP8 activations
@@ -285,7 +300,8 @@ def router_logits(T, E, *, cfg_id=3, seed=BASE_SEED, bias_std=1.5):
 __all__ = [
     "BASE_SEED", "Stream", "stream", "uniform_int", "uniform", "normal", "random_bytes",
     "to_bf16_bits", "to_e4m3_codes", "pack_int4", "pack_int3", "pack_int2", "pack_nibbles",
-    "unpack_nibbles_layout", "w4a16_problem", "w4a16_zp_problem", "w4a8_problem", "w8a8_problem",
+    "unpack_nibbles_layout", "w4a16_problem", "w4a16_zp_problem", "fp8w_problem", "w4a8_problem",
+    "w8a8_problem",
     "w4a4_problem",
     "router_logits",
 ]

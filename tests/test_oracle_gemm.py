@@ -401,3 +401,79 @@ def test_w4a16_int2_from_canonical_exact():
     one = synth.to_bf16_bits(np.ones((N, K // 128)))
     R, _ = Q.w4a16_from_canonical(synth.to_bf16_bits(a.astype(np.float64)), words, one, K, 2)
     assert np.array_equal(R, (a @ q.T).astype(np.float64))
+
+
+# ----------------------------------------------------------------------------- FP8 weights
+def _e4m3_codes_torch(x):
+    """E4M3 codes by PyTorch's float8_e4m3fn cast (independent of the oracle's decoder)."""
+    t = torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
+def _e4m3_values_torch(codes):
+    return torch.from_numpy(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+
+
+def test_fp8w_equals_w4a16_on_integer_codes():
+    """E4M3 codes of the integers -7..7 are exact: the FP8-weight GEMM must equal the W4A16
+    GEMM on those integers bit for bit, with the same BF16 group scales and bias."""
+    p = synth.w4a16_problem(4, 24, 384, bits=4, cfg_id=60, bias=True)
+    q = F.unpack_int4(p["w_canon"][0], 384).astype(np.int64)
+    codes = _e4m3_codes_torch(q)
+    R1, S1 = Q.gemm_w4a16(p["A"], q, p["s_canon"][0], p["bias"][0])
+    R2, S2 = Q.gemm_w8a16_fp8(p["A"], codes, p["s_canon"][0], p["bias"][0])
+    assert np.array_equal(R1, R2) and np.array_equal(S1, S2)
+
+
+def test_fp8w_fraction_brute_force_with_subnormal_codes():
+    """Random codes over every finite E4M3 code (subnormals included), two groups with
+    different scales: exact rationals from PyTorch's E4M3 values."""
+    rng = np.random.default_rng(61)
+    M, N, K = 2, 3, 256
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    codes = rng.choice(finite, (N, K))
+    codes[0, :16] = np.arange(16, dtype=np.uint8)  # zero and the subnormal / small codes
+    s = synth.to_bf16_bits(rng.uniform(0.25, 4.0, (N, K // 128)))
+    a = synth.to_bf16_bits(rng.normal(size=(M, K)))
+    R, absum = Q.fp8w_from_canonical(a, codes, s)
+    wv = _e4m3_values_torch(codes)
+    av, sv = F.decode_bf16(a), F.decode_bf16(s)
+    for m in range(M):
+        for n in range(N):
+            ex = sum(Fraction(float(av[m, k])) * Fraction(float(wv[n, k])) *
+                     Fraction(float(sv[n, k // 128])) for k in range(K))
+            assert abs(Fraction(R[m, n]) - ex) <= Fraction(2.0 ** -50) * Fraction(absum[m, n])
+
+
+def test_fp8w_from_canonical_rows_and_cols():
+    p = synth.fp8w_problem(6, 20, 256, cfg_id=62, bias=True)
+    R, S = Q.fp8w_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], p["bias"][0])
+    rows, cols = np.array([1, 4]), np.array([0, 7, 19])
+    R2, S2 = Q.fp8w_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], p["bias"][0],
+                                   rows=rows, cols=cols)
+    assert np.array_equal(R[np.ix_(rows, cols)], R2) and np.array_equal(S[np.ix_(rows, cols)], S2)
+
+
+def test_fp8w_rejects_nan_codes():
+    codes = np.zeros((2, 128), np.uint8)
+    codes[1, 5] = 0xFF
+    with pytest.raises(F.FormatError):
+        Q.gemm_w8a16_fp8(synth.to_bf16_bits(np.ones((1, 128))), codes,
+                         synth.to_bf16_bits(np.ones((2, 1))))
+
+
+def test_planted_subnormal_e4m3_decode_is_caught(monkeypatch):
+    """A decoder that treats exponent 0 as normal must fail the brute-force pin."""
+    good = F.decode_e4m3
+
+    def bad(codes):
+        c = np.asarray(codes).astype(np.int64)
+        v = good(codes)
+        e, m = (c >> 3) & 0xF, c & 7
+        wrong = (1.0 + m / 8.0) * 2.0 ** -7 * np.where((c >> 7) & 1, -1.0, 1.0)
+        return np.where((e == 0) & (m != 0), wrong, v)
+
+    monkeypatch.setattr(F, "decode_e4m3", bad)
+    with pytest.raises(AssertionError):
+        test_fp8w_fraction_brute_force_with_subnormal_codes()
