@@ -265,6 +265,53 @@ def extra_w4a16(steps, warmup, world, only=None):
     return out
 
 
+def extra_fp8w(steps, warmup, world, only=None):
+    """FP8-weight WnA16 (E4M3 codes, BF16 group-128 scales, BF16 activations): the M=1 decode
+    shapes (weight GB/s of codes + scales) and one large-M dense GEMM on the tcgen05 path
+    (TFLOP/s against the measured BF16 burst: the MMAs are BF16)."""
+    import moe_qw_repack_gb300.qw as Q
+    out = {}
+    peaks, _ = measured_peaks()
+    for name, M, N, K in [("fp8w_m1_14336x4096", 1, 14336, 4096),
+                          ("fp8w_m1_4096x14336", 1, 4096, 14336),
+                          ("fp8w_4096x14336x4096", 4096, 14336, 4096)]:
+        if only and only not in name:
+            continue
+        p = synth.fp8w_problem(M, N, K, cfg_id=970)
+        d = Q.qw_repack_query(Q.QW_W_FP8E4M3_G128_BF16, 1, N, K)
+        wp, sp = Q.empty_packed(d)
+        Q.qw_repack(d, torch.from_numpy(p["w_canon"]).cuda(), torch.from_numpy(p["s_canon"]).cuda(),
+                    wp, sp)
+        A = torch.from_numpy(p["A"].view(np.int16)).cuda()
+        step_in = d.w_bytes + d.s_bytes + (A.numel() * 2 if M > 1 else 0)
+        R = replicas_for(step_in)
+        copies = [(wp, sp, A)] + [(wp.clone(), sp.clone(), A.clone() if M > 1 else A)
+                                  for _ in range(R - 1)]
+        C = torch.empty((M, N), dtype=torch.int16, device="cuda")
+        wsn = Q.qgemm_workspace_size(d, Q.QW_A_BF16, M)
+        ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
+
+        def fn(i, copies=copies, d=d, C=C, M=M, ws=ws, wsn=wsn):
+            w, s_, a = copies[i % len(copies)]
+            Q.qgemm_dense(d, w, s_, Q.QW_A_BF16, a, None, None, C, M, ws, wsn)
+        if M == 1:
+            ms, n, graph = time_region([fn], max(steps, R), warmup, world, graph_steps=R)
+            wbytes = N * K + N * (K // 128) * 2
+            gbs = wbytes / (ms * 1e-3) / 1e9
+            out[name] = {"us": round(ms * 1e3, 2), "weight_GBps": round(gbs, 1),
+                         "hbm_frac": round(gbs / peaks["hbm_gbs"], 3), "launches": n,
+                         "weight_copies": R, "graph": graph}
+        else:
+            ms, n, _ = time_region([fn], max(5, min(steps, 50)), warmup, world)
+            tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+            out[name] = {"us": round(ms * 1e3, 1), "tflops": round(tf, 1),
+                         "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 3),
+                         "input_copies": R, "steps": n}
+        del copies
+        torch.cuda.empty_cache()
+    return out
+
+
 def extra_w4a8_decode(steps, warmup, world):
     """Single-token W4A8 (MXFP4 weights x MXFP8 activations) decode on the M=1 decode
     shapes: device time per GEMM (CUDA graph of back-to-back launches over weight copies
@@ -555,6 +602,7 @@ def run_ours(args, world, rank):
         line["extra"].update(extra_w8a8(max(5, min(args.steps, 100)), 3, world))
         line["extra"].update(extra_w4a4(max(5, min(args.steps, 100)), 3, world))
         line["extra"].update(extra_w4a8_decode(max(5, min(args.steps, 200)), 3, world))
+        line["extra"].update(extra_fp8w(max(5, min(args.steps, 200)), 3, world))
         line["extra"].update(extra_moe(max(5, min(args.steps, 40)), 3, world))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
@@ -638,9 +686,11 @@ def main():
                     help="time only the W4A16 GEMV workloads (a profiling aid)")
     ap.add_argument("--only-moe", action="store_true",
                     help="time only the grouped MoE workloads (a profiling aid)")
+    ap.add_argument("--only-fp8w", action="store_true",
+                    help="time only the FP8-weight WnA16 workloads (a profiling aid)")
     ap.add_argument("--case", default=None,
-                    help="with --only-w4a16 / --only-moe: run only the cases whose name "
-                         "contains this string")
+                    help="with --only-w4a16 / --only-moe / --only-fp8w: run only the cases "
+                         "whose name contains this string")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     if args.impl == "reference":
@@ -653,6 +703,9 @@ def main():
     elif args.only_moe:
         world, rank, _ = dist_setup()
         line = {"extra": extra_moe(args.steps, args.warmup, world, args.case)}
+    elif args.only_fp8w:
+        world, rank, _ = dist_setup()
+        line = {"extra": extra_fp8w(args.steps, args.warmup, world, args.case)}
     else:
         world, rank, _ = dist_setup()
         line = run_ours(args, world, rank)

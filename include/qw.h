@@ -70,7 +70,8 @@ typedef enum qw_wfmt {
   QW_W_NVFP4_G16 = 4,      /* E2M1 codes, unsigned E4M3 scale per 16 along K (W4A4)       */
   QW_W_UINT4ZP_G128_BF16 = 5, /* unsigned 4-bit codes, BF16 scale and zero point per 128:
                                  w = s * (q - z) (asymmetric INT4)                         */
-  QW_W_INT2_G128_BF16 = 6  /* symmetric INT2 in {-1, 0, 1}, BF16 scale per 128 along K    */
+  QW_W_INT2_G128_BF16 = 6, /* symmetric INT2 in {-1, 0, 1}, BF16 scale per 128 along K    */
+  QW_W_FP8E4M3_G128_BF16 = 7 /* E4M3 codes, BF16 scale per 128 along K (FP8-weight WnA16) */
 } qw_wfmt;
 
 typedef enum qw_afmt {
@@ -126,6 +127,7 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *   NVFP4: w_canon uint8 [E][N][K/2] as MXFP4.  s_canon uint8 E4M3 [E][N][K/16] (unsigned).
  *   INT2:  w_canon uint32 [E][N][K/16]; element k = 16j+i at bits [2i,2i+2) of word j,
  *          two's complement (-2 rejected).  s_canon BF16 [E][N][K/128].
+ *   FP8E4M3: w_canon uint8 [E][N][K] E4M3 codes.  s_canon BF16 [E][N][K/128].
  *   UINT4ZP: w_canon uint32 [E][N][K/8] packed as INT4 but read unsigned (q in [0, 15]).
  *          s_canon uint32 [E][N][K/128]: bits 0-15 the BF16 scale, bits 16-23 the zero
  *          point z in [0, 15], bits 24-31 zero (else a value error).
@@ -147,6 +149,11 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *   INT2:  per expert [K/128][N_pad/16] blocks of 512 B: 32 lanes x 4 words holding q + 2
  *          for the lane's 64 weights (the INT4 (row, k) assignment) in the INT3 low-plane
  *          bit positions.  Scales BF16 [K/128][N_pad].
+ *   FP8E4M3: per expert [K/128][N_pad/16] blocks of 2 KiB: 32 lanes x 16 words; byte b of
+ *          word 2s + j of lane l = 4g + t is the code of row g + 8 (b >> 1) at
+ *          k = 16s + 4t + 2j + (b & 1) (the INT4 (row, k) assignment, one byte per weight:
+ *          each 16-bit half is one BF16 pair of the MMA fragment once decoded).
+ *          Scales BF16 [K/128][N_pad].
  *   UINT4ZP: codes in the INT4 block layout with the nibble q itself (an excess code
  *          whose excess is the group's zero point); scales: BF16 [K/128][N_pad] as INT4,
  *          then (at s_expert_stride / 2) the BF16 numbers 128 + z in the same layout.
@@ -187,7 +194,8 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
 /* --------------------------------------------------------------------------------------
  * qgemm_dense - C[M][N] = bf16( sum_k a[m,k] * w[n,k] + bias[n] ) with the weight
  * dequantization (and, for W4A8, both block scales) applied inside the kernel.
- *   W4A16: desc->wfmt INT4/INT3/INT2/UINT4ZP, afmt QW_A_BF16, A BF16 [M][K], A_sf NULL.
+ *   W4A16: desc->wfmt INT4/INT3/INT2/UINT4ZP/FP8E4M3, afmt QW_A_BF16, A BF16 [M][K],
+ *          A_sf NULL.
  *   W4A8:  desc->wfmt MXFP4,     afmt QW_A_MXFP8_G32, A E4M3 [M][K], A_sf E8M0 [M][K/32].
  *   W8A8:  desc->wfmt MXFP8,     afmt QW_A_MXFP8_G32, as W4A8.
  *   W4A4:  desc->wfmt NVFP4,     afmt QW_A_NVFP4_G16, A E2M1 [M][K/2], A_sf E4M3 [M][K/16]

@@ -361,6 +361,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 v[4 * st + 1] = bf16x2_sub_u32(and_or(w[st] >> 8, 0x000F000Fu, magic), ex_lo);
                 v[4 * st + 3] = bf16x2_sub_u32(and_or(w[st] >> 12, 0x000F000Fu, magic), ex_hi);
               }
+            } else if constexpr (BITS == 8) {
+              // E4M3 codes: words 2st (rows g, g + 8 at k + 0/1) and 2st + 1 (k + 2/3),
+              // decoded exactly, no excess
+              uint32_t w[16];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 x4 = lds128(blk + lane * 64 + 16 * i);
+                w[4 * i] = x4.x; w[4 * i + 1] = x4.y; w[4 * i + 2] = x4.z; w[4 * i + 3] = x4.w;
+              }
+#pragma unroll
+              for (int st = 0; st < 8; ++st) {
+                v[4 * st + 0] = e4m3x2_to_bf16x2(w[2 * st]);
+                v[4 * st + 2] = e4m3x2_to_bf16x2(w[2 * st] >> 16);
+                v[4 * st + 1] = e4m3x2_to_bf16x2(w[2 * st + 1]);
+                v[4 * st + 3] = e4m3x2_to_bf16x2(w[2 * st + 1] >> 16);
+              }
             } else if constexpr (BITS == 2) {
               const uint4 lo = lds128(blk + lane * 16);
               const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w};
@@ -512,7 +528,9 @@ qw_status launch_bits(const CUtensorMap& tmA, const CUtensorMap& tmC, const Para
                       int64_t tiles_max, cudaStream_t st) {
   using GE = Geo<BITS, ZP>;
   // ring + output staging + barriers + alignment
-  const size_t smem = (size_t)STAGES * GE::STAGE + STAGING_BYTES + 256 + 1024;
+  constexpr size_t kSmem = (size_t)STAGES * GE::STAGE + STAGING_BYTES + 256 + 1024;
+  static_assert(kSmem <= 232448, "shared memory of one CTA");
+  const size_t smem = kSmem;
   static const cudaError_t attr = cudaFuncSetAttribute(
       gemm_w4a16_tc_kernel<BITS, ZP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (attr != cudaSuccess) return QW_ERR_CUDA;
@@ -590,6 +608,7 @@ qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
   const int64_t tiles_max = max_m * p.num_n_tiles;
   if (d.wfmt == QW_W_UINT4ZP_G128_BF16) return launch_bits<4, true>(tmA, tmC, p, tiles_max, st);
   if (d.wfmt == QW_W_INT2_G128_BF16) return launch_bits<2, false>(tmA, tmC, p, tiles_max, st);
+  if (d.wfmt == QW_W_FP8E4M3_G128_BF16) return launch_bits<8, false>(tmA, tmC, p, tiles_max, st);
   return d.wfmt == QW_W_INT4_G128_BF16 ? launch_bits<4, false>(tmA, tmC, p, tiles_max, st)
                                        : launch_bits<3, false>(tmA, tmC, p, tiles_max, st);
 }

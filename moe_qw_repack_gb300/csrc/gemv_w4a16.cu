@@ -165,7 +165,8 @@ template <int BITS>
 struct Geo {
   static constexpr int BLK = BITS * 256;                      // one 16 x 128 block
   static constexpr int WPG = BITS * 2;                        // words per lane and group
-  static constexpr float BIAS = 128.f + (1 << (BITS - 1));   // 128 + excess
+  static constexpr bool FP = BITS == 8;                       // E4M3 codes: no excess
+  static constexpr float BIAS = FP ? 0.f : 128.f + (1 << (BITS - 1));  // 128 + excess
 };
 
 // groups per batch = register ring depth (token rows cost registers)
@@ -231,7 +232,7 @@ __device__ __forceinline__ void item_of(const Params& p, uint32_t item, uint32_t
 }
 
 // The lane's packed words of one 16 x 128 block (INT4: 8 words; INT3: 4 lo + 2 hi words;
-// INT2: 4 words).
+// INT2: 4 words; E4M3: 16 words).
 template <int BITS>
 __device__ __forceinline__ void load_words(const uint8_t* blk, int lane,
                                            uint32_t (&w)[Geo<BITS>::WPG]) {
@@ -243,6 +244,12 @@ __device__ __forceinline__ void load_words(const uint8_t* blk, int lane,
   } else if constexpr (BITS == 2) {
     const uint4 v = __ldcs(reinterpret_cast<const uint4*>(blk) + lane);
     w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else if constexpr (BITS == 8) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(blk) + lane * 4 + i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
   } else {
     const uint4 lo = __ldcs(reinterpret_cast<const uint4*>(blk) + lane);
     const uint2 hi = __ldcs(reinterpret_cast<const uint2*>(blk + 512) + lane);
@@ -277,15 +284,40 @@ __device__ __forceinline__ BatchPtr batch_ptr(const Params& p, uint32_t qb, uint
 }
 
 // Step S of a group -> four BF16x2 A-fragment registers holding 128 + code.
+// E4M3 codes: words 2s (rows g, g + 8 at k + 0/1) and 2s + 1 (at k + 2/3) -> the four
+// registers as they are (no excess).
 template <int BITS>
 __device__ __forceinline__ void biased_all(const uint32_t (&w)[Geo<BITS>::WPG], int s,
                                            uint32_t (&a)[4]) {
-  uint32_t w8[8];
+  if constexpr (BITS == 8) {
+    a[0] = e4m3x2_to_bf16x2(w[2 * s]);
+    a[1] = e4m3x2_to_bf16x2(w[2 * s] >> 16);
+    a[2] = e4m3x2_to_bf16x2(w[2 * s + 1]);
+    a[3] = e4m3x2_to_bf16x2(w[2 * s + 1] >> 16);
+  } else {
+    uint32_t w8[8];
 #pragma unroll
-  for (int i = 0; i < Geo<BITS>::WPG; ++i) w8[i] = w[i];
+    for (int i = 0; i < Geo<BITS>::WPG; ++i) w8[i] = w[i];
 #pragma unroll
-  for (int i = Geo<BITS>::WPG; i < 8; ++i) w8[i] = 0;
-  biased<BITS>(s, w8, a);
+    for (int i = Geo<BITS>::WPG; i < 8; ++i) w8[i] = 0;
+    biased<BITS>(s, w8, a);
+  }
+}
+
+// Step s of a group from a lane's words held in an array of any length (the TMA ring's
+// consumers keep 8 words for the integer formats, 16 for E4M3).
+template <int BITS, int NW>
+__device__ __forceinline__ void decode_step(const uint32_t (&w)[NW], int s, uint32_t (&a)[4]) {
+  if constexpr (BITS == 8) {
+    static_assert(NW == 16, "E4M3 blocks hold 16 words per lane");
+    a[0] = e4m3x2_to_bf16x2(w[2 * s]);
+    a[1] = e4m3x2_to_bf16x2(w[2 * s] >> 16);
+    a[2] = e4m3x2_to_bf16x2(w[2 * s + 1]);
+    a[3] = e4m3x2_to_bf16x2(w[2 * s + 1] >> 16);
+  } else {
+    static_assert(NW == 8, "integer words are passed as 8");
+    biased<BITS>(s, w, a);
+  }
 }
 
 template <int BITS, int MCH, bool ZP>
@@ -293,7 +325,8 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
     gemv_reg_kernel(const Params p) {
   using GE = Geo<BITS>;
   constexpr int WPG = GE::WPG;
-  constexpr int NB = batch_groups(MCH);
+  // E4M3 groups are twice the bytes: half the ring depth in the same registers
+  constexpr int NB = GE::FP ? (batch_groups(MCH) + 1) / 2 : batch_groups(MCH);
   extern __shared__ float red[];  // [warp][MCH][4][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -394,7 +427,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
                 uint32_t a[4];
                 biased_all<BITS>(w, st, a);
                 mma_bf16_16816(pr[0], a, x.x, x.y);
-                mma_bf16_16816(sm[0], ones, x.x, x.y);
+                if constexpr (!GE::FP) mma_bf16_16816(sm[0], ones, x.x, x.y);
               }
             } else {
 #pragma unroll
@@ -405,7 +438,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
                 for (int c = 0; c < MCH; ++c) {
                   const uint2 x = __ldg(reinterpret_cast<const uint2*>(abase[c] + j * 128 + 16 * s));
                   mma_bf16_16816(pr[c], a, x.x, x.y);
-                  mma_bf16_16816(sm[c], ones, x.x, x.y);
+                  if constexpr (!GE::FP) mma_bf16_16816(sm[c], ones, x.x, x.y);
                 }
               }
             }
@@ -430,8 +463,10 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
             for (int s = 0; s < 8; ++s) {
               uint32_t a[4];
               biased_all<BITS>(w, s, a);
+              if constexpr (!GE::FP) {
 #pragma unroll
-              for (int r = 0; r < 4; ++r) a[r] = bf16x2_sub(a[r], bias2);  // exact
+                for (int r = 0; r < 4; ++r) a[r] = bf16x2_sub(a[r], bias2);  // exact
+              }
 #pragma unroll
               for (int c = 0; c < MCH; ++c) {
                 const uint2 x = __ldg(reinterpret_cast<const uint2*>(abase[c] + j * 128 + 16 * s));
@@ -533,7 +568,7 @@ template <int BITS, bool ZP>
 __global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Params p) {
   using GE = Geo<BITS>;
   constexpr int WPG = GE::WPG;
-  constexpr int R = kM8Ring;
+  constexpr int R = GE::FP ? kM8Ring / 2 : kM8Ring;  // E4M3: twice the words per group
   extern __shared__ uint4 m8_smem[];
   const int G = p.K >> 7;
   uint8_t* act = reinterpret_cast<uint8_t*>(m8_smem);
@@ -734,6 +769,8 @@ struct Ring {
 };
 // grouped (MoE) calls: many short items, several CTAs per SM
 using GroupedRing = Ring<4, 4, 4>;
+// E4M3 weights: 16 KiB stages, three CTAs per SM fit
+using GroupedRing8 = Ring<4, 4, 3>;
 
 template <int BITS, bool ZP>
 struct TmaGeo {
@@ -742,7 +779,8 @@ struct TmaGeo {
   static constexpr int S_STAGE = kStageGroups * 16 * 2;  // BF16 scales of 16 rows x 8 groups
   // asymmetric INT4: the same rows and groups of BF16 128 + z follow the scales
   static constexpr int STAGE = W_STAGE + S_STAGE * (ZP ? 2 : 1);
-  static constexpr float BIAS = 128.f + (1 << (BITS - 1));  // 128 + excess
+  static constexpr bool FP = BITS == 8;  // E4M3 codes: no excess
+  static constexpr float BIAS = FP ? 0.f : 128.f + (1 << (BITS - 1));  // 128 + excess
 };
 
 template <int BITS, int MCH, class R, bool ZP>
@@ -894,7 +932,7 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
             const int gg = ch * kStageGroups + j;
             if (gg < G) {
               const uint32_t blk = sbase + j * GE::BLK;
-              uint32_t w[8];
+              uint32_t w[BITS == 8 ? 16 : 8];
               if constexpr (BITS == 4) {
                 const uint4 v0 = lds128(blk + lane * 32), v1 = lds128(blk + lane * 32 + 16);
                 w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
@@ -903,6 +941,12 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
                 const uint4 v = lds128(blk + lane * 16);
                 w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
                 w[4] = w[5] = w[6] = w[7] = 0;
+              } else if constexpr (BITS == 8) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const uint4 v = lds128(blk + lane * 64 + 16 * i);
+                  w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+                }
               } else {
                 const uint4 lo = lds128(blk + lane * 16);
                 const uint2 hi = lds64(blk + 512 + lane * 8);
@@ -937,12 +981,12 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
 #pragma unroll
                 for (int st = 0; st < 8; ++st) {
                   uint32_t a[4];
-                  biased<BITS>(st, w, a);
+                  decode_step<BITS>(w, st, a);
 #pragma unroll
                   for (int c = 0; c < MCH; ++c) {
                     const uint2 x = __ldg(reinterpret_cast<const uint2*>(arow[c] + koff + 16 * st));
                     mma_bf16_16816(pr[c], a, x.x, x.y);
-                    mma_bf16_16816(sm[c], ones, x.x, x.y);
+                    if constexpr (!GE::FP) mma_bf16_16816(sm[c], ones, x.x, x.y);
                   }
                 }
 #pragma unroll
@@ -962,9 +1006,11 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
 #pragma unroll
                 for (int st = 0; st < 8; ++st) {
                   uint32_t a[4];
-                  biased<BITS>(st, w, a);
+                  decode_step<BITS>(w, st, a);
+                  if constexpr (!GE::FP) {
 #pragma unroll
-                  for (int r = 0; r < 4; ++r) a[r] = bf16x2_sub(a[r], bias2);  // exact
+                    for (int r = 0; r < 4; ++r) a[r] = bf16x2_sub(a[r], bias2);  // exact
+                  }
 #pragma unroll
                   for (int c = 0; c < MCH; ++c) {
                     const uint2 x = __ldg(reinterpret_cast<const uint2*>(arow[c] + koff + 16 * st));
@@ -1079,6 +1125,7 @@ qw_status launch_dense_m8(const qw_packed_desc& d, const void* w_packed, const v
     return launch_m8_variant<4, true>(p, st);
   }
   if (d.wfmt == QW_W_INT2_G128_BF16) return launch_m8_variant<2, false>(p, st);
+  if (d.wfmt == QW_W_FP8E4M3_G128_BF16) return launch_m8_variant<8, false>(p, st);
   return d.wfmt == QW_W_INT4_G128_BF16 ? launch_m8_variant<4, false>(p, st)
                                        : launch_m8_variant<3, false>(p, st);
 }
@@ -1111,6 +1158,9 @@ qw_status launch_dense_reg(const qw_packed_desc& d, const void* w_packed, const 
   if (d.wfmt == QW_W_INT2_G128_BF16)
     return mch == 1 ? launch_reg_variant<2, 1, false>(p, items, st)
                     : launch_reg_variant<2, 2, false>(p, items, st);
+  if (d.wfmt == QW_W_FP8E4M3_G128_BF16)
+    return mch == 1 ? launch_reg_variant<8, 1, false>(p, items, st)
+                    : launch_reg_variant<8, 2, false>(p, items, st);
   const bool int4 = d.wfmt == QW_W_INT4_G128_BF16;
   if (mch == 1)
     return int4 ? launch_reg_variant<4, 1, false>(p, items, st)
@@ -1144,7 +1194,11 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   const bool zp = d.wfmt == QW_W_UINT4ZP_G128_BF16;
   const bool int4 = d.wfmt == QW_W_INT4_G128_BF16 || zp;
   const bool int2 = d.wfmt == QW_W_INT2_G128_BF16;
-  const int blk = int4 ? kInt4BlockBytes : (int2 ? kInt2BlockBytes : kInt3BlockBytes);
+  const bool fp8 = d.wfmt == QW_W_FP8E4M3_G128_BF16;
+  const int blk = int4 ? kInt4BlockBytes
+                  : int2 ? kInt2BlockBytes
+                  : fp8  ? kFp8BlockBytes
+                         : kInt3BlockBytes;
   const int G = d.K / kIntGroup;
   const int64_t nblocks = d.N_pad / 16;
   auto enc = encode_fn();
@@ -1215,10 +1269,12 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
     return zp     ? launch_tma_variant<4, 1, GroupedRing, true>(tmW, tmS, tmZ, p, size_items, st)
            : int4 ? launch_tma_variant<4, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
            : int2 ? launch_tma_variant<2, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
+           : fp8  ? launch_tma_variant<8, 1, GroupedRing8, false>(tmW, tmS, tmZ, p, size_items, st)
                   : launch_tma_variant<3, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st);
   return zp     ? launch_tma_variant<4, 2, GroupedRing, true>(tmW, tmS, tmZ, p, size_items, st)
          : int4 ? launch_tma_variant<4, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
          : int2 ? launch_tma_variant<2, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
+         : fp8  ? launch_tma_variant<8, 2, GroupedRing8, false>(tmW, tmS, tmZ, p, size_items, st)
                 : launch_tma_variant<3, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st);
 }
 

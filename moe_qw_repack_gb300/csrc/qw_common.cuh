@@ -216,6 +216,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Two E4M3 codes (the low 16 bits of `pair`, first code in the low byte) -> BF16 pair,
+// exactly: every E4M3 value is an FP16 number (one hardware conversion), and FP16 -> FP32
+// -> BF16 keeps it (at most 4 significant bits, exponents -9 .. 8).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t pair) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)pair));
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0; }
 
 }  // namespace qw

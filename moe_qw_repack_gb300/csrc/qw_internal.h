@@ -17,6 +17,7 @@ constexpr int kMxGroup = 32;         // K elements per E8M0 scale (MX formats)
 constexpr int kInt4BlockBytes = 1024;  // 16 rows x 128 k of INT4, fragment order
 constexpr int kInt2BlockBytes = 512;   // 16 rows x 128 k of INT2, fragment order
 constexpr int kInt3BlockBytes = 768;   // 16 rows x 128 k of INT3 (two bit planes)
+constexpr int kFp8BlockBytes = 2048;   // 16 rows x 128 k of E4M3 codes, fragment order
 constexpr int kSfChunkBytes = 512;     // 128 rows x 4 groups of E8M0 scales
 constexpr int kNvGroup = 16;           // K elements per E4M3 scale (NVFP4)
 constexpr int kNvChunkBytes = 2048;    // 128 rows x 16 groups of E4M3 scales (NVFP4)

@@ -258,10 +258,76 @@ __global__ void unpack_int2_kernel(const uint32_t* __restrict__ wp, uint32_t* __
   }
 }
 
+// ----------------------------------------------------------------------------- FP8 weights
+// Packed FP8 (E4M3) weights: byte b of word u = 2s + j of lane l = 4g + t holds the code of
+// row g + 8 (b >> 1), k = 16s + 4t + 2j + (b & 1) - the INT4 (row, k) assignment with one
+// byte per weight, so each 16-bit half decodes to one BF16 pair of the m16n8k16 A fragment
+// (and of the 16-lane TMEM store).  NaN codes (0x7F, 0xFF) are value errors, packed as 0.
+__global__ void repack_fp8w_kernel(const uint8_t* __restrict__ wc, uint32_t* __restrict__ wp,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K, int32_t* err) {
+  const int64_t per_expert = (int64_t)(K / 128) * (N_pad / 16) * 512;  // words
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t blk = rem / 512;
+    const int w = (int)(rem % 512);
+    const int lane = w >> 4, u = w & 15;
+    const int G = (int)(blk / (N_pad / 16));
+    const int nb = (int)(blk % (N_pad / 16));
+    const int g = lane >> 2, t = lane & 3, s = u >> 1, j = u & 1;
+    const uint8_t* wce = wc + e * (int64_t)N * K;
+    uint32_t out = 0;
+    for (int b = 0; b < 4; ++b) {
+      const int64_t n = (int64_t)nb * 16 + g + 8 * (b >> 1);
+      const int k = G * 128 + 16 * s + 4 * t + 2 * j + (b & 1);
+      uint32_t c = 0;  // padding rows: zero
+      if (n < N) {
+        c = wce[n * K + k];
+        if ((c & 0x7Fu) == 0x7Fu) {
+          set_error(err, QW_ERR_VALUE);
+          c = 0;
+        }
+      }
+      out |= c << (8 * b);
+    }
+    wp[idx] = out;
+  }
+}
+
+__global__ void unpack_fp8w_kernel(const uint32_t* __restrict__ wp, uint32_t* __restrict__ wc,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K) {
+  // one thread per 4 consecutive canonical codes of one row (k0 % 4 == 0)
+  const int64_t per_expert = (int64_t)N * (K / 4);
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t n = rem / (K / 4);
+    const int k0 = (int)(rem % (K / 4)) * 4;
+    const uint32_t* wpe = wp + e * (int64_t)(K / 128) * (N_pad / 16) * 512;
+    const int G = k0 / 128, kk = k0 % 128;
+    const int nb = (int)(n / 16), row = (int)(n % 16);
+    const int g = row & 7, hi = row >> 3, t = (kk >> 2) & 3, s = kk >> 4;
+    const uint32_t* lw = wpe + ((int64_t)G * (N_pad / 16) + nb) * 512 + (g * 4 + t) * 16 + 2 * s;
+    uint32_t out = 0;
+    for (int i = 0; i < 4; ++i) {  // k0 + i: word 2s + (i >> 1), byte 2 hi + (i & 1)
+      const uint32_t c = (lw[i >> 1] >> (8 * (2 * hi + (i & 1)))) & 0xFFu;
+      out |= c << (8 * i);
+    }
+    wc[idx] = out;
+  }
+}
+
 // ----------------------------------------------------------------------------- INT scales
 // canonical [E][N][K/128] <-> packed [E][K/128][N_pad] (zero padded)
+// Experts sit `estride` halfwords apart (the descriptor's scale stride: G * N_pad rounded up
+// to 256 bytes).
 __global__ void repack_int_scales_kernel(const uint16_t* __restrict__ sc, uint16_t* __restrict__ sp,
-                                         int32_t E, int32_t N, int32_t N_pad, int32_t G) {
+                                         int32_t E, int32_t N, int32_t N_pad, int32_t G,
+                                         int64_t estride) {
   const int64_t total = (int64_t)E * G * N_pad;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -269,11 +335,12 @@ __global__ void repack_int_scales_kernel(const uint16_t* __restrict__ sc, uint16
     const int64_t rem = idx % ((int64_t)G * N_pad);
     const int g = (int)(rem / N_pad);
     const int n = (int)(rem % N_pad);
-    sp[idx] = (n < N) ? sc[(e * N + n) * G + g] : (uint16_t)0;
+    sp[e * estride + rem] = (n < N) ? sc[(e * N + n) * G + g] : (uint16_t)0;
   }
 }
 __global__ void unpack_int_scales_kernel(const uint16_t* __restrict__ sp, uint16_t* __restrict__ sc,
-                                         int32_t E, int32_t N, int32_t N_pad, int32_t G) {
+                                         int32_t E, int32_t N, int32_t N_pad, int32_t G,
+                                         int64_t estride) {
   const int64_t total = (int64_t)E * N * G;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -281,7 +348,7 @@ __global__ void unpack_int_scales_kernel(const uint16_t* __restrict__ sp, uint16
     const int64_t rem = idx % ((int64_t)N * G);
     const int n = (int)(rem / G);
     const int g = (int)(rem % G);
-    sc[idx] = sp[(e * G + g) * N_pad + n];
+    sc[idx] = sp[e * estride + (int64_t)g * N_pad + n];
   }
 }
 
@@ -530,6 +597,13 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
                                                         d.K, err);
       break;
     }
+    case QW_W_FP8E4M3_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 512;
+      repack_fp8w_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint8_t*)w_canon,
+                                                        (uint32_t*)w_packed, d.E, d.N, d.N_pad,
+                                                        d.K, err);
+      break;
+    }
     case QW_W_INT3_G128_BF16: {
       const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 32;
       repack_int3_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_canon,
@@ -566,10 +640,11 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
       return QW_ERR_UNSUPPORTED;
   }
   if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16 ||
-      d.wfmt == QW_W_INT2_G128_BF16) {
+      d.wfmt == QW_W_INT2_G128_BF16 || d.wfmt == QW_W_FP8E4M3_G128_BF16) {
     const int64_t ts = (int64_t)d.E * (d.K / 128) * d.N_pad;
     repack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
-        (const uint16_t*)s_canon, (uint16_t*)s_packed, d.E, d.N, d.N_pad, d.K / 128);
+        (const uint16_t*)s_canon, (uint16_t*)s_packed, d.E, d.N, d.N_pad, d.K / 128,
+        (int64_t)(d.s_expert_stride / 2));
   }
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
@@ -597,6 +672,13 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
     case QW_W_INT2_G128_BF16: {
       const int64_t tw = (int64_t)d.E * d.N * (d.K / 16);
       unpack_int2_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_packed,
+                                                        (uint32_t*)w_canon, d.E, d.N, d.N_pad,
+                                                        d.K);
+      break;
+    }
+    case QW_W_FP8E4M3_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * d.N * (d.K / 4);
+      unpack_fp8w_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_packed,
                                                         (uint32_t*)w_canon, d.E, d.N, d.N_pad,
                                                         d.K);
       break;
@@ -637,10 +719,11 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
       return QW_ERR_UNSUPPORTED;
   }
   if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16 ||
-      d.wfmt == QW_W_INT2_G128_BF16) {
+      d.wfmt == QW_W_INT2_G128_BF16 || d.wfmt == QW_W_FP8E4M3_G128_BF16) {
     const int64_t ts = (int64_t)d.E * d.N * (d.K / 128);
     unpack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
-        (const uint16_t*)s_packed, (uint16_t*)s_canon, d.E, d.N, d.N_pad, d.K / 128);
+        (const uint16_t*)s_packed, (uint16_t*)s_canon, d.E, d.N, d.N_pad, d.K / 128,
+        (int64_t)(d.s_expert_stride / 2));
   }
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }

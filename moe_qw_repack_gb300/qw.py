@@ -31,6 +31,7 @@ QW_W_MXFP8_G32 = 3
 QW_W_NVFP4_G16 = 4
 QW_W_UINT4ZP_G128_BF16 = 5
 QW_W_INT2_G128_BF16 = 6
+QW_W_FP8E4M3_G128_BF16 = 7
 QW_A_BF16 = 0
 QW_A_MXFP8_G32 = 1
 QW_A_NVFP4_G16 = 2

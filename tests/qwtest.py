@@ -58,6 +58,23 @@ def dense_w4a16(prob, bias=None, M=None):
     return u16_view(C)
 
 
+def dense_fp8w(prob, bias=None):
+    """FP8-weight WnA16 (E4M3 codes, BF16 group-128 scales) through qgemm_dense."""
+    Q = qw()
+    N, K = prob["N"], prob["K"]
+    d, wp, sp = repack(Q.QW_W_FP8E4M3_G128_BF16, 1, N, K, prob["w_canon"], prob["s_canon"])
+    M = prob["A"].shape[0]
+    C = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    b = None if bias is None else dev(bias.view(np.int16))
+    wsn = Q.qgemm_workspace_size(d, Q.QW_A_BF16, M)
+    ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
+    err = Q.new_error_flag()
+    Q.qgemm_dense(d, wp, sp, Q.QW_A_BF16, dev(prob["A"].view(np.int16)), None, b, C, M, ws, wsn,
+                  err)
+    assert Q.qw_read_error(err) == 0
+    return u16_view(C)
+
+
 def dense_w4a8(prob, bias=None, wfmt=None):
     Q = qw()
     wfmt = Q.QW_W_MXFP4_G32 if wfmt is None else wfmt

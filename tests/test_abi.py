@@ -47,6 +47,8 @@ def test_status_strings(Q):
     (1, 4096, 4096, 4096, 4096, 4096 * 4096 * 3 // 8, 4096 * 32 * 2),
     (2, 3072, 4096, 3072, 4096, 3072 * 2048, 3072 * 128),
     (2, 640, 96, 640, 128, 640 * 64, 640 * 4),
+    (7, 14336, 4096, 14336, 4096, 14336 * 4096, 14336 * 32 * 2),  # E4M3: one byte per weight
+    (7, 40, 384, 48, 384, 48 * 384, 512),
 ])
 def test_repack_query_sizes(Q, wfmt, N, K, npad, kpad, wb, sb):
     d = Q.qw_repack_query(wfmt, 1, N, K)
@@ -55,7 +57,7 @@ def test_repack_query_sizes(Q, wfmt, N, K, npad, kpad, wb, sb):
 
 def test_repack_query_rejects(Q):
     for args in [(0, 1, 16, 100), (1, 1, 16, 64), (2, 1, 16, 48), (9, 1, 16, 128), (0, 0, 16, 128),
-                 (0, 1, 0, 128)]:
+                 (0, 1, 0, 128), (7, 1, 16, 64)]:
         with pytest.raises(Q.QwError):
             Q.qw_repack_query(*args)
 

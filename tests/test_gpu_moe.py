@@ -169,6 +169,22 @@ def test_moe_grouped_w4a16_around_the_path_switch(T):
     assert ok, (ratio, frob)
 
 
+@pytest.mark.parametrize("T", [12, 32])
+@pytest.mark.parametrize("bits", [4, 3, 2])
+def test_moe_grouped_w4a16_ragged_n(T, bits):
+    """N = 264 (a 16-row block and a 128-row tile end inside the matrix; an expert's scale
+    plane, G * N_pad BF16, is not a multiple of 256 bytes, so experts sit at the
+    descriptor's rounded stride): every expert, through the GEMV and the tcgen05 path."""
+    Q = qw()
+    p, logits, sp, off, C = run_moe(Q.QW_A_BF16, {4: 0, 3: 1, 2: 6}[bits], 8, T, 512, 264, 8,
+                                    6 + bits, bits=bits)
+    _, _, roff, rsp = OM.route(logits, 8)
+    q = {4: OF.unpack_int4, 3: OF.unpack_int3, 2: OF.unpack_int2}[bits](p["w_canon"], 512)
+    R, S = OM.grouped_w4a16(p["A"][rsp // 8], roff, q, p["s_canon"])
+    ok, ratio, frob = OQ.check_bf16_result(C, R, S)
+    assert ok, (ratio, frob)
+
+
 def test_moe_grouped_w4a16_down_k640():
     """Down-projection K=640 -> N=4096 (K not a multiple of 256) on a per-pair input."""
     Q = qw()
