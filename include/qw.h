@@ -74,6 +74,14 @@ typedef enum qw_wfmt {
   QW_W_FP8E4M3_G128_BF16 = 7 /* E4M3 codes, BF16 scale per 128 along K (FP8-weight WnA16) */
 } qw_wfmt;
 
+/* Second-level scales (the announcement, section "統一されたquantization表現": the
+ * quantization description carries second-level scales as a parameter of its own).  OR'ed
+ * into any qw_wfmt, it adds one FP32 scale t per output channel and expert on top of the
+ * format's group scales:  C[m][n] = bf16( t[e][n] * sum_k a[m,k] * w[n,k] + bias[n] ).
+ * The descriptor's s_bytes then also covers an FP32 plane [E][N_pad] at byte offset
+ * E * s_expert_stride of s_packed; qw_repack sets it to 1.0 and qw_repack_scale2 writes it. */
+#define QW_W_SCALE2 0x100
+
 typedef enum qw_afmt {
   QW_A_BF16 = 0,           /* BF16 [rows][K]                                          */
   QW_A_MXFP8_G32 = 1,      /* E4M3 codes [rows][K] + E8M0 scales [rows][K/32]          */
@@ -180,6 +188,15 @@ qw_status qw_repack(const qw_packed_desc* desc, const void* w_canon, const void*
 qw_status qw_unpack(const qw_packed_desc* desc, const void* w_packed, const void* s_packed,
                     void* w_canon, void* s_canon, int32_t* d_err, void* stream);
 
+/* qw_repack_scale2 - write the second-level scales t_canon (device FP32 [E][N], 4-byte
+ * aligned) into the packed scale buffer of a descriptor whose wfmt carries QW_W_SCALE2
+ * (QW_ERR_INVALID_ARG otherwise).  A non-finite t is a value error in *d_err (packed as 0).
+ * qw_unpack_scale2 - the inverse: t_canon from s_packed. */
+qw_status qw_repack_scale2(const qw_packed_desc* desc, const float* t_canon, void* s_packed,
+                           int32_t* d_err, void* stream);
+qw_status qw_unpack_scale2(const qw_packed_desc* desc, const void* s_packed, float* t_canon,
+                           void* stream);
+
 /* --------------------------------------------------------------------------------------
  * qgemm_workspace_size - bytes of device workspace qgemm_dense / qgemm_moe_grouped need
  * for up to `max_rows` activation rows (host output `bytes`; 0 is a valid answer).
@@ -201,7 +218,8 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
  *   W4A4:  desc->wfmt NVFP4,     afmt QW_A_NVFP4_G16, A E2M1 [M][K/2], A_sf E4M3 [M][K/16]
  *          (NVFP4 x NVFP4 on tcgen05 kind::mxf4nvf4; a per-tensor FP32 factor of the
  *          format, if any, is the caller's to apply to C).
- *   bias:  BF16 [N] or NULL.  C: BF16 [M][N].  desc->E must be 1.
+ *   bias:  BF16 [N] or NULL.  C: BF16 [M][N].  desc->E must be 1.  With QW_W_SCALE2 in
+ *          desc->wfmt each channel's sum is multiplied by its second-level scale first.
  * Dispatch by M (the device heuristic of the announcement, section "デバイスパラメータに
  * 基づくパフォーマンスチューニング"): W4A16 with M <= 16 streams the weights through a
  * split-K tensor-core GEMV, larger M dequantizes into tensor memory and runs tcgen05 BF16

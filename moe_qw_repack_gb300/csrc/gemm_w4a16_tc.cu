@@ -88,6 +88,7 @@ struct Params {
   const int32_t* queue;
   int32_t* err;
   int32_t tma_store;  // C's tensor map is valid (row pitch a multiple of 16 bytes)
+  const float* scale2;  // second-level scales [E][N_pad] or null
 };
 
 struct Tile {
@@ -470,6 +471,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float bias =
           (p.bias && nvalid) ? __uint_as_float((uint32_t)__ldg(p.bias + (int64_t)x.e * p.N + n) << 16)
                              : 0.f;
+      if (p.scale2) {  // second-level scale of this output channel, before the bias
+        const float t2 = nvalid ? __ldg(p.scale2 + (int64_t)x.e * p.N_pad + n) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] *= t2;
+      }
       // dense tiles may run past the last row (the store clips them); MoE tiles may not
       if (p.tma_store && (!p.queue || x.re - x.rb == BT)) {
         const bool issuer = warp == EPI_WARP0 && lane == 0;
@@ -594,6 +600,7 @@ qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
   p.bias = static_cast<const uint16_t*>(bias);
   p.C = static_cast<uint16_t*>(C);
   p.err = err;
+  p.scale2 = rs.scale2;
   int64_t max_m = p.num_m_tiles;
   if (rs.offsets) {
     const uint64_t need = tile_queue_bytes(rs.E, rs.rows, BT);

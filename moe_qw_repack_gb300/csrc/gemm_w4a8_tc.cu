@@ -129,6 +129,7 @@ struct Params {
   const int32_t* gather;
   int32_t topk;
   int64_t a_rows;
+  const float* scale2;  // second-level scales [E][N_pad] or null
 };
 
 struct Tile {
@@ -492,6 +493,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const int64_t row = x.rb + 32 * q + lane;
       const int col0 = x.n0 + 128 * half;
+      if (p.scale2) {
+        // second-level scales: C = t[n] * acc + bias[n], one 32-column chunk at a time,
+        // stored as it is done (the accumulator is released after the last chunk)
+        const float* tp = p.scale2 + (int64_t)x.e * p.N_pad + col0;
+        uint16_t* crow = p.C + row * (int64_t)p.N + col0;
+        const bool vec = col0 + 128 <= p.N && (p.N & 7) == 0;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          tc_ld_32x32b_x32(tbase + ((uint32_t)(32 * q) << 16) + 128 * half + 32 * j, r);
+          tc_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = col0 + 32 * j + 2 * i;
+            const float2 t2 = __ldg(reinterpret_cast<const float2*>(tp + 32 * j) + i);
+            float b0 = 0.f, b1 = 0.f;
+            if (p.bias) {
+              const uint16_t* bp = p.bias + (int64_t)x.e * p.N + c;
+              if (c < p.N) b0 = __uint_as_float((uint32_t)__ldg(bp) << 16);
+              if (c + 1 < p.N) b1 = __uint_as_float((uint32_t)__ldg(bp + 1) << 16);
+            }
+            pk[i] = pack_bf16x2(fmaf(__uint_as_float(r[2 * i]), t2.x, b0),
+                                fmaf(__uint_as_float(r[2 * i + 1]), t2.y, b1));
+          }
+          if (row < x.re) {
+            if (vec) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                reinterpret_cast<uint4*>(crow + 32 * j)[v] =
+                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int c = col0 + 32 * j + 2 * i;
+                if (c < p.N) crow[32 * j + 2 * i] = (uint16_t)(pk[i] & 0xFFFFu);
+                if (c + 1 < p.N) crow[32 * j + 2 * i + 1] = (uint16_t)(pk[i] >> 16);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+        acc_phase ^= 1u;
+        continue;
+      }
       uint32_t packed[64];
       // two 32-column loads in flight per wait: the drain gates the next tile's first MMA
 #pragma unroll
@@ -624,6 +672,7 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   p.s_packed = static_cast<const uint8_t*>(s_packed);
   p.s_estride = (int64_t)d.s_expert_stride;
   p.bias = static_cast<const uint16_t*>(bias);
+  p.scale2 = rs.scale2;
   p.C = static_cast<uint16_t*>(C);
   p.err = err;
   p.gather = rs.gather;

@@ -212,6 +212,7 @@ struct Params {
   int64_t w_estride, s_estride;  // bytes, BF16 elements
   int32_t gpw;           // scale groups per warp
   int64_t zplane;        // asymmetric INT4: BF16 elements from a scale to its 128 + z
+  const float* scale2;   // second-level scales [E][N_pad] or null
 };
 
 // One work item = (expert e, 16-row block nb, token rows [rb, re)), re - rb <= 8 * MCH.
@@ -502,6 +503,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
       const int n = nb * 16 + gq + 8 * (i >> 1);
       const int64_t r = rb + 8 * c + 2 * tt + (i & 1);
       if (n < p.N && r < re) {
+        if (p.scale2) v *= __ldg(p.scale2 + (int64_t)e * p.N_pad + n);
         if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + (int64_t)e * p.N + n) << 16);
         __nv_bfloat16 h = __float2bfloat16_rn(v);
         p.C[r * p.N + n] = *reinterpret_cast<uint16_t*>(&h);
@@ -555,6 +557,7 @@ struct M8Params {
   int32_t N, N_pad, K, M;  // M <= 8
   int32_t gpw;             // scale groups per warp
   int64_t zplane;          // asymmetric INT4: BF16 elements from a scale to its 128 + z
+  const float* scale2;     // second-level scales [N_pad] or null
 };
 
 __host__ __device__ constexpr size_t m8_act_bytes(int K, int M) {
@@ -728,6 +731,7 @@ __global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Param
       for (int w2 = 0; w2 < kM8Warps; ++w2) v += rb[(w2 * 4 + i) * 32 + l];
       const int n = (int)nb * 16 + nl;
       if (n < p.N) {
+        if (p.scale2) v *= __ldg(p.scale2 + n);
         if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + n) << 16);
         __nv_bfloat16 h = __float2bfloat16_rn(v);
         p.C[(int64_t)m * p.N + n] = *reinterpret_cast<uint16_t*>(&h);
@@ -797,6 +801,7 @@ struct TmaParams {
   int64_t M;             // dense rows (unused when grouped)
   const int32_t* queue;  // grouped tile queue or null
   int32_t* err;
+  const float* scale2;   // second-level scales [E][N_pad] or null
 };
 
 // One work item = (expert e, 16-row block nb, token rows [rb, re)), re - rb <= 8 * MCH.
@@ -1051,6 +1056,7 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
         const int n = nb * 16 + gq + 8 * (i >> 1);
         const int64_t r = rb + 8 * c + 2 * tt + (i & 1);
         if (n < p.N && r < re) {
+          if (p.scale2) v *= __ldg(p.scale2 + (int64_t)e * p.N_pad + n);
           if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + (int64_t)e * p.N + n) << 16);
           __nv_bfloat16 h = __float2bfloat16_rn(v);
           p.C[r * p.N + n] = *reinterpret_cast<uint16_t*>(&h);
@@ -1107,7 +1113,8 @@ int mch_for(const qw_packed_desc& d, int64_t rows, bool grouped) {
 
 // Dense calls of at most 8 token rows whose activations fit the staging buffer.
 qw_status launch_dense_m8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
-                          const void* A, const void* bias, void* C, int M, cudaStream_t st) {
+                          const void* A, const void* bias, const float* scale2, void* C, int M,
+                          cudaStream_t st) {
   const int G = d.K / kIntGroup;
   M8Params p{};
   p.wp = static_cast<const uint8_t*>(w_packed);
@@ -1120,6 +1127,7 @@ qw_status launch_dense_m8(const qw_packed_desc& d, const void* w_packed, const v
   p.K = d.K;
   p.M = M;
   p.gpw = (G + kM8Warps - 1) / kM8Warps;
+  p.scale2 = scale2;
   if (d.wfmt == QW_W_UINT4ZP_G128_BF16) {
     p.zplane = (int64_t)(d.s_expert_stride / 4);  // the second BF16 plane
     return launch_m8_variant<4, true>(p, st);
@@ -1132,8 +1140,8 @@ qw_status launch_dense_m8(const qw_packed_desc& d, const void* w_packed, const v
 
 // Other dense calls with up to 16 token rows: the register-ring kernel.
 qw_status launch_dense_reg(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
-                           const void* A, const void* bias, void* C, int64_t M, int mch,
-                           cudaStream_t st) {
+                           const void* A, const void* bias, const float* scale2, void* C,
+                           int64_t M, int mch, cudaStream_t st) {
   const int G = d.K / kIntGroup;
   Params p{};
   p.wp = static_cast<const uint8_t*>(w_packed);
@@ -1148,6 +1156,7 @@ qw_status launch_dense_reg(const qw_packed_desc& d, const void* w_packed, const 
   p.w_estride = (int64_t)d.w_expert_stride;
   p.s_estride = (int64_t)(d.s_expert_stride / 2);
   p.gpw = (G + kWarps - 1) / kWarps;
+  p.scale2 = scale2;
   const int64_t items = (d.N_pad / 16) * ((M + 8 * mch - 1) / (8 * mch));
   if (items > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
   if (d.wfmt == QW_W_UINT4ZP_G128_BF16) {
@@ -1186,9 +1195,9 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   // warp streams many groups; measured slower on matrices of 16 M weights and below)
   if (!grouped && rs.rows == 1 && (int64_t)d.N * d.K >= kM8MinWeights &&
       (reinterpret_cast<uintptr_t>(A) & 15) == 0 && m8_smem_bytes(d.K, 1) <= kM8MaxSmem)
-    return launch_dense_m8(d, w_packed, s_packed, A, bias, C, 1, st);
+    return launch_dense_m8(d, w_packed, s_packed, A, bias, rs.scale2, C, 1, st);
   if (!grouped)
-    return launch_dense_reg(d, w_packed, s_packed, A, bias, C, rs.rows, mch, st);
+    return launch_dense_reg(d, w_packed, s_packed, A, bias, rs.scale2, C, rs.rows, mch, st);
   // Grouped calls (over the device tile queue), and dense calls the dispatcher sends here
   // with more rows: the TMA ring.
   const bool zp = d.wfmt == QW_W_UINT4ZP_G128_BF16;
@@ -1246,6 +1255,7 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   p.K = d.K;
   p.M = rs.rows;
   p.err = err;
+  p.scale2 = rs.scale2;
   int64_t max_items = nblocks * ((rs.rows + 8 * mch - 1) / (8 * mch));
   int64_t size_items = max_items;  // what the grid is sized for
   if (grouped) {

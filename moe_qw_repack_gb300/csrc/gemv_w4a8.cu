@@ -75,6 +75,7 @@ struct W4A8GemvParams {
   uint16_t* C;
   int32_t N, N_pad, K, K_pad, M;
   int32_t gpw;  // scale groups per warp, a multiple of 4
+  const float* scale2;  // second-level scales [N_pad] or null
 };
 
 // Byte offset of the 4 scales (row r, groups 4q .. 4q + 3) in the chunked layout.
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
       for (int w2 = 0; w2 < kW8Warps; ++w2) v += rb[(w2 * 4 + i) * 32 + l];
       const int n = (int)nb * 16 + nl;
       if (n < p.N) {
+        if (p.scale2) v *= __ldg(p.scale2 + n);
         if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + n) << 16);
         __nv_bfloat16 h = __float2bfloat16_rn(v);
         p.C[(int64_t)m * p.N + n] = *reinterpret_cast<uint16_t*>(&h);
@@ -253,8 +255,8 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
 }  // namespace
 
 qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
-                           const void* A, const void* A_sf, const void* bias, void* C, int M,
-                           cudaStream_t st) {
+                           const void* A, const void* A_sf, const void* bias, const float* scale2,
+                           void* C, int M, cudaStream_t st) {
   if (M < 1 || M > kW4A8GemvRows || d.E != 1 || d.wfmt != QW_W_MXFP4_G32 ||
       w4a8_gemv_smem_bytes(d.K, M) > kW4A8GemvMaxSmem)
     return QW_ERR_UNSUPPORTED;
@@ -270,6 +272,7 @@ qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   p.K = d.K;
   p.K_pad = d.K_pad;
   p.M = M;
+  p.scale2 = scale2;
   const int G = d.K / kMxGroup;
   p.gpw = ((G + kW8Warps - 1) / kW8Warps + 3) / 4 * 4;
   auto kern = gemv_w4a8_kernel;

@@ -39,6 +39,24 @@ bool is_mx(int32_t wfmt) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// Bytes of the second-level scale plane (FP32 [E][N_pad]) at the end of s_packed.
+uint64_t scale2_bytes(const qw_packed_desc& d) {
+  return (d.wfmt & QW_W_SCALE2) ? (uint64_t)round_up((int64_t)d.E * d.N_pad * 4, 256) : 0;
+}
+// The descriptor of the base format (no second-level scales) the kernels are launched with.
+qw_packed_desc base_desc(const qw_packed_desc& d) {
+  qw_packed_desc b = d;
+  b.s_bytes -= scale2_bytes(d);
+  b.wfmt &= ~QW_W_SCALE2;
+  return b;
+}
+// Device FP32 [E][N_pad] second-level scales of a packed scale buffer, or null.
+const float* scale2_of(const qw_packed_desc& d, const void* s_packed) {
+  if (!(d.wfmt & QW_W_SCALE2) || !s_packed) return nullptr;
+  return reinterpret_cast<const float*>(static_cast<const uint8_t*>(s_packed) +
+                                        d.s_expert_stride * (uint64_t)d.E);
+}
+
 qw_status check_desc(const qw_packed_desc* d) {
   if (!d) return QW_ERR_INVALID_ARG;
   qw_packed_desc ref;
@@ -50,8 +68,9 @@ qw_status check_desc(const qw_packed_desc* d) {
 }
 
 qw_status check_afmt(const qw_packed_desc* d, int32_t afmt, const void* A_sf) {
-  if (is_mx(d->wfmt)) {
-    if (afmt != (d->wfmt == QW_W_NVFP4_G16 ? QW_A_NVFP4_G16 : QW_A_MXFP8_G32))
+  const int32_t wfmt = d->wfmt & ~QW_W_SCALE2;
+  if (is_mx(wfmt)) {
+    if (afmt != (wfmt == QW_W_NVFP4_G16 ? QW_A_NVFP4_G16 : QW_A_MXFP8_G32))
       return QW_ERR_UNSUPPORTED;
     if (!A_sf) return QW_ERR_INVALID_ARG;
   } else {
@@ -81,12 +100,14 @@ const char* qw_status_str(int32_t s) {
   }
 }
 
-int32_t qw_version(void) { return 200; }
+int32_t qw_version(void) { return 210; }
 
-qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_packed_desc* out) {
+qw_status qw_repack_query(int32_t wfmt_in, int32_t E, int32_t N, int32_t K, qw_packed_desc* out) {
   if (!out || E < 1 || N < 1 || K < 1) return QW_ERR_INVALID_ARG;
+  if (wfmt_in & ~(QW_W_SCALE2 | 0xFF)) return QW_ERR_UNSUPPORTED;
+  const int32_t wfmt = wfmt_in & ~QW_W_SCALE2;
   qw_packed_desc d{};
-  d.wfmt = wfmt;
+  d.wfmt = wfmt_in;
   d.E = E;
   d.N = N;
   d.K = K;
@@ -136,7 +157,7 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
   }
   if ((int64_t)d.N_pad * E > 0x7FFFFFFFLL) return QW_ERR_UNSUPPORTED;
   d.w_bytes = d.w_expert_stride * (uint64_t)E;
-  d.s_bytes = d.s_expert_stride * (uint64_t)E;
+  d.s_bytes = d.s_expert_stride * (uint64_t)E + scale2_bytes(d);
   *out = d;
   return QW_OK;
 }
@@ -146,12 +167,16 @@ qw_status qw_repack(const qw_packed_desc* desc, const void* w_canon, const void*
   qw_status s = check_desc(desc);
   if (s != QW_OK) return s;
   if (!w_canon || !s_canon || !w_packed || !s_packed) return QW_ERR_INVALID_ARG;
-  if (!is_mx(desc->wfmt) && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
+  const qw_packed_desc bd = base_desc(*desc);
+  if (!is_mx(bd.wfmt) && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
     return QW_ERR_ALIGNMENT;
-  if (desc->wfmt == QW_W_UINT4ZP_G128_BF16 && !aligned(s_canon, 4)) return QW_ERR_ALIGNMENT;
+  if (bd.wfmt == QW_W_UINT4ZP_G128_BF16 && !aligned(s_canon, 4)) return QW_ERR_ALIGNMENT;
   if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
-  return launch_repack(*desc, w_canon, s_canon, w_packed, s_packed, d_err,
-                       static_cast<cudaStream_t>(stream));
+  s = launch_repack(bd, w_canon, s_canon, w_packed, s_packed, d_err,
+                    static_cast<cudaStream_t>(stream));
+  if (s != QW_OK || !(desc->wfmt & QW_W_SCALE2)) return s;
+  return launch_scale2_fill(const_cast<float*>(scale2_of(*desc, s_packed)),
+                            (int64_t)desc->E * desc->N_pad, static_cast<cudaStream_t>(stream));
 }
 
 qw_status qw_unpack(const qw_packed_desc* desc, const void* w_packed, const void* s_packed,
@@ -159,12 +184,33 @@ qw_status qw_unpack(const qw_packed_desc* desc, const void* w_packed, const void
   qw_status s = check_desc(desc);
   if (s != QW_OK) return s;
   if (!w_canon || !s_canon || !w_packed || !s_packed) return QW_ERR_INVALID_ARG;
-  if (!is_mx(desc->wfmt) && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
+  const qw_packed_desc bd = base_desc(*desc);
+  if (!is_mx(bd.wfmt) && (!aligned(w_canon, 4) || !aligned(s_canon, 2)))
     return QW_ERR_ALIGNMENT;
-  if (desc->wfmt == QW_W_UINT4ZP_G128_BF16 && !aligned(s_canon, 4)) return QW_ERR_ALIGNMENT;
+  if (bd.wfmt == QW_W_UINT4ZP_G128_BF16 && !aligned(s_canon, 4)) return QW_ERR_ALIGNMENT;
   if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
-  return launch_unpack(*desc, w_packed, s_packed, w_canon, s_canon, d_err,
+  return launch_unpack(bd, w_packed, s_packed, w_canon, s_canon, d_err,
                        static_cast<cudaStream_t>(stream));
+}
+
+qw_status qw_repack_scale2(const qw_packed_desc* desc, const float* t_canon, void* s_packed,
+                           int32_t* d_err, void* stream) {
+  qw_status s = check_desc(desc);
+  if (s != QW_OK) return s;
+  if (!(desc->wfmt & QW_W_SCALE2) || !t_canon || !s_packed) return QW_ERR_INVALID_ARG;
+  if (!aligned(t_canon, 4) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
+  return launch_scale2_repack(t_canon, const_cast<float*>(scale2_of(*desc, s_packed)), desc->E,
+                              desc->N, desc->N_pad, d_err, static_cast<cudaStream_t>(stream));
+}
+
+qw_status qw_unpack_scale2(const qw_packed_desc* desc, const void* s_packed, float* t_canon,
+                           void* stream) {
+  qw_status s = check_desc(desc);
+  if (s != QW_OK) return s;
+  if (!(desc->wfmt & QW_W_SCALE2) || !t_canon || !s_packed) return QW_ERR_INVALID_ARG;
+  if (!aligned(t_canon, 4) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
+  return launch_scale2_unpack(scale2_of(*desc, s_packed), t_canon, desc->E, desc->N, desc->N_pad,
+                              static_cast<cudaStream_t>(stream));
 }
 
 qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t max_rows,
@@ -173,11 +219,12 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
   if (s != QW_OK) return s;
   if (!bytes || max_rows < 0) return QW_ERR_INVALID_ARG;
   if ((s = check_afmt(desc, afmt, reinterpret_cast<const void*>(1))) != QW_OK) return s;
-  if (is_mx(desc->wfmt)) {
-    *bytes = gemm_w4a8_workspace(*desc, max_rows);
+  const qw_packed_desc bd = base_desc(*desc);
+  if (is_mx(bd.wfmt)) {
+    *bytes = gemm_w4a8_workspace(bd, max_rows);
   } else {
-    const uint64_t a = gemv_w4a16_workspace(*desc, max_rows);
-    const uint64_t b = gemm_w4a16_tc_workspace(*desc, max_rows);
+    const uint64_t a = gemv_w4a16_workspace(bd, max_rows);
+    const uint64_t b = gemm_w4a16_tc_workspace(bd, max_rows);
     *bytes = a > b ? a : b;
   }
   return QW_OK;
@@ -193,9 +240,10 @@ static qw_status check_gemm_args(const qw_packed_desc* desc, const void* w_packe
   if (rows > 0 && (!w_packed || !s_packed || !A || !C)) return QW_ERR_INVALID_ARG;
   if (!aligned(w_packed, 256) || !aligned(s_packed, 256)) return QW_ERR_ALIGNMENT;
   if (!aligned(A, 16) || !aligned(C, 4)) return QW_ERR_ALIGNMENT;
-  if (is_mx(desc->wfmt)) {
+  const int32_t wfmt = desc->wfmt & ~QW_W_SCALE2;
+  if (is_mx(wfmt)) {
     // TMA row pitch of the activations: K bytes (E4M3) or K/2 bytes (E2M1), 16-byte multiple
-    if (desc->K % (desc->wfmt == QW_W_NVFP4_G16 ? 32 : 16)) return QW_ERR_ALIGNMENT;
+    if (desc->K % (wfmt == QW_W_NVFP4_G16 ? 32 : 16)) return QW_ERR_ALIGNMENT;
     if (!aligned(A_sf, 4)) return QW_ERR_ALIGNMENT;
   } else if (desc->K % 8) {
     return QW_ERR_ALIGNMENT;
@@ -213,17 +261,19 @@ qw_status qgemm_dense(const qw_packed_desc* desc, const void* w_packed, const vo
   if (bias && !aligned(bias, 2)) return QW_ERR_ALIGNMENT;
   if (M == 0) return QW_OK;
   RowSet rs{M, nullptr, 1};
+  rs.scale2 = scale2_of(*desc, s_packed);
+  const qw_packed_desc bd = base_desc(*desc);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (desc->wfmt == QW_W_MXFP4_G32 && M <= kW4A8GemvRows &&
-      w4a8_gemv_smem_bytes(desc->K, (int)M) <= kW4A8GemvMaxSmem)
-    return launch_gemv_w4a8(*desc, w_packed, s_packed, A, A_sf, bias, C, (int)M, st);
-  if (is_mx(desc->wfmt))
-    return launch_gemm_w4a8(*desc, w_packed, s_packed, A, A_sf, bias, C, rs, workspace, ws_bytes,
+  if (bd.wfmt == QW_W_MXFP4_G32 && M <= kW4A8GemvRows &&
+      w4a8_gemv_smem_bytes(bd.K, (int)M) <= kW4A8GemvMaxSmem)
+    return launch_gemv_w4a8(bd, w_packed, s_packed, A, A_sf, bias, rs.scale2, C, (int)M, st);
+  if (is_mx(bd.wfmt))
+    return launch_gemm_w4a8(bd, w_packed, s_packed, A, A_sf, bias, C, rs, workspace, ws_bytes,
                             d_err, st);
   if (M > kW4A16TensorCoreRows)
-    return launch_gemm_w4a16_tc(*desc, w_packed, s_packed, A, bias, C, rs, workspace, ws_bytes,
+    return launch_gemm_w4a16_tc(bd, w_packed, s_packed, A, bias, C, rs, workspace, ws_bytes,
                                 d_err, st);
-  return launch_gemv_w4a16(*desc, w_packed, s_packed, A, bias, C, rs, workspace, ws_bytes, d_err,
+  return launch_gemv_w4a16(bd, w_packed, s_packed, A, bias, C, rs, workspace, ws_bytes, d_err,
                            st);
 }
 
@@ -330,14 +380,16 @@ qw_status qgemm_moe_grouped(const qw_packed_desc* desc, const void* w_packed,
   qgemm_workspace_size(desc, afmt, total_rows, &need);
   if (!workspace || ws_bytes < need) return QW_ERR_WORKSPACE;
   RowSet rs{total_rows, expert_offsets, desc->E};
+  rs.scale2 = scale2_of(*desc, s_packed);
+  const qw_packed_desc bd = base_desc(*desc);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (is_mx(desc->wfmt))
-    return launch_gemm_w4a8(*desc, w_packed, s_packed, A_sorted, A_sf_sorted, bias, C, rs,
+  if (is_mx(bd.wfmt))
+    return launch_gemm_w4a8(bd, w_packed, s_packed, A_sorted, A_sf_sorted, bias, C, rs,
                             workspace, ws_bytes, d_err, st);
-  if (total_rows >= kW4A16TensorCoreRows * desc->E)
-    return launch_gemm_w4a16_tc(*desc, w_packed, s_packed, A_sorted, bias, C, rs, workspace,
+  if (total_rows >= kW4A16TensorCoreRows * bd.E)
+    return launch_gemm_w4a16_tc(bd, w_packed, s_packed, A_sorted, bias, C, rs, workspace,
                                 ws_bytes, d_err, st);
-  return launch_gemv_w4a16(*desc, w_packed, s_packed, A_sorted, bias, C, rs, workspace, ws_bytes,
+  return launch_gemv_w4a16(bd, w_packed, s_packed, A_sorted, bias, C, rs, workspace, ws_bytes,
                            d_err, st);
 }
 
@@ -350,7 +402,7 @@ qw_status qgemm_moe_grouped_indexed(const qw_packed_desc* desc, const void* w_pa
                                     void* stream) {
   qw_status s = check_gemm_args(desc, w_packed, s_packed, afmt, A, A_sf, C, total_rows);
   if (s != QW_OK) return s;
-  if (!is_mx(desc->wfmt)) return QW_ERR_UNSUPPORTED;
+  if (!is_mx(desc->wfmt & ~QW_W_SCALE2)) return QW_ERR_UNSUPPORTED;
   if (!expert_offsets || !aligned(expert_offsets, 4)) return QW_ERR_INVALID_ARG;
   if (desc->E > 1024) return QW_ERR_UNSUPPORTED;
   if (topk < 1 || T < 0 || T > 0x7FFFFFFFLL || total_rows > T * (int64_t)topk)
@@ -362,8 +414,9 @@ qw_status qgemm_moe_grouped_indexed(const qw_packed_desc* desc, const void* w_pa
   qgemm_workspace_size(desc, afmt, total_rows, &need);
   if (!workspace || ws_bytes < need) return QW_ERR_WORKSPACE;
   RowSet rs{total_rows, expert_offsets, desc->E, sorted_pairs, topk, T};
-  return launch_gemm_w4a8(*desc, w_packed, s_packed, A, A_sf, bias, C, rs, workspace, ws_bytes,
-                          d_err, static_cast<cudaStream_t>(stream));
+  rs.scale2 = scale2_of(*desc, s_packed);
+  return launch_gemm_w4a8(base_desc(*desc), w_packed, s_packed, A, A_sf, bias, C, rs, workspace,
+                          ws_bytes, d_err, static_cast<cudaStream_t>(stream));
 }
 
 qw_status qw_read_error(const int32_t* d_err, void* stream, int32_t* host_code) {

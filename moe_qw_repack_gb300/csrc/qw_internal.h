@@ -26,6 +26,12 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
                         void* w_packed, void* s_packed, int32_t* err, cudaStream_t st);
 qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
                         void* w_canon, void* s_canon, int32_t* err, cudaStream_t st);
+// second-level scales: fill the packed plane with 1.0, copy [E][N] <-> [E][N_pad]
+qw_status launch_scale2_fill(float* t_packed, int64_t n, cudaStream_t st);
+qw_status launch_scale2_repack(const float* t_canon, float* t_packed, int32_t E, int32_t N,
+                               int32_t N_pad, int32_t* err, cudaStream_t st);
+qw_status launch_scale2_unpack(const float* t_packed, float* t_canon, int32_t E, int32_t N,
+                               int32_t N_pad, cudaStream_t st);
 
 // Rows of a GEMM call: dense (offsets == nullptr, rows [0, M)) or grouped by expert
 // (device offsets [E+1]; the work list of (expert, row tile) is built on the device).
@@ -38,6 +44,9 @@ struct RowSet {
   const int32_t* gather = nullptr;
   int32_t topk = 1;
   int64_t a_rows = 0;
+  // second-level scales: device FP32 [E][N_pad] multiplying each output channel's sum
+  // before the bias, or nullptr
+  const float* scale2 = nullptr;
 };
 
 // Small-M W4A16: tensor-core GEMV over the fragment-ordered packed weights.
@@ -84,8 +93,8 @@ constexpr size_t w4a8_gemv_smem_bytes(int K, int M) {
   return (size_t)(K / 32) * ((size_t)M * 64 + 32);
 }
 qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
-                           const void* A, const void* A_sf, const void* bias, void* C, int M,
-                           cudaStream_t st);
+                           const void* A, const void* A_sf, const void* bias, const float* scale2,
+                           void* C, int M, cudaStream_t st);
 
 // MoE scheduling.
 qw_status launch_moe_route(const float* logits, int32_t T, int32_t E, int32_t topk,

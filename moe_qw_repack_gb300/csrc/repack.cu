@@ -321,6 +321,40 @@ __global__ void unpack_fp8w_kernel(const uint32_t* __restrict__ wp, uint32_t* __
   }
 }
 
+// ----------------------------------------------------------------------------- second-level scales
+// FP32 [E][N] <-> the packed plane [E][N_pad] (padding channels 0; a non-finite t is a value
+// error, packed as 0).
+__global__ void scale2_fill_kernel(float* __restrict__ tp, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    tp[i] = 1.0f;
+}
+__global__ void scale2_repack_kernel(const float* __restrict__ tc, float* __restrict__ tp,
+                                     int32_t E, int32_t N, int32_t N_pad, int32_t* err) {
+  const int64_t total = (int64_t)E * N_pad;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i / N_pad;
+    const int n = (int)(i % N_pad);
+    float v = 0.f;
+    if (n < N) {
+      v = tc[e * N + n];
+      if (!isfinite(v)) {
+        set_error(err, QW_ERR_VALUE);
+        v = 0.f;
+      }
+    }
+    tp[i] = v;
+  }
+}
+__global__ void scale2_unpack_kernel(const float* __restrict__ tp, float* __restrict__ tc,
+                                     int32_t E, int32_t N, int32_t N_pad) {
+  const int64_t total = (int64_t)E * N;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x)
+    tc[i] = tp[(i / N) * N_pad + i % N];
+}
+
 // ----------------------------------------------------------------------------- INT scales
 // canonical [E][N][K/128] <-> packed [E][K/128][N_pad] (zero padded)
 // Experts sit `estride` halfwords apart (the descriptor's scale stride: G * N_pad rounded up
@@ -570,6 +604,23 @@ int grid_for(int64_t total, int threads) {
 }
 
 }  // namespace
+
+qw_status launch_scale2_fill(float* t_packed, int64_t n, cudaStream_t st) {
+  scale2_fill_kernel<<<grid_for(n, 256), 256, 0, st>>>(t_packed, n);
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
+qw_status launch_scale2_repack(const float* t_canon, float* t_packed, int32_t E, int32_t N,
+                               int32_t N_pad, int32_t* err, cudaStream_t st) {
+  scale2_repack_kernel<<<grid_for((int64_t)E * N_pad, 256), 256, 0, st>>>(t_canon, t_packed, E,
+                                                                          N, N_pad, err);
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
+qw_status launch_scale2_unpack(const float* t_packed, float* t_canon, int32_t E, int32_t N,
+                               int32_t N_pad, cudaStream_t st) {
+  scale2_unpack_kernel<<<grid_for((int64_t)E * N, 256), 256, 0, st>>>(t_packed, t_canon, E, N,
+                                                                       N_pad);
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
 
 qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void* s_canon,
                         void* w_packed, void* s_packed, int32_t* err, cudaStream_t st) {

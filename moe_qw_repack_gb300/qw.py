@@ -32,12 +32,14 @@ QW_W_NVFP4_G16 = 4
 QW_W_UINT4ZP_G128_BF16 = 5
 QW_W_INT2_G128_BF16 = 6
 QW_W_FP8E4M3_G128_BF16 = 7
+QW_W_SCALE2 = 0x100  # flag: second-level FP32 scale per output channel (and expert)
 QW_A_BF16 = 0
 QW_A_MXFP8_G32 = 1
 QW_A_NVFP4_G16 = 2
 
 EXPORTS = (
     "qw_status_str", "qw_version", "qw_repack_query", "qw_repack", "qw_unpack",
+    "qw_repack_scale2", "qw_unpack_scale2",
     "qgemm_workspace_size", "qgemm_dense", "qgemm_moe_route_workspace_size", "qgemm_moe_route",
     "qgemm_moe_permute", "qgemm_moe_grouped", "qgemm_moe_grouped_indexed", "qw_read_error",
     "qw_test_wait_timeout",
@@ -74,6 +76,8 @@ _SIGS = {
     "qw_repack_query": (_I32, [_I32, _I32, _I32, _I32, _DESC]),
     "qw_repack": (_I32, [_DESC, _P, _P, _P, _P, _P, _P]),
     "qw_unpack": (_I32, [_DESC, _P, _P, _P, _P, _P, _P]),
+    "qw_repack_scale2": (_I32, [_DESC, _P, _P, _P, _P]),
+    "qw_unpack_scale2": (_I32, [_DESC, _P, _P, _P]),
     "qgemm_workspace_size": (_I32, [_DESC, _I32, _I64, ctypes.POINTER(_U64)]),
     "qgemm_dense": (_I32, [_DESC, _P, _P, _I32, _P, _P, _P, _P, _I64, _P, _U64, _P, _P]),
     "qgemm_moe_route_workspace_size": (_I32, [_I32, _I32, _I32, ctypes.POINTER(_U64)]),
@@ -160,6 +164,17 @@ def qw_unpack(desc, w_packed, s_packed, w_canon, s_canon, d_err=None, stream=Non
     _check("qw_unpack", LIB.qw_unpack(ctypes.byref(desc), _ptr(w_packed), _ptr(s_packed),
                                       _ptr(w_canon), _ptr(s_canon), _ptr(d_err),
                                       _stream(stream)))
+
+
+def qw_repack_scale2(desc, t_canon, s_packed, d_err=None, stream=None):
+    _check("qw_repack_scale2", LIB.qw_repack_scale2(ctypes.byref(desc), _ptr(t_canon),
+                                                    _ptr(s_packed), _ptr(d_err),
+                                                    _stream(stream)))
+
+
+def qw_unpack_scale2(desc, s_packed, t_canon, stream=None):
+    _check("qw_unpack_scale2", LIB.qw_unpack_scale2(ctypes.byref(desc), _ptr(s_packed),
+                                                    _ptr(t_canon), _stream(stream)))
 
 
 def qgemm_workspace_size(desc, afmt: int, max_rows: int) -> int:

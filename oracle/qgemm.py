@@ -21,6 +21,11 @@ output stage; section "WnA16": low-bit weights times 16-bit activations; section
           with an unsigned E4M3 scale per 16 along K; the format's optional per-tensor
           FP32 factor is left to the caller, as a plain multiplier of C)
 
+Second-level scales (section "統一されたquantization表現": the quantization description
+carries them as a parameter of its own): an FP32 scale t per output channel on top of
+the format's group scales, applied to the finished sum before the bias:
+          R'[m,n] = t[n] * R[m,n] + bias[n]    (apply_scale2)
+
 Every operand is decoded exactly into float64 and the sum over k is a float64
 matrix product (a library matmul used as one step, no blocking or reordering
 beyond it).  Weights are [N][K] (out x in), activations [M][K], results [M][N].
@@ -76,6 +81,21 @@ def gemm_w8a16_fp8(A_bits, w_codes, s_bits, bias_bits=None, group: int = 128):
     """A_bits [M][K] BF16, w_codes [N][K] E4M3, s_bits [N][K/group] BF16 -> (R, absum) of
     w = e4m3(code) * s: the W4A16 product with decoded E4M3 values in place of integers."""
     return gemm_w4a16(A_bits, F.decode_e4m3(w_codes), s_bits, bias_bits, group)
+
+
+def apply_scale2(R, absum, t, bias_bits=None):
+    """Second-level scales: R and absum of a GEMM computed without bias, t float32 [N] ->
+    (t[n] * R + bias[n], |t[n]| * absum + |bias[n]|)."""
+    t = np.asarray(t, dtype=np.float32).astype(np.float64)
+    if not np.all(np.isfinite(t)):
+        raise F.FormatError("non-finite second-level scale")
+    r = np.asarray(R) * t[None, :]
+    a = np.asarray(absum) * np.abs(t)[None, :]
+    if bias_bits is not None:
+        b = F.decode_bf16(bias_bits)
+        r = r + b[None, :]
+        a = a + np.abs(b)[None, :]
+    return r, a
 
 
 def gemm_w4a8(A_codes, A_sf, w_codes, w_sf, bias_bits=None):

@@ -24,7 +24,8 @@ def Q():
 def test_header_declares_the_boundary():
     fns = header_functions()
     for name in ("qw_repack", "qw_unpack", "qw_repack_query", "qgemm_dense", "qgemm_moe_grouped",
-                 "qgemm_moe_route", "qgemm_moe_permute", "qgemm_workspace_size"):
+                 "qgemm_moe_route", "qgemm_moe_permute", "qgemm_workspace_size",
+                 "qw_repack_scale2", "qw_unpack_scale2"):
         assert name in fns
 
 
@@ -171,3 +172,23 @@ def test_activation_steps_host_validation(Q):
     with pytest.raises(Q.QwError) as e:
         Q.qgemm_moe_combine(good, good, good, good, 4, 8, 2, 64, good, good, 8, stream=0)
     assert e.value.status == Q.QW_ERR_WORKSPACE
+
+
+def test_scale2_flag_sizes_and_host_validation(Q):
+    """The second-level scale plane adds FP32 [E][N_pad] (rounded to 256 bytes) to s_bytes;
+    unknown flag bits are rejected; the scale2 entry points want the flag (host checks only)."""
+    for wfmt in (Q.QW_W_INT4_G128_BF16, Q.QW_W_MXFP4_G32, Q.QW_W_NVFP4_G16, Q.QW_W_FP8E4M3_G128_BF16):
+        base = Q.qw_repack_query(wfmt, 3, 200, 512)
+        d = Q.qw_repack_query(wfmt | Q.QW_W_SCALE2, 3, 200, 512)
+        assert d.wfmt == wfmt | Q.QW_W_SCALE2 and d.N_pad == base.N_pad
+        assert d.s_expert_stride == base.s_expert_stride and d.w_bytes == base.w_bytes
+        assert d.s_bytes == base.s_bytes + (3 * base.N_pad * 4 + 255) // 256 * 256
+    with pytest.raises(Q.QwError):
+        Q.qw_repack_query(0x200, 1, 16, 128)
+    plain = Q.qw_repack_query(Q.QW_W_INT4_G128_BF16, 1, 16, 128)
+    good = 1 << 20
+    for call in (lambda: Q.qw_repack_scale2(plain, good, good, stream=0),
+                 lambda: Q.qw_unpack_scale2(plain, good, good, stream=0)):
+        with pytest.raises(Q.QwError) as e:
+            call()
+        assert e.value.status == Q.QW_ERR_INVALID_ARG

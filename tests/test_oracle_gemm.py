@@ -477,3 +477,40 @@ def test_planted_subnormal_e4m3_decode_is_caught(monkeypatch):
     monkeypatch.setattr(F, "decode_e4m3", bad)
     with pytest.raises(AssertionError):
         test_fp8w_fraction_brute_force_with_subnormal_codes()
+
+
+# ----------------------------------------------------------------------------- second-level scales
+def test_scale2_of_ones_is_the_identity():
+    p = synth.w4a16_problem(3, 20, 256, bits=4, cfg_id=63, bias=True)
+    q = F.unpack_int4(p["w_canon"][0], 256)
+    R, S = Q.gemm_w4a16(p["A"], q, p["s_canon"][0])
+    Rb, Sb = Q.gemm_w4a16(p["A"], q, p["s_canon"][0], p["bias"][0])
+    R2, S2 = Q.apply_scale2(R, S, np.ones(20, np.float32), p["bias"][0])
+    assert np.array_equal(R2, Rb) and np.array_equal(S2, Sb)
+
+
+def test_scale2_equals_scaled_weights_exactly():
+    """Integer activations, unit group scales and power-of-two t per channel: t * (a w) must
+    equal a (t w) exactly, with t folded into the weights of an independent integer GEMM;
+    N != M so a t applied along the wrong axis cannot broadcast."""
+    rng = np.random.default_rng(64)
+    M, N, K = 3, 7, 256
+    a = rng.integers(-50, 51, (M, K))
+    q = rng.integers(-7, 8, (N, K))
+    e = rng.integers(-6, 7, N)
+    t = np.ldexp(np.ones(N, np.float32), e).astype(np.float32) * np.where(rng.random(N) < 0.3, -1, 1)
+    R, S = Q.gemm_w4a16(bf16_bits_of(a), q, np.full((N, 2), 0x3F80, np.uint16))
+    R2, S2 = Q.apply_scale2(R, S, t)
+    want = (a.astype(np.float64) @ (q.astype(np.float64) * t[:, None].astype(np.float64)).T)
+    assert np.array_equal(R2, want)
+    assert np.array_equal(S2, np.abs(a) @ np.abs(q * t[:, None].astype(np.float64)).T)
+
+
+def test_scale2_applies_before_the_bias_and_rejects_non_finite():
+    R = np.array([[2.0, 4.0]])
+    S = np.array([[2.0, 4.0]])
+    b = bf16_bits_of(np.array([1.0, -1.0]))
+    R2, S2 = Q.apply_scale2(R, S, np.array([0.5, 3.0], np.float32), b)
+    assert np.array_equal(R2, np.array([[2.0, 11.0]])) and np.array_equal(S2, np.array([[2.0, 13.0]]))
+    with pytest.raises(F.FormatError):
+        Q.apply_scale2(R, S, np.array([1.0, np.inf], np.float32))
