@@ -123,12 +123,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The slowest rank's value (NCCL on the GPUs; gloo on host tensors)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(flop_per_rank_step, world, ms_per_step):
+    """Every rank runs the same step on its own replica (weak scaling): the job's throughput
+    is all ranks' FLOP over the slowest rank's step time."""
+    return flop_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -547,7 +555,7 @@ def run_ours(args, world, rank):
             raise RuntimeError(f"device error flag {code}")
     per_gemm = [time_region([f], args.steps, args.warmup, world)[0] for f in fns]
     F = flops_of(SHAPES)
-    value = F * world / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(F, world, ms)
     # roofline of the dominant kernel: every launch in the timed region is the W4A8 GEMM,
     # so its average launch time is the region time over the launches
     achieved = F / (ms * 1e-3) / 1e12
@@ -585,7 +593,7 @@ def run_ours(args, world, rank):
                    "timing": "K steps back to back between one CUDA event pair",
                    "per_gemm_ms": [round(t, 4) for t in per_gemm],
                    "parallelism": f"replicas x{world}"},
-        "e2e": {"value": round(F * world / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_tflops(F, world, e_ms), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": len(fns) * n,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
