@@ -216,8 +216,9 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
  *   W4A8:  desc->wfmt MXFP4,     afmt QW_A_MXFP8_G32, A E4M3 [M][K], A_sf E8M0 [M][K/32].
  *   W8A8:  desc->wfmt MXFP8,     afmt QW_A_MXFP8_G32, as W4A8.
  *   W4A4:  desc->wfmt NVFP4,     afmt QW_A_NVFP4_G16, A E2M1 [M][K/2], A_sf E4M3 [M][K/16]
- *          (NVFP4 x NVFP4 on tcgen05 kind::mxf4nvf4; a per-tensor FP32 factor of the
- *          format, if any, is the caller's to apply to C).
+ *          (NVFP4 x NVFP4 on tcgen05 kind::mxf4nvf4; the weights' per-tensor FP32 factor
+ *          of the format rides on QW_W_SCALE2, the activations' is the caller's to apply
+ *          to C).
  *   bias:  BF16 [N] or NULL.  C: BF16 [M][N].  desc->E must be 1.  With QW_W_SCALE2 in
  *          desc->wfmt each channel's sum is multiplied by its second-level scale first.
  * Dispatch by M (the device heuristic of the announcement, section "デバイスパラメータに

@@ -18,8 +18,8 @@ output stage; section "WnA16": low-bit weights times 16-bit activations; section
   W4A4:   R[m,n] = sum_k e2m1(a[m,k]) e4m3(sa[m,k//16])
                           * e2m1(w[n,k]) e4m3(sw[n,k//16])        (+ bias[n])
           (NVFP4 x NVFP4, the section's W4A4 / "NVFP4 x NVFP4 W4A4": E2M1 elements
-          with an unsigned E4M3 scale per 16 along K; the format's optional per-tensor
-          FP32 factor is left to the caller, as a plain multiplier of C)
+          with an unsigned E4M3 scale per 16 along K; the format's per-tensor FP32
+          factors are a plain multiplier of the result: apply_scale2 with equal t)
 
 Second-level scales (section "統一されたquantization表現": the quantization description
 carries them as a parameter of its own): an FP32 scale t per output channel on top of
