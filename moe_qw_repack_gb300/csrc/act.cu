@@ -112,14 +112,29 @@ __global__ void invert_pairs_kernel(const int32_t* __restrict__ sp, int64_t P,
 }
 
 // out[t][n] = sum_j w[t][j] Y[inv[t k + j]][n], w = softmax of token t's k selected logits.
-// One CTA per token; a thread owns 8 consecutive columns at a time.
+// One CTA per token; a thread owns 8 consecutive columns at a time.  With `inv` null (small
+// batches) the CTA finds its k rows itself by scanning the sorted pair list, which saves
+// the inversion launch.
 __global__ void combine_kernel(const uint16_t* __restrict__ Y, const int32_t* __restrict__ inv,
-                               const int32_t* __restrict__ ids, const float* __restrict__ logits,
-                               int32_t E, int32_t k, int32_t N, int64_t P,
-                               uint16_t* __restrict__ out, int32_t* err) {
+                               const int32_t* __restrict__ sp, const int32_t* __restrict__ ids,
+                               const float* __restrict__ logits, int32_t E, int32_t k, int32_t N,
+                               int64_t P, uint16_t* __restrict__ out, int32_t* err) {
   const int64_t t = blockIdx.x;
   __shared__ float w[32];
   __shared__ int32_t row[32];
+  if (!inv) {
+    if (threadIdx.x < 32) row[threadIdx.x] = -1;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < P; i += blockDim.x) {
+      const int32_t pair = __ldg(sp + i);
+      if (pair < 0 || pair >= P) {
+        set_error(err, QW_ERR_INVALID_ARG);
+        continue;
+      }
+      if (pair / k == t) row[pair - t * k] = (int32_t)i;
+    }
+    __syncthreads();
+  }
   if (threadIdx.x < 32) {
     const int j = threadIdx.x;
     float l = -INFINITY;
@@ -129,7 +144,7 @@ __global__ void combine_kernel(const uint16_t* __restrict__ Y, const int32_t* __
       const bool ok_e = e >= 0 && e < E;
       if (!ok_e) set_error(err, QW_ERR_INVALID_ARG);
       l = ok_e ? __ldg(logits + t * E + e) : 0.f;
-      r = __ldg(inv + t * k + j);
+      r = inv ? __ldg(inv + t * k + j) : row[j];
       if (r < 0 || r >= P) {
         set_error(err, QW_ERR_INVALID_ARG);
         r = 0;
@@ -168,6 +183,9 @@ __global__ void combine_kernel(const uint16_t* __restrict__ Y, const int32_t* __
   }
 }
 
+// pairs up to which the combine scans the sorted pair list per token instead of inverting it
+constexpr int64_t kCombineScanPairs = 2048;
+
 unsigned stream_grid(int64_t work_items, int threads) {
   const int64_t want = (work_items + threads - 1) / threads;
   const int64_t cap = (int64_t)device_sm_count() * 8;
@@ -194,12 +212,17 @@ qw_status launch_moe_combine(const void* Y, const int32_t* sorted_pairs, const i
                              const float* logits, int32_t T, int32_t E, int32_t topk, int32_t N,
                              void* out, int32_t* inv, int32_t* err, cudaStream_t st) {
   const int64_t P = (int64_t)T * topk;
-  invert_pairs_kernel<<<stream_grid(P, 256), 256, 0, st>>>(sorted_pairs, P, inv, err);
-  if (cudaGetLastError() != cudaSuccess) return QW_ERR_CUDA;
+  // decode-sized batches: each token's CTA scans the pair list itself (no inversion launch)
+  const bool scan = P <= kCombineScanPairs;
+  if (!scan) {
+    invert_pairs_kernel<<<stream_grid(P, 256), 256, 0, st>>>(sorted_pairs, P, inv, err);
+    if (cudaGetLastError() != cudaSuccess) return QW_ERR_CUDA;
+  }
   int threads = (N / 8 + 31) / 32 * 32;
   if (threads > 512) threads = 512;
   if (threads < 32) threads = 32;
-  combine_kernel<<<(unsigned)T, threads, 0, st>>>(static_cast<const uint16_t*>(Y), inv, topk_ids,
+  combine_kernel<<<(unsigned)T, threads, 0, st>>>(static_cast<const uint16_t*>(Y),
+                                                   scan ? nullptr : inv, sorted_pairs, topk_ids,
                                                    logits, E, topk, N, P,
                                                    static_cast<uint16_t*>(out), err);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;

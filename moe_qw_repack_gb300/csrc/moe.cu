@@ -17,13 +17,13 @@ namespace {
 constexpr int kChunk = 256;  // pairs per histogram / scatter CTA
 
 // -------------------------------------------------------------------- top-k (warp per token)
+// One warp selects token t's k experts: ids[t k + r] for r = 0 .. k - 1 (and, when `sh` is
+// given, the same ids in shared memory).
 template <int VPL>  // logits held per lane: E <= 32 * VPL
-__global__ void __launch_bounds__(256)
-    topk_kernel(const float* __restrict__ logits, int32_t T, int32_t E, int32_t k,
-                int32_t* __restrict__ ids, int32_t* err) {
+__device__ __forceinline__ void topk_token(const float* __restrict__ logits, int64_t t, int32_t E,
+                                           int32_t k, int32_t* __restrict__ ids, int32_t* sh,
+                                           int32_t* err) {
   const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
   float v[VPL];
   uint32_t taken = 0;
 #pragma unroll
@@ -62,7 +62,91 @@ __global__ void __launch_bounds__(256)
     } else if ((bi & 31) == lane) {
       taken |= 1u << (bi >> 5);
     }
-    if (lane == 0) ids[t * k + r] = bi;
+    if (lane == 0) {
+      ids[t * k + r] = bi;
+      if (sh) sh[t * k + r] = bi;
+    }
+  }
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256)
+    topk_kernel(const float* __restrict__ logits, int32_t T, int32_t E, int32_t k,
+                int32_t* __restrict__ ids, int32_t* err) {
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  topk_token<VPL>(logits, t, E, k, ids, nullptr, err);
+}
+
+// -------------------------------------------------------------------- small batches: one CTA
+// For at most kSmallPairs pairs and kSmallExperts experts (decode-sized batches) the whole
+// routing runs in one CTA of 32 warps, with the same results as the four kernels below:
+// top-k (warp per token), per-expert counts, the offsets scan, then the stable scatter in
+// pair order, 1024 pairs at a time (ranks within a warp by __match_any_sync, across warps by
+// per-warp counts in shared memory).
+constexpr int kSmallPairs = 1024, kSmallExperts = 256;
+
+template <int VPL>
+__global__ void __launch_bounds__(1024)
+    route_small_kernel(const float* __restrict__ logits, int32_t T, int32_t E, int32_t k,
+                       int32_t* __restrict__ ids, int32_t* __restrict__ sorted_pairs,
+                       int32_t* __restrict__ offsets, int32_t* err) {
+  __shared__ int32_t sid[kSmallPairs];
+  __shared__ int32_t base[kSmallExperts + 1];
+  __shared__ int32_t wcnt[32][kSmallExperts];
+  __shared__ int32_t warp_sums[32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int P = T * k;
+  for (int t = w; t < T; t += 32) topk_token<VPL>(logits, t, E, k, ids, sid, err);
+  for (int e = threadIdx.x; e < E; e += 1024) base[e] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += 1024) atomicAdd(&base[sid[p]], 1);
+  __syncthreads();
+  // exclusive scan of the counts over experts (E <= 256: warps 0 .. 7)
+  {
+    const int e = threadIdx.x;
+    const int32_t x = e < E ? base[e] : 0;
+    int32_t incl = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      const int32_t s0 = warp_sums[lane];
+      int32_t si = s0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, si, off);
+        if (lane >= off) si += y;
+      }
+      warp_sums[lane] = si - s0;
+    }
+    __syncthreads();
+    const int32_t excl = incl - x + warp_sums[w];
+    if (e < E) {
+      offsets[e] = excl;
+      if (e == E - 1) offsets[E] = excl + x;
+      base[e] = excl;
+    }
+    __syncthreads();
+  }
+  // stable scatter, pair order; P <= 1024: one pass of 32 warps
+  for (int i = threadIdx.x; i < 32 * kSmallExperts; i += 1024) (&wcnt[0][0])[i] = 0;
+  __syncthreads();
+  const int p = threadIdx.x;
+  const bool valid = p < P;
+  const int e = valid ? sid[p] : -1 - lane;  // distinct dummies never match
+  const uint32_t m = __match_any_sync(0xFFFFFFFFu, e);
+  const int wrank = __popc(m & ((1u << lane) - 1u));
+  if (valid && wrank == 0) wcnt[w][e] = __popc(m);
+  __syncthreads();
+  if (valid) {
+    int32_t r = base[e] + wrank;
+    for (int ww = 0; ww < w; ++ww) r += wcnt[ww][e];
+    sorted_pairs[r] = p;
   }
 }
 
@@ -270,6 +354,14 @@ qw_status launch_moe_route(const float* logits, int32_t T, int32_t E, int32_t to
   if (ws_bytes < moe_route_workspace(T, E, topk) || ws == nullptr) return QW_ERR_WORKSPACE;
   int32_t* hist = static_cast<int32_t*>(ws);
   const int64_t nchunks = (P + kChunk - 1) / kChunk;
+  if (T > 0 && P <= kSmallPairs && E <= kSmallExperts) {
+    const int vpl = (E + 31) / 32;
+    if (vpl <= 1) route_small_kernel<1><<<1, 1024, 0, st>>>(logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
+    else if (vpl <= 2) route_small_kernel<2><<<1, 1024, 0, st>>>(logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
+    else if (vpl <= 4) route_small_kernel<4><<<1, 1024, 0, st>>>(logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
+    else route_small_kernel<8><<<1, 1024, 0, st>>>(logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
+    return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+  }
   if (T > 0) {
     const unsigned gt = (unsigned)((T + 7) / 8);
     const int vpl = (E + 31) / 32;
