@@ -35,6 +35,8 @@ __device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
 // group never straddles rows and its four threads sit in the same warp).
 __global__ void quantize_mxfp8_kernel(const uint4* __restrict__ A, int64_t n8, uint2* __restrict__ Q,
                                       uint8_t* __restrict__ SF, int32_t* err) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   // every thread of a warp runs the same number of iterations (n8 % 4 == 0, stride % 32 == 0)
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < n8;
@@ -75,6 +77,8 @@ __global__ void quantize_mxfp8_kernel(const uint4* __restrict__ A, int64_t n8, u
 // One thread = 8 outputs of one row: y = silu(g) * u, g the first half, u the second half.
 __global__ void silu_mul_kernel(const uint16_t* __restrict__ GU, int64_t rows, int32_t I,
                                 uint16_t* __restrict__ Y) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   const int32_t per_row = I / 8;
   const int64_t total = rows * per_row;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -100,6 +104,8 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ GU, int64_t rows, i
 // position of every pair in the sorted order: inv[sorted_pairs[i]] = i
 __global__ void invert_pairs_kernel(const int32_t* __restrict__ sp, int64_t P,
                                     int32_t* __restrict__ inv, int32_t* err) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < P;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t pair = __ldg(sp + i);
@@ -119,6 +125,8 @@ __global__ void combine_kernel(const uint16_t* __restrict__ Y, const int32_t* __
                                const int32_t* __restrict__ sp, const int32_t* __restrict__ ids,
                                const float* __restrict__ logits, int32_t E, int32_t k, int32_t N,
                                int64_t P, uint16_t* __restrict__ out, int32_t* err) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   const int64_t t = blockIdx.x;
   __shared__ float w[32];
   __shared__ int32_t row[32];
@@ -197,14 +205,12 @@ unsigned stream_grid(int64_t work_items, int threads) {
 qw_status launch_quantize_mxfp8(const void* A, int64_t rows, int32_t K, void* Q, void* SF,
                                 int32_t* err, cudaStream_t st) {
   const int64_t n8 = rows * (int64_t)(K / 8);
-  quantize_mxfp8_kernel<<<stream_grid(n8, 256), 256, 0, st>>>(
-      static_cast<const uint4*>(A), n8, static_cast<uint2*>(Q), static_cast<uint8_t*>(SF), err);
+  (void)launch_pdl(quantize_mxfp8_kernel, dim3(stream_grid(n8, 256)), dim3(256), 0, st, static_cast<const uint4*>(A), n8, static_cast<uint2*>(Q), static_cast<uint8_t*>(SF), err);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 
 qw_status launch_silu_mul(const void* GU, int64_t rows, int32_t I, void* Y, cudaStream_t st) {
-  silu_mul_kernel<<<stream_grid(rows * (int64_t)(I / 8), 256), 256, 0, st>>>(
-      static_cast<const uint16_t*>(GU), rows, I, static_cast<uint16_t*>(Y));
+  (void)launch_pdl(silu_mul_kernel, dim3(stream_grid(rows * (int64_t)(I / 8), 256)), dim3(256), 0, st, static_cast<const uint16_t*>(GU), rows, I, static_cast<uint16_t*>(Y));
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 
@@ -215,13 +221,13 @@ qw_status launch_moe_combine(const void* Y, const int32_t* sorted_pairs, const i
   // decode-sized batches: each token's CTA scans the pair list itself (no inversion launch)
   const bool scan = P <= kCombineScanPairs;
   if (!scan) {
-    invert_pairs_kernel<<<stream_grid(P, 256), 256, 0, st>>>(sorted_pairs, P, inv, err);
+    (void)launch_pdl(invert_pairs_kernel, dim3(stream_grid(P, 256)), dim3(256), 0, st, sorted_pairs, P, inv, err);
     if (cudaGetLastError() != cudaSuccess) return QW_ERR_CUDA;
   }
   int threads = (N / 8 + 31) / 32 * 32;
   if (threads > 512) threads = 512;
   if (threads < 32) threads = 32;
-  combine_kernel<<<(unsigned)T, threads, 0, st>>>(static_cast<const uint16_t*>(Y),
+  (void)launch_pdl(combine_kernel, dim3((unsigned)T), dim3(threads), 0, st, static_cast<const uint16_t*>(Y),
                                                    scan ? nullptr : inv, sorted_pairs, topk_ids,
                                                    logits, E, topk, N, P,
                                                    static_cast<uint16_t*>(out), err);

@@ -171,35 +171,6 @@ struct Geo {
 
 // groups per batch = register ring depth (token rows cost registers)
 __host__ __device__ constexpr int batch_groups(int mch) { return mch >= 4 ? 2 : 4; }
-// Programmatic dependent launch: the next kernel on the stream may start once every CTA of
-// this one has run this (its CTAs then fill SMs as this kernel's CTAs retire) ...
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-// ... and waits here until the previous kernel has finished and its writes are visible.
-// Only the packed weights and scales are read before this point.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Launch as a programmatic dependent of the previous kernel on the stream: the kernel may
-// start streaming weights while that kernel drains; it executes griddepcontrol.wait before
-// it touches anything the previous kernel may have written.
-template <class Kern, class... Args>
-qw_status launch_pdl(Kern kern, unsigned grid, unsigned threads, size_t smem, cudaStream_t st,
-                     const Args&... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return QW_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
-}
-
 struct Params {
   const uint8_t* wp;
   const uint16_t* sp;

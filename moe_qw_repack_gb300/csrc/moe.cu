@@ -73,6 +73,8 @@ template <int VPL>
 __global__ void __launch_bounds__(256)
     topk_kernel(const float* __restrict__ logits, int32_t T, int32_t E, int32_t k,
                 int32_t* __restrict__ ids, int32_t* err) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   topk_token<VPL>(logits, t, E, k, ids, nullptr, err);
@@ -91,6 +93,8 @@ __global__ void __launch_bounds__(1024)
     route_small_kernel(const float* __restrict__ logits, int32_t T, int32_t E, int32_t k,
                        int32_t* __restrict__ ids, int32_t* __restrict__ sorted_pairs,
                        int32_t* __restrict__ offsets, int32_t* err) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   __shared__ int32_t sid[kSmallPairs];
   __shared__ int32_t base[kSmallExperts + 1];
   __shared__ int32_t wcnt[32][kSmallExperts];
@@ -154,6 +158,8 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(kChunk)
     chunk_hist_kernel(const int32_t* __restrict__ ids, int64_t P, int32_t E,
                       int32_t* __restrict__ hist) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   extern __shared__ int32_t sh[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
   __syncthreads();
@@ -169,6 +175,8 @@ __global__ void __launch_bounds__(kChunk)
 __global__ void __launch_bounds__(1024)
     offsets_kernel(int32_t* __restrict__ hist, int64_t nchunks, int32_t E,
                    int32_t* __restrict__ offsets) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   __shared__ int32_t warp_sums[32];
   const int e = threadIdx.x;
   int32_t run = 0;
@@ -212,6 +220,8 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(kChunk)
     scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int32_t E,
                    const int32_t* __restrict__ base, int32_t* __restrict__ sorted_pairs) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   extern __shared__ int32_t cnt[];  // [kChunk / 32][E]
   constexpr int W = kChunk / 32;
   for (int i = threadIdx.x; i < W * E; i += blockDim.x) cnt[i] = 0;
@@ -236,6 +246,8 @@ __global__ void __launch_bounds__(1024)
     tile_queue_kernel(const int32_t* __restrict__ offsets, int32_t E, int32_t TR,
                       int64_t total_rows, int32_t* __restrict__ queue, int64_t max_entries,
                       int32_t* err) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   __shared__ int32_t warp_sums[32];
   __shared__ int32_t carry;
   if (threadIdx.x == 0) carry = 0;
@@ -298,6 +310,8 @@ __global__ void __launch_bounds__(1024)
 __global__ void permute_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                     int64_t row_vecs, const int32_t* __restrict__ sorted_pairs,
                                     int64_t P, int32_t topk) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   const int64_t total = P * row_vecs;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -309,6 +323,8 @@ __global__ void permute_rows_kernel(const uint4* __restrict__ src, uint4* __rest
 __global__ void permute_bytes_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                      int64_t row_bytes, const int32_t* __restrict__ sorted_pairs,
                                      int64_t P, int32_t topk) {
+  pdl_wait();  // the previous kernel's outputs (launched as its dependent)
+  pdl_launch_dependents();
   const int64_t total = P * row_bytes;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -356,26 +372,26 @@ qw_status launch_moe_route(const float* logits, int32_t T, int32_t E, int32_t to
   const int64_t nchunks = (P + kChunk - 1) / kChunk;
   if (T > 0 && P <= kSmallPairs && E <= kSmallExperts) {
     const int vpl = (E + 31) / 32;
-    if (vpl <= 1) route_small_kernel<1><<<1, 1024, 0, st>>>(logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
-    else if (vpl <= 2) route_small_kernel<2><<<1, 1024, 0, st>>>(logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
-    else if (vpl <= 4) route_small_kernel<4><<<1, 1024, 0, st>>>(logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
-    else route_small_kernel<8><<<1, 1024, 0, st>>>(logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
+    if (vpl <= 1) (void)launch_pdl(route_small_kernel<1>, dim3(1), dim3(1024), 0, st, logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
+    else if (vpl <= 2) (void)launch_pdl(route_small_kernel<2>, dim3(1), dim3(1024), 0, st, logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
+    else if (vpl <= 4) (void)launch_pdl(route_small_kernel<4>, dim3(1), dim3(1024), 0, st, logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
+    else (void)launch_pdl(route_small_kernel<8>, dim3(1), dim3(1024), 0, st, logits, T, E, topk, topk_ids, sorted_pairs, offsets, err);
     return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
   }
   if (T > 0) {
     const unsigned gt = (unsigned)((T + 7) / 8);
     const int vpl = (E + 31) / 32;
-    if (vpl <= 1) topk_kernel<1><<<gt, 256, 0, st>>>(logits, T, E, topk, topk_ids, err);
-    else if (vpl <= 2) topk_kernel<2><<<gt, 256, 0, st>>>(logits, T, E, topk, topk_ids, err);
-    else if (vpl <= 4) topk_kernel<4><<<gt, 256, 0, st>>>(logits, T, E, topk, topk_ids, err);
-    else if (vpl <= 8) topk_kernel<8><<<gt, 256, 0, st>>>(logits, T, E, topk, topk_ids, err);
-    else if (vpl <= 16) topk_kernel<16><<<gt, 256, 0, st>>>(logits, T, E, topk, topk_ids, err);
-    else topk_kernel<32><<<gt, 256, 0, st>>>(logits, T, E, topk, topk_ids, err);
-    chunk_hist_kernel<<<(unsigned)nchunks, kChunk, E * 4, st>>>(topk_ids, P, E, hist);
+    if (vpl <= 1) (void)launch_pdl(topk_kernel<1>, dim3(gt), dim3(256), 0, st, logits, T, E, topk, topk_ids, err);
+    else if (vpl <= 2) (void)launch_pdl(topk_kernel<2>, dim3(gt), dim3(256), 0, st, logits, T, E, topk, topk_ids, err);
+    else if (vpl <= 4) (void)launch_pdl(topk_kernel<4>, dim3(gt), dim3(256), 0, st, logits, T, E, topk, topk_ids, err);
+    else if (vpl <= 8) (void)launch_pdl(topk_kernel<8>, dim3(gt), dim3(256), 0, st, logits, T, E, topk, topk_ids, err);
+    else if (vpl <= 16) (void)launch_pdl(topk_kernel<16>, dim3(gt), dim3(256), 0, st, logits, T, E, topk, topk_ids, err);
+    else (void)launch_pdl(topk_kernel<32>, dim3(gt), dim3(256), 0, st, logits, T, E, topk, topk_ids, err);
+    (void)launch_pdl(chunk_hist_kernel, dim3((unsigned)nchunks), dim3(kChunk), E * 4, st, topk_ids, P, E, hist);
   }
-  offsets_kernel<<<1, 1024, 0, st>>>(hist, nchunks, E, offsets);
+  (void)launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, st, hist, nchunks, E, offsets);
   if (T > 0)
-    scatter_kernel<<<(unsigned)nchunks, kChunk, (kChunk / 32) * E * 4, st>>>(topk_ids, P, E, hist,
+    (void)launch_pdl(scatter_kernel, dim3((unsigned)nchunks), dim3(kChunk), (kChunk / 32) * E * 4, st, topk_ids, P, E, hist,
                                                                              sorted_pairs);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
@@ -387,12 +403,10 @@ qw_status launch_moe_permute(int32_t afmt, const void* A, const void* A_sf, int3
   const int64_t row_bytes =
       afmt == QW_A_BF16 ? 2 * (int64_t)K : (afmt == QW_A_NVFP4_G16 ? K / 2 : (int64_t)K);
   const int64_t vecs = row_bytes / 16;
-  permute_rows_kernel<<<grid_cap(P * vecs, 256), 256, 0, st>>>(
-      (const uint4*)A, (uint4*)A_sorted, vecs, sorted_pairs, P, topk);
+  (void)launch_pdl(permute_rows_kernel, dim3(grid_cap(P * vecs, 256)), dim3(256), 0, st, (const uint4*)A, (uint4*)A_sorted, vecs, sorted_pairs, P, topk);
   if (afmt != QW_A_BF16) {
     const int64_t sb = K / (afmt == QW_A_NVFP4_G16 ? 16 : 32);  // scale bytes per row
-    permute_bytes_kernel<<<grid_cap(P * sb, 256), 256, 0, st>>>(
-        (const uint8_t*)A_sf, (uint8_t*)A_sf_sorted, sb, sorted_pairs, P, topk);
+    (void)launch_pdl(permute_bytes_kernel, dim3(grid_cap(P * sb, 256)), dim3(256), 0, st, (const uint8_t*)A_sf, (uint8_t*)A_sf_sorted, sb, sorted_pairs, P, topk);
   }
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
@@ -405,7 +419,7 @@ uint64_t tile_queue_bytes(int32_t E, int64_t rows, int32_t tile_rows) {
 qw_status launch_build_tile_queue(const int32_t* offsets, int32_t E, int32_t tile_rows,
                                   int64_t total_rows, int32_t* queue, int64_t max_entries,
                                   int32_t* err, cudaStream_t st) {
-  tile_queue_kernel<<<1, 1024, 0, st>>>(offsets, E, tile_rows, total_rows, queue, max_entries,
+  (void)launch_pdl(tile_queue_kernel, dim3(1), dim3(1024), 0, st, offsets, E, tile_rows, total_rows, queue, max_entries,
                                         err);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
