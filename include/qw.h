@@ -92,10 +92,10 @@ typedef enum qw_afmt {
 /* Description of one repacked weight set (E experts; E = 1 for a dense layer).
  * Filled by qw_repack_query; treat as read-only. */
 typedef struct qw_packed_desc {
-  int32_t wfmt;            /* qw_wfmt                                                  */
+  int32_t wfmt;            /* qw_wfmt, possibly | QW_W_SCALE2                          */
   int32_t E, N, K;         /* logical sizes                                            */
   int32_t N_pad, K_pad;    /* padded sizes of the packed layout                        */
-  int32_t group;           /* 128 (INT), 32 (MXFP4 / MXFP8) or 16 (NVFP4)              */
+  int32_t group;           /* 128 (INT, FP8E4M3), 32 (MXFP4 / MXFP8) or 16 (NVFP4)     */
   int32_t reserved;
   uint64_t w_bytes;        /* size of w_packed in bytes (all experts)                  */
   uint64_t s_bytes;        /* size of s_packed in bytes (all experts)                  */
