@@ -34,12 +34,20 @@ namespace {
 constexpr int kW8Warps = 8;
 constexpr int kW8Ring = 16;  // scale groups per batch (two code words per group and lane)
 
-// two E2M1 codes (the low byte of `byte`, first code in the low nibble) -> FP16 pair
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+// the four bytes of `x` (two E2M1 codes each, first code in the low nibble) -> four FP16
+// pairs, d[i] from byte i (the bytes feed the conversions directly)
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t x, uint32_t (&d)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(x));
+}
+// two E8M0 scales (the low 16 bits of `pair`) -> 2^(s - 127) as a BF16 pair, exactly (the
+// smallest, 2^-127, is a BF16 subnormal)
+__device__ __forceinline__ uint32_t e8m0x2_to_bf16x2(uint32_t pair) {
   uint32_t d;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
-      : "=r"(d)
-      : "r"(byte));
+  asm("cvt.rn.bf16x2.ue8m0x2 %0, %1;" : "=r"(d) : "h"((uint16_t)pair));
   return d;
 }
 // two E4M3 codes (the low 16 bits of `pair`, first code in the low byte) -> FP16 pair
@@ -195,20 +203,19 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
           refill_w(j);
           if ((j & 3) == 3) refill_s(j >> 2);
           float pr[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t ca[4], cb[4];  // FP16 pairs of the code bytes of rows g and g + 8
+          e2m1x8_to_f16x2(wa, ca);
+          e2m1x8_to_f16x2(wb, cb);
 #pragma unroll
-          for (int st = 0; st < 2; ++st) {
-            const int sh = 16 * st;  // code bytes 2st, 2st + 1 of each row
-            uint32_t a[4];
-            // (the conversion reads the low byte of its operand)
-            a[0] = e2m1x2_to_f16x2(wa >> sh);
-            a[1] = e2m1x2_to_f16x2(wb >> sh);
-            a[2] = e2m1x2_to_f16x2(wa >> (sh + 8));
-            a[3] = e2m1x2_to_f16x2(wb >> (sh + 8));
+          for (int st = 0; st < 2; ++st) {  // code bytes 2st, 2st + 1 of each row
+            const uint32_t a[4] = {ca[2 * st], cb[2 * st], ca[2 * st + 1], cb[2 * st + 1]};
             mma_f16_16816(pr, a, st ? x.z : x.x, st ? x.w : x.y);
           }
-          const int sb = 8 * (j & 3);  // this group's byte in the scale words (gb % 4 == 0)
-          const float fw0 = e8m0_to_f32((swa >> sb) & 0xFFu);
-          const float fw1 = e8m0_to_f32((swb >> sb) & 0xFFu);
+          // this group's byte of each row's scale word (gb % 4 == 0), both converted at once
+          const uint32_t sbyte = (uint32_t)(j & 3);
+          const uint32_t wsc = e8m0x2_to_bf16x2(__byte_perm(swa, swb, sbyte | ((4u + sbyte) << 4)));
+          const float fw0 = __uint_as_float(wsc << 16);
+          const float fw1 = __uint_as_float(wsc & 0xFFFF0000u);
           const float fa0 = __uint_as_float(f2.x), fa1 = __uint_as_float(f2.y);
           acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
           acc[1] = fmaf(pr[1] * fw0, fa1, acc[1]);
