@@ -146,17 +146,20 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *          k = 16s + 4t + 2 ((i >> 1) & 1) + (i >> 2) - rows g and g + 8 at the four k's
  *          16s + 4t .. 16s + 4t + 3 (also the register layout of a 16-lane TMEM store).
  *          Scales BF16 [K/128][N_pad].
- *   INT3:  per expert [K/128][N_pad/16] blocks of 768 B: 32 lanes x 4 words holding the
- *          low two bits of q + 4 for the lane's 64 weights (the INT4 (row, k) assignment),
- *          then 32 lanes x 2 words holding their third bit.  Scales BF16 [K/128][N_pad].
+ *   INT3:  per expert [K/128][N_pad/16] blocks of 768 B: 32 lanes x 4 words, then 32
+ *          lanes x 2 words; the lane's six words hold u = q + 4 for its 64 weights (the
+ *          INT4 (row, k) assignment) as 32 pairs, pair j = 4s + r for rows g + 8 (r & 1)
+ *          at k = 16s + 4t + 2 (r >> 1) + h: for j < 30, bits 3 (j % 5) + 16h of word
+ *          j / 5; pairs 30 and 31 keep bit i of u at bit 15 + 16h of word i and 3 + i.
+ *          Scales BF16 [K/128][N_pad].
  *   MXFP4: codes uint8 [N_pad][K_pad/2] (canonical order, zero-padded); scales E8M0 in
  *          512-byte chunks per 128 rows x 4 groups, chunk (r/128, g/4) at
  *          ((r/128) * (K_pad/128) + g/4) * 512, byte (r%32)*16 + ((r%128)/32)*4 + g%4;
  *          padding bytes are 127 (scale 1).
  *   MXFP8: codes uint8 [N_pad][K_pad] (canonical order, zero-padded); scales as MXFP4.
  *   INT2:  per expert [K/128][N_pad/16] blocks of 512 B: 32 lanes x 4 words holding q + 2
- *          for the lane's 64 weights (the INT4 (row, k) assignment) in the INT3 low-plane
- *          bit positions.  Scales BF16 [K/128][N_pad].
+ *          for the lane's 64 weights (the INT4 (row, k) assignment): pair j = 4s + r at
+ *          bits 2 (4 (s % 2) + r) + 16h of word s / 2.  Scales BF16 [K/128][N_pad].
  *   FP8E4M3: per expert [K/128][N_pad/16] blocks of 2 KiB: 32 lanes x 16 words; byte b of
  *          word 2s + j of lane l = 4g + t is the code of row g + 8 (b >> 1) at
  *          k = 16s + 4t + 2j + (b & 1) (the INT4 (row, k) assignment, one byte per weight:

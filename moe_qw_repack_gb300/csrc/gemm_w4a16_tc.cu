@@ -391,17 +391,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   v[4 * st + ((r & 1) << 1) + (r >> 1)] = bf16x2_sub_u32(biased, excess);
                 }
             } else {
+              // INT3: register j = 4st + r is the 3-bit field j % 5 of word j / 5, except
+              // j = 30, 31, gathered from the spare bit 15 + 16h of words 0..2 and 3..5
               const uint4 lo = lds128(blk + lane * 16);
               const uint2 hi = lds64(blk + 512 + lane * 8);
-              const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w}, H[2] = {hi.x, hi.y};
+              const uint32_t W[6] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y};
 #pragma unroll
               for (int st = 0; st < 8; ++st)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                  const int ls = 2 * (4 * (st & 1) + r), hs = 4 * (st & 3) + r;
-                  const uint32_t hb = hs >= 2 ? H[st >> 2] >> (hs - 2) : H[st >> 2] << (2 - hs);
-                  const uint32_t biased =
-                      and_or(hb, 0x00040004u, and_or(L[st >> 1] >> ls, 0x00030003u, magic));
+                  const int j = 4 * st + r;
+                  uint32_t biased;
+                  if (j < 30) {
+                    biased = and_or(W[j / 5] >> (3 * (j % 5)), 0x00070007u, magic);
+                  } else {
+                    const int b = j == 30 ? 0 : 3;
+                    biased = and_or(W[b + 2] >> 13, 0x00040004u,
+                                    and_or(W[b + 1] >> 14, 0x00020002u,
+                                           and_or(W[b] >> 15, 0x00010001u, magic)));
+                  }
                   // register r (row g + 8 (r & 1), k + 2 (r >> 1)) -> store slot
                   v[4 * st + ((r & 1) << 1) + (r >> 1)] = bf16x2_sub_u32(biased, excess);
                 }

@@ -71,8 +71,9 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 
 // Step S of a group -> four BF16x2 A-fragment registers holding 128 + code.
 // INT4: word S of the lane's eight, nibble pairs at shifts 0, 4, 8, 12 (one shift and one
-// logic op per pair).  INT3: low two bits from lo-plane word S/2, third bit from hi-plane
-// word S/4 (two shifts and two logic ops per pair).  INT2: the INT3 lo plane alone.
+// logic op per pair).  INT3: register j = 4S + r is the 3-bit field j % 5 of word j / 5
+// (one shift and one logic op, like INT4), except j = 30, 31, gathered from the spare bit
+// 15 + 16h of words 0..2 and 3..5.  INT2: 2-bit fields of word S/2 at 2 (4 (S & 1) + r).
 template <int BITS, int S>
 __device__ __forceinline__ void biased_step(const uint32_t (&w)[8], uint32_t (&a)[4]) {
   const uint32_t magic = 0x43004300u;  // BF16 pair (128, 128)
@@ -87,13 +88,16 @@ __device__ __forceinline__ void biased_step(const uint32_t (&w)[8], uint32_t (&a
 #pragma unroll
     for (int r = 0; r < 4; ++r) a[r] = and_or(L >> (2 * (4 * (S & 1) + r)), 0x00030003u, magic);
   } else {
-    const uint32_t L = w[S / 2], H = w[4 + S / 4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int ls = 2 * (4 * (S & 1) + r);
-      const int hs = 4 * (S & 3) + r;  // hi bit to bit 2 of each half
-      const uint32_t hb = hs >= 2 ? H >> (hs - 2) : H << (2 - hs);
-      a[r] = and_or(hb, 0x00040004u, and_or(L >> ls, 0x00030003u, magic));
+      const int j = 4 * S + r;
+      if (j < 30) {
+        a[r] = and_or(w[j / 5] >> (3 * (j % 5)), 0x00070007u, magic);
+      } else {
+        const int b = j == 30 ? 0 : 3;
+        a[r] = and_or(w[b + 2] >> 13, 0x00040004u,
+                      and_or(w[b + 1] >> 14, 0x00020002u, and_or(w[b] >> 15, 0x00010001u, magic)));
+      }
     }
   }
 }
@@ -203,7 +207,7 @@ __device__ __forceinline__ void item_of(const Params& p, uint32_t item, uint32_t
   }
 }
 
-// The lane's packed words of one 16 x 128 block (INT4: 8 words; INT3: 4 lo + 2 hi words;
+// The lane's packed words of one 16 x 128 block (INT4: 8 words; INT3: 4 + 2 words;
 // INT2: 4 words; E4M3: 16 words).
 template <int BITS>
 __device__ __forceinline__ void load_words(const uint8_t* blk, int lane,

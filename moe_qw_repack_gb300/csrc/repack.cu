@@ -113,9 +113,12 @@ __device__ __forceinline__ int32_t int3_canon(const uint32_t* wc, int32_t K, int
 }
 
 // Packed INT3 of lane l, step s, register r, half h (same (row, k) as the INT4 words:
-// row g + 8 (r & 1), k 16s + 4t + 2 (r >> 1) + h): the lo plane keeps u & 3 in word
-// s/2 at bits 2 * (4 * (s % 2) + r) + 16 h; the hi plane keeps u >> 2 in word s/4 at bit
-// 4 * (s % 4) + r + 16 h; u = q + 4.
+// row g + 8 (r & 1), k 16s + 4t + 2 (r >> 1) + h), u = q + 4 in three bits.  The lane's six
+// words (four in the first 512 bytes of the block, two in the last 256) each hold five
+// registers: register j = 4s + r < 30 is field j % 5 of word j / 5, u at bits
+// 3 (j % 5) + 16 h, so that one shift and one logic op give a BF16 pair, as for INT4.
+// The two registers left over use the spare bit 15 + 16 h of each word: bit i of u is in
+// word i (j = 30) or word 3 + i (j = 31).
 __global__ void repack_int3_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
                                    int32_t E, int32_t N, int32_t N_pad, int32_t K, int32_t* err) {
   const int64_t per_expert = (int64_t)(K / 128) * (N_pad / 16) * 32;  // (block, lane)
@@ -129,7 +132,7 @@ __global__ void repack_int3_kernel(const uint32_t* __restrict__ wc, uint32_t* __
     const int G = (int)(blk / (N_pad / 16));
     const int nb = (int)(blk % (N_pad / 16));
     const uint32_t* wce = wc + e * (int64_t)N * (K / 32) * 3;
-    uint32_t lo[4] = {0, 0, 0, 0}, hi[2] = {0, 0};
+    uint32_t W[6] = {0, 0, 0, 0, 0, 0};
     const int g = lane >> 2, t = lane & 3;
     for (int s = 0; s < 8; ++s)
       for (int r = 0; r < 4; ++r)
@@ -146,12 +149,17 @@ __global__ void repack_int3_kernel(const uint32_t* __restrict__ wc, uint32_t* __
             }
           }
           const uint32_t u = (uint32_t)(q + 4);
-          lo[s / 2] |= (u & 3u) << (2 * (4 * (s % 2) + r) + 16 * h);
-          hi[s / 4] |= ((u >> 2) & 1u) << (4 * (s % 4) + r + 16 * h);
+          const int j = 4 * s + r;
+          if (j < 30) {
+            W[j / 5] |= u << (3 * (j % 5) + 16 * h);
+          } else {
+            const int b = j == 30 ? 0 : 3;
+            for (int i = 0; i < 3; ++i) W[b + i] |= ((u >> i) & 1u) << (15 + 16 * h);
+          }
         }
     uint32_t* out = wp + e * (int64_t)(K / 128) * (N_pad / 16) * 192 + blk * 192;
-    for (int i = 0; i < 4; ++i) out[lane * 4 + i] = lo[i];
-    for (int i = 0; i < 2; ++i) out[128 + lane * 2 + i] = hi[i];
+    for (int i = 0; i < 4; ++i) out[lane * 4 + i] = W[i];
+    for (int i = 0; i < 2; ++i) out[128 + lane * 2 + i] = W[4 + i];
   }
 }
 
@@ -176,9 +184,20 @@ __global__ void unpack_int3_kernel(const uint32_t* __restrict__ wp, uint32_t* __
       const int g = row & 7, r = (row >> 3) | (((kk >> 1) & 1) << 1);
       const int lane = g * 4 + t;
       const uint32_t* blk = wpe + ((int64_t)G * (N_pad / 16) + nb) * 192;
-      const uint32_t L = blk[lane * 4 + s / 2], H = blk[128 + lane * 2 + s / 4];
-      const uint32_t u = ((L >> (2 * (4 * (s % 2) + r) + 16 * h)) & 3u) |
-                         (((H >> (4 * (s % 4) + r + 16 * h)) & 1u) << 2);
+      const int jr = 4 * s + r;  // the lane's register; its words as in repack_int3_kernel
+      uint32_t u = 0;
+      if (jr < 30) {
+        const int wi = jr / 5;
+        const uint32_t x = wi < 4 ? blk[lane * 4 + wi] : blk[128 + lane * 2 + (wi - 4)];
+        u = (x >> (3 * (jr % 5) + 16 * h)) & 7u;
+      } else {
+        const int b = jr == 30 ? 0 : 3;
+        for (int i = 0; i < 3; ++i) {
+          const int wi = b + i;
+          const uint32_t x = wi < 4 ? blk[lane * 4 + wi] : blk[128 + lane * 2 + (wi - 4)];
+          u |= ((x >> (15 + 16 * h)) & 1u) << i;
+        }
+      }
       const uint32_t code = (uint32_t)((int32_t)u - 4) & 7u;  // back to two's complement
       const int bit = 3 * j;
       w3[bit / 32] |= code << (bit % 32);
@@ -193,7 +212,7 @@ __global__ void unpack_int3_kernel(const uint32_t* __restrict__ wp, uint32_t* __
 
 // ----------------------------------------------------------------------------- INT2
 // Packed INT2 of lane l, step s, register r, half h (the INT4 (row, k) assignment): word s/2
-// of the lane's four keeps u = q + 2 at bits 2 * (4 * (s % 2) + r) + 16 h (the INT3 low plane).
+// of the lane's four keeps u = q + 2 at bits 2 * (4 * (s % 2) + r) + 16 h.
 __global__ void repack_int2_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
                                    int32_t E, int32_t N, int32_t N_pad, int32_t K, int32_t* err) {
   const int64_t per_expert = (int64_t)(K / 128) * (N_pad / 16) * 32;  // (block, lane)
