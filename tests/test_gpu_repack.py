@@ -64,6 +64,58 @@ def test_int4_packed_codes_are_excess8_fragments():
                 assert (words[lane, step] >> (4 * i)) & 0xF == q[0, row, k] + 8
 
 
+def test_int3_packed_codes_are_three_bit_fields():
+    """One 16 x 128 block: the lane's six words (4 at lane*16, 2 at 512 + lane*8) hold
+    u = q + 4 of pair j = 4s + r (rows g + 8(r & 1), k = 16s + 4t + 2(r >> 1) + h) at
+    bits 3(j % 5) + 16h of word j / 5 for j < 30, and bit i of u at bit 15 + 16h of word
+    i (j = 30) or 3 + i (j = 31)."""
+    rng = np.random.default_rng(7)
+    q = rng.integers(-3, 4, (1, 16, 128))
+    s = synth.to_bf16_bits(np.ones((1, 16, 1)))
+    Q = qw()
+    d = Q.qw_repack_query(1, 1, 16, 128)
+    wp, sp = Q.empty_packed(d)
+    Q.qw_repack(d, dev(synth.pack_int3(q)), dev(s), wp, sp)
+    raw = host(wp).view(np.uint32)
+    assert raw.size == 192
+    for lane in range(32):
+        g, t = lane // 4, lane % 4
+        w = [int(x) for x in raw[lane * 4:lane * 4 + 4]] + \
+            [int(x) for x in raw[128 + lane * 2:128 + lane * 2 + 2]]
+        for step in range(8):
+            for r in range(4):
+                j = 4 * step + r
+                for h in range(2):
+                    row, k = g + 8 * (r & 1), 16 * step + 4 * t + 2 * (r >> 1) + h
+                    if j < 30:
+                        u = (w[j // 5] >> (3 * (j % 5) + 16 * h)) & 7
+                    else:
+                        b = 0 if j == 30 else 3
+                        u = sum(((w[b + i] >> (15 + 16 * h)) & 1) << i for i in range(3))
+                    assert u == q[0, row, k] + 4, (lane, step, r, h)
+
+
+def test_int2_packed_codes_are_two_bit_fields():
+    """One 16 x 128 block: word s // 2 of lane l holds u = q + 2 of pair (s, r) at bits
+    2(4(s % 2) + r) + 16h, the (row, k) assignment as for INT4."""
+    rng = np.random.default_rng(8)
+    q = rng.integers(-1, 2, (1, 16, 128))
+    s = synth.to_bf16_bits(np.ones((1, 16, 1)))
+    Q = qw()
+    d = Q.qw_repack_query(6, 1, 16, 128)
+    wp, sp = Q.empty_packed(d)
+    Q.qw_repack(d, dev(synth.pack_int2(q)), dev(s), wp, sp)
+    words = host(wp).view(np.uint32).reshape(32, 4)
+    for lane in range(32):
+        g, t = lane // 4, lane % 4
+        for step in range(8):
+            for r in range(4):
+                for h in range(2):
+                    row, k = g + 8 * (r & 1), 16 * step + 4 * t + 2 * (r >> 1) + h
+                    u = (int(words[lane, step // 2]) >> (2 * (4 * (step % 2) + r) + 16 * h)) & 3
+                    assert u == q[0, row, k] + 2, (lane, step, r, h)
+
+
 def test_value_errors_flagged():
     Q = qw()
     # INT4 code -8
