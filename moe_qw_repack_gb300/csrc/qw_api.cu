@@ -12,17 +12,19 @@
 
 namespace qw {
 
+// SM count of the current device, cached per device (152 on GB300, also the value taken if
+// the query fails); it only sizes the grids of kernels that stride over their work.
 int device_sm_count() {
   static std::atomic<int> cache[64];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
   if (dev < 64) {
     int v = cache[dev].load(std::memory_order_relaxed);
     if (v > 0) return v;
   }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 148;
+    n = 152;
   if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
