@@ -113,8 +113,9 @@ int32_t qw_version(void);
  * qw_repack_query - sizes of the packed layout for E experts of an N x K weight.
  * Requirements: E >= 1, N >= 1, K >= 1; K % 128 == 0 for the INT formats, K % 32 == 0
  * for MXFP4 / MXFP8 / NVFP4.  Padding: INT formats pad N to a multiple of 16; the MX
- * formats pad N to a multiple of 128 and K to a multiple of 128 (NVFP4: 256).  `out` is a
- * host pointer.
+ * formats pad N to a multiple of 128 and K to a multiple of 128 (NVFP4: 256).  N and K
+ * are at most 2^31 - 256 (so the padded sizes fit in int32) and N_pad * E < 2^31.  `out`
+ * is a host pointer.
  * Returns QW_ERR_INVALID_ARG / QW_ERR_UNSUPPORTED on a bad request, else QW_OK.
  */
 qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_packed_desc* out);

@@ -107,6 +107,9 @@ int32_t qw_version(void) { return 210; }
 qw_status qw_repack_query(int32_t wfmt_in, int32_t E, int32_t N, int32_t K, qw_packed_desc* out) {
   if (!out || E < 1 || N < 1 || K < 1) return QW_ERR_INVALID_ARG;
   if (wfmt_in & ~(QW_W_SCALE2 | 0xFF)) return QW_ERR_UNSUPPORTED;
+  // every padded size (N to 128, K to 256 at most) must still fit in int32
+  constexpr int32_t kMaxDim = 0x7FFFFF00;
+  if (N > kMaxDim || K > kMaxDim) return QW_ERR_UNSUPPORTED;
   const int32_t wfmt = wfmt_in & ~QW_W_SCALE2;
   qw_packed_desc d{};
   d.wfmt = wfmt_in;

@@ -63,6 +63,22 @@ def test_repack_query_rejects(Q):
             Q.qw_repack_query(*args)
 
 
+def test_repack_query_int32_limits(Q):
+    """Sizes whose padding would overflow int32 are refused; the largest accepted ones give
+    padded sizes and byte counts that are exact."""
+    big = 2**31 - 1
+    for args in [(0, 1, big, 128), (Q.QW_W_MXFP4_G32, 1, big, 128),
+                 (Q.QW_W_MXFP4_G32, 1, 128, 2**31 - 32), (Q.QW_W_NVFP4_G16, 1, 128, 2**31 - 32),
+                 (0, 2, 2**30, 128)]:  # N_pad * E = 2^31
+        with pytest.raises(Q.QwError):
+            Q.qw_repack_query(*args)
+    kmax = 2**31 - 256
+    d = Q.qw_repack_query(Q.QW_W_NVFP4_G16, 1, 128, kmax)
+    assert (d.N_pad, d.K_pad, d.w_bytes) == (128, kmax, 128 * kmax // 2)
+    d = Q.qw_repack_query(0, 1, kmax, 128)
+    assert (d.N_pad, d.w_bytes, d.s_bytes) == (kmax, kmax // 16 * 1024, kmax * 2)
+
+
 def test_gemm_host_validation(Q):
     d = Q.qw_repack_query(Q.QW_W_MXFP4_G32, 1, 256, 256)
     good = 1 << 20  # fake, never dereferenced: every call below fails validation first
