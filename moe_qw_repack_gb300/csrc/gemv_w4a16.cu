@@ -26,8 +26,7 @@
 //     in shared memory in B-fragment order and per-group activation sums, which replace the
 //     all-ones MMA below (fewer issued instructions per weight: the decode GEMV is bound by
 //     issue slots as much as by HBM).
-//   - Grouped (gemv_tma_kernel): one producer thread per CTA
-//     streams an item's groups
+//   - Grouped (gemv_tma_kernel): one producer thread per CTA streams an item's groups
 //     eight at a time: a 4-D tensor map views the packed weights as [expert][group][16-row
 //     block][1 KiB], so one TMA copy brings 8 groups of a block (8 KiB; 1 KiB copies
 //     measured far below HBM speed on this GPU, 4-8 KiB ones reach it) plus a 3-D copy of
@@ -36,8 +35,8 @@
 //     alias).  With MoE tiles of a few rows and short K (e.g. 640) this keeps more bytes in
 //     flight than the register ring; with dense shapes of few items the register ring's
 //     finer split of K wins (both measured).
-// Codes become BF16 with one logic op per two weights: code | 0x4300 is the BF16 number
-// 128 + code.  With up to 16 token rows the MMA takes these biased values as they are and
+// Codes become BF16 with one shift and one logic op per two weights: code | 0x4300 is the
+// BF16 number 128 + code.  With up to 16 token rows the MMA takes these biased values as they are and
 // one extra MMA per step against an all-ones fragment yields the activation sums, so the
 // group sum is P - (128 + excess) * sum(a) in FP32 (no BF16 subtracts); with more rows the
 // bias is subtracted in BF16 (exact, small integers).  Per-group sums are scaled by the
