@@ -32,8 +32,11 @@
  *     their dependents early, so the GEMV starts after they complete).
  *   - Shape, pointer-alignment and size errors are detected on the host before any
  *     launch and returned as a qw_status; nothing is enqueued in that case.
- *   - Value errors found on the device (an INT4 code -8, an INT3 code -4, an E8M0 scale
- *     0xFF, an E4M3 NaN scale is not checked) and bounded waits that gave up are
+ *   - Value errors found on the device (while repacking: an INT4 code -8, an INT3 code
+ *     -4, an INT2 code -2, a zero point above 15, an E4M3 NaN code, an E8M0 scale 0xFF,
+ *     a negative or NaN NVFP4 scale, a non-finite second-level scale; a NaN router
+ *     logit; a non-finite input to the MXFP8 quantizer - the GEMMs take their operands
+ *     as valid) and bounded waits that gave up are
  *     reported through `d_err` (int32 in device memory, may be NULL): the first error
  *     code written wins (atomic compare-and-swap from 0).  The caller zeroes it and
  *     reads it when convenient, e.g. with qw_read_error.
@@ -179,9 +182,9 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  * symmetric INT without its minimum has the value set of a float with zero exponent
  * bits; the excess code used here is that value set shifted so that its bit pattern
  * drops straight into a BF16 mantissa (one logic op and one subtract per two weights).
- * Device-detected errors: INT4 -8, INT3 -4, E4M3 NaN (0x7F, 0xFF), E8M0 0xFF ->
- * QW_ERR_VALUE in *d_err (the
- * offending element is packed as 0).  Alignment: w_canon / s_canon 4-byte aligned
+ * Device-detected errors: INT4 -8, INT3 -4, INT2 -2, a zero point above 15, E4M3 NaN
+ * (0x7F, 0xFF), E8M0 0xFF, an NVFP4 scale with its sign bit set or NaN -> QW_ERR_VALUE in
+ * *d_err (an offending code is packed as 0, an offending E8M0 or NVFP4 scale as scale 1).  Alignment: w_canon / s_canon 4-byte aligned
  * (INT) or 1 (MXFP4); w_packed / s_packed 256-byte aligned.
  */
 qw_status qw_repack(const qw_packed_desc* desc, const void* w_canon, const void* s_canon,
