@@ -16,7 +16,10 @@
  * Formats: W4A16 = group-128 symmetric INT4 / INT3 weights with BF16 scales times BF16
  * activations; W4A8 = MXFP4 (E2M1 + group-32 E8M0) weights times MXFP8 (E4M3 + group-32
  * E8M0) activations (aireiter.com "vLLM Humming performance benchmark", section
- * "H100 group-32 W4A8").
+ * "H100 group-32 W4A8").  Also on the same kernels (announcement sections "WnA16" and
+ * "W8A8 / W4A8 / W4A4"): INT2, asymmetric INT4 and FP8 E4M3 weights times BF16; MXFP8
+ * times MXFP8; NVFP4 times NVFP4; and an optional FP32 second-level scale per output
+ * channel on any of them (QW_W_SCALE2).
  *
  * Conventions shared by every entry point
  *   - The caller owns every buffer.  Pointers are DEVICE pointers unless the comment
