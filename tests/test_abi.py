@@ -36,6 +36,26 @@ def test_library_exports_every_declared_symbol(Q):
     assert set(header_functions()) <= set(Q.EXPORTS)
 
 
+def test_binding_constants_and_descriptor_match_the_header(Q):
+    """The binding's enum values, the QW_W_SCALE2 flag and the descriptor struct (field
+    order and C types) are those include/qw.h declares."""
+    src = open(os.path.join(ROOT, "include", "qw.h")).read()
+    code = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    enums = dict((k, int(v)) for k, v in re.findall(r"\b(QW_[A-Z0-9_]+)\s*=\s*(\d+)", code))
+    assert len(enums) >= 8 + 8 + 3
+    for name, value in enums.items():
+        assert getattr(Q, name) == value, name
+    flag = re.search(r"#define\s+QW_W_SCALE2\s+(0x[0-9A-Fa-f]+)", code)
+    assert flag and Q.QW_W_SCALE2 == int(flag.group(1), 16)
+    body = re.search(r"typedef struct qw_packed_desc \{(.*?)\} qw_packed_desc;", code, re.S).group(1)
+    fields = []
+    for ctype, names in re.findall(r"(int32_t|uint64_t)\s+([^;]+);", body):
+        for n in names.split(","):
+            fields.append((n.strip(), ctypes.c_int32 if ctype == "int32_t" else ctypes.c_uint64))
+    assert [(n, t) for n, t in Q.PackedDesc._fields_] == fields
+    assert ctypes.sizeof(Q.PackedDesc) == 8 * 4 + 4 * 8
+
+
 def test_status_strings(Q):
     for s in range(8):
         assert Q.status_str(s)
