@@ -238,6 +238,14 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
  * tcgen05 block-scaled GEMM.
  * Alignment: A, C 16-byte aligned with K % 8 == 0 (BF16) or K % 16 == 0 (E4M3);
  * A_sf 4-byte aligned.  M >= 0 (M == 0 is a no-op).
+ * Ordering: the small-M kernels (W4A16 M <= 16, W4A8 M <= 8) start as programmatic
+ * dependents of the kernel before them on the stream and read w_packed and s_packed
+ * before waiting for it, so that their weight stream overlaps that kernel's tail.  The
+ * packed weights and scales must therefore not be written by the kernel enqueued directly
+ * before the call on the same stream.  qw_repack ends with an ordering point, so calling
+ * qgemm_dense right after it is safe; after a kernel of your own that writes the packed
+ * buffers, put a stream-ordered operation between (an event record/wait, a memcpy, or any
+ * other library call).  A, bias, C and the workspace are only touched after the wait.
  */
 qw_status qgemm_dense(const qw_packed_desc* desc, const void* w_packed, const void* s_packed,
                       int32_t afmt, const void* A, const void* A_sf, const void* bias,
@@ -270,8 +278,10 @@ qw_status qgemm_moe_route(const float* logits, int32_t T, int32_t E, int32_t top
  *   the library holds until the process exits; requests needing more scratch than that
  *   (ceil(T * topk / 256) * E * 4 bytes) are rejected with QW_ERR_WORKSPACE.  Nothing is
  *   allocated.  All calls share the array: calls that overlap on the GPU race and give
- *   undefined results.  The first call on each device looks up the array's device address
- *   (with that device current); make it before any stream capture.
+ *   undefined results.  `stream` must belong to the current device (a stream of another
+ *   device is rejected with QW_ERR_INVALID_ARG before anything is enqueued).  The first
+ *   call on each device looks up the array's device address (with that device current);
+ *   make it before any stream capture.
  */
 #define QW_NOALLOC_ROUTE_SCRATCH_BYTES (1u << 20)
 qw_status qgemm_moe_route_noalloc(const float* logits, int32_t T, int32_t E, int32_t topk,

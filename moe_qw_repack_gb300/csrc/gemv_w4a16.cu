@@ -307,6 +307,9 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
   const int g = lane >> 2, t = lane & 3;
   const uint32_t nblocks = (uint32_t)(p.N_pad / 16);
   const int G = p.K / 128;
+  // The tile queue is the previous kernel's output: with a queue, nothing (not even the
+  // item count) is read before the wait; dense calls prefetch weights before it.
+  if (p.queue) pdl_wait();
   // item counts stay below 2^31 (checked on the host): 32-bit index arithmetic
   const uint32_t n_items = p.queue ? (uint32_t)__ldg(p.queue) * nblocks
                                    : nblocks * (uint32_t)((p.M + 8 * MCH - 1) / (8 * MCH));
@@ -825,9 +828,13 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
   const uint32_t nblocks = (uint32_t)(p.N_pad / 16);
   const int G = p.K / 128;
   const int chunks = (G + kStageGroups - 1) / kStageGroups;  // stages per item
-  // item counts stay below 2^31 (checked on the host): 32-bit index arithmetic
-  const uint32_t n_items = p.queue ? (uint32_t)__ldg(p.queue) * nblocks
-                                   : nblocks * (uint32_t)((p.M + 8 * MCH - 1) / (8 * MCH));
+  // Work items.  The tile queue (and so its count) is the previous kernel's output: every
+  // role reads it only after its griddepcontrol.wait.  Item counts stay below 2^31
+  // (checked on the host): 32-bit index arithmetic.
+  auto count_items = [&]() -> uint32_t {
+    return p.queue ? (uint32_t)__ldg(p.queue) * nblocks
+                   : nblocks * (uint32_t)((p.M + 8 * MCH - 1) / (8 * MCH));
+  };
   volatile int* abort_flag = flags;
 
   if (warp == 0) {
@@ -837,6 +844,7 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
       tma_prefetch_desc(&tmS);
       // dense calls stream weights at once; the tile queue is the previous kernel's output
       if (p.queue) pdl_wait();
+      const uint32_t n_items = count_items();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_phase = 0;  // per stage: used, phase of its last copy
@@ -878,6 +886,7 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
     const int cw = warp - 1;
     const int g = lane >> 2, t = lane & 3;
     pdl_wait();  // activations, queue, bias and output
+    const uint32_t n_items = count_items();
     const uint32_t ring_base = smem_u32(ring);
     int stage = 0;
     uint32_t phase = 0;

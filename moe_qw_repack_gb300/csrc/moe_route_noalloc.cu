@@ -16,6 +16,8 @@
 //     needs to start at zero: each call overwrites every element it later reads.
 //     Calls that overlap on the GPU (on different streams, or from several threads
 //     without ordering) race on the array and give undefined results.
+//   - The stream must belong to the current device: the device address looked up below
+//     is that of the current device, so a stream of another device is rejected.
 //   - The first call on a device looks the array's device address up (with that device
 //     current) and caches it; make that first call before any stream capture.
 #include <cuda_runtime.h>
@@ -38,10 +40,14 @@ constexpr int kMaxDevices = 64;
 std::atomic<int32_t*> g_scratch_ptr[kMaxDevices];
 std::mutex g_setup_mutex;
 
-// Device address of g_route_scratch on the current device.
-qw_status scratch_for_current_device(int32_t** out) {
-  int dev = -1;
+// Device address of g_route_scratch on the current device, which must be the device of
+// `stream` (QW_ERR_INVALID_ARG otherwise: the kernels would run on the stream's device with
+// another device's address).
+qw_status scratch_for_stream(cudaStream_t stream, int32_t** out) {
+  int dev = -1, sdev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QW_ERR_CUDA;
+  if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return QW_ERR_INVALID_ARG;
+  if (sdev != dev) return QW_ERR_INVALID_ARG;
   int32_t* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
   if (p == nullptr) {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
@@ -71,7 +77,7 @@ extern "C" qw_status qgemm_moe_route_noalloc(const float* logits, int32_t T, int
   if (qw::moe_route_workspace(T, E, topk) > (uint64_t)QW_NOALLOC_ROUTE_SCRATCH_BYTES)
     return QW_ERR_WORKSPACE;
   int32_t* scratch = nullptr;
-  const qw_status s = scratch_for_current_device(&scratch);
+  const qw_status s = scratch_for_stream(static_cast<cudaStream_t>(stream), &scratch);
   if (s != QW_OK) return s;
   return qgemm_moe_route(logits, T, E, topk, topk_ids, sorted_pairs, expert_offsets, scratch,
                          (uint64_t)QW_NOALLOC_ROUTE_SCRATCH_BYTES, d_err, stream);

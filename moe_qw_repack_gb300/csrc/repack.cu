@@ -615,6 +615,13 @@ __global__ void unpack_nv_scales_kernel(const uint8_t* __restrict__ sp, uint8_t*
   }
 }
 
+// An empty kernel launched in plain stream order after the repack kernels.  The small-M
+// GEMVs are programmatic dependents of the kernel before them and read packed weights and
+// scales before their griddepcontrol.wait; with this kernel between, the kernel right
+// before a GEMV that directly follows qw_repack is this one, which began only after every
+// repack kernel had finished and its writes were visible.
+__global__ void stream_order_kernel() {}
+
 int grid_for(int64_t total, int threads) {
   int64_t b = (total + threads - 1) / threads;
   const int64_t cap = (int64_t)device_sm_count() * 32;
@@ -716,6 +723,7 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
         (const uint16_t*)s_canon, (uint16_t*)s_packed, d.E, d.N, d.N_pad, d.K / 128,
         (int64_t)(d.s_expert_stride / 2));
   }
+  stream_order_kernel<<<1, 32, 0, st>>>();
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 

@@ -215,3 +215,45 @@ def test_grouped_rejects_bad_device_offsets(bad):
     Q.qgemm_moe_grouped(d, wp, sp_, Q.QW_A_BF16, A, None, off, P, None, C, ws, wsn, err)
     assert Q.qw_read_error(err) == Q.QW_ERR_INVALID_ARG
     assert float((torch.ones(2, device="cuda") * 3).sum()) == 6.0  # context still usable
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_grouped_gemv_reads_the_tile_queue_of_this_call(T):
+    """The grouped GEMV starts as a programmatic dependent of the kernel that builds its
+    tile queue in the workspace: it must read the queue (its tile count included) only
+    after waiting for that kernel.  The workspace is zeroed before every call (a stale
+    count of 0 would schedule no tile) and C is filled with NaN, so a row the kernel never
+    wrote shows up; every row must match the oracle on each of several calls."""
+    Q = qw()
+    E, K, N, topk = 128, 4096, 1280, 8
+    w = _weights("int", E, N, K, 4, 4)
+    a = synth.w4a16_problem(T, 16, K, cfg_id=1004)
+    logits = synth.router_logits(T, E, cfg_id=4)
+    d, wp, sp_ = repack(Q.QW_W_INT4_G128_BF16, E, N, K, w["w_canon"], w["s_canon"])
+    P = T * topk
+    ids = torch.empty((T, topk), dtype=torch.int32, device="cuda")
+    sp = torch.empty((P,), dtype=torch.int32, device="cuda")
+    off = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
+    n = Q.qgemm_moe_route_workspace_size(T, E, topk)
+    rws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    A = dev(a["A"].view(np.int16))
+    As = torch.empty((P, K), dtype=torch.int16, device="cuda")
+    wsn = Q.qgemm_workspace_size(d, Q.QW_A_BF16, P)
+    ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
+    C = torch.empty((P, N), dtype=torch.int16, device="cuda")
+    err = Q.new_error_flag()
+    _, _, roff, rsp = OM.route(logits, topk)
+    R, S = OM.grouped_w4a16(a["A"][rsp // topk], roff, OF.unpack_int4(w["w_canon"], K),
+                            w["s_canon"])
+    lg = dev(logits)
+    for _ in range(4):
+        ws.zero_()
+        C.fill_(0x7FC0)  # BF16 NaN
+        Q.qgemm_moe_route(lg, T, E, topk, ids, sp, off, rws, n)
+        Q.qgemm_moe_permute(Q.QW_A_BF16, A, None, K, sp, P, topk, As, None)
+        Q.qgemm_moe_grouped(d, wp, sp_, Q.QW_A_BF16, As, None, off, P, None, C, ws, wsn, err)
+        assert Q.qw_read_error(err) == 0
+        got = u16_view(C)
+        assert not np.any(got == 0x7FC0), "rows left unwritten"
+        ok, ratio, frob = OQ.check_bf16_result(got, R, S)
+        assert ok, (ratio, frob)

@@ -67,3 +67,23 @@ def test_noalloc_route_rejects_requests_beyond_its_scratch():
     fake = 1 << 20  # never dereferenced
     status = Q.LIB.qgemm_moe_route_noalloc(fake, T, E, k, fake, fake, fake, None, None)
     assert status == Q.QW_ERR_WORKSPACE
+
+
+@pytest.mark.gpu
+def test_noalloc_route_matches_the_oracle():
+    """The routing the no-alloc entry point returns is the oracle's, bit for bit (heavy
+    ties included), on consecutive calls that reuse the shared scratch."""
+    import numpy as np
+    from oracle import moe as OM
+    Q = _lib()
+    rng = np.random.default_rng(17)
+    cases = [(synth.router_logits(16, 128, cfg_id=4), 8),
+             (rng.integers(-2, 3, (300, 40)).astype(np.float32), 6),
+             (synth.router_logits(2048, 128, cfg_id=5), 8)]
+    for logits, k in cases:
+        T, E = logits.shape
+        got = _route_noalloc_c_abi(Q, torch.from_numpy(logits).cuda(), T, E, k)
+        rids, _, roff, rsp = OM.route(logits, k)
+        assert np.array_equal(got[0].numpy(), rids)
+        assert np.array_equal(got[1].numpy(), rsp)
+        assert np.array_equal(got[2].numpy(), roff)
