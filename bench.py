@@ -170,13 +170,87 @@ class W4A8Problem:
         Q.qgemm_dense(self.desc, wp, sp, Q.QW_A_MXFP8_G32, A, Asf, None, self.C, self.M, None, 0,
                       self.err)
 
-    def run_e2e(self, i=0):
-        """Pinned host activations in, GEMM, BF16 result back to pinned host memory."""
-        wp, sp, A, Asf = self.copies[i % len(self.copies)]
+    # end to end, two slots: slot k holds one step's activations and results on the device
+    def _slot(self, k):
+        if not hasattr(self, "_slots"):
+            self._slots = []
+            for j in range(2):
+                A, Asf = self.copies[j % len(self.copies)][2:]
+                if j >= len(self.copies):
+                    A, Asf = A.clone(), Asf.clone()
+                C = self.C if j == 0 else torch.empty_like(self.C)
+                Ch = self.C_host if j == 0 else torch.empty_like(self.C_host).pin_memory()
+                self._slots.append((A, Asf, C, Ch))
+        return self._slots[k]
+
+    def load_slot(self, k):
+        """Pinned host activations and scales -> slot k (on the current stream)."""
+        A, Asf, _, _ = self._slot(k)
         A.copy_(self.A_host, non_blocking=True)
         Asf.copy_(self.Asf_host, non_blocking=True)
-        self.run(i)
-        self.C_host.copy_(self.C, non_blocking=True)
+
+    def run_slot(self, k, i):
+        """The GEMM on slot k's activations with weight copy i (public call)."""
+        Q = self.Q
+        A, Asf, C, _ = self._slot(k)
+        wp, sp = self.copies[i % len(self.copies)][:2]
+        Q.qgemm_dense(self.desc, wp, sp, Q.QW_A_MXFP8_G32, A, Asf, None, C, self.M, None, 0,
+                      self.err)
+
+    def store_slot(self, k):
+        """Slot k's BF16 result -> pinned host memory (on the current stream)."""
+        _, _, C, Ch = self._slot(k)
+        Ch.copy_(C, non_blocking=True)
+
+
+def time_e2e_pipelined(probs, steps, warmup, world):
+    """End-to-end time per step through the public call: every step copies its activations
+    in from pinned host memory and its results out to pinned host memory.  Copies in run on
+    one stream, the GEMMs on the current stream and copies out on a third, over two device
+    slots, so a step's copies overlap the GEMMs of its neighbours (events order each slot's
+    reuse).  Returns (ms per step, steps timed)."""
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    gemm_done = [torch.cuda.Event(), torch.cuda.Event()]
+    out_done = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def step(i):
+        k = i % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(gemm_done[k])  # the GEMMs two steps back are done with slot k
+            for pr in probs:
+                pr.load_slot(k)
+            in_ready[k].record(s_in)
+        comp.wait_event(in_ready[k])
+        comp.wait_event(out_done[k])  # slot k's previous results have left the device
+        for pr in probs:
+            pr.run_slot(k, i)
+        gemm_done[k].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(gemm_done[k])
+            for pr in probs:
+                pr.store_slot(k)
+            out_done[k].record(s_out)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    s_in.wait_event(a)
+    s_out.wait_event(a)
+    for i in range(steps):
+        step(warmup + i)
+    comp.wait_stream(s_in)
+    comp.wait_stream(s_out)
+    b.record(comp)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return max_over_ranks(a.elapsed_time(b) / steps, world), steps
 
 
 def l2_bytes():
@@ -268,9 +342,32 @@ def extra_w4a16(steps, warmup, world, only=None):
                      "hbm_frac": round(gbs / peaks["hbm_gbs"], 3),
                      "tflops": round(2 * M * N * K / (ms * 1e-3) / 1e12, 3),
                      "launches": n, "weight_copies": R, "graph": graph}
+        if M == 1:
+            out[name].update(stream_read_reference(copies, steps, warmup, world, wbytes, peaks))
         del copies
         torch.cuda.empty_cache()
     return out
+
+
+def stream_read_reference(copies, steps, warmup, world, nbytes, peaks):
+    """A plain streaming read of the same packed weights (qw_stream_read), timed like the
+    GEMV: a CUDA graph of back-to-back launches over the same copies.  'plain' launches in
+    stream order; 'chained' as programmatic dependents with every load before the wait (the
+    overlap a kernel that needs nothing from its predecessor can have; a GEMV must wait for
+    its activations)."""
+    import moe_qw_repack_gb300.qw as Q
+    sink = torch.zeros(Q.QW_STREAM_READ_SINK_WORDS, dtype=torch.int32, device="cuda")
+    res = {}
+    for chained in (False, True):
+        def rd(i, chained=chained):
+            w, _ = copies[i % len(copies)]
+            Q.qw_stream_read(w, w.numel(), sink, chained)
+        ms, _, _ = time_region([rd], max(steps, len(copies)), warmup, world,
+                               graph_steps=len(copies))
+        wb = copies[0][0].numel()
+        key = "stream_read_chained_frac" if chained else "stream_read_frac"
+        res[key] = round(wb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)
+    return res
 
 
 def extra_fp8w(steps, warmup, world, only=None):
@@ -573,10 +670,7 @@ def run_ours(args, world, rank):
             traffic = None
 
     # end to end: pinned host activations -> device, both GEMMs, results -> pinned host
-    def e2e_step(i):
-        for pr in probs:
-            pr.run_e2e(i)
-    e_ms, e_n, _ = time_region([e2e_step], max(3, args.steps // 2), 2, world)
+    e_ms, e_n = time_e2e_pipelined(probs, max(3, args.steps), 2, world)
     h2d = sum(pr.A_host.numel() + pr.Asf_host.numel() for pr in probs)
     d2h = sum(pr.C.numel() * 2 for pr in probs)
 
@@ -594,11 +688,18 @@ def run_ours(args, world, rank):
                    "per_gemm_ms": [round(t, 4) for t in per_gemm],
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(whole_job_tflops(F, world, e_ms), 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "how": "qgemm_dense per step with its activations copied in from pinned host "
+                       "memory and its BF16 results copied out to pinned host memory; copies in, "
+                       "GEMMs and copies out on three streams over two device slots",
+                "steps": e_n},
         "gpu_launches": len(fns) * n,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(achieved / fp8_peak, 4), "traffic": traffic,
+                     "traffic_note": "DRAM read + write bytes per step from one ncu capture; "
+                                     "writes of C still dirty in L2 when a launch ends are not "
+                                     "in it, so it reads below the algorithmic bytes",
                      "peak_source": f"{peak_src} bf16 burst x 2 (FP8 / BF16 nominal)"},
         "clocks": clk.summary(),
         "wall_s_timed_loop": round(wall, 3),
@@ -614,7 +715,35 @@ def run_ours(args, world, rank):
         line["extra"].update(extra_moe(max(5, min(args.steps, 40)), 3, world))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+    line["summary"] = summarize(line)  # last key: every configured workload's fraction
     return line
+
+
+def summarize(line):
+    """One compact entry per configured workload (fraction of its roofline), in the order
+    of the workload list, so that the end of the printed line carries all of them."""
+    ex = line.get("extra", {})
+    sm = {"cfg2_w4a8_frac_fp8": line["roofline"]["frac"],
+          "e2e_over_device": round(line["e2e"]["value"] / line["value"], 3)}
+
+    def get(name, key):
+        v = ex.get(name, {}).get(key)
+        return v if v is not None else None
+    sm["cfg1_m8_frac_hbm"] = get("cfg1_w4a16_m8_2048x2048_int4", "hbm_frac")
+    for bits in (4, 3):
+        sm[f"cfg3_int{bits}_frac_hbm"] = [get(f"cfg3_m1_{n}x{k}_int{bits}", "hbm_frac")
+                                          for n, k in ((14336, 4096), (4096, 14336), (4096, 4096))]
+    sm["cfg3_stream_read_frac"] = [get(f"cfg3_m1_{n}x{k}_int4", "stream_read_frac")
+                                   for n, k in ((14336, 4096), (4096, 14336), (4096, 4096))]
+    sm["cfg3_stream_read_chained_frac"] = [get(f"cfg3_m1_{n}x{k}_int4", "stream_read_chained_frac")
+                                           for n, k in ((14336, 4096), (4096, 14336), (4096, 4096))]
+    sm["cfg4_gemm_frac_fp8"] = get("cfg4_moe_w4a8_E256_T4096", "gemm_frac_fp8_peak")
+    sm["cfg5_weight_frac_hbm"] = {t: get(f"cfg5_moe_w4a16_E128_T{t}", "weight_frac_hbm")
+                                  for t in (1, 16, 256)}
+    sm["cfg5_tflops"] = {t: get(f"cfg5_moe_w4a16_E128_T{t}", "gemm_tflops") for t in (2048, 8192)}
+    sm["cfg5_us_step"] = {t: get(f"cfg5_moe_w4a16_E128_T{t}", "us_total")
+                          for t in (1, 16, 256, 2048, 8192)}
+    return sm
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -623,7 +752,10 @@ def _oracle_inputs(M, N, K):
     return synth.w4a8_problem(M, N, K, cfg_id=1)
 
 
-def cpu_baseline(rows_b=4096, min_seconds=10.0, rows_a=None):
+CPU_SAMPLE_ROWS_B = 4096  # rows of (4096,14336,4096) in the oracle's timed sample
+
+
+def cpu_baseline(rows_b=CPU_SAMPLE_ROWS_B, min_seconds=10.0, rows_a=None):
     """Time the float64 oracle on a bounded sample: the first `rows_a` rows (default all) of
     (4096,3072,4096) plus the first `rows_b` rows of (4096,14336,4096) (rows_b = 0: none),
     repeated until at least `min_seconds` of CPU work."""
@@ -662,10 +794,17 @@ def run_reference(args, world, rank):
     # each step is a bounded sample sized so that the whole run stays within a few minutes:
     # a few steps take a large sample, many steps a row subset of the smaller shape (each
     # call decodes that shape's weights, ~0.3 s on these hosts)
-    if args.steps <= 5:
-        kw = dict(rows_b=1024, min_seconds=0.0)
+    # One step is one repetition of the cpu_baseline leg's sample (the same shapes and rows,
+    # so the two report the same rate), about 3 s on these hosts; past 40 steps the
+    # sample keeps its shapes with proportionally fewer rows so the run stays short.
+    if args.oracle_rows:
+        kw = dict(rows_b=args.oracle_rows, min_seconds=0.0, rows_a=args.oracle_rows)
+    elif args.steps <= 40:
+        kw = dict(rows_b=CPU_SAMPLE_ROWS_B, min_seconds=0.0)
     else:
-        kw = dict(rows_b=0, min_seconds=0.0, rows_a=max(32, min(4096, 2048 * 5 // args.steps)))
+        f = 40.0 / args.steps
+        kw = dict(rows_b=max(64, int(CPU_SAMPLE_ROWS_B * f)), min_seconds=0.0,
+                  rows_a=max(64, int(4096 * f)))
     t0 = time.perf_counter()
     for _ in range(args.steps):
         cb = cpu_baseline(**kw)
@@ -699,6 +838,9 @@ def main():
     ap.add_argument("--case", default=None,
                     help="with --only-w4a16 / --only-moe / --only-fp8w: run only the cases "
                          "whose name contains this string")
+    ap.add_argument("--oracle-rows", type=int, default=0,
+                    help="with --impl reference: rows of each shape in a step's oracle sample "
+                         "(default: the cpu_baseline leg's sample)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     if args.impl == "reference":

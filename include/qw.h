@@ -390,6 +390,22 @@ qw_status qw_read_error(const int32_t* d_err, void* stream, int32_t* host_code);
  */
 qw_status qw_test_wait_timeout(int32_t* d_err, int64_t limit_ns, void* stream);
 
+/* --------------------------------------------------------------------------------------
+ * qw_stream_read - diagnostics: the reference point of the HBM-bound kernels.  Reads
+ * `bytes` of device memory at `src` once with 16-byte loads from a full grid (eight CTAs
+ * of 256 threads per SM) and writes one fold word per CTA to `sink` (device uint32,
+ * QW_STREAM_READ_SINK_WORDS of them).  `chained` = 1 launches it as a programmatic
+ * dependent of the previous kernel with every load before its griddepcontrol.wait (only
+ * the sink write waits), the overlap a kernel that needs nothing from its predecessor can
+ * have; 0 launches it in plain stream order.  The pages measure decode kernels as a
+ * fraction of memory bandwidth (aireiter.com, "SM80 single-request decode: do not infer
+ * Ampere gains"); this is the read such a fraction is compared with on this GPU.
+ * Requires src 16-byte aligned and bytes % 16 == 0 (QW_ERR_ALIGNMENT otherwise).
+ */
+#define QW_STREAM_READ_SINK_WORDS 4096
+qw_status qw_stream_read(const void* src, uint64_t bytes, uint32_t* sink, int32_t chained,
+                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif

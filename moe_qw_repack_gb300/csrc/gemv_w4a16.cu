@@ -737,6 +737,311 @@ qw_status launch_m8_variant(const M8Params& p, cudaStream_t st) {
   return launch_pdl(kern, (unsigned)grid, kM8Warps * 32, smem, st, p);
 }
 
+// ---------------------------------------------------------------- single-token decode, INT4
+// M = 1 over symmetric INT4 weights: the same packed words and (16-row block, scale group)
+// work as gemv_m8_kernel, rebuilt around fewer issued instructions per 1 KiB group.
+//  - FP16 operands.  With the FP16 pattern 0x6400 (the number 1024, unit in the last place
+//    1) one masking op turns the nibbles at bits 0-3 and 16-19 of a word into 1024 + u and
+//    the nibbles at bits 4-7 and 20-23, left in place, into 1024 + 16 u: one shift per four
+//    fragment registers instead of three.  In the packed words the in-place nibbles are
+//    exactly the registers of rows g + 8, so rows g hold 1032 + q and rows g + 8 hold
+//    16 (72 + q) (u = q + 8): the two halves of a block differ by a row factor that goes
+//    out with the excess after the MMA.
+//  - Activations are staged once per CTA as FP16, each scale group multiplied by the power
+//    of two 2^f that puts its largest magnitude in [2^14, 2^15).  That is exact (a BF16
+//    value times a power of two is an FP16 number) except for values 2^28 or more below the
+//    group maximum, which round to FP16 subnormals.  Beside each group sit its constants
+//    (2^-f, 2^-f / 16, -1032 * 2^-f * S, -72 * 2^-f * S), S the sum of its FP16 values,
+//    so that per group two FMAs remove the excess and two apply the weight scales:
+//      sum_k q a = 2^-f (P_g - 1032 S)   (rows g),   2^-f (P_g+8 / 16 - 72 S)   (rows g + 8).
+//  - Only token 0 exists: the lanes with t = 0 carry the outputs (fragment registers 0 and
+//    2); the other columns of the MMA are never read.
+// A CTA's warps split the scale groups of a block (gpw groups each, a whole number of ring
+// batches) and meet in shared memory once per block; CTAs take blocks round-robin.  Each
+// thread may use 128 registers: measured on GB300 (14336 x 4096), the schedule the compiler
+// builds with that budget streams 1.25x faster than the same code held to 64 or 80 registers
+// (which would let more CTAs share an SM), and splitting a block's K over several CTAs (slice
+// sums in the workspace, last arrival adds them) was slower at every shape tried.
+constexpr int kDecRing = 4;                 // groups per warp in flight (register ring)
+constexpr int kDecMaxWarps = 16;            // 512 threads x 128 registers fill an SM
+constexpr int kDecMaxGpw = 16;              // groups per warp the staging is sized for
+constexpr size_t kDecMaxSmem = 100 * 1024;  // largest staging sent to the decode kernel
+
+struct DecParams {
+  const uint8_t* wp;
+  const uint16_t* sp;
+  const uint16_t* A;
+  const uint16_t* bias;
+  const float* scale2;  // second-level scales [N_pad] or null
+  uint16_t* C;
+  int32_t N, N_pad, K;
+  int32_t gpw;          // scale groups per warp (a multiple of kDecRing, at most kDecMaxGpw)
+};
+
+// shared memory: FP16 activations [group][step pair][t][16 B] and the group constants
+// (float4), then the reduction [2][warp][16] floats
+__host__ __device__ constexpr size_t dec_smem_bytes(int groups, int warps) {
+  return (size_t)groups * (256 + 16) + 2 * (size_t)warps * 16 * 4;
+}
+
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int R>
+__global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const DecParams p) {
+  extern __shared__ uint4 dec_smem[];
+  const int warps = (int)(blockDim.x >> 5);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = p.K >> 7;
+  const uint32_t nblocks = (uint32_t)(p.N_pad >> 4);
+  const uint32_t my_items = blockIdx.x < nblocks ? (nblocks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int wg0 = warp * p.gpw;                 // the warp's first group
+  const uint32_t gstride = nblocks * 1024u;     // bytes between groups of a block
+  uint8_t* act = reinterpret_cast<uint8_t*>(dec_smem);           // [G][4][4][16 B]
+  float4* gconst = reinterpret_cast<float4*>(act + (size_t)G * 256);
+  float* red = reinterpret_cast<float*>(gconst + G);              // [2][warps][16]
+
+  pdl_launch_dependents();
+
+  // ---- register ring: the packed words and scales of R consecutive groups of an item
+  uint32_t wb[R][8];
+  uint32_t sl_[R], sh_[R];  // BF16 scale bits of rows g and g + 8
+  // byte offset of (item it, the warp's first group) for this lane, and its scale index
+  auto unit_w = [&](uint32_t it) {
+    return (blockIdx.x + it * gridDim.x) * 1024u + (uint32_t)wg0 * gstride + (uint32_t)lane * 32u;
+  };
+  auto unit_s = [&](uint32_t it) {
+    return (uint32_t)wg0 * (uint32_t)p.N_pad + (blockIdx.x + it * gridDim.x) * 16u + (uint32_t)g;
+  };
+  auto load = [&](int r, uint32_t woff, uint32_t soff) {
+    const uint4 v0 = __ldcs(reinterpret_cast<const uint4*>(p.wp + woff));
+    const uint4 v1 = __ldcs(reinterpret_cast<const uint4*>(p.wp + woff) + 1);
+    wb[r][0] = v0.x; wb[r][1] = v0.y; wb[r][2] = v0.z; wb[r][3] = v0.w;
+    wb[r][4] = v1.x; wb[r][5] = v1.y; wb[r][6] = v1.z; wb[r][7] = v1.w;
+    sl_[r] = __ldg(p.sp + soff);
+    sh_[r] = __ldg(p.sp + soff + 8);
+  };
+  // weights and scales are never written by the kernel before this one on the stream (a
+  // documented precondition): the first batch streams before the wait
+  if (my_items > 0) {
+    const uint32_t w0 = unit_w(0), s0 = unit_s(0);
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      load(r, w0 + (uint32_t)r * gstride, s0 + (uint32_t)r * (uint32_t)p.N_pad);
+  }
+
+  // ---- activations of the warp's groups, as FP16 B fragments, and their constants.  A
+  // half warp covers one group; up to four chunks per lane load before any is converted.
+  pdl_wait();
+  {
+    constexpr int kBatch = 4;
+    const int nchunk = p.gpw * 16;         // 16-byte chunks (8 BF16) of the warp's groups
+    const int iters = (nchunk + 31) >> 5;  // per lane
+    for (int u0 = 0; u0 < iters; u0 += kBatch) {
+      uint4 v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (u0 + u < iters) {
+          const int q = lane + 32 * (u0 + u);
+          const int gl = wg0 + (q >> 4), c = q & 15;  // group, chunk
+          v[u] = q < nchunk ? __ldg(reinterpret_cast<const uint4*>(p.A + gl * 128 + c * 8))
+                            : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (u0 + u < iters) {
+          const int q = lane + 32 * (u0 + u);
+          const int gl = wg0 + (q >> 4), c = q & 15;
+          // group maximum magnitude: BF16 magnitudes order like their bit patterns
+          uint32_t m = __vmaxu2(__vmaxu2(v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu),
+                                __vmaxu2(v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu));
+          m = max(m & 0xFFFFu, m >> 16);
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+          const int ex = (int)(m >> 7);      // biased exponent of the maximum
+          const int f = min(141 - ex, 126);  // 2^f puts the maximum in [2^14, 2^15)
+          const float up = __uint_as_float((uint32_t)(127 + f) << 23);
+          const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          uint32_t h[4];
+          float sum = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            h[i] = f16x2_of(__uint_as_float(w4[i] << 16) * up,
+                            __uint_as_float(w4[i] & 0xFFFF0000u) * up);
+            const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+            sum += back.x + back.y;
+          }
+          // chunk c holds k = 8c .. 8c + 7: step c / 2, lanes t = 2 (c & 1) and 2 (c & 1) + 1
+          if (q < nchunk) {
+            uint8_t* dst = act + ((gl * 4 + (c >> 2)) * 4 + 2 * (c & 1)) * 16 + ((c >> 1) & 1) * 8;
+            *reinterpret_cast<uint2*>(dst) = make_uint2(h[0], h[1]);
+            *reinterpret_cast<uint2*>(dst + 16) = make_uint2(h[2], h[3]);
+          }
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+          if ((lane & 15) == 0 && q < nchunk) {
+            const float e = __uint_as_float((uint32_t)(127 - f) << 23);  // 2^-f
+            gconst[gl] = make_float4(e, e * 0.0625f, -1032.f * e * sum, -72.f * e * sum);
+          }
+        }
+    }
+  }
+  __syncwarp();
+
+  const uint32_t act_lane = smem_u32(act) + (uint32_t)(wg0 * 256 + t * 16);
+  const uint32_t const_base = smem_u32(gconst) + (uint32_t)wg0 * 16;
+  for (uint32_t it = 0; it < my_items; ++it) {
+    const uint32_t nb = blockIdx.x + it * gridDim.x;
+    const uint32_t wit = unit_w(it), sit = unit_s(it);
+    const uint32_t wnx = unit_w(it + 1), snx = unit_s(it + 1);
+    const bool has_next = it + 1 < my_items;
+    float acc_lo = 0.f, acc_hi = 0.f;
+    for (int jb = 0; jb < p.gpw; jb += R) {
+      // the ring's next batch: (it, jb + R ..) or the next item's first R groups
+      const bool same = jb + R < p.gpw;
+      const uint32_t nw = same ? wit + (uint32_t)(jb + R) * gstride : wnx;
+      const uint32_t ns = same ? sit + (uint32_t)(jb + R) * (uint32_t)p.N_pad : snx;
+      const bool more = same || has_next;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int j = jb + r;
+        const uint32_t ab = act_lane + (uint32_t)j * 256u;
+        float pr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const uint4 x = lds128(ab + jj * 64);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const uint32_t wv = wb[r][2 * jj + h2];
+            const uint32_t ws = wv >> 8;
+            uint32_t a[4];
+            a[0] = and_or(wv, 0x000F000Fu, 0x64006400u);
+            a[1] = and_or(wv, 0x00F000F0u, 0x64006400u);
+            a[2] = and_or(ws, 0x000F000Fu, 0x64006400u);
+            a[3] = and_or(ws, 0x00F000F0u, 0x64006400u);
+            mma_f16_16816(pr, a, h2 ? x.z : x.x, h2 ? x.w : x.y);
+          }
+        }
+        float4 c4;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(c4.x), "=f"(c4.y), "=f"(c4.z), "=f"(c4.w)
+                     : "r"(const_base + (uint32_t)j * 16u));
+        const float s_lo = __uint_as_float(sl_[r] << 16);
+        const float s_hi = __uint_as_float(sh_[r] << 16);
+        acc_lo = fmaf(s_lo, fmaf(pr[0], c4.x, c4.z), acc_lo);
+        acc_hi = fmaf(s_hi, fmaf(pr[2], c4.y, c4.w), acc_hi);
+        // the slot is free: load the ring's next group into it
+        if (more) load(r, nw + (uint32_t)r * gstride, ns + (uint32_t)r * (uint32_t)p.N_pad);
+      }
+    }
+
+    // ---- the CTA's warps meet: fixed-order sum of their 16 rows; one barrier per item
+    float* rb = red + (it & 1) * (warps * 16);
+    if (t == 0) {
+      rb[warp * 16 + g] = acc_lo;
+      rb[warp * 16 + g + 8] = acc_hi;
+    }
+    __syncthreads();
+    if (warp == 0 && lane < 16) {
+      float v = 0.f;
+      for (int w2 = 0; w2 < warps; ++w2) v += rb[w2 * 16 + lane];
+      const int n = (int)nb * 16 + lane;
+      if (n < p.N) {
+        if (p.scale2) v *= __ldg(p.scale2 + n);
+        if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + n) << 16);
+        __nv_bfloat16 hb = __float2bfloat16_rn(v);
+        p.C[n] = *reinterpret_cast<uint16_t*>(&hb);
+      }
+    }
+  }
+}
+
+// How a decode call is split: warps per CTA (each streaming gpw groups of every block the
+// CTA takes) and resident CTAs per SM.
+struct DecPlan {
+  int warps = 0, gpw = 0, per_sm = 0;  // warps == 0: no plan (the shape goes to gemv_m8_kernel)
+};
+
+// The split with the most warps per SM (16 at 128 registers each), ties to more warps per
+// CTA (fewer blocks per SM to wait on); measured best at K = 4096 (8 warps x 4 groups, two
+// CTAs per SM) and K = 14336 (14 warps x 8 groups, one CTA per SM).
+DecPlan decode_plan(int K) {
+  DecPlan best;
+  const int G = K / 128;
+  for (int warps = 1; warps <= kDecMaxWarps; ++warps) {
+    if (G % warps) continue;
+    const int gpw = G / warps;
+    if (gpw % kDecRing || gpw > kDecMaxGpw) continue;
+    if (dec_smem_bytes(G, warps) > kDecMaxSmem) continue;
+    const int per_sm = kDecMaxWarps / warps;
+    const int score = warps * per_sm;
+    if (best.warps == 0 || score > best.warps * best.per_sm ||
+        (score == best.warps * best.per_sm && warps > best.warps)) {
+      best.warps = warps;
+      best.gpw = gpw;
+      best.per_sm = per_sm;
+    }
+  }
+  return best;
+}
+
+qw_status launch_decode(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                        const void* A, const void* bias, const float* scale2, void* C,
+                        cudaStream_t st) {
+  const DecPlan pl = decode_plan(d.K);
+  if (pl.warps == 0) return QW_ERR_UNSUPPORTED;
+  DecParams p{};
+  p.wp = static_cast<const uint8_t*>(w_packed);
+  p.sp = static_cast<const uint16_t*>(s_packed);
+  p.A = static_cast<const uint16_t*>(A);
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.scale2 = scale2;
+  p.C = static_cast<uint16_t*>(C);
+  p.N = d.N;
+  p.N_pad = d.N_pad;
+  p.K = d.K;
+  p.gpw = pl.gpw;
+  auto kern = gemv_decode_kernel<kDecRing>;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecMaxSmem);
+  if (attr != cudaSuccess) return QW_ERR_CUDA;
+  const size_t smem = dec_smem_bytes(d.K / 128, pl.warps);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, pl.warps * 32, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  if (per_sm > pl.per_sm) per_sm = pl.per_sm;
+  const int64_t items = d.N_pad / 16;
+  int64_t grid = (int64_t)device_sm_count() * per_sm;
+  if (grid > items) grid = items;
+  if (grid < 1) grid = 1;
+  return launch_pdl(kern, (unsigned)grid, pl.warps * 32, smem, st, p);
+}
+
+// Dense single-token INT4 calls the decode kernel takes (32-bit offsets into the packed
+// buffers; a split with a whole number of ring batches per warp).
+bool decode_eligible(const qw_packed_desc& d, const void* A) {
+  if (d.wfmt != QW_W_INT4_G128_BF16) return false;
+  if ((reinterpret_cast<uintptr_t>(A) & 15) != 0) return false;
+  if (d.w_expert_stride >= (uint64_t(1) << 32)) return false;
+  if ((uint64_t)(d.K / 128) * (uint64_t)d.N_pad >= (uint64_t(1) << 31)) return false;
+  return decode_plan(d.K).warps != 0;
+}
+
 // ---------------------------------------------------------------- TMA-ring kernel
 constexpr int kStageGroups = 8;  // scale groups per stage (one TMA copy)
 
@@ -1174,6 +1479,9 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
                             void* ws, uint64_t ws_bytes, int32_t* err, cudaStream_t st) {
   const bool grouped = rs.offsets != nullptr;
   const int mch = mch_for(d, rs.rows, grouped);
+  // single-token decode, symmetric INT4: the FP16-operand decode kernel
+  if (!grouped && rs.rows == 1 && decode_eligible(d, A))
+    return launch_decode(d, w_packed, s_packed, A, bias, rs.scale2, C, st);
   // single-token decode over a large matrix: the staged kernel (its staging pays off once a
   // warp streams many groups; measured slower on matrices of 16 M weights and below)
   if (!grouped && rs.rows == 1 && (int64_t)d.N * d.K >= kM8MinWeights &&

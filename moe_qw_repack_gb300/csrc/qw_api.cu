@@ -437,4 +437,11 @@ qw_status qw_test_wait_timeout(int32_t* d_err, int64_t limit_ns, void* stream) {
   return launch_wait_timeout_probe(d_err, limit_ns, static_cast<cudaStream_t>(stream));
 }
 
+qw_status qw_stream_read(const void* src, uint64_t bytes, uint32_t* sink, int32_t chained,
+                         void* stream) {
+  if (!sink || (bytes > 0 && !src)) return QW_ERR_INVALID_ARG;
+  if (!aligned(src, 16) || bytes % 16 || !aligned(sink, 4)) return QW_ERR_ALIGNMENT;
+  return launch_stream_read(src, bytes, sink, chained != 0, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -115,5 +115,8 @@ qw_status launch_build_tile_queue(const int32_t* offsets, int32_t E, int32_t til
                                   int32_t* err, cudaStream_t st);
 
 qw_status launch_wait_timeout_probe(int32_t* err, int64_t limit_ns, cudaStream_t st);
+// Diagnostics: a plain streaming read of `bytes` at `src` (one fold word per CTA to `sink`).
+qw_status launch_stream_read(const void* src, uint64_t bytes, uint32_t* sink, bool chained,
+                             cudaStream_t st);
 
 }  // namespace qw

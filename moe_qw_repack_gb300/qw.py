@@ -44,7 +44,7 @@ EXPORTS = (
     "qgemm_moe_permute", "qgemm_moe_grouped", "qgemm_moe_grouped_indexed", "qw_read_error",
     "qw_test_wait_timeout",
     "qgemm_moe_route_noalloc", "qw_quantize_mxfp8", "qw_silu_mul",
-    "qgemm_moe_combine_workspace_size", "qgemm_moe_combine",
+    "qgemm_moe_combine_workspace_size", "qgemm_moe_combine", "qw_stream_read",
 )
 
 
@@ -93,6 +93,7 @@ _SIGS = {
     "qw_silu_mul": (_I32, [_P, _I64, _I32, _P, _P]),
     "qgemm_moe_combine_workspace_size": (_I32, [_I32, _I32, ctypes.POINTER(_U64)]),
     "qgemm_moe_combine": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _U64, _P, _P]),
+    "qw_stream_read": (_I32, [_P, _U64, _P, _I32, _P]),
 }
 
 
@@ -271,6 +272,14 @@ def qw_read_error(d_err, stream=None) -> int:
 def qw_test_wait_timeout(d_err, limit_ns: int, stream=None):
     _check("qw_test_wait_timeout", LIB.qw_test_wait_timeout(_ptr(d_err), limit_ns,
                                                             _stream(stream)))
+
+
+QW_STREAM_READ_SINK_WORDS = 4096
+
+
+def qw_stream_read(src, nbytes: int, sink, chained: bool = False, stream=None):
+    _check("qw_stream_read", LIB.qw_stream_read(_ptr(src), nbytes, _ptr(sink), int(chained),
+                                                _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- conveniences

@@ -228,3 +228,15 @@ def test_scale2_flag_sizes_and_host_validation(Q):
         with pytest.raises(Q.QwError) as e:
             call()
         assert e.value.status == Q.QW_ERR_INVALID_ARG
+
+
+def test_stream_read_validates_on_the_host(Q):
+    """The diagnostic streaming read rejects a missing sink and unaligned sizes or
+    addresses before launching anything; its sink length is the header's."""
+    src = open(os.path.join(ROOT, "include", "qw.h")).read()
+    m = re.search(r"#define\s+QW_STREAM_READ_SINK_WORDS\s+(\d+)", src)
+    assert m and Q.QW_STREAM_READ_SINK_WORDS == int(m.group(1))
+    fake = 1 << 20  # never dereferenced
+    assert Q.LIB.qw_stream_read(fake, 64, None, 0, None) == Q.QW_ERR_INVALID_ARG
+    assert Q.LIB.qw_stream_read(fake, 40, fake, 0, None) == Q.QW_ERR_ALIGNMENT
+    assert Q.LIB.qw_stream_read(fake + 8, 64, fake, 0, None) == Q.QW_ERR_ALIGNMENT

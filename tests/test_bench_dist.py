@@ -47,7 +47,7 @@ def test_two_gloo_ranks_take_the_slowest_time():
 def test_reference_arm_prints_on_rank_zero_only(rank):
     env = dict(os.environ, RANK=str(rank), WORLD_SIZE="2", LOCAL_RANK=str(rank))
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--steps", "3", "--warmup", "1"], cwd=ROOT, env=env,
+                        "--steps", "3", "--warmup", "1", "--oracle-rows", "64"], cwd=ROOT, env=env,
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
