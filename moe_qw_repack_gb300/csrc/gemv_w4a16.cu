@@ -799,8 +799,11 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int R>
+template <int BITS, int R>
 __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const DecParams p) {
+  using GE = Geo<BITS>;
+  constexpr int WPG = GE::WPG;        // packed words per lane and group
+  constexpr bool F16 = BITS == 4;     // FP16 operands (INT4); BF16 (INT3, INT2)
   extern __shared__ uint4 dec_smem[];
   const int warps = (int)(blockDim.x >> 5);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -808,29 +811,26 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
   const int G = p.K >> 7;
   const uint32_t nblocks = (uint32_t)(p.N_pad >> 4);
   const uint32_t my_items = blockIdx.x < nblocks ? (nblocks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int wg0 = warp * p.gpw;                 // the warp's first group
-  const uint32_t gstride = nblocks * 1024u;     // bytes between groups of a block
-  uint8_t* act = reinterpret_cast<uint8_t*>(dec_smem);           // [G][4][4][16 B]
+  const int wg0 = warp * p.gpw;                       // the warp's first group
+  const uint32_t gstride = nblocks * (uint32_t)GE::BLK;  // bytes between groups of a block
+  uint8_t* act = reinterpret_cast<uint8_t*>(dec_smem);  // [G][4][4][16 B]
   float4* gconst = reinterpret_cast<float4*>(act + (size_t)G * 256);
-  float* red = reinterpret_cast<float*>(gconst + G);              // [2][warps][16]
+  float* red = reinterpret_cast<float*>(gconst + G);     // [2][warps][16]
 
   pdl_launch_dependents();
 
   // ---- register ring: the packed words and scales of R consecutive groups of an item
-  uint32_t wb[R][8];
+  uint32_t wb[R][WPG];
   uint32_t sl_[R], sh_[R];  // BF16 scale bits of rows g and g + 8
-  // byte offset of (item it, the warp's first group) for this lane, and its scale index
+  // byte offset of (item it, the warp's first group) and its scale index
   auto unit_w = [&](uint32_t it) {
-    return (blockIdx.x + it * gridDim.x) * 1024u + (uint32_t)wg0 * gstride + (uint32_t)lane * 32u;
+    return (blockIdx.x + it * gridDim.x) * (uint32_t)GE::BLK + (uint32_t)wg0 * gstride;
   };
   auto unit_s = [&](uint32_t it) {
     return (uint32_t)wg0 * (uint32_t)p.N_pad + (blockIdx.x + it * gridDim.x) * 16u + (uint32_t)g;
   };
   auto load = [&](int r, uint32_t woff, uint32_t soff) {
-    const uint4 v0 = __ldcs(reinterpret_cast<const uint4*>(p.wp + woff));
-    const uint4 v1 = __ldcs(reinterpret_cast<const uint4*>(p.wp + woff) + 1);
-    wb[r][0] = v0.x; wb[r][1] = v0.y; wb[r][2] = v0.z; wb[r][3] = v0.w;
-    wb[r][4] = v1.x; wb[r][5] = v1.y; wb[r][6] = v1.z; wb[r][7] = v1.w;
+    load_words<BITS>(p.wp + woff, lane, wb[r]);
     sl_[r] = __ldg(p.sp + soff);
     sh_[r] = __ldg(p.sp + soff + 8);
   };
@@ -843,8 +843,8 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
       load(r, w0 + (uint32_t)r * gstride, s0 + (uint32_t)r * (uint32_t)p.N_pad);
   }
 
-  // ---- activations of the warp's groups, as FP16 B fragments, and their constants.  A
-  // half warp covers one group; up to four chunks per lane load before any is converted.
+  // ---- activations of the warp's groups as B fragments, and their constants.  A half warp
+  // covers one group; up to four chunks per lane load before any is converted.
   pdl_wait();
   {
     constexpr int kBatch = 4;
@@ -865,24 +865,33 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
         if (u0 + u < iters) {
           const int q = lane + 32 * (u0 + u);
           const int gl = wg0 + (q >> 4), c = q & 15;
-          // group maximum magnitude: BF16 magnitudes order like their bit patterns
-          uint32_t m = __vmaxu2(__vmaxu2(v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu),
-                                __vmaxu2(v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu));
-          m = max(m & 0xFFFFu, m >> 16);
-#pragma unroll
-          for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-          const int ex = (int)(m >> 7);      // biased exponent of the maximum
-          const int f = min(141 - ex, 126);  // 2^f puts the maximum in [2^14, 2^15)
-          const float up = __uint_as_float((uint32_t)(127 + f) << 23);
           const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
           uint32_t h[4];
           float sum = 0.f;
+          int f = 0;
+          if constexpr (F16) {
+            // group maximum magnitude: BF16 magnitudes order like their bit patterns
+            uint32_t m = __vmaxu2(__vmaxu2(v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu),
+                                  __vmaxu2(v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu));
+            m = max(m & 0xFFFFu, m >> 16);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            h[i] = f16x2_of(__uint_as_float(w4[i] << 16) * up,
-                            __uint_as_float(w4[i] & 0xFFFF0000u) * up);
-            const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
-            sum += back.x + back.y;
+            for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            const int ex = (int)(m >> 7);  // biased exponent of the maximum
+            f = min(141 - ex, 126);        // 2^f puts the maximum in [2^14, 2^15)
+            const float up = __uint_as_float((uint32_t)(127 + f) << 23);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              h[i] = f16x2_of(__uint_as_float(w4[i] << 16) * up,
+                              __uint_as_float(w4[i] & 0xFFFF0000u) * up);
+              const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+              sum += back.x + back.y;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              h[i] = w4[i];
+              sum += __uint_as_float(w4[i] << 16) + __uint_as_float(w4[i] & 0xFFFF0000u);
+            }
           }
           // chunk c holds k = 8c .. 8c + 7: step c / 2, lanes t = 2 (c & 1) and 2 (c & 1) + 1
           if (q < nchunk) {
@@ -893,8 +902,13 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
           if ((lane & 15) == 0 && q < nchunk) {
-            const float e = __uint_as_float((uint32_t)(127 - f) << 23);  // 2^-f
-            gconst[gl] = make_float4(e, e * 0.0625f, -1032.f * e * sum, -72.f * e * sum);
+            if constexpr (F16) {
+              const float e = __uint_as_float((uint32_t)(127 - f) << 23);  // 2^-f
+              gconst[gl] = make_float4(e, e * 0.0625f, -1032.f * e * sum, -72.f * e * sum);
+            } else {
+              // biased codes 128 + excess + q on both row halves
+              gconst[gl] = make_float4(1.f, 1.f, -GE::BIAS * sum, -GE::BIAS * sum);
+            }
           }
         }
     }
@@ -925,14 +939,19 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
           const uint4 x = lds128(ab + jj * 64);
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-            const uint32_t wv = wb[r][2 * jj + h2];
-            const uint32_t ws = wv >> 8;
             uint32_t a[4];
-            a[0] = and_or(wv, 0x000F000Fu, 0x64006400u);
-            a[1] = and_or(wv, 0x00F000F0u, 0x64006400u);
-            a[2] = and_or(ws, 0x000F000Fu, 0x64006400u);
-            a[3] = and_or(ws, 0x00F000F0u, 0x64006400u);
-            mma_f16_16816(pr, a, h2 ? x.z : x.x, h2 ? x.w : x.y);
+            if constexpr (F16) {
+              const uint32_t wv = wb[r][2 * jj + h2];
+              const uint32_t ws = wv >> 8;
+              a[0] = and_or(wv, 0x000F000Fu, 0x64006400u);
+              a[1] = and_or(wv, 0x00F000F0u, 0x64006400u);
+              a[2] = and_or(ws, 0x000F000Fu, 0x64006400u);
+              a[3] = and_or(ws, 0x00F000F0u, 0x64006400u);
+              mma_f16_16816(pr, a, h2 ? x.z : x.x, h2 ? x.w : x.y);
+            } else {
+              biased_all<BITS>(wb[r], 2 * jj + h2, a);
+              mma_bf16_16816(pr, a, h2 ? x.z : x.x, h2 ? x.w : x.y);
+            }
           }
         }
         float4 c4;
@@ -998,6 +1017,10 @@ DecPlan decode_plan(int K) {
   return best;
 }
 
+template <int BITS>
+qw_status launch_decode_variant(const qw_packed_desc& d, const DecPlan& pl, const DecParams& p,
+                                cudaStream_t st);
+
 qw_status launch_decode(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
                         const void* A, const void* bias, const float* scale2, void* C,
                         cudaStream_t st) {
@@ -1014,7 +1037,15 @@ qw_status launch_decode(const qw_packed_desc& d, const void* w_packed, const voi
   p.N_pad = d.N_pad;
   p.K = d.K;
   p.gpw = pl.gpw;
-  auto kern = gemv_decode_kernel<kDecRing>;
+  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_decode_variant<4>(d, pl, p, st)
+         : d.wfmt == QW_W_INT3_G128_BF16 ? launch_decode_variant<3>(d, pl, p, st)
+                                         : launch_decode_variant<2>(d, pl, p, st);
+}
+
+template <int BITS>
+qw_status launch_decode_variant(const qw_packed_desc& d, const DecPlan& pl, const DecParams& p,
+                                cudaStream_t st) {
+  auto kern = gemv_decode_kernel<BITS, kDecRing>;
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecMaxSmem);
   if (attr != cudaSuccess) return QW_ERR_CUDA;
@@ -1032,10 +1063,12 @@ qw_status launch_decode(const qw_packed_desc& d, const void* w_packed, const voi
   return launch_pdl(kern, (unsigned)grid, pl.warps * 32, smem, st, p);
 }
 
-// Dense single-token INT4 calls the decode kernel takes (32-bit offsets into the packed
-// buffers; a split with a whole number of ring batches per warp).
+// Dense single-token symmetric INT4 / INT3 / INT2 calls the decode kernel takes (32-bit
+// offsets into the packed buffers; a split with a whole number of ring batches per warp).
 bool decode_eligible(const qw_packed_desc& d, const void* A) {
-  if (d.wfmt != QW_W_INT4_G128_BF16) return false;
+  if (d.wfmt != QW_W_INT4_G128_BF16 && d.wfmt != QW_W_INT3_G128_BF16 &&
+      d.wfmt != QW_W_INT2_G128_BF16)
+    return false;
   if ((reinterpret_cast<uintptr_t>(A) & 15) != 0) return false;
   if (d.w_expert_stride >= (uint64_t(1) << 32)) return false;
   if ((uint64_t)(d.K / 128) * (uint64_t)d.N_pad >= (uint64_t(1) << 31)) return false;
@@ -1479,7 +1512,7 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
                             void* ws, uint64_t ws_bytes, int32_t* err, cudaStream_t st) {
   const bool grouped = rs.offsets != nullptr;
   const int mch = mch_for(d, rs.rows, grouped);
-  // single-token decode, symmetric INT4: the FP16-operand decode kernel
+  // single-token decode, symmetric INT4 / INT3 / INT2: the decode kernel
   if (!grouped && rs.rows == 1 && decode_eligible(d, A))
     return launch_decode(d, w_packed, s_packed, A, bias, rs.scale2, C, st);
   // single-token decode over a large matrix: the staged kernel (its staging pays off once a

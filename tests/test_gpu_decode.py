@@ -22,15 +22,19 @@ def assert_parity(C, R, absum, what=""):
     assert ok, f"{what}: worst |err|/bound = {ratio:.3g}, rel frob = {frob:.3g}"
 
 
-@pytest.mark.parametrize("N,K", [(40, 512), (264, 2048), (1000, 4096), (4104, 14336),
-                                 (520, 16384), (2056, 5120), (16, 128), (72, 640)])
-def test_decode_int4_shapes(N, K):
+@pytest.mark.parametrize("bits", [4, 3, 2])
+@pytest.mark.parametrize("N,K", [(1000, 512), (1032, 2048), (1000, 4096), (4104, 14336),
+                                 (1032, 16384), (2056, 5120), (1000, 128), (1032, 640)])
+def test_decode_shapes(bits, N, K):
     """K = 512 .. 16384 (4 to 128 groups: one to sixteen warps per CTA), N not a multiple of
-    16; K = 128 and 640 have no split with whole ring batches and take the staged kernel."""
-    p = synth.w4a16_problem(1, N, K, bits=4, cfg_id=700 + K // 128)
+    16; K = 128 and 640 have no split with whole ring batches and take the staged kernel.
+    INT4 runs on FP16 operands, INT3 and INT2 on BF16 operands.  Every case has about a
+    thousand outputs or more: with a few dozen, BF16 rounding of the exact result alone can
+    exceed the Frobenius bound."""
+    p = synth.w4a16_problem(1, N, K, bits=bits, cfg_id=700 + K // 128)
     C = dense_w4a16(p)
-    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, 4)
-    assert_parity(C, R, S, f"decode {N}x{K}")
+    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, bits)
+    assert_parity(C, R, S, f"decode INT{bits} {N}x{K}")
 
 
 def test_decode_int4_bias_and_scale2():
@@ -62,19 +66,21 @@ def _scaled_activations(K, exps, cfg):
     return synth.to_bf16_bits(a)
 
 
+@pytest.mark.parametrize("bits", [4, 3])
 @pytest.mark.parametrize("exps", [
     [0, -60, 60, None, -20, 20, 100, -100],       # groups many binades apart, one all zero
     [-100] * 8,                                   # every group tiny
     [100] * 8,                                    # every group huge
 ])
-def test_decode_int4_group_magnitudes(exps):
-    """The per-group power-of-two scaling keeps every group exact, whatever its magnitude:
-    each output is checked against its own sum of |a w| (no absolute floor)."""
+def test_decode_group_magnitudes(bits, exps):
+    """INT4's per-group power-of-two scaling keeps every group exact, whatever its
+    magnitude (INT3 takes BF16 operands as they are): each output is checked against its
+    own sum of |a w| (no absolute floor)."""
     N, K = 520, 128 * len(exps)
-    p = synth.w4a16_problem(1, N, K, bits=4, cfg_id=740)
+    p = synth.w4a16_problem(1, N, K, bits=bits, cfg_id=740)
     p["A"] = _scaled_activations(K, exps, 741)
     C = dense_w4a16(p)
-    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, 4)
+    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, bits)
     c = torch.from_numpy(C.astype(np.int16)).view(torch.bfloat16).double().numpy()
     assert np.all(np.isfinite(c))
     bad = np.abs(c - R) > 2.0 ** -7 * S

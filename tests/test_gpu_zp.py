@@ -51,16 +51,31 @@ def test_zp_bias(M):
     assert ok, (ratio, frob)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 8192, 4096), (5, 100, 256), (40, 256, 512)])
+def _as_zero_point_8(p, N, K):
+    q = OF.unpack_int4(p["w_canon"][0], K).astype(np.int64) + 8
+    words = np.ascontiguousarray(synth.pack_nibbles(q.astype(np.uint8))).view("<u4")
+    sz = p["s_canon"][0].astype(np.uint32) | np.uint32(8 << 16)
+    return dict(A=p["A"], w_canon=words[None].astype(np.uint32), s_canon=sz[None], N=N, K=K)
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 100, 256), (40, 256, 512)])
 def test_zp_with_zero_point_8_equals_symmetric_int4(M, N, K):
     """q + 8 with z = 8 is the symmetric code: same kernels' arithmetic, same bits."""
     p = synth.w4a16_problem(M, N, K, bits=4, cfg_id=860 + M)
     C_sym = dense_w4a16(p)
-    q = OF.unpack_int4(p["w_canon"][0], K).astype(np.int64) + 8
-    words = np.ascontiguousarray(synth.pack_nibbles(q.astype(np.uint8))).view("<u4")
-    sz = p["s_canon"][0].astype(np.uint32) | np.uint32(8 << 16)
-    pz = dict(A=p["A"], w_canon=words[None].astype(np.uint32), s_canon=sz[None], N=N, K=K)
-    assert np.array_equal(dense_zp(pz), C_sym)
+    assert np.array_equal(dense_zp(_as_zero_point_8(p, N, K)), C_sym)
+
+
+def test_zp_with_zero_point_8_single_token():
+    """Single-token decode: symmetric INT4 runs the FP16-operand decode kernel and the
+    asymmetric format the staged BF16 kernel, so the two round differently; with z = 8 both
+    match the same oracle result."""
+    M, N, K = 1, 8192, 4096
+    p = synth.w4a16_problem(M, N, K, bits=4, cfg_id=861)
+    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, 4)
+    for C in (dense_w4a16(p), dense_zp(_as_zero_point_8(p, N, K))):
+        ok, ratio, frob = OQ.check_bf16_result(C, R, S)
+        assert ok, (ratio, frob)
 
 
 def test_zp_repack_round_trip_and_value_flag():
