@@ -17,6 +17,8 @@ Pins (tests/test_oracle_formats.py):
   unpack_int4   hand-written words in tests/golden/int4_words.txt
   unpack_int3   hand-written stream in tests/golden/int3_stream.txt + bit-string build
   unpack_e2m1_bytes  hand-written bytes in tests/golden/e2m1_bytes.txt
+  unpack_int1   hand-written words in tests/golden/int1_words.txt, random words against a
+                bit-string construction
   e0m_encode / e0m_decode  the zero-exponent-float equivalence of the spke.com page,
                 section "量子化サポート" (INT8 without -128 == float8e0m7 value set)
 """
@@ -93,6 +95,23 @@ def unpack_int2(words, K: int) -> np.ndarray:
         out[..., i::16] = np.where(f >= 2, f - 4, f)
     if np.any(out == -2):
         raise FormatError("INT2 code -2 is outside the symmetric range")
+    return out
+
+
+def unpack_int1(words, K: int) -> np.ndarray:
+    """uint32 [..., K/32] -> int8 [..., K] in {-1, +1}; element k = 32j + i is bit i of
+    word j, and bit b stands for the weight 2b - 1.
+
+    Reading: the announcement (section "WnA16") lists INT1 among the weight types without
+    defining it.  A one-bit two's-complement integer without its minimum (the rule the
+    other symmetric widths follow) would hold only 0, so INT1 is read as sign
+    quantisation: the two codes are -1 and +1 and the group scale sets the magnitude."""
+    w = np.asarray(words).astype(np.uint32)
+    assert w.shape[-1] * 32 == K
+    out = np.empty((*w.shape[:-1], K), dtype=np.int8)
+    for i in range(32):
+        b = ((w >> np.uint32(i)) & np.uint32(1)).astype(np.int8)
+        out[..., i::32] = 2 * b - 1
     return out
 
 

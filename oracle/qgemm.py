@@ -13,6 +13,11 @@ output stage; section "WnA16": low-bit weights times 16-bit activations; section
   FP8-weight WnA16 (the section "WnA16"'s floating-point weights up to FP8; E4M3 codes
   with the same BF16 group-128 scales as the integer formats):
           R[m,n] = sum_k a[m,k] * e4m3(w[n,k]) * s[n, k // G]          (+ bias[n])
+  FP4-weight WnA16 (the same section's FP4 weights; E2M1 codes with the BF16 group-128
+  scales of the integer formats):
+          R[m,n] = sum_k a[m,k] * e2m1(w[n,k]) * s[n, k // G]          (+ bias[n])
+  INT1 WnA16 (the same section's INT1; sign quantisation, w = s * (2b - 1)):
+          R[m,n] = sum_k a[m,k] * (2 b[n,k] - 1) * s[n, k // G]        (+ bias[n])
   W4A8:   R[m,n] = sum_k e4m3(a[m,k]) 2^(sa[m,k//32]-127)
                           * e2m1(w[n,k]) 2^(sw[n,k//32]-127)      (+ bias[n])
   W4A4:   R[m,n] = sum_k e2m1(a[m,k]) e4m3(sa[m,k//16])
@@ -35,7 +40,9 @@ Pins (tests/test_oracle_gemm.py): exact int64 dot products when every scale is
 on tiny shapes with several groups; non-square shapes so that a transposed
 operand or a wrong group index changes the result; FP8-weight: equality with the W4A16
 GEMM on E4M3 codes of integers, and exact rationals over every finite E4M3 code from
-PyTorch's float8_e4m3fn values.
+PyTorch's float8_e4m3fn values.  FP4-weight and INT1 (tests/test_oracle_fp4_int1.py):
+exact int64 dot products on integer-valued codes, exact rationals over all sixteen E2M1
+codes, hand-written INT1 words, and planted mistakes.
 """
 from __future__ import annotations
 
@@ -81,6 +88,12 @@ def gemm_w8a16_fp8(A_bits, w_codes, s_bits, bias_bits=None, group: int = 128):
     """A_bits [M][K] BF16, w_codes [N][K] E4M3, s_bits [N][K/group] BF16 -> (R, absum) of
     w = e4m3(code) * s: the W4A16 product with decoded E4M3 values in place of integers."""
     return gemm_w4a16(A_bits, F.decode_e4m3(w_codes), s_bits, bias_bits, group)
+
+
+def gemm_w4a16_fp4(A_bits, w_codes, s_bits, bias_bits=None, group: int = 128):
+    """A_bits [M][K] BF16, w_codes [N][K] E2M1 codes, s_bits [N][K/group] BF16 -> (R, absum)
+    of w = e2m1(code) * s: the W4A16 product with decoded E2M1 values in place of integers."""
+    return gemm_w4a16(A_bits, F.decode_e2m1(w_codes), s_bits, bias_bits, group)
 
 
 def apply_scale2(R, absum, t, bias_bits=None):
@@ -154,7 +167,7 @@ def gemm_w4a4(A_codes, A_sf, w_codes, w_sf, bias_bits=None):
 def w4a16_from_canonical(A_bits, w_canon, s_canon, K, bits, bias_bits=None, rows=None, cols=None):
     """Unpack canonical packed words (one expert) and run :func:`gemm_w4a16`.
     ``rows`` / ``cols`` optionally select a sample of output rows / columns."""
-    q = {4: F.unpack_int4, 3: F.unpack_int3, 2: F.unpack_int2}[bits](w_canon, K)
+    q = {4: F.unpack_int4, 3: F.unpack_int3, 2: F.unpack_int2, 1: F.unpack_int1}[bits](w_canon, K)
     A = np.asarray(A_bits)
     s = np.asarray(s_canon)
     if rows is not None:
@@ -163,6 +176,20 @@ def w4a16_from_canonical(A_bits, w_canon, s_canon, K, bits, bias_bits=None, rows
         q, s = q[cols], s[cols]
         bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
     return gemm_w4a16(A, q, s, bias_bits)
+
+
+def fp4w_from_canonical(A_bits, w_canon, s_canon, K, bias_bits=None, rows=None, cols=None):
+    """E2M1 codes two per byte [N][K/2] (even k in the low nibble) and BF16 group-128
+    scales of one expert -> :func:`gemm_w4a16_fp4`."""
+    codes = F.unpack_e2m1_bytes(w_canon, K)
+    A = np.asarray(A_bits)
+    s = np.asarray(s_canon)
+    if rows is not None:
+        A = A[rows]
+    if cols is not None:
+        codes, s = codes[cols], s[cols]
+        bias_bits = None if bias_bits is None else np.asarray(bias_bits)[cols]
+    return gemm_w4a16_fp4(A, codes, s, bias_bits)
 
 
 def fp8w_from_canonical(A_bits, w_canon, s_canon, bias_bits=None, rows=None, cols=None):

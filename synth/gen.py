@@ -181,6 +181,18 @@ def pack_int3(codes: np.ndarray) -> np.ndarray:
     return out
 
 
+def pack_int1(signs: np.ndarray) -> np.ndarray:
+    """weights in {-1, +1}, shape [..., K] (K % 32 == 0) -> uint32 [..., K/32]; element
+    k = 32j + i is bit i of word j, set for +1."""
+    b = (np.asarray(signs).astype(np.int64) > 0).astype(np.uint64)
+    assert b.shape[-1] % 32 == 0
+    b = b.reshape(*b.shape[:-1], b.shape[-1] // 32, 32)
+    w = np.zeros(b.shape[:-1], dtype=np.uint64)
+    for i in range(32):
+        w |= b[..., i] << np.uint64(i)
+    return w.astype(np.uint32)
+
+
 def pack_nibbles(codes: np.ndarray) -> np.ndarray:
     """4-bit codes [..., K] (K even) -> uint8 [..., K/2], even k in the low nibble."""
     c = np.asarray(codes, dtype=np.uint8)
@@ -192,12 +204,28 @@ def pack_nibbles(codes: np.ndarray) -> np.ndarray:
 def w4a16_problem(M, N, K, *, bits=4, E=1, cfg_id=0, seed=BASE_SEED,
                   scale_lo=0.005, scale_hi=0.02, bias=False):
     """Group-128 symmetric INT weights with BF16 scales and BF16 N(0,1) activations."""
-    qmax = {4: 7, 3: 3, 2: 1}[bits]
-    q = uniform_int(stream(cfg_id, 1, seed), (E, N, K), -qmax, qmax).astype(np.int8)
+    if bits == 1:  # INT1: the two codes -1 and +1, equally likely
+        q = (2 * uniform_int(stream(cfg_id, 1, seed), (E, N, K), 0, 1) - 1).astype(np.int8)
+    else:
+        qmax = {4: 7, 3: 3, 2: 1}[bits]
+        q = uniform_int(stream(cfg_id, 1, seed), (E, N, K), -qmax, qmax).astype(np.int8)
     s = to_bf16_bits(uniform(stream(cfg_id, 2, seed), (E, N, K // 128), scale_lo, scale_hi))
     a = to_bf16_bits(normal(stream(cfg_id, 3, seed), (M, K)))
-    w = {4: pack_int4, 3: pack_int3, 2: pack_int2}[bits](q)
+    w = {4: pack_int4, 3: pack_int3, 2: pack_int2, 1: pack_int1}[bits](q)
     out = dict(A=a, q=q, w_canon=w, s_canon=s, E=E, N=N, K=K, M=M, bits=bits)
+    if bias:
+        out["bias"] = to_bf16_bits(normal(stream(cfg_id, 4, seed), (E, N)))
+    return out
+
+
+def fp4w_problem(M, N, K, *, E=1, cfg_id=0, seed=BASE_SEED, scale_lo=0.005, scale_hi=0.02,
+                 bias=False):
+    """FP4-weight WnA16: E2M1 codes uniform over the 16 codes (two per byte, even k in the
+    low nibble), BF16 scales per 128 along K, BF16 N(0,1) activations."""
+    codes = uniform_int(stream(cfg_id, 1, seed), (E, N, K), 0, 15).astype(np.uint8)
+    s = to_bf16_bits(uniform(stream(cfg_id, 2, seed), (E, N, K // 128), scale_lo, scale_hi))
+    a = to_bf16_bits(normal(stream(cfg_id, 3, seed), (M, K)))
+    out = dict(A=a, codes=codes, w_canon=pack_nibbles(codes), s_canon=s, E=E, N=N, K=K, M=M)
     if bias:
         out["bias"] = to_bf16_bits(normal(stream(cfg_id, 4, seed), (E, N)))
     return out
@@ -299,8 +327,9 @@ def router_logits(T, E, *, cfg_id=3, seed=BASE_SEED, bias_std=1.5):
 
 __all__ = [
     "BASE_SEED", "Stream", "stream", "uniform_int", "uniform", "normal", "random_bytes",
-    "to_bf16_bits", "to_e4m3_codes", "pack_int4", "pack_int3", "pack_int2", "pack_nibbles",
-    "unpack_nibbles_layout", "w4a16_problem", "w4a16_zp_problem", "fp8w_problem", "w4a8_problem",
+    "to_bf16_bits", "to_e4m3_codes", "pack_int4", "pack_int3", "pack_int2", "pack_int1",
+    "pack_nibbles", "unpack_nibbles_layout", "w4a16_problem", "w4a16_zp_problem",
+    "fp8w_problem", "fp4w_problem", "w4a8_problem",
     "w8a8_problem",
     "w4a4_problem",
     "router_logits",
