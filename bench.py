@@ -797,8 +797,8 @@ def run_reference(args, world, rank):
     # One step is one repetition of the cpu_baseline leg's sample (the same shapes and rows,
     # so the two report the same rate), about 3 s on these hosts; past 40 steps the
     # sample keeps its shapes with proportionally fewer rows so the run stays short.
-    if args.oracle_rows:
-        kw = dict(rows_b=args.oracle_rows, min_seconds=0.0, rows_a=args.oracle_rows)
+    if args.oracle_rows:  # a short sample: that many rows of the (4096, 3072, 4096) GEMM
+        kw = dict(rows_b=0, min_seconds=0.0, rows_a=args.oracle_rows)
     elif args.steps <= 40:
         kw = dict(rows_b=CPU_SAMPLE_ROWS_B, min_seconds=0.0)
     else:
@@ -839,8 +839,8 @@ def main():
                     help="with --only-w4a16 / --only-moe / --only-fp8w: run only the cases "
                          "whose name contains this string")
     ap.add_argument("--oracle-rows", type=int, default=0,
-                    help="with --impl reference: rows of each shape in a step's oracle sample "
-                         "(default: the cpu_baseline leg's sample)")
+                    help="with --impl reference: a short step sample of that many rows of the "
+                         "(4096, 3072, 4096) GEMM (default: the cpu_baseline leg's sample)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup) if args.impl == "ours" else args.warmup
     if args.impl == "reference":

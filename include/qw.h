@@ -77,7 +77,10 @@ typedef enum qw_wfmt {
   QW_W_UINT4ZP_G128_BF16 = 5, /* unsigned 4-bit codes, BF16 scale and zero point per 128:
                                  w = s * (q - z) (asymmetric INT4)                         */
   QW_W_INT2_G128_BF16 = 6, /* symmetric INT2 in {-1, 0, 1}, BF16 scale per 128 along K    */
-  QW_W_FP8E4M3_G128_BF16 = 7 /* E4M3 codes, BF16 scale per 128 along K (FP8-weight WnA16) */
+  QW_W_FP8E4M3_G128_BF16 = 7, /* E4M3 codes, BF16 scale per 128 along K (FP8-weight WnA16) */
+  QW_W_INT1_G128_BF16 = 8, /* INT1 sign codes: bit b is the weight 2b - 1 (-1 or +1), BF16
+                              scale per 128 along K                                     */
+  QW_W_FP4E2M1_G128_BF16 = 9 /* E2M1 codes, BF16 scale per 128 along K (FP4-weight WnA16) */
 } qw_wfmt;
 
 /* Second-level scales (the announcement, section "統一されたquantization表現": the
@@ -101,7 +104,8 @@ typedef struct qw_packed_desc {
   int32_t wfmt;            /* qw_wfmt, possibly | QW_W_SCALE2                          */
   int32_t E, N, K;         /* logical sizes                                            */
   int32_t N_pad, K_pad;    /* padded sizes of the packed layout                        */
-  int32_t group;           /* 128 (INT, FP8E4M3), 32 (MXFP4 / MXFP8) or 16 (NVFP4)     */
+  int32_t group;           /* 128 (INT, FP8E4M3, FP4E2M1), 32 (MXFP4 / MXFP8) or 16
+                              (NVFP4)                                                  */
   int32_t reserved;
   uint64_t w_bytes;        /* size of w_packed in bytes (all experts)                  */
   uint64_t s_bytes;        /* size of s_packed in bytes (all experts)                  */
@@ -143,6 +147,10 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *   INT2:  w_canon uint32 [E][N][K/16]; element k = 16j+i at bits [2i,2i+2) of word j,
  *          two's complement (-2 rejected).  s_canon BF16 [E][N][K/128].
  *   FP8E4M3: w_canon uint8 [E][N][K] E4M3 codes.  s_canon BF16 [E][N][K/128].
+ *   INT1:  w_canon uint32 [E][N][K/32]; element k = 32j+i is bit i of word j, bit b
+ *          standing for the weight 2b - 1.  s_canon BF16 [E][N][K/128].
+ *   FP4E2M1: w_canon uint8 [E][N][K/2] E2M1 codes, even k in the low nibble.  s_canon BF16
+ *          [E][N][K/128].
  *   UINT4ZP: w_canon uint32 [E][N][K/8] packed as INT4 but read unsigned (q in [0, 15]).
  *          s_canon uint32 [E][N][K/128]: bits 0-15 the BF16 scale, bits 16-23 the zero
  *          point z in [0, 15], bits 24-31 zero (else a value error).
@@ -172,6 +180,14 @@ qw_status qw_repack_query(int32_t wfmt, int32_t E, int32_t N, int32_t K, qw_pack
  *          k = 16s + 4t + 2j + (b & 1) (the INT4 (row, k) assignment, one byte per weight:
  *          each 16-bit half is one BF16 pair of the MMA fragment once decoded).
  *          Scales BF16 [K/128][N_pad].
+ *   INT1:  per expert [K/128][N_pad/16] blocks of 256 B: 32 lanes x 2 words holding the
+ *          lane's 64 sign bits (the INT4 (row, k) assignment): register r of MMA step s
+ *          (rows g + 8 (r & 1), k = 16s + 4t + 2 (r >> 1) + h) at bit 4 (s % 4) + r + 16h
+ *          of word s / 4.  Padding rows hold bit 0.  Scales BF16 [K/128][N_pad].
+ *   FP4E2M1: per expert [K/128][N_pad/16] blocks of 1 KiB: 32 lanes x 8 words, word s for
+ *          MMA step s; byte r of it holds register r - the E2M1 codes of row g + 8 (r & 1)
+ *          at k = 16s + 4t + 2 (r >> 1) (low nibble) and k + 1 (high nibble).  Scales BF16
+ *          [K/128][N_pad].
  *   UINT4ZP: codes in the INT4 block layout with the nibble q itself (an excess code
  *          whose excess is the group's zero point); scales: BF16 [K/128][N_pad] as INT4,
  *          then (at s_expert_stride / 2) the BF16 numbers 128 + z in the same layout.
@@ -221,7 +237,8 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
 /* --------------------------------------------------------------------------------------
  * qgemm_dense - C[M][N] = bf16( sum_k a[m,k] * w[n,k] + bias[n] ) with the weight
  * dequantization (and, for W4A8, both block scales) applied inside the kernel.
- *   W4A16: desc->wfmt INT4/INT3/INT2/UINT4ZP/FP8E4M3, afmt QW_A_BF16, A BF16 [M][K],
+ *   W4A16: desc->wfmt INT4/INT3/INT2/INT1/UINT4ZP/FP8E4M3/FP4E2M1, afmt QW_A_BF16,
+ *          A BF16 [M][K],
  *          A_sf NULL.
  *   W4A8:  desc->wfmt MXFP4,     afmt QW_A_MXFP8_G32, A E4M3 [M][K], A_sf E8M0 [M][K/32].
  *   W8A8:  desc->wfmt MXFP8,     afmt QW_A_MXFP8_G32, as W4A8.

@@ -65,7 +65,7 @@ constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BT >
 
 template <int BITS, bool ZP>
 struct Geo {
-  static constexpr int BLK = BITS * 256;  // one packed 16 x 128 block
+  static constexpr int BLK = wna16_block_bytes(BITS);  // one packed 16 x 128 block
   static constexpr int WBYTES = 8 * BLK;
   // asymmetric INT4: the tile's 128 rows of BF16 128 + zero point for the stage's group
   static constexpr int ZBYTES = ZP ? BW * 2 : 0;
@@ -378,6 +378,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 v[4 * st + 1] = e4m3x2_to_bf16x2(w[2 * st + 1]);
                 v[4 * st + 3] = e4m3x2_to_bf16x2(w[2 * st + 1] >> 16);
               }
+            } else if constexpr (BITS == kBitsFp4) {
+              // E2M1 codes: byte r of word st is register r (rows g + 8 (r & 1), k + 2 (r >> 1)),
+              // one hardware conversion to FP16, then to BF16 (exact), no excess
+              const uint4 w0 = lds128(blk + lane * 32), w1 = lds128(blk + lane * 32 + 16);
+              const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+              for (int st = 0; st < 8; ++st) {
+                uint32_t h[4];
+                e2m1x8_to_f16x2(w[st], h);
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                  v[4 * st + ((r & 1) << 1) + (r >> 1)] = f16x2_to_bf16x2(h[r]);
+              }
+            } else if constexpr (BITS == 1) {
+              // INT1 sign codes: register r of step st at bits 4 (st % 4) + r (+ 16) of word
+              // st / 4, decoded to BF16 +-1 pairs
+              const uint2 W = lds64(blk + lane * 8);
+#pragma unroll
+              for (int st = 0; st < 8; ++st)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                  v[4 * st + ((r & 1) << 1) + (r >> 1)] =
+                      int1_pair(st < 4 ? W.x : W.y, 4 * (st & 3) + r, 0x3F803F80u);
             } else if constexpr (BITS == 2) {
               const uint4 lo = lds128(blk + lane * 16);
               const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w};
@@ -624,6 +647,9 @@ qw_status launch_gemm_w4a16_tc(const qw_packed_desc& d, const void* w_packed,
   if (d.wfmt == QW_W_UINT4ZP_G128_BF16) return launch_bits<4, true>(tmA, tmC, p, tiles_max, st);
   if (d.wfmt == QW_W_INT2_G128_BF16) return launch_bits<2, false>(tmA, tmC, p, tiles_max, st);
   if (d.wfmt == QW_W_FP8E4M3_G128_BF16) return launch_bits<8, false>(tmA, tmC, p, tiles_max, st);
+  if (d.wfmt == QW_W_INT1_G128_BF16) return launch_bits<1, false>(tmA, tmC, p, tiles_max, st);
+  if (d.wfmt == QW_W_FP4E2M1_G128_BF16)
+    return launch_bits<kBitsFp4, false>(tmA, tmC, p, tiles_max, st);
   return d.wfmt == QW_W_INT4_G128_BF16 ? launch_bits<4, false>(tmA, tmC, p, tiles_max, st)
                                        : launch_bits<3, false>(tmA, tmC, p, tiles_max, st);
 }

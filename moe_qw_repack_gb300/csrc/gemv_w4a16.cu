@@ -164,11 +164,14 @@ constexpr int kWarps = 8;        // warps per CTA (split K of one item)
 // resident CTAs per SM a variant is built for (token rows cost registers)
 __host__ __device__ constexpr int ctas_per_sm(int mch) { return 2; }
 
+// Format codes (the BITS template argument): 4, 3, 2, 1 for INT4 / INT3 / INT2 / INT1, 8 for
+// E4M3 weights, kBitsFp4 for E2M1 weights.
 template <int BITS>
 struct Geo {
-  static constexpr int BLK = BITS * 256;                      // one 16 x 128 block
-  static constexpr int WPG = BITS * 2;                        // words per lane and group
-  static constexpr bool FP = BITS == 8;                       // E4M3 codes: no excess
+  static constexpr int BLK = wna16_block_bytes(BITS);        // one 16 x 128 block
+  static constexpr int WPG = BLK / 128;                      // words per lane and group
+  // values decoded as they are (E4M3, E2M1, INT1 +-1): no excess to remove
+  static constexpr bool FP = BITS == 8 || BITS == kBitsFp4 || BITS == 1;
   static constexpr float BIAS = FP ? 0.f : 128.f + (1 << (BITS - 1));  // 128 + excess
 };
 
@@ -225,6 +228,14 @@ __device__ __forceinline__ void load_words(const uint8_t* blk, int lane,
       const uint4 v = __ldcs(reinterpret_cast<const uint4*>(blk) + lane * 4 + i);
       w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
     }
+  } else if constexpr (BITS == kBitsFp4) {
+    const uint4 v0 = __ldcs(reinterpret_cast<const uint4*>(blk) + lane * 2);
+    const uint4 v1 = __ldcs(reinterpret_cast<const uint4*>(blk) + lane * 2 + 1);
+    w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+    w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+  } else if constexpr (BITS == 1) {
+    const uint2 v = __ldcs(reinterpret_cast<const uint2*>(blk) + lane);
+    w[0] = v.x; w[1] = v.y;
   } else {
     const uint4 lo = __ldcs(reinterpret_cast<const uint4*>(blk) + lane);
     const uint2 hi = __ldcs(reinterpret_cast<const uint2*>(blk + 512) + lane);
@@ -258,17 +269,36 @@ __device__ __forceinline__ BatchPtr batch_ptr(const Params& p, uint32_t qb, uint
   return b;
 }
 
-// Step S of a group -> four BF16x2 A-fragment registers holding 128 + code.
-// E4M3 codes: words 2s (rows g, g + 8 at k + 0/1) and 2s + 1 (at k + 2/3) -> the four
-// registers as they are (no excess).
-template <int BITS>
-__device__ __forceinline__ void biased_all(const uint32_t (&w)[Geo<BITS>::WPG], int s,
-                                           uint32_t (&a)[4]) {
+// Values decoded as they are (no excess), step s of a group -> four BF16x2 A-fragment
+// registers.  E4M3: words 2s (rows g, g + 8 at k + 0/1) and 2s + 1 (at k + 2/3).  E2M1:
+// byte r of word s is register r (one hardware conversion to FP16, then to BF16).  INT1:
+// register r's two bits are bits 4 (s % 4) + r and 16 + 4 (s % 4) + r of word s / 4.
+template <int BITS, int NW>
+__device__ __forceinline__ void direct_step(const uint32_t (&w)[NW], int s, uint32_t (&a)[4]) {
   if constexpr (BITS == 8) {
     a[0] = e4m3x2_to_bf16x2(w[2 * s]);
     a[1] = e4m3x2_to_bf16x2(w[2 * s] >> 16);
     a[2] = e4m3x2_to_bf16x2(w[2 * s + 1]);
     a[3] = e4m3x2_to_bf16x2(w[2 * s + 1] >> 16);
+  } else if constexpr (BITS == kBitsFp4) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2(w[s], h);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a[r] = f16x2_to_bf16x2(h[r]);
+  } else {
+    static_assert(BITS == 1, "direct decode of E4M3, E2M1 or INT1");
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a[r] = int1_pair(w[s >> 2], 4 * (s & 3) + r, 0x3F803F80u);
+  }
+}
+
+// Step S of a group -> four BF16x2 A-fragment registers holding 128 + code (integer
+// formats) or the decoded values (E4M3, E2M1, INT1).
+template <int BITS>
+__device__ __forceinline__ void biased_all(const uint32_t (&w)[Geo<BITS>::WPG], int s,
+                                           uint32_t (&a)[4]) {
+  if constexpr (Geo<BITS>::FP) {
+    direct_step<BITS>(w, s, a);
   } else {
     uint32_t w8[8];
 #pragma unroll
@@ -283,12 +313,9 @@ __device__ __forceinline__ void biased_all(const uint32_t (&w)[Geo<BITS>::WPG], 
 // consumers keep 8 words for the integer formats, 16 for E4M3).
 template <int BITS, int NW>
 __device__ __forceinline__ void decode_step(const uint32_t (&w)[NW], int s, uint32_t (&a)[4]) {
-  if constexpr (BITS == 8) {
-    static_assert(NW == 16, "E4M3 blocks hold 16 words per lane");
-    a[0] = e4m3x2_to_bf16x2(w[2 * s]);
-    a[1] = e4m3x2_to_bf16x2(w[2 * s] >> 16);
-    a[2] = e4m3x2_to_bf16x2(w[2 * s + 1]);
-    a[3] = e4m3x2_to_bf16x2(w[2 * s + 1] >> 16);
+  if constexpr (Geo<BITS>::FP) {
+    static_assert(BITS != 8 || NW == 16, "E4M3 blocks hold 16 words per lane");
+    direct_step<BITS>(w, s, a);
   } else {
     static_assert(NW == 8, "integer words are passed as 8");
     biased<BITS>(s, w, a);
@@ -301,7 +328,7 @@ __global__ void __launch_bounds__(kWarps * 32, ctas_per_sm(MCH))
   using GE = Geo<BITS>;
   constexpr int WPG = GE::WPG;
   // E4M3 groups are twice the bytes: half the ring depth in the same registers
-  constexpr int NB = GE::FP ? (batch_groups(MCH) + 1) / 2 : batch_groups(MCH);
+  constexpr int NB = WPG > 8 ? (batch_groups(MCH) + 1) / 2 : batch_groups(MCH);
   extern __shared__ float red[];  // [warp][MCH][4][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -548,7 +575,7 @@ template <int BITS, bool ZP>
 __global__ void __launch_bounds__(kM8Warps * 32, 2) gemv_m8_kernel(const M8Params p) {
   using GE = Geo<BITS>;
   constexpr int WPG = GE::WPG;
-  constexpr int R = GE::FP ? kM8Ring / 2 : kM8Ring;  // E4M3: twice the words per group
+  constexpr int R = GE::WPG > 8 ? kM8Ring / 2 : kM8Ring;  // E4M3: twice the words per group
   extern __shared__ uint4 m8_smem[];
   const int G = p.K >> 7;
   uint8_t* act = reinterpret_cast<uint8_t*>(m8_smem);
@@ -803,7 +830,9 @@ template <int BITS, int R>
 __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const DecParams p) {
   using GE = Geo<BITS>;
   constexpr int WPG = GE::WPG;        // packed words per lane and group
-  constexpr bool F16 = BITS == 4;     // FP16 operands (INT4); BF16 (INT3, INT2)
+  // FP16 operands for INT4 (the in-place nibble trick), E2M1 (hardware conversion) and
+  // INT1 (sign pairs); BF16 for INT3 and INT2
+  constexpr bool F16 = BITS == 4 || BITS == kBitsFp4 || BITS == 1;
   extern __shared__ uint4 dec_smem[];
   const int warps = (int)(blockDim.x >> 5);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -902,9 +931,12 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
           if ((lane & 15) == 0 && q < nchunk) {
-            if constexpr (F16) {
+            if constexpr (BITS == 4) {
               const float e = __uint_as_float((uint32_t)(127 - f) << 23);  // 2^-f
               gconst[gl] = make_float4(e, e * 0.0625f, -1032.f * e * sum, -72.f * e * sum);
+            } else if constexpr (F16) {
+              const float e = __uint_as_float((uint32_t)(127 - f) << 23);  // 2^-f, no excess
+              gconst[gl] = make_float4(e, e, 0.f, 0.f);
             } else {
               // biased codes 128 + excess + q on both row halves
               gconst[gl] = make_float4(1.f, 1.f, -GE::BIAS * sum, -GE::BIAS * sum);
@@ -940,13 +972,22 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t a[4];
-            if constexpr (F16) {
+            if constexpr (BITS == 4) {
               const uint32_t wv = wb[r][2 * jj + h2];
               const uint32_t ws = wv >> 8;
               a[0] = and_or(wv, 0x000F000Fu, 0x64006400u);
               a[1] = and_or(wv, 0x00F000F0u, 0x64006400u);
               a[2] = and_or(ws, 0x000F000Fu, 0x64006400u);
               a[3] = and_or(ws, 0x00F000F0u, 0x64006400u);
+              mma_f16_16816(pr, a, h2 ? x.z : x.x, h2 ? x.w : x.y);
+            } else if constexpr (BITS == kBitsFp4) {
+              e2m1x8_to_f16x2(wb[r][2 * jj + h2], a);  // byte i of the word is register i
+              mma_f16_16816(pr, a, h2 ? x.z : x.x, h2 ? x.w : x.y);
+            } else if constexpr (BITS == 1) {
+              const int s2 = 2 * jj + h2;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                a[q] = int1_pair(wb[r][s2 >> 2], 4 * (s2 & 3) + q, 0x3C003C00u);
               mma_f16_16816(pr, a, h2 ? x.z : x.x, h2 ? x.w : x.y);
             } else {
               biased_all<BITS>(wb[r], 2 * jj + h2, a);
@@ -1037,9 +1078,13 @@ qw_status launch_decode(const qw_packed_desc& d, const void* w_packed, const voi
   p.N_pad = d.N_pad;
   p.K = d.K;
   p.gpw = pl.gpw;
-  return d.wfmt == QW_W_INT4_G128_BF16 ? launch_decode_variant<4>(d, pl, p, st)
-         : d.wfmt == QW_W_INT3_G128_BF16 ? launch_decode_variant<3>(d, pl, p, st)
-                                         : launch_decode_variant<2>(d, pl, p, st);
+  switch (d.wfmt) {
+    case QW_W_INT4_G128_BF16: return launch_decode_variant<4>(d, pl, p, st);
+    case QW_W_INT3_G128_BF16: return launch_decode_variant<3>(d, pl, p, st);
+    case QW_W_INT2_G128_BF16: return launch_decode_variant<2>(d, pl, p, st);
+    case QW_W_INT1_G128_BF16: return launch_decode_variant<1>(d, pl, p, st);
+    default: return launch_decode_variant<kBitsFp4>(d, pl, p, st);
+  }
 }
 
 template <int BITS>
@@ -1063,11 +1108,12 @@ qw_status launch_decode_variant(const qw_packed_desc& d, const DecPlan& pl, cons
   return launch_pdl(kern, (unsigned)grid, pl.warps * 32, smem, st, p);
 }
 
-// Dense single-token symmetric INT4 / INT3 / INT2 calls the decode kernel takes (32-bit
+// Dense single-token symmetric INT4 / INT3 / INT2 / INT1 and E2M1 calls the decode kernel takes (32-bit
 // offsets into the packed buffers; a split with a whole number of ring batches per warp).
 bool decode_eligible(const qw_packed_desc& d, const void* A) {
   if (d.wfmt != QW_W_INT4_G128_BF16 && d.wfmt != QW_W_INT3_G128_BF16 &&
-      d.wfmt != QW_W_INT2_G128_BF16)
+      d.wfmt != QW_W_INT2_G128_BF16 && d.wfmt != QW_W_INT1_G128_BF16 &&
+      d.wfmt != QW_W_FP4E2M1_G128_BF16)
     return false;
   if ((reinterpret_cast<uintptr_t>(A) & 15) != 0) return false;
   if (d.w_expert_stride >= (uint64_t(1) << 32)) return false;
@@ -1093,13 +1139,13 @@ using GroupedRing8 = Ring<4, 4, 3>;
 
 template <int BITS, bool ZP>
 struct TmaGeo {
-  static constexpr int BLK = BITS * 256;  // one 16 x 128 block
+  static constexpr int BLK = wna16_block_bytes(BITS);  // one 16 x 128 block
   static constexpr int W_STAGE = kStageGroups * BLK;
   static constexpr int S_STAGE = kStageGroups * 16 * 2;  // BF16 scales of 16 rows x 8 groups
   // asymmetric INT4: the same rows and groups of BF16 128 + z follow the scales
   static constexpr int STAGE = W_STAGE + S_STAGE * (ZP ? 2 : 1);
-  static constexpr bool FP = BITS == 8;  // E4M3 codes: no excess
-  static constexpr float BIAS = FP ? 0.f : 128.f + (1 << (BITS - 1));  // 128 + excess
+  static constexpr bool FP = Geo<BITS>::FP;  // values decoded as they are: no excess
+  static constexpr float BIAS = Geo<BITS>::BIAS;
 };
 
 template <int BITS, int MCH, class R, bool ZP>
@@ -1259,10 +1305,14 @@ __global__ void __launch_bounds__(R::THREADS, R::CTAS)
             if (gg < G) {
               const uint32_t blk = sbase + j * GE::BLK;
               uint32_t w[BITS == 8 ? 16 : 8];
-              if constexpr (BITS == 4) {
+              if constexpr (BITS == 4 || BITS == kBitsFp4) {
                 const uint4 v0 = lds128(blk + lane * 32), v1 = lds128(blk + lane * 32 + 16);
                 w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
                 w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+              } else if constexpr (BITS == 1) {
+                const uint2 v = lds64(blk + lane * 8);
+                w[0] = v.x; w[1] = v.y;
+                w[2] = w[3] = w[4] = w[5] = w[6] = w[7] = 0;
               } else if constexpr (BITS == 2) {
                 const uint4 v = lds128(blk + lane * 16);
                 w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
@@ -1455,6 +1505,8 @@ qw_status launch_dense_m8(const qw_packed_desc& d, const void* w_packed, const v
   }
   if (d.wfmt == QW_W_INT2_G128_BF16) return launch_m8_variant<2, false>(p, st);
   if (d.wfmt == QW_W_FP8E4M3_G128_BF16) return launch_m8_variant<8, false>(p, st);
+  if (d.wfmt == QW_W_INT1_G128_BF16) return launch_m8_variant<1, false>(p, st);
+  if (d.wfmt == QW_W_FP4E2M1_G128_BF16) return launch_m8_variant<kBitsFp4, false>(p, st);
   return d.wfmt == QW_W_INT4_G128_BF16 ? launch_m8_variant<4, false>(p, st)
                                        : launch_m8_variant<3, false>(p, st);
 }
@@ -1491,6 +1543,12 @@ qw_status launch_dense_reg(const qw_packed_desc& d, const void* w_packed, const 
   if (d.wfmt == QW_W_FP8E4M3_G128_BF16)
     return mch == 1 ? launch_reg_variant<8, 1, false>(p, items, st)
                     : launch_reg_variant<8, 2, false>(p, items, st);
+  if (d.wfmt == QW_W_INT1_G128_BF16)
+    return mch == 1 ? launch_reg_variant<1, 1, false>(p, items, st)
+                    : launch_reg_variant<1, 2, false>(p, items, st);
+  if (d.wfmt == QW_W_FP4E2M1_G128_BF16)
+    return mch == 1 ? launch_reg_variant<kBitsFp4, 1, false>(p, items, st)
+                    : launch_reg_variant<kBitsFp4, 2, false>(p, items, st);
   const bool int4 = d.wfmt == QW_W_INT4_G128_BF16;
   if (mch == 1)
     return int4 ? launch_reg_variant<4, 1, false>(p, items, st)
@@ -1528,9 +1586,13 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
   const bool int4 = d.wfmt == QW_W_INT4_G128_BF16 || zp;
   const bool int2 = d.wfmt == QW_W_INT2_G128_BF16;
   const bool fp8 = d.wfmt == QW_W_FP8E4M3_G128_BF16;
+  const bool int1 = d.wfmt == QW_W_INT1_G128_BF16;
+  const bool fp4 = d.wfmt == QW_W_FP4E2M1_G128_BF16;
   const int blk = int4 ? kInt4BlockBytes
                   : int2 ? kInt2BlockBytes
                   : fp8  ? kFp8BlockBytes
+                  : int1 ? kInt1BlockBytes
+                  : fp4  ? kFp4BlockBytes
                          : kInt3BlockBytes;
   const int G = d.K / kIntGroup;
   const int64_t nblocks = d.N_pad / 16;
@@ -1604,11 +1666,15 @@ qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const
            : int4 ? launch_tma_variant<4, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
            : int2 ? launch_tma_variant<2, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
            : fp8  ? launch_tma_variant<8, 1, GroupedRing8, false>(tmW, tmS, tmZ, p, size_items, st)
+           : int1 ? launch_tma_variant<1, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
+           : fp4  ? launch_tma_variant<kBitsFp4, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
                   : launch_tma_variant<3, 1, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st);
   return zp     ? launch_tma_variant<4, 2, GroupedRing, true>(tmW, tmS, tmZ, p, size_items, st)
          : int4 ? launch_tma_variant<4, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
          : int2 ? launch_tma_variant<2, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
          : fp8  ? launch_tma_variant<8, 2, GroupedRing8, false>(tmW, tmS, tmZ, p, size_items, st)
+         : int1 ? launch_tma_variant<1, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
+         : fp4  ? launch_tma_variant<kBitsFp4, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st)
                 : launch_tma_variant<3, 2, GroupedRing, false>(tmW, tmS, tmZ, p, size_items, st);
 }
 

@@ -34,15 +34,6 @@ namespace {
 constexpr int kW8Warps = 8;
 constexpr int kW8Ring = 16;  // scale groups per batch (two code words per group and lane)
 
-// the four bytes of `x` (two E2M1 codes each, first code in the low nibble) -> four FP16
-// pairs, d[i] from byte i (the bytes feed the conversions directly)
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t x, uint32_t (&d)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-      : "r"(x));
-}
 // two E8M0 scales (the low 16 bits of `pair`) -> 2^(s - 127) as a BF16 pair, exactly (the
 // smallest, 2^-127, is a BF16 subnormal)
 __device__ __forceinline__ uint32_t e8m0x2_to_bf16x2(uint32_t pair) {

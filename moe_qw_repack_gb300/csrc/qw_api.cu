@@ -121,6 +121,8 @@ qw_status qw_repack_query(int32_t wfmt_in, int32_t E, int32_t N, int32_t K, qw_p
     case QW_W_INT3_G128_BF16:
     case QW_W_INT2_G128_BF16:
     case QW_W_FP8E4M3_G128_BF16:
+    case QW_W_INT1_G128_BF16:
+    case QW_W_FP4E2M1_G128_BF16:
     case QW_W_UINT4ZP_G128_BF16: {
       if (K % kIntGroup) return QW_ERR_UNSUPPORTED;
       d.group = kIntGroup;
@@ -131,6 +133,8 @@ qw_status qw_repack_query(int32_t wfmt_in, int32_t E, int32_t N, int32_t K, qw_p
           (uint64_t)blocks * (wfmt == QW_W_INT3_G128_BF16   ? kInt3BlockBytes
                               : wfmt == QW_W_INT2_G128_BF16   ? kInt2BlockBytes
                               : wfmt == QW_W_FP8E4M3_G128_BF16 ? kFp8BlockBytes
+                              : wfmt == QW_W_INT1_G128_BF16    ? kInt1BlockBytes
+                              : wfmt == QW_W_FP4E2M1_G128_BF16 ? kFp4BlockBytes
                                                                : kInt4BlockBytes);
       // one BF16 plane of scales (UINT4ZP: a second plane of 128 + zero point)
       d.s_expert_stride = (uint64_t)round_up((int64_t)(K / kIntGroup) * d.N_pad * 2, 256) *

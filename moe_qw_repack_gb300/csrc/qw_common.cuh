@@ -2,7 +2,8 @@
 //
 // Inline-PTX wrappers for mbarrier, TMA (cp.async.bulk[.tensor]), tcgen05 (TMEM
 // allocation, MMA, copies, loads) and the bounded waits every spin in this library
-// goes through.  Nothing here is format arithmetic.
+// goes through, plus the few element decodes several kernels share (hardware E4M3 / E2M1
+// conversions, INT1 sign pairs).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -255,6 +256,34 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t pair) {
   const float hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
   __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// The four bytes of `x` (two E2M1 codes each, the first in the low nibble) -> four FP16
+// pairs, d[i] from byte i.  Every E2M1 value is an FP16 number: exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t x, uint32_t (&d)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+      : "r"(x));
+}
+
+// FP16 pair -> BF16 pair of the same values; exact for values BF16 holds (every E2M1 and
+// E4M3 value: at most 4 significant bits, exponents -9 .. 8).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// INT1 sign codes: bits p and 16 + p of `w` (bit b = weight 2b - 1) -> the pair (+-1, +-1)
+// with sign = not b, in the 16-bit float whose 1.0 is `one2` (BF16 0x3F80 or FP16 0x3C00,
+// both halves): one shift moves the two bits to the sign positions, one logic op does the
+// rest.
+__device__ __forceinline__ uint32_t int1_pair(uint32_t w, int p, uint32_t one2) {
+  const uint32_t x = w << (15 - p);
+  return (~x & 0x80008000u) | one2;
 }
 
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0; }

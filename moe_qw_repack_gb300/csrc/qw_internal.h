@@ -18,6 +18,15 @@ constexpr int kInt4BlockBytes = 1024;  // 16 rows x 128 k of INT4, fragment orde
 constexpr int kInt2BlockBytes = 512;   // 16 rows x 128 k of INT2, fragment order
 constexpr int kInt3BlockBytes = 768;   // 16 rows x 128 k of INT3 (two bit planes)
 constexpr int kFp8BlockBytes = 2048;   // 16 rows x 128 k of E4M3 codes, fragment order
+constexpr int kInt1BlockBytes = 256;   // 16 rows x 128 k of INT1 sign bits, fragment order
+constexpr int kFp4BlockBytes = 1024;   // 16 rows x 128 k of E2M1 codes, fragment order
+// Format codes of the WnA16 kernels' templates: the integer bit width (4, 3, 2, 1), 8 for
+// E4M3 weights and kBitsFp4 for E2M1 weights (FP4 codes in the INT4 block geometry).
+constexpr int kBitsFp4 = 5;
+// Bytes of one packed 16 x 128 block of a WnA16 format code.
+__host__ __device__ constexpr int wna16_block_bytes(int bits) {
+  return bits == kBitsFp4 ? kFp4BlockBytes : bits * 256;
+}
 constexpr int kSfChunkBytes = 512;     // 128 rows x 4 groups of E8M0 scales
 constexpr int kNvGroup = 16;           // K elements per E4M3 scale (NVFP4)
 constexpr int kNvChunkBytes = 2048;    // 128 rows x 16 groups of E4M3 scales (NVFP4)

@@ -340,6 +340,119 @@ __global__ void unpack_fp8w_kernel(const uint32_t* __restrict__ wp, uint32_t* __
   }
 }
 
+// ----------------------------------------------------------------------------- INT1
+// Packed INT1 (sign codes, bit b = weight 2b - 1): 256-byte blocks of 32 lanes x 2 words.
+// Register r of MMA step s (rows g + 8 (r & 1), k = 16s + 4t + 2 (r >> 1) + h) keeps its two
+// bits at bit 4 (s % 4) + r + 16h of word s / 4: one shift moves both to the sign positions
+// 15 and 31 of a BF16 (or FP16) pair.
+__global__ void repack_int1_kernel(const uint32_t* __restrict__ wc, uint32_t* __restrict__ wp,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K) {
+  const int64_t per_expert = (int64_t)(K / 128) * (N_pad / 16) * 64;  // words
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t blk = rem / 64;
+    const int w = (int)(rem % 64);
+    const int lane = w >> 1, half = w & 1;  // word `half` holds steps 4 half .. 4 half + 3
+    const int G = (int)(blk / (N_pad / 16));
+    const int nb = (int)(blk % (N_pad / 16));
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t* wce = wc + e * (int64_t)N * (K / 32);
+    uint32_t out = 0;
+    for (int s4 = 0; s4 < 4; ++s4)
+      for (int r = 0; r < 4; ++r)
+        for (int h = 0; h < 2; ++h) {
+          const int s = 4 * half + s4;
+          const int64_t n = (int64_t)nb * 16 + g + 8 * (r & 1);
+          const int k = G * 128 + 16 * s + 4 * t + 2 * (r >> 1) + h;
+          // padding rows: bit 0 (weight -1 times a zero scale)
+          const uint32_t b = n < N ? (wce[n * (K / 32) + k / 32] >> (k % 32)) & 1u : 0u;
+          out |= b << (4 * s4 + r + 16 * h);
+        }
+    wp[idx] = out;
+  }
+}
+
+__global__ void unpack_int1_kernel(const uint32_t* __restrict__ wp, uint32_t* __restrict__ wc,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K) {
+  // one thread per canonical word (32 consecutive k of one row)
+  const int64_t per_expert = (int64_t)N * (K / 32);
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t n = rem / (K / 32);
+    const int k0 = (int)(rem % (K / 32)) * 32;
+    const uint32_t* wpe = wp + e * (int64_t)(K / 128) * (N_pad / 16) * 64;
+    uint32_t out = 0;
+    for (int j = 0; j < 32; ++j) {
+      const int k = k0 + j;
+      const int G = k / 128, kk = k % 128;
+      const int nb = (int)(n / 16), row = (int)(n % 16);
+      const int g = row & 7, t = (kk >> 2) & 3, s = kk >> 4, h = kk & 1;
+      const int r = (row >> 3) | (((kk >> 1) & 1) << 1);
+      const uint32_t W = wpe[((int64_t)G * (N_pad / 16) + nb) * 64 + (g * 4 + t) * 2 + s / 4];
+      out |= ((W >> (4 * (s % 4) + r + 16 * h)) & 1u) << j;
+    }
+    wc[idx] = out;
+  }
+}
+
+// ----------------------------------------------------------------------------- FP4 weights
+// Packed FP4 (E2M1) weights: the INT4 block of 1 KiB (32 lanes x 8 words, word s = MMA step
+// s), but byte r of a word holds register r - the codes at k = 16s + 4t + 2 (r >> 1) and
+// k + 1 of row g + 8 (r & 1), the first in the low nibble - so one hardware conversion
+// (cvt.rn.f16x2.e2m1x2) turns a byte into the register's FP16 pair.  Every code is valid.
+__global__ void repack_fp4w_kernel(const uint8_t* __restrict__ wc, uint32_t* __restrict__ wp,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K) {
+  const int64_t per_expert = (int64_t)(K / 128) * (N_pad / 16) * 256;  // words
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t blk = rem / 256;
+    const int w = (int)(rem % 256);
+    const int lane = w / 8, s = w % 8;
+    const int G = (int)(blk / (N_pad / 16));
+    const int nb = (int)(blk % (N_pad / 16));
+    const int g = lane >> 2, t = lane & 3;
+    const uint8_t* wce = wc + e * (int64_t)N * (K / 2);
+    uint32_t out = 0;
+    for (int r = 0; r < 4; ++r) {
+      const int64_t n = (int64_t)nb * 16 + g + 8 * (r & 1);
+      const int k = G * 128 + 16 * s + 4 * t + 2 * (r >> 1);  // even: one canonical byte
+      const uint32_t byte = n < N ? wce[n * (K / 2) + k / 2] : 0u;  // padding rows: 0
+      out |= byte << (8 * r);
+    }
+    wp[idx] = out;
+  }
+}
+
+__global__ void unpack_fp4w_kernel(const uint32_t* __restrict__ wp, uint8_t* __restrict__ wc,
+                                   int32_t E, int32_t N, int32_t N_pad, int32_t K) {
+  // one thread per canonical byte (k, k + 1 of one row, k even)
+  const int64_t per_expert = (int64_t)N * (K / 2);
+  const int64_t total = per_expert * E;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = idx / per_expert;
+    const int64_t rem = idx % per_expert;
+    const int64_t n = rem / (K / 2);
+    const int k = (int)(rem % (K / 2)) * 2;
+    const uint32_t* wpe = wp + e * (int64_t)(K / 128) * (N_pad / 16) * 256;
+    const int G = k / 128, kk = k % 128;
+    const int nb = (int)(n / 16), row = (int)(n % 16);
+    const int g = row & 7, t = (kk >> 2) & 3, s = kk >> 4;
+    const int r = (row >> 3) | (((kk >> 1) & 1) << 1);
+    const uint32_t W = wpe[((int64_t)G * (N_pad / 16) + nb) * 256 + (g * 4 + t) * 8 + s];
+    wc[idx] = (uint8_t)((W >> (8 * r)) & 0xFFu);
+  }
+}
+
 // ----------------------------------------------------------------------------- second-level scales
 // FP32 [E][N] <-> the packed plane [E][N_pad] (padding channels 0; a non-finite t is a value
 // error, packed as 0).
@@ -681,6 +794,20 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
                                                         d.K, err);
       break;
     }
+    case QW_W_INT1_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 64;
+      repack_int1_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_canon,
+                                                        (uint32_t*)w_packed, d.E, d.N, d.N_pad,
+                                                        d.K);
+      break;
+    }
+    case QW_W_FP4E2M1_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 256;
+      repack_fp4w_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint8_t*)w_canon,
+                                                        (uint32_t*)w_packed, d.E, d.N, d.N_pad,
+                                                        d.K);
+      break;
+    }
     case QW_W_INT3_G128_BF16: {
       const int64_t tw = (int64_t)d.E * (d.K / 128) * (d.N_pad / 16) * 32;
       repack_int3_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_canon,
@@ -717,7 +844,8 @@ qw_status launch_repack(const qw_packed_desc& d, const void* w_canon, const void
       return QW_ERR_UNSUPPORTED;
   }
   if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16 ||
-      d.wfmt == QW_W_INT2_G128_BF16 || d.wfmt == QW_W_FP8E4M3_G128_BF16) {
+      d.wfmt == QW_W_INT2_G128_BF16 || d.wfmt == QW_W_FP8E4M3_G128_BF16 ||
+      d.wfmt == QW_W_INT1_G128_BF16 || d.wfmt == QW_W_FP4E2M1_G128_BF16) {
     const int64_t ts = (int64_t)d.E * (d.K / 128) * d.N_pad;
     repack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
         (const uint16_t*)s_canon, (uint16_t*)s_packed, d.E, d.N, d.N_pad, d.K / 128,
@@ -761,6 +889,20 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
                                                         d.K);
       break;
     }
+    case QW_W_INT1_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * d.N * (d.K / 32);
+      unpack_int1_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_packed,
+                                                        (uint32_t*)w_canon, d.E, d.N, d.N_pad,
+                                                        d.K);
+      break;
+    }
+    case QW_W_FP4E2M1_G128_BF16: {
+      const int64_t tw = (int64_t)d.E * d.N * (d.K / 2);
+      unpack_fp4w_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_packed,
+                                                        (uint8_t*)w_canon, d.E, d.N, d.N_pad,
+                                                        d.K);
+      break;
+    }
     case QW_W_INT3_G128_BF16: {
       const int64_t tw = (int64_t)d.E * d.N * (d.K / 32);
       unpack_int3_kernel<<<grid_for(tw, T), T, 0, st>>>((const uint32_t*)w_packed,
@@ -797,7 +939,8 @@ qw_status launch_unpack(const qw_packed_desc& d, const void* w_packed, const voi
       return QW_ERR_UNSUPPORTED;
   }
   if (d.wfmt == QW_W_INT4_G128_BF16 || d.wfmt == QW_W_INT3_G128_BF16 ||
-      d.wfmt == QW_W_INT2_G128_BF16 || d.wfmt == QW_W_FP8E4M3_G128_BF16) {
+      d.wfmt == QW_W_INT2_G128_BF16 || d.wfmt == QW_W_FP8E4M3_G128_BF16 ||
+      d.wfmt == QW_W_INT1_G128_BF16 || d.wfmt == QW_W_FP4E2M1_G128_BF16) {
     const int64_t ts = (int64_t)d.E * d.N * (d.K / 128);
     unpack_int_scales_kernel<<<grid_for(ts, T), T, 0, st>>>(
         (const uint16_t*)s_packed, (uint16_t*)s_canon, d.E, d.N, d.N_pad, d.K / 128,

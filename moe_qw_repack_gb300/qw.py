@@ -32,6 +32,8 @@ QW_W_NVFP4_G16 = 4
 QW_W_UINT4ZP_G128_BF16 = 5
 QW_W_INT2_G128_BF16 = 6
 QW_W_FP8E4M3_G128_BF16 = 7
+QW_W_INT1_G128_BF16 = 8
+QW_W_FP4E2M1_G128_BF16 = 9
 QW_W_SCALE2 = 0x100  # flag: second-level FP32 scale per output channel (and expert)
 QW_A_BF16 = 0
 QW_A_MXFP8_G32 = 1

@@ -70,6 +70,8 @@ def test_status_strings(Q):
     (2, 640, 96, 640, 128, 640 * 64, 640 * 4),
     (7, 14336, 4096, 14336, 4096, 14336 * 4096, 14336 * 32 * 2),  # E4M3: one byte per weight
     (7, 40, 384, 48, 384, 48 * 384, 512),
+    (8, 40, 384, 48, 384, 48 * 384 // 8, 512),  # INT1: one bit per weight
+    (9, 14336, 4096, 14336, 4096, 14336 * 4096 // 2, 14336 * 32 * 2),  # E2M1: half a byte
 ])
 def test_repack_query_sizes(Q, wfmt, N, K, npad, kpad, wb, sb):
     d = Q.qw_repack_query(wfmt, 1, N, K)
@@ -77,8 +79,8 @@ def test_repack_query_sizes(Q, wfmt, N, K, npad, kpad, wb, sb):
 
 
 def test_repack_query_rejects(Q):
-    for args in [(0, 1, 16, 100), (1, 1, 16, 64), (2, 1, 16, 48), (9, 1, 16, 128), (0, 0, 16, 128),
-                 (0, 1, 0, 128), (7, 1, 16, 64)]:
+    for args in [(0, 1, 16, 100), (1, 1, 16, 64), (2, 1, 16, 48), (10, 1, 16, 128), (0, 0, 16, 128),
+                 (0, 1, 0, 128), (7, 1, 16, 64), (8, 1, 16, 96), (9, 1, 16, 64)]:
         with pytest.raises(Q.QwError):
             Q.qw_repack_query(*args)
 
