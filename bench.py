@@ -316,16 +316,25 @@ def extra_w4a16(steps, warmup, world, only=None):
     for bits in (4, 3):
         for (N, K) in [(14336, 4096), (4096, 14336), (4096, 4096)]:
             cases.append((f"cfg3_m1_{N}x{K}_int{bits}", 1, N, K, bits))
-    cases.append(("m1_14336x4096_int2", 1, 14336, 4096, 2))  # INT2 WnA16 (no workload of its own)
+    # WnA16 formats with no workload of their own, on the first decode shape
+    cases.append(("m1_14336x4096_int2", 1, 14336, 4096, 2))
+    cases.append(("m1_14336x4096_int1", 1, 14336, 4096, 1))
+    cases.append(("m1_14336x4096_fp4", 1, 14336, 4096, "fp4"))
     for name, M, N, K, bits in cases:
         if only and only not in name:
             continue
-        p = synth.w4a16_problem(M, N, K, bits=bits, cfg_id=0 if M == 8 else 2)
-        wfmt = {4: Q.QW_W_INT4_G128_BF16, 3: Q.QW_W_INT3_G128_BF16, 2: Q.QW_W_INT2_G128_BF16}[bits]
+        if bits == "fp4":
+            p = synth.fp4w_problem(M, N, K, cfg_id=2)
+            wfmt, wbits = Q.QW_W_FP4E2M1_G128_BF16, 4
+        else:
+            p = synth.w4a16_problem(M, N, K, bits=bits, cfg_id=0 if M == 8 else 2)
+            wfmt = {4: Q.QW_W_INT4_G128_BF16, 3: Q.QW_W_INT3_G128_BF16,
+                    2: Q.QW_W_INT2_G128_BF16, 1: Q.QW_W_INT1_G128_BF16}[bits]
+            wbits = bits
         d = Q.qw_repack_query(wfmt, 1, N, K)
         wp, sp = Q.empty_packed(d)
         Q.qw_repack(d, torch.from_numpy(p["w_canon"]).cuda(), torch.from_numpy(p["s_canon"]).cuda(), wp, sp)
-        wbytes = N * K * bits / 8 + N * (K // 128) * 2  # packed weights + BF16 scales
+        wbytes = N * K * wbits / 8 + N * (K // 128) * 2  # packed weights + BF16 scales
         R = replicas_for(wp.numel() + sp.numel())
         copies = [(wp, sp)] + [(wp.clone(), sp.clone()) for _ in range(R - 1)]
         A = torch.from_numpy(p["A"].view(np.int16)).cuda()

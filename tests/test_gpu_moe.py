@@ -257,3 +257,43 @@ def test_grouped_gemv_reads_the_tile_queue_of_this_call(T):
         assert not np.any(got == 0x7FC0), "rows left unwritten"
         ok, ratio, frob = OQ.check_bf16_result(got, R, S)
         assert ok, (ratio, frob)
+
+
+@pytest.mark.parametrize("bits", [4, 3, 1])
+def test_grouped_decode_bias_scale2_ragged(bits):
+    """Grouped calls of a few rows per expert (the grouped decode kernel): ragged N, tiles
+    shorter than 8 rows, a bias per expert and second-level scales per expert and channel."""
+    Q = qw()
+    E, T, k, K, N = 16, 6, 4, 1024, 264
+    p = synth.w4a16_problem(T, N, K, bits=bits, E=E, cfg_id=1200 + bits, bias=True)
+    logits = synth.router_logits(T, E, cfg_id=1201)
+    wfmt = {4: Q.QW_W_INT4_G128_BF16, 3: Q.QW_W_INT3_G128_BF16,
+            1: Q.QW_W_INT1_G128_BF16}[bits] | Q.QW_W_SCALE2
+    d, wp, sp_ = repack(wfmt, E, N, K, p["w_canon"], p["s_canon"])
+    rng = np.random.default_rng(1202)
+    t = (2.0 ** rng.integers(-2, 3, (E, N))).astype(np.float32)
+    err = Q.new_error_flag()
+    Q.qw_repack_scale2(d, dev(t), sp_, err)
+    ids, spairs, off = route(logits, k)
+    P = T * k
+    A = dev(p["A"].view(np.int16))
+    As = torch.empty((P, K), dtype=torch.int16, device="cuda")
+    sp_dev, off_dev = dev(spairs.astype(np.int32)), dev(off.astype(np.int32))
+    Q.qgemm_moe_permute(Q.QW_A_BF16, A, None, K, sp_dev, P, k, As, None)
+    C = torch.full((P, N), -1, dtype=torch.int16, device="cuda")
+    wsn = Q.qgemm_workspace_size(d, Q.QW_A_BF16, P)
+    ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
+    Q.qgemm_moe_grouped(d, wp, sp_, Q.QW_A_BF16, As, None, off_dev, P,
+                        dev(p["bias"].view(np.int16)), C, ws, wsn, err)
+    assert Q.qw_read_error(err) == 0
+    tok = spairs // k
+    e_of = np.searchsorted(off, np.arange(P), side="right") - 1
+    Cn = u16_view(C)
+    Rall, Sall = np.zeros((P, N)), np.zeros((P, N))
+    for e in np.unique(e_of):
+        sel = np.nonzero(e_of == e)[0]
+        R, S = OQ.w4a16_from_canonical(p["A"][tok[sel]], p["w_canon"][e], p["s_canon"][e], K,
+                                       bits)
+        Rall[sel], Sall[sel] = OQ.apply_scale2(R, S, t[e], p["bias"][e])
+    ok, ratio, frob = OQ.check_bf16_result(Cn, Rall, Sall)
+    assert ok, (ratio, frob)
