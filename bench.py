@@ -513,7 +513,7 @@ def extra_w8a8(steps, warmup, world):
                                            "input_copies": R, "steps": n}}
 
 
-def extra_moe(steps, warmup, world, only=None):
+def extra_moe(steps, warmup, world, only=None, scale=1):
     """Grouped MoE workloads: W4A8 (E=256, top-8, T=4096, 7168 -> 4096) and the W4A16
     intermediate-640 token sweep (E=128, top-8, up 4096 -> 1280 plus down 640 -> 4096).
     One step = route + permute + grouped GEMM(s) (+ for W4A16 the SiLU*mul between the
@@ -530,9 +530,11 @@ def extra_moe(steps, warmup, world, only=None):
         tot, n, graph = time_region(fns, n_steps, warmup, world, graph_steps=graph_steps)
         each = [time_region([f], n_steps, 1, world, graph_steps=graph_steps)[0] for f in fns]
         return tot, each, n, graph
-    # -- W4A8, E=256 (the active experts' weights alone are ~2.4 GB per step)
-    E, T, K, N, k = 256, 4096, 7168, 4096, 8
-    if only and only not in "cfg4_moe_w4a8_E256_T4096":
+    # -- W4A8, E=256 (the active experts' weights alone are ~2.4 GB per step); `scale`
+    # divides E and T (a smaller case of the same kernels for profiler captures)
+    E, T, K, N, k = 256 // scale, 4096 // scale, 7168, 4096, 8
+    name4 = f"cfg4_moe_w4a8_E{E}_T{T}"
+    if only and only not in name4:
         return _extra_moe_w4a16(steps, warmup, world, only, parts, out, peaks)
     r = moe_pipeline(Q.QW_A_MXFP8_G32, Q.QW_W_MXFP4_G32, E, T, K, N, k, cfg_id=3)
     tot, each, n, graph = parts([r["route"], r["permute"], r["gemm"]], steps, 4)
@@ -548,7 +550,7 @@ def extra_moe(steps, warmup, world, only=None):
     flop = 2.0 * P * N * K
     gemm_ms = each[2]
     wbytes = active * (N * K // 2 + N * K // 32)
-    out["cfg4_moe_w4a8_E256_T4096"] = {
+    out[name4] = {
         "us_total": round(tot * 1e3, 1), "us_route": round(each[0] * 1e3, 1),
         "us_permute": round(each[1] * 1e3, 1), "us_gemm": round(gemm_ms * 1e3, 1),
         "gemm_tflops": round(flop / (gemm_ms * 1e-3) / 1e12, 1),
@@ -566,7 +568,7 @@ def extra_moe(steps, warmup, world, only=None):
                        world, graph_steps=4)[0]
     assert Q.qw_read_error(qerr) == 0
     qbytes = T * K * 2 + T * K + T * K // 32
-    out["cfg4_moe_w4a8_E256_T4096"].update({
+    out[name4].update({
         "us_quantize_bf16_to_mxfp8": round(q_ms * 1e3, 1),
         "quantize_frac_hbm": round(qbytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)})
     del r, xa, qa, qsf
@@ -844,6 +846,9 @@ def main():
                     help="time only the grouped MoE workloads (a profiling aid)")
     ap.add_argument("--only-fp8w", action="store_true",
                     help="time only the FP8-weight WnA16 workloads (a profiling aid)")
+    ap.add_argument("--moe-scale", type=int, default=1,
+                    help="with --only-moe: divide the E=256 W4A8 workload's experts and tokens "
+                         "by this (a smaller case for profiler captures)")
     ap.add_argument("--case", default=None,
                     help="with --only-w4a16 / --only-moe / --only-fp8w: run only the cases "
                          "whose name contains this string")
@@ -861,7 +866,7 @@ def main():
         line = {"extra": extra_w4a16(args.steps, args.warmup, world, args.case)}
     elif args.only_moe:
         world, rank, _ = dist_setup()
-        line = {"extra": extra_moe(args.steps, args.warmup, world, args.case)}
+        line = {"extra": extra_moe(args.steps, args.warmup, world, args.case, args.moe_scale)}
     elif args.only_fp8w:
         world, rank, _ = dist_setup()
         line = {"extra": extra_fp8w(args.steps, args.warmup, world, args.case)}

@@ -45,7 +45,9 @@ def test_config4_moe_w4a8_full_size():
     off, sp = host(r["offsets"]), host(r["sorted_pairs"])
     _, _, roff, rsp = OM.route(r["logits"], k)
     assert np.array_equal(off, roff) and np.array_equal(sp, rsp)
-    rows = sample_rows_per_expert(off, per_expert=3, max_experts=24, seed=1)
+    # every active expert, its first and last row (and a middle one)
+    rows = sample_rows_per_expert(off, per_expert=3, max_experts=None, seed=1)
+    assert np.unique(_expert_of(off, rows)).size == np.count_nonzero(np.diff(off))
     cols = _cols(N, 2)
     tok = sp[rows] // k
     A, Asf = host(r["A"])[tok], host(r["A_sf"])[tok]
@@ -99,7 +101,7 @@ def test_config5_moe_w4a16_up_projection(T):
     _w4a16_case(T, up=True)
 
 
-@pytest.mark.parametrize("T", [1, 256, 8192])
+@pytest.mark.parametrize("T", [1, 16, 256, 2048, 8192])
 def test_config5_moe_w4a16_down_projection(T):
     """Down projection 640 -> 4096 (K not a multiple of 256) on a per-pair input."""
     _w4a16_case(T, up=False)
