@@ -1562,7 +1562,9 @@ qw_status launch_dense_reg(const qw_packed_desc& d, const void* w_packed, const 
 uint64_t gemv_w4a16_workspace(const qw_packed_desc& d, int64_t max_rows) {
   // only grouped calls need device memory of their own: the tile queue
   if (d.E <= 1) return 0;
-  return tile_queue_bytes(d.E, max_rows, 8 * mch_for(d, max_rows, true));
+  // the tile rows shrink with the rows of a call: size the queue for the smallest tile, so
+  // that it holds every call of at most max_rows rows
+  return tile_queue_bytes(d.E, max_rows, 8);
 }
 
 qw_status launch_gemv_w4a16(const qw_packed_desc& d, const void* w_packed, const void* s_packed,

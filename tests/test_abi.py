@@ -242,3 +242,19 @@ def test_stream_read_validates_on_the_host(Q):
     assert Q.LIB.qw_stream_read(fake, 64, None, 0, None) == Q.QW_ERR_INVALID_ARG
     assert Q.LIB.qw_stream_read(fake, 40, fake, 0, None) == Q.QW_ERR_ALIGNMENT
     assert Q.LIB.qw_stream_read(fake + 8, 64, fake, 0, None) == Q.QW_ERR_ALIGNMENT
+
+
+def test_grouped_workspace_covers_every_smaller_call(Q):
+    """A workspace sized for max_rows serves every grouped call of at most max_rows rows:
+    the size never decreases as max_rows grows, across the switches of the GEMV's token
+    tile (8 -> 16 rows at 8 rows per expert) and of the tensor-core path (16 rows per
+    expert), for the W4A16 and W4A8 formats."""
+    for wfmt, afmt in ((Q.QW_W_INT4_G128_BF16, Q.QW_A_BF16), (Q.QW_W_INT3_G128_BF16, Q.QW_A_BF16),
+                       (Q.QW_W_MXFP4_G32, Q.QW_A_MXFP8_G32)):
+        for E in (8, 128):
+            d = Q.qw_repack_query(wfmt, E, 1280, 4096)
+            prev = 0
+            for rows in range(0, 40 * E + 1, max(1, E // 16)):
+                n = Q.qgemm_workspace_size(d, afmt, rows)
+                assert n >= prev, (wfmt, E, rows, n, prev)
+                prev = n

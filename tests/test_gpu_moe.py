@@ -297,3 +297,49 @@ def test_grouped_decode_bias_scale2_ragged(bits):
         Rall[sel], Sall[sel] = OQ.apply_scale2(R, S, t[e], p["bias"][e])
     ok, ratio, frob = OQ.check_bf16_result(Cn, Rall, Sall)
     assert ok, (ratio, frob)
+
+
+@pytest.mark.parametrize("T", [80, 160, 240])
+@pytest.mark.parametrize("bits", [4, 3, 2, 1])
+def test_grouped_wide_token_tiles_bias_scale2_ragged(T, bits):
+    """Grouped calls of 10 to 30 rows per expert on average (E=16, top-2): T=80 runs the
+    grouped GEMV (16-row tiles), T=160 and 240 the tcgen05 path with partly filled 128-token
+    tiles.  Expert 0 takes every token (its logit is raised), so it spans several tiles;
+    ragged N, K of ten groups (a partial second stage), a bias per expert and second-level
+    scales."""
+    Q = qw()
+    E, k, K, N = 16, 2, 1280, 264
+    p = synth.w4a16_problem(T, N, K, bits=bits, E=E, cfg_id=1300 + bits, bias=True)
+    logits = synth.router_logits(T, E, cfg_id=1301 + T)
+    logits[:, 0] += 100.0
+    wfmt = {4: Q.QW_W_INT4_G128_BF16, 3: Q.QW_W_INT3_G128_BF16, 2: Q.QW_W_INT2_G128_BF16,
+            1: Q.QW_W_INT1_G128_BF16}[bits] | Q.QW_W_SCALE2
+    d, wp, sp_ = repack(wfmt, E, N, K, p["w_canon"], p["s_canon"])
+    rng = np.random.default_rng(1302)
+    t = (2.0 ** rng.integers(-2, 3, (E, N))).astype(np.float32)
+    err = Q.new_error_flag()
+    Q.qw_repack_scale2(d, dev(t), sp_, err)
+    ids, spairs, off = route(logits, k)
+    P = T * k
+    assert off[1] - off[0] == T
+    A = dev(p["A"].view(np.int16))
+    As = torch.empty((P, K), dtype=torch.int16, device="cuda")
+    sp_dev, off_dev = dev(spairs.astype(np.int32)), dev(off.astype(np.int32))
+    Q.qgemm_moe_permute(Q.QW_A_BF16, A, None, K, sp_dev, P, k, As, None)
+    C = torch.full((P, N), -1, dtype=torch.int16, device="cuda")
+    wsn = Q.qgemm_workspace_size(d, Q.QW_A_BF16, P)
+    ws = torch.zeros(max(wsn, 16), dtype=torch.uint8, device="cuda")
+    Q.qgemm_moe_grouped(d, wp, sp_, Q.QW_A_BF16, As, None, off_dev, P,
+                        dev(p["bias"].view(np.int16)), C, ws, wsn, err)
+    assert Q.qw_read_error(err) == 0
+    tok = spairs // k
+    e_of = np.searchsorted(off, np.arange(P), side="right") - 1
+    Cn = u16_view(C)
+    Rall, Sall = np.zeros((P, N)), np.zeros((P, N))
+    for e in np.unique(e_of):
+        sel = np.nonzero(e_of == e)[0]
+        R, S = OQ.w4a16_from_canonical(p["A"][tok[sel]], p["w_canon"][e], p["s_canon"][e], K,
+                                       bits)
+        Rall[sel], Sall[sel] = OQ.apply_scale2(R, S, t[e], p["bias"][e])
+    ok, ratio, frob = OQ.check_bf16_result(Cn, Rall, Sall)
+    assert ok, (ratio, frob)
