@@ -218,6 +218,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the next kernel may start its own set-up on SMs this grid has left
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -241,6 +243,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // Launched as a programmatic dependent: the set-up above overlaps the previous kernel's
+  // tail; every global access (tile queue, operands, scales, bias, output) comes after this.
+  pdl_wait();
 
   const int64_t num_m = p.queue ? (int64_t)__ldg(p.queue) : (int64_t)p.num_m_tiles;
   const int64_t num_tiles = num_m * p.num_n_tiles;
@@ -573,8 +578,8 @@ qw_status launch_bits(const CUtensorMap& tmA, const CUtensorMap& tmC, const Para
   if (attr != cudaSuccess) return QW_ERR_CUDA;
   const int sms = device_sm_count();
   const unsigned grid = (unsigned)(tiles_max < sms ? (tiles_max < 1 ? 1 : tiles_max) : sms);
-  gemm_w4a16_tc_kernel<BITS, ZP><<<grid, NUM_THREADS, smem, st>>>(tmA, tmC, p);
-  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+  return launch_pdl(gemm_w4a16_tc_kernel<BITS, ZP>, dim3(grid), dim3(NUM_THREADS), smem, st, tmA,
+                    tmC, p);
 }
 
 }  // namespace

@@ -229,6 +229,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the next kernel may start its own set-up on SMs this grid has left
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -257,6 +259,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // Launched as a programmatic dependent: the set-up above overlaps the previous kernel's
+  // tail; every global access (tile queue, operands, scales, bias, output) comes after this.
+  pdl_wait();
 
   const int64_t num_m = p.queue ? (int64_t)__ldg(p.queue) : (int64_t)p.num_m_tiles;
   const int64_t num_tiles = num_m * p.num_n_tiles;
@@ -711,12 +716,13 @@ qw_status launch_gemm_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   const int sms = device_sm_count();
   const unsigned grid = (unsigned)(tiles_max < sms ? (tiles_max < 1 ? 1 : tiles_max) : sms);
   if (w8)
-    gemm_w4a8_kernel<kW8A8><<<grid, NUM_THREADS, KT<kW8A8>::SMEM_BYTES, st>>>(tmA, tmB, p);
-  else if (nv)
-    gemm_w4a8_kernel<kW4A4><<<grid, NUM_THREADS, KT<kW4A4>::SMEM_BYTES, st>>>(tmA, tmB, p);
-  else
-    gemm_w4a8_kernel<kW4A8><<<grid, NUM_THREADS, KT<kW4A8>::SMEM_BYTES, st>>>(tmA, tmB, p);
-  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+    return launch_pdl(gemm_w4a8_kernel<kW8A8>, dim3(grid), dim3(NUM_THREADS),
+                      KT<kW8A8>::SMEM_BYTES, st, tmA, tmB, p);
+  if (nv)
+    return launch_pdl(gemm_w4a8_kernel<kW4A4>, dim3(grid), dim3(NUM_THREADS),
+                      KT<kW4A4>::SMEM_BYTES, st, tmA, tmB, p);
+  return launch_pdl(gemm_w4a8_kernel<kW4A8>, dim3(grid), dim3(NUM_THREADS),
+                    KT<kW4A8>::SMEM_BYTES, st, tmA, tmB, p);
 }
 
 }  // namespace qw
