@@ -258,3 +258,22 @@ def test_grouped_workspace_covers_every_smaller_call(Q):
                 n = Q.qgemm_workspace_size(d, afmt, rows)
                 assert n >= prev, (wfmt, E, rows, n, prev)
                 prev = n
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """No fallback: with the shared library absent, importing the binding raises ImportError
+    naming the missing file (run in a fresh interpreter so this process keeps its library)."""
+    import subprocess
+    import sys
+    missing = tmp_path / "libqw.so"
+    code = ("import moe_qw_repack_gb300.build as b; b.LIB = %r\n"
+            "try:\n"
+            "    import moe_qw_repack_gb300.qw\n"
+            "except ImportError as e:\n"
+            "    print('IMPORT-ERROR', e)\n"
+            "else:\n"
+            "    print('LOADED')\n" % str(missing))
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=300)
+    assert "IMPORT-ERROR" in r.stdout and str(missing) in r.stdout, r.stdout + r.stderr
