@@ -513,6 +513,28 @@ def extra_w8a8(steps, warmup, world):
                                            "input_copies": R, "steps": n}}
 
 
+MMA_PROBES = (  # (name, mode, N, FLOP per MMA): the instruction forms the GEMMs issue
+    ("f16_tmem_a_n128", 0, 128, 2 * 128 * 128 * 16),   # W4A16 tcgen05 GEMM
+    ("f16_smem_n256", 1, 256, 2 * 128 * 256 * 16),
+    ("mxf8f6f4_n256", 2, 256, 2 * 128 * 256 * 32),     # W4A8 GEMM, MMAs only
+    ("mxf8f6f4_cp_n256", 3, 256, 2 * 128 * 256 * 32),  # ... with its scale copies
+)
+
+
+def extra_mma_rate(iters=4096):
+    """The tcgen05 MMA issue rate (qw_mma_rate_probe): per instruction form, the median over
+    SMs of cycles and ns per MMA, and the TF/s ceiling that rate gives on all SMs."""
+    import moe_qw_repack_gb300.qw as Q
+    out = {}
+    for name, mode, n, flop in MMA_PROBES:
+        cyc, ns = Q.mma_rate(mode, n, iters)
+        c, t = float(np.median(cyc)), float(np.median(ns))
+        out[name] = {"cycles_per_mma": round(c, 1), "ns_per_mma": round(t, 2),
+                     "sm_ghz": round(c / t, 3), "sms": int(cyc.size),
+                     "ceiling_tflops": round(flop * cyc.size / t / 1e3, 1)}
+    return {"mma_rate": out}
+
+
 def extra_moe(steps, warmup, world, only=None, scale=1):
     """Grouped MoE workloads: W4A8 (E=256, top-8, T=4096, 7168 -> 4096) and the W4A16
     intermediate-640 token sweep (E=128, top-8, up 4096 -> 1280 plus down 640 -> 4096).
@@ -724,6 +746,7 @@ def run_ours(args, world, rank):
         line["extra"].update(extra_w4a8_decode(max(5, min(args.steps, 200)), 3, world))
         line["extra"].update(extra_fp8w(max(5, min(args.steps, 200)), 3, world))
         line["extra"].update(extra_moe(max(5, min(args.steps, 40)), 3, world))
+        line["extra"].update(extra_mma_rate())
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     line["summary"] = summarize(line)  # last key: every configured workload's fraction
@@ -754,6 +777,14 @@ def summarize(line):
     sm["cfg5_tflops"] = {t: get(f"cfg5_moe_w4a16_E128_T{t}", "gemm_tflops") for t in (2048, 8192)}
     sm["cfg5_us_step"] = {t: get(f"cfg5_moe_w4a16_E128_T{t}", "us_total")
                           for t in (1, 16, 256, 2048, 8192)}
+    # the tensor-core GEMMs against the issue rate of the MMA form they use (measured above)
+    mr = ex.get("mma_rate", {})
+    ceil_mx = mr.get("mxf8f6f4_cp_n256", {}).get("ceiling_tflops")
+    ceil_f16 = mr.get("f16_tmem_a_n128", {}).get("ceiling_tflops")
+    t8192 = sm["cfg5_tflops"].get(8192)
+    sm["frac_of_mma_issue_ceiling"] = {
+        "cfg2_w4a8": round(line["value"] / ceil_mx, 3) if ceil_mx else None,
+        "cfg5_T8192_w4a16": round(t8192 / ceil_f16, 3) if (ceil_f16 and t8192) else None}
     return sm
 
 

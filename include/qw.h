@@ -423,6 +423,36 @@ qw_status qw_test_wait_timeout(int32_t* d_err, int64_t limit_ns, void* stream);
 qw_status qw_stream_read(const void* src, uint64_t bytes, uint32_t* sink, int32_t chained,
                          void* stream);
 
+/* --------------------------------------------------------------------------------------
+ * qw_mma_rate_probe - diagnostics: the tcgen05 MMA issue rate the tensor-core GEMMs are
+ * bounded by (the pages tune per instruction shape and kind: spke.com Humming announcement,
+ * "フォーマットとアーキテクチャを横断して共有されるCUDAコンポーネント"; "W8A8 / W4A8 / W4A4").
+ * One CTA per SM (at most QW_MMA_PROBE_MAX_CTAS, 120 KiB of shared memory each, 512 TMEM
+ * columns), one thread issuing `iters` back-to-back M = 128 MMAs into one accumulator on
+ * zero operands, after a 64-MMA warm-up; then a commit and a bounded wait.  Modes:
+ *   QW_MMA_PROBE_F16_TMEM_A   kind::f16, A (BF16) in TMEM, B (BF16, 128-byte swizzle) in
+ *                             shared memory, N = n: the W4A16 GEMM's form (accumulation
+ *                             restarts every 8 MMAs, one 128-k group);
+ *   QW_MMA_PROBE_F16_SMEM     the same with A in shared memory;
+ *   QW_MMA_PROBE_MXF8F6F4     kind::mxf8f6f4.block_scale.scale_vec::1X, E4M3 x E2M1 (one
+ *                             byte per code), N = 256: the W4A8 GEMM's MMA;
+ *   QW_MMA_PROBE_MXF8F6F4_CP  the same plus its three tcgen05.cp.32x128b.warpx4 scale
+ *                             copies per four MMAs (one 128-k stage), into scale columns
+ *                             that rotate over four stages as in the GEMM's ring.
+ * n: 64, 128 or 256 for the f16 modes, 256 for the block-scaled ones; iters in [64, 2^20].
+ * Writes, per CTA c, out[2c] = SM clock cycles and out[2c + 1] = nanoseconds from the first
+ * issue to the completion (device uint64, 2 x QW_MMA_PROBE_MAX_CTAS of them); a wait that
+ * gave up writes zeros and raises QW_ERR_TIMEOUT in *d_err.  Invalid mode / n / iters:
+ * QW_ERR_INVALID_ARG; out not 8-byte aligned: QW_ERR_ALIGNMENT.
+ */
+#define QW_MMA_PROBE_F16_TMEM_A 0
+#define QW_MMA_PROBE_F16_SMEM 1
+#define QW_MMA_PROBE_MXF8F6F4 2
+#define QW_MMA_PROBE_MXF8F6F4_CP 3
+#define QW_MMA_PROBE_MAX_CTAS 1024
+qw_status qw_mma_rate_probe(int32_t mode, int32_t n, int32_t iters, uint64_t* out,
+                            int32_t* d_err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,6 +1,9 @@
-// diag.cu - a plain streaming read, the reference point the HBM-bound kernels are measured
-// against: the same bytes read with 16-byte loads by a full grid, folded into one word per
-// CTA (written out so the loads cannot be dropped).  No method arithmetic.
+// diag.cu - reference points the kernels are measured against; no method arithmetic.
+//  - A plain streaming read: the same bytes read with 16-byte loads by a full grid, folded
+//    into one word per CTA (written out so the loads cannot be dropped).
+//  - The tcgen05 MMA issue rate: one CTA per SM, one thread issuing back-to-back MMAs of the
+//    kind and shape a tensor-core GEMM uses, on zero operands, timed from the first issue to
+//    the completion seen through a commit.
 #include "qw_common.cuh"
 #include "qw_internal.h"
 
@@ -41,7 +44,129 @@ __global__ void __launch_bounds__(256) stream_read_kernel(const uint4* __restric
   }
 }
 
+// ---------------------------------------------------------------- tcgen05 MMA issue rate
+constexpr int kProbeABox = 128 * 128;  // 128 rows x 128 bytes (one swizzle atom per row)
+constexpr int kProbeBBox = 256 * 128;  // up to 256 rows x 128 bytes
+constexpr int kProbeOperands = 2 * kProbeABox + 2 * kProbeBBox;
+constexpr int kProbeSf = 3 * 512;      // one A and two B scale images (128 rows x 4 groups)
+// 120 KiB of shared memory: one probe CTA per SM (two would share its tensor core)
+constexpr size_t kProbeSmem = 120 * 1024;
+static_assert(kProbeOperands + kProbeSf + 64 + 1024 <= (int)kProbeSmem, "probe layout");
+constexpr uint32_t kProbeACol = 256;   // A operand in TMEM (the W4A16 form): 64 columns
+// scale factors: A 4 columns, B 8 columns per stage; four stages rotate through 48 columns
+// (as the GEMM's ring does, so a copy never overwrites columns an MMA in flight reads)
+constexpr uint32_t kProbeSfCol = 320;
+
+template <int MODE>
+__global__ void __launch_bounds__(128, 1)
+    mma_probe_kernel(int n, int iters, uint64_t* __restrict__ out, int32_t* err) {
+  extern __shared__ uint8_t probe_raw[];
+  uint8_t* sA = reinterpret_cast<uint8_t*>(((uintptr_t)probe_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sB = sA + 2 * kProbeABox;
+  uint8_t* sSF = sB + 2 * kProbeBBox;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sSF + kProbeSf);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
+  const int warp = threadIdx.x >> 5;
+
+  // zero operands (BF16, E4M3 and E2M1 zeros), scale bytes 127 (2^0)
+  for (int i = threadIdx.x; i < kProbeOperands / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(sA)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < kProbeSf / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(sSF)[i] = 0x7F7F7F7Fu;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  fence_proxy_async_smem();  // the tensor core reads what the threads wrote
+  if (warp == 0) {
+    tmem_alloc(slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *slot;
+
+  if (threadIdx.x == 0) {
+    // kind::f16: FP32 accumulator, A = B = BF16, K-major, N at bit 17, M = 128 at bit 24;
+    // kind::mxf8f6f4: A = E4M3, B = E2M1, UE8M0 scales, N = 256, M = 128, the scale byte of
+    // each 32-k MMA selected at bits 4 and 29
+    const uint32_t id_f16 =
+        (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (8u << 24);
+    const uint32_t id_mx = (5u << 10) | (32u << 17) | (1u << 23) | (8u << 24);
+    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB), sf0 = smem_u32(sSF);
+    auto issue = [&](int i) {
+      if constexpr (MODE == QW_MMA_PROBE_F16_TMEM_A || MODE == QW_MMA_PROBE_F16_SMEM) {
+        const int s = i & 7;  // 16-k step of a 128-k group (two 64-k boxes)
+        const uint64_t bd = smem_desc(b0 + (s >> 2) * kProbeBBox + (s & 3) * 32, 16, 1024, 2);
+        if constexpr (MODE == QW_MMA_PROBE_F16_TMEM_A)
+          tc_mma_f16_tmem_a(tbase, tbase + kProbeACol + 8 * s, bd, id_f16, s != 0 ? 1u : 0u);
+        else
+          tc_mma_f16(tbase, smem_desc(a0 + (s >> 2) * kProbeABox + (s & 3) * 32, 16, 1024, 2),
+                     bd, id_f16, s != 0 ? 1u : 0u);
+      } else {
+        const int kk = i & 3;  // 32-k MMA of a 128-k stage
+        const uint32_t sfc = tbase + kProbeSfCol + 12u * (uint32_t)((i >> 2) & 3);
+        if (MODE == QW_MMA_PROBE_MXF8F6F4_CP && kk == 0) {
+          // the stage's scale images, as the W4A8 GEMM copies them
+          tc_cp_32x128b_warpx4(sfc, smem_desc(sf0, 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfc + 4, smem_desc(sf0 + 512, 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfc + 8, smem_desc(sf0 + 1024, 0, 128, 0));
+        }
+        tc_mma_mxf8f6f4(tbase, smem_desc(a0 + kk * 32, 16, 1024, 2),
+                        smem_desc(b0 + kk * 32, 16, 1024, 2),
+                        id_mx | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), sfc, sfc + 4,
+                        i != 0 ? 1u : 0u);
+      }
+    };
+    for (int i = 0; i < 64; ++i) issue(i);  // warm-up
+    tc_commit(bar);
+    bool ok = mbar_wait(bar, 0, abort_flag, err);
+    const uint64_t c0 = clock64(), t0 = globaltimer_ns();
+    for (int i = 0; ok && i < iters; ++i) issue(i);
+    tc_commit(bar);
+    ok = mbar_wait(bar, 1, abort_flag, err) && ok;
+    const uint64_t c1 = clock64(), t1 = globaltimer_ns();
+    out[2 * blockIdx.x] = ok ? c1 - c0 : 0;
+    out[2 * blockIdx.x + 1] = ok ? t1 - t0 : 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int MODE>
+qw_status launch_probe_mode(int n, int iters, uint64_t* out, int32_t* err, int grid,
+                            cudaStream_t st) {
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      mma_probe_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kProbeSmem);
+  if (attr != cudaSuccess) return QW_ERR_CUDA;
+  mma_probe_kernel<MODE><<<grid, 128, kProbeSmem, st>>>(n, iters, out, err);
+  return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+}
+
 }  // namespace
+
+qw_status launch_mma_probe(int mode, int n, int iters, uint64_t* out, int32_t* err,
+                           cudaStream_t st) {
+  int grid = device_sm_count();
+  if (grid > QW_MMA_PROBE_MAX_CTAS) grid = QW_MMA_PROBE_MAX_CTAS;
+  switch (mode) {
+    case QW_MMA_PROBE_F16_TMEM_A:
+      return launch_probe_mode<QW_MMA_PROBE_F16_TMEM_A>(n, iters, out, err, grid, st);
+    case QW_MMA_PROBE_F16_SMEM:
+      return launch_probe_mode<QW_MMA_PROBE_F16_SMEM>(n, iters, out, err, grid, st);
+    case QW_MMA_PROBE_MXF8F6F4:
+      return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4>(n, iters, out, err, grid, st);
+    default:
+      return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4_CP>(n, iters, out, err, grid, st);
+  }
+}
 
 qw_status launch_stream_read(const void* src, uint64_t bytes, uint32_t* sink, bool chained,
                              cudaStream_t st) {

@@ -129,16 +129,6 @@ __device__ __forceinline__ void tc_st_16x256b_x8(uint32_t taddr, const uint32_t 
 __device__ __forceinline__ void tc_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-// D(tmem) (+)= A(tmem) x B(smem)^T, BF16 operands, FP32 accumulation.
-__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d, uint32_t a_tmem, uint64_t b_desc,
-                                                  uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __device__ __forceinline__ uint32_t bf16x2_sub_u32(uint32_t x, uint32_t y) {
   // x - y for a pair of BF16 values; here the difference is an exact small integer
   __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&x);

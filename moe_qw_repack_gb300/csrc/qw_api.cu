@@ -448,4 +448,18 @@ qw_status qw_stream_read(const void* src, uint64_t bytes, uint32_t* sink, int32_
   return launch_stream_read(src, bytes, sink, chained != 0, static_cast<cudaStream_t>(stream));
 }
 
+qw_status qw_mma_rate_probe(int32_t mode, int32_t n, int32_t iters, uint64_t* out,
+                            int32_t* d_err, void* stream) {
+  const bool f16 = mode == QW_MMA_PROBE_F16_TMEM_A || mode == QW_MMA_PROBE_F16_SMEM;
+  const bool mx = mode == QW_MMA_PROBE_MXF8F6F4 || mode == QW_MMA_PROBE_MXF8F6F4_CP;
+  if (!f16 && !mx) return QW_ERR_INVALID_ARG;
+  // only the shapes the GEMMs issue (a shape outside the MMA's table would not assemble to
+  // a valid instruction)
+  if (f16 && n != 64 && n != 128 && n != 256) return QW_ERR_INVALID_ARG;
+  if (mx && n != 256) return QW_ERR_INVALID_ARG;
+  if (iters < 64 || iters > (1 << 20) || !out || !d_err) return QW_ERR_INVALID_ARG;
+  if (!aligned(out, 8) || !aligned(d_err, 4)) return QW_ERR_ALIGNMENT;
+  return launch_mma_probe(mode, n, iters, out, d_err, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -127,5 +127,8 @@ qw_status launch_wait_timeout_probe(int32_t* err, int64_t limit_ns, cudaStream_t
 // Diagnostics: a plain streaming read of `bytes` at `src` (one fold word per CTA to `sink`).
 qw_status launch_stream_read(const void* src, uint64_t bytes, uint32_t* sink, bool chained,
                              cudaStream_t st);
+// Diagnostics: the tcgen05 MMA issue rate (qw_mma_rate_probe; arguments checked there).
+qw_status launch_mma_probe(int mode, int n, int iters, uint64_t* out, int32_t* err,
+                           cudaStream_t st);
 
 }  // namespace qw

@@ -47,6 +47,7 @@ EXPORTS = (
     "qw_test_wait_timeout",
     "qgemm_moe_route_noalloc", "qw_quantize_mxfp8", "qw_silu_mul",
     "qgemm_moe_combine_workspace_size", "qgemm_moe_combine", "qw_stream_read",
+    "qw_mma_rate_probe",
 )
 
 
@@ -96,6 +97,7 @@ _SIGS = {
     "qgemm_moe_combine_workspace_size": (_I32, [_I32, _I32, ctypes.POINTER(_U64)]),
     "qgemm_moe_combine": (_I32, [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _P, _P, _U64, _P, _P]),
     "qw_stream_read": (_I32, [_P, _U64, _P, _I32, _P]),
+    "qw_mma_rate_probe": (_I32, [_I32, _I32, _I32, _P, _P, _P]),
 }
 
 
@@ -282,6 +284,33 @@ QW_STREAM_READ_SINK_WORDS = 4096
 def qw_stream_read(src, nbytes: int, sink, chained: bool = False, stream=None):
     _check("qw_stream_read", LIB.qw_stream_read(_ptr(src), nbytes, _ptr(sink), int(chained),
                                                 _stream(stream)))
+
+
+QW_MMA_PROBE_F16_TMEM_A = 0
+QW_MMA_PROBE_F16_SMEM = 1
+QW_MMA_PROBE_MXF8F6F4 = 2
+QW_MMA_PROBE_MXF8F6F4_CP = 3
+QW_MMA_PROBE_MAX_CTAS = 1024
+
+
+def qw_mma_rate_probe(mode: int, n: int, iters: int, out, d_err, stream=None):
+    """out: device uint64 (int64 tensor) of 2 * QW_MMA_PROBE_MAX_CTAS entries."""
+    _check("qw_mma_rate_probe", LIB.qw_mma_rate_probe(mode, n, iters, _ptr(out), _ptr(d_err),
+                                                      _stream(stream)))
+
+
+def mma_rate(mode: int, n: int, iters: int = 4096):
+    """Runs the probe once and returns (cycles per MMA, ns per MMA) for each CTA that ran
+    (one per SM), as float64 arrays."""
+    import numpy as np
+    out = torch.zeros(2 * QW_MMA_PROBE_MAX_CTAS, dtype=torch.int64, device="cuda")
+    err = new_error_flag()
+    qw_mma_rate_probe(mode, n, iters, out, err)
+    if qw_read_error(err) != 0:
+        raise QwError("qw_mma_rate_probe", qw_read_error(err))
+    v = out.cpu().numpy().astype(np.float64).reshape(-1, 2)
+    v = v[v[:, 0] > 0]
+    return v[:, 0] / iters, v[:, 1] / iters
 
 
 # ----------------------------------------------------------------------------- conveniences

@@ -277,3 +277,19 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
                        timeout=300)
     assert "IMPORT-ERROR" in r.stdout and str(missing) in r.stdout, r.stdout + r.stderr
+
+
+def test_mma_rate_probe_validates_on_the_host(Q):
+    """The MMA-rate diagnostic takes only the shapes the GEMMs issue; nothing launches."""
+    out = ctypes.c_void_p(64)
+    err = ctypes.c_void_p(64)
+    bad = [(4, 128, 4096), (-1, 128, 4096),  # unknown mode
+           (Q.QW_MMA_PROBE_F16_TMEM_A, 96, 4096), (Q.QW_MMA_PROBE_F16_SMEM, 512, 4096),
+           (Q.QW_MMA_PROBE_MXF8F6F4, 128, 4096), (Q.QW_MMA_PROBE_MXF8F6F4_CP, 64, 4096),
+           (Q.QW_MMA_PROBE_F16_SMEM, 128, 63), (Q.QW_MMA_PROBE_F16_SMEM, 128, (1 << 20) + 1)]
+    for mode, n, iters in bad:
+        assert Q.LIB.qw_mma_rate_probe(mode, n, iters, out, err, None) == Q.QW_ERR_INVALID_ARG
+    assert Q.LIB.qw_mma_rate_probe(0, 128, 4096, None, err, None) == Q.QW_ERR_INVALID_ARG
+    assert Q.LIB.qw_mma_rate_probe(0, 128, 4096, out, None, None) == Q.QW_ERR_INVALID_ARG
+    assert Q.LIB.qw_mma_rate_probe(0, 128, 4096, ctypes.c_void_p(68), err, None) == \
+        Q.QW_ERR_ALIGNMENT
