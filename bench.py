@@ -320,6 +320,9 @@ def extra_w4a16(steps, warmup, world, only=None):
     cases.append(("m1_14336x4096_int2", 1, 14336, 4096, 2))
     cases.append(("m1_14336x4096_int1", 1, 14336, 4096, 1))
     cases.append(("m1_14336x4096_fp4", 1, 14336, 4096, "fp4"))
+    # few 16-row blocks and long K: the decode GEMV splits K across the CTAs of a cluster
+    cases.append(("m1_1024x32768_int4_splitk", 1, 1024, 32768, 4))
+    cases.append(("m1_512x16384_int4_splitk", 1, 512, 16384, 4))
     for name, M, N, K, bits in cases:
         if only and only not in name:
             continue

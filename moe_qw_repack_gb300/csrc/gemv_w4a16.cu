@@ -803,12 +803,16 @@ struct DecParams {
   uint16_t* C;
   int32_t N, N_pad, K;
   int32_t gpw;          // scale groups per warp (a multiple of kDecRing, at most kDecMaxGpw)
+  // K split across CTAs (S > 1): a cluster of S CTAs takes one block, CTA rank r its slice r
+  // (gs = warps x gpw groups); rank 0 adds the slice sums in rank order through distributed
+  // shared memory and applies scale2 and bias
+  int32_t S, gs;
 };
 
 // shared memory: FP16 activations [group][step pair][t][16 B] and the group constants
-// (float4), then the reduction [2][warp][16] floats
-__host__ __device__ constexpr size_t dec_smem_bytes(int groups, int warps) {
-  return (size_t)groups * (256 + 16) + 2 * (size_t)warps * 16 * 4;
+// (float4), then the reduction [2][warp][16] floats (and, split, the CTA's 16 slice sums)
+__host__ __device__ constexpr size_t dec_smem_bytes(int groups, int warps, bool split = false) {
+  return (size_t)groups * (256 + 16) + 2 * (size_t)warps * 16 * 4 + (split ? 16 * 4 : 0);
 }
 
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
@@ -826,7 +830,9 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int BITS, int R>
+// SPLIT: the cluster form (one slice of one block per CTA); otherwise whole blocks per CTA
+// (compiled without any of the split's code).
+template <int BITS, int R, bool SPLIT>
 __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const DecParams p) {
   using GE = Geo<BITS>;
   constexpr int WPG = GE::WPG;        // packed words per lane and group
@@ -839,12 +845,23 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
   const int g = lane >> 2, t = lane & 3;
   const int G = p.K >> 7;
   const uint32_t nblocks = (uint32_t)(p.N_pad >> 4);
-  const uint32_t my_items = blockIdx.x < nblocks ? (nblocks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int wg0 = warp * p.gpw;                       // the warp's first group
+  const int S = SPLIT ? p.S : 1;
+  const uint32_t my_items =
+      S > 1 ? (blockIdx.x < nblocks * (uint32_t)S ? 1u : 0u)
+            : (blockIdx.x < nblocks ? (nblocks - 1 - blockIdx.x) / gridDim.x + 1 : 0);
+  // the warp's first group (its slice's first group plus its share)
+  const int wg0 = (S > 1 ? (int)(blockIdx.x % (uint32_t)S) * p.gs : 0) + warp * p.gpw;
+  auto block_of = [&](uint32_t it) -> uint32_t {
+    return S > 1 ? blockIdx.x / (uint32_t)S : blockIdx.x + it * gridDim.x;
+  };
   const uint32_t gstride = nblocks * (uint32_t)GE::BLK;  // bytes between groups of a block
   uint8_t* act = reinterpret_cast<uint8_t*>(dec_smem);  // [G][4][4][16 B]
-  float4* gconst = reinterpret_cast<float4*>(act + (size_t)G * 256);
-  float* red = reinterpret_cast<float*>(gconst + G);     // [2][warps][16]
+  // staged groups: the whole K, or the CTA's slice (indexed from its first group gbase)
+  const int gbase = S > 1 ? (int)(blockIdx.x % (uint32_t)S) * p.gs : 0;
+  const int gstaged = S > 1 ? p.gs : G;
+  float4* gconst = reinterpret_cast<float4*>(act + (size_t)gstaged * 256);
+  float* red = reinterpret_cast<float*>(gconst + gstaged);  // [2][warps][16]
+  float* cpart = red + 2 * warps * 16;                        // split: this CTA's slice sums
 
   pdl_launch_dependents();
 
@@ -853,10 +870,10 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
   uint32_t sl_[R], sh_[R];  // BF16 scale bits of rows g and g + 8
   // byte offset of (item it, the warp's first group) and its scale index
   auto unit_w = [&](uint32_t it) {
-    return (blockIdx.x + it * gridDim.x) * (uint32_t)GE::BLK + (uint32_t)wg0 * gstride;
+    return block_of(it) * (uint32_t)GE::BLK + (uint32_t)wg0 * gstride;
   };
   auto unit_s = [&](uint32_t it) {
-    return (uint32_t)wg0 * (uint32_t)p.N_pad + (blockIdx.x + it * gridDim.x) * 16u + (uint32_t)g;
+    return (uint32_t)wg0 * (uint32_t)p.N_pad + block_of(it) * 16u + (uint32_t)g;
   };
   auto load = [&](int r, uint32_t woff, uint32_t soff) {
     load_words<BITS>(p.wp + woff, lane, wb[r]);
@@ -924,7 +941,8 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
           }
           // chunk c holds k = 8c .. 8c + 7: step c / 2, lanes t = 2 (c & 1) and 2 (c & 1) + 1
           if (q < nchunk) {
-            uint8_t* dst = act + ((gl * 4 + (c >> 2)) * 4 + 2 * (c & 1)) * 16 + ((c >> 1) & 1) * 8;
+            uint8_t* dst =
+                act + (((gl - gbase) * 4 + (c >> 2)) * 4 + 2 * (c & 1)) * 16 + ((c >> 1) & 1) * 8;
             *reinterpret_cast<uint2*>(dst) = make_uint2(h[0], h[1]);
             *reinterpret_cast<uint2*>(dst + 16) = make_uint2(h[2], h[3]);
           }
@@ -933,13 +951,13 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
           if ((lane & 15) == 0 && q < nchunk) {
             if constexpr (BITS == 4) {
               const float e = __uint_as_float((uint32_t)(127 - f) << 23);  // 2^-f
-              gconst[gl] = make_float4(e, e * 0.0625f, -1032.f * e * sum, -72.f * e * sum);
+              gconst[gl - gbase] = make_float4(e, e * 0.0625f, -1032.f * e * sum, -72.f * e * sum);
             } else if constexpr (F16) {
               const float e = __uint_as_float((uint32_t)(127 - f) << 23);  // 2^-f, no excess
-              gconst[gl] = make_float4(e, e, 0.f, 0.f);
+              gconst[gl - gbase] = make_float4(e, e, 0.f, 0.f);
             } else {
               // biased codes 128 + excess + q on both row halves
-              gconst[gl] = make_float4(1.f, 1.f, -GE::BIAS * sum, -GE::BIAS * sum);
+              gconst[gl - gbase] = make_float4(1.f, 1.f, -GE::BIAS * sum, -GE::BIAS * sum);
             }
           }
         }
@@ -947,10 +965,10 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
   }
   __syncwarp();
 
-  const uint32_t act_lane = smem_u32(act) + (uint32_t)(wg0 * 256 + t * 16);
-  const uint32_t const_base = smem_u32(gconst) + (uint32_t)wg0 * 16;
+  const uint32_t act_lane = smem_u32(act) + (uint32_t)((wg0 - gbase) * 256 + t * 16);
+  const uint32_t const_base = smem_u32(gconst) + (uint32_t)(wg0 - gbase) * 16;
   for (uint32_t it = 0; it < my_items; ++it) {
-    const uint32_t nb = blockIdx.x + it * gridDim.x;
+    const uint32_t nb = block_of(it);
     const uint32_t wit = unit_w(it), sit = unit_s(it);
     const uint32_t wnx = unit_w(it + 1), snx = unit_s(it + 1);
     const bool has_next = it + 1 < my_items;
@@ -1019,7 +1037,9 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
       float v = 0.f;
       for (int w2 = 0; w2 < warps; ++w2) v += rb[w2 * 16 + lane];
       const int n = (int)nb * 16 + lane;
-      if (n < p.N) {
+      if (S > 1) {
+        cpart[lane] = v;  // this slice's sums, read by the cluster's rank 0 below
+      } else if (n < p.N) {
         if (p.scale2) v *= __ldg(p.scale2 + n);
         if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + n) << 16);
         __nv_bfloat16 hb = __float2bfloat16_rn(v);
@@ -1027,13 +1047,35 @@ __global__ void __launch_bounds__(kDecMaxWarps * 32, 1) gemv_decode_kernel(const
       }
     }
   }
+  if (S > 1) {
+    // the cluster's S CTAs hold one block's slice sums: rank 0 adds them in rank order
+    // (deterministic) from the CTAs' shared memory; every thread of every CTA takes both
+    // cluster barriers (each CTA has exactly one item), the second keeping the peers'
+    // shared memory alive until rank 0 has read it
+    cluster_sync();
+    if (cluster_ctarank() == 0 && warp == 0 && lane < 16) {
+      const uint32_t own = smem_u32(cpart + lane);
+      float v = 0.f;
+      for (int r = 0; r < S; ++r) v += ld_shared_cluster_f32(mapa_shared(own, (uint32_t)r));
+      const int n = (int)(blockIdx.x / (uint32_t)S) * 16 + lane;
+      if (n < p.N) {
+        if (p.scale2) v *= __ldg(p.scale2 + n);
+        if (p.bias) v += __uint_as_float((uint32_t)__ldg(p.bias + n) << 16);
+        __nv_bfloat16 hb = __float2bfloat16_rn(v);
+        p.C[n] = *reinterpret_cast<uint16_t*>(&hb);
+      }
+    }
+    cluster_sync();
+  }
 }
 
 // How a decode call is split: warps per CTA (each streaming gpw groups of every block the
 // CTA takes) and resident CTAs per SM.
 struct DecPlan {
   int warps = 0, gpw = 0, per_sm = 0;  // warps == 0: no plan (the shape goes to gemv_m8_kernel)
+  int S = 1;                           // K slices per block, one CTA each (1: no split)
 };
+constexpr int kDecMaxSlices = 8;  // a slice per CTA of a cluster (portable cluster size)
 
 // The split with the most warps per SM (16 at 128 registers each), ties to more warps per
 // CTA (fewer blocks per SM to wait on); measured best at K = 4096 (8 warps x 4 groups, two
@@ -1058,14 +1100,53 @@ DecPlan decode_plan(int K) {
   return best;
 }
 
+// Shapes with fewer 16-row blocks than SMs leave SMs idle when every CTA takes whole blocks:
+// split each block's K into S slices (a cluster of S CTAs, one slice each, the slice sums
+// added through distributed shared memory) when that puts CTAs on more SMs and fills more of their warp slots over the waves (CTAs
+// of `warps` warps, 16 / warps of them per SM).  Measured on GB300 (M = 1, INT4): 1024 x
+// 32768 and 512 x 16384 ran at half a plain streaming read unsplit.
+DecPlan decode_plan_for(int K, int64_t nblocks, int sms) {
+  DecPlan best = decode_plan(K);
+  // measured: a split pays at 32 blocks x 128 groups and 64 x 256 (the CTAs' streams are
+  // long enough to cover the cluster's set-up), not at 64 x 64 or 128 x 64..128
+  if (best.warps == 0 || 2 * nblocks > sms || K / 128 < 128) return best;
+  const int G = K / 128;
+  auto score = [&](int64_t ctas, int warps, int per_sm) {
+    const int64_t slots = (int64_t)sms * per_sm;
+    const int64_t waves = (ctas + slots - 1) / slots;
+    const double busy = (double)(ctas < sms ? ctas : sms) / sms;  // SMs with a CTA
+    return busy + (double)(ctas * warps) / (double)(waves * sms * kDecMaxWarps);
+  };
+  double best_score = score(nblocks, best.warps, best.per_sm);
+  for (int S = 2; S <= kDecMaxSlices; ++S) {
+    if (G % S) continue;
+    const int gs = G / S;
+    for (int warps = 1; warps <= kDecMaxWarps; ++warps) {
+      if (gs % warps) continue;
+      const int gpw = gs / warps;
+      if (gpw % kDecRing || gpw > kDecMaxGpw) continue;
+      if (dec_smem_bytes(gs, warps, true) > kDecMaxSmem) continue;
+      const int per_sm = kDecMaxWarps / warps;
+      const double sc = score(nblocks * S, warps, per_sm);
+      if (sc > best_score + 1e-9) {
+        best.warps = warps;
+        best.gpw = gpw;
+        best.per_sm = per_sm;
+        best.S = S;
+        best_score = sc;
+      }
+    }
+  }
+  return best;
+}
+
 template <int BITS>
 qw_status launch_decode_variant(const qw_packed_desc& d, const DecPlan& pl, const DecParams& p,
                                 cudaStream_t st);
 
-qw_status launch_decode(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
-                        const void* A, const void* bias, const float* scale2, void* C,
-                        cudaStream_t st) {
-  const DecPlan pl = decode_plan(d.K);
+qw_status launch_decode_plan(const qw_packed_desc& d, const DecPlan& pl, const void* w_packed,
+                             const void* s_packed, const void* A, const void* bias,
+                             const float* scale2, void* C, cudaStream_t st) {
   if (pl.warps == 0) return QW_ERR_UNSUPPORTED;
   DecParams p{};
   p.wp = static_cast<const uint8_t*>(w_packed);
@@ -1078,6 +1159,8 @@ qw_status launch_decode(const qw_packed_desc& d, const void* w_packed, const voi
   p.N_pad = d.N_pad;
   p.K = d.K;
   p.gpw = pl.gpw;
+  p.S = pl.S;
+  p.gs = pl.warps * pl.gpw;
   switch (d.wfmt) {
     case QW_W_INT4_G128_BF16: return launch_decode_variant<4>(d, pl, p, st);
     case QW_W_INT3_G128_BF16: return launch_decode_variant<3>(d, pl, p, st);
@@ -1087,13 +1170,54 @@ qw_status launch_decode(const qw_packed_desc& d, const void* w_packed, const voi
   }
 }
 
+qw_status launch_decode(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
+                        const void* A, const void* bias, const float* scale2, void* C,
+                        cudaStream_t st) {
+  const DecPlan pl = decode_plan_for(d.K, d.N_pad / 16, device_sm_count());
+  const qw_status s = launch_decode_plan(d, pl, w_packed, s_packed, A, bias, scale2, C, st);
+  // a cluster of pl.S CTAs that cannot be placed: the unsplit schedule
+  if (s == QW_ERR_UNSUPPORTED && pl.S > 1)
+    return launch_decode_plan(d, decode_plan(d.K), w_packed, s_packed, A, bias, scale2, C, st);
+  return s;
+}
+
 template <int BITS>
 qw_status launch_decode_variant(const qw_packed_desc& d, const DecPlan& pl, const DecParams& p,
                                 cudaStream_t st) {
-  auto kern = gemv_decode_kernel<BITS, kDecRing>;
+  auto kern = gemv_decode_kernel<BITS, kDecRing, false>;
   static const cudaError_t attr =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecMaxSmem);
   if (attr != cudaSuccess) return QW_ERR_CUDA;
+  const int64_t items = d.N_pad / 16;
+  if (pl.S > 1) {
+    auto skern = gemv_decode_kernel<BITS, kDecRing, true>;
+    static const cudaError_t sattr =
+        cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecMaxSmem);
+    if (sattr != cudaSuccess) return QW_ERR_CUDA;
+    const size_t smem = dec_smem_bytes(p.gs, pl.warps, true);
+    // one cluster of S CTAs per block, launched as a programmatic dependent like the rest
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(items * pl.S));
+    cfg.blockDim = dim3((unsigned)(pl.warps * 32));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)pl.S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, skern, &cfg) != cudaSuccess || clusters < 1) {
+      (void)cudaGetLastError();
+      return QW_ERR_UNSUPPORTED;
+    }
+    if (cudaLaunchKernelEx(&cfg, skern, p) != cudaSuccess) return QW_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
+  }
   const size_t smem = dec_smem_bytes(d.K / 128, pl.warps);
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, pl.warps * 32, smem) !=
@@ -1101,7 +1225,6 @@ qw_status launch_decode_variant(const qw_packed_desc& d, const DecPlan& pl, cons
       per_sm < 1)
     per_sm = 1;
   if (per_sm > pl.per_sm) per_sm = pl.per_sm;
-  const int64_t items = d.N_pad / 16;
   int64_t grid = (int64_t)device_sm_count() * per_sm;
   if (grid > items) grid = items;
   if (grid < 1) grid = 1;

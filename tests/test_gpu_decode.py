@@ -116,3 +116,55 @@ def test_stream_read_reads_every_word(chained):
     torch.cuda.synchronize()
     got = np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint32))
     assert got == np.bitwise_xor.reduce(words)
+
+
+def _split_call(Q, wfmt, N, K, w_canon, s_canon, A, bias=None, t=None):
+    d, wp, sp = repack(wfmt | (Q.QW_W_SCALE2 if t is not None else 0), 1, N, K, w_canon, s_canon)
+    err = Q.new_error_flag()
+    if t is not None:
+        Q.qw_repack_scale2(d, dev(t), sp, err)
+    C = torch.full((1, N), -1, dtype=torch.int16, device="cuda")
+    b = None if bias is None else dev(bias.view(np.int16))
+    Q.qgemm_dense(d, wp, sp, Q.QW_A_BF16, dev(A.view(np.int16)), None, b, C, 1, None, 0, err)
+    assert Q.qw_read_error(err) == 0
+    return u16_view(C)
+
+
+@pytest.mark.parametrize("N,K", [(512, 16384), (1000, 32768), (200, 16384), (760, 24576)])
+def test_decode_split_k_bias_scale2(N, K):
+    """At most half as many 16-row blocks as SMs and K of 128 groups or more (the shapes the
+    launcher splits; S = 8, 4, 8 and 6 slices here): K is split across the CTAs of a
+    cluster, whose rank 0
+    adds the slice sums in rank order through distributed shared memory, then applies the
+    second-level scales and the bias.  Two calls give identical bits."""
+    Q = qw()
+    p = synth.w4a16_problem(1, N, K, bits=4, cfg_id=760 + K // 1024, bias=True)
+    rng = np.random.default_rng(K + N)
+    t = (2.0 ** rng.integers(-3, 4, N)).astype(np.float32)
+    C1 = _split_call(Q, Q.QW_W_INT4_G128_BF16, N, K, p["w_canon"], p["s_canon"], p["A"],
+                     p["bias"][0], t)
+    C2 = _split_call(Q, Q.QW_W_INT4_G128_BF16, N, K, p["w_canon"], p["s_canon"], p["A"],
+                     p["bias"][0], t)
+    assert np.array_equal(C1, C2), "split-K results must be deterministic"
+    R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, 4)
+    R2, S2 = OQ.apply_scale2(R, S, t, p["bias"][0])
+    assert_parity(C1, R2, S2, f"split decode {N}x{K}")
+
+
+@pytest.mark.parametrize("kind", ["int3", "int2", "int1", "fp4"])
+def test_decode_split_k_formats(kind):
+    """The split schedule for every format the decode kernel takes (1000 x 16384)."""
+    Q = qw()
+    N, K = 1000, 16384
+    if kind == "fp4":
+        p = synth.fp4w_problem(1, N, K, cfg_id=771)
+        wfmt = Q.QW_W_FP4E2M1_G128_BF16
+        R, S = OQ.fp4w_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K)
+    else:
+        bits = {"int3": 3, "int2": 2, "int1": 1}[kind]
+        p = synth.w4a16_problem(1, N, K, bits=bits, cfg_id=772 + bits)
+        wfmt = {3: Q.QW_W_INT3_G128_BF16, 2: Q.QW_W_INT2_G128_BF16,
+                1: Q.QW_W_INT1_G128_BF16}[bits]
+        R, S = OQ.w4a16_from_canonical(p["A"], p["w_canon"][0], p["s_canon"][0], K, bits)
+    C = _split_call(Q, wfmt, N, K, p["w_canon"], p["s_canon"], p["A"])
+    assert_parity(C, R, S, f"split decode {kind}")
