@@ -774,6 +774,8 @@ def summarize(line):
                                    for n, k in ((14336, 4096), (4096, 14336), (4096, 4096))]
     sm["cfg3_stream_read_chained_frac"] = [get(f"cfg3_m1_{n}x{k}_int4", "stream_read_chained_frac")
                                            for n, k in ((14336, 4096), (4096, 14336), (4096, 4096))]
+    sm["m1_splitk_frac_hbm"] = [get("m1_1024x32768_int4_splitk", "hbm_frac"),
+                                get("m1_512x16384_int4_splitk", "hbm_frac")]
     sm["cfg4_gemm_frac_fp8"] = get("cfg4_moe_w4a8_E256_T4096", "gemm_frac_fp8_peak")
     sm["cfg5_weight_frac_hbm"] = {t: get(f"cfg5_moe_w4a16_E128_T{t}", "weight_frac_hbm")
                                   for t in (1, 16, 256)}
