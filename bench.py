@@ -782,10 +782,17 @@ def summarize(line):
     sm["cfg5_tflops"] = {t: get(f"cfg5_moe_w4a16_E128_T{t}", "gemm_tflops") for t in (2048, 8192)}
     sm["cfg5_us_step"] = {t: get(f"cfg5_moe_w4a16_E128_T{t}", "us_total")
                           for t in (1, 16, 256, 2048, 8192)}
-    # the tensor-core GEMMs against the issue rate of the MMA form they use (measured above)
+    # the tensor-core GEMMs against the issue rate of the MMA form they use (measured above,
+    # scaled from the probe's SM clock to the one sampled during the timed region)
     mr = ex.get("mma_rate", {})
-    ceil_mx = mr.get("mxf8f6f4_cp_n256", {}).get("ceiling_tflops")
-    ceil_f16 = mr.get("f16_tmem_a_n128", {}).get("ceiling_tflops")
+
+    def ceiling(name):
+        r = mr.get(name, {})
+        c, ghz = r.get("ceiling_tflops"), r.get("sm_ghz")
+        mhz = line.get("clocks", {}).get("sm_mhz")
+        return c * (mhz / 1e3) / ghz if (c and ghz and mhz) else c
+    ceil_mx = ceiling("mxf8f6f4_cp_n256")
+    ceil_f16 = ceiling("f16_tmem_a_n128")
     t8192 = sm["cfg5_tflops"].get(8192)
     sm["frac_of_mma_issue_ceiling"] = {
         "cfg2_w4a8": round(line["value"] / ceil_mx, 3) if ceil_mx else None,
