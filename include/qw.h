@@ -226,10 +226,10 @@ qw_status qw_unpack_scale2(const qw_packed_desc* desc, const void* s_packed, flo
 /* --------------------------------------------------------------------------------------
  * qgemm_workspace_size - bytes of device workspace qgemm_dense / qgemm_moe_grouped need
  * for up to `max_rows` activation rows (host output `bytes`; 0 is a valid answer).
- * The workspace holds split-K partial sums, split-K tickets and the grouped tile queue.
- * Zero-fill it once after allocating it: the tickets must start at zero, and every call
- * that completes leaves them at zero again.  After a call that reported QW_ERR_TIMEOUT,
- * zero it again.  Calls that share one workspace must not overlap on the GPU.
+ * The workspace holds the grouped calls' device tile queue, which every call writes in
+ * full before reading it (no initialisation needed); dense calls need none (0 bytes; the
+ * single-token GEMV's split of K across the CTAs of a cluster keeps its partial sums in
+ * shared memory).  Calls that share one workspace must not overlap on the GPU.
  */
 qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t max_rows,
                                uint64_t* bytes);
