@@ -252,7 +252,9 @@ qw_status qgemm_workspace_size(const qw_packed_desc* desc, int32_t afmt, int64_t
  * 基づくパフォーマンスチューニング"): W4A16 with M <= 16 streams the weights through a
  * split-K tensor-core GEMV, larger M dequantizes into tensor memory and runs tcgen05 BF16
  * MMAs (grouped calls switch at 16 rows per expert on average); W4A8 runs the TMA +
- * tcgen05 block-scaled GEMM.
+ * tcgen05 block-scaled GEMM.  With M = 1, at most half as many 16-row blocks of N as SMs
+ * and K of 16384 or more, the GEMV splits K across the CTAs of thread-block clusters of up
+ * to 8 (rank 0 adds the slices in a fixed order: results do not depend on timing).
  * Alignment: A, C 16-byte aligned with K % 8 == 0 (BF16) or K % 16 == 0 (E4M3);
  * A_sf 4-byte aligned.  M >= 0 (M == 0 is a no-op).
  * Ordering: the small-M kernels (W4A16 M <= 16, W4A8 M <= 8) start as programmatic
