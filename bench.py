@@ -521,6 +521,8 @@ MMA_PROBES = (  # (name, mode, N, FLOP per MMA): the instruction forms the GEMMs
     ("f16_smem_n256", 1, 256, 2 * 128 * 256 * 16),
     ("mxf8f6f4_n256", 2, 256, 2 * 128 * 256 * 32),     # W4A8 GEMM, MMAs only
     ("mxf8f6f4_cp_n256", 3, 256, 2 * 128 * 256 * 32),  # ... with its scale copies
+    ("mxf8f6f4_cp_ahead_n256", 4, 256, 2 * 128 * 256 * 32),  # copies a stage ahead
+    ("mxf8f6f4_cp_wide_n256", 5, 256, 2 * 128 * 256 * 32),   # two 128-lane copies a stage
 )
 
 

@@ -440,7 +440,14 @@ qw_status qw_stream_read(const void* src, uint64_t bytes, uint32_t* sink, int32_
  *                             byte per code), N = 256: the W4A8 GEMM's MMA;
  *   QW_MMA_PROBE_MXF8F6F4_CP  the same plus its three tcgen05.cp.32x128b.warpx4 scale
  *                             copies per four MMAs (one 128-k stage), into scale columns
- *                             that rotate over four stages as in the GEMM's ring.
+ *                             that rotate over four stages as in the GEMM's ring;
+ *   QW_MMA_PROBE_MXF8F6F4_CP_AHEAD  the same copies issued one stage ahead (into the next
+ *                             stage's columns, so no MMA reads what was just copied);
+ *   QW_MMA_PROBE_MXF8F6F4_CP_WIDE   two copies per stage instead of three: A's image as one
+ *                             tcgen05.cp.128x128b, B's two as one 128x256b (sources with
+ *                             each 32-row image repeated for the four lane quarters).
+ * QW_MMA_PROBE_RANDOM or'ed into a mode fills the operands with hashed finite values
+ * instead of zeros (the tensor core's rate may depend on the data it multiplies).
  * n: 64, 128 or 256 for the f16 modes, 256 for the block-scaled ones; iters in [64, 2^20].
  * Writes, per CTA c, out[2c] = SM clock cycles and out[2c + 1] = nanoseconds from the first
  * issue to the completion (device uint64, 2 x QW_MMA_PROBE_MAX_CTAS of them); a wait that
@@ -451,6 +458,9 @@ qw_status qw_stream_read(const void* src, uint64_t bytes, uint32_t* sink, int32_
 #define QW_MMA_PROBE_F16_SMEM 1
 #define QW_MMA_PROBE_MXF8F6F4 2
 #define QW_MMA_PROBE_MXF8F6F4_CP 3
+#define QW_MMA_PROBE_MXF8F6F4_CP_AHEAD 4
+#define QW_MMA_PROBE_MXF8F6F4_CP_WIDE 5
+#define QW_MMA_PROBE_RANDOM 8
 #define QW_MMA_PROBE_MAX_CTAS 1024
 qw_status qw_mma_rate_probe(int32_t mode, int32_t n, int32_t iters, uint64_t* out,
                             int32_t* d_err, void* stream);

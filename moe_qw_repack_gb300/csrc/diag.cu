@@ -48,7 +48,9 @@ __global__ void __launch_bounds__(256) stream_read_kernel(const uint4* __restric
 constexpr int kProbeABox = 128 * 128;  // 128 rows x 128 bytes (one swizzle atom per row)
 constexpr int kProbeBBox = 256 * 128;  // up to 256 rows x 128 bytes
 constexpr int kProbeOperands = 2 * kProbeABox + 2 * kProbeBBox;
-constexpr int kProbeSf = 3 * 512;      // one A and two B scale images (128 rows x 4 groups)
+// one A and two B scale images (128 rows x 4 groups, 512 B each), or (wide copies) the same
+// with every 32-row image repeated for the four lane quarters: 2 KiB of A and 4 KiB of B
+constexpr int kProbeSf = 6 * 1024;
 // 120 KiB of shared memory: one probe CTA per SM (two would share its tensor core)
 constexpr size_t kProbeSmem = 120 * 1024;
 static_assert(kProbeOperands + kProbeSf + 64 + 1024 <= (int)kProbeSmem, "probe layout");
@@ -59,7 +61,7 @@ constexpr uint32_t kProbeSfCol = 320;
 
 template <int MODE>
 __global__ void __launch_bounds__(128, 1)
-    mma_probe_kernel(int n, int iters, uint64_t* __restrict__ out, int32_t* err) {
+    mma_probe_kernel(int n, int iters, int random, uint64_t* __restrict__ out, int32_t* err) {
   extern __shared__ uint8_t probe_raw[];
   uint8_t* sA = reinterpret_cast<uint8_t*>(((uintptr_t)probe_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sB = sA + 2 * kProbeABox;
@@ -69,9 +71,19 @@ __global__ void __launch_bounds__(128, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
   const int warp = threadIdx.x >> 5;
 
-  // zero operands (BF16, E4M3 and E2M1 zeros), scale bytes 127 (2^0)
-  for (int i = threadIdx.x; i < kProbeOperands / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(sA)[i] = make_uint4(0u, 0u, 0u, 0u);
+  // zero operands (BF16, E4M3 and E2M1 zeros), or (random) hashed bits, finite by their
+  // masks: BF16 with the top exponent bit clear (magnitudes below 2), E4M3 bytes with the
+  // lowest exponent bit clear (never the NaN code); scale bytes 127 (2^0)
+  const uint32_t mask = (MODE == QW_MMA_PROBE_F16_TMEM_A || MODE == QW_MMA_PROBE_F16_SMEM)
+                            ? 0xBF7FBF7Fu
+                            : 0xF7F7F7F7u;
+  for (int i = threadIdx.x; i < kProbeOperands / 4; i += blockDim.x) {
+    uint32_t h = (uint32_t)i * 0x9E3779B1u + 0x7F4A7C15u;  // a multiplicative hash of i
+    h ^= h >> 15;
+    h *= 0x2C1B3C6Du;
+    h ^= h >> 12;
+    reinterpret_cast<uint32_t*>(sA)[i] = random ? (h & mask) : 0u;
+  }
   for (int i = threadIdx.x; i < kProbeSf / 4; i += blockDim.x)
     reinterpret_cast<uint32_t*>(sSF)[i] = 0x7F7F7F7Fu;
   if (threadIdx.x == 0) {
@@ -109,11 +121,25 @@ __global__ void __launch_bounds__(128, 1)
       } else {
         const int kk = i & 3;  // 32-k MMA of a 128-k stage
         const uint32_t sfc = tbase + kProbeSfCol + 12u * (uint32_t)((i >> 2) & 3);
+        // scale columns of the next stage (copies issued a stage ahead of their MMAs)
+        const uint32_t sfn = tbase + kProbeSfCol + 12u * (uint32_t)(((i >> 2) + 1) & 3);
         if (MODE == QW_MMA_PROBE_MXF8F6F4_CP && kk == 0) {
           // the stage's scale images, as the W4A8 GEMM copies them
           tc_cp_32x128b_warpx4(sfc, smem_desc(sf0, 0, 128, 0));
           tc_cp_32x128b_warpx4(sfc + 4, smem_desc(sf0 + 512, 0, 128, 0));
           tc_cp_32x128b_warpx4(sfc + 8, smem_desc(sf0 + 1024, 0, 128, 0));
+        }
+        if (MODE == QW_MMA_PROBE_MXF8F6F4_CP_AHEAD && kk == 0) {
+          // the same three copies, into the next stage's columns
+          tc_cp_32x128b_warpx4(sfn, smem_desc(sf0, 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfn + 4, smem_desc(sf0 + 512, 0, 128, 0));
+          tc_cp_32x128b_warpx4(sfn + 8, smem_desc(sf0 + 1024, 0, 128, 0));
+        }
+        if (MODE == QW_MMA_PROBE_MXF8F6F4_CP_WIDE && kk == 0) {
+          // A's 4 columns in one 128-lane copy, B's 8 columns in another (rows of 32 bytes:
+          // two 16-byte core-matrix columns 128 bytes apart, 8-row groups 256 bytes apart)
+          tc_cp_128x128b(sfc, smem_desc(sf0, 0, 128, 0));
+          tc_cp_128x256b(sfc + 4, smem_desc(sf0 + 2048, 128, 256, 0));
         }
         tc_mma_mxf8f6f4(tbase, smem_desc(a0 + kk * 32, 16, 1024, 2),
                         smem_desc(b0 + kk * 32, 16, 1024, 2),
@@ -141,12 +167,12 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 template <int MODE>
-qw_status launch_probe_mode(int n, int iters, uint64_t* out, int32_t* err, int grid,
+qw_status launch_probe_mode(int n, int iters, int random, uint64_t* out, int32_t* err, int grid,
                             cudaStream_t st) {
   static const cudaError_t attr = cudaFuncSetAttribute(
       mma_probe_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kProbeSmem);
   if (attr != cudaSuccess) return QW_ERR_CUDA;
-  mma_probe_kernel<MODE><<<grid, 128, kProbeSmem, st>>>(n, iters, out, err);
+  mma_probe_kernel<MODE><<<grid, 128, kProbeSmem, st>>>(n, iters, random, out, err);
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 
@@ -154,17 +180,23 @@ qw_status launch_probe_mode(int n, int iters, uint64_t* out, int32_t* err, int g
 
 qw_status launch_mma_probe(int mode, int n, int iters, uint64_t* out, int32_t* err,
                            cudaStream_t st) {
+  const int random = (mode & QW_MMA_PROBE_RANDOM) != 0;
+  mode &= ~QW_MMA_PROBE_RANDOM;
   int grid = device_sm_count();
   if (grid > QW_MMA_PROBE_MAX_CTAS) grid = QW_MMA_PROBE_MAX_CTAS;
   switch (mode) {
     case QW_MMA_PROBE_F16_TMEM_A:
-      return launch_probe_mode<QW_MMA_PROBE_F16_TMEM_A>(n, iters, out, err, grid, st);
+      return launch_probe_mode<QW_MMA_PROBE_F16_TMEM_A>(n, iters, random, out, err, grid, st);
     case QW_MMA_PROBE_F16_SMEM:
-      return launch_probe_mode<QW_MMA_PROBE_F16_SMEM>(n, iters, out, err, grid, st);
+      return launch_probe_mode<QW_MMA_PROBE_F16_SMEM>(n, iters, random, out, err, grid, st);
     case QW_MMA_PROBE_MXF8F6F4:
-      return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4>(n, iters, out, err, grid, st);
+      return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4>(n, iters, random, out, err, grid, st);
+    case QW_MMA_PROBE_MXF8F6F4_CP:
+      return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4_CP>(n, iters, random, out, err, grid, st);
+    case QW_MMA_PROBE_MXF8F6F4_CP_AHEAD:
+      return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4_CP_AHEAD>(n, iters, random, out, err, grid, st);
     default:
-      return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4_CP>(n, iters, out, err, grid, st);
+      return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4_CP_WIDE>(n, iters, random, out, err, grid, st);
   }
 }
 

@@ -450,8 +450,10 @@ qw_status qw_stream_read(const void* src, uint64_t bytes, uint32_t* sink, int32_
 
 qw_status qw_mma_rate_probe(int32_t mode, int32_t n, int32_t iters, uint64_t* out,
                             int32_t* d_err, void* stream) {
-  const bool f16 = mode == QW_MMA_PROBE_F16_TMEM_A || mode == QW_MMA_PROBE_F16_SMEM;
-  const bool mx = mode == QW_MMA_PROBE_MXF8F6F4 || mode == QW_MMA_PROBE_MXF8F6F4_CP;
+  const int32_t base = mode & ~QW_MMA_PROBE_RANDOM;
+  const bool f16 = base == QW_MMA_PROBE_F16_TMEM_A || base == QW_MMA_PROBE_F16_SMEM;
+  const bool mx = base == QW_MMA_PROBE_MXF8F6F4 || base == QW_MMA_PROBE_MXF8F6F4_CP ||
+                  base == QW_MMA_PROBE_MXF8F6F4_CP_AHEAD || base == QW_MMA_PROBE_MXF8F6F4_CP_WIDE;
   if (!f16 && !mx) return QW_ERR_INVALID_ARG;
   // only the shapes the GEMMs issue (a shape outside the MMA's table would not assemble to
   // a valid instruction)

@@ -290,6 +290,9 @@ QW_MMA_PROBE_F16_TMEM_A = 0
 QW_MMA_PROBE_F16_SMEM = 1
 QW_MMA_PROBE_MXF8F6F4 = 2
 QW_MMA_PROBE_MXF8F6F4_CP = 3
+QW_MMA_PROBE_MXF8F6F4_CP_AHEAD = 4
+QW_MMA_PROBE_MXF8F6F4_CP_WIDE = 5
+QW_MMA_PROBE_RANDOM = 8
 QW_MMA_PROBE_MAX_CTAS = 1024
 
 
