@@ -253,6 +253,36 @@ def time_e2e_pipelined(probs, steps, warmup, world):
     return max_over_ranks(a.elapsed_time(b) / steps, world), steps
 
 
+def time_copies_only(probs, steps, world):
+    """The same per-step host copies as time_e2e_pipelined with no GEMM: copies in on one
+    stream, copies out on another, both directions at once.  Returns ms per step: the time
+    the node's host link alone needs for a step's bytes."""
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def step(i):
+        with torch.cuda.stream(s_in):
+            for pr in probs:
+                pr.load_slot(i % 2)
+        with torch.cuda.stream(s_out):
+            for pr in probs:
+                pr.store_slot((i + 1) % 2)
+    for i in range(2):
+        step(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    s_in.wait_event(a)
+    s_out.wait_event(a)
+    for i in range(steps):
+        step(i)
+    comp.wait_stream(s_in)
+    comp.wait_stream(s_out)
+    b.record(comp)
+    torch.cuda.synchronize()
+    return max_over_ranks(a.elapsed_time(b) / steps, world)
+
+
 def l2_bytes():
     return int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or (126 << 20))
 
@@ -711,6 +741,7 @@ def run_ours(args, world, rank):
     e_ms, e_n = time_e2e_pipelined(probs, max(3, args.steps), 2, world)
     h2d = sum(pr.A_host.numel() + pr.Asf_host.numel() for pr in probs)
     d2h = sum(pr.C.numel() * 2 for pr in probs)
+    link_ms = time_copies_only(probs, max(3, min(args.steps, 100)), world)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -730,7 +761,11 @@ def run_ours(args, world, rank):
                 "how": "qgemm_dense per step with its activations copied in from pinned host "
                        "memory and its BF16 results copied out to pinned host memory; copies in, "
                        "GEMMs and copies out on three streams over two device slots",
-                "steps": e_n},
+                "steps": e_n,
+                # the same copies with no GEMM: what the host link alone allows
+                "copies_only_ms_per_step": round(link_ms, 4),
+                "host_link_GBps": round((h2d + d2h) / (link_ms * 1e-3) / 1e9, 1),
+                "frac_of_copies_only": round(link_ms / e_ms, 3)},
         "gpu_launches": len(fns) * n,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
@@ -763,7 +798,8 @@ def summarize(line):
     of the workload list, so that the end of the printed line carries all of them."""
     ex = line.get("extra", {})
     sm = {"cfg2_w4a8_frac_fp8": line["roofline"]["frac"],
-          "e2e_over_device": round(line["e2e"]["value"] / line["value"], 3)}
+          "e2e_over_device": round(line["e2e"]["value"] / line["value"], 3),
+          "e2e_frac_of_host_link": line["e2e"].get("frac_of_copies_only")}
 
     def get(name, key):
         v = ex.get(name, {}).get(key)

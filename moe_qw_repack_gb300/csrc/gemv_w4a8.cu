@@ -20,11 +20,20 @@
 // weight rows g and g + 8, and the same k of token row g for the B fragment - any fixed
 // assignment of k to MMA slots gives the same sum, as long as both operands use it.
 // Work item = 16 weight rows over all of K; the 8 warps of a CTA split the groups and meet
-// in shared memory (fixed-order sum).  Each warp keeps the next 16 groups' code words in a
-// register ring (4 KiB per warp in flight) and stages its groups' activations once, already
-// decoded (FP16 B fragments and FP32 scales in shared memory), so the inner loop is two
-// shared loads, eight conversions and two MMAs per group.  Launched as a programmatic
-// dependent: only weights and their scales are read before griddepcontrol.wait.
+// in shared memory (fixed-order sum).  Each warp streams its groups through its own ring of
+// 2-4 shared-memory stages, one TMA box of 16 rows x 128 bytes (eight groups) each, stored
+// with the 128-byte swizzle so that the lanes' 4-byte fragment reads (word t of chunk j of
+// rows g and g + 8) fall in 32 different banks; lane 0 refills a slot as soon as the warp
+// has read it.  (Reading the fragments straight from global memory, 4 bytes per lane from
+// 8 rows at a time, used half of every 32-byte sector per instruction: 2.2x the sector
+// traffic.)  The activations are staged once per warp, already decoded (FP16 B fragments
+// and FP32 scales in shared memory).  Launched as a programmatic dependent: only weights
+// and their scales are read before griddepcontrol.wait.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "qw_common.cuh"
 #include "qw_internal.h"
 
@@ -32,7 +41,9 @@ namespace qw {
 namespace {
 
 constexpr int kW8Warps = 8;
-constexpr int kW8Ring = 16;  // scale groups per batch (two code words per group and lane)
+constexpr int kW8StageGroups = 8;                       // scale groups per ring stage
+constexpr int kW8StageBytes = 16 * kW8StageGroups * 16;  // one TMA box: 16 rows x 128 bytes
+constexpr int kW8MaxStages = 4;                          // ring stages per warp
 
 // two E8M0 scales (the low 16 bits of `pair`) -> 2^(s - 127) as a BF16 pair, exactly (the
 // smallest, 2^-127, is a BF16 subnormal)
@@ -62,15 +73,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
 }
 
 struct W4A8GemvParams {
-  const uint8_t* wp;   // codes [N_pad][K_pad / 2]
   const uint8_t* sp;   // E8M0 in 512-byte chunks of 128 rows x 4 groups
   const uint8_t* A;    // E4M3 [M][K]
   const uint8_t* Asf;  // E8M0 [M][K / 32]
   const uint16_t* bias;
   uint16_t* C;
   int32_t N, N_pad, K, K_pad, M;
-  int32_t gpw;  // scale groups per warp, a multiple of 4
+  int32_t gpw;          // scale groups per warp, a multiple of kW8StageGroups
+  int32_t stages;       // ring stages per warp, 2 .. kW8MaxStages
   const float* scale2;  // second-level scales [N_pad] or null
+  int32_t* err;         // QW_ERR_TIMEOUT if a ring wait gives up
 };
 
 // Byte offset of the 4 scales (row r, groups 4q .. 4q + 3) in the chunked layout.
@@ -78,77 +90,88 @@ __device__ __forceinline__ int64_t sf_word_offset(int64_t r, int q, int K_pad) {
   return ((r >> 7) * (K_pad >> 7) + q) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
 }
 
-__global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8GemvParams p) {
-  constexpr int R = kW8Ring;
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// ONE: a single token row (only the D fragment's column 0 is ever stored: lanes t = 0 keep
+// rows g and g + 8; the other columns' scale work is skipped)
+template <bool ONE>
+__global__ void __launch_bounds__(kW8Warps * 32, 2)
+    gemv_w4a8_kernel(const __grid_constant__ CUtensorMap tmW, const W4A8GemvParams p) {
   __shared__ float red[2][kW8Warps * 128];
-  extern __shared__ uint4 w8_smem[];
+  __shared__ uint64_t full[kW8Warps][kW8MaxStages];
+  __shared__ int abort_flag;
+  extern __shared__ uint8_t w8_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
+  const int S = p.stages;
   const int G = p.K >> 5;
   const uint32_t nblocks = (uint32_t)(p.N_pad >> 4);
   const int g0 = min(G, warp * p.gpw);
   const int cnt = min(G, g0 + p.gpw) - g0;  // this warp's groups per item (may be 0)
-  const int nbat = (cnt + R - 1) / R;
-  const int64_t row_bytes = p.K_pad >> 1;
+  const int nst = (cnt + kW8StageGroups - 1) / kW8StageGroups;  // its stages per item
   const uint32_t my_items =
       blockIdx.x < nblocks ? (nblocks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const uint32_t total = my_items * (uint32_t)nst;  // the warp's stage sequence
+  // the warps' rings (1 KiB aligned: the 128-byte swizzle repeats every 1 KiB), then the
+  // staged activations
+  const uint32_t pad = (1024u - (smem_u32(w8_smem) & 1023u)) & 1023u;
+  uint8_t* ring = w8_smem + pad + (size_t)warp * S * kW8StageBytes;
+  uint8_t* act = w8_smem + pad + (size_t)kW8Warps * S * kW8StageBytes;
+  uint64_t* bar = full[warp];
+  volatile int* abort = &abort_flag;
 
+  if (threadIdx.x == 0) abort_flag = 0;
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
   pdl_launch_dependents();
 
-  // ring: code words of rows g and g + 8 for the batch's groups, and their scale words
-  uint32_t wr[R][2];
-  uint32_t sw[R / 4][2];
-  const uint8_t* rw = nullptr;  // row g's code bytes at the refilling batch's first group
-  int rg = 0;                   // first group of the refilling batch
-  int rng = 0;                  // its group count (0: nothing left)
-  int64_t rrow = 0;             // row g of the refilling batch's item
-  uint32_t nx_it = 0;
-  int nx_c = 0;
-  auto point = [&](uint32_t it, int c) {
-    rng = 0;
-    if (it < my_items && c < nbat) {
-      const uint32_t nb = blockIdx.x + it * gridDim.x;
-      rg = g0 + R * c;
-      rrow = (int64_t)nb * 16 + g;
-      rw = p.wp + rrow * row_bytes + rg * 16 + 4 * t;
-      rng = min(R, g0 + cnt - rg);
+  // stage q of the warp's sequence: item q / nst, groups g0 + 8 (q % nst) .. + 7 of its
+  // 16-row block, one TMA box into slot q % S (lane 0 only)
+  auto issue = [&](uint32_t q) {
+    const uint32_t it = q / (uint32_t)nst;
+    const int c = (int)(q - it * (uint32_t)nst);
+    const int s = (int)(q % (uint32_t)S);
+    mbar_arrive_expect_tx(&bar[s], kW8StageBytes);
+    tma_load_2d(ring + s * kW8StageBytes, &tmW, &bar[s], (g0 + kW8StageGroups * c) * 16,
+                (int32_t)((blockIdx.x + it * gridDim.x) * 16));
+  };
+  // the scale words of stage q: rows g and g + 8 for its (at most two) groups of four
+  auto load_scales = [&](uint32_t q, uint32_t (&w)[4]) {
+    if (q >= total) return;
+    const uint32_t it = q / (uint32_t)nst;
+    const int c = (int)(q - it * (uint32_t)nst);
+    const int64_t row = (int64_t)(blockIdx.x + it * gridDim.x) * 16 + g;
+    const int gb = g0 + kW8StageGroups * c;
+    const int qd = gb >> 2;
+    w[0] = __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(row, qd, p.K_pad)));
+    w[1] = __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(row + 8, qd, p.K_pad)));
+    if (gb + 4 < g0 + cnt) {
+      w[2] = __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(row, qd + 1, p.K_pad)));
+      w[3] =
+          __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(row + 8, qd + 1, p.K_pad)));
     }
   };
-  auto advance = [&]() {
-    if (++nx_c == nbat) {
-      nx_c = 0;
-      ++nx_it;
-    }
-    point(nx_it, nx_c);
-  };
-  // slot j's code words; scale word b covers slots 4b .. 4b + 3 (rg is a multiple of 4)
-  auto refill_w = [&](int j) {
-    if (j < rng) {
-      wr[j][0] = __ldcs(reinterpret_cast<const uint32_t*>(rw + j * 16));
-      wr[j][1] = __ldcs(reinterpret_cast<const uint32_t*>(rw + 8 * row_bytes + j * 16));
-    }
-  };
-  auto refill_s = [&](int b) {
-    if (4 * b < rng) {
-      const int q = (rg >> 2) + b;
-      sw[b][0] = __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(rrow, q, p.K_pad)));
-      sw[b][1] =
-          __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(rrow + 8, q, p.K_pad)));
-    }
-  };
-  point(0, 0);
-#pragma unroll
-  for (int j = 0; j < R; ++j) refill_w(j);
-#pragma unroll
-  for (int b = 0; b < R / 4; ++b) refill_s(b);
-  advance();
+
+  // weights do not depend on the previous kernel: the first stages stream before the wait
+  uint32_t issued = 0;
+  if (lane == 0)
+    for (; issued < total && issued < (uint32_t)S; ++issued) issue(issued);
+  issued = __shfl_sync(0xFFFFFFFFu, issued, 0);
+  uint32_t sc_a[4] = {0u, 0u, 0u, 0u}, sc_b[4] = {0u, 0u, 0u, 0u};
+  load_scales(0, sc_a);
 
   // ---- activations (the previous kernel's output may be A): each warp stages its own
   // groups once, decoded - B fragments as FP16 pairs [group][row][t][4 x f16x2] and the
   // scales as FP32 [group][8 tokens] (tokens past M get 0: never stored)
   pdl_wait();
   const int KG = p.K >> 5;
-  uint8_t* act = reinterpret_cast<uint8_t*>(w8_smem);
   float* fa = reinterpret_cast<float*>(act + (size_t)G * p.M * 64);
   for (int q = lane; q < cnt * p.M * 4; q += 32) {
     const int tt = q & 3, m = (q >> 2) % p.M, gl = (q >> 2) / p.M;
@@ -168,31 +191,45 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
   const uint32_t act_lane = smem_u32(act) + (uint32_t)(((g < p.M ? g : 0) * 4 + t) * 16);
   const uint32_t grp_stride = (uint32_t)p.M * 64;
   const uint32_t fa_lane = smem_u32(fa) + (uint32_t)(2 * t * 4);
+  // lane (g, t) reads word t of 16-byte chunk j of rows g and g + 8 of a slot; the TMA's
+  // 128-byte swizzle stores chunk j of row r at chunk j ^ (r % 8)
+  const uint32_t ring_lane = smem_u32(ring) + (uint32_t)(g * 128 + 4 * t);
 
-  for (uint32_t it = 0; it < my_items; ++it) {
-    const uint32_t nb = blockIdx.x + it * gridDim.x;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c = 0; c < nbat; ++c) {
-      const int gb = g0 + R * c;
-      const int ng = min(R, g0 + cnt - gb);
+  bool ok = true;       // warp-uniform
+  uint32_t done = 0;    // stages whose copies have landed
+  // one stage: wait for its slot, eight groups of MMAs, refill the slot with stage q + S;
+  // `cur` holds this stage's scale words, `nxt` receives the next stage's
+  auto stage = [&](uint32_t q, int c, const uint32_t (&cur)[4], uint32_t (&nxt)[4],
+                   float (&acc)[4]) {
+    load_scales(q + 1, nxt);
+    const int s = (int)(q % (uint32_t)S);
+    if (ok) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[s], (q / (uint32_t)S) & 1u, abort, p.err));
+      if (ok) ++done;
+    }
+    if (ok) {
+      const uint32_t slot = ring_lane + (uint32_t)(s * kW8StageBytes);
+      const int gb = g0 + kW8StageGroups * c;
+      const int ng = min(kW8StageGroups, g0 + cnt - gb);
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
+      for (int j = 0; j < kW8StageGroups; ++j) {
         if (j < ng) {
           const int gg = gb + j;
+          const uint32_t off = (uint32_t)((j ^ g) << 4);
+          const uint32_t wa = lds32(slot + off), wb = lds32(slot + 1024u + off);
           uint4 x;
           asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
                        : "r"(act_lane + (uint32_t)gg * grp_stride));
           uint2 f2;
-          asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                       : "=r"(f2.x), "=r"(f2.y)
-                       : "r"(fa_lane + (uint32_t)gg * 32));
-          const uint32_t wa = wr[j][0], wb = wr[j][1];
-          const uint32_t swa = sw[j >> 2][0], swb = sw[j >> 2][1];
-          // slot j (and after its last group, scale word j / 4) is free: start loading the
-          // next batch's
-          refill_w(j);
-          if ((j & 3) == 3) refill_s(j >> 2);
+          if constexpr (ONE) {
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(f2.x) : "r"(fa_lane + (uint32_t)gg * 32));
+            f2.y = 0u;
+          } else {
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(f2.x), "=r"(f2.y)
+                         : "r"(fa_lane + (uint32_t)gg * 32));
+          }
           float pr[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t ca[4], cb[4];  // FP16 pairs of the code bytes of rows g and g + 8
           e2m1x8_to_f16x2(wa, ca);
@@ -202,26 +239,42 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
             const uint32_t a[4] = {ca[2 * st], cb[2 * st], ca[2 * st + 1], cb[2 * st + 1]};
             mma_f16_16816(pr, a, st ? x.z : x.x, st ? x.w : x.y);
           }
-          // this group's byte of each row's scale word (gb % 4 == 0), both converted at once
+          // this group's byte of each row's scale word, both converted at once
+          const uint32_t swa = cur[(j >> 2) * 2], swb = cur[(j >> 2) * 2 + 1];
           const uint32_t sbyte = (uint32_t)(j & 3);
           const uint32_t wsc = e8m0x2_to_bf16x2(__byte_perm(swa, swb, sbyte | ((4u + sbyte) << 4)));
           const float fw0 = __uint_as_float(wsc << 16);
           const float fw1 = __uint_as_float(wsc & 0xFFFF0000u);
           const float fa0 = __uint_as_float(f2.x), fa1 = __uint_as_float(f2.y);
-          acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
-          acc[1] = fmaf(pr[1] * fw0, fa1, acc[1]);
-          acc[2] = fmaf(pr[2] * fw1, fa0, acc[2]);
-          acc[3] = fmaf(pr[3] * fw1, fa1, acc[3]);
+          if constexpr (ONE) {
+            acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
+            acc[2] = fmaf(pr[2] * fw1, fa0, acc[2]);
+          } else {
+            acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
+            acc[1] = fmaf(pr[1] * fw0, fa1, acc[1]);
+            acc[2] = fmaf(pr[2] * fw1, fa0, acc[2]);
+            acc[3] = fmaf(pr[3] * fw1, fa1, acc[3]);
+          }
         }
       }
-      // slots and scale words the loop did not reach
-#pragma unroll
-      for (int j = 0; j < R; ++j)
-        if (j >= ng) refill_w(j);
-#pragma unroll
-      for (int b = 0; b < R / 4; ++b)
-        if (4 * b + 3 >= ng) refill_s(b);
-      advance();
+    }
+    // every lane has read the slot: it takes stage q + S
+    __syncwarp();
+    if (ok && issued < total) {
+      if (lane == 0) issue(issued);
+      ++issued;
+    }
+  };
+
+  uint32_t q = 0;
+  for (uint32_t it = 0; it < my_items; ++it) {
+    const uint32_t nb = blockIdx.x + it * gridDim.x;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < nst; ++c, ++q) {
+      if (q & 1u)
+        stage(q, c, sc_b, sc_a, acc);
+      else
+        stage(q, c, sc_a, sc_b, acc);
     }
 
     // split-K reduction over the CTA's warps, fixed order; one barrier per item
@@ -244,18 +297,54 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2) gemv_w4a8_kernel(const W4A8G
       }
     }
   }
+  // a wait that gave up leaves copies in flight: let them land before shared memory goes
+  if (!ok && lane == 0) {
+    for (uint32_t qq = done; qq < issued; ++qq) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&bar[qq % (uint32_t)S], (qq / (uint32_t)S) & 1u))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 w8_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &r) == cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
 }
 
 }  // namespace
 
 qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
                            const void* A, const void* A_sf, const void* bias, const float* scale2,
-                           void* C, int M, cudaStream_t st) {
+                           void* C, int M, int32_t* err, cudaStream_t st) {
   if (M < 1 || M > kW4A8GemvRows || d.E != 1 || d.wfmt != QW_W_MXFP4_G32 ||
       w4a8_gemv_smem_bytes(d.K, M) > kW4A8GemvMaxSmem)
     return QW_ERR_UNSUPPORTED;
+  auto enc = w8_encode_fn();
+  if (!enc) return QW_ERR_CUDA;
+  // the packed codes as [N_pad rows][K_pad / 2 bytes]; a box is 16 rows x 128 bytes (eight
+  // groups of 32 codes), stored with the 128-byte swizzle
+  CUtensorMap tmW;
+  {
+    cuuint64_t gdim[2] = {(cuuint64_t)(d.K_pad / 2), (cuuint64_t)d.N_pad};
+    cuuint64_t gstr[1] = {(cuuint64_t)(d.K_pad / 2)};
+    cuuint32_t box[2] = {128, 16};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w_packed), gdim, gstr, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QW_ERR_ALIGNMENT;
+  }
   W4A8GemvParams p{};
-  p.wp = static_cast<const uint8_t*>(w_packed);
   p.sp = static_cast<const uint8_t*>(s_packed);
   p.A = static_cast<const uint8_t*>(A);
   p.Asf = static_cast<const uint8_t*>(A_sf);
@@ -267,12 +356,32 @@ qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   p.K_pad = d.K_pad;
   p.M = M;
   p.scale2 = scale2;
+  p.err = err;
   const int G = d.K / kMxGroup;
-  p.gpw = ((G + kW8Warps - 1) / kW8Warps + 3) / 4 * 4;
-  auto kern = gemv_w4a8_kernel;
-  const size_t smem = w4a8_gemv_smem_bytes(d.K, M);
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kW4A8GemvMaxSmem);
+  p.gpw = ((G + kW8Warps - 1) / kW8Warps + kW8StageGroups - 1) / kW8StageGroups * kW8StageGroups;
+  // the deepest ring that still lets two CTAs share an SM (one CTA per SM otherwise)
+  const size_t act = w4a8_gemv_smem_bytes(d.K, M);
+  auto dyn = [&](int stages) {
+    return act + 1024 + (size_t)kW8Warps * stages * kW8StageBytes;
+  };
+  constexpr size_t kStatic = sizeof(float) * 2 * kW8Warps * 128 + 8 * kW8Warps * kW8MaxStages + 64;
+  constexpr size_t kSmPerSm = 228 * 1024, kReserve = 1024;  // per SM; per CTA
+  p.stages = kW8MaxStages;
+  for (int stages = kW8MaxStages; stages >= 2; --stages)
+    if (2 * (dyn(stages) + kStatic + kReserve) <= kSmPerSm) {
+      p.stages = stages;
+      break;
+    }
+  auto kern = M == 1 ? gemv_w4a8_kernel<true> : gemv_w4a8_kernel<false>;
+  const size_t smem = dyn(p.stages);
+  const int max_dyn =
+      (int)(kW4A8GemvMaxSmem + 1024 + (size_t)kW8Warps * kW8MaxStages * kW8StageBytes);
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(gemv_w4a8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           max_dyn) == cudaSuccess
+          ? cudaFuncSetAttribute(gemv_w4a8_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn)
+          : cudaErrorInvalidValue;
   if (attr != cudaSuccess) return QW_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kW8Warps * 32, smem) !=
@@ -293,7 +402,7 @@ qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return QW_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, tmW, p) != cudaSuccess) return QW_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ERR_CUDA;
 }
 

@@ -275,7 +275,8 @@ qw_status qgemm_dense(const qw_packed_desc* desc, const void* w_packed, const vo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (bd.wfmt == QW_W_MXFP4_G32 && M <= kW4A8GemvRows &&
       w4a8_gemv_smem_bytes(bd.K, (int)M) <= kW4A8GemvMaxSmem)
-    return launch_gemv_w4a8(bd, w_packed, s_packed, A, A_sf, bias, rs.scale2, C, (int)M, st);
+    return launch_gemv_w4a8(bd, w_packed, s_packed, A, A_sf, bias, rs.scale2, C, (int)M, d_err,
+                            st);
   if (is_mx(bd.wfmt))
     return launch_gemm_w4a8(bd, w_packed, s_packed, A, A_sf, bias, C, rs, workspace, ws_bytes,
                             d_err, st);

@@ -103,7 +103,7 @@ constexpr size_t w4a8_gemv_smem_bytes(int K, int M) {
 }
 qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const void* s_packed,
                            const void* A, const void* A_sf, const void* bias, const float* scale2,
-                           void* C, int M, cudaStream_t st);
+                           void* C, int M, int32_t* err, cudaStream_t st);
 
 // MoE scheduling.
 qw_status launch_moe_route(const float* logits, int32_t T, int32_t E, int32_t topk,
