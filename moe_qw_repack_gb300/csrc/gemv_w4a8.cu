@@ -85,11 +85,6 @@ struct W4A8GemvParams {
   int32_t* err;         // QW_ERR_TIMEOUT if a ring wait gives up
 };
 
-// Byte offset of the 4 scales (row r, groups 4q .. 4q + 3) in the chunked layout.
-__device__ __forceinline__ int64_t sf_word_offset(int64_t r, int q, int K_pad) {
-  return ((r >> 7) * (K_pad >> 7) + q) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
-}
-
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -132,40 +127,56 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2)
   __syncthreads();
   pdl_launch_dependents();
 
-  // stage q of the warp's sequence: item q / nst, groups g0 + 8 (q % nst) .. + 7 of its
-  // 16-row block, one TMA box into slot q % S (lane 0 only)
-  auto issue = [&](uint32_t q) {
-    const uint32_t it = q / (uint32_t)nst;
-    const int c = (int)(q - it * (uint32_t)nst);
-    const int s = (int)(q % (uint32_t)S);
-    mbar_arrive_expect_tx(&bar[s], kW8StageBytes);
-    tma_load_2d(ring + s * kW8StageBytes, &tmW, &bar[s], (g0 + kW8StageGroups * c) * 16,
-                (int32_t)((blockIdx.x + it * gridDim.x) * 16));
+  // issue cursor: the next stage to copy (item, stage within the item, ring slot); every
+  // lane advances it, lane 0 issues the copy
+  uint32_t i_it = 0;
+  int i_c = 0, i_s = 0;
+  uint32_t issued = 0;
+  auto issue_next = [&]() {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar[i_s], kW8StageBytes);
+      tma_load_2d(ring + i_s * kW8StageBytes, &tmW, &bar[i_s], (g0 + kW8StageGroups * i_c) * 16,
+                  (int32_t)((blockIdx.x + i_it * gridDim.x) * 16));
+    }
+    ++issued;
+    if (++i_c == nst) {
+      i_c = 0;
+      ++i_it;
+    }
+    if (++i_s == S) i_s = 0;
   };
-  // the scale words of stage q: rows g and g + 8 for its (at most two) groups of four
-  auto load_scales = [&](uint32_t q, uint32_t (&w)[4]) {
-    if (q >= total) return;
-    const uint32_t it = q / (uint32_t)nst;
-    const int c = (int)(q - it * (uint32_t)nst);
-    const int64_t row = (int64_t)(blockIdx.x + it * gridDim.x) * 16 + g;
-    const int gb = g0 + kW8StageGroups * c;
-    const int qd = gb >> 2;
-    w[0] = __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(row, qd, p.K_pad)));
-    w[1] = __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(row + 8, qd, p.K_pad)));
+  // scale cursor: the next stage whose scale words are loaded.  Row g's word of groups
+  // 4Q .. 4Q + 3 sits at srow + 512 Q; row g + 8's 128 bytes after it (rows g and g + 8 of
+  // a 16-row block share their 32-row lane group)
+  uint32_t s_q = 0, s_it = 0;
+  int s_c = 0;
+  const uint8_t* srow = nullptr;
+  auto load_scales_next = [&](uint32_t (&w)[4]) {
+    if (s_q >= total) return;
+    ++s_q;
+    if (s_c == 0) {
+      const int64_t row = (int64_t)(blockIdx.x + s_it * gridDim.x) * 16 + g;
+      srow = p.sp + (row >> 7) * (int64_t)(p.K_pad >> 7) * 512 + (row & 31) * 16 +
+             ((row & 127) >> 5) * 4;
+    }
+    const int gb = g0 + kW8StageGroups * s_c;
+    const uint8_t* a = srow + (gb >> 2) * 512;
+    w[0] = __ldg(reinterpret_cast<const uint32_t*>(a));
+    w[1] = __ldg(reinterpret_cast<const uint32_t*>(a + 128));
     if (gb + 4 < g0 + cnt) {
-      w[2] = __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(row, qd + 1, p.K_pad)));
-      w[3] =
-          __ldg(reinterpret_cast<const uint32_t*>(p.sp + sf_word_offset(row + 8, qd + 1, p.K_pad)));
+      w[2] = __ldg(reinterpret_cast<const uint32_t*>(a + 512));
+      w[3] = __ldg(reinterpret_cast<const uint32_t*>(a + 640));
+    }
+    if (++s_c == nst) {
+      s_c = 0;
+      ++s_it;
     }
   };
 
   // weights do not depend on the previous kernel: the first stages stream before the wait
-  uint32_t issued = 0;
-  if (lane == 0)
-    for (; issued < total && issued < (uint32_t)S; ++issued) issue(issued);
-  issued = __shfl_sync(0xFFFFFFFFu, issued, 0);
+  while (issued < total && issued < (uint32_t)S) issue_next();
   uint32_t sc_a[4] = {0u, 0u, 0u, 0u}, sc_b[4] = {0u, 0u, 0u, 0u};
-  load_scales(0, sc_a);
+  load_scales_next(sc_a);
 
   // ---- activations (the previous kernel's output may be A): each warp stages its own
   // groups once, decoded - B fragments as FP16 pairs [group][row][t][4 x f16x2] and the
@@ -197,73 +208,79 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2)
 
   bool ok = true;       // warp-uniform
   uint32_t done = 0;    // stages whose copies have landed
-  // one stage: wait for its slot, eight groups of MMAs, refill the slot with stage q + S;
-  // `cur` holds this stage's scale words, `nxt` receives the next stage's
-  auto stage = [&](uint32_t q, int c, const uint32_t (&cur)[4], uint32_t (&nxt)[4],
-                   float (&acc)[4]) {
-    load_scales(q + 1, nxt);
-    const int s = (int)(q % (uint32_t)S);
+  int w_s = 0;          // ring slot of the stage being consumed
+  uint32_t w_ph = 0;    // and the phase it completes
+  // one group: MMAs over its 32 k, then the two scales
+  auto group = [&](uint32_t slot, int j, int gg, const uint32_t (&cur)[4], float (&acc)[4]) {
+    const uint32_t off = (uint32_t)((j ^ g) << 4);
+    const uint32_t wa = lds32(slot + off), wb = lds32(slot + 1024u + off);
+    uint4 x;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                 : "r"(act_lane + (uint32_t)gg * grp_stride));
+    uint2 f2;
+    if constexpr (ONE) {
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(f2.x) : "r"(fa_lane + (uint32_t)gg * 32));
+      f2.y = 0u;
+    } else {
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                   : "=r"(f2.x), "=r"(f2.y)
+                   : "r"(fa_lane + (uint32_t)gg * 32));
+    }
+    float pr[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t ca[4], cb[4];  // FP16 pairs of the code bytes of rows g and g + 8
+    e2m1x8_to_f16x2(wa, ca);
+    e2m1x8_to_f16x2(wb, cb);
+#pragma unroll
+    for (int st = 0; st < 2; ++st) {  // code bytes 2st, 2st + 1 of each row
+      const uint32_t a[4] = {ca[2 * st], cb[2 * st], ca[2 * st + 1], cb[2 * st + 1]};
+      mma_f16_16816(pr, a, st ? x.z : x.x, st ? x.w : x.y);
+    }
+    // this group's byte of each row's scale word, both converted at once
+    const uint32_t swa = cur[(j >> 2) * 2], swb = cur[(j >> 2) * 2 + 1];
+    const uint32_t sbyte = (uint32_t)(j & 3);
+    const uint32_t wsc = e8m0x2_to_bf16x2(__byte_perm(swa, swb, sbyte | ((4u + sbyte) << 4)));
+    const float fw0 = __uint_as_float(wsc << 16);
+    const float fw1 = __uint_as_float(wsc & 0xFFFF0000u);
+    const float fa0 = __uint_as_float(f2.x), fa1 = __uint_as_float(f2.y);
+    if constexpr (ONE) {
+      acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
+      acc[2] = fmaf(pr[2] * fw1, fa0, acc[2]);
+    } else {
+      acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
+      acc[1] = fmaf(pr[1] * fw0, fa1, acc[1]);
+      acc[2] = fmaf(pr[2] * fw1, fa0, acc[2]);
+      acc[3] = fmaf(pr[3] * fw1, fa1, acc[3]);
+    }
+  };
+  // one stage: wait for its slot, its groups' MMAs, refill the slot with the next stage to
+  // copy; `cur` holds this stage's scale words, `nxt` receives the next stage's
+  auto stage = [&](int c, const uint32_t (&cur)[4], uint32_t (&nxt)[4], float (&acc)[4]) {
+    load_scales_next(nxt);
     if (ok) {
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[s], (q / (uint32_t)S) & 1u, abort, p.err));
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[w_s], w_ph, abort, p.err));
       if (ok) ++done;
     }
     if (ok) {
-      const uint32_t slot = ring_lane + (uint32_t)(s * kW8StageBytes);
+      const uint32_t slot = ring_lane + (uint32_t)(w_s * kW8StageBytes);
       const int gb = g0 + kW8StageGroups * c;
       const int ng = min(kW8StageGroups, g0 + cnt - gb);
+      if (ng == kW8StageGroups) {
 #pragma unroll
-      for (int j = 0; j < kW8StageGroups; ++j) {
-        if (j < ng) {
-          const int gg = gb + j;
-          const uint32_t off = (uint32_t)((j ^ g) << 4);
-          const uint32_t wa = lds32(slot + off), wb = lds32(slot + 1024u + off);
-          uint4 x;
-          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
-                       : "r"(act_lane + (uint32_t)gg * grp_stride));
-          uint2 f2;
-          if constexpr (ONE) {
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(f2.x) : "r"(fa_lane + (uint32_t)gg * 32));
-            f2.y = 0u;
-          } else {
-            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                         : "=r"(f2.x), "=r"(f2.y)
-                         : "r"(fa_lane + (uint32_t)gg * 32));
-          }
-          float pr[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t ca[4], cb[4];  // FP16 pairs of the code bytes of rows g and g + 8
-          e2m1x8_to_f16x2(wa, ca);
-          e2m1x8_to_f16x2(wb, cb);
+        for (int j = 0; j < kW8StageGroups; ++j) group(slot, j, gb + j, cur, acc);
+      } else {
 #pragma unroll
-          for (int st = 0; st < 2; ++st) {  // code bytes 2st, 2st + 1 of each row
-            const uint32_t a[4] = {ca[2 * st], cb[2 * st], ca[2 * st + 1], cb[2 * st + 1]};
-            mma_f16_16816(pr, a, st ? x.z : x.x, st ? x.w : x.y);
-          }
-          // this group's byte of each row's scale word, both converted at once
-          const uint32_t swa = cur[(j >> 2) * 2], swb = cur[(j >> 2) * 2 + 1];
-          const uint32_t sbyte = (uint32_t)(j & 3);
-          const uint32_t wsc = e8m0x2_to_bf16x2(__byte_perm(swa, swb, sbyte | ((4u + sbyte) << 4)));
-          const float fw0 = __uint_as_float(wsc << 16);
-          const float fw1 = __uint_as_float(wsc & 0xFFFF0000u);
-          const float fa0 = __uint_as_float(f2.x), fa1 = __uint_as_float(f2.y);
-          if constexpr (ONE) {
-            acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
-            acc[2] = fmaf(pr[2] * fw1, fa0, acc[2]);
-          } else {
-            acc[0] = fmaf(pr[0] * fw0, fa0, acc[0]);
-            acc[1] = fmaf(pr[1] * fw0, fa1, acc[1]);
-            acc[2] = fmaf(pr[2] * fw1, fa0, acc[2]);
-            acc[3] = fmaf(pr[3] * fw1, fa1, acc[3]);
-          }
-        }
+        for (int j = 0; j < kW8StageGroups; ++j)
+          if (j < ng) group(slot, j, gb + j, cur, acc);
       }
     }
-    // every lane has read the slot: it takes stage q + S
-    __syncwarp();
-    if (ok && issued < total) {
-      if (lane == 0) issue(issued);
-      ++issued;
+    if (++w_s == S) {
+      w_s = 0;
+      w_ph ^= 1u;
     }
+    // every lane has read the slot: it takes the next stage to copy
+    __syncwarp();
+    if (ok && issued < total) issue_next();
   };
 
   uint32_t q = 0;
@@ -272,9 +289,9 @@ __global__ void __launch_bounds__(kW8Warps * 32, 2)
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int c = 0; c < nst; ++c, ++q) {
       if (q & 1u)
-        stage(q, c, sc_b, sc_a, acc);
+        stage(c, sc_b, sc_a, acc);
       else
-        stage(q, c, sc_a, sc_b, acc);
+        stage(c, sc_a, sc_b, acc);
     }
 
     // split-K reduction over the CTA's warps, fixed order; one barrier per item
