@@ -21,7 +21,7 @@
 // assignment of k to MMA slots gives the same sum, as long as both operands use it.
 // Work item = 16 weight rows over all of K; the 8 warps of a CTA split the groups and meet
 // in shared memory (fixed-order sum).  Each warp streams its groups through its own ring of
-// 2-4 shared-memory stages, one TMA box of 16 rows x 128 bytes (eight groups) each, stored
+// two shared-memory stages, one TMA box of 16 rows x 128 bytes (eight groups) each, stored
 // with the 128-byte swizzle so that the lanes' 4-byte fragment reads (word t of chunk j of
 // rows g and g + 8) fall in 32 different banks; lane 0 refills a slot as soon as the warp
 // has read it.  (Reading the fragments straight from global memory, 4 bytes per lane from
@@ -43,7 +43,9 @@ namespace {
 constexpr int kW8Warps = 8;
 constexpr int kW8StageGroups = 8;                       // scale groups per ring stage
 constexpr int kW8StageBytes = 16 * kW8StageGroups * 16;  // one TMA box: 16 rows x 128 bytes
-constexpr int kW8MaxStages = 4;                          // ring stages per warp
+// ring stages per warp: measured on GB300 (M = 1, 14336 x 4096 / 4096 x 14336 / 4096 x
+// 4096), two stages ran 9.4 / 10.5 / 4.3 us, three 10.4 / 10.9 / 4.6, four 10.8 / 11.1 / 4.3
+constexpr int kW8MaxStages = 2;
 
 // two E8M0 scales (the low 16 bits of `pair`) -> 2^(s - 127) as a BF16 pair, exactly (the
 // smallest, 2^-127, is a BF16 subnormal)
@@ -80,7 +82,7 @@ struct W4A8GemvParams {
   uint16_t* C;
   int32_t N, N_pad, K, K_pad, M;
   int32_t gpw;          // scale groups per warp, a multiple of kW8StageGroups
-  int32_t stages;       // ring stages per warp, 2 .. kW8MaxStages
+  int32_t stages;       // ring stages per warp (kW8MaxStages)
   const float* scale2;  // second-level scales [N_pad] or null
   int32_t* err;         // QW_ERR_TIMEOUT if a ring wait gives up
 };
@@ -376,21 +378,10 @@ qw_status launch_gemv_w4a8(const qw_packed_desc& d, const void* w_packed, const 
   p.err = err;
   const int G = d.K / kMxGroup;
   p.gpw = ((G + kW8Warps - 1) / kW8Warps + kW8StageGroups - 1) / kW8StageGroups * kW8StageGroups;
-  // the deepest ring that still lets two CTAs share an SM (one CTA per SM otherwise)
-  const size_t act = w4a8_gemv_smem_bytes(d.K, M);
-  auto dyn = [&](int stages) {
-    return act + 1024 + (size_t)kW8Warps * stages * kW8StageBytes;
-  };
-  constexpr size_t kStatic = sizeof(float) * 2 * kW8Warps * 128 + 8 * kW8Warps * kW8MaxStages + 64;
-  constexpr size_t kSmPerSm = 228 * 1024, kReserve = 1024;  // per SM; per CTA
   p.stages = kW8MaxStages;
-  for (int stages = kW8MaxStages; stages >= 2; --stages)
-    if (2 * (dyn(stages) + kStatic + kReserve) <= kSmPerSm) {
-      p.stages = stages;
-      break;
-    }
+  const size_t act = w4a8_gemv_smem_bytes(d.K, M);
   auto kern = M == 1 ? gemv_w4a8_kernel<true> : gemv_w4a8_kernel<false>;
-  const size_t smem = dyn(p.stages);
+  const size_t smem = act + 1024 + (size_t)kW8Warps * p.stages * kW8StageBytes;
   const int max_dyn =
       (int)(kW4A8GemvMaxSmem + 1024 + (size_t)kW8Warps * kW8MaxStages * kW8StageBytes);
   static const cudaError_t attr =
