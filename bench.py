@@ -384,8 +384,7 @@ def extra_w4a16(steps, warmup, world, only=None):
                      "hbm_frac": round(gbs / peaks["hbm_gbs"], 3),
                      "tflops": round(2 * M * N * K / (ms * 1e-3) / 1e12, 3),
                      "launches": n, "weight_copies": R, "graph": graph}
-        if M == 1:
-            out[name].update(stream_read_reference(copies, steps, warmup, world, wbytes, peaks))
+        out[name].update(stream_read_reference(copies, steps, warmup, world, wbytes, peaks))
         del copies
         torch.cuda.empty_cache()
     return out
@@ -486,6 +485,8 @@ def extra_w4a8_decode(steps, warmup, world):
         out[f"w4a8_m1_{N}x{K}"] = {"us": round(ms * 1e3, 2), "weight_GBps": round(gbs, 1),
                                    "hbm_frac": round(gbs / peaks["hbm_gbs"], 3),
                                    "launches": n, "weight_copies": R, "graph": graph}
+        out[f"w4a8_m1_{N}x{K}"].update(
+            stream_read_reference(copies, steps, warmup, world, wbytes, peaks))
         del copies
         torch.cuda.empty_cache()
     return out
@@ -805,6 +806,10 @@ def summarize(line):
         v = ex.get(name, {}).get(key)
         return v if v is not None else None
     sm["cfg1_m8_frac_hbm"] = get("cfg1_w4a16_m8_2048x2048_int4", "hbm_frac")
+    sm["cfg1_stream_read_frac"] = [get("cfg1_w4a16_m8_2048x2048_int4", "stream_read_frac"),
+                                   get("cfg1_w4a16_m8_2048x2048_int4", "stream_read_chained_frac")]
+    sm["w4a8_m1_frac_hbm"] = [get(f"w4a8_m1_{n}x{k}", "hbm_frac")
+                              for n, k in ((14336, 4096), (4096, 14336), (4096, 4096))]
     for bits in (4, 3):
         sm[f"cfg3_int{bits}_frac_hbm"] = [get(f"cfg3_m1_{n}x{k}_int{bits}", "hbm_frac")
                                           for n, k in ((14336, 4096), (4096, 14336), (4096, 4096))]
