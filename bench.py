@@ -930,6 +930,8 @@ def main():
                     help="time only the W4A16 GEMV workloads (a profiling aid)")
     ap.add_argument("--only-moe", action="store_true",
                     help="time only the grouped MoE workloads (a profiling aid)")
+    ap.add_argument("--only-w4a8-decode", action="store_true",
+                    help="only the single-token W4A8 (MXFP4 x MXFP8) decode rows")
     ap.add_argument("--only-fp8w", action="store_true",
                     help="time only the FP8-weight WnA16 workloads (a profiling aid)")
     ap.add_argument("--moe-scale", type=int, default=1,
@@ -953,6 +955,9 @@ def main():
     elif args.only_moe:
         world, rank, _ = dist_setup()
         line = {"extra": extra_moe(args.steps, args.warmup, world, args.case, args.moe_scale)}
+    elif args.only_w4a8_decode:
+        world, rank, _ = dist_setup()
+        line = {"extra": extra_w4a8_decode(args.steps, args.warmup, world)}
     elif args.only_fp8w:
         world, rank, _ = dist_setup()
         line = {"extra": extra_fp8w(args.steps, args.warmup, world, args.case)}
