@@ -136,6 +136,16 @@ def test_w4a8_gemv_shapes(M, N, K):
     assert_parity(C, R, S, f"W4A8 GEMV {M}x{N}x{K}")
 
 
+def test_w4a8_gemv_largest_staging():
+    """M = 8 at the largest K whose staged activations the GEMV takes (176 groups: 95.7 KB of
+    FP16 fragments and scales, one CTA per SM beside its rings): seven warps stream 24
+    groups each, the last 8."""
+    p = synth.w4a8_problem(8, 272, 5632, cfg_id=255)
+    C = dense_w4a8(p)
+    R, S = OQ.w4a8_from_canonical(p["A"], p["A_sf"], p["w_canon"][0], p["s_canon"][0], 5632)
+    assert_parity(C, R, S, "W4A8 GEMV M=8 K=5632")
+
+
 def test_w4a8_gemv_bias_and_wide_scales():
     """Bias, and E8M0 scales over a wide range (2^-47 .. 2^43) on both sides, so group
     products span ~2^-94 .. 2^86 (inside BF16's range)."""
