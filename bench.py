@@ -554,6 +554,8 @@ MMA_PROBES = (  # (name, mode, N, FLOP per MMA): the instruction forms the GEMMs
     ("mxf8f6f4_cp_n256", 3, 256, 2 * 128 * 256 * 32),  # ... with its scale copies
     ("mxf8f6f4_cp_ahead_n256", 4, 256, 2 * 128 * 256 * 32),  # copies a stage ahead
     ("mxf8f6f4_cp_wide_n256", 5, 256, 2 * 128 * 256 * 32),   # two 128-lane copies a stage
+    ("mxf4nvf4_n256", 6, 256, 2 * 128 * 256 * 64),           # W4A4 GEMM, MMAs only
+    ("mxf4nvf4_cp_n256", 7, 256, 2 * 128 * 256 * 64),        # ... with its scale copies
 )
 
 

@@ -445,7 +445,11 @@ qw_status qw_stream_read(const void* src, uint64_t bytes, uint32_t* sink, int32_
  *                             stage's columns, so no MMA reads what was just copied);
  *   QW_MMA_PROBE_MXF8F6F4_CP_WIDE   two copies per stage instead of three: A's image as one
  *                             tcgen05.cp.128x128b, B's two as one 128x256b (sources with
- *                             each 32-row image repeated for the four lane quarters).
+ *                             each 32-row image repeated for the four lane quarters);
+ *   QW_MMA_PROBE_MXF4NVF4     kind::mxf4nvf4.block_scale.scale_vec::4X, E2M1 x E2M1 packed,
+ *                             UE4M3 scales, 128 x 256 x 64: the W4A4 GEMM's MMA;
+ *   QW_MMA_PROBE_MXF4NVF4_CP  the same plus its twelve tcgen05.cp.32x128b.warpx4 scale
+ *                             copies per four MMAs (one 256-k stage).
  * QW_MMA_PROBE_RANDOM or'ed into a mode fills the operands with hashed finite values
  * instead of zeros (the tensor core's rate may depend on the data it multiplies).
  * n: 64, 128 or 256 for the f16 modes, 256 for the block-scaled ones; iters in [64, 2^20].
@@ -460,6 +464,8 @@ qw_status qw_stream_read(const void* src, uint64_t bytes, uint32_t* sink, int32_
 #define QW_MMA_PROBE_MXF8F6F4_CP 3
 #define QW_MMA_PROBE_MXF8F6F4_CP_AHEAD 4
 #define QW_MMA_PROBE_MXF8F6F4_CP_WIDE 5
+#define QW_MMA_PROBE_MXF4NVF4 6
+#define QW_MMA_PROBE_MXF4NVF4_CP 7
 #define QW_MMA_PROBE_RANDOM 8
 #define QW_MMA_PROBE_MAX_CTAS 1024
 qw_status qw_mma_rate_probe(int32_t mode, int32_t n, int32_t iters, uint64_t* out,

@@ -84,8 +84,10 @@ __global__ void __launch_bounds__(128, 1)
     h ^= h >> 12;
     reinterpret_cast<uint32_t*>(sA)[i] = random ? (h & mask) : 0u;
   }
+  // scale bytes 1.0: E8M0 127, or (4X kind) unsigned E4M3 0x38
+  constexpr bool NV = MODE == QW_MMA_PROBE_MXF4NVF4 || MODE == QW_MMA_PROBE_MXF4NVF4_CP;
   for (int i = threadIdx.x; i < kProbeSf / 4; i += blockDim.x)
-    reinterpret_cast<uint32_t*>(sSF)[i] = 0x7F7F7F7Fu;
+    reinterpret_cast<uint32_t*>(sSF)[i] = NV ? 0x38383838u : 0x7F7F7F7Fu;
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     *abort_flag = 0;
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t id_f16 =
         (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (8u << 24);
     const uint32_t id_mx = (5u << 10) | (32u << 17) | (1u << 23) | (8u << 24);
+    // kind::mxf4nvf4: A = B = E2M1 packed, UE4M3 scales (bit 23 clear), N = 256, M = 128
+    const uint32_t id_nv = (1u << 7) | (1u << 10) | (32u << 17) | (8u << 24);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB), sf0 = smem_u32(sSF);
     auto issue = [&](int i) {
       if constexpr (MODE == QW_MMA_PROBE_F16_TMEM_A || MODE == QW_MMA_PROBE_F16_SMEM) {
@@ -118,6 +122,25 @@ __global__ void __launch_bounds__(128, 1)
         else
           tc_mma_f16(tbase, smem_desc(a0 + (s >> 2) * kProbeABox + (s & 3) * 32, 16, 1024, 2),
                      bd, id_f16, s != 0 ? 1u : 0u);
+      } else if constexpr (NV) {
+        // one 64-k MMA per 32 bytes of each row: four per 256-k stage, which copies twelve
+        // scale images (A: one per MMA, B: two 128-row chunks per MMA) into 48 columns that
+        // rotate over four stages
+        const int kk = i & 3;
+        const uint32_t sfc = tbase + kProbeSfCol + 48u * (uint32_t)((i >> 2) & 3);
+        if (MODE == QW_MMA_PROBE_MXF4NVF4_CP && kk == 0) {
+#pragma unroll
+          for (int img = 0; img < 4; ++img) {
+            tc_cp_32x128b_warpx4(sfc + 4 * img, smem_desc(sf0 + img * 512, 0, 128, 0));
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              tc_cp_32x128b_warpx4(sfc + 16 + 8 * img + 4 * c,
+                                   smem_desc(sf0 + 2048 + (c * 4 + img) * 512, 0, 128, 0));
+          }
+        }
+        tc_mma_mxf4nvf4_4x(tbase, smem_desc(a0 + kk * 32, 16, 1024, 2),
+                           smem_desc(b0 + kk * 32, 16, 1024, 2), id_nv, sfc + 4 * kk,
+                           sfc + 16 + 8 * kk, i != 0 ? 1u : 0u);
       } else {
         const int kk = i & 3;  // 32-k MMA of a 128-k stage
         const uint32_t sfc = tbase + kProbeSfCol + 12u * (uint32_t)((i >> 2) & 3);
@@ -195,6 +218,10 @@ qw_status launch_mma_probe(int mode, int n, int iters, uint64_t* out, int32_t* e
       return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4_CP>(n, iters, random, out, err, grid, st);
     case QW_MMA_PROBE_MXF8F6F4_CP_AHEAD:
       return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4_CP_AHEAD>(n, iters, random, out, err, grid, st);
+    case QW_MMA_PROBE_MXF4NVF4:
+      return launch_probe_mode<QW_MMA_PROBE_MXF4NVF4>(n, iters, random, out, err, grid, st);
+    case QW_MMA_PROBE_MXF4NVF4_CP:
+      return launch_probe_mode<QW_MMA_PROBE_MXF4NVF4_CP>(n, iters, random, out, err, grid, st);
     default:
       return launch_probe_mode<QW_MMA_PROBE_MXF8F6F4_CP_WIDE>(n, iters, random, out, err, grid, st);
   }

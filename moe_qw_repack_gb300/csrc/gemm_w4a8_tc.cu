@@ -97,21 +97,6 @@ __host__ __device__ constexpr uint32_t idesc() {
                 (1u << 23) | ((uint32_t)(BM >> 4) << 24));
 }
 
-// D(tmem) (+)= A x B^T, both packed E2M1 in shared memory, a UE4M3 scale per 16 k read from
-// TMEM (four per row and MMA).
-__device__ __forceinline__ void tc_mma_mxf4nvf4_4x(uint32_t d_tmem, uint64_t a_desc,
-                                                   uint64_t b_desc, uint32_t idesc,
-                                                   uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                                   uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-      : "memory");
-}
-
 struct Params {
   int64_t rows;           // activation rows (M, or total grouped rows)
   int32_t N, N_pad, K, K_pad;
@@ -168,6 +153,24 @@ __device__ __forceinline__ uint32_t load_sf_word(const Params& p, int64_t ar, in
   for (int j = 0; j < 4; ++j)
     w |= (uint32_t)(g0 + j < G ? __ldg(row + g0 + j) : (T::SF_PAD & 0xFFu)) << (8 * j);
   return w;
+}
+
+// The 4X kind's four scale words of activation row `ar` for K step kb (16 bytes: groups
+// 16 kb .. 16 kb + 15), one 16-byte load where the row allows it.  (Sixteen 4-byte loads
+// per lane and stage held the W4A4 GEMM back: a timing-only copy whose scale fetcher made
+// no loads ran 157 against 199 us on (4096, 14336, 4096).)
+template <int KIND>
+__device__ __forceinline__ uint4 load_sf_row(const Params& p, int64_t ar, int kb) {
+  using T = KT<KIND>;
+  static_assert(T::IMG == 4, "four images per stage");
+  const int G = p.K / T::GROUP;
+  const int g0 = kb * 16;
+  if (ar < 0) return make_uint4(T::SF_PAD, T::SF_PAD, T::SF_PAD, T::SF_PAD);
+  const uint8_t* row = p.A_sf + ar * (int64_t)G;
+  if (g0 + 15 < G && (reinterpret_cast<uintptr_t>(row + g0) & 15) == 0)
+    return __ldg(reinterpret_cast<const uint4*>(row + g0));
+  return make_uint4(load_sf_word<KIND>(p, ar, kb, 0), load_sf_word<KIND>(p, ar, kb, 1),
+                    load_sf_word<KIND>(p, ar, kb, 2), load_sf_word<KIND>(p, ar, kb, 3));
 }
 
 // Activation row of problem row r: itself, or (indexed calls) the token of pair gather[r].
@@ -415,12 +418,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int i = 0; i < IMG; ++i) e.v[i] = make_uint4(T::SF_PAD, T::SF_PAD, T::SF_PAD, T::SF_PAD);
       if (lt < num_tiles) {
+        if constexpr (IMG == 4) {
+          // a row's 16 bytes hold word i of every image i
+          uint4 r[4];
 #pragma unroll
-        for (int i = 0; i < IMG; ++i) {
-          e.v[i].x = load_sf_word<KIND>(p, ar[0], lkb, i);
-          e.v[i].y = load_sf_word<KIND>(p, ar[1], lkb, i);
-          e.v[i].z = load_sf_word<KIND>(p, ar[2], lkb, i);
-          e.v[i].w = load_sf_word<KIND>(p, ar[3], lkb, i);
+          for (int j = 0; j < 4; ++j) r[j] = load_sf_row<KIND>(p, ar[j], lkb);
+          e.v[0] = make_uint4(r[0].x, r[1].x, r[2].x, r[3].x);
+          e.v[1] = make_uint4(r[0].y, r[1].y, r[2].y, r[3].y);
+          e.v[2] = make_uint4(r[0].z, r[1].z, r[2].z, r[3].z);
+          e.v[3] = make_uint4(r[0].w, r[1].w, r[2].w, r[3].w);
+        } else {
+#pragma unroll
+          for (int i = 0; i < IMG; ++i) {
+            e.v[i].x = load_sf_word<KIND>(p, ar[0], lkb, i);
+            e.v[i].y = load_sf_word<KIND>(p, ar[1], lkb, i);
+            e.v[i].z = load_sf_word<KIND>(p, ar[2], lkb, i);
+            e.v[i].w = load_sf_word<KIND>(p, ar[3], lkb, i);
+          }
         }
         if (++lkb == KB) {
           lkb = 0;

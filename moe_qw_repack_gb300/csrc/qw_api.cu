@@ -454,7 +454,8 @@ qw_status qw_mma_rate_probe(int32_t mode, int32_t n, int32_t iters, uint64_t* ou
   const int32_t base = mode & ~QW_MMA_PROBE_RANDOM;
   const bool f16 = base == QW_MMA_PROBE_F16_TMEM_A || base == QW_MMA_PROBE_F16_SMEM;
   const bool mx = base == QW_MMA_PROBE_MXF8F6F4 || base == QW_MMA_PROBE_MXF8F6F4_CP ||
-                  base == QW_MMA_PROBE_MXF8F6F4_CP_AHEAD || base == QW_MMA_PROBE_MXF8F6F4_CP_WIDE;
+                  base == QW_MMA_PROBE_MXF8F6F4_CP_AHEAD || base == QW_MMA_PROBE_MXF8F6F4_CP_WIDE ||
+                  base == QW_MMA_PROBE_MXF4NVF4 || base == QW_MMA_PROBE_MXF4NVF4_CP;
   if (!f16 && !mx) return QW_ERR_INVALID_ARG;
   // only the shapes the GEMMs issue (a shape outside the MMA's table would not assemble to
   // a valid instruction)

@@ -292,6 +292,8 @@ QW_MMA_PROBE_MXF8F6F4 = 2
 QW_MMA_PROBE_MXF8F6F4_CP = 3
 QW_MMA_PROBE_MXF8F6F4_CP_AHEAD = 4
 QW_MMA_PROBE_MXF8F6F4_CP_WIDE = 5
+QW_MMA_PROBE_MXF4NVF4 = 6
+QW_MMA_PROBE_MXF4NVF4_CP = 7
 QW_MMA_PROBE_RANDOM = 8
 QW_MMA_PROBE_MAX_CTAS = 1024
 

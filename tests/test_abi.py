@@ -283,8 +283,9 @@ def test_mma_rate_probe_validates_on_the_host(Q):
     """The MMA-rate diagnostic takes only the shapes the GEMMs issue; nothing launches."""
     out = ctypes.c_void_p(64)
     err = ctypes.c_void_p(64)
-    bad = [(6, 256, 4096), (7, 128, 4096), (16, 128, 4096), (-1, 128, 4096),  # unknown mode
-           (Q.QW_MMA_PROBE_RANDOM | 6, 256, 4096), (Q.QW_MMA_PROBE_RANDOM | 16, 128, 4096),
+    bad = [(16, 256, 4096), (24, 256, 4096), (32, 128, 4096), (-1, 128, 4096),  # unknown mode
+           (Q.QW_MMA_PROBE_RANDOM | 16, 128, 4096), (Q.QW_MMA_PROBE_MXF4NVF4, 128, 4096),
+           (Q.QW_MMA_PROBE_MXF4NVF4_CP | Q.QW_MMA_PROBE_RANDOM, 64, 4096),
            (Q.QW_MMA_PROBE_F16_TMEM_A, 96, 4096), (Q.QW_MMA_PROBE_F16_SMEM, 512, 4096),
            (Q.QW_MMA_PROBE_MXF8F6F4, 128, 4096), (Q.QW_MMA_PROBE_MXF8F6F4_CP, 64, 4096),
            (Q.QW_MMA_PROBE_MXF8F6F4_CP_AHEAD, 128, 4096),

@@ -8,7 +8,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("mode,n", [(0, 64), (0, 128), (0, 256), (1, 128), (1, 256), (2, 256),
-                                    (3, 256), (4, 256), (5, 256), (8 | 1, 256), (8 | 3, 256)])
+                                    (3, 256), (4, 256), (5, 256), (6, 256), (7, 256),
+                                    (8 | 1, 256), (8 | 3, 256)])
 def test_mma_rate_probe_runs_on_every_sm(mode, n):
     import torch
     Q = qw()
