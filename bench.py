@@ -163,12 +163,16 @@ class W4A8Problem:
         self.C = torch.empty((M, N), dtype=torch.int16, device="cuda")
         self.C_host = torch.empty((M, N), dtype=torch.int16).pin_memory()
         self.err = Q.new_error_flag()
+        # the workspace the call asks for (none for a dense call today; passed as a caller
+        # should)
+        self.wsn = Q.qgemm_workspace_size(self.desc, Q.QW_A_MXFP8_G32, M)
+        self.ws = torch.empty(max(self.wsn, 16), dtype=torch.uint8, device="cuda")
 
     def run(self, i=0):
         Q = self.Q
         wp, sp, A, Asf = self.copies[i % len(self.copies)]
-        Q.qgemm_dense(self.desc, wp, sp, Q.QW_A_MXFP8_G32, A, Asf, None, self.C, self.M, None, 0,
-                      self.err)
+        Q.qgemm_dense(self.desc, wp, sp, Q.QW_A_MXFP8_G32, A, Asf, None, self.C, self.M, self.ws,
+                      self.wsn, self.err)
 
     # end to end, two slots: slot k holds one step's activations and results on the device
     def _slot(self, k):
@@ -194,8 +198,8 @@ class W4A8Problem:
         Q = self.Q
         A, Asf, C, _ = self._slot(k)
         wp, sp = self.copies[i % len(self.copies)][:2]
-        Q.qgemm_dense(self.desc, wp, sp, Q.QW_A_MXFP8_G32, A, Asf, None, C, self.M, None, 0,
-                      self.err)
+        Q.qgemm_dense(self.desc, wp, sp, Q.QW_A_MXFP8_G32, A, Asf, None, C, self.M, self.ws,
+                      self.wsn, self.err)
 
     def store_slot(self, k):
         """Slot k's BF16 result -> pinned host memory (on the current stream)."""
@@ -509,10 +513,12 @@ def extra_w4a4(steps, warmup, world):
     copies = [(wp, sp, A, Asf)] + [(wp.clone(), sp.clone(), A.clone(), Asf.clone())
                                    for _ in range(R - 1)]
     C = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    wsn = Q.qgemm_workspace_size(d, Q.QW_A_NVFP4_G16, M)
+    ws = torch.empty(max(wsn, 16), dtype=torch.uint8, device="cuda")
 
     def fn(i):
         w, s, a, asf = copies[i % R]
-        Q.qgemm_dense(d, w, s, Q.QW_A_NVFP4_G16, a, asf, None, C, M, None, 0)
+        Q.qgemm_dense(d, w, s, Q.QW_A_NVFP4_G16, a, asf, None, C, M, ws, wsn)
     ms, n, _ = time_region([fn], steps, warmup, world)
     tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
     return {"w4a4_nvfp4_4096x14336x4096": {"us": round(ms * 1e3, 1), "tflops": round(tf, 1),
@@ -536,10 +542,12 @@ def extra_w8a8(steps, warmup, world):
     copies = [(wp, sp, A, Asf)] + [(wp.clone(), sp.clone(), A.clone(), Asf.clone())
                                    for _ in range(R - 1)]
     C = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    wsn = Q.qgemm_workspace_size(d, Q.QW_A_MXFP8_G32, M)
+    ws = torch.empty(max(wsn, 16), dtype=torch.uint8, device="cuda")
 
     def fn(i):
         w, s, a, asf = copies[i % R]
-        Q.qgemm_dense(d, w, s, Q.QW_A_MXFP8_G32, a, asf, None, C, M, None, 0)
+        Q.qgemm_dense(d, w, s, Q.QW_A_MXFP8_G32, a, asf, None, C, M, ws, wsn)
     ms, n, _ = time_region([fn], steps, warmup, world)
     tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
     return {"w8a8_mxfp8_4096x14336x4096": {"us": round(ms * 1e3, 1), "tflops": round(tf, 1),

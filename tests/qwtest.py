@@ -75,7 +75,7 @@ def dense_fp8w(prob, bias=None):
     return u16_view(C)
 
 
-def dense_w4a8(prob, bias=None, wfmt=None):
+def dense_w4a8(prob, bias=None, wfmt=None, workspace=True):
     Q = qw()
     wfmt = Q.QW_W_MXFP4_G32 if wfmt is None else wfmt
     d, wp, sp = repack(wfmt, 1, prob["N"], prob["K"], prob["w_canon"], prob["s_canon"])
@@ -84,8 +84,9 @@ def dense_w4a8(prob, bias=None, wfmt=None):
     M = prob["A"].shape[0]
     C = torch.full((M, prob["N"]), -1, dtype=torch.int16, device="cuda")
     b = None if bias is None else dev(bias.view(np.int16))
-    ws_n = Q.qgemm_workspace_size(d, Q.QW_A_MXFP8_G32, M)
-    ws = torch.zeros(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    # the workspace the call asks for (none for a dense call today)
+    ws_n = Q.qgemm_workspace_size(d, Q.QW_A_MXFP8_G32, M) if workspace else 0
+    ws = torch.zeros(max(ws_n, 16), dtype=torch.uint8, device="cuda") if workspace else None
     err = Q.new_error_flag()
     Q.qgemm_dense(d, wp, sp, Q.QW_A_MXFP8_G32, A, Asf, b, C, M, ws, ws_n, err)
     code = Q.qw_read_error(err)

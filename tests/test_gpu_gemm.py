@@ -165,6 +165,20 @@ def test_w4a8_gemv_m1_decode_full(N, K):
     assert_parity(C, R, S, f"W4A8 M=1 {N}x{K}")
 
 
+def test_w4a8_last_wave_shape_bias_ragged_and_repeatable():
+    """A dense W4A8 call whose 10 x 16 tiles leave a last wave of 8 tiles for 152 SMs, with
+    bias and ragged N, K = 8192: every element against the oracle, with and without the
+    workspace the call asks for, and twice: the results are the same bits every time."""
+    p = synth.w4a8_problem(1280, 4000, 8192, cfg_id=270, bias=True)
+    C1 = dense_w4a8(p, bias=p["bias"][0])
+    C2 = dense_w4a8(p, bias=p["bias"][0])
+    C0 = dense_w4a8(p, bias=p["bias"][0], workspace=False)
+    R, S = OQ.w4a8_from_canonical(p["A"], p["A_sf"], p["w_canon"][0], p["s_canon"][0], 8192,
+                                  bias_bits=p["bias"][0])
+    assert_parity(C1, R, S, "W4A8 1280 x 4000 x 8192")
+    assert np.array_equal(C1, C2) and np.array_equal(C1, C0)
+
+
 def test_config2a_w4a8_full():
     """(M,N,K) = (4096, 3072, 4096) MXFP4 x MXFP8 group-32, every output element."""
     p = synth.w4a8_problem(4096, 3072, 4096, cfg_id=1)
