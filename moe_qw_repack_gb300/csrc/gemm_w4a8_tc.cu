@@ -395,7 +395,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ A scale fetcher
-    // Global loads run three elements ahead of the staging writes; this warp never fences.
+    // Global loads run ahead of the staging writes; this warp never fences.  1X kinds: a
+    // three-deep register ring shifted each stage.  4X: two register sets of four words per
+    // lane used in turn, two stages ahead (no copies between them: a copy of a register
+    // whose load is in flight waits for it; the shifted ring ran the W4A4 GEMM at 166
+    // against 162 us on (4096, 14336, 4096), and cost the W4A8 headline nothing).
     constexpr int AHEAD = 3;
     int64_t lt = blockIdx.x;  // load cursor: tile and K step
     int lkb = 0;
@@ -444,28 +448,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       return e;
     };
-    Entry ring[AHEAD];
-#pragma unroll
-    for (int i = 0; i < AHEAD; ++i) ring[i] = load_next();
     int slot = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-      for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(&sempty[slot], phase ^ 1u, abort_flag, p.err)) {
-          ok = false;
-          break;
+    auto write = [&](const Entry& e) {
+#pragma unroll
+      for (int i = 0; i < IMG; ++i)
+        *reinterpret_cast<uint4*>(sStage + slot * SFA_BYTES + i * 512 + lane * 16) = e.v[i];
+      mbar_arrive(&sfull[slot]);
+    };
+    if constexpr (IMG == 4) {
+      Entry set_a = load_next(), set_b = load_next();
+      uint32_t n = 0;  // staging writes so far (even: set_a's turn)
+      for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb, ++n) {
+          if (!mbar_wait(&sempty[slot], phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          if (n & 1u) {
+            write(set_b);
+            set_b = load_next();
+          } else {
+            write(set_a);
+            set_a = load_next();
+          }
+          if (++slot == SF_STAGING) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
+      }
+    } else {
+      Entry ring[AHEAD];
 #pragma unroll
-        for (int i = 0; i < IMG; ++i)
-          *reinterpret_cast<uint4*>(sStage + slot * SFA_BYTES + i * 512 + lane * 16) = ring[0].v[i];
-        mbar_arrive(&sfull[slot]);
+      for (int i = 0; i < AHEAD; ++i) ring[i] = load_next();
+      for (int64_t t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&sempty[slot], phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          write(ring[0]);
 #pragma unroll
-        for (int i = 0; i + 1 < AHEAD; ++i) ring[i] = ring[i + 1];
-        ring[AHEAD - 1] = load_next();
-        if (++slot == SF_STAGING) {
-          slot = 0;
-          phase ^= 1u;
+          for (int i = 0; i + 1 < AHEAD; ++i) ring[i] = ring[i + 1];
+          ring[AHEAD - 1] = load_next();
+          if (++slot == SF_STAGING) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
       }
     }
