@@ -942,6 +942,8 @@ def main():
                     help="time only the grouped MoE workloads (a profiling aid)")
     ap.add_argument("--only-w4a8-decode", action="store_true",
                     help="only the single-token W4A8 (MXFP4 x MXFP8) decode rows")
+    ap.add_argument("--only-mx-dense", action="store_true",
+                    help="only the dense W8A8 and W4A4 GEMM rows (--case w8a8 / w4a4: one)")
     ap.add_argument("--only-fp8w", action="store_true",
                     help="time only the FP8-weight WnA16 workloads (a profiling aid)")
     ap.add_argument("--moe-scale", type=int, default=1,
@@ -965,6 +967,13 @@ def main():
     elif args.only_moe:
         world, rank, _ = dist_setup()
         line = {"extra": extra_moe(args.steps, args.warmup, world, args.case, args.moe_scale)}
+    elif args.only_mx_dense:
+        world, rank, _ = dist_setup()
+        line = {"extra": {}}
+        if not args.case or args.case in "w8a8_mxfp8":
+            line["extra"].update(extra_w8a8(args.steps, args.warmup, world))
+        if not args.case or args.case in "w4a4_nvfp4":
+            line["extra"].update(extra_w4a4(args.steps, args.warmup, world))
     elif args.only_w4a8_decode:
         world, rank, _ = dist_setup()
         line = {"extra": extra_w4a8_decode(args.steps, args.warmup, world)}
