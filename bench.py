@@ -463,14 +463,14 @@ def extra_fp8w(steps, warmup, world, only=None):
 
 
 def extra_w4a8_decode(steps, warmup, world):
-    """Single-token W4A8 (MXFP4 weights x MXFP8 activations) decode on the M=1 decode
-    shapes: device time per GEMM (CUDA graph of back-to-back launches over weight copies
-    that do not fit L2), weight GB/s (E2M1 codes + E8M0 scales)."""
+    """W4A8 (MXFP4 weights x MXFP8 activations) decode on the M=1 decode shapes, and an
+    8-row batch on the first: device time per GEMM (CUDA graph of back-to-back launches over
+    weight copies that do not fit L2), weight GB/s (E2M1 codes + E8M0 scales)."""
     import moe_qw_repack_gb300.qw as Q
     out = {}
     peaks, _ = measured_peaks()
-    for (N, K) in [(14336, 4096), (4096, 14336), (4096, 4096)]:
-        p = synth.w4a8_problem(1, N, K, cfg_id=260)
+    for (M, N, K) in [(1, 14336, 4096), (1, 4096, 14336), (1, 4096, 4096), (8, 14336, 4096)]:
+        p = synth.w4a8_problem(M, N, K, cfg_id=260)
         d = Q.qw_repack_query(Q.QW_W_MXFP4_G32, 1, N, K)
         wp, sp = Q.empty_packed(d)
         Q.qw_repack(d, torch.from_numpy(p["w_canon"]).cuda(), torch.from_numpy(p["s_canon"]).cuda(),
@@ -479,18 +479,18 @@ def extra_w4a8_decode(steps, warmup, world):
         R = replicas_for(wp.numel() + sp.numel())
         copies = [(wp, sp)] + [(wp.clone(), sp.clone()) for _ in range(R - 1)]
         A, Asf = torch.from_numpy(p["A"]).cuda(), torch.from_numpy(p["A_sf"]).cuda()
-        C = torch.empty((1, N), dtype=torch.int16, device="cuda")
+        C = torch.empty((M, N), dtype=torch.int16, device="cuda")
 
-        def fn(i, copies=copies, d=d, A=A, Asf=Asf, C=C):
+        def fn(i, copies=copies, d=d, A=A, Asf=Asf, C=C, M=M):
             w, s = copies[i % len(copies)]
-            Q.qgemm_dense(d, w, s, Q.QW_A_MXFP8_G32, A, Asf, None, C, 1, None, 0)
+            Q.qgemm_dense(d, w, s, Q.QW_A_MXFP8_G32, A, Asf, None, C, M, None, 0)
         ms, n, graph = time_region([fn], max(steps, R), warmup, world, graph_steps=R)
         gbs = wbytes / (ms * 1e-3) / 1e9
-        out[f"w4a8_m1_{N}x{K}"] = {"us": round(ms * 1e3, 2), "weight_GBps": round(gbs, 1),
-                                   "hbm_frac": round(gbs / peaks["hbm_gbs"], 3),
-                                   "launches": n, "weight_copies": R, "graph": graph}
-        out[f"w4a8_m1_{N}x{K}"].update(
-            stream_read_reference(copies, steps, warmup, world, wbytes, peaks))
+        name = f"w4a8_m{M}_{N}x{K}"
+        out[name] = {"us": round(ms * 1e3, 2), "weight_GBps": round(gbs, 1),
+                     "hbm_frac": round(gbs / peaks["hbm_gbs"], 3),
+                     "launches": n, "weight_copies": R, "graph": graph}
+        out[name].update(stream_read_reference(copies, steps, warmup, world, wbytes, peaks))
         del copies
         torch.cuda.empty_cache()
     return out
